@@ -1,0 +1,222 @@
+/*
+ * verkv.h -- C ABI of libverkv, VerKV's decode-time hot path on one GPU (sm_103a).
+ *
+ * Method: "Verify Before You Fetch: Reliable KV Cache Compression for LLM Inference" (arXiv
+ * abstract page; Markdown summary page of the same title, whose section, equation, definition,
+ * lemma and theorem names are cited below).  The abstract states the problem this interface
+ * follows: a compact set of pivotal tokens and a token-level sketch of the full KV cache live on
+ * the GPU, the complete cache lives in CPU memory, and each decode query either certifies its
+ * attention against a user (epsilon, delta) tolerance or fetches extra tokens from the CPU and
+ * refines.
+ *
+ * Conventions for every call:
+ *  - The caller owns every tensor.  Device pointers are plain CUDA device addresses; "host"
+ *    pointers must be page-locked (cudaHostAlloc / cudaHostRegister or torch pin_memory) because
+ *    the GPU reads or writes them directly.  Nothing is allocated on the hot path: the context
+ *    allocates its side stream, events and (only in VERKV_FETCH_MEMCPY mode) page-locked staging
+ *    in verkv_create / verkv_set_fetch_mode, and all device scratch lives in the caller's
+ *    workspace of verkv_workspace_size() bytes.
+ *  - Calls are asynchronous and stream-ordered on the stream given to verkv_create, except that
+ *    verkv_fetch_refine in VERKV_FETCH_MEMCPY mode waits on the host for the selection of the
+ *    preceding verkv_attend_verified.  Errors detected on the device (invalid tau, pivotal
+ *    capacity overflow, a solve that hit its iteration cap) are latched in a device error word
+ *    and returned by the next verkv_sync.  No call throws; a call that returns an error has not
+ *    launched work unless stated.
+ *  - Layouts.  A "unit" is one (sequence b, layer l, KV head h) of a verkv_shape; units are
+ *    numbered u = (b * layers + l) * kv_heads + h.  Query head j of sequence b belongs to KV head
+ *    j / q_per_kv (grouped-query attention).  bf16 is IEEE bfloat16 (uint16 bit patterns).
+ *  - One context per host thread; calls on one context must not overlap.
+ */
+#ifndef VERKV_H
+#define VERKV_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    VERKV_OK = 0,
+    VERKV_EINVAL = 1,      /* bad argument, or tau outside (0, 1] / not finite (device) */
+    VERKV_EBUDGET = 2,     /* eta * n does not exceed the forced H set */
+    VERKV_ECAPACITY = 3,   /* a pivotal set larger than shape.cap (device; truncated) */
+    VERKV_ENOCONVERGE = 4, /* a solve hit its iteration cap (device; result still written) */
+    VERKV_ECUDA = 5,       /* CUDA runtime error (see verkv_last_error) */
+    VERKV_ECOPY = 6,       /* host-to-device fetch failed */
+    VERKV_ETIMEOUT = 7,    /* a bounded device wait expired */
+    VERKV_ESTATE = 8       /* calls out of order, e.g. fetch_refine without attend */
+} verkv_status;
+
+typedef struct verkv_ctx verkv_ctx;
+
+/* Sizes of one cache.  n is the context length per unit; cap the pivotal capacity per unit. */
+typedef struct {
+    int32_t batch;     /* B sequences                                    >= 1        */
+    int32_t layers;    /* L                                              >= 1        */
+    int32_t kv_heads;  /* h_kv                                           >= 1        */
+    int32_t q_per_kv;  /* G query heads per KV head                      1, 2, 4, 8  */
+    int32_t head_dim;  /* d                                              64 or 128   */
+    int32_t n;         /* tokens per unit                                1 .. 131072 */
+    int32_t cap;       /* pivotal capacity per unit                      1 .. n      */
+} verkv_shape;
+
+/* Tokens forced into H (summary page, PoissonComp: H includes the sink and local tokens):
+ * the first n_sink and the last n_local tokens of every unit. */
+typedef struct {
+    int32_t n_sink;
+    int32_t n_local;
+} verkv_hset;
+
+/* The GPU-resident pivotal set H u S of every unit (caller-owned device memory).
+ *   ids       int32  [units][cap]        token ids of H u S, ascending
+ *   r         float  [units][cap]        r_i of each pivotal token (1 for H)
+ *   kv        bf16   [units][cap][2][d]  K row then V row of each pivotal token
+ *   count     int32  [units]             |H u S|
+ *   resident  uint32 [units][ceil(n/32)] bit i%32 of word i/32 set iff token i is in H u S
+ *   c         float  [units]             the PoissonComp constant c (float32; +inf if eta n >= n) */
+typedef struct {
+    int32_t *ids;
+    float *r;
+    void *kv;
+    int32_t *count;
+    uint32_t *resident;
+    float *c;
+} verkv_pivotal;
+
+/* Token-level sketch of the full cache (abstract page; summary page, KVFETCH step 1).
+ * VERKV_SKETCH_EXACT: a bf16 copy of every key, [units][n][d] -- the "perfect sketch" of the
+ * summary page's Figure 5 and the setting of Theorem 2. */
+enum { VERKV_SKETCH_EXACT = 0 };
+typedef struct {
+    int32_t format;
+    const void *data;
+} verkv_sketch;
+
+/* How verkv_fetch_refine moves the selected rows from the host-resident full cache.
+ * ZEROCOPY: a gather kernel on the side stream reads the rows straight from page-locked host
+ *           memory (no host round trip; default).
+ * MEMCPY:   the host waits for the selection, gathers the rows into page-locked staging with a
+ *           thread pool, and cudaMemcpyAsync moves them on the side stream. */
+enum { VERKV_FETCH_ZEROCOPY = 0, VERKV_FETCH_MEMCPY = 1 };
+
+/* Per query head results of one attend + fetch_refine, written by verkv_fetch_refine.
+ *   m          max sketch logit q.k/sqrt(d) (the shift of every weight below)
+ *   D          sum of sketch weights over all tokens (the certificate's D)
+ *   beta       beta(L) of the fixed point of Definition 2
+ *   V, b       V(L) and b(L) of Lemma 1
+ *   eps_hat    eps-hat(L) of Eq. (7)
+ *   eps_final  eps-hat(L_g[k*:]) of Eq. (10) (equals eps_hat when certified)
+ *   D_hat      the returned estimator of D (shift m)
+ *   M2         sum over sampled, unfetched tokens of (lambda w / r)^2 (1 - r), an unbiased
+ *              estimate of V(L_g[k*:])
+ *   lse        m + log(D_hat)
+ *   certified  1 iff eps_hat < eps (no fetch needed)
+ *   k_star     k* of Eq. (10)
+ *   n_L        |L|
+ *   n_fetch    |F \ S| for this head (rows not already resident)
+ *   iters      iterations of the beta solve
+ *   flags      nonzero if the beta solve hit its cap */
+typedef struct {
+    float m, D, beta, V, b, eps_hat, eps_final, D_hat, M2, lse;
+    int32_t certified, k_star, n_L, n_fetch, iters, flags;
+} verkv_head_stats;
+
+/* Bytes of device workspace a context for `shape` needs (0 if the shape is invalid). */
+size_t verkv_workspace_size(const verkv_shape *shape);
+
+/* Create a context on `device` that issues work on `stream` (a cudaStream_t; NULL = legacy
+ * default stream).  `workspace` is caller-owned device memory of at least
+ * verkv_workspace_size(shape) bytes, 256-byte aligned; it must outlive the context and must not
+ * be shared by two contexts.  Returns VERKV_EINVAL for a bad shape or workspace, VERKV_ECUDA if
+ * the side stream or events cannot be created. */
+verkv_status verkv_create(verkv_ctx **ctx, int device, void *stream, const verkv_shape *shape,
+                          void *workspace, size_t workspace_bytes);
+
+/* Release the side stream, events, staging and thread pool (after synchronising). */
+void verkv_destroy(verkv_ctx *ctx);
+
+/* Select VERKV_FETCH_ZEROCOPY or VERKV_FETCH_MEMCPY.  MEMCPY allocates page-locked staging of
+ * units_per_layer * n * 4d bytes on first use. */
+verkv_status verkv_set_fetch_mode(verkv_ctx *ctx, int mode);
+
+/* PoissonComp (summary page, Methodology, POISSONCOMP: Eq. (3), the H / L partition and the
+ * Poisson sample S), for every unit of the shape.
+ *   tau     device float [units][n]: normalised importance scores; must be finite and in (0, 1]
+ *           outside the forced H set (VERKV_EINVAL on the device otherwise)
+ *   eta     budget fraction in (0, 1]; requires eta * n > n_sink + n_local when tokens remain
+ *           outside the forced set (VERKV_EBUDGET, checked on the host before any launch)
+ *   H       the forced H set
+ *   seed    Philox4x32-10 key; token i of unit (b, l, h) draws word i%4 of the block at counter
+ *           (i/4, h, l, b), u_i = (word >> 8) * 2^-24, and is kept iff u_i < r_i
+ *   kv_full device bf16 [units][n][2][d]: the full cache, read to fill out->kv
+ *   r_full  device float [units][n] out: r_i = min(1, c tau_i) for every token (1 in H)
+ *   out     the pivotal set (every member must point to caller device memory of the sizes above)
+ * c is the exact root of sum_i min(1, c tau_i) = eta n, located by bisection and finished
+ * exactly on its linear piece, then published as float32; r_i is the float32 product. */
+verkv_status verkv_poissoncomp(verkv_ctx *ctx, const float *tau, double eta, verkv_hset H,
+                               uint64_t seed, const void *kv_full, float *r_full,
+                               const verkv_pivotal *out);
+
+/* Build the sketch from the full device cache.  VERKV_SKETCH_EXACT: copies every key row,
+ * kv_full bf16 [units][n][2][d] -> sketch_out bf16 [units][n][d]. */
+verkv_status verkv_sketch_build(verkv_ctx *ctx, const void *kv_full, int32_t format,
+                                void *sketch_out);
+
+/* KVFetch steps 1-4 for one layer (summary page, KVFETCH: Verification and Adaptive Fetching;
+ * Definition 2, Lemma 1, Eqs. (5), (7), (9), (10)) plus the estimator over the resident tokens.
+ *   layer          which layer of the shape
+ *   q              device bf16 [batch][kv_heads * q_per_kv][d]: one decode query per sequence
+ *   pivotal        the PoissonComp output (all layers; this call reads layer `layer`)
+ *   r_full         device float [units][n] from verkv_poissoncomp
+ *   sketch         the sketch (all layers)
+ *   eps, delta     the tolerance: certified iff eps-hat(L) < eps; 0 < delta < 1; eps > 0
+ *   fetch_ids_out  optional (NULL) device or page-locked host int32 [batch*kv_heads][n]: for each
+ *                  KV head of this layer, the ascending ids of the union over its query heads of
+ *                  F \ S (the rows that must move)
+ *   fetch_counts_out optional int32 [batch*kv_heads]: the number of ids per KV head
+ * Per query head: sketch logits for all n tokens, w-hat = exp(logit - max), the beta fixed point,
+ * the certificate, and when it fails the order of Eq. (9) (ties to the lower token id) and the
+ * minimal k* of Eq. (10); then the shrinkage-weighted partial sums over the pivotal set.
+ * Asynchronous; results are completed by verkv_fetch_refine, which reads q, the pivotal set and
+ * the sketch again: keep them unchanged until it has been issued. */
+verkv_status verkv_attend_verified(verkv_ctx *ctx, int32_t layer, const void *q,
+                                   const verkv_pivotal *pivotal, const float *r_full,
+                                   const verkv_sketch *sketch, float eps, float delta,
+                                   int32_t *fetch_ids_out, int32_t *fetch_counts_out);
+
+/* KVFetch step 5 and the refined attention (summary page, KVFETCH step 5 and Theorem 2;
+ * abstract page: fetch additional tokens from the CPU and refine).
+ *   ids, counts  NULL, or exactly the fetch_ids_out / fetch_counts_out pointers given to the
+ *                preceding verkv_attend_verified (VERKV_EINVAL otherwise)
+ *   host_kv      page-locked host bf16 [units][n][2][d]: the complete cache
+ *   o_out        device float [batch][kv_heads * q_per_kv][d]: N-hat / D-hat
+ *   lse_out      optional device float [batch][kv_heads * q_per_kv]: m + log D-hat
+ *   stats_out    optional device verkv_head_stats [batch][kv_heads * q_per_kv]
+ * Returns VERKV_ESTATE without a preceding attend on this context. */
+verkv_status verkv_fetch_refine(verkv_ctx *ctx, const int32_t *ids, const int32_t *counts,
+                                const void *host_kv, float *o_out, float *lse_out,
+                                verkv_head_stats *stats_out);
+
+/* Copy the per-query-head fetch sets F of the preceding verkv_attend_verified (Eq. (10):
+ * F = L \ L_g[k*:]) into `out`, device or page-locked host uint32
+ * [batch * kv_heads * q_per_kv][ceil(n/32)] (bit i%32 of word i/32 set iff token i is in F).
+ * Stream-ordered; VERKV_ESTATE if no attend has run on this context. */
+verkv_status verkv_selection_bitmap(verkv_ctx *ctx, uint32_t *out);
+
+/* Wait for all work on the context's streams, then return (and clear) the first error latched
+ * by the device since the previous verkv_sync, or a pending CUDA error. */
+verkv_status verkv_sync(verkv_ctx *ctx);
+
+/* Text of the last error on this context ("" if none). */
+const char *verkv_last_error(verkv_ctx *ctx);
+
+/* Name of a status code. */
+const char *verkv_status_string(int status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* VERKV_H */

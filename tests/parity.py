@@ -1,0 +1,174 @@
+"""GPU-vs-oracle parity harness: runs a seeded workload through libverkv (via the engine, i.e. the
+C ABI) and through the fp64 oracle, and compares them element by element.
+
+Tolerances (derivation in DESIGN.md, "Parity bar"):
+  * PoissonComp: c32, r, the resident bitmap, pivotal ids / r / rows -- bit-exact.
+  * Certificate decision: may differ only when the oracle's eps-hat(L) lies within EPS_TIE = 1e-5
+    relative of eps (the stated bar).
+  * k*: must lie in the oracle's acceptable set {k : eps_o(k) < eps (1 + EPS_TIE) and
+    (k = 0 or eps_o(k-1) >= eps (1 - EPS_TIE))} along the oracle's order.
+  * F: equal to the oracle's top-k* set, except for swaps among tokens whose oracle g lies within
+    G_TIE relative of g at the cut (float32 logits carry up to ~1e-5 relative error into w-hat).
+  * D-hat, N-hat, o: relative error <= 1e-3 (bf16 storage, fp32 accumulation); checked on every
+    head whose F equals the oracle's (a near-tie swap changes which estimator is returned).
+"""
+import numpy as np
+import torch
+
+import oracle as O
+from verified_kv_cache_poissoncomp_gb300 import binding as B
+from verified_kv_cache_poissoncomp_gb300.engine import VerKV, default_cap, stats_to_dict
+
+EPS_TIE = 1e-5
+G_TIE = 1e-4
+EST_TOL = 1e-3
+
+
+def bits_to_bool(words, n):
+    w = np.ascontiguousarray(words).view(np.uint32)
+    bits = ((w[..., None] >> np.arange(32, dtype=np.uint32)) & 1).astype(bool)
+    return bits.reshape(*w.shape[:-1], -1)[..., :n]
+
+
+# ------------------------------------------------------------------------------------------------
+def make_engine(w, cap=None, fetch_mode=B.VERKV_FETCH_ZEROCOPY):
+    cap = cap or default_cap(w.n, w.eta)
+    eng = VerKV(w.B, w.L, w.h_kv, w.G, w.d, w.n, cap, fetch_mode=fetch_mode)
+    eng.load(w.tau.reshape(-1, w.n), w.kv.reshape(-1, w.n, 2, w.d))
+    return eng
+
+
+def oracle_poissoncomp(w):
+    out = {}
+    for b in range(w.B):
+        for l in range(w.L):
+            for h in range(w.h_kv):
+                out[(b, l, h)] = O.poissoncomp(w.tau[b, l, h], w.eta, w.n_sink, w.n_local,
+                                               w.seed, b, l, h)
+    return out
+
+
+def check_poissoncomp(eng, w, pcs):
+    """Bit-exact comparison of the pivotal set against the oracle."""
+    torch.cuda.synchronize()
+    r = eng.r_full.cpu().numpy()
+    res = bits_to_bool(eng.p_res.cpu().numpy(), w.n)
+    ids = eng.p_ids.cpu().numpy()
+    pr = eng.p_r.cpu().numpy()
+    cnt = eng.p_count.cpu().numpy()
+    c = eng.p_c.cpu().numpy()
+    pkv = eng.p_kv.cpu().numpy().view(np.uint16)
+    u = 0
+    for b in range(w.B):
+        for l in range(w.L):
+            for h in range(w.h_kv):
+                o = pcs[(b, l, h)]
+                assert np.float32(c[u]) == o["c32"], (u, c[u], o["c32"])
+                assert np.array_equal(r[u], o["r32"]), u
+                assert np.array_equal(res[u], o["resident"]), u
+                want = np.nonzero(o["resident"])[0]
+                assert cnt[u] == len(want) == o["count"], (u, cnt[u], len(want))
+                assert np.array_equal(ids[u, :cnt[u]], want), u
+                assert np.array_equal(pr[u, :cnt[u]], o["r32"][want]), u
+                assert np.array_equal(pkv[u, :cnt[u]], w.kv[b, l, h][want]), u
+                u += 1
+
+
+# ------------------------------------------------------------------------------------------------
+def gpu_query(eng, w, t, eps=None, delta=None):
+    eps = w.eps if eps is None else eps
+    delta = w.delta if delta is None else delta
+    q = torch.as_tensor(w.queries[t].view(np.int16)).to(eng.dev)
+    eng.attend(int(w.query_layer[t]), q, eps, delta)
+    F = eng.selection_bitmap()
+    o, lse, stats = eng.fetch_refine()
+    eng.sync()
+    return dict(o=o.cpu().numpy().copy(), lse=lse.cpu().numpy().copy(),
+                stats=stats_to_dict(stats), F=bits_to_bool(F.cpu().numpy(), w.n),
+                ids=eng.fetch_ids.cpu().numpy().copy(), counts=eng.fetch_counts.cpu().numpy().copy())
+
+
+def oracle_query(w, t, pcs, eps=None, delta=None):
+    eps = w.eps if eps is None else eps
+    delta = w.delta if delta is None else delta
+    l = int(w.query_layer[t])
+    units = []
+    for b in range(w.B):
+        for h in range(w.h_kv):
+            pc = pcs[(b, l, h)]
+            K = O.bf16_to_f64(w.kv[b, l, h, :, 0, :])
+            V = O.bf16_to_f64(w.kv[b, l, h, :, 1, :])
+            qs = O.bf16_to_f64(w.queries[t, b, h * w.G:(h + 1) * w.G])
+            units.append(O.attend_unit(qs, K, K, V, pc["r32"], pc["resident"], eps, delta))
+    return units
+
+
+def compare_query(g, units, w, eps=None, report=None):
+    """Asserts the tie-aware parity bar for one query; returns counters."""
+    eps = w.eps if eps is None else eps
+    rep = report if report is not None else dict(heads=0, exact_F=0, tie_F=0, tie_decision=0,
+                                                 max_lse=0.0, max_o=0.0, max_eps_rel=0.0,
+                                                 max_beta_rel=0.0)
+    st = g["stats"]
+    for ul, unit in enumerate(units):
+        unit_exact = True
+        tie_tokens = set()
+        for gi, hd in enumerate(unit["heads"]):
+            qh = ul * w.G + gi
+            cert, est = hd["cert"], hd["est"]
+            rep["heads"] += 1
+            gcert = bool(st["certified"][qh])
+            # eps-hat and beta
+            e_rel = abs(float(st["eps_hat"][qh]) - cert["eps_L"]) / max(cert["eps_L"], 1e-30)
+            rep["max_eps_rel"] = max(rep["max_eps_rel"], e_rel)
+            if cert["beta"] > 0:
+                b_rel = abs(float(st["beta"][qh]) * np.exp(float(st["m"][qh]) - cert["m"]) -
+                            cert["beta"]) / cert["beta"]
+                rep["max_beta_rel"] = max(rep["max_beta_rel"], b_rel)
+            assert st["n_L"][qh] == cert["n_L"], (qh, st["n_L"][qh], cert["n_L"])
+            if gcert != cert["certified"]:
+                assert abs(cert["eps_L"] - eps) <= EPS_TIE * eps, \
+                    (qh, gcert, cert["eps_L"], float(st["eps_hat"][qh]))
+                rep["tie_decision"] += 1
+                unit_exact = False
+                tie_tokens |= set(np.nonzero(g["F"][qh] | cert["F"])[0].tolist())
+                continue
+            Fg = g["F"][qh]
+            k = int(st["k_star"][qh])
+            assert int(Fg.sum()) == k, (qh, int(Fg.sum()), k)
+            ek = cert["eps_k"]
+            if not gcert:
+                assert k >= 1 and ek[k] < eps * (1 + EPS_TIE) and ek[k - 1] >= eps * (1 - EPS_TIE), \
+                    (qh, k, cert["k_star"], ek[max(k - 1, 0)], ek[k])
+            else:
+                assert k == 0 and not Fg.any()
+            if np.array_equal(Fg, cert["F"]):
+                rep["exact_F"] += 1
+                assert st["n_fetch"][qh] == cert["n_fetch"]
+                # estimator: lse (log D-hat) and o
+                dl = abs(float(g["lse"][qh]) - est["lse"])
+                rep["max_lse"] = max(rep["max_lse"], dl)
+                assert dl <= EST_TOL, (qh, float(g["lse"][qh]), est["lse"])
+                oe = np.linalg.norm(g["o"][qh] - est["o"]) / max(np.linalg.norm(est["o"]), 1e-30)
+                rep["max_o"] = max(rep["max_o"], oe)
+                assert oe <= EST_TOL, (qh, oe)
+            else:
+                rep["tie_F"] += 1
+                unit_exact = False
+                order = cert["order"]
+                gv = cert["g"]
+                top = np.zeros(w.n, dtype=bool)
+                top[order[:k]] = True
+                diff = np.nonzero(Fg ^ top)[0]
+                gb = gv[order[k - 1]] if k >= 1 else gv[order[0]]
+                for tok in diff:
+                    assert abs(gv[tok] - gb) <= G_TIE * gb, (qh, int(tok), gv[tok], gb)
+                    tie_tokens.add(int(tok))
+        got = set(g["ids"][ul, :g["counts"][ul]].tolist())
+        want = set(unit["fetch_ids"].tolist())
+        assert list(g["ids"][ul, :g["counts"][ul]]) == sorted(got)
+        if unit_exact:
+            assert got == want, (ul, len(got), len(want))
+        else:
+            assert (got ^ want) <= tie_tokens, (ul, sorted(got ^ want)[:10])
+    return rep

@@ -1,0 +1,64 @@
+"""The C ABI library builds, loads without a GPU and exports every function include/verkv.h
+declares; shape validation and status names need no GPU either."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from verified_kv_cache_poissoncomp_gb300 import binding as B
+from verified_kv_cache_poissoncomp_gb300 import build as build_mod
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build_mod.build()
+    return B.lib()
+
+
+def declared_functions():
+    with open(os.path.join(ROOT, "include", "verkv.h")) as f:
+        text = f.read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(verkv_[a-z_]+)\s*\(", text)))
+
+
+def test_exports_every_declared_symbol(lib):
+    names = declared_functions()
+    assert len(names) >= 12
+    for name in names:
+        assert hasattr(lib, name), name
+    assert sorted(B.EXPORTED) == names
+
+
+def test_workspace_size_and_shape_validation(lib):
+    good = B.verkv_shape(1, 1, 8, 4, 128, 32768, 2600)
+    ws = B.verkv_workspace_size(good)
+    # scores 32*32768*4 + staging 8*32768*512 dominate
+    assert ws >= 32 * 32768 * 4 + 8 * 32768 * 512
+    bad = [B.verkv_shape(1, 1, 8, 3, 128, 32768, 2600),     # G not a power of two
+           B.verkv_shape(1, 1, 8, 4, 96, 32768, 2600),      # d
+           B.verkv_shape(1, 1, 8, 4, 128, 200000, 2600),    # n too large
+           B.verkv_shape(1, 1, 8, 4, 128, 1000, 2000),      # cap > n
+           B.verkv_shape(0, 1, 8, 4, 128, 1000, 100)]       # batch
+    for s in bad:
+        assert B.verkv_workspace_size(s) == 0
+    # verkv_create rejects a bad shape or workspace before touching CUDA.
+    ctx = ctypes.c_void_p()
+    assert lib.verkv_create(ctypes.byref(ctx), 0, None, ctypes.byref(bad[0]), 256, 1 << 30) == \
+        B.VERKV_EINVAL
+    assert lib.verkv_create(ctypes.byref(ctx), 0, None, ctypes.byref(good), 0, ws) == B.VERKV_EINVAL
+    assert lib.verkv_create(ctypes.byref(ctx), 0, None, ctypes.byref(good), 256, ws - 1) == \
+        B.VERKV_EINVAL
+    assert lib.verkv_create(ctypes.byref(ctx), 0, None, ctypes.byref(good), 257, ws) == \
+        B.VERKV_EINVAL
+
+
+def test_null_context_and_status_names(lib):
+    assert lib.verkv_sync(None) == B.VERKV_EINVAL
+    assert lib.verkv_fetch_refine(None, None, None, None, None, None, None) == B.VERKV_EINVAL
+    assert lib.verkv_last_error(None) == b""
+    for st, name in [(0, "VERKV_OK"), (2, "VERKV_EBUDGET"), (8, "VERKV_ESTATE")]:
+        assert B.verkv_status_string(st) == name

@@ -1,0 +1,108 @@
+"""GPU KVFetch (certificate, selection, estimator, fetch and refine) against the fp64 oracle
+under the tie-aware parity bar of tests/parity.py."""
+import numpy as np
+import pytest
+import torch
+
+from tests import parity as P
+from verified_kv_cache_poissoncomp_gb300 import binding as B
+from verified_kv_cache_poissoncomp_gb300 import inputs as I
+
+pytestmark = pytest.mark.gpu
+
+
+def _run_all(w, queries=None, eps=None, fetch_mode=B.VERKV_FETCH_ZEROCOPY, cap=None):
+    eng = P.make_engine(w, cap=cap, fetch_mode=fetch_mode)
+    eng.compress(w.eta, w.n_sink, w.n_local, w.seed)
+    eng.sync()
+    pcs = P.oracle_poissoncomp(w)
+    P.check_poissoncomp(eng, w, pcs)
+    rep = None
+    outs = []
+    for t in (range(w.queries.shape[0]) if queries is None else queries):
+        g = P.gpu_query(eng, w, t, eps=eps)
+        units = P.oracle_query(w, t, pcs, eps=eps)
+        rep = P.compare_query(g, units, w, eps=eps, report=rep)
+        outs.append(g)
+    print(rep)
+    return rep, outs
+
+
+def test_tiny_all_queries():
+    rep, _ = _run_all(I.tiny())
+    assert rep["exact_F"] >= 0.9 * rep["heads"]
+
+
+def test_multi_cta_ragged():
+    # n = 20000: three-CTA certify cluster, ragged last CTA; batch 2, two layers, 2 KV heads.
+    w = I.make_workload("mid", B=2, L=2, h_kv=2, G=4, d=128, n=20000, n_queries=6, n_local=512)
+    rep, _ = _run_all(w)
+    assert rep["exact_F"] >= 0.9 * rep["heads"]
+
+
+@pytest.mark.parametrize("G,d", [(1, 64), (2, 64), (8, 64), (2, 128), (8, 128)])
+def test_gqa_and_head_dims(G, d):
+    w = I.make_workload("gqa", B=1, L=1, h_kv=2, G=G, d=d, n=3000, eta=1 / 8, n_local=64,
+                        n_queries=4, plant_every=2)
+    rep, _ = _run_all(w)
+    assert rep["exact_F"] >= 0.9 * rep["heads"]
+
+
+def test_single_layer_32k_sampled_queries():
+    # The benchmark's layer shape at full size: 8 KV heads x 4 query heads, d = 128, n = 32768,
+    # eta = 1/16; plain and planted queries.
+    w = I.single_layer_32k(layers=1, n_queries=8)
+    rep, _ = _run_all(w, queries=[0, 1, 2, 3, 7])
+    assert rep["exact_F"] >= 0.9 * rep["heads"]
+
+
+def test_128k_context():
+    w = I.make_workload("128k", B=1, L=1, h_kv=1, G=4, d=128, n=131072, eta=1 / 32,
+                        n_queries=4, plant_every=2)
+    rep, _ = _run_all(w)
+    assert rep["exact_F"] >= 0.9 * rep["heads"]
+
+
+def test_memcpy_mode_matches_zerocopy():
+    w = I.make_workload("modes", B=1, L=1, h_kv=2, G=4, d=128, n=8192, eta=1 / 8, n_queries=4,
+                        plant_every=2)
+    _, a = _run_all(w)
+    _, b = _run_all(w, fetch_mode=B.VERKV_FETCH_MEMCPY)
+    for x, y in zip(a, b):
+        assert np.array_equal(x["o"], y["o"]) and np.array_equal(x["F"], y["F"])
+        assert np.array_equal(x["counts"], y["counts"])
+        for ul, c in enumerate(x["counts"]):
+            assert np.array_equal(x["ids"][ul, :c], y["ids"][ul, :c])
+
+
+def test_eta_one_is_dense_attention():
+    import oracle as O
+    w = I.make_workload("dense", B=1, L=1, h_kv=2, G=4, d=128, n=2048, eta=1.0, n_local=64,
+                        n_queries=2)
+    eng = P.make_engine(w, cap=2048)
+    eng.compress(w.eta, w.n_sink, w.n_local, w.seed)
+    for t in range(2):
+        g = P.gpu_query(eng, w, t)
+        assert np.all(g["stats"]["certified"] == 1) and np.all(g["stats"]["n_L"] == 0)
+        for h in range(w.h_kv):
+            K = O.bf16_to_f64(w.kv[0, 0, h, :, 0, :])
+            V = O.bf16_to_f64(w.kv[0, 0, h, :, 1, :])
+            for gi in range(w.G):
+                q = O.bf16_to_f64(w.queries[t, 0, h * w.G + gi])
+                dn = O.dense(O.logits(q, K), V)
+                qh = h * w.G + gi
+                assert np.linalg.norm(g["o"][qh] - dn["o"]) <= 1e-4 * np.linalg.norm(dn["o"])
+                assert abs(g["lse"][qh] - (dn["m"] + np.log(dn["D"]))) <= 1e-4
+
+
+def test_tiny_tolerance_fetches_all_of_L():
+    import oracle as O
+    w = I.tiny()
+    eng = P.make_engine(w)
+    eng.compress(w.eta, w.n_sink, w.n_local, w.seed)
+    K = O.bf16_to_f64(w.kv[0, 0, 0, :, 0, :])
+    V = O.bf16_to_f64(w.kv[0, 0, 0, :, 1, :])
+    g = P.gpu_query(eng, w, 0, eps=1e-30)
+    for gi in range(w.G):
+        dn = O.dense(O.logits(O.bf16_to_f64(w.queries[0, 0, gi]), K), V)
+        assert np.linalg.norm(g["o"][gi] - dn["o"]) <= 1e-4 * np.linalg.norm(dn["o"])

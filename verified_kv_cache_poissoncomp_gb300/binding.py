@@ -1,0 +1,186 @@
+"""ctypes binding of libverkv (include/verkv.h): the same names, argument marshalling only.
+
+Every function takes plain integers for device / host addresses (e.g. ``tensor.data_ptr()``) and
+raises ``VerkvError`` on a status other than VERKV_OK.  The library is loaded from this package
+directory; ``lib()`` raises if it has not been built (there is no fallback).
+"""
+import ctypes
+import os
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libverkv.so")
+
+VERKV_OK = 0
+VERKV_EINVAL = 1
+VERKV_EBUDGET = 2
+VERKV_ECAPACITY = 3
+VERKV_ENOCONVERGE = 4
+VERKV_ECUDA = 5
+VERKV_ECOPY = 6
+VERKV_ETIMEOUT = 7
+VERKV_ESTATE = 8
+
+VERKV_SKETCH_EXACT = 0
+VERKV_FETCH_ZEROCOPY = 0
+VERKV_FETCH_MEMCPY = 1
+
+EXPORTED = ["verkv_workspace_size", "verkv_create", "verkv_destroy", "verkv_set_fetch_mode",
+            "verkv_poissoncomp", "verkv_sketch_build", "verkv_attend_verified",
+            "verkv_fetch_refine", "verkv_selection_bitmap", "verkv_sync", "verkv_last_error",
+            "verkv_status_string"]
+
+
+class verkv_shape(ctypes.Structure):
+    _fields_ = [("batch", ctypes.c_int32), ("layers", ctypes.c_int32),
+                ("kv_heads", ctypes.c_int32), ("q_per_kv", ctypes.c_int32),
+                ("head_dim", ctypes.c_int32), ("n", ctypes.c_int32), ("cap", ctypes.c_int32)]
+
+
+class verkv_hset(ctypes.Structure):
+    _fields_ = [("n_sink", ctypes.c_int32), ("n_local", ctypes.c_int32)]
+
+
+class verkv_pivotal(ctypes.Structure):
+    _fields_ = [("ids", ctypes.c_void_p), ("r", ctypes.c_void_p), ("kv", ctypes.c_void_p),
+                ("count", ctypes.c_void_p), ("resident", ctypes.c_void_p),
+                ("c", ctypes.c_void_p)]
+
+
+class verkv_sketch(ctypes.Structure):
+    _fields_ = [("format", ctypes.c_int32), ("data", ctypes.c_void_p)]
+
+
+class verkv_head_stats(ctypes.Structure):
+    _fields_ = [(k, ctypes.c_float) for k in
+                ["m", "D", "beta", "V", "b", "eps_hat", "eps_final", "D_hat", "M2", "lse"]] + \
+               [(k, ctypes.c_int32) for k in
+                ["certified", "k_star", "n_L", "n_fetch", "iters", "flags"]]
+
+
+STATS_FLOAT_FIELDS = ["m", "D", "beta", "V", "b", "eps_hat", "eps_final", "D_hat", "M2", "lse"]
+STATS_INT_FIELDS = ["certified", "k_star", "n_L", "n_fetch", "iters", "flags"]
+assert ctypes.sizeof(verkv_head_stats) == 64
+
+
+class VerkvError(RuntimeError):
+    def __init__(self, status, msg=""):
+        self.status = status
+        super().__init__(f"{_status_name(status)}: {msg}")
+
+
+_lib = None
+
+
+def lib():
+    """Load libverkv.so; raise if it was not built."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"{LIB_PATH} is missing: build it with "
+                               "`python -m verified_kv_cache_poissoncomp_gb300.build`")
+        L = ctypes.CDLL(LIB_PATH)
+        vp, i32, sz = ctypes.c_void_p, ctypes.c_int32, ctypes.c_size_t
+        L.verkv_workspace_size.argtypes = [ctypes.POINTER(verkv_shape)]
+        L.verkv_workspace_size.restype = sz
+        L.verkv_create.argtypes = [ctypes.POINTER(vp), ctypes.c_int, vp,
+                                   ctypes.POINTER(verkv_shape), vp, sz]
+        L.verkv_create.restype = ctypes.c_int
+        L.verkv_destroy.argtypes = [vp]
+        L.verkv_destroy.restype = None
+        L.verkv_set_fetch_mode.argtypes = [vp, ctypes.c_int]
+        L.verkv_set_fetch_mode.restype = ctypes.c_int
+        L.verkv_poissoncomp.argtypes = [vp, vp, ctypes.c_double, verkv_hset, ctypes.c_uint64, vp,
+                                        vp, ctypes.POINTER(verkv_pivotal)]
+        L.verkv_poissoncomp.restype = ctypes.c_int
+        L.verkv_sketch_build.argtypes = [vp, vp, i32, vp]
+        L.verkv_sketch_build.restype = ctypes.c_int
+        L.verkv_attend_verified.argtypes = [vp, i32, vp, ctypes.POINTER(verkv_pivotal), vp,
+                                            ctypes.POINTER(verkv_sketch), ctypes.c_float,
+                                            ctypes.c_float, vp, vp]
+        L.verkv_attend_verified.restype = ctypes.c_int
+        L.verkv_fetch_refine.argtypes = [vp, vp, vp, vp, vp, vp, vp]
+        L.verkv_fetch_refine.restype = ctypes.c_int
+        L.verkv_selection_bitmap.argtypes = [vp, vp]
+        L.verkv_selection_bitmap.restype = ctypes.c_int
+        L.verkv_sync.argtypes = [vp]
+        L.verkv_sync.restype = ctypes.c_int
+        L.verkv_last_error.argtypes = [vp]
+        L.verkv_last_error.restype = ctypes.c_char_p
+        L.verkv_status_string.argtypes = [ctypes.c_int]
+        L.verkv_status_string.restype = ctypes.c_char_p
+        _lib = L
+    return _lib
+
+
+def _status_name(st):
+    try:
+        return lib().verkv_status_string(st).decode()
+    except Exception:  # noqa: BLE001 -- naming only
+        return f"status {st}"
+
+
+def _check(st, ctx=None):
+    if st != VERKV_OK:
+        msg = lib().verkv_last_error(ctx).decode() if ctx else ""
+        raise VerkvError(st, msg)
+
+
+# ------------------------------------------------------------------------------------------------
+def verkv_workspace_size(shape):
+    return int(lib().verkv_workspace_size(ctypes.byref(shape)))
+
+
+def verkv_create(device, stream, shape, workspace, workspace_bytes):
+    ctx = ctypes.c_void_p()
+    _check(lib().verkv_create(ctypes.byref(ctx), int(device), stream or None,
+                              ctypes.byref(shape), workspace, int(workspace_bytes)))
+    return ctx
+
+
+def verkv_destroy(ctx):
+    lib().verkv_destroy(ctx)
+
+
+def verkv_set_fetch_mode(ctx, mode):
+    _check(lib().verkv_set_fetch_mode(ctx, int(mode)), ctx)
+
+
+def verkv_poissoncomp(ctx, tau, eta, H, seed, kv_full, r_full, pivotal):
+    _check(lib().verkv_poissoncomp(ctx, tau, float(eta), H, int(seed), kv_full, r_full,
+                                   ctypes.byref(pivotal)), ctx)
+
+
+def verkv_sketch_build(ctx, kv_full, fmt, sketch_out):
+    _check(lib().verkv_sketch_build(ctx, kv_full, int(fmt), sketch_out), ctx)
+
+
+def verkv_attend_verified(ctx, layer, q, pivotal, r_full, sketch, eps, delta,
+                          fetch_ids_out=None, fetch_counts_out=None):
+    _check(lib().verkv_attend_verified(ctx, int(layer), q, ctypes.byref(pivotal), r_full,
+                                       ctypes.byref(sketch), float(eps), float(delta),
+                                       fetch_ids_out, fetch_counts_out), ctx)
+
+
+def verkv_fetch_refine(ctx, ids, counts, host_kv, o_out, lse_out=None, stats_out=None):
+    _check(lib().verkv_fetch_refine(ctx, ids, counts, host_kv, o_out, lse_out, stats_out), ctx)
+
+
+def verkv_selection_bitmap(ctx, out):
+    _check(lib().verkv_selection_bitmap(ctx, out), ctx)
+
+
+def verkv_sync(ctx):
+    _check(lib().verkv_sync(ctx), ctx)
+
+
+def verkv_sync_status(ctx):
+    """verkv_sync returning the raw status instead of raising."""
+    return int(lib().verkv_sync(ctx))
+
+
+def verkv_last_error(ctx):
+    return lib().verkv_last_error(ctx).decode()
+
+
+def verkv_status_string(status):
+    return lib().verkv_status_string(int(status)).decode()

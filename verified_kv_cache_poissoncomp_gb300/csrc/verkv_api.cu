@@ -1,0 +1,573 @@
+// verkv_api.cu -- the C ABI of libverkv: argument checks, workspace carve-up, stream and event
+// orchestration, and the host side of the fetch ("Verify Before You Fetch": the abstract page's
+// GPU-resident pivotal tokens and sketch with the complete cache in CPU memory; summary page,
+// KVFETCH steps 1-5).
+#include <cuda_runtime.h>
+#include <math.h>
+#include <stdint.h>
+#include <string.h>
+
+#include <algorithm>
+#include <condition_variable>
+#include <functional>
+#include <mutex>
+#include <string>
+#include <thread>
+#include <vector>
+
+#include "verkv_internal.h"
+
+using namespace verkv;
+
+namespace {
+
+size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
+
+struct Layout {
+    size_t err, scores, qstats, F, fids, fcounts, staging, part_piv, part_fet, total;
+    int W, units_layer, qh_layer, max_piv, max_fet;
+};
+
+bool valid_shape(const verkv_shape *s) {
+    if (!s) return false;
+    const int G = s->q_per_kv;
+    return s->batch >= 1 && s->layers >= 1 && s->kv_heads >= 1 &&
+           (G == 1 || G == 2 || G == 4 || G == 8) && (s->head_dim == 64 || s->head_dim == 128) &&
+           s->n >= 1 && s->n <= 131072 && s->cap >= 1 && s->cap <= s->n &&
+           (int64_t)s->batch * s->layers * s->kv_heads <= (1 << 24);
+}
+
+bool make_layout(const verkv_shape *s, Layout &L) {
+    if (!valid_shape(s)) return false;
+    const size_t n = (size_t)s->n, d = (size_t)s->head_dim, G = (size_t)s->q_per_kv;
+    L.W = (s->n + 31) / 32;
+    L.units_layer = s->batch * s->kv_heads;
+    L.qh_layer = L.units_layer * s->q_per_kv;
+    L.max_piv = (s->cap + PART_ROWS - 1) / PART_ROWS;
+    L.max_fet = (s->n + PART_ROWS - 1) / PART_ROWS;
+    size_t off = 0;
+    auto take = [&](size_t bytes) {
+        const size_t o = off;
+        off = align256(off + bytes);
+        return o;
+    };
+    L.err = take(256);
+    L.scores = take((size_t)L.qh_layer * n * 4);
+    L.qstats = take((size_t)L.qh_layer * sizeof(verkv_head_stats));
+    L.F = take((size_t)L.qh_layer * L.W * 4);
+    L.fids = take((size_t)L.units_layer * n * 4);
+    L.fcounts = take((size_t)L.units_layer * 4);
+    L.staging = take((size_t)L.units_layer * n * 4 * d);
+    L.part_piv = take((size_t)L.units_layer * L.max_piv * G * (d + 2) * 4);
+    L.part_fet = take((size_t)L.units_layer * L.max_fet * G * (d + 2) * 4);
+    L.total = off;
+    return true;
+}
+
+// A small fixed pool of host threads for the MEMCPY-mode gather.
+class Pool {
+  public:
+    explicit Pool(int nthreads) {
+        for (int i = 0; i < nthreads; ++i) workers_.emplace_back([this, i] { loop(i); });
+    }
+    ~Pool() {
+        {
+            std::lock_guard<std::mutex> g(mu_);
+            stop_ = true;
+        }
+        cv_.notify_all();
+        for (auto &t : workers_) t.join();
+    }
+    int size() const { return (int)workers_.size(); }
+    // Runs fn(worker_index) on every worker and waits for all of them.
+    void run(const std::function<void(int)> &fn) {
+        std::unique_lock<std::mutex> lk(mu_);
+        job_ = &fn;
+        pending_ = (int)workers_.size();
+        ++generation_;
+        cv_.notify_all();
+        done_cv_.wait(lk, [this] { return pending_ == 0; });
+        job_ = nullptr;
+    }
+
+  private:
+    void loop(int idx) {
+        uint64_t seen = 0;
+        for (;;) {
+            const std::function<void(int)> *job;
+            {
+                std::unique_lock<std::mutex> lk(mu_);
+                cv_.wait(lk, [&] { return stop_ || generation_ != seen; });
+                if (stop_) return;
+                seen = generation_;
+                job = job_;
+            }
+            (*job)(idx);
+            {
+                std::lock_guard<std::mutex> g(mu_);
+                if (--pending_ == 0) done_cv_.notify_all();
+            }
+        }
+    }
+    std::vector<std::thread> workers_;
+    std::mutex mu_;
+    std::condition_variable cv_, done_cv_;
+    const std::function<void(int)> *job_ = nullptr;
+    int pending_ = 0;
+    uint64_t generation_ = 0;
+    bool stop_ = false;
+};
+
+}  // namespace
+
+struct verkv_ctx {
+    int device = 0;
+    int sms = 0;
+    cudaStream_t main = nullptr, side = nullptr;
+    cudaEvent_t e_sel = nullptr, e_fetch = nullptr;
+    verkv_shape sh{};
+    Layout L{};
+    unsigned char *ws = nullptr;
+    uint32_t *err = nullptr;
+    float *scores = nullptr;
+    verkv_head_stats *qstats = nullptr;
+    uint32_t *F = nullptr;
+    int32_t *fids = nullptr, *fcounts = nullptr;
+    uint16_t *staging = nullptr;
+    float *part_piv = nullptr, *part_fet = nullptr;
+    int fetch_mode = VERKV_FETCH_ZEROCOPY;
+    // MEMCPY mode
+    unsigned char *host_staging = nullptr;
+    int32_t *host_ids = nullptr, *host_counts = nullptr;     // mapped page-locked
+    int32_t *host_ids_dev = nullptr, *host_counts_dev = nullptr;
+    Pool *pool = nullptr;
+    // The preceding attend
+    bool pending = false;
+    bool attended = false;
+    int layer = 0;
+    verkv_pivotal piv{};
+    const int32_t *user_ids = nullptr, *user_counts = nullptr;
+    const void *q = nullptr;
+    std::string last_error;
+};
+
+namespace {
+
+verkv_status fail(verkv_ctx *c, verkv_status st, const std::string &msg) {
+    if (c) c->last_error = msg;
+    return st;
+}
+
+verkv_status cuda_fail(verkv_ctx *c, cudaError_t e, const char *where) {
+    return fail(c, VERKV_ECUDA, std::string(where) + ": " + cudaGetErrorString(e));
+}
+
+#define VERKV_CUDA(call, where)                              \
+    do {                                                     \
+        cudaError_t e_ = (call);                             \
+        if (e_ != cudaSuccess) return cuda_fail(ctx, e_, where); \
+    } while (0)
+
+LayerIdx layer_idx(const verkv_ctx *ctx, int layer) {
+    LayerIdx li;
+    li.layers = ctx->sh.layers;
+    li.layer = layer;
+    li.kv_heads = ctx->sh.kv_heads;
+    li.G = ctx->sh.q_per_kv;
+    return li;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char *verkv_status_string(int st) {
+    switch (st) {
+        case VERKV_OK: return "VERKV_OK";
+        case VERKV_EINVAL: return "VERKV_EINVAL";
+        case VERKV_EBUDGET: return "VERKV_EBUDGET";
+        case VERKV_ECAPACITY: return "VERKV_ECAPACITY";
+        case VERKV_ENOCONVERGE: return "VERKV_ENOCONVERGE";
+        case VERKV_ECUDA: return "VERKV_ECUDA";
+        case VERKV_ECOPY: return "VERKV_ECOPY";
+        case VERKV_ETIMEOUT: return "VERKV_ETIMEOUT";
+        case VERKV_ESTATE: return "VERKV_ESTATE";
+        default: return "VERKV_UNKNOWN";
+    }
+}
+
+size_t verkv_workspace_size(const verkv_shape *shape) {
+    Layout L;
+    return make_layout(shape, L) ? L.total : 0;
+}
+
+verkv_status verkv_create(verkv_ctx **out, int device, void *stream, const verkv_shape *shape,
+                          void *workspace, size_t workspace_bytes) {
+    if (!out) return VERKV_EINVAL;
+    *out = nullptr;
+    Layout L;
+    if (!make_layout(shape, L)) return VERKV_EINVAL;
+    if (!workspace || workspace_bytes < L.total || ((uintptr_t)workspace & 255u)) return VERKV_EINVAL;
+    verkv_ctx *ctx = new verkv_ctx();
+    ctx->device = device;
+    ctx->sh = *shape;
+    ctx->L = L;
+    ctx->main = (cudaStream_t)stream;
+    ctx->ws = (unsigned char *)workspace;
+    cudaError_t e = cudaSetDevice(device);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&ctx->sms, cudaDevAttrMultiProcessorCount, device);
+    if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&ctx->side, cudaStreamNonBlocking);
+    if (e == cudaSuccess) e = cudaEventCreateWithFlags(&ctx->e_sel, cudaEventDisableTiming);
+    if (e == cudaSuccess) e = cudaEventCreateWithFlags(&ctx->e_fetch, cudaEventDisableTiming);
+    if (e != cudaSuccess) {
+        verkv_destroy(ctx);
+        return VERKV_ECUDA;
+    }
+    unsigned char *w = ctx->ws;
+    ctx->err = (uint32_t *)(w + L.err);
+    ctx->scores = (float *)(w + L.scores);
+    ctx->qstats = (verkv_head_stats *)(w + L.qstats);
+    ctx->F = (uint32_t *)(w + L.F);
+    ctx->fids = (int32_t *)(w + L.fids);
+    ctx->fcounts = (int32_t *)(w + L.fcounts);
+    ctx->staging = (uint16_t *)(w + L.staging);
+    ctx->part_piv = (float *)(w + L.part_piv);
+    ctx->part_fet = (float *)(w + L.part_fet);
+    e = cudaMemsetAsync(ctx->err, 0, 256, ctx->main);
+    if (e == cudaSuccess) e = cudaMemsetAsync(ctx->fcounts, 0, (size_t)L.units_layer * 4, ctx->main);
+    if (e != cudaSuccess) {
+        verkv_destroy(ctx);
+        return VERKV_ECUDA;
+    }
+    *out = ctx;
+    return VERKV_OK;
+}
+
+void verkv_destroy(verkv_ctx *ctx) {
+    if (!ctx) return;
+    if (ctx->main || ctx->side) {
+        if (ctx->main) cudaStreamSynchronize(ctx->main);
+        if (ctx->side) cudaStreamSynchronize(ctx->side);
+    }
+    delete ctx->pool;
+    if (ctx->host_staging) cudaFreeHost(ctx->host_staging);
+    if (ctx->host_ids) cudaFreeHost(ctx->host_ids);
+    if (ctx->host_counts) cudaFreeHost(ctx->host_counts);
+    if (ctx->e_sel) cudaEventDestroy(ctx->e_sel);
+    if (ctx->e_fetch) cudaEventDestroy(ctx->e_fetch);
+    if (ctx->side) cudaStreamDestroy(ctx->side);
+    delete ctx;
+}
+
+verkv_status verkv_set_fetch_mode(verkv_ctx *ctx, int mode) {
+    if (!ctx) return VERKV_EINVAL;
+    if (mode != VERKV_FETCH_ZEROCOPY && mode != VERKV_FETCH_MEMCPY)
+        return fail(ctx, VERKV_EINVAL, "unknown fetch mode");
+    if (mode == VERKV_FETCH_MEMCPY && !ctx->host_staging) {
+        const size_t rows = (size_t)ctx->L.units_layer * ctx->sh.n;
+        VERKV_CUDA(cudaSetDevice(ctx->device), "cudaSetDevice");
+        VERKV_CUDA(cudaHostAlloc((void **)&ctx->host_staging, rows * 4 * ctx->sh.head_dim,
+                                 cudaHostAllocDefault), "cudaHostAlloc(staging)");
+        VERKV_CUDA(cudaHostAlloc((void **)&ctx->host_ids, rows * 4, cudaHostAllocMapped),
+                   "cudaHostAlloc(ids)");
+        VERKV_CUDA(cudaHostAlloc((void **)&ctx->host_counts, (size_t)ctx->L.units_layer * 4,
+                                 cudaHostAllocMapped), "cudaHostAlloc(counts)");
+        VERKV_CUDA(cudaHostGetDevicePointer((void **)&ctx->host_ids_dev, ctx->host_ids, 0),
+                   "cudaHostGetDevicePointer(ids)");
+        VERKV_CUDA(cudaHostGetDevicePointer((void **)&ctx->host_counts_dev, ctx->host_counts, 0),
+                   "cudaHostGetDevicePointer(counts)");
+        unsigned hw = std::thread::hardware_concurrency();
+        ctx->pool = new Pool((int)std::max(1u, std::min(hw, 16u)));
+    }
+    ctx->fetch_mode = mode;
+    return VERKV_OK;
+}
+
+verkv_status verkv_poissoncomp(verkv_ctx *ctx, const float *tau, double eta, verkv_hset H,
+                               uint64_t seed, const void *kv_full, float *r_full,
+                               const verkv_pivotal *out) {
+    if (!ctx) return VERKV_EINVAL;
+    if (!tau || !kv_full || !r_full || !out || !out->ids || !out->r || !out->kv || !out->count ||
+        !out->resident || !out->c)
+        return fail(ctx, VERKV_EINVAL, "poissoncomp: null pointer");
+    if (!(eta > 0.0) || eta > 1.0 || H.n_sink < 0 || H.n_local < 0)
+        return fail(ctx, VERKV_EINVAL, "poissoncomp: eta must be in (0, 1], H sizes >= 0");
+    const int n = ctx->sh.n;
+    const int64_t forced = std::min<int64_t>(n, (int64_t)H.n_sink + H.n_local);
+    const int n_rest = (int)(n - forced);
+    const double eta_n = eta * (double)n;
+    const double b_rest = eta_n - (double)forced;
+    if (n_rest > 0 && !(b_rest > 0.0))
+        return fail(ctx, VERKV_EBUDGET, "poissoncomp: eta * n must exceed the forced H set");
+    VERKV_CUDA(cudaSetDevice(ctx->device), "cudaSetDevice");
+    const int units = ctx->sh.batch * ctx->sh.layers * ctx->sh.kv_heads;
+    PcArgs a{};
+    a.tau = tau;
+    a.r_full = r_full;
+    a.ids = out->ids;
+    a.pr = out->r;
+    a.count = out->count;
+    a.resident = out->resident;
+    a.c_out = out->c;
+    a.err = ctx->err;
+    a.b_rest = b_rest;
+    a.eta_n = eta_n;
+    a.n = n;
+    a.W = ctx->L.W;
+    a.cap = ctx->sh.cap;
+    a.n_sink = H.n_sink;
+    a.n_local = H.n_local;
+    a.layers = ctx->sh.layers;
+    a.kv_heads = ctx->sh.kv_heads;
+    a.n_rest = n_rest;
+    int cl = (n + 32767) / 32768;
+    cl = std::max(1, std::min(cl, 8));
+    int chunk = (n + cl - 1) / cl;
+    chunk = (chunk + 1023) / 1024 * 1024;
+    a.cl = cl;
+    a.chunk = chunk;
+    a.seed_lo = (uint32_t)seed;
+    a.seed_hi = (uint32_t)(seed >> 32);
+    VERKV_CUDA(launch_pc_solve(a, units, ctx->main), "k_pc_solve");
+    VERKV_CUDA(launch_pc_gather((const uint16_t *)kv_full, out->ids, out->count,
+                                (uint16_t *)out->kv, units, ctx->sh.cap, n, ctx->sh.head_dim,
+                                ctx->main), "k_pc_gather");
+    return VERKV_OK;
+}
+
+verkv_status verkv_sketch_build(verkv_ctx *ctx, const void *kv_full, int32_t format,
+                                void *sketch_out) {
+    if (!ctx) return VERKV_EINVAL;
+    if (!kv_full || !sketch_out) return fail(ctx, VERKV_EINVAL, "sketch_build: null pointer");
+    if (format != VERKV_SKETCH_EXACT) return fail(ctx, VERKV_EINVAL, "sketch_build: unknown format");
+    VERKV_CUDA(cudaSetDevice(ctx->device), "cudaSetDevice");
+    const int64_t rows = (int64_t)ctx->sh.batch * ctx->sh.layers * ctx->sh.kv_heads * ctx->sh.n;
+    VERKV_CUDA(launch_sketch_exact((const uint16_t *)kv_full, (uint16_t *)sketch_out, rows,
+                                   ctx->sh.head_dim, ctx->main), "k_sketch_exact");
+    return VERKV_OK;
+}
+
+verkv_status verkv_attend_verified(verkv_ctx *ctx, int32_t layer, const void *q,
+                                   const verkv_pivotal *pivotal, const float *r_full,
+                                   const verkv_sketch *sketch, float eps, float delta,
+                                   int32_t *fetch_ids_out, int32_t *fetch_counts_out) {
+    if (!ctx) return VERKV_EINVAL;
+    if (layer < 0 || layer >= ctx->sh.layers) return fail(ctx, VERKV_EINVAL, "attend: bad layer");
+    if (!q || !pivotal || !r_full || !sketch || !sketch->data || !pivotal->ids || !pivotal->r ||
+        !pivotal->kv || !pivotal->count || !pivotal->resident)
+        return fail(ctx, VERKV_EINVAL, "attend: null pointer");
+    if (sketch->format != VERKV_SKETCH_EXACT) return fail(ctx, VERKV_EINVAL, "attend: unknown sketch format");
+    if (!(eps > 0.0f) || !(delta > 0.0f) || !(delta < 1.0f) || !isfinite(eps))
+        return fail(ctx, VERKV_EINVAL, "attend: need eps > 0 and 0 < delta < 1");
+    if ((fetch_ids_out == nullptr) != (fetch_counts_out == nullptr))
+        return fail(ctx, VERKV_EINVAL, "attend: give both fetch_ids_out and fetch_counts_out or neither");
+    VERKV_CUDA(cudaSetDevice(ctx->device), "cudaSetDevice");
+    const LayerIdx li = layer_idx(ctx, layer);
+    const int n = ctx->sh.n, d = ctx->sh.head_dim;
+
+    ScoreArgs sa{};
+    sa.sketch = (const uint16_t *)sketch->data;
+    sa.q = (const uint16_t *)q;
+    sa.scores = ctx->scores;
+    sa.n = n;
+    sa.d = d;
+    sa.scale = (float)(1.0 / sqrt((double)d));
+    sa.li = li;
+    VERKV_CUDA(launch_score(sa, ctx->L.units_layer, ctx->main), "k_score");
+
+    CertifyArgs ca{};
+    ca.scores = ctx->scores;
+    ca.r_full = r_full;
+    ca.resident = pivotal->resident;
+    ca.F = ctx->F;
+    ca.qstats = ctx->qstats;
+    ca.err = ctx->err;
+    ca.n = n;
+    ca.W = ctx->L.W;
+    ca.cl = certify_cluster_size(n);
+    ca.chunk = certify_chunk(n, ca.cl);
+    ca.eps = eps;
+    ca.ldelta = (float)log(2.0 / (double)delta);
+    ca.li = li;
+    VERKV_CUDA(launch_certify(ca, ctx->L.qh_layer, certify_smem_bytes(ca.chunk), ctx->main),
+               "k_certify");
+
+    FetchListArgs fa{};
+    fa.F = ctx->F;
+    fa.resident = pivotal->resident;
+    fa.ids = ctx->fids;
+    fa.counts = ctx->fcounts;
+    fa.ids_user = fetch_ids_out;
+    fa.counts_user = fetch_counts_out;
+    if (ctx->fetch_mode == VERKV_FETCH_MEMCPY) {
+        fa.ids_host = ctx->host_ids_dev;
+        fa.counts_host = ctx->host_counts_dev;
+    }
+    fa.qstats = ctx->qstats;
+    fa.n = n;
+    fa.W = ctx->L.W;
+    fa.li = li;
+    VERKV_CUDA(launch_fetchlist(fa, ctx->L.units_layer, ctx->main), "k_fetchlist");
+    VERKV_CUDA(cudaEventRecord(ctx->e_sel, ctx->main), "cudaEventRecord");
+
+    PartialArgs pa{};
+    pa.rows = (const uint16_t *)pivotal->kv;
+    pa.ids = pivotal->ids;
+    pa.pr = pivotal->r;
+    pa.count = pivotal->count;
+    pa.q = (const uint16_t *)q;
+    pa.F = ctx->F;
+    pa.qstats = ctx->qstats;
+    pa.part = ctx->part_piv;
+    pa.row_stride = ctx->sh.cap;
+    pa.max_chunks = ctx->L.max_piv;
+    pa.n = n;
+    pa.W = ctx->L.W;
+    pa.d = d;
+    pa.pivotal = 1;
+    pa.scale = sa.scale;
+    pa.li = li;
+    int grid = std::min(ctx->L.units_layer * ctx->L.max_piv, ctx->sms * 8);
+    VERKV_CUDA(launch_partial(pa, ctx->L.units_layer, std::max(grid, 1), ctx->main), "k_partial");
+
+    ctx->pending = true;
+    ctx->attended = true;
+    ctx->layer = layer;
+    ctx->piv = *pivotal;
+    ctx->user_ids = fetch_ids_out;
+    ctx->user_counts = fetch_counts_out;
+    ctx->q = q;
+    return VERKV_OK;
+}
+
+verkv_status verkv_fetch_refine(verkv_ctx *ctx, const int32_t *ids, const int32_t *counts,
+                                const void *host_kv, float *o_out, float *lse_out,
+                                verkv_head_stats *stats_out) {
+    if (!ctx) return VERKV_EINVAL;
+    if (!ctx->pending) return fail(ctx, VERKV_ESTATE, "fetch_refine: no preceding attend_verified");
+    if ((ids || counts) && (ids != ctx->user_ids || counts != ctx->user_counts))
+        return fail(ctx, VERKV_EINVAL, "fetch_refine: ids/counts must be the attend outputs or NULL");
+    if (!host_kv || !o_out) return fail(ctx, VERKV_EINVAL, "fetch_refine: null pointer");
+    VERKV_CUDA(cudaSetDevice(ctx->device), "cudaSetDevice");
+    const LayerIdx li = layer_idx(ctx, ctx->layer);
+    const int n = ctx->sh.n, d = ctx->sh.head_dim;
+    const size_t row_bytes = (size_t)4 * d;
+
+    if (ctx->fetch_mode == VERKV_FETCH_ZEROCOPY) {
+        cudaPointerAttributes attr;
+        cudaError_t e = cudaPointerGetAttributes(&attr, host_kv);
+        if (e != cudaSuccess || attr.type != cudaMemoryTypeHost || !attr.devicePointer) {
+            cudaGetLastError();
+            return fail(ctx, VERKV_EINVAL, "fetch_refine: host_kv is not page-locked host memory");
+        }
+        VERKV_CUDA(cudaStreamWaitEvent(ctx->side, ctx->e_sel, 0), "cudaStreamWaitEvent");
+        GatherArgs ga{};
+        ga.host_kv = (const uint16_t *)attr.devicePointer;
+        ga.ids = ctx->fids;
+        ga.counts = ctx->fcounts;
+        ga.staging = ctx->staging;
+        ga.n = n;
+        ga.d = d;
+        ga.li = li;
+        VERKV_CUDA(launch_gather_host(ga, ctx->L.units_layer, ctx->side), "k_gather_host");
+    } else {
+        VERKV_CUDA(cudaEventSynchronize(ctx->e_sel), "cudaEventSynchronize");
+        const int U = ctx->L.units_layer;
+        const unsigned char *src_base = (const unsigned char *)host_kv;
+        // Flatten (unit, row) into one index space and split it evenly over the pool.
+        std::vector<int64_t> start(U + 1, 0);
+        for (int ul = 0; ul < U; ++ul) start[ul + 1] = start[ul] + ctx->host_counts[ul];
+        const int64_t total = start[U];
+        const int P = ctx->pool->size();
+        ctx->pool->run([&](int w) {
+            const int64_t lo = total * w / P, hi = total * (w + 1) / P;
+            int ul = (int)(std::upper_bound(start.begin(), start.end(), lo) - start.begin()) - 1;
+            for (int64_t x = lo; x < hi; ++x) {
+                while (x >= start[ul + 1]) ++ul;
+                const int64_t j = x - start[ul];
+                const int ug = li.unit_global(ul);
+                const int id = ctx->host_ids[(size_t)ul * n + j];
+                memcpy(ctx->host_staging + ((size_t)ul * n + j) * row_bytes,
+                       src_base + ((size_t)ug * n + id) * row_bytes, row_bytes);
+            }
+        });
+        for (int ul = 0; ul < U; ++ul) {
+            const int cnt = ctx->host_counts[ul];
+            if (cnt <= 0) continue;
+            cudaError_t e = cudaMemcpyAsync((unsigned char *)ctx->staging + (size_t)ul * n * row_bytes,
+                                            ctx->host_staging + (size_t)ul * n * row_bytes,
+                                            (size_t)cnt * row_bytes, cudaMemcpyHostToDevice, ctx->side);
+            if (e != cudaSuccess)
+                return fail(ctx, VERKV_ECOPY, std::string("fetch copy: ") + cudaGetErrorString(e));
+        }
+    }
+    VERKV_CUDA(cudaEventRecord(ctx->e_fetch, ctx->side), "cudaEventRecord");
+    VERKV_CUDA(cudaStreamWaitEvent(ctx->main, ctx->e_fetch, 0), "cudaStreamWaitEvent");
+
+    PartialArgs pa{};
+    pa.rows = ctx->staging;
+    pa.ids = ctx->fids;
+    pa.pr = nullptr;
+    pa.count = ctx->fcounts;
+    pa.q = (const uint16_t *)ctx->q;
+    pa.F = ctx->F;
+    pa.qstats = ctx->qstats;
+    pa.part = ctx->part_fet;
+    pa.row_stride = n;
+    pa.max_chunks = ctx->L.max_fet;
+    pa.n = n;
+    pa.W = ctx->L.W;
+    pa.d = d;
+    pa.pivotal = 0;
+    pa.scale = (float)(1.0 / sqrt((double)d));
+    pa.li = li;
+    const int grid = std::max(1, std::min(ctx->L.units_layer * ctx->L.max_fet, ctx->sms * 8));
+    VERKV_CUDA(launch_partial(pa, ctx->L.units_layer, grid, ctx->main), "k_partial(fetched)");
+
+    MergeArgs ma{};
+    ma.part_piv = ctx->part_piv;
+    ma.part_fet = ctx->part_fet;
+    ma.pcount = ctx->piv.count;
+    ma.fcount = ctx->fcounts;
+    ma.qstats = ctx->qstats;
+    ma.o = o_out;
+    ma.lse = lse_out;
+    ma.stats = stats_out;
+    ma.max_piv = ctx->L.max_piv;
+    ma.max_fet = ctx->L.max_fet;
+    ma.cap = ctx->sh.cap;
+    ma.d = d;
+    ma.li = li;
+    VERKV_CUDA(launch_merge(ma, ctx->L.qh_layer, ctx->main), "k_merge");
+    ctx->pending = false;
+    return VERKV_OK;
+}
+
+verkv_status verkv_sync(verkv_ctx *ctx) {
+    if (!ctx) return VERKV_EINVAL;
+    VERKV_CUDA(cudaSetDevice(ctx->device), "cudaSetDevice");
+    VERKV_CUDA(cudaStreamSynchronize(ctx->side), "cudaStreamSynchronize(side)");
+    VERKV_CUDA(cudaStreamSynchronize(ctx->main), "cudaStreamSynchronize(main)");
+    uint32_t word = 0;
+    VERKV_CUDA(cudaMemcpy(&word, ctx->err, sizeof(word), cudaMemcpyDeviceToHost), "read error word");
+    if (word == 0) return VERKV_OK;
+    VERKV_CUDA(cudaMemset(ctx->err, 0, sizeof(word)), "clear error word");
+    if (word & ERR_TAU) return fail(ctx, VERKV_EINVAL, "tau outside (0, 1] or not finite");
+    if (word & ERR_CAPACITY) return fail(ctx, VERKV_ECAPACITY, "pivotal set exceeded cap (truncated)");
+    if (word & ERR_BUDGET_SUM) return fail(ctx, VERKV_ENOCONVERGE, "|sum r - eta n| >= 1e-6 n");
+    return fail(ctx, VERKV_ENOCONVERGE, "a solve hit its iteration cap");
+}
+
+verkv_status verkv_selection_bitmap(verkv_ctx *ctx, uint32_t *out) {
+    if (!ctx) return VERKV_EINVAL;
+    if (!ctx->attended) return fail(ctx, VERKV_ESTATE, "selection_bitmap: no attend has run");
+    if (!out) return fail(ctx, VERKV_EINVAL, "selection_bitmap: null pointer");
+    VERKV_CUDA(cudaSetDevice(ctx->device), "cudaSetDevice");
+    VERKV_CUDA(cudaMemcpyAsync(out, ctx->F, (size_t)ctx->L.qh_layer * ctx->L.W * 4,
+                               cudaMemcpyDefault, ctx->main), "copy F");
+    return VERKV_OK;
+}
+
+const char *verkv_last_error(verkv_ctx *ctx) { return ctx ? ctx->last_error.c_str() : ""; }
+
+}  // extern "C"

@@ -1,0 +1,189 @@
+// verkv_common.cuh -- device helpers shared by libverkv's kernels (sm_103a).
+#pragma once
+
+#include <cooperative_groups.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "verkv_internal.h"
+
+namespace verkv {
+
+namespace cg = cooperative_groups;
+
+__device__ __forceinline__ void raise_error(uint32_t *err, uint32_t bit) { atomicOr(err, bit); }
+
+// ---------------------------------------------------------------------------------------------
+// bf16 pairs packed in a 32-bit word: element 0 in the low half.
+__device__ __forceinline__ float bf16lo(uint32_t x) { return __uint_as_float(x << 16); }
+__device__ __forceinline__ float bf16hi(uint32_t x) { return __uint_as_float(x & 0xFFFF0000u); }
+
+__device__ __forceinline__ void unpack8(const uint4 &v, float (&f)[8]) {
+    f[0] = bf16lo(v.x); f[1] = bf16hi(v.x);
+    f[2] = bf16lo(v.y); f[3] = bf16hi(v.y);
+    f[4] = bf16lo(v.z); f[5] = bf16hi(v.z);
+    f[6] = bf16lo(v.w); f[7] = bf16hi(v.w);
+}
+
+// Streaming 16-byte load that does not allocate in L1 (data read once per launch).
+__device__ __forceinline__ uint4 ldg_stream(const uint4 *p) {
+    uint4 v;
+    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(p));
+    return v;
+}
+
+// ---------------------------------------------------------------------------------------------
+// Warp reductions (fixed butterfly order: deterministic).
+template <typename T>
+__device__ __forceinline__ T warp_sum(T v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, o);
+    return v;
+}
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xFFFFFFFFu, v, o));
+    return v;
+}
+
+// Largest b with its token id (lower id wins a tie) and the second-largest b.
+struct Top2 {
+    float b1;
+    int id1;
+    float b2;
+};
+__device__ __forceinline__ Top2 top2_merge(Top2 x, Top2 y) {
+    const bool x_wins = x.b1 > y.b1 || (x.b1 == y.b1 && x.id1 < y.id1);
+    Top2 r;
+    if (x_wins) {
+        r.b1 = x.b1; r.id1 = x.id1; r.b2 = fmaxf(x.b2, y.b1);
+    } else {
+        r.b1 = y.b1; r.id1 = y.id1; r.b2 = fmaxf(y.b2, x.b1);
+    }
+    return r;
+}
+__device__ __forceinline__ Top2 warp_top2(Top2 v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        Top2 p;
+        p.b1 = __shfl_xor_sync(0xFFFFFFFFu, v.b1, o);
+        p.id1 = __shfl_xor_sync(0xFFFFFFFFu, v.id1, o);
+        p.b2 = __shfl_xor_sync(0xFFFFFFFFu, v.b2, o);
+        // Order the operands by lane so every lane computes the same merge.
+        v = (threadIdx.x & o) ? top2_merge(p, v) : top2_merge(v, p);
+    }
+    return v;
+}
+
+// ---------------------------------------------------------------------------------------------
+// All-reduce over every thread of a thread-block cluster.  Each warp reduces with shuffles and
+// stores its partial into slot [my rank][warp] of every CTA's shared buffer (distributed shared
+// memory); one cluster barrier; then every warp reduces the CL*NW partials itself, in the same
+// fixed order, so every thread of every CTA gets bitwise the same result.  Two buffers alternate
+// between calls: a CTA can only overwrite a buffer after the next barrier, i.e. after every peer
+// has finished reading it.
+template <int NW, int K>
+struct ClusterReducer {
+    float *slots;  // [2][cl][NW][K] floats in shared memory
+    int cl;
+    int parity;
+
+    __device__ __forceinline__ float *buf(int p) const { return slots + p * cl * NW * K; }
+
+    template <typename Op>
+    __device__ __forceinline__ void run(float (&v)[K], Op op) {
+        const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+        for (int k = 0; k < K; ++k) {
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) v[k] = op(v[k], __shfl_xor_sync(0xFFFFFFFFu, v[k], o));
+        }
+        cg::cluster_group cluster = cg::this_cluster();
+        const unsigned me = cluster.block_rank();
+        float *b = buf(parity);
+        if (lane < cl) {
+            float *peer = cluster.map_shared_rank(b, lane);
+#pragma unroll
+            for (int k = 0; k < K; ++k) peer[(me * NW + warp) * K + k] = v[k];
+        }
+        cluster.sync();
+        const int total = cl * NW;  // <= 8 * 32
+#pragma unroll
+        for (int k = 0; k < K; ++k) {
+            float acc = (lane < total) ? b[lane * K + k] : op.identity();
+            for (int e = lane + 32; e < total; e += 32) acc = op(acc, b[e * K + k]);
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) acc = op(acc, __shfl_xor_sync(0xFFFFFFFFu, acc, o));
+            v[k] = acc;
+        }
+        parity ^= 1;
+    }
+};
+
+struct OpSum {
+    __device__ __forceinline__ float operator()(float a, float b) const { return a + b; }
+    __device__ __forceinline__ float identity() const { return 0.0f; }
+};
+struct OpMax {
+    __device__ __forceinline__ float operator()(float a, float b) const { return fmaxf(a, b); }
+    __device__ __forceinline__ float identity() const { return -__int_as_float(0x7F800000); }
+};
+
+// Same pattern for fp64 sums and int counts (PoissonComp's exact finish and compaction).
+template <int NW>
+struct ClusterReducer64 {
+    double *slots;  // [2][cl][NW][2]
+    int cl;
+    int parity;
+
+    // Sums (a, b) over the cluster: a fp64 and b an integer count carried exactly in fp64.
+    __device__ __forceinline__ void run(double &a, double &b) {
+        const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+            a += __shfl_xor_sync(0xFFFFFFFFu, a, o);
+            b += __shfl_xor_sync(0xFFFFFFFFu, b, o);
+        }
+        cg::cluster_group cluster = cg::this_cluster();
+        const unsigned me = cluster.block_rank();
+        double *buf = slots + parity * cl * NW * 2;
+        if (lane < cl) {
+            double *peer = cluster.map_shared_rank(buf, lane);
+            peer[(me * NW + warp) * 2 + 0] = a;
+            peer[(me * NW + warp) * 2 + 1] = b;
+        }
+        cluster.sync();
+        const int total = cl * NW;
+        double sa = 0.0, sb = 0.0;
+        for (int e = lane; e < total; e += 32) {
+            sa += buf[e * 2 + 0];
+            sb += buf[e * 2 + 1];
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+            sa += __shfl_xor_sync(0xFFFFFFFFu, sa, o);
+            sb += __shfl_xor_sync(0xFFFFFFFFu, sb, o);
+        }
+        a = sa;
+        b = sb;
+        parity ^= 1;
+    }
+};
+
+// ---------------------------------------------------------------------------------------------
+// Philox4x32-10 (Salmon, Moraes, Dror, Shaw, SC'11): ten rounds of two 32x32->64 multiplies
+// with the round key xored in, the key advancing by two Weyl constants per round.
+__device__ __forceinline__ uint4 philox4x32_10(uint4 c, uint32_t k0, uint32_t k1) {
+#pragma unroll
+    for (int round = 0; round < 10; ++round) {
+        const uint32_t lo0 = 0xD2511F53u * c.x, hi0 = __umulhi(0xD2511F53u, c.x);
+        const uint32_t lo1 = 0xCD9E8D57u * c.z, hi1 = __umulhi(0xCD9E8D57u, c.z);
+        c = make_uint4(hi1 ^ c.y ^ k0, lo1, hi0 ^ c.w ^ k1, lo0);
+        k0 += 0x9E3779B9u;
+        k1 += 0xBB67AE85u;
+    }
+    return c;
+}
+
+}  // namespace verkv

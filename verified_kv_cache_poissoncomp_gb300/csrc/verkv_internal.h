@@ -1,0 +1,149 @@
+// verkv_internal.h -- kernel argument blocks and launchers shared by libverkv's translation units.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/verkv.h"
+
+namespace verkv {
+
+// Device error word bits (latched with atomicOr, read and cleared by verkv_sync).
+enum : uint32_t {
+    ERR_TAU = 1u << 0,         // tau outside (0, 1] or not finite
+    ERR_CAPACITY = 1u << 1,    // pivotal set larger than cap
+    ERR_NOCONVERGE = 1u << 2,  // a solve hit its iteration cap
+    ERR_BUDGET_SUM = 1u << 3,  // |sum r - eta n| >= 1e-6 n after the c solve
+};
+
+// ---------------------------------------------------------------------------------------------
+// PoissonComp: c solve, r, Philox sample, compaction (one cluster per unit).
+struct PcArgs {
+    const float *tau;        // [units][n]
+    float *r_full;           // [units][n]
+    int32_t *ids;            // [units][cap]
+    float *pr;               // [units][cap]
+    int32_t *count;          // [units]
+    uint32_t *resident;      // [units][W]
+    float *c_out;            // [units]
+    uint32_t *err;
+    double b_rest;           // eta n - |forced|
+    double eta_n;            // eta n
+    int n, W, cap, n_sink, n_local, layers, kv_heads;
+    int n_rest;              // n - |forced|
+    int cl, chunk;           // CTAs per cluster, tokens per CTA (multiple of 1024)
+    uint32_t seed_lo, seed_hi;
+};
+cudaError_t launch_pc_solve(const PcArgs &a, int units, cudaStream_t s);
+
+// Pivotal row gather: pkv[u][slot] = kv_full[u][ids[u][slot]].
+cudaError_t launch_pc_gather(const uint16_t *kv_full, const int32_t *ids, const int32_t *count,
+                             uint16_t *pkv, int units, int cap, int n, int d, cudaStream_t s);
+
+// Exact sketch: sketch[u][i] = K row of kv_full[u][i].
+cudaError_t launch_sketch_exact(const uint16_t *kv_full, uint16_t *sketch, int64_t rows, int d,
+                                cudaStream_t s);
+
+// ---------------------------------------------------------------------------------------------
+// Layer-local indexing of a decode call: u' = b * kv_heads + h (units of the layer), query head
+// qh = u' * G + g, global unit u = (b * layers + layer) * kv_heads + h.
+struct LayerIdx {
+    int layers, layer, kv_heads, G;
+    __host__ __device__ __forceinline__ int unit_global(int ul) const {
+        const int b = ul / kv_heads, h = ul - b * kv_heads;
+        return (b * layers + layer) * kv_heads + h;
+    }
+};
+
+// Sketch scores s[qh][i] = q_qh . sketch_i / sqrt(d).
+struct ScoreArgs {
+    const uint16_t *sketch;  // [units][n][d]
+    const uint16_t *q;       // [B][hq][d]
+    float *scores;           // [B*hq][n]
+    int n, d;
+    float scale;
+    LayerIdx li;
+};
+cudaError_t launch_score(const ScoreArgs &a, int units_layer, cudaStream_t s);
+
+// Certificate and selection per query head (one cluster per query head).
+struct CertifyArgs {
+    const float *scores;          // [qh][n]
+    const float *r_full;          // [units][n]
+    const uint32_t *resident;     // [units][W]
+    uint32_t *F;                  // [qh][W]
+    verkv_head_stats *qstats;     // [qh]
+    uint32_t *err;
+    int n, W, cl, chunk;
+    float eps, ldelta;
+    LayerIdx li;
+};
+cudaError_t launch_certify(const CertifyArgs &a, int qheads, size_t smem, cudaStream_t s);
+int certify_cluster_size(int n);
+int certify_chunk(int n, int cl);
+size_t certify_smem_bytes(int chunk);
+
+// Fetch list per KV head: ascending ids of (OR_g F_g) & ~resident.
+struct FetchListArgs {
+    const uint32_t *F;
+    const uint32_t *resident;
+    int32_t *ids;       // [units_layer][n]  (device, used by the fetch)
+    int32_t *counts;    // [units_layer]
+    int32_t *ids_user;  // optional copy (device or mapped host)
+    int32_t *counts_user;
+    int32_t *ids_host;  // optional copy into mapped host memory (MEMCPY mode)
+    int32_t *counts_host;
+    verkv_head_stats *qstats;
+    int n, W;
+    LayerIdx li;
+};
+cudaError_t launch_fetchlist(const FetchListArgs &a, int units_layer, cudaStream_t s);
+
+// ---------------------------------------------------------------------------------------------
+// Shrinkage-weighted partial sums over a row set (pivotal rows, or fetched rows).
+constexpr int PART_ROWS = 128;
+struct PartialArgs {
+    const uint16_t *rows;     // [src units][row_stride][2][d]
+    const int32_t *ids;       // [src units][row_stride]
+    const float *pr;          // pivotal r [src units][row_stride], or null for fetched rows
+    const int32_t *count;     // [src units]
+    const uint16_t *q;        // [B][hq][d]
+    const uint32_t *F;        // [qh][W]
+    const verkv_head_stats *qstats;
+    float *part;              // [units_layer][max_chunks][G][d + 2]
+    int row_stride;           // cap (pivotal) or n (fetched)
+    int max_chunks;
+    int n, W, d;
+    int pivotal;              // 1: pivotal rows of global units; 0: fetched rows of layer units
+    float scale;
+    LayerIdx li;
+};
+cudaError_t launch_partial(const PartialArgs &a, int units_layer, int grid, cudaStream_t s);
+
+// Zero-copy fetch: staging[u'][j] = host_kv[u][ids[u'][j]].
+struct GatherArgs {
+    const uint16_t *host_kv;  // device-accessible pointer to page-locked [units][n][2][d]
+    const int32_t *ids;       // [units_layer][n]
+    const int32_t *counts;    // [units_layer]
+    uint16_t *staging;        // [units_layer][n][2][d]
+    int n, d;
+    LayerIdx li;
+};
+cudaError_t launch_gather_host(const GatherArgs &a, int units_layer, cudaStream_t s);
+
+// Merge partials into o, lse and the per-head stats.
+struct MergeArgs {
+    const float *part_piv;
+    const float *part_fet;
+    const int32_t *pcount;       // pivotal count [units]
+    const int32_t *fcount;       // fetch count [units_layer]
+    const verkv_head_stats *qstats;
+    float *o;                    // [qh][d]
+    float *lse;                  // [qh] or null
+    verkv_head_stats *stats;     // [qh] or null
+    int max_piv, max_fet, cap, d;
+    LayerIdx li;
+};
+cudaError_t launch_merge(const MergeArgs &a, int qheads, cudaStream_t s);
+
+}  // namespace verkv

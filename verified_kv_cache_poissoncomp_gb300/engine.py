@@ -1,0 +1,123 @@
+"""A small Python front end over the C ABI: PyTorch allocates the device and page-locked host
+memory and supplies the CUDA stream; every step of the hot path runs in libverkv's kernels.
+
+    eng = VerKV(shape)                   # workspace + context on the current CUDA device/stream
+    eng.load(tau, kv)                    # numpy -> device tensors and a page-locked host copy
+    eng.compress(eta, n_sink, n_local, seed)   # verkv_poissoncomp + verkv_sketch_build
+    eng.attend(layer, q_dev, eps, delta)        # verkv_attend_verified
+    o, lse, stats = eng.fetch_refine()          # verkv_fetch_refine
+"""
+import numpy as np
+import torch
+
+from . import binding as B
+
+
+def default_cap(n, eta):
+    """Pivotal capacity: eta n plus 8 standard deviations of a Poisson sample size, plus 64."""
+    m = eta * n
+    return int(min(n, np.ceil(m + 8.0 * np.sqrt(m)) + 64))
+
+
+class VerKV:
+    def __init__(self, batch, layers, kv_heads, q_per_kv, head_dim, n, cap, device=None,
+                 fetch_mode=B.VERKV_FETCH_ZEROCOPY):
+        self.dev = torch.device("cuda", torch.cuda.current_device() if device is None else device)
+        self.shape = B.verkv_shape(batch, layers, kv_heads, q_per_kv, head_dim, n, cap)
+        self.B, self.L, self.h, self.G, self.d, self.n, self.cap = (
+            batch, layers, kv_heads, q_per_kv, head_dim, n, cap)
+        self.units = batch * layers * kv_heads
+        self.W = (n + 31) // 32
+        ws = B.verkv_workspace_size(self.shape)
+        if ws == 0:
+            raise B.VerkvError(B.VERKV_EINVAL, "invalid shape")
+        self.workspace = torch.empty(ws, dtype=torch.uint8, device=self.dev)
+        self.stream = torch.cuda.current_stream(self.dev)
+        self.ctx = B.verkv_create(self.dev.index, self.stream.cuda_stream, self.shape,
+                                  self.workspace.data_ptr(), ws)
+        if fetch_mode != B.VERKV_FETCH_ZEROCOPY:
+            B.verkv_set_fetch_mode(self.ctx, fetch_mode)
+        dv = self.dev
+        u, hq = self.units, batch * kv_heads * q_per_kv
+        self.r_full = torch.empty((u, n), dtype=torch.float32, device=dv)
+        self.p_ids = torch.empty((u, cap), dtype=torch.int32, device=dv)
+        self.p_r = torch.empty((u, cap), dtype=torch.float32, device=dv)
+        self.p_kv = torch.empty((u, cap, 2, head_dim), dtype=torch.int16, device=dv)
+        self.p_count = torch.empty((u,), dtype=torch.int32, device=dv)
+        self.p_res = torch.empty((u, self.W), dtype=torch.int32, device=dv)
+        self.p_c = torch.empty((u,), dtype=torch.float32, device=dv)
+        self.pivotal = B.verkv_pivotal(self.p_ids.data_ptr(), self.p_r.data_ptr(),
+                                       self.p_kv.data_ptr(), self.p_count.data_ptr(),
+                                       self.p_res.data_ptr(), self.p_c.data_ptr())
+        self.o = torch.empty((hq, head_dim), dtype=torch.float32, device=dv)
+        self.lse = torch.empty((hq,), dtype=torch.float32, device=dv)
+        self.stats = torch.empty((hq, 16), dtype=torch.int32, device=dv)  # verkv_head_stats
+        self.fetch_ids = torch.empty((batch * kv_heads, n), dtype=torch.int32, device=dv)
+        self.fetch_counts = torch.empty((batch * kv_heads,), dtype=torch.int32, device=dv)
+        self.tau = self.kv = self.sketch = self.host_kv = None
+
+    # --------------------------------------------------------------------------------------------
+    def load(self, tau, kv):
+        """tau float32 [units][n], kv uint16 (bf16 bits) [units][n][2][d] (numpy or torch CPU)."""
+        tau_t = torch.as_tensor(np.ascontiguousarray(tau, dtype=np.float32)).reshape(self.units, self.n)
+        kv_t = torch.as_tensor(np.ascontiguousarray(kv).view(np.int16)).reshape(
+            self.units, self.n, 2, self.d)
+        self.tau = tau_t.to(self.dev)
+        self.host_kv = torch.empty(kv_t.shape, dtype=torch.int16, pin_memory=True)
+        self.host_kv.copy_(kv_t)
+        self.kv = self.host_kv.to(self.dev)
+        self.sketch = torch.empty((self.units, self.n, self.d), dtype=torch.int16, device=self.dev)
+        self.sketch_desc = B.verkv_sketch(B.VERKV_SKETCH_EXACT, self.sketch.data_ptr())
+
+    def compress(self, eta, n_sink, n_local, seed):
+        B.verkv_poissoncomp(self.ctx, self.tau.data_ptr(), eta, B.verkv_hset(n_sink, n_local),
+                            seed, self.kv.data_ptr(), self.r_full.data_ptr(), self.pivotal)
+        B.verkv_sketch_build(self.ctx, self.kv.data_ptr(), B.VERKV_SKETCH_EXACT,
+                             self.sketch.data_ptr())
+
+    def attend(self, layer, q, eps, delta, with_ids=True):
+        """q: device bf16 (int16 view) [batch][kv_heads * q_per_kv][d]."""
+        self._q = q
+        ids = self.fetch_ids.data_ptr() if with_ids else None
+        cnt = self.fetch_counts.data_ptr() if with_ids else None
+        B.verkv_attend_verified(self.ctx, layer, q.data_ptr(), self.pivotal,
+                                self.r_full.data_ptr(), self.sketch_desc, eps, delta, ids, cnt)
+        self._ids, self._cnt = ids, cnt
+
+    def fetch_refine(self, o=None, lse=None, stats=None):
+        o = self.o if o is None else o
+        lse = self.lse if lse is None else lse
+        stats = self.stats if stats is None else stats
+        B.verkv_fetch_refine(self.ctx, self._ids, self._cnt, self.host_kv.data_ptr(),
+                             o.data_ptr(), lse.data_ptr() if lse is not None else None,
+                             stats.data_ptr() if stats is not None else None)
+        return o, lse, stats
+
+    def selection_bitmap(self):
+        out = torch.empty((self.B * self.h * self.G, self.W), dtype=torch.int32, device=self.dev)
+        B.verkv_selection_bitmap(self.ctx, out.data_ptr())
+        return out
+
+    def sync(self):
+        B.verkv_sync(self.ctx)
+
+    def close(self):
+        if self.ctx is not None:
+            B.verkv_destroy(self.ctx)
+            self.ctx = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:  # noqa: BLE001 -- interpreter shutdown
+            pass
+
+
+def stats_to_dict(stats):
+    """[hq][16] int32 tensor of verkv_head_stats -> dict of numpy arrays."""
+    a = stats.cpu().numpy()
+    f = a[:, :10].view(np.float32)
+    out = {k: f[:, i].copy() for i, k in enumerate(B.STATS_FLOAT_FIELDS)}
+    for i, k in enumerate(B.STATS_INT_FIELDS):
+        out[k] = a[:, 10 + i].copy()
+    return out
