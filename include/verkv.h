@@ -205,6 +205,38 @@ verkv_status verkv_fetch_refine(verkv_ctx *ctx, const int32_t *ids, const int32_
  * Stream-ordered; VERKV_ESTATE if no attend has run on this context. */
 verkv_status verkv_selection_bitmap(verkv_ctx *ctx, uint32_t *out);
 
+/* Measurement.  Every kernel launch is counted per kernel; with profiling enabled each launch is
+ * also bracketed by two CUDA events on the stream it runs on (host cost ~2 event records).
+ * Kernel ids, in launch order: */
+enum {
+    VERKV_K_PC_SOLVE = 0,      /* PoissonComp c solve, r, sample, compaction     */
+    VERKV_K_PC_GATHER,         /* pivotal K/V row gather                          */
+    VERKV_K_SKETCH,            /* exact sketch build                              */
+    VERKV_K_SCORE,             /* sketch logits for every token and query head    */
+    VERKV_K_CERTIFY,           /* beta solve, certificate, selection (Eq. 7-10)   */
+    VERKV_K_FETCHLIST,         /* per-KV-head fetch id list                       */
+    VERKV_K_PARTIAL_PIVOTAL,   /* shrinkage-weighted sums over the pivotal set    */
+    VERKV_K_GATHER_HOST,       /* zero-copy fetch of selected rows from host      */
+    VERKV_K_PARTIAL_FETCHED,   /* exact sums over the fetched rows                */
+    VERKV_K_MERGE,             /* merge partials into o, lse and statistics       */
+    VERKV_K_COUNT
+};
+
+/* Start (on != 0) or stop recording per-launch events.  Do not enable during stream capture. */
+verkv_status verkv_profile_enable(verkv_ctx *ctx, int on);
+
+/* Wait for the context's streams, then add the recorded launches and their event-timed
+ * milliseconds per kernel id into launches[VERKV_K_COUNT] and total_ms[VERKV_K_COUNT]
+ * (caller-zeroed host arrays) and discard the records. */
+verkv_status verkv_profile_read(verkv_ctx *ctx, int64_t *launches, double *total_ms);
+
+/* Kernel launches issued by this context since it was created, per kernel id
+ * (out[VERKV_K_COUNT], host).  Counts launches made during stream capture once. */
+verkv_status verkv_launch_counts(verkv_ctx *ctx, int64_t *out);
+
+/* Name of a kernel id ("" if out of range). */
+const char *verkv_kernel_name(int kernel);
+
 /* Wait for all work on the context's streams, then return (and clear) the first error latched
  * by the device since the previous verkv_sync, or a pending CUDA error. */
 verkv_status verkv_sync(verkv_ctx *ctx);

@@ -26,8 +26,10 @@ VERKV_FETCH_MEMCPY = 1
 
 EXPORTED = ["verkv_workspace_size", "verkv_create", "verkv_destroy", "verkv_set_fetch_mode",
             "verkv_poissoncomp", "verkv_sketch_build", "verkv_attend_verified",
-            "verkv_fetch_refine", "verkv_selection_bitmap", "verkv_sync", "verkv_last_error",
-            "verkv_status_string"]
+            "verkv_fetch_refine", "verkv_selection_bitmap", "verkv_profile_enable",
+            "verkv_profile_read", "verkv_launch_counts", "verkv_kernel_name", "verkv_sync",
+            "verkv_last_error", "verkv_status_string"]
+VERKV_K_COUNT = 10
 
 
 class verkv_shape(ctypes.Structure):
@@ -102,6 +104,14 @@ def lib():
         L.verkv_fetch_refine.restype = ctypes.c_int
         L.verkv_selection_bitmap.argtypes = [vp, vp]
         L.verkv_selection_bitmap.restype = ctypes.c_int
+        L.verkv_profile_enable.argtypes = [vp, ctypes.c_int]
+        L.verkv_profile_enable.restype = ctypes.c_int
+        L.verkv_profile_read.argtypes = [vp, vp, vp]
+        L.verkv_profile_read.restype = ctypes.c_int
+        L.verkv_launch_counts.argtypes = [vp, vp]
+        L.verkv_launch_counts.restype = ctypes.c_int
+        L.verkv_kernel_name.argtypes = [ctypes.c_int]
+        L.verkv_kernel_name.restype = ctypes.c_char_p
         L.verkv_sync.argtypes = [vp]
         L.verkv_sync.restype = ctypes.c_int
         L.verkv_last_error.argtypes = [vp]
@@ -167,6 +177,29 @@ def verkv_fetch_refine(ctx, ids, counts, host_kv, o_out, lse_out=None, stats_out
 
 def verkv_selection_bitmap(ctx, out):
     _check(lib().verkv_selection_bitmap(ctx, out), ctx)
+
+
+def verkv_profile_enable(ctx, on):
+    _check(lib().verkv_profile_enable(ctx, int(bool(on))), ctx)
+
+
+def verkv_profile_read(ctx):
+    """-> (launches int64[K], total_ms float64[K]) accumulated since the last read."""
+    n = (ctypes.c_int64 * VERKV_K_COUNT)()
+    t = (ctypes.c_double * VERKV_K_COUNT)()
+    _check(lib().verkv_profile_read(ctx, ctypes.cast(n, ctypes.c_void_p),
+                                    ctypes.cast(t, ctypes.c_void_p)), ctx)
+    return list(n), list(t)
+
+
+def verkv_launch_counts(ctx):
+    n = (ctypes.c_int64 * VERKV_K_COUNT)()
+    _check(lib().verkv_launch_counts(ctx, ctypes.cast(n, ctypes.c_void_p)), ctx)
+    return list(n)
+
+
+def verkv_kernel_name(k):
+    return lib().verkv_kernel_name(int(k)).decode()
 
 
 def verkv_sync(ctx):

@@ -149,6 +149,16 @@ struct verkv_ctx {
     const int32_t *user_ids = nullptr, *user_counts = nullptr;
     const void *q = nullptr;
     std::string last_error;
+    // Measurement
+    int64_t launches[VERKV_K_COUNT] = {};
+    bool prof_on = false;
+    std::vector<cudaEvent_t> prof_pool;
+    size_t prof_used = 0;
+    struct Rec {
+        int kernel;
+        cudaEvent_t a, b;
+    };
+    std::vector<Rec> prof_recs;
 };
 
 namespace {
@@ -167,6 +177,30 @@ verkv_status cuda_fail(verkv_ctx *c, cudaError_t e, const char *where) {
         cudaError_t e_ = (call);                             \
         if (e_ != cudaSuccess) return cuda_fail(ctx, e_, where); \
     } while (0)
+
+cudaEvent_t prof_event(verkv_ctx *ctx) {
+    if (ctx->prof_used == ctx->prof_pool.size()) {
+        cudaEvent_t e = nullptr;
+        if (cudaEventCreate(&e) != cudaSuccess) return nullptr;
+        ctx->prof_pool.push_back(e);
+    }
+    return ctx->prof_pool[ctx->prof_used++];
+}
+
+// Launch with accounting: counts the launch and, when profiling, brackets it with events.
+template <typename F>
+cudaError_t tracked(verkv_ctx *ctx, int kernel, cudaStream_t s, F &&launch) {
+    cudaEvent_t a = nullptr, b = nullptr;
+    if (ctx->prof_on && (a = prof_event(ctx)) != nullptr) cudaEventRecord(a, s);
+    const cudaError_t e = launch();
+    if (e != cudaSuccess) return e;
+    ctx->launches[kernel]++;
+    if (a && (b = prof_event(ctx)) != nullptr) {
+        cudaEventRecord(b, s);
+        ctx->prof_recs.push_back({kernel, a, b});
+    }
+    return cudaSuccess;
+}
 
 LayerIdx layer_idx(const verkv_ctx *ctx, int layer) {
     LayerIdx li;
@@ -253,6 +287,7 @@ void verkv_destroy(verkv_ctx *ctx) {
     if (ctx->host_staging) cudaFreeHost(ctx->host_staging);
     if (ctx->host_ids) cudaFreeHost(ctx->host_ids);
     if (ctx->host_counts) cudaFreeHost(ctx->host_counts);
+    for (cudaEvent_t e : ctx->prof_pool) cudaEventDestroy(e);
     if (ctx->e_sel) cudaEventDestroy(ctx->e_sel);
     if (ctx->e_fetch) cudaEventDestroy(ctx->e_fetch);
     if (ctx->side) cudaStreamDestroy(ctx->side);
@@ -328,10 +363,12 @@ verkv_status verkv_poissoncomp(verkv_ctx *ctx, const float *tau, double eta, ver
     a.chunk = chunk;
     a.seed_lo = (uint32_t)seed;
     a.seed_hi = (uint32_t)(seed >> 32);
-    VERKV_CUDA(launch_pc_solve(a, units, ctx->main), "k_pc_solve");
-    VERKV_CUDA(launch_pc_gather((const uint16_t *)kv_full, out->ids, out->count,
-                                (uint16_t *)out->kv, units, ctx->sh.cap, n, ctx->sh.head_dim,
-                                ctx->main), "k_pc_gather");
+    VERKV_CUDA(tracked(ctx, VERKV_K_PC_SOLVE, ctx->main, [&] { return launch_pc_solve(a, units, ctx->main); }), "k_pc_solve");
+    VERKV_CUDA(tracked(ctx, VERKV_K_PC_GATHER, ctx->main, [&] {
+                   return launch_pc_gather((const uint16_t *)kv_full, out->ids, out->count,
+                                           (uint16_t *)out->kv, units, ctx->sh.cap, n,
+                                           ctx->sh.head_dim, ctx->main);
+               }), "k_pc_gather");
     return VERKV_OK;
 }
 
@@ -342,8 +379,10 @@ verkv_status verkv_sketch_build(verkv_ctx *ctx, const void *kv_full, int32_t for
     if (format != VERKV_SKETCH_EXACT) return fail(ctx, VERKV_EINVAL, "sketch_build: unknown format");
     VERKV_CUDA(cudaSetDevice(ctx->device), "cudaSetDevice");
     const int64_t rows = (int64_t)ctx->sh.batch * ctx->sh.layers * ctx->sh.kv_heads * ctx->sh.n;
-    VERKV_CUDA(launch_sketch_exact((const uint16_t *)kv_full, (uint16_t *)sketch_out, rows,
-                                   ctx->sh.head_dim, ctx->main), "k_sketch_exact");
+    VERKV_CUDA(tracked(ctx, VERKV_K_SKETCH, ctx->main, [&] {
+                   return launch_sketch_exact((const uint16_t *)kv_full, (uint16_t *)sketch_out,
+                                              rows, ctx->sh.head_dim, ctx->main);
+               }), "k_sketch_exact");
     return VERKV_OK;
 }
 
@@ -373,7 +412,7 @@ verkv_status verkv_attend_verified(verkv_ctx *ctx, int32_t layer, const void *q,
     sa.d = d;
     sa.scale = (float)(1.0 / sqrt((double)d));
     sa.li = li;
-    VERKV_CUDA(launch_score(sa, ctx->L.units_layer, ctx->main), "k_score");
+    VERKV_CUDA(tracked(ctx, VERKV_K_SCORE, ctx->main, [&] { return launch_score(sa, ctx->L.units_layer, ctx->main); }), "k_score");
 
     CertifyArgs ca{};
     ca.scores = ctx->scores;
@@ -389,8 +428,9 @@ verkv_status verkv_attend_verified(verkv_ctx *ctx, int32_t layer, const void *q,
     ca.eps = eps;
     ca.ldelta = (float)log(2.0 / (double)delta);
     ca.li = li;
-    VERKV_CUDA(launch_certify(ca, ctx->L.qh_layer, certify_smem_bytes(ca.chunk), ctx->main),
-               "k_certify");
+    VERKV_CUDA(tracked(ctx, VERKV_K_CERTIFY, ctx->main, [&] {
+                   return launch_certify(ca, ctx->L.qh_layer, certify_smem_bytes(ca.chunk), ctx->main);
+               }), "k_certify");
 
     FetchListArgs fa{};
     fa.F = ctx->F;
@@ -407,7 +447,7 @@ verkv_status verkv_attend_verified(verkv_ctx *ctx, int32_t layer, const void *q,
     fa.n = n;
     fa.W = ctx->L.W;
     fa.li = li;
-    VERKV_CUDA(launch_fetchlist(fa, ctx->L.units_layer, ctx->main), "k_fetchlist");
+    VERKV_CUDA(tracked(ctx, VERKV_K_FETCHLIST, ctx->main, [&] { return launch_fetchlist(fa, ctx->L.units_layer, ctx->main); }), "k_fetchlist");
     VERKV_CUDA(cudaEventRecord(ctx->e_sel, ctx->main), "cudaEventRecord");
 
     PartialArgs pa{};
@@ -428,7 +468,7 @@ verkv_status verkv_attend_verified(verkv_ctx *ctx, int32_t layer, const void *q,
     pa.scale = sa.scale;
     pa.li = li;
     int grid = std::min(ctx->L.units_layer * ctx->L.max_piv, ctx->sms * 8);
-    VERKV_CUDA(launch_partial(pa, ctx->L.units_layer, std::max(grid, 1), ctx->main), "k_partial");
+    VERKV_CUDA(tracked(ctx, VERKV_K_PARTIAL_PIVOTAL, ctx->main, [&] { return launch_partial(pa, ctx->L.units_layer, std::max(grid, 1), ctx->main); }), "k_partial");
 
     ctx->pending = true;
     ctx->attended = true;
@@ -469,7 +509,7 @@ verkv_status verkv_fetch_refine(verkv_ctx *ctx, const int32_t *ids, const int32_
         ga.n = n;
         ga.d = d;
         ga.li = li;
-        VERKV_CUDA(launch_gather_host(ga, ctx->L.units_layer, ctx->side), "k_gather_host");
+        VERKV_CUDA(tracked(ctx, VERKV_K_GATHER_HOST, ctx->side, [&] { return launch_gather_host(ga, ctx->L.units_layer, ctx->side); }), "k_gather_host");
     } else {
         VERKV_CUDA(cudaEventSynchronize(ctx->e_sel), "cudaEventSynchronize");
         const int U = ctx->L.units_layer;
@@ -522,7 +562,7 @@ verkv_status verkv_fetch_refine(verkv_ctx *ctx, const int32_t *ids, const int32_
     pa.scale = (float)(1.0 / sqrt((double)d));
     pa.li = li;
     const int grid = std::max(1, std::min(ctx->L.units_layer * ctx->L.max_fet, ctx->sms * 8));
-    VERKV_CUDA(launch_partial(pa, ctx->L.units_layer, grid, ctx->main), "k_partial(fetched)");
+    VERKV_CUDA(tracked(ctx, VERKV_K_PARTIAL_FETCHED, ctx->main, [&] { return launch_partial(pa, ctx->L.units_layer, grid, ctx->main); }), "k_partial(fetched)");
 
     MergeArgs ma{};
     ma.part_piv = ctx->part_piv;
@@ -538,7 +578,7 @@ verkv_status verkv_fetch_refine(verkv_ctx *ctx, const int32_t *ids, const int32_
     ma.cap = ctx->sh.cap;
     ma.d = d;
     ma.li = li;
-    VERKV_CUDA(launch_merge(ma, ctx->L.qh_layer, ctx->main), "k_merge");
+    VERKV_CUDA(tracked(ctx, VERKV_K_MERGE, ctx->main, [&] { return launch_merge(ma, ctx->L.qh_layer, ctx->main); }), "k_merge");
     ctx->pending = false;
     return VERKV_OK;
 }
@@ -566,6 +606,41 @@ verkv_status verkv_selection_bitmap(verkv_ctx *ctx, uint32_t *out) {
     VERKV_CUDA(cudaMemcpyAsync(out, ctx->F, (size_t)ctx->L.qh_layer * ctx->L.W * 4,
                                cudaMemcpyDefault, ctx->main), "copy F");
     return VERKV_OK;
+}
+
+verkv_status verkv_profile_enable(verkv_ctx *ctx, int on) {
+    if (!ctx) return VERKV_EINVAL;
+    ctx->prof_on = on != 0;
+    return VERKV_OK;
+}
+
+verkv_status verkv_profile_read(verkv_ctx *ctx, int64_t *launches, double *total_ms) {
+    if (!ctx || !launches || !total_ms) return VERKV_EINVAL;
+    VERKV_CUDA(cudaSetDevice(ctx->device), "cudaSetDevice");
+    VERKV_CUDA(cudaStreamSynchronize(ctx->side), "cudaStreamSynchronize(side)");
+    VERKV_CUDA(cudaStreamSynchronize(ctx->main), "cudaStreamSynchronize(main)");
+    for (const auto &r : ctx->prof_recs) {
+        float ms = 0.0f;
+        VERKV_CUDA(cudaEventElapsedTime(&ms, r.a, r.b), "cudaEventElapsedTime");
+        launches[r.kernel] += 1;
+        total_ms[r.kernel] += ms;
+    }
+    ctx->prof_recs.clear();
+    ctx->prof_used = 0;
+    return VERKV_OK;
+}
+
+verkv_status verkv_launch_counts(verkv_ctx *ctx, int64_t *out) {
+    if (!ctx || !out) return VERKV_EINVAL;
+    for (int k = 0; k < VERKV_K_COUNT; ++k) out[k] = ctx->launches[k];
+    return VERKV_OK;
+}
+
+const char *verkv_kernel_name(int k) {
+    static const char *names[VERKV_K_COUNT] = {
+        "k_pc_solve", "k_pc_gather", "k_sketch_exact", "k_score", "k_certify", "k_fetchlist",
+        "k_partial(pivotal)", "k_gather_host", "k_partial(fetched)", "k_merge"};
+    return (k >= 0 && k < VERKV_K_COUNT) ? names[k] : "";
 }
 
 const char *verkv_last_error(verkv_ctx *ctx) { return ctx ? ctx->last_error.c_str() : ""; }
