@@ -268,6 +268,7 @@ def run_ours(args, world, rank, local):
         o_all = torch.empty((Q, hq, w.d), dtype=torch.float32, device=dev)
         lse_all = torch.empty((Q, hq), dtype=torch.float32, device=dev)
         st_all = torch.empty((Q, hq, 16), dtype=torch.int32, device=dev)
+        fc_all = torch.zeros((Q, w.B * w.h_kv), dtype=torch.int32, device=dev)  # rows fetched
         tau_dev = eng.tau
         kv_dev = eng.kv
 
@@ -277,7 +278,7 @@ def run_ours(args, world, rank, local):
         for t in range(Q):
             B.verkv_attend_verified(eng.ctx, int(w.query_layer[t]), q_dev[t].data_ptr(),
                                     eng.pivotal, eng.r_full.data_ptr(), eng.sketch_desc, w.eps,
-                                    w.delta, None, None)
+                                    w.delta, None, fc_all[t].data_ptr())
             B.verkv_fetch_refine(eng.ctx, None, None, eng.host_kv.data_ptr(),
                                  o_all[t].data_ptr(), lse_all[t].data_ptr(), st_all[t].data_ptr())
 
@@ -341,32 +342,61 @@ def run_ours(args, world, rank, local):
                                            "total_ms": total_ms[k]}
                   for k in range(B.VERKV_K_COUNT) if launches[k] > 0}
 
-    # Algorithmic bytes per launch of each decode kernel ("Roofline").
+    # Host-to-device link: a 256 MiB page-locked cudaMemcpyAsync, best of 5.
+    hbuf = torch.empty(256 << 20, dtype=torch.uint8, pin_memory=True)
+    dbuf = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    link = 0.0
+    for _ in range(5):
+        l0 = torch.cuda.Event(enable_timing=True)
+        l1 = torch.cuda.Event(enable_timing=True)
+        l0.record(stream)
+        with torch.cuda.stream(stream):
+            dbuf.copy_(hbuf, non_blocking=True)
+        l1.record(stream)
+        l1.synchronize()
+        link = max(link, hbuf.nbytes / (l0.elapsed_time(l1) * 1e-3) / 1e9)
+    del hbuf, dbuf
+    peak, peak_src = measured_peaks()
+    link_src = "measured: 256 MiB page-locked cudaMemcpyAsync, best of 5"
+
+    # Algorithmic bytes per launch of each kernel of the step ("Roofline"); the bound
+    # is HBM except for the fetch, which is bound by the host link.
     counts = eng.p_count.cpu().numpy().astype(np.int64)
     st = st_all.cpu().numpy()
+    fetched_rows = fc_all.cpu().numpy().astype(np.int64)          # [Q][units] of the last step
     units_layer = w.B * w.h_kv
-    sketch_bytes = units_layer * w.n * w.d * 2
+    units_all = w.B * w.L * w.h_kv
     algo = {
-        "k_score": sketch_bytes,
-        "k_certify": units_layer * (w.n * 4 + (w.n // 8)),
-        "k_partial(pivotal)": int(counts.mean() * units_layer * (4 * w.d + 8)),
+        "k_score": ("hbm", units_layer * w.n * w.d * 2),
+        "k_certify": ("hbm", units_layer * (w.n * 4 + w.n // 8)),
+        "k_partial(pivotal)": ("hbm", int(counts.mean() * units_layer * (4 * w.d + 8))),
+        # with the exact sketch only V rows (2 d bytes) cross the host link
+        "k_partial(host)": ("h2d", int(fetched_rows.sum(1).mean() * 2 * w.d)),
+        "k_pc_solve": ("hbm", int(units_all * w.n * 8.125 + counts.sum() * 8)),
+        "k_pc_gather": ("hbm", int(counts.sum() * 2 * 4 * w.d)),
     }
-    peak, peak_src = measured_peaks()
+    rooflines = {}
+    for k, (bound, nbytes) in algo.items():
+        if k in per_kernel and nbytes > 0:
+            t_us = per_kernel[k]["avg_us"]
+            ach = nbytes / (t_us * 1e-6) / 1e9
+            pk = link if bound == "h2d" else peak
+            rooflines[k] = {"bound": bound, "achieved": round(ach, 1), "peak": round(pk, 1),
+                            "unit": "GB/s", "frac": round(ach / pk, 4), "avg_us": round(t_us, 3),
+                            "algorithmic_bytes_per_launch": int(nbytes),
+                            "traffic": traffic_for(k),
+                            "peak_source": link_src if bound == "h2d" else peak_src}
     dom = max(per_kernel, key=lambda k: per_kernel[k]["total_ms"])
-    dom_bytes = algo.get(dom)
-    roof = None
-    if dom_bytes is not None:
-        ach = dom_bytes / (per_kernel[dom]["avg_us"] * 1e-6) / 1e9
-        roof = {"bound": "hbm", "kernel": dom, "achieved": round(ach, 1), "peak": peak,
-                "unit": "GB/s", "frac": round(ach / peak, 4), "traffic": traffic_for(dom),
-                "algorithmic_bytes_per_launch": int(dom_bytes), "peak_source": peak_src}
-    kernel_frac = {}
-    for k, b in algo.items():
-        if k in per_kernel:
-            a = b / (per_kernel[k]["avg_us"] * 1e-6) / 1e9
-            kernel_frac[k] = {"avg_us": round(per_kernel[k]["avg_us"], 3),
-                              "GB_s": round(a, 1), "frac": round(a / peak, 4)}
-
+    roof = dict(rooflines[dom], kernel=dom) if dom in rooflines else None
+    hbm = {k: v for k, v in rooflines.items() if v["bound"] == "hbm"}
+    dom_hbm = max(hbm, key=lambda k: per_kernel[k]["total_ms"]) if hbm else None
+    roof_hbm = dict(hbm[dom_hbm], kernel=dom_hbm) if dom_hbm else None
+    fetch = None
+    if "k_partial(host)" in rooflines:
+        f = rooflines["k_partial(host)"]
+        fetch = {"kernel": "k_partial(host)", "bytes_per_query": f["algorithmic_bytes_per_launch"],
+                 "avg_us": f["avg_us"], "achieved_GBs": f["achieved"], "link_peak_GBs": f["peak"],
+                 "frac": f["frac"], "link_peak_source": link_src}
     stats_f = st[..., :10].view(np.float32)
     certified = st[..., 10]
     nfetch = st[..., 13]
@@ -431,9 +461,10 @@ def run_ours(args, world, rank, local):
                           "l2": "inputs larger than L2 (4 x 73 MiB resident state per step)",
                           "fetch": args.fetch_mode, "graph": graph is not None,
                           "parallelism": f"replicas x{world}"},
-               "roofline": roof, "kernels": kernel_frac, "per_kernel_us": {
+               "roofline": roof, "roofline_hbm": roof_hbm, "rooflines": rooflines,
+               "per_kernel_us": {
                    k: round(v["avg_us"], 3) for k, v in per_kernel.items()},
-               "fetch_stats": fetch_stats, "clocks": clk.summary(),
+               "fetch_stats": fetch_stats, "fetch": fetch, "clocks": clk.summary(),
                "gpu_launches": launches_per_step * args.steps,
                "launches_per_step": launches_per_step,
                "e2e": e2e, "cpu_baseline": cpu}

@@ -95,11 +95,15 @@ typedef struct {
 } verkv_sketch;
 
 /* How verkv_fetch_refine moves the selected rows from the host-resident full cache.
- * ZEROCOPY: a gather kernel on the side stream reads the rows straight from page-locked host
- *           memory (no host round trip; default).
+ * ZEROCOPY: a kernel on the side stream reads the selected rows straight from page-locked host
+ *           memory and accumulates them into the refined estimator in the same pass (no host
+ *           round trip, no staging; default).
  * MEMCPY:   the host waits for the selection, gathers the rows into page-locked staging with a
- *           thread pool, and cudaMemcpyAsync moves them on the side stream. */
-enum { VERKV_FETCH_ZEROCOPY = 0, VERKV_FETCH_MEMCPY = 1 };
+ *           thread pool, and cudaMemcpyAsync moves them on the side stream.
+ * With the exact sketch the GPU already holds every key, so by default only the V row of a
+ * fetched token crosses the host link and its K row is read from the sketch; or-ing in
+ * VERKV_FETCH_KEYS moves the full K|V row instead (same results, twice the link bytes). */
+enum { VERKV_FETCH_ZEROCOPY = 0, VERKV_FETCH_MEMCPY = 1, VERKV_FETCH_KEYS = 4 };
 
 /* Per query head results of one attend + fetch_refine, written by verkv_fetch_refine.
  *   m          max sketch logit q.k/sqrt(d) (the shift of every weight below)
@@ -137,9 +141,9 @@ verkv_status verkv_create(verkv_ctx **ctx, int device, void *stream, const verkv
 /* Release the side stream, events, staging and thread pool (after synchronising). */
 void verkv_destroy(verkv_ctx *ctx);
 
-/* Select VERKV_FETCH_ZEROCOPY or VERKV_FETCH_MEMCPY.  MEMCPY allocates page-locked staging of
- * units_per_layer * n * 4d bytes on first use. */
-verkv_status verkv_set_fetch_mode(verkv_ctx *ctx, int mode);
+/* Select VERKV_FETCH_ZEROCOPY or VERKV_FETCH_MEMCPY, optionally or-ed with VERKV_FETCH_KEYS.
+ * MEMCPY allocates page-locked staging of units_per_layer * n * 4d bytes on first use. */
+verkv_status verkv_set_fetch_mode(verkv_ctx *ctx, int mode_flags);
 
 /* PoissonComp (summary page, Methodology, POISSONCOMP: Eq. (3), the H / L partition and the
  * Poisson sample S), for every unit of the shape.
@@ -175,7 +179,8 @@ verkv_status verkv_sketch_build(verkv_ctx *ctx, const void *kv_full, int32_t for
  *   fetch_ids_out  optional (NULL) device or page-locked host int32 [batch*kv_heads][n]: for each
  *                  KV head of this layer, the ascending ids of the union over its query heads of
  *                  F \ S (the rows that must move)
- *   fetch_counts_out optional int32 [batch*kv_heads]: the number of ids per KV head
+ *   fetch_counts_out optional int32 [batch*kv_heads]: the number of ids per KV head (either
+ *                  output may be given without the other)
  * Per query head: sketch logits for all n tokens, w-hat = exp(logit - max), the beta fixed point,
  * the certificate, and when it fails the order of Eq. (9) (ties to the lower token id) and the
  * minimal k* of Eq. (10); then the shrinkage-weighted partial sums over the pivotal set.
@@ -216,8 +221,8 @@ enum {
     VERKV_K_CERTIFY,           /* beta solve, certificate, selection (Eq. 7-10)   */
     VERKV_K_FETCHLIST,         /* per-KV-head fetch id list                       */
     VERKV_K_PARTIAL_PIVOTAL,   /* shrinkage-weighted sums over the pivotal set    */
-    VERKV_K_GATHER_HOST,       /* zero-copy fetch of selected rows from host      */
-    VERKV_K_PARTIAL_FETCHED,   /* exact sums over the fetched rows                */
+    VERKV_K_FETCH_HOST,        /* zero-copy fetch + exact sums over fetched rows  */
+    VERKV_K_PARTIAL_STAGED,    /* exact sums over rows staged by cudaMemcpyAsync  */
     VERKV_K_MERGE,             /* merge partials into o, lse and statistics       */
     VERKV_K_COUNT
 };

@@ -75,6 +75,19 @@ def test_memcpy_mode_matches_zerocopy():
             assert np.array_equal(x["ids"][ul, :c], y["ids"][ul, :c])
 
 
+def test_fetching_keys_too_matches_values_only():
+    # With the exact sketch the fetch moves only V rows by default; moving full K|V rows must give
+    # bitwise the same results, in both fetch modes.
+    w = I.make_workload("keys", B=1, L=2, h_kv=2, G=4, d=128, n=8192, eta=1 / 8, n_queries=4,
+                        plant_every=2)
+    _, a = _run_all(w)
+    _, b = _run_all(w, fetch_mode=B.VERKV_FETCH_ZEROCOPY | B.VERKV_FETCH_KEYS)
+    _, c = _run_all(w, fetch_mode=B.VERKV_FETCH_MEMCPY | B.VERKV_FETCH_KEYS)
+    for x, y, z in zip(a, b, c):
+        assert np.array_equal(x["o"], y["o"]) and np.array_equal(x["o"], z["o"])
+        assert np.array_equal(x["lse"], y["lse"]) and np.array_equal(x["lse"], z["lse"])
+
+
 def test_eta_one_is_dense_attention():
     import oracle as O
     w = I.make_workload("dense", B=1, L=1, h_kv=2, G=4, d=128, n=2048, eta=1.0, n_local=64,

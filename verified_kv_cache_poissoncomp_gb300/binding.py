@@ -23,6 +23,7 @@ VERKV_ESTATE = 8
 VERKV_SKETCH_EXACT = 0
 VERKV_FETCH_ZEROCOPY = 0
 VERKV_FETCH_MEMCPY = 1
+VERKV_FETCH_KEYS = 4
 
 EXPORTED = ["verkv_workspace_size", "verkv_create", "verkv_destroy", "verkv_set_fetch_mode",
             "verkv_poissoncomp", "verkv_sketch_build", "verkv_attend_verified",

@@ -136,6 +136,7 @@ struct verkv_ctx {
     uint16_t *staging = nullptr;
     float *part_piv = nullptr, *part_fet = nullptr;
     int fetch_mode = VERKV_FETCH_ZEROCOPY;
+    bool fetch_keys = false;  // move K rows too, although the exact sketch holds every key
     // MEMCPY mode
     unsigned char *host_staging = nullptr;
     int32_t *host_ids = nullptr, *host_counts = nullptr;     // mapped page-locked
@@ -148,6 +149,7 @@ struct verkv_ctx {
     verkv_pivotal piv{};
     const int32_t *user_ids = nullptr, *user_counts = nullptr;
     const void *q = nullptr;
+    const void *sketch = nullptr;
     std::string last_error;
     // Measurement
     int64_t launches[VERKV_K_COUNT] = {};
@@ -294,10 +296,12 @@ void verkv_destroy(verkv_ctx *ctx) {
     delete ctx;
 }
 
-verkv_status verkv_set_fetch_mode(verkv_ctx *ctx, int mode) {
+verkv_status verkv_set_fetch_mode(verkv_ctx *ctx, int mode_flags) {
     if (!ctx) return VERKV_EINVAL;
+    const int mode = mode_flags & ~VERKV_FETCH_KEYS;
     if (mode != VERKV_FETCH_ZEROCOPY && mode != VERKV_FETCH_MEMCPY)
         return fail(ctx, VERKV_EINVAL, "unknown fetch mode");
+    ctx->fetch_keys = (mode_flags & VERKV_FETCH_KEYS) != 0;
     if (mode == VERKV_FETCH_MEMCPY && !ctx->host_staging) {
         const size_t rows = (size_t)ctx->L.units_layer * ctx->sh.n;
         VERKV_CUDA(cudaSetDevice(ctx->device), "cudaSetDevice");
@@ -398,8 +402,6 @@ verkv_status verkv_attend_verified(verkv_ctx *ctx, int32_t layer, const void *q,
     if (sketch->format != VERKV_SKETCH_EXACT) return fail(ctx, VERKV_EINVAL, "attend: unknown sketch format");
     if (!(eps > 0.0f) || !(delta > 0.0f) || !(delta < 1.0f) || !isfinite(eps))
         return fail(ctx, VERKV_EINVAL, "attend: need eps > 0 and 0 < delta < 1");
-    if ((fetch_ids_out == nullptr) != (fetch_counts_out == nullptr))
-        return fail(ctx, VERKV_EINVAL, "attend: give both fetch_ids_out and fetch_counts_out or neither");
     VERKV_CUDA(cudaSetDevice(ctx->device), "cudaSetDevice");
     const LayerIdx li = layer_idx(ctx, layer);
     const int n = ctx->sh.n, d = ctx->sh.head_dim;
@@ -464,7 +466,10 @@ verkv_status verkv_attend_verified(verkv_ctx *ctx, int32_t layer, const void *q,
     pa.n = n;
     pa.W = ctx->L.W;
     pa.d = d;
-    pa.pivotal = 1;
+    pa.mode = ROWS_PIVOTAL;
+    pa.keys = nullptr;
+    pa.row16 = d / 4;
+    pa.voff16 = d / 8;
     pa.scale = sa.scale;
     pa.li = li;
     int grid = std::min(ctx->L.units_layer * ctx->L.max_piv, ctx->sms * 8);
@@ -477,6 +482,7 @@ verkv_status verkv_attend_verified(verkv_ctx *ctx, int32_t layer, const void *q,
     ctx->user_ids = fetch_ids_out;
     ctx->user_counts = fetch_counts_out;
     ctx->q = q;
+    ctx->sketch = sketch->data;
     return VERKV_OK;
 }
 
@@ -485,31 +491,55 @@ verkv_status verkv_fetch_refine(verkv_ctx *ctx, const int32_t *ids, const int32_
                                 verkv_head_stats *stats_out) {
     if (!ctx) return VERKV_EINVAL;
     if (!ctx->pending) return fail(ctx, VERKV_ESTATE, "fetch_refine: no preceding attend_verified");
-    if ((ids || counts) && (ids != ctx->user_ids || counts != ctx->user_counts))
+    if ((ids && ids != ctx->user_ids) || (counts && counts != ctx->user_counts))
         return fail(ctx, VERKV_EINVAL, "fetch_refine: ids/counts must be the attend outputs or NULL");
     if (!host_kv || !o_out) return fail(ctx, VERKV_EINVAL, "fetch_refine: null pointer");
     VERKV_CUDA(cudaSetDevice(ctx->device), "cudaSetDevice");
     const LayerIdx li = layer_idx(ctx, ctx->layer);
     const int n = ctx->sh.n, d = ctx->sh.head_dim;
-    const size_t row_bytes = (size_t)4 * d;
+    // With the exact sketch every key is already on the GPU: only V rows move, unless asked.
+    const bool v_only = !ctx->fetch_keys;
+    const size_t row_bytes = (size_t)4 * d;                 // a K|V row of the host cache
+    const size_t move_bytes = v_only ? (size_t)2 * d : row_bytes;
+    const size_t move_off = v_only ? (size_t)2 * d : 0;     // V follows K inside a row
+
+    PartialArgs pa{};
+    pa.q = (const uint16_t *)ctx->q;
+    pa.F = ctx->F;
+    pa.qstats = ctx->qstats;
+    pa.part = ctx->part_fet;
+    pa.ids = ctx->fids;
+    pa.pr = nullptr;
+    pa.count = ctx->fcounts;
+    pa.row_stride = n;
+    pa.max_chunks = ctx->L.max_fet;
+    pa.n = n;
+    pa.W = ctx->L.W;
+    pa.d = d;
+    pa.scale = (float)(1.0 / sqrt((double)d));
+    pa.li = li;
+    pa.keys = v_only ? (const uint16_t *)ctx->sketch : nullptr;
+    int grid = std::max(1, std::min(ctx->L.units_layer * ctx->L.max_fet, ctx->sms * 8));
 
     if (ctx->fetch_mode == VERKV_FETCH_ZEROCOPY) {
+        // The fetch and the refine in one kernel on the side stream, reading page-locked host
+        // memory directly; it overlaps the pivotal partial sums on the main stream.
         cudaPointerAttributes attr;
         cudaError_t e = cudaPointerGetAttributes(&attr, host_kv);
         if (e != cudaSuccess || attr.type != cudaMemoryTypeHost || !attr.devicePointer) {
             cudaGetLastError();
             return fail(ctx, VERKV_EINVAL, "fetch_refine: host_kv is not page-locked host memory");
         }
+        pa.rows = (const uint16_t *)attr.devicePointer;
+        pa.mode = ROWS_HOST;
+        pa.row16 = d / 4;
+        pa.voff16 = d / 8;
+        // One CTA per SM keeps the link busy and leaves room for the pivotal partial sums.
+        grid = std::max(1, std::min(ctx->L.units_layer * ctx->L.max_fet, ctx->sms));
         VERKV_CUDA(cudaStreamWaitEvent(ctx->side, ctx->e_sel, 0), "cudaStreamWaitEvent");
-        GatherArgs ga{};
-        ga.host_kv = (const uint16_t *)attr.devicePointer;
-        ga.ids = ctx->fids;
-        ga.counts = ctx->fcounts;
-        ga.staging = ctx->staging;
-        ga.n = n;
-        ga.d = d;
-        ga.li = li;
-        VERKV_CUDA(tracked(ctx, VERKV_K_GATHER_HOST, ctx->side, [&] { return launch_gather_host(ga, ctx->L.units_layer, ctx->side); }), "k_gather_host");
+        VERKV_CUDA(tracked(ctx, VERKV_K_FETCH_HOST, ctx->side, [&] { return launch_partial(pa, ctx->L.units_layer, grid, ctx->side); }), "k_partial(host)");
+        VERKV_CUDA(cudaEventRecord(ctx->e_fetch, ctx->side), "cudaEventRecord");
+        VERKV_CUDA(cudaStreamWaitEvent(ctx->main, ctx->e_fetch, 0), "cudaStreamWaitEvent");
     } else {
         VERKV_CUDA(cudaEventSynchronize(ctx->e_sel), "cudaEventSynchronize");
         const int U = ctx->L.units_layer;
@@ -527,42 +557,27 @@ verkv_status verkv_fetch_refine(verkv_ctx *ctx, const int32_t *ids, const int32_
                 const int64_t j = x - start[ul];
                 const int ug = li.unit_global(ul);
                 const int id = ctx->host_ids[(size_t)ul * n + j];
-                memcpy(ctx->host_staging + ((size_t)ul * n + j) * row_bytes,
-                       src_base + ((size_t)ug * n + id) * row_bytes, row_bytes);
+                memcpy(ctx->host_staging + ((size_t)ul * n + j) * move_bytes,
+                       src_base + ((size_t)ug * n + id) * row_bytes + move_off, move_bytes);
             }
         });
         for (int ul = 0; ul < U; ++ul) {
             const int cnt = ctx->host_counts[ul];
             if (cnt <= 0) continue;
-            cudaError_t e = cudaMemcpyAsync((unsigned char *)ctx->staging + (size_t)ul * n * row_bytes,
-                                            ctx->host_staging + (size_t)ul * n * row_bytes,
-                                            (size_t)cnt * row_bytes, cudaMemcpyHostToDevice, ctx->side);
+            cudaError_t e = cudaMemcpyAsync((unsigned char *)ctx->staging + (size_t)ul * n * move_bytes,
+                                            ctx->host_staging + (size_t)ul * n * move_bytes,
+                                            (size_t)cnt * move_bytes, cudaMemcpyHostToDevice, ctx->side);
             if (e != cudaSuccess)
                 return fail(ctx, VERKV_ECOPY, std::string("fetch copy: ") + cudaGetErrorString(e));
         }
+        VERKV_CUDA(cudaEventRecord(ctx->e_fetch, ctx->side), "cudaEventRecord");
+        VERKV_CUDA(cudaStreamWaitEvent(ctx->main, ctx->e_fetch, 0), "cudaStreamWaitEvent");
+        pa.rows = ctx->staging;
+        pa.mode = ROWS_STAGED;
+        pa.row16 = (int)(move_bytes / 16);
+        pa.voff16 = v_only ? 0 : d / 8;
+        VERKV_CUDA(tracked(ctx, VERKV_K_PARTIAL_STAGED, ctx->main, [&] { return launch_partial(pa, ctx->L.units_layer, grid, ctx->main); }), "k_partial(staged)");
     }
-    VERKV_CUDA(cudaEventRecord(ctx->e_fetch, ctx->side), "cudaEventRecord");
-    VERKV_CUDA(cudaStreamWaitEvent(ctx->main, ctx->e_fetch, 0), "cudaStreamWaitEvent");
-
-    PartialArgs pa{};
-    pa.rows = ctx->staging;
-    pa.ids = ctx->fids;
-    pa.pr = nullptr;
-    pa.count = ctx->fcounts;
-    pa.q = (const uint16_t *)ctx->q;
-    pa.F = ctx->F;
-    pa.qstats = ctx->qstats;
-    pa.part = ctx->part_fet;
-    pa.row_stride = n;
-    pa.max_chunks = ctx->L.max_fet;
-    pa.n = n;
-    pa.W = ctx->L.W;
-    pa.d = d;
-    pa.pivotal = 0;
-    pa.scale = (float)(1.0 / sqrt((double)d));
-    pa.li = li;
-    const int grid = std::max(1, std::min(ctx->L.units_layer * ctx->L.max_fet, ctx->sms * 8));
-    VERKV_CUDA(tracked(ctx, VERKV_K_PARTIAL_FETCHED, ctx->main, [&] { return launch_partial(pa, ctx->L.units_layer, grid, ctx->main); }), "k_partial(fetched)");
 
     MergeArgs ma{};
     ma.part_piv = ctx->part_piv;
@@ -639,7 +654,7 @@ verkv_status verkv_launch_counts(verkv_ctx *ctx, int64_t *out) {
 const char *verkv_kernel_name(int k) {
     static const char *names[VERKV_K_COUNT] = {
         "k_pc_solve", "k_pc_gather", "k_sketch_exact", "k_score", "k_certify", "k_fetchlist",
-        "k_partial(pivotal)", "k_gather_host", "k_partial(fetched)", "k_merge"};
+        "k_partial(pivotal)", "k_partial(host)", "k_partial(staged)", "k_merge"};
     return (k >= 0 && k < VERKV_K_COUNT) ? names[k] : "";
 }
 

@@ -100,10 +100,16 @@ struct FetchListArgs {
 cudaError_t launch_fetchlist(const FetchListArgs &a, int units_layer, cudaStream_t s);
 
 // ---------------------------------------------------------------------------------------------
-// Shrinkage-weighted partial sums over a row set (pivotal rows, or fetched rows).
-constexpr int PART_ROWS = 128;
+// Shrinkage-weighted partial sums over a row set: the pivotal rows in HBM, fetched rows staged in
+// HBM, or fetched rows read by token id straight from page-locked host memory.
+constexpr int PART_ROWS = 64;
+enum { ROWS_PIVOTAL = 0, ROWS_STAGED = 1, ROWS_HOST = 2 };
 struct PartialArgs {
-    const uint16_t *rows;     // [src units][row_stride][2][d]
+    const uint16_t *rows;     // [src units][row_stride][row16 vectors]; ROWS_HOST: [units][n][2][d]
+    const uint16_t *keys;     // if set, K rows come from here by token id ([units][n][d], the
+                              // exact sketch) and `rows` supply only V
+    int row16;                // 16-byte vectors per row of `rows`
+    int voff16;               // offset of the V row inside a row of `rows`, in 16-byte vectors
     const int32_t *ids;       // [src units][row_stride]
     const float *pr;          // pivotal r [src units][row_stride], or null for fetched rows
     const int32_t *count;     // [src units]
@@ -114,22 +120,11 @@ struct PartialArgs {
     int row_stride;           // cap (pivotal) or n (fetched)
     int max_chunks;
     int n, W, d;
-    int pivotal;              // 1: pivotal rows of global units; 0: fetched rows of layer units
+    int mode;                 // ROWS_PIVOTAL (global units) / ROWS_STAGED / ROWS_HOST (layer units)
     float scale;
     LayerIdx li;
 };
 cudaError_t launch_partial(const PartialArgs &a, int units_layer, int grid, cudaStream_t s);
-
-// Zero-copy fetch: staging[u'][j] = host_kv[u][ids[u'][j]].
-struct GatherArgs {
-    const uint16_t *host_kv;  // device-accessible pointer to page-locked [units][n][2][d]
-    const int32_t *ids;       // [units_layer][n]
-    const int32_t *counts;    // [units_layer]
-    uint16_t *staging;        // [units_layer][n][2][d]
-    int n, d;
-    LayerIdx li;
-};
-cudaError_t launch_gather_host(const GatherArgs &a, int units_layer, cudaStream_t s);
 
 // Merge partials into o, lse and the per-head stats.
 struct MergeArgs {
