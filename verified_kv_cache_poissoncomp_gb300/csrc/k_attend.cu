@@ -287,12 +287,13 @@ cudaError_t launch_partial(const PartialArgs &a, int units_layer, int grid, cuda
 }
 
 // ---------------------------------------------------------------------------------------------
-// One CTA per query head; thread t sums every fourth chunk of one column (loads in flight across
-// the four groups), then the groups are added in a fixed order.
-constexpr int MG_NT = 512;
+// One CTA per query head; 8 groups of 128 threads each sum every eighth chunk of their columns
+// (loads in flight across the groups), then the groups are added in a fixed order.
+constexpr int MG_NT = 1024;
+constexpr int MG_GROUPS = MG_NT / 128;
 
 __global__ void __launch_bounds__(MG_NT) k_merge(MergeArgs a) {
-    extern __shared__ float red[];  // [4][d + 2]
+    extern __shared__ float red[];  // [MG_GROUPS][d + 2]
     const int qh = blockIdx.x;
     const int G = a.li.G;
     const int ul = qh / G, g = qh - ul * G;
@@ -309,27 +310,26 @@ __global__ void __launch_bounds__(MG_NT) k_merge(MergeArgs a) {
     for (int c = c0; c < ncol; c += 128) {
         float s = 0.0f;
 #pragma unroll 4
-        for (int ch = grp; ch < npc; ch += 4) s += pp[ch * stride + c];
+        for (int ch = grp; ch < npc; ch += MG_GROUPS) s += pp[ch * stride + c];
 #pragma unroll 4
-        for (int ch = grp; ch < nfc; ch += 4) s += pf[ch * stride + c];
+        for (int ch = grp; ch < nfc; ch += MG_GROUPS) s += pf[ch * stride + c];
         red[grp * ncol + c] = s;
     }
     __syncthreads();
-    float *tot = red;  // reuse row 0 after reading
-    float colsum[2];
-    int nmine = 0;
-    for (int c = threadIdx.x; c < ncol; c += MG_NT)
-        colsum[nmine++] = ((red[c] + red[ncol + c]) + red[2 * ncol + c]) + red[3 * ncol + c];
+    if (threadIdx.x < ncol) {
+        const int c = threadIdx.x;
+        float t = red[c];
+#pragma unroll
+        for (int k = 1; k < MG_GROUPS; ++k) t += red[k * ncol + c];
+        red[c] = t;  // only this thread reads or writes column c of row 0 now
+    }
     __syncthreads();
-    nmine = 0;
-    for (int c = threadIdx.x; c < ncol; c += MG_NT) tot[c] = colsum[nmine++];
-    __syncthreads();
-    const float Dh = tot[D];
-    for (int c = threadIdx.x; c < D; c += MG_NT) a.o[(size_t)qh * D + c] = tot[c] / Dh;
+    const float Dh = red[D];
+    for (int c = threadIdx.x; c < D; c += MG_NT) a.o[(size_t)qh * D + c] = red[c] / Dh;
     if (threadIdx.x == 0) {
         verkv_head_stats st = a.qstats[qh];
         st.D_hat = Dh;
-        st.M2 = tot[D + 1];
+        st.M2 = red[D + 1];
         st.lse = st.m + logf(Dh);
         if (a.lse) a.lse[qh] = st.lse;
         if (a.stats) a.stats[qh] = st;
@@ -337,7 +337,7 @@ __global__ void __launch_bounds__(MG_NT) k_merge(MergeArgs a) {
 }
 
 cudaError_t launch_merge(const MergeArgs &a, int qheads, cudaStream_t s) {
-    k_merge<<<qheads, MG_NT, 4 * (a.d + 2) * sizeof(float), s>>>(a);
+    k_merge<<<qheads, MG_NT, MG_GROUPS * (a.d + 2) * sizeof(float), s>>>(a);
     return cudaGetLastError();
 }
 

@@ -1,9 +1,10 @@
 // k_score.cu -- KVFetch step 1 and the fetch list ("Verify Before You Fetch", summary page,
 // KVFETCH: Verification and Adaptive Fetching, steps 1 and 5).
 //
-// k_score     streams the bf16 sketch once per KV head with coalesced 16-byte loads and scores it
-//             against all G query heads of the group (q slices held in registers; a recursive-
-//             halving shuffle reduce leaves each head's logit in a quarter of the row's lanes).
+// k_score     streams the bf16 sketch once per KV head through a TMA bulk-copy ring in shared
+//             memory and scores it against all G query heads of the group (q slices held in
+//             registers; a recursive-halving shuffle reduce leaves each head's logit in a quarter
+//             of the row's lanes).
 // k_fetchlist ORs the G bitmaps of a KV head, removes resident tokens and writes the ascending
 //             id list of rows to fetch.
 #include <math.h>
@@ -44,17 +45,80 @@ __device__ __forceinline__ float reduce_heads(float (&p)[G], int lane, int &head
     return p[0];
 }
 
+// TMA bulk-copy pipeline.  Each CTA streams a contiguous span of sketch rows of one KV head (the
+// span is sized so the grid is about three CTAs per SM) through a ring of SC_STAGES shared-memory stages of SC_ROWS rows: thread 0 issues one
+// cp.async.bulk per stage that completes on the stage's mbarrier; every warp waits on the barrier,
+// scores its rows from shared memory (16 lanes per 256-byte row: conflict-free 16-byte loads), and
+// after a block barrier the freed stage is refilled.  Waits are bounded by %globaltimer: on expiry
+// the kernel latches ERR_TIMEOUT, waits (bounded again) for its own copies in flight and returns.
+constexpr int SC_NT = 256;
+constexpr int SC_STAGES = 4;
+constexpr int SC_ROWS = 64;
+constexpr unsigned long long SC_WAIT_NS = 1000000000ull;  // 1 s
+
+__device__ __forceinline__ unsigned long long globaltimer_ns() {
+    unsigned long long t;
+    asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
+    return t;
+}
+__device__ __forceinline__ uint32_t smem_addr(const void *p) {
+    return (uint32_t)__cvta_generic_to_shared(p);
+}
+__device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(count));
+}
+__device__ __forceinline__ void mbar_expect_tx(uint64_t *bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)), "r"(bytes)
+                 : "memory");
+}
+__device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t bytes, uint64_t *bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+            smem_addr(dst)),
+        "l"(src), "r"(bytes), "r"(smem_addr(bar))
+        : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
+    uint32_t done;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(done)
+        : "r"(smem_addr(bar)), "r"(parity)
+        : "memory");
+    return done != 0;
+}
+// Wait for phase `parity` of the barrier; false if SC_WAIT_NS elapsed first.
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const unsigned long long t0 = globaltimer_ns();
+    while (!mbar_try_wait(bar, parity))
+        if (globaltimer_ns() - t0 > SC_WAIT_NS) return false;
+    return true;
+}
+
 template <int D, int G>
-__global__ void __launch_bounds__(256) k_score(ScoreArgs a) {
-    constexpr int LPR = D / 8, RPW = 32 / LPR, NW = 8, ROWS = 256, U = 4;
-    constexpr int ITER = (ROWS / NW) / RPW;  // row groups per warp
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+__global__ void __launch_bounds__(SC_NT) k_score(ScoreArgs a, int spans_per_unit, int span_rows) {
+    constexpr int LPR = D / 8, RPW = 32 / LPR, NW = SC_NT / 32;
+    constexpr int ROWB = D * 2;                       // bytes per sketch row
+    constexpr int WROWS = SC_ROWS / NW;               // rows per warp per stage
+    constexpr int SUBMASK = LPR / G - 1;
+    extern __shared__ __align__(128) unsigned char ring[];  // [SC_STAGES][SC_ROWS][ROWB]
+    __shared__ __align__(8) uint64_t full[SC_STAGES];
+    __shared__ int s_abort;
+
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int cgp = lane % LPR, rg = lane / LPR;
-    const int ul = blockIdx.y;
+    const int ul = blockIdx.x / spans_per_unit;
+    const int span = blockIdx.x - ul * spans_per_unit;
     const int b = ul / a.li.kv_heads, h = ul - b * a.li.kv_heads;
     const int ug = a.li.unit_global(ul);
     const int hq = a.li.kv_heads * G;
-    const uint4 *rows = reinterpret_cast<const uint4 *>(a.sketch) + (size_t)ug * a.n * (D / 8);
+    const int row0 = span * span_rows;
+    const int nrows = min(a.n - row0, span_rows);
+    if (nrows <= 0) return;  // uniform over the CTA
+    const int nst = (nrows + SC_ROWS - 1) / SC_ROWS;
+    const unsigned char *src = reinterpret_cast<const unsigned char *>(a.sketch) +
+                               ((size_t)ug * a.n + row0) * ROWB;
 
     float qv[G][8];
 #pragma unroll
@@ -62,44 +126,93 @@ __global__ void __launch_bounds__(256) k_score(ScoreArgs a) {
         const uint4 v = *reinterpret_cast<const uint4 *>(a.q + ((size_t)b * hq + h * G + g) * D + cgp * 8);
         unpack8(v, qv[g]);
     }
-    const int row0 = blockIdx.x * ROWS + warp * (ROWS / NW);
-    float *out = a.scores + (size_t)ul * G * a.n;
-    constexpr int SUBMASK = LPR / G - 1;
-#pragma unroll 1
-    for (int it = 0; it < ITER; it += U) {
-        uint4 kv[U];
+    if (tid == 0) {
+        for (int k = 0; k < SC_STAGES; ++k) mbar_init(&full[k], 1);
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        s_abort = 0;
+    }
+    __syncthreads();
+    auto issue = [&](int k) {
+        const int rows_k = min(SC_ROWS, nrows - k * SC_ROWS);
+        const uint32_t bytes = (uint32_t)rows_k * ROWB;
+        uint64_t *bar = &full[k % SC_STAGES];
+        mbar_expect_tx(bar, bytes);
+        bulk_g2s(ring + (size_t)(k % SC_STAGES) * SC_ROWS * ROWB, src + (size_t)k * SC_ROWS * ROWB,
+                 bytes, bar);
+    };
+    if (tid == 0)
+        for (int k = 0; k < min(SC_STAGES, nst); ++k) issue(k);
+
+    float *out = a.scores + (size_t)ul * G * a.n + row0;
+    int consumed = 0;
+    for (int k = 0; k < nst; ++k) {
+        const uint32_t parity = (uint32_t)((k / SC_STAGES) & 1);
+        if (!mbar_wait_bounded(&full[k % SC_STAGES], parity)) s_abort = 1;
+        __syncthreads();
+        if (s_abort) break;
+        consumed = k + 1;
+        const int rows_k = min(SC_ROWS, nrows - k * SC_ROWS);
+        const unsigned char *stage = ring + (size_t)(k % SC_STAGES) * SC_ROWS * ROWB;
 #pragma unroll
-        for (int j = 0; j < U; ++j) {
-            const int row = row0 + (it + j) * RPW + rg;
-            kv[j] = (it + j < ITER && row < a.n) ? ldg_stream(rows + (size_t)row * (D / 8) + cgp)
-                                                 : make_uint4(0, 0, 0, 0);
-        }
-#pragma unroll
-        for (int j = 0; j < U; ++j) {
-            const int row = row0 + (it + j) * RPW + rg;
-            float k[8];
-            unpack8(kv[j], k);
+        for (int j = 0; j < WROWS / RPW; ++j) {
+            const int r = warp * WROWS + j * RPW + rg;  // row within the stage
+            uint4 kv = make_uint4(0, 0, 0, 0);
+            if (r < rows_k) kv = *reinterpret_cast<const uint4 *>(stage + (size_t)r * ROWB + cgp * 16);
+            float kf[8];
+            unpack8(kv, kf);
             float p[G];
 #pragma unroll
             for (int g = 0; g < G; ++g) {
                 float acc = 0.0f;
 #pragma unroll
-                for (int c = 0; c < 8; ++c) acc = fmaf(qv[g][c], k[c], acc);
+                for (int c = 0; c < 8; ++c) acc = fmaf(qv[g][c], kf[c], acc);
                 p[g] = acc;
             }
             int head;
-            const float s = reduce_heads<G, LPR>(p, lane, head);
-            if ((cgp & SUBMASK) == 0 && it + j < ITER && row < a.n)
-                out[(size_t)head * a.n + row] = s * a.scale;
+            const float sc = reduce_heads<G, LPR>(p, lane, head);
+            if ((cgp & SUBMASK) == 0 && r < rows_k)
+                out[(size_t)head * a.n + k * SC_ROWS + r] = sc * a.scale;
         }
+        __syncthreads();  // every warp is done with the stage: refill it
+        if (tid == 0 && k + SC_STAGES < nst) issue(k + SC_STAGES);
+    }
+    if (s_abort) {
+        // Latch the timeout and let the copies this CTA issued land before it exits.
+        if (tid == 0) {
+            raise_error(a.err, ERR_TIMEOUT);
+            const int issued = min(nst, consumed + SC_STAGES);
+            for (int k = consumed; k < issued; ++k)
+                mbar_wait_bounded(&full[k % SC_STAGES], (uint32_t)((k / SC_STAGES) & 1));
+        }
+        __syncthreads();
     }
 }
 
 cudaError_t launch_score(const ScoreArgs &a, int units_layer, cudaStream_t s) {
-    dim3 grid((a.n + 255) / 256, units_layer);
+    int sms = 0, dev = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    const long long total = (long long)units_layer * a.n;
+    long long span_rows = (total + 3LL * sms - 1) / (3LL * sms);
+    span_rows = (span_rows + SC_ROWS - 1) / SC_ROWS * SC_ROWS;
+    if (span_rows < SC_ROWS) span_rows = SC_ROWS;
+    const int spans = (int)((a.n + span_rows - 1) / span_rows);
+    dim3 grid(spans * units_layer);
+    const size_t smem = (size_t)SC_STAGES * SC_ROWS * a.d * 2;
     const int G = a.li.G;
-#define VERKV_SCORE(DD, GG) \
-    if (a.d == DD && G == GG) { k_score<DD, GG><<<grid, 256, 0, s>>>(a); return cudaGetLastError(); }
+#define VERKV_SCORE(DD, GG)                                                                     \
+    if (a.d == DD && G == GG) {                                                                 \
+        static bool attr = false;                                                               \
+        if (!attr) {                                                                            \
+            cudaError_t e = cudaFuncSetAttribute(k_score<DD, GG>,                               \
+                                                 cudaFuncAttributeMaxDynamicSharedMemorySize,   \
+                                                 (int)smem);                                    \
+            if (e != cudaSuccess) return e;                                                     \
+            attr = true;                                                                        \
+        }                                                                                       \
+        k_score<DD, GG><<<grid, SC_NT, smem, s>>>(a, spans, (int)span_rows);                                    \
+        return cudaGetLastError();                                                              \
+    }
     VERKV_SCORE(128, 1) VERKV_SCORE(128, 2) VERKV_SCORE(128, 4) VERKV_SCORE(128, 8)
     VERKV_SCORE(64, 1) VERKV_SCORE(64, 2) VERKV_SCORE(64, 4) VERKV_SCORE(64, 8)
 #undef VERKV_SCORE

@@ -410,6 +410,7 @@ verkv_status verkv_attend_verified(verkv_ctx *ctx, int32_t layer, const void *q,
     sa.sketch = (const uint16_t *)sketch->data;
     sa.q = (const uint16_t *)q;
     sa.scores = ctx->scores;
+    sa.err = ctx->err;
     sa.n = n;
     sa.d = d;
     sa.scale = (float)(1.0 / sqrt((double)d));
@@ -534,8 +535,9 @@ verkv_status verkv_fetch_refine(verkv_ctx *ctx, const int32_t *ids, const int32_
         pa.mode = ROWS_HOST;
         pa.row16 = d / 4;
         pa.voff16 = d / 8;
-        // One CTA per SM keeps the link busy and leaves room for the pivotal partial sums.
-        grid = std::max(1, std::min(ctx->L.units_layer * ctx->L.max_fet, ctx->sms));
+        // Many rows in flight keep the host link busy; the pivotal partial sums on the main
+        // stream finish well within the fetch.
+        grid = std::max(1, std::min(ctx->L.units_layer * ctx->L.max_fet, ctx->sms * 8));
         VERKV_CUDA(cudaStreamWaitEvent(ctx->side, ctx->e_sel, 0), "cudaStreamWaitEvent");
         VERKV_CUDA(tracked(ctx, VERKV_K_FETCH_HOST, ctx->side, [&] { return launch_partial(pa, ctx->L.units_layer, grid, ctx->side); }), "k_partial(host)");
         VERKV_CUDA(cudaEventRecord(ctx->e_fetch, ctx->side), "cudaEventRecord");
@@ -609,6 +611,7 @@ verkv_status verkv_sync(verkv_ctx *ctx) {
     VERKV_CUDA(cudaMemset(ctx->err, 0, sizeof(word)), "clear error word");
     if (word & ERR_TAU) return fail(ctx, VERKV_EINVAL, "tau outside (0, 1] or not finite");
     if (word & ERR_CAPACITY) return fail(ctx, VERKV_ECAPACITY, "pivotal set exceeded cap (truncated)");
+    if (word & ERR_TIMEOUT) return fail(ctx, VERKV_ETIMEOUT, "a bounded wait on a copy barrier expired");
     if (word & ERR_BUDGET_SUM) return fail(ctx, VERKV_ENOCONVERGE, "|sum r - eta n| >= 1e-6 n");
     return fail(ctx, VERKV_ENOCONVERGE, "a solve hit its iteration cap");
 }

@@ -14,6 +14,7 @@ enum : uint32_t {
     ERR_CAPACITY = 1u << 1,    // pivotal set larger than cap
     ERR_NOCONVERGE = 1u << 2,  // a solve hit its iteration cap
     ERR_BUDGET_SUM = 1u << 3,  // |sum r - eta n| >= 1e-6 n after the c solve
+    ERR_TIMEOUT = 1u << 4,     // a bounded wait on a copy barrier expired
 };
 
 // ---------------------------------------------------------------------------------------------
@@ -60,6 +61,7 @@ struct ScoreArgs {
     const uint16_t *sketch;  // [units][n][d]
     const uint16_t *q;       // [B][hq][d]
     float *scores;           // [B*hq][n]
+    uint32_t *err;
     int n, d;
     float scale;
     LayerIdx li;
