@@ -46,7 +46,8 @@ typedef enum {
     VERKV_ECUDA = 5,       /* CUDA runtime error (see verkv_last_error) */
     VERKV_ECOPY = 6,       /* host-to-device fetch failed */
     VERKV_ETIMEOUT = 7,    /* a bounded device wait expired */
-    VERKV_ESTATE = 8       /* calls out of order, e.g. fetch_refine without attend */
+    VERKV_ESTATE = 8,      /* calls out of order, e.g. fetch_refine without attend */
+    VERKV_ETOOLARGE = 9    /* verkv_certify_noalloc: more logits than its fixed scratch holds */
 } verkv_status;
 
 typedef struct verkv_ctx verkv_ctx;
@@ -209,6 +210,46 @@ verkv_status verkv_fetch_refine(verkv_ctx *ctx, const int32_t *ids, const int32_
  * [batch * kv_heads * q_per_kv][ceil(n/32)] (bit i%32 of word i/32 set iff token i is in F).
  * Stream-ordered; VERKV_ESTATE if no attend has run on this context. */
 verkv_status verkv_selection_bitmap(verkv_ctx *ctx, uint32_t *out);
+
+/* Allocation-free certificate.  The paper has no counterpart: this is a convenience of the
+ * library.  Some callers cannot call cudaMalloc -- for instance code inside a serving runtime that
+ * has already reserved the GPU's memory for its own KV pools, or a plugin interface that hands an
+ * operator only its input and output buffers -- and so cannot provide the workspace a context
+ * needs.  This call runs the same sketch-logit and certificate/selection kernels as
+ * verkv_attend_verified (the certificate, beta, k* and F of every query head) without a context
+ * and without allocating: the logits live in one array of VERKV_NOALLOC_MAX_LOGITS floats
+ * (16 MiB) that the library keeps on every GPU that loads it, until the process exits.
+ *   device     the GPU to run on; made current for the call
+ *   stream     cudaStream_t the kernels are issued on (NULL = legacy default stream)
+ *   units      KV heads in this call (consecutive in every array below)   >= 1
+ *   q_per_kv   query heads per KV head                                    1, 2, 4, 8
+ *   head_dim   d                                                          64 or 128
+ *   n          tokens per unit                                            1 .. 131072
+ *   q          device bf16 [units * q_per_kv][d], 16-byte aligned
+ *   sketch     device bf16 [units][n][d] exact sketch, 16-byte aligned
+ *   r_full     device float [units][n] from verkv_poissoncomp (r_i < 1 marks L)
+ *   eps, delta the tolerance, as in verkv_attend_verified
+ *   stats_out  device verkv_head_stats [units * q_per_kv]: the certificate fields (m, D, beta,
+ *              V, b, eps_hat, eps_final, certified, k_star, n_L, iters, flags); D_hat, M2, lse
+ *              and n_fetch are written as 0
+ *   F_out      device uint32 [units * q_per_kv][ceil(n/32)]: the fetch set F of each query head,
+ *              laid out as in verkv_selection_bitmap
+ *   err_out    device uint32, one word: set to 0 by the call, then or-ed on the device with 4
+ *              if a beta solve hit its iteration cap, 16 if a bounded copy wait expired (the
+ *              outputs of that call are then not valid)
+ * Returns VERKV_ETOOLARGE, launching nothing, when units * q_per_kv * n exceeds
+ * VERKV_NOALLOC_MAX_LOGITS; VERKV_EINVAL for another bad argument; VERKV_ECUDA if a CUDA call
+ * fails.  The first call on a device also looks up the device address of the array (set-up that
+ * runs once per device); make that first call before any stream capture.  All calls on a GPU
+ * share the array, which keeps the last call's logits: nothing in it has to start at zero, as
+ * every call writes each logit before reading it, but calls that overlap on the GPU (other
+ * streams, other host threads) race on it and must be ordered by the caller. */
+enum { VERKV_NOALLOC_MAX_LOGITS = 1 << 22 };
+verkv_status verkv_certify_noalloc(int device, void *stream, int32_t units, int32_t q_per_kv,
+                                   int32_t head_dim, int32_t n, const void *q, const void *sketch,
+                                   const float *r_full, float eps, float delta,
+                                   verkv_head_stats *stats_out, uint32_t *F_out,
+                                   uint32_t *err_out);
 
 /* Measurement.  Every kernel launch is counted per kernel; with profiling enabled each launch is
  * also bracketed by two CUDA events on the stream it runs on (host cost ~2 event records).

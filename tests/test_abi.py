@@ -60,5 +60,22 @@ def test_null_context_and_status_names(lib):
     assert lib.verkv_sync(None) == B.VERKV_EINVAL
     assert lib.verkv_fetch_refine(None, None, None, None, None, None, None) == B.VERKV_EINVAL
     assert lib.verkv_last_error(None) == b""
-    for st, name in [(0, "VERKV_OK"), (2, "VERKV_EBUDGET"), (8, "VERKV_ESTATE")]:
+    for st, name in [(0, "VERKV_OK"), (2, "VERKV_EBUDGET"), (8, "VERKV_ESTATE"),
+                     (9, "VERKV_ETOOLARGE")]:
         assert B.verkv_status_string(st) == name
+
+
+def test_noalloc_argument_checks_need_no_gpu(lib):
+    # The allocation-free certificate rejects an oversized or malformed call before touching CUDA
+    # (dummy pointers: never dereferenced).
+    c = lib.verkv_certify_noalloc
+    args = [0, None, 8, 4, 128, 32768, 16, 16, 16, 0.05, 0.05, 16, 16, 16]
+    big = list(args)
+    big[5] = 131072  # 8 x 4 x 131072 = 2^22 logits: at the limit, so one more KV head is over
+    big[2] = 9
+    assert c(*big) == B.VERKV_ETOOLARGE
+    for i, v in [(3, 3), (4, 96), (5, 0), (5, 131073), (2, 0), (6, None), (13, None), (9, 0.0),
+                 (10, 1.0)]:
+        bad = list(args)
+        bad[i] = v
+        assert c(*bad) == B.VERKV_EINVAL, (i, v)

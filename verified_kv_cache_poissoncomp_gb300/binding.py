@@ -19,6 +19,8 @@ VERKV_ECUDA = 5
 VERKV_ECOPY = 6
 VERKV_ETIMEOUT = 7
 VERKV_ESTATE = 8
+VERKV_ETOOLARGE = 9
+VERKV_NOALLOC_MAX_LOGITS = 1 << 22
 
 VERKV_SKETCH_EXACT = 0
 VERKV_FETCH_ZEROCOPY = 0
@@ -29,7 +31,7 @@ EXPORTED = ["verkv_workspace_size", "verkv_create", "verkv_destroy", "verkv_set_
             "verkv_poissoncomp", "verkv_sketch_build", "verkv_attend_verified",
             "verkv_fetch_refine", "verkv_selection_bitmap", "verkv_profile_enable",
             "verkv_profile_read", "verkv_launch_counts", "verkv_kernel_name", "verkv_sync",
-            "verkv_last_error", "verkv_status_string"]
+            "verkv_last_error", "verkv_status_string", "verkv_certify_noalloc"]
 VERKV_K_COUNT = 10
 
 
@@ -119,6 +121,9 @@ def lib():
         L.verkv_last_error.restype = ctypes.c_char_p
         L.verkv_status_string.argtypes = [ctypes.c_int]
         L.verkv_status_string.restype = ctypes.c_char_p
+        L.verkv_certify_noalloc.argtypes = [ctypes.c_int, vp, i32, i32, i32, i32, vp, vp, vp,
+                                            ctypes.c_float, ctypes.c_float, vp, vp, vp]
+        L.verkv_certify_noalloc.restype = ctypes.c_int
         _lib = L
     return _lib
 
@@ -218,3 +223,12 @@ def verkv_last_error(ctx):
 
 def verkv_status_string(status):
     return lib().verkv_status_string(int(status)).decode()
+
+
+def verkv_certify_noalloc(device, stream, units, q_per_kv, head_dim, n, q, sketch, r_full, eps,
+                          delta, stats_out, F_out, err_out):
+    """The certificate and selection without a context or any allocation (logits in the
+    library's fixed scratch); raises VerkvError, e.g. VERKV_ETOOLARGE above its size limit."""
+    _check(lib().verkv_certify_noalloc(int(device), stream or None, int(units), int(q_per_kv),
+                                       int(head_dim), int(n), q, sketch, r_full, float(eps),
+                                       float(delta), stats_out, F_out, err_out))

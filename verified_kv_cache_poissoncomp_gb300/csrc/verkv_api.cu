@@ -228,6 +228,7 @@ const char *verkv_status_string(int st) {
         case VERKV_ECOPY: return "VERKV_ECOPY";
         case VERKV_ETIMEOUT: return "VERKV_ETIMEOUT";
         case VERKV_ESTATE: return "VERKV_ESTATE";
+        case VERKV_ETOOLARGE: return "VERKV_ETOOLARGE";
         default: return "VERKV_UNKNOWN";
     }
 }
