@@ -4,7 +4,9 @@
 //
 // One thread-block cluster per query head.  Each CTA keeps three words per token in shared
 // memory (the logit, then w-hat; r; r/(1-r), later the g key) and every global quantity is one
-// cluster-wide exchange over distributed shared memory:
+// cluster-wide all-reduce: the warps' records are combined into one record per CTA, each CTA
+// sends its record to every peer over distributed shared memory, and after one cluster barrier
+// every thread combines the CTA records in rank order (the same bits everywhere):
 //   1  max logit, D, sum_L w (1 - r) and |L| in one exchange (per-warp online-softmax records);
 //   2+ beta = sum_L w (1 - lambda(beta)) by safeguarded piece-wise Newton: each pass classifies
 //      every token at the current beta -- at its floor (A += w (1 - r)), in the middle (B += w,
@@ -15,12 +17,13 @@
 //      (g bits << 24 | 2^24-1-token id) -- g descending, ties to the lower id.  Each pass builds a
 //      256-bin histogram of (count, max b_i, sum beta_i, sum v_i) with the sums in 64-bit fixed
 //      point scaled by beta(L) and V(L), added as two 32-bit halves (native integer atomics;
-//      exact, order-independent sums),
-//      and eight warps scan it for the bin in which eps-hat of the remaining tokens drops below
-//      eps.  The first window spans 32 octaves under the largest possible g at 8 bins per octave
+//      exact, order-independent sums); the CTAs' histograms are merged over distributed shared
+//      memory and one warp scans the 256 bins for the bin in which eps-hat of the remaining
+//      tokens drops below eps.  The first window spans 32 octaves under the largest possible g at 8 bins per octave
 //      and folds everything below into bin 0; the select ends when the cut bin holds one token.
 // Per-token terms use lambda w = clip(beta rho, r w, w) with rho = r / (1 - r): no division.
 #include <math.h>
+#include <stddef.h>
 
 #include "verkv_common.cuh"
 #include "verkv_internal.h"
@@ -30,24 +33,24 @@ namespace verkv {
 constexpr int CT_NT = 1024;
 constexpr int CT_NW = CT_NT / 32;
 constexpr int CT_MAX_CL = 8;
-constexpr int CT_REC = 8;   // floats per warp record in a cluster exchange
+constexpr int CT_REC = 8;   // floats per record in a cluster all-reduce
 constexpr int BETA_MAXIT = 64;
 constexpr int SEL_MAXPASS = 16;
-constexpr int SCAN_WARPS = 8;
 
-// Per-CTA histogram bin, built with 32-bit atomics.  A sum is kept in 64-bit fixed point split
-// into a high part (q >> 18) and the low 18 bits, added separately: with the whole mapped to
-// 2^49 the high parts sum below 2^31 and at most 16384 low parts below 2^32, so neither wraps.
-struct HistBin {
-    uint32_t cnt;
-    uint32_t bm;    // max b_i (float bits; b_i >= 0)
-    uint32_t sbh, sbl, svh, svl;
+// Per-CTA 256-bin histogram, built with 32-bit atomics, one array per field (consecutive bins in
+// consecutive banks).  A sum is kept in 64-bit fixed point split into a high part (q >> 18) and
+// the low 18 bits, added separately: with the whole mapped to 2^49 the high parts sum below 2^31
+// and at most 16384 low parts below 2^32, so neither wraps.
+struct Hist {
+    uint32_t cnt[256];
+    uint32_t bm[256];  // max b_i (float bits; b_i >= 0)
+    uint32_t sbh[256], sbl[256], svh[256], svl[256];
 };
-// The cluster-merged bin, with the split sums recombined.
-struct MergedBin {
-    uint32_t cnt;
-    uint32_t bm;
-    unsigned long long sb, sv;
+// The cluster-merged histogram, with the split sums recombined.
+struct Merged {
+    uint32_t cnt[256];
+    uint32_t bm[256];
+    unsigned long long sb[256], sv[256];
 };
 constexpr int FIX_SPLIT = 18;
 
@@ -61,38 +64,59 @@ int certify_chunk(int n, int cl) {
     return (chunk + 31) / 32 * 32;
 }
 size_t certify_smem_bytes(int chunk) {
-    return (size_t)2 * CT_MAX_CL * CT_NW * CT_REC * 4   // exchange slots
-           + 2 * 256 * sizeof(HistBin)                  // two histogram buffers
-           + 256 * sizeof(MergedBin)                    // merged copy
+    return (size_t)CT_NW * CT_REC * 4                   // warp records of this CTA
+           + (size_t)2 * CT_MAX_CL * CT_REC * 4         // CTA records from the cluster, two buffers
+           + 2 * sizeof(Hist)                           // two histogram buffers
+           + sizeof(Merged)                             // merged copy
            + (size_t)chunk * 12 + 64;
 }
 
-// Every warp contributes one record (identical in its lanes).  Lane c writes the record into
-// slot [my rank][warp] of CTA c; after one cluster barrier every CTA holds the cl * NW records in
-// the same order.  Two buffers alternate so a slot is rewritten only after the next barrier.
-template <int K>
-__device__ __forceinline__ const float *cluster_exchange(float *slots, int &parity, int cl,
-                                                         const float (&rec)[K]) {
+// Cluster-wide all-reduce of a K-float record held identically by the lanes of each warp.
+// `comb(x, y)` sets x to x (+) y and must give the same bits for (x, y) and (y, x).  Warp 0
+// combines the CTA's warp records with a butterfly (so its lanes agree), lanes 0..CL-1 send the
+// CTA record into slot [my rank] of each peer, and after one cluster barrier every thread
+// combines the CL records in rank order.  The two CTA-record buffers alternate: a buffer is
+// rewritten two calls later, after a barrier every peer passes only once it has read it.
+template <int CL, int K, class Comb>
+__device__ __forceinline__ void cluster_allreduce(float (&v)[K], float *wrec, float *xrec,
+                                                  int &parity, Comb comb) {
     cg::cluster_group cluster = cg::this_cluster();
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const unsigned me = cluster.block_rank();
-    float *buf = slots + parity * (CT_MAX_CL * CT_NW * CT_REC);
-    if (lane < cl) {
-        float *peer = cluster.map_shared_rank(buf, lane);
+    if (lane == 0) {
 #pragma unroll
-        for (int k = 0; k < K; ++k) peer[(me * CT_NW + warp) * CT_REC + k] = rec[k];
+        for (int k = 0; k < K; ++k) wrec[warp * CT_REC + k] = v[k];
+    }
+    __syncthreads();
+    float *buf = xrec + parity * (CT_MAX_CL * CT_REC);
+    if (warp == 0) {
+        float x[K];
+#pragma unroll
+        for (int k = 0; k < K; ++k) x[k] = wrec[lane * CT_REC + k];
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+            float y[K];
+#pragma unroll
+            for (int k = 0; k < K; ++k) y[k] = __shfl_xor_sync(0xFFFFFFFFu, x[k], o);
+            comb(x, y);
+        }
+        if (lane < CL) {
+            float *peer = cluster.map_shared_rank(buf, lane);
+            const int me = (int)cluster.block_rank();
+#pragma unroll
+            for (int k = 0; k < K; ++k) peer[me * CT_REC + k] = x[k];
+        }
     }
     cluster.sync();
     parity ^= 1;
-    return buf;
-}
-
-// Sum of field k over all records of an exchange, in a fixed order (same bits everywhere).
-__device__ __forceinline__ float records_sum(const float *buf, int total, int k) {
-    const int lane = threadIdx.x & 31;
-    float acc = 0.0f;
-    for (int e = lane; e < total; e += 32) acc += buf[e * CT_REC + k];
-    return warp_sum(acc);
+#pragma unroll
+    for (int k = 0; k < K; ++k) v[k] = buf[k];
+#pragma unroll
+    for (int c = 1; c < CL; ++c) {
+        float y[K];
+#pragma unroll
+        for (int k = 0; k < K; ++k) y[k] = buf[c * CT_REC + k];
+        comb(v, y);
+    }
 }
 
 __device__ __forceinline__ float bern(float b, float V, float l) {
@@ -118,37 +142,207 @@ __device__ __forceinline__ unsigned long long key64(uint32_t gbits, int token) {
     return ((unsigned long long)gbits << 24) | (unsigned long long)(0xFFFFFF - token);
 }
 
-__device__ __forceinline__ unsigned long long to_fixed(float x, float scale) {
-    const float y = x * scale;
-    return y < 1.8e19f ? __float2ull_rn(y) : 18000000000000000000ull;
+// round(x * scale) as its high part (>> FIX_SPLIT) and its low FIX_SPLIT bits, in 32-bit
+// arithmetic (64-bit conversions are slow on this part).  x * scale < 2^50 by construction: a
+// term is at most the whole, which maps to 2^49.  Both the split y = yh 2^18 + rem and rem are
+// exact in float, and yh 2^18 is even, so this is round-half-even of y.
+__device__ __forceinline__ void fixed_split(float x, float scale, uint32_t &hi, uint32_t &lo) {
+    const float y = fminf(x * scale, 1.0e15f);
+    const float yh = truncf(y * (1.0f / (float)(1u << FIX_SPLIT)));
+    const float rem = fmaf(-yh, (float)(1u << FIX_SPLIT), y);
+    uint32_t h = __float2uint_rz(yh), l = __float2uint_rn(rem);
+    if (l >= (1u << FIX_SPLIT)) {
+        l -= 1u << FIX_SPLIT;
+        h += 1u;
+    }
+    hi = h;
+    lo = l;
 }
 
+// Nearest float of a 64-bit integer from two 32-bit conversions (within an ulp).
+__device__ __forceinline__ float u64_to_float(unsigned long long x) {
+    return fmaf((float)(uint32_t)(x >> 32), 4294967296.0f, (float)(uint32_t)x);
+}
+
+// 32-bit shared::cluster address of a local shared-memory address in CTA `rank`.
+__device__ __forceinline__ uint32_t map_cluster(uint32_t local, int rank) {
+    uint32_t r;
+    asm("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(local), "r"(rank));
+    return r;
+}
+__device__ __forceinline__ uint32_t ld_cluster_u32(uint32_t addr) {
+    uint32_t v;
+    asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
+    return v;
+}
+
+// State of the windowed select, uniform over the CTA.
+struct SelState {
+    unsigned long long lo;                // key of the window's first bin
+    unsigned long long cand_lo, cand_hi;  // candidates: keys in [cand_lo, cand_hi)
+    unsigned long long Bb, Bv;            // fixed-point sums of the tokens known to remain
+    unsigned long long fthr;              // result: F = { keys >= fthr }
+    uint32_t Bm;                          // max b of the tokens known to remain (float bits)
+    int shift;                            // bin width 2^shift keys
+    int absorb;                           // bin 0 also takes every candidate below lo
+    int above;                            // tokens known to be in F
+    int done, kstar;
+    float eps_final;
+};
+
+// One pass's scan of the merged histogram by warp 0 and the select's next state (Eq. (10):
+// eps-hat of the remaining set, nonincreasing as tokens are taken in g order).
+__device__ __forceinline__ void select_step(const Merged &mh, SelState &ss, int lane, float SB,
+                                            float SV, float l, float epsD, float D) {
+    const float iSB = SB > 0.0f ? 1.0f / SB : 0.0f;
+    const float iSV = SV > 0.0f ? 1.0f / SV : 0.0f;
+    const unsigned long long Bb = ss.Bb, Bv = ss.Bv;
+    const uint32_t Bm = ss.Bm;
+    // Lane l holds bins 8l .. 8l+7, read with 16-byte loads (conflict-free).
+    const uint4 *pc = reinterpret_cast<const uint4 *>(mh.cnt) + 2 * lane;
+    const uint4 *pm = reinterpret_cast<const uint4 *>(mh.bm) + 2 * lane;
+    const ulonglong2 *pb = reinterpret_cast<const ulonglong2 *>(mh.sb) + 4 * lane;
+    const ulonglong2 *pv = reinterpret_cast<const ulonglong2 *>(mh.sv) + 4 * lane;
+    uint32_t lc, lm;
+    unsigned long long lb = 0ull, lv = 0ull;
+    {
+        const uint4 c0 = pc[0], c1 = pc[1], m0 = pm[0], m1 = pm[1];
+        lc = c0.x + c0.y + c0.z + c0.w + c1.x + c1.y + c1.z + c1.w;
+        lm = max(max(max(m0.x, m0.y), max(m0.z, m0.w)), max(max(m1.x, m1.y), max(m1.z, m1.w)));
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const ulonglong2 b = pb[k], v = pv[k];
+            lb += b.x + b.y;
+            lv += v.x + v.y;
+        }
+    }
+    uint32_t ic = lc, im = lm;
+    unsigned long long ib = lb, iv = lv;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t yc = __shfl_up_sync(0xFFFFFFFFu, ic, o);
+        const uint32_t ym = __shfl_up_sync(0xFFFFFFFFu, im, o);
+        const unsigned long long yb = __shfl_up_sync(0xFFFFFFFFu, ib, o);
+        const unsigned long long yv = __shfl_up_sync(0xFFFFFFFFu, iv, o);
+        if (lane >= o) {
+            ic += yc;
+            im = max(im, ym);
+            ib += yb;
+            iv += yv;
+        }
+    }
+    const uint32_t total = __shfl_sync(0xFFFFFFFFu, ic, 31);
+    uint32_t xc = ic - lc, xm = __shfl_up_sync(0xFFFFFFFFu, im, 1);
+    if (lane == 0) xm = 0u;
+    unsigned long long xb = ib - lb, xv = iv - lv;
+    int best = -1;
+    uint32_t best_c = 0u, best_n = 0u, best_m = 0u;
+    unsigned long long best_b = 0ull, best_v = 0ull;
+    float best_e = 0.0f;
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+        const uint4 c4 = pc[h], m4 = pm[h];
+        const uint32_t cc[4] = {c4.x, c4.y, c4.z, c4.w}, mm[4] = {m4.x, m4.y, m4.z, m4.w};
+        const ulonglong2 b01 = pb[2 * h], b23 = pb[2 * h + 1], v01 = pv[2 * h], v23 = pv[2 * h + 1];
+        const unsigned long long bb[4] = {b01.x, b01.y, b23.x, b23.y};
+        const unsigned long long vv[4] = {v01.x, v01.y, v23.x, v23.y};
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const unsigned long long rsb = Bb + xb, rsv = Bv + xv;
+            const uint32_t rm = max(Bm, xm);
+            const float e = u64_to_float(rsb) * iSB + bern(__uint_as_float(rm), u64_to_float(rsv) * iSV, l);
+            if (cc[k] > 0u && e < epsD) {
+                best = lane * 8 + 4 * h + k;
+                best_c = xc;
+                best_n = cc[k];
+                best_m = rm;
+                best_b = rsb;
+                best_v = rsv;
+                best_e = e;
+            }
+            xc += cc[k];
+            xm = max(xm, mm[k]);
+            xb += bb[k];
+            xv += vv[k];
+        }
+    }
+    int jb = best;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) jb = max(jb, __shfl_xor_sync(0xFFFFFFFFu, jb, o));
+    if (jb < 0) {
+        if (lane == 0) {  // rounding left no bin qualifying: take every candidate
+            ss.kstar = ss.above + (int)total;
+            ss.fthr = ss.absorb ? 0ull : ss.cand_lo;
+            ss.eps_final =
+                (u64_to_float(Bb) * iSB + bern(__uint_as_float(Bm), u64_to_float(Bv) * iSV, l)) / D;
+            ss.done = 1;
+        }
+        return;
+    }
+    if (best != jb) return;
+    const int cj = (int)best_n;
+    ss.Bb = best_b;
+    ss.Bv = best_v;
+    ss.Bm = best_m;
+    ss.eps_final = best_e / D;
+    const int above = ss.above + (int)(total - best_c - best_n);  // bins above the cut
+    ss.above = above;
+    const unsigned long long lo = ss.lo;
+    const int shift = ss.shift;
+    const unsigned long long cut_lo = lo + ((unsigned long long)jb << shift);
+    if (ss.absorb && jb == 0) {
+        // The cut lies in bin 0, which also holds every candidate below the window.
+        if (cj == 1) {  // one token left: it is taken, and so is every other token
+            ss.kstar = above + 1;
+            ss.fthr = 0ull;
+            ss.done = 1;
+            return;
+        }
+        // Slide the window down at the same resolution; it ends where bin 0 ended.
+        ss.cand_lo = 0ull;
+        ss.cand_hi = lo + (1ull << shift);
+        const unsigned long long span = 255ull << shift;
+        if (lo > span) {
+            ss.lo = lo - span;
+        } else {
+            ss.lo = 0ull;
+            ss.absorb = 0;
+        }
+        return;
+    }
+    if (cj == 1 || shift == 0) {
+        ss.kstar = above + cj;
+        ss.fthr = cut_lo;
+        ss.done = 1;
+        return;
+    }
+    ss.cand_lo = cut_lo;
+    ss.cand_hi = cut_lo + (1ull << shift);
+    ss.lo = cut_lo;
+    ss.shift = shift >= 8 ? shift - 8 : 0;
+    ss.absorb = 0;
+}
+
+template <int CL>
 __global__ void __launch_bounds__(CT_NT, 1) k_certify(CertifyArgs a) {
     extern __shared__ __align__(16) unsigned char smem_raw[];
-    float *slots = reinterpret_cast<float *>(smem_raw);
-    MergedBin *mh = reinterpret_cast<MergedBin *>(slots + 2 * CT_MAX_CL * CT_NW * CT_REC);
-    HistBin *hist = reinterpret_cast<HistBin *>(mh + 256);
-    float *W = reinterpret_cast<float *>(hist + 512);  // logit, then w-hat
+    float *wrec = reinterpret_cast<float *>(smem_raw);
+    float *xrec = wrec + CT_NW * CT_REC;
+    Merged &mh = *reinterpret_cast<Merged *>(xrec + 2 * CT_MAX_CL * CT_REC);
+    Hist *hist = reinterpret_cast<Hist *>(&mh + 1);
+    float *W = reinterpret_cast<float *>(hist + 2);  // logit, then w-hat
     float *R = W + a.chunk;                          // r (1 for H and padding)
     uint32_t *X = reinterpret_cast<uint32_t *>(R + a.chunk);  // r/(1-r), later the g key
-    __shared__ unsigned long long s_wsb[SCAN_WARPS], s_wsv[SCAN_WARPS];
-    __shared__ uint32_t s_wcnt[SCAN_WARPS], s_wbm[SCAN_WARPS];
-    __shared__ int s_wbest[SCAN_WARPS];
-    __shared__ int bc_int[3];
-    __shared__ unsigned long long bc_u64[2];
-    __shared__ uint32_t bc_bm;
-    __shared__ float bc_e;
 
     cg::cluster_group cluster = cg::this_cluster();
     const int crank = (int)cluster.block_rank();
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int G = a.li.G;
-    const int qh = blockIdx.x / a.cl;
+    const int qh = blockIdx.x / CL;
     const int ul = qh / G;
     const int ug = a.li.unit_global(ul);
-    const int n = a.n, chunk = a.chunk, cl = a.cl;
+    const int n = a.n, chunk = a.chunk;
     const int base = crank * chunk;
-    const int total_rec = cl * CT_NW;
     const float *sc = a.scores + (size_t)qh * n;
     const float *rf = a.r_full + (size_t)ug * n;
     const float eps = a.eps, l = a.ldelta;
@@ -182,21 +376,21 @@ __global__ void __launch_bounds__(CT_NT, 1) k_certify(CertifyArgs a) {
         }
         const float wmax = warp_max(tmax);
         const float sc_t = tmax == NEG_INF ? 0.0f : expf(tmax - wmax);
-        const float rec[4] = {wmax, warp_sum(d * sc_t), warp_sum(c * sc_t), warp_sum(cnt)};
-        const float *buf = cluster_exchange<4>(slots, parity, cl, rec);
-        float mm = NEG_INF;
-        for (int e = lane; e < total_rec; e += 32) mm = fmaxf(mm, buf[e * CT_REC]);
-        m = warp_max(mm);
-        float dd = 0.f, ccs = 0.f;
-        for (int e = lane; e < total_rec; e += 32) {
-            const float mj = buf[e * CT_REC];
-            const float f = mj == NEG_INF ? 0.0f : expf(mj - m);
-            dd += buf[e * CT_REC + 1] * f;
-            ccs += buf[e * CT_REC + 2] * f;
-        }
-        D = warp_sum(dd);
-        C = warp_sum(ccs);
-        nL = records_sum(buf, total_rec, 3);
+        // (max logit, D, C) combine as online-softmax partials; |L| adds.
+        float rec[4] = {wmax, warp_sum(d * sc_t), warp_sum(c * sc_t), warp_sum(cnt)};
+        cluster_allreduce<CL>(rec, wrec, xrec, parity, [&](float (&x)[4], const float (&y)[4]) {
+            const float M = fmaxf(x[0], y[0]);
+            const float fx = x[0] == NEG_INF ? 0.0f : expf(x[0] - M);
+            const float fy = y[0] == NEG_INF ? 0.0f : expf(y[0] - M);
+            x[0] = M;
+            x[1] = x[1] * fx + y[1] * fy;
+            x[2] = x[2] * fx + y[2] * fy;
+            x[3] = x[3] + y[3];
+        });
+        m = rec[0];
+        D = rec[1];
+        C = rec[2];
+        nL = rec[3];
     }
 
     // ---- 2. beta: safeguarded piece-wise Newton from the top of the bracket ----
@@ -207,7 +401,11 @@ __global__ void __launch_bounds__(CT_NT, 1) k_certify(CertifyArgs a) {
         float lo = 0.0f, hi = C;  // h(0) <= 0 <= h(C)
         beta = C;
         for (iters = 1; iters <= BETA_MAXIT; ++iters) {
-            float ab = 0.f, S = 0.f;
+            // Besides the piece's sums, the nearest breakpoints on either side of beta: the
+            // largest one below (pl) and the smallest one at or above (ph).  A token's
+            // breakpoints are w (1 - r), where lambda leaves its floor, and w (1 - r) / r, where
+            // it reaches 1.
+            float ab = 0.f, S = 0.f, pl = 0.f, ph = INFINITY;
             for (int i = tid; i < chunk; i += CT_NT) {
                 const float r = R[i];
                 float w;
@@ -222,22 +420,37 @@ __global__ void __launch_bounds__(CT_NT, 1) k_certify(CertifyArgs a) {
                     const float fl = w * (1.0f - r);
                     if (beta <= fl) {
                         ab += fl;
+                        ph = fminf(ph, fl);
                     } else if (beta * r < fl) {
                         ab += w;
                         S += __uint_as_float(X[i]);
+                        pl = fmaxf(pl, fl);
+                        if (fl < r * ph) ph = fminf(ph, __fdiv_rn(fl, r));
+                    } else if (fl > r * pl) {
+                        pl = fmaxf(pl, __fdiv_rn(fl, r));
                     }
                 }
             }
             first = false;
-            const float rec[2] = {warp_sum(ab), warp_sum(S)};
-            const float *buf = cluster_exchange<2>(slots, parity, cl, rec);
-            ab = records_sum(buf, total_rec, 0);
-            S = records_sum(buf, total_rec, 1);
-            // The root of the linear piece through beta.  When it reproduces beta (to 1e-6
-            // relative: float32 sums jitter by an ulp or two), beta is the fixed point; this is
-            // tested before the bracket, which rounding can leave an ulp off the root.
+            float rec[4] = {warp_sum(ab), warp_sum(S), warp_max(pl), warp_min(ph)};
+            cluster_allreduce<CL>(rec, wrec, xrec, parity,
+                                  [](float (&x)[4], const float (&y)[4]) {
+                                      x[0] += y[0];
+                                      x[1] += y[1];
+                                      x[2] = fmaxf(x[2], y[2]);
+                                      x[3] = fminf(x[3], y[3]);
+                                  });
+            ab = rec[0];
+            S = rec[1];
+            pl = rec[2];
+            ph = rec[3];
+            // The root of the linear piece through beta.  When it lies strictly between the
+            // nearest breakpoints, every token keeps its piece there: it is the fixed point.
+            // When it reproduces beta (to 1e-6 relative: float32 sums jitter by an ulp or two),
+            // likewise; both are tested before the bracket, which rounding can leave an ulp off
+            // the root.
             float nb = __fdiv_rn(ab, 1.0f + S);
-            if (fabsf(nb - beta) <= 1e-6f * beta) {
+            if ((nb > pl && nb < ph) || fabsf(nb - beta) <= 1e-6f * beta) {
                 beta = nb;
                 break;
             }
@@ -276,15 +489,19 @@ __global__ void __launch_bounds__(CT_NT, 1) k_certify(CertifyArgs a) {
             }
         }
         tb = warp_top2(tb);
-        const float rec[5] = {warp_sum(sb), warp_sum(sv), tb.b1, __int_as_float(tb.id1), tb.b2};
-        const float *buf = cluster_exchange<5>(slots, parity, cl, rec);
-        betaL = records_sum(buf, total_rec, 0);
-        VL = records_sum(buf, total_rec, 1);
-        Top2 acc{-1.0f, 0x7FFFFFFF, -1.0f};
-        for (int e = lane; e < total_rec; e += 32)
-            acc = top2_merge(acc, Top2{buf[e * CT_REC + 2], __float_as_int(buf[e * CT_REC + 3]),
-                                       buf[e * CT_REC + 4]});
-        tb = warp_top2(acc);
+        float rec[5] = {warp_sum(sb), warp_sum(sv), tb.b1, __int_as_float(tb.id1), tb.b2};
+        cluster_allreduce<CL>(rec, wrec, xrec, parity, [](float (&x)[5], const float (&y)[5]) {
+            x[0] += y[0];
+            x[1] += y[1];
+            const Top2 t = top2_merge(Top2{x[2], __float_as_int(x[3]), x[4]},
+                                      Top2{y[2], __float_as_int(y[3]), y[4]});
+            x[2] = t.b1;
+            x[3] = __int_as_float(t.id1);
+            x[4] = t.b2;
+        });
+        betaL = rec[0];
+        VL = rec[1];
+        tb = Top2{rec[2], __float_as_int(rec[3]), rec[4]};
     }
     const float b1 = fmaxf(tb.b1, 0.0f), b2 = fmaxf(tb.b2, 0.0f);
     const int id1 = tb.id1;
@@ -292,33 +509,44 @@ __global__ void __launch_bounds__(CT_NT, 1) k_certify(CertifyArgs a) {
     const bool certified = eps_hat < eps;
 
     // ---- 4. selection ----
+    // The select's state is uniform over the CTA and lives in shared memory: one lane of warp 0
+    // decides each pass and every thread reads the outcome after a barrier.
+    __shared__ SelState ss;
     int kstar = 0;
     unsigned long long fthr = ~0ull;  // F = { L tokens with key >= fthr }
     float eps_final = eps_hat;
     if (!certified) {
         const float A = b1 * l * (1.0f / 3.0f);
         const float Rr = sqrtf(fmaf(A, A, 2.0f * VL * l));
-        const float epsD = eps * D;
         // Fixed-point scales: every partial sum is at most the whole, which maps to 2^49 (a scale
         // is capped below the float range; a zero total gives zero sums).
         const float SB = betaL > 0.0f ? fminf(562949953421312.0f / betaL, 1e38f) : 0.0f;
         const float SV = VL > 0.0f ? fminf(562949953421312.0f / VL, 1e38f) : 0.0f;
-        const float iSB = SB > 0.0f ? 1.0f / SB : 0.0f;
-        const float iSV = SV > 0.0f ? 1.0f / SV : 0.0f;
-        // Every g_i D is at most eps-hat(L) D; the first window ends just above that.
-        const uint32_t top = __float_as_uint(betaL + bern(b1, VL, l)) + 256u;
-        const unsigned long long wend = ((unsigned long long)top + 1ull) << 24;
-        unsigned long long lo = wend > (1ull << 52) ? wend - (1ull << 52) : 0ull;
-        int shift = 44;
-        bool absorb = true;  // bin 0 also takes every candidate below lo
-        unsigned long long cand_lo = 0ull, cand_hi = ~0ull;
-        unsigned long long Bb = 0ull, Bv = 0ull;  // tokens known to remain below the candidates
-        uint32_t Bm = 0u;
-        int above = 0;
+        if (tid == 0) {
+            // Every g_i D is at most eps-hat(L) D; the first window ends just above that.
+            const uint32_t top = __float_as_uint(betaL + bern(b1, VL, l)) + 256u;
+            const unsigned long long wend = ((unsigned long long)top + 1ull) << 24;
+            ss.lo = wend > (1ull << 52) ? wend - (1ull << 52) : 0ull;
+            ss.cand_lo = 0ull;
+            ss.cand_hi = ~0ull;
+            ss.Bb = 0ull;  // tokens known to remain below the candidates
+            ss.Bv = 0ull;
+            ss.fthr = ~0ull;
+            ss.Bm = 0u;
+            ss.shift = 44;
+            ss.absorb = 1;  // bin 0 also takes every candidate below lo
+            ss.above = 0;
+            ss.done = 0;
+            ss.kstar = 0;
+            ss.eps_final = eps_hat;
+        }
         for (int pass = 0; pass < SEL_MAXPASS; ++pass) {
-            HistBin *hb = hist + (pass & 1) * 256;
-            for (int j = tid; j < 256; j += CT_NT) hb[j] = HistBin{0u, 0u, 0u, 0u, 0u, 0u};
+            Hist &hb = hist[pass & 1];
+            for (int j = tid; j < 6 * 256; j += CT_NT) (&hb.cnt[0])[j] = 0u;
             __syncthreads();
+            const unsigned long long lo = ss.lo, cand_lo = ss.cand_lo, cand_hi = ss.cand_hi;
+            const int shift = ss.shift;
+            const bool absorb = ss.absorb != 0;
             uint32_t bc = 0u, bbm = 0u, bsbh = 0u, bsbl = 0u, bsvh = 0u, bsvl = 0u;
             for (int i = tid; i < chunk; i += CT_NT) {
                 const float r = R[i];
@@ -347,9 +575,9 @@ __global__ void __launch_bounds__(CT_NT, 1) k_certify(CertifyArgs a) {
                         if (!(k >= cand_lo && k < cand_hi)) continue;
                         token_terms(W[i], r, rho_of(r), beta, bi, vi, bb);
                     }
-                    const unsigned long long qb = to_fixed(bi, SB), qv = to_fixed(vi, SV);
-                    const uint32_t qbh = (uint32_t)(qb >> FIX_SPLIT), qbl = (uint32_t)qb & ((1u << FIX_SPLIT) - 1u);
-                    const uint32_t qvh = (uint32_t)(qv >> FIX_SPLIT), qvl = (uint32_t)qv & ((1u << FIX_SPLIT) - 1u);
+                    uint32_t qbh, qbl, qvh, qvl;
+                    fixed_split(bi, SB, qbh, qbl);
+                    fixed_split(vi, SV, qvh, qvl);
                     if (absorb && k < lo) {
                         bc += 1u;
                         bsbh += qbh;
@@ -360,13 +588,12 @@ __global__ void __launch_bounds__(CT_NT, 1) k_certify(CertifyArgs a) {
                     } else {
                         const unsigned long long dj = (k - lo) >> shift;
                         const int bin = dj > 255ull ? 255 : (int)dj;
-                        HistBin *hx = &hb[bin];
-                        atomicAdd(&hx->cnt, 1u);
-                        atomicMax(&hx->bm, __float_as_uint(bb));
-                        atomicAdd(&hx->sbh, qbh);
-                        atomicAdd(&hx->sbl, qbl);
-                        atomicAdd(&hx->svh, qvh);
-                        atomicAdd(&hx->svl, qvl);
+                        atomicAdd(&hb.cnt[bin], 1u);
+                        atomicMax(&hb.bm[bin], __float_as_uint(bb));
+                        atomicAdd(&hb.sbh[bin], qbh);
+                        atomicAdd(&hb.sbl[bin], qbl);
+                        atomicAdd(&hb.svh[bin], qvh);
+                        atomicAdd(&hb.svl[bin], qvl);
                     }
                 }
             }
@@ -379,159 +606,58 @@ __global__ void __launch_bounds__(CT_NT, 1) k_certify(CertifyArgs a) {
 #pragma unroll
                 for (int o = 16; o > 0; o >>= 1) bbm = max(bbm, __shfl_xor_sync(0xFFFFFFFFu, bbm, o));
                 if (lane == 0 && bc) {
-                    atomicAdd(&hb[0].cnt, bc);
-                    atomicMax(&hb[0].bm, bbm);
-                    atomicAdd(&hb[0].sbh, bsbh);
-                    atomicAdd(&hb[0].sbl, bsbl);
-                    atomicAdd(&hb[0].svh, bsvh);
-                    atomicAdd(&hb[0].svl, bsvl);
+                    atomicAdd(&hb.cnt[0], bc);
+                    atomicMax(&hb.bm[0], bbm);
+                    atomicAdd(&hb.sbh[0], bsbh);
+                    atomicAdd(&hb.sbl[0], bsbl);
+                    atomicAdd(&hb.svh[0], bsvh);
+                    atomicAdd(&hb.svl[0], bsvl);
                 }
             }
             cluster.sync();
             {
-                // thread t merges field t / 256 of bin t % 256 over the cluster, in rank order
+                // Thread t merges field t / 256 of bin t % 256 over the cluster, in rank order;
+                // the CL remote loads are independent and issue together.
                 const int j = tid & 255, f = tid >> 8;
-                MergedBin *mj = &mh[j];
                 if (f <= 1) {
-                    uint32_t acc = 0u;
+                    const uint32_t local = (uint32_t)__cvta_generic_to_shared(f == 0 ? &hb.cnt[j] : &hb.bm[j]);
+                    uint32_t v[CL];
 #pragma unroll
-                    for (int c2 = 0; c2 < CT_MAX_CL; ++c2) {
-                        if (c2 < cl) {
-                            const HistBin *p = cluster.map_shared_rank(hb, c2) + j;
-                            const uint32_t v = f == 0 ? p->cnt : p->bm;
-                            acc = f == 0 ? acc + v : max(acc, v);
-                        }
-                    }
-                    if (f == 0) mj->cnt = acc; else mj->bm = acc;
+                    for (int c2 = 0; c2 < CL; ++c2) v[c2] = ld_cluster_u32(map_cluster(local, c2));
+                    uint32_t acc = v[0];
+#pragma unroll
+                    for (int c2 = 1; c2 < CL; ++c2) acc = f == 0 ? acc + v[c2] : max(acc, v[c2]);
+                    if (f == 0) mh.cnt[j] = acc; else mh.bm[j] = acc;
                 } else {
+                    const uint32_t lh = (uint32_t)__cvta_generic_to_shared(f == 2 ? &hb.sbh[j] : &hb.svh[j]);
+                    const uint32_t ll = (uint32_t)__cvta_generic_to_shared(f == 2 ? &hb.sbl[j] : &hb.svl[j]);
+                    uint32_t hi[CL], lw[CL];
+#pragma unroll
+                    for (int c2 = 0; c2 < CL; ++c2) {
+                        hi[c2] = ld_cluster_u32(map_cluster(lh, c2));
+                        lw[c2] = ld_cluster_u32(map_cluster(ll, c2));
+                    }
                     unsigned long long acc = 0ull;
 #pragma unroll
-                    for (int c2 = 0; c2 < CT_MAX_CL; ++c2) {
-                        if (c2 < cl) {
-                            const HistBin *p = cluster.map_shared_rank(hb, c2) + j;
-                            const uint32_t hi = f == 2 ? p->sbh : p->svh;
-                            const uint32_t lo32 = f == 2 ? p->sbl : p->svl;
-                            acc += ((unsigned long long)hi << FIX_SPLIT) + lo32;
-                        }
-                    }
-                    if (f == 2) mj->sb = acc; else mj->sv = acc;
+                    for (int c2 = 0; c2 < CL; ++c2)
+                        acc += ((unsigned long long)hi[c2] << FIX_SPLIT) + lw[c2];
+                    if (f == 2) mh.sb[j] = acc; else mh.sv[j] = acc;
                 }
             }
             __syncthreads();
-            // Eight warps scan the 256 bins: remaining(j) = below + bins < j (exact integers).
-            unsigned long long xsb = 0ull, xsv = 0ull;
-            uint32_t xcnt = 0u, xbm = 0u, bcnt = 0u;
-            if (warp < SCAN_WARPS) {
-                const MergedBin hbin = mh[warp * 32 + lane];
-                bcnt = hbin.cnt;
-                unsigned long long isb = hbin.sb, isv = hbin.sv;
-                uint32_t icnt = hbin.cnt, ibm = hbin.bm;
-#pragma unroll
-                for (int o = 1; o < 32; o <<= 1) {
-                    const unsigned long long y1 = __shfl_up_sync(0xFFFFFFFFu, isb, o);
-                    const unsigned long long y2 = __shfl_up_sync(0xFFFFFFFFu, isv, o);
-                    const uint32_t y3 = __shfl_up_sync(0xFFFFFFFFu, icnt, o);
-                    const uint32_t y4 = __shfl_up_sync(0xFFFFFFFFu, ibm, o);
-                    if (lane >= o) {
-                        isb += y1;
-                        isv += y2;
-                        icnt += y3;
-                        ibm = max(ibm, y4);
-                    }
-                }
-                xsb = isb - hbin.sb;   // exclusive within the warp (integer: exact)
-                xsv = isv - hbin.sv;
-                xcnt = icnt - hbin.cnt;
-                xbm = __shfl_up_sync(0xFFFFFFFFu, ibm, 1);
-                if (lane == 0) xbm = 0u;
-                if (lane == 31) {
-                    s_wsb[warp] = isb;
-                    s_wsv[warp] = isv;
-                    s_wcnt[warp] = icnt;
-                    s_wbm[warp] = ibm;
-                }
-            }
+            // Warp 0 scans the 256 bins, 8 consecutive bins per lane: remaining(j) = below + bins
+            // < j (exact integers); the cut bin is the last non-empty bin whose remaining set
+            // already certifies.  One lane then moves the select on.
+            if (warp == 0) select_step(mh, ss, lane, SB, SV, l, eps * D, D);
             __syncthreads();
-            int mybest = -1;
-            if (warp < SCAN_WARPS) {
-                for (int w2 = 0; w2 < warp; ++w2) {
-                    xsb += s_wsb[w2];
-                    xsv += s_wsv[w2];
-                    xcnt += s_wcnt[w2];
-                    xbm = max(xbm, s_wbm[w2]);
-                }
-                const unsigned long long rsb = Bb + xsb, rsv = Bv + xsv;
-                const float rb = (float)rsb * iSB, rv = (float)rsv * iSV;
-                const float rm = __uint_as_float(max(Bm, xbm));
-                const float e = rb + bern(rm, rv, l);  // eps-hat of the remaining set, times D
-                if (bcnt > 0u && e < epsD) mybest = warp * 32 + lane;
-                int wb = mybest;
-#pragma unroll
-                for (int o = 16; o > 0; o >>= 1) wb = max(wb, __shfl_xor_sync(0xFFFFFFFFu, wb, o));
-                if (lane == 0) s_wbest[warp] = wb;
-            }
-            __syncthreads();
-            int jb = -1;
-#pragma unroll
-            for (int w2 = 0; w2 < SCAN_WARPS; ++w2) jb = max(jb, s_wbest[w2]);
-            uint32_t total_cnt = 0u;
-#pragma unroll
-            for (int w2 = 0; w2 < SCAN_WARPS; ++w2) total_cnt += s_wcnt[w2];
-            if (jb >= 0 && warp * 32 + lane == jb) {
-                bc_int[0] = (int)(total_cnt - xcnt - bcnt);  // above the cut bin
-                bc_int[1] = (int)bcnt;
-                bc_u64[0] = Bb + xsb;
-                bc_u64[1] = Bv + xsv;
-                bc_bm = max(Bm, xbm);
-                bc_e = ((float)(Bb + xsb) * iSB +
-                        bern(__uint_as_float(max(Bm, xbm)), (float)(Bv + xsv) * iSV, l)) / D;
-            }
-            __syncthreads();
-            if (jb < 0) {  // rounding left no bin qualifying: take every candidate
-                kstar = above + (int)total_cnt;
-                fthr = absorb ? 0ull : cand_lo;
-                eps_final = ((float)Bb * iSB + bern(__uint_as_float(Bm), (float)Bv * iSV, l)) / D;
-                break;
-            }
-            const int cnt_above = bc_int[0], cj = bc_int[1];
-            Bb = bc_u64[0];
-            Bv = bc_u64[1];
-            Bm = bc_bm;
-            eps_final = bc_e;
-            above += cnt_above;
-            const unsigned long long cut_lo = lo + ((unsigned long long)jb << shift);
-            if (absorb && jb == 0) {
-                // The cut lies in bin 0, which also holds every candidate below the window.
-                if (cj == 1) {  // one token left: it is taken, and so is every other token
-                    kstar = above + 1;
-                    fthr = 0ull;
-                    break;
-                }
-                // Slide the window down at the same resolution; it ends where bin 0 ended.
-                cand_lo = 0ull;
-                cand_hi = lo + (1ull << shift);
-                const unsigned long long span = 255ull << shift;
-                if (lo > span) {
-                    lo -= span;
-                } else {
-                    lo = 0ull;
-                    absorb = false;
-                }
-                continue;
-            }
-            if (cj == 1 || shift == 0) {
-                kstar = above + cj;
-                fthr = cut_lo;
-                break;
-            }
-            cand_lo = cut_lo;
-            cand_hi = cut_lo + (1ull << shift);
-            lo = cut_lo;
-            shift = shift >= 8 ? shift - 8 : 0;
-            absorb = false;
+            if (ss.done) break;
         }
         // Peers may still be reading this CTA's last histogram: no CTA leaves before all have.
         cluster.sync();
+        if (!ss.done) flags |= 2;  // the select ran out of passes
+        kstar = ss.kstar;
+        fthr = ss.fthr;
+        eps_final = ss.eps_final;
     }
 
     // ---- 5. F bitmap and statistics ----
@@ -567,11 +693,12 @@ __global__ void __launch_bounds__(CT_NT, 1) k_certify(CertifyArgs a) {
     }
 }
 
-cudaError_t launch_certify(const CertifyArgs &a, int qheads, size_t smem, cudaStream_t s) {
+template <int CL>
+static cudaError_t launch_certify_cl(const CertifyArgs &a, int qheads, size_t smem, cudaStream_t s) {
     static size_t configured = 0;
     if (smem > configured) {
-        cudaError_t e = cudaFuncSetAttribute(k_certify, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             (int)smem);
+        cudaError_t e = cudaFuncSetAttribute(k_certify<CL>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return e;
         configured = smem;
     }
@@ -582,12 +709,21 @@ cudaError_t launch_certify(const CertifyArgs &a, int qheads, size_t smem, cudaSt
     cfg.stream = s;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = a.cl;
+    attr[0].val.clusterDim.x = CL;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, k_certify, a);
+    return cudaLaunchKernelEx(&cfg, k_certify<CL>, a);
+}
+
+cudaError_t launch_certify(const CertifyArgs &a, int qheads, size_t smem, cudaStream_t s) {
+    switch (a.cl) {
+        case 1: return launch_certify_cl<1>(a, qheads, smem, s);
+        case 4: return launch_certify_cl<4>(a, qheads, smem, s);
+        case CT_MAX_CL: return launch_certify_cl<CT_MAX_CL>(a, qheads, smem, s);
+        default: return cudaErrorInvalidValue;
+    }
 }
 
 }  // namespace verkv
