@@ -259,8 +259,8 @@ enum {
     VERKV_K_PC_GATHER,         /* pivotal K/V row gather                          */
     VERKV_K_SKETCH,            /* exact sketch build                              */
     VERKV_K_SCORE,             /* sketch logits for every token and query head    */
-    VERKV_K_CERTIFY,           /* beta solve, certificate, selection (Eq. 7-10)   */
-    VERKV_K_FETCHLIST,         /* per-KV-head fetch id list                       */
+    VERKV_K_CERTIFY,           /* beta solve, certificate, selection (Eq. 7-10),
+                                  and the per-KV-head fetch id list               */
     VERKV_K_PARTIAL_PIVOTAL,   /* shrinkage-weighted sums over the pivotal set    */
     VERKV_K_FETCH_HOST,        /* zero-copy fetch + exact sums over fetched rows  */
     VERKV_K_PARTIAL_STAGED,    /* exact sums over rows staged by cudaMemcpyAsync  */

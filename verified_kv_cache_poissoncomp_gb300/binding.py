@@ -32,7 +32,7 @@ EXPORTED = ["verkv_workspace_size", "verkv_create", "verkv_destroy", "verkv_set_
             "verkv_fetch_refine", "verkv_selection_bitmap", "verkv_profile_enable",
             "verkv_profile_read", "verkv_launch_counts", "verkv_kernel_name", "verkv_sync",
             "verkv_last_error", "verkv_status_string", "verkv_certify_noalloc"]
-VERKV_K_COUNT = 10
+VERKV_K_COUNT = 9
 
 
 class verkv_shape(ctypes.Structure):

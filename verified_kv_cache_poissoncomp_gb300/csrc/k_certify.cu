@@ -11,7 +11,9 @@
 //   2+ beta = sum_L w (1 - lambda(beta)) by safeguarded piece-wise Newton: each pass classifies
 //      every token at the current beta -- at its floor (A += w (1 - r)), in the middle (B += w,
 //      S += r / (1 - r)) or at lambda = 1 -- and moves to the root (A + B) / (1 + S) of that
-//      linear piece, a ratio of positive sums; about five passes from the top of the bracket;
+//      linear piece, a ratio of positive sums; the pass also finds the nearest breakpoints on
+//      either side, and the solve ends as soon as the new root lies between them (three to four
+//      passes from the top of the bracket);
 //   +1 beta(L), V(L), the top two b_i (with the argmax id) of Lemma 1;
 //   +k when the certificate fails, a windowed most-significant-digit select over the 56-bit key
 //      (g bits << 24 | 2^24-1-token id) -- g descending, ties to the lower id.  Each pass builds a
@@ -19,9 +21,13 @@
 //      point scaled by beta(L) and V(L), added as two 32-bit halves (native integer atomics;
 //      exact, order-independent sums); the CTAs' histograms are merged over distributed shared
 //      memory and one warp scans the 256 bins for the bin in which eps-hat of the remaining
-//      tokens drops below eps.  The first window spans 32 octaves under the largest possible g at 8 bins per octave
-//      and folds everything below into bin 0; the select ends when the cut bin holds one token.
-// Per-token terms use lambda w = clip(beta rho, r w, w) with rho = r / (1 - r): no division.
+//      tokens drops below eps.  The first window spans 32 octaves under the largest possible g
+//      at 8 bins per octave and folds everything below into bin 0; the select ends when the cut
+//      bin holds one token;
+//   tail  the last of a KV head's G clusters to finish builds that head's fetch list (KVFetch
+//      step 5: the rows of the union of the G sets F that are not resident), so the list is
+//      ready when the kernel ends.
+// Per-token terms use lambda w = clip(beta rho, r w, w) with rho = r / (1 - r).
 #include <math.h>
 #include <stddef.h>
 
@@ -124,7 +130,15 @@ __device__ __forceinline__ float bern(float b, float V, float l) {
     return A + sqrtf(fmaf(A, A, 2.0f * V * l));
 }
 
-__device__ __forceinline__ float rho_of(float r) { return r * __frcp_rn(1.0f - r); }
+// Per-token terms use the hardware's approximate reciprocal, quotient and square root (about one
+// ulp): their errors stay far below the 1e-5 relative resolution the decisions are held to.
+__device__ __forceinline__ float sqrt_approx(float x) {
+    float y;
+    asm("sqrt.approx.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+__device__ __forceinline__ float rho_of(float r) { return __fdividef(r, 1.0f - r); }
 
 // lambda at beta and the three per-token terms of Lemma 1 for a token of L (0 < r < 1):
 // lambda w = clip(beta rho, r w, w);  beta_i = w - lambda w;  v_i = (lambda w)^2 (1 - r) / r =
@@ -132,7 +146,7 @@ __device__ __forceinline__ float rho_of(float r) { return r * __frcp_rn(1.0f - r
 __device__ __forceinline__ void token_terms(float w, float r, float rho, float beta, float &bi,
                                             float &vi, float &bb) {
     const float t = fminf(w, fmaxf(r * w, beta * rho));
-    const float inv_rho = __frcp_rn(rho);
+    const float inv_rho = __fdividef(1.0f, rho);
     bi = w - t;
     vi = t * t * inv_rho;
     bb = t * fmaxf(1.0f, inv_rho);
@@ -323,6 +337,120 @@ __device__ __forceinline__ void select_step(const Merged &mh, SelState &ss, int 
     ss.absorb = 0;
 }
 
+// The per-KV-head fetch list, built by the last of the KV head's G clusters to finish.  The
+// cluster barrier orders every CTA's F words before rank 0's acquire-release increment of the
+// KV head's counter; the cluster that completes the count (its rank-0 CTA) ORs the G bitmaps,
+// removes the resident tokens, scans the counts and writes the ascending ids, one coalesced
+// store per bitmap word and warp; it then rearms the counter for the next call.
+constexpr int FL_MAX_WPT = 4;  // bitmap words per thread: n <= 131072 = 4 * 32 * CT_NT
+
+__device__ __forceinline__ int atomic_add_acq_rel(int *p, int v) {
+    int old;
+    asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+    return old;
+}
+
+template <int CL>
+__device__ __forceinline__ void fetch_list_tail(const CertifyArgs &a, int ul, int ug) {
+    __shared__ int s_last;
+    __shared__ int s_wsum[CT_NW];
+    __shared__ int s_nf[CT_NW][8];
+    cg::cluster_group cluster = cg::this_cluster();
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int G = a.li.G, W = a.W;
+    cluster.sync();
+    if (cluster.block_rank() != 0) return;
+    if (tid == 0) {
+        const int old = atomic_add_acq_rel(&a.fl_counter[ul], 1);
+        s_last = old == G - 1;
+        if (old == G - 1) a.fl_counter[ul] = 0;
+    }
+    __syncthreads();
+    if (!s_last) return;
+    const uint32_t *res = a.resident + (size_t)ug * W;
+    const uint32_t *F0 = a.F + (size_t)ul * G * W;
+    const int wpt = (W + CT_NT - 1) / CT_NT;  // <= FL_MAX_WPT
+    const int w0 = tid * wpt;
+    uint32_t fw[FL_MAX_WPT];
+    int cnt[FL_MAX_WPT];
+    int my = 0;
+    int nf[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+#pragma unroll
+    for (int i = 0; i < FL_MAX_WPT; ++i) {
+        const int w = w0 + i;
+        uint32_t f = 0u;
+        if (i < wpt && w < W) {
+            const uint32_t rw = __ldcg(res + w);
+#pragma unroll
+            for (int g = 0; g < 8; ++g) {
+                if (g < G) {
+                    const uint32_t fg = __ldcg(F0 + (size_t)g * W + w) & ~rw;
+                    f |= fg;
+                    nf[g] += __popc(fg);
+                }
+            }
+        }
+        fw[i] = f;
+        cnt[i] = __popc(f);
+        my += cnt[i];
+    }
+    int incl = my;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+        if (lane >= o) incl += y;
+    }
+    if (lane == 31) s_wsum[warp] = incl;
+    for (int g = 0; g < G; ++g) {
+        const int t = warp_sum(nf[g]);
+        if (lane == 0) s_nf[warp][g] = t;
+    }
+    __syncthreads();
+    if (warp == 0) {
+        const int v = lane < CT_NW ? s_wsum[lane] : 0;
+        int x = v;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int y = __shfl_up_sync(0xFFFFFFFFu, x, o);
+            if (lane >= o) x += y;
+        }
+        if (lane < CT_NW) s_wsum[lane] = x - v;  // exclusive
+        if (lane == 31) {
+            a.counts[ul] = x;
+            if (a.counts_user) a.counts_user[ul] = x;
+            if (a.counts_host) a.counts_host[ul] = x;
+        }
+        if (lane < G) {
+            int t = 0;
+            for (int w = 0; w < CT_NW; ++w) t += s_nf[w][lane];
+            a.qstats[ul * G + lane].n_fetch = t;
+        }
+    }
+    __syncthreads();
+    // Lane j's words, in order, are written by the whole warp: lane l stores the id of bit l.
+    int pos = s_wsum[warp] + incl - my;
+    int32_t *ids = a.ids + (size_t)ul * a.n;
+    int32_t *idsu = a.ids_user ? a.ids_user + (size_t)ul * a.n : nullptr;
+    int32_t *idsh = a.ids_host ? a.ids_host + (size_t)ul * a.n : nullptr;
+    const uint32_t below = (1u << lane) - 1u;
+    for (int j = 0; j < 32; ++j) {
+        int base = __shfl_sync(0xFFFFFFFFu, pos, j);
+        const int wj = __shfl_sync(0xFFFFFFFFu, w0, j);
+#pragma unroll
+        for (int i = 0; i < FL_MAX_WPT; ++i) {
+            const uint32_t f = __shfl_sync(0xFFFFFFFFu, fw[i], j);
+            if ((f >> lane) & 1u) {
+                const int p = base + __popc(f & below);
+                const int id = 32 * (wj + i) + lane;
+                ids[p] = id;
+                if (idsu) idsu[p] = id;
+                if (idsh) idsh[p] = id;
+            }
+            base += __popc(f);
+        }
+    }
+}
+
 template <int CL>
 __global__ void __launch_bounds__(CT_NT, 1) k_certify(CertifyArgs a) {
     extern __shared__ __align__(16) unsigned char smem_raw[];
@@ -351,8 +479,8 @@ __global__ void __launch_bounds__(CT_NT, 1) k_certify(CertifyArgs a) {
 
     // ---- 1. logits, r; max logit, D, sum_L w (1 - r), |L| in one exchange ----
     float m, D, C, nL;
+    float tmax = NEG_INF;
     {
-        float tmax = NEG_INF;
         for (int i = tid; i < chunk; i += CT_NT) {
             const int t = base + i;
             float s = NEG_INF, r = 1.0f;
@@ -367,6 +495,7 @@ __global__ void __launch_bounds__(CT_NT, 1) k_certify(CertifyArgs a) {
         float d = 0.f, c = 0.f, cnt = 0.f;
         for (int i = tid; i < chunk; i += CT_NT) {
             const float e = tmax == NEG_INF ? 0.0f : expf(W[i] - tmax);  // 0 for padding
+            W[i] = e;  // exp(logit - this thread's max); rescaled to w-hat once m is known
             d += e;
             const float r = R[i];
             if (r < 1.0f) {
@@ -397,6 +526,7 @@ __global__ void __launch_bounds__(CT_NT, 1) k_certify(CertifyArgs a) {
     float beta = 0.0f;
     int iters = 0, flags = 0;
     bool first = true;
+    const float wscale = tmax == NEG_INF ? 0.0f : expf(tmax - m);  // w-hat = W * wscale
     if (C > 0.0f) {
         float lo = 0.0f, hi = C;  // h(0) <= 0 <= h(C)
         beta = C;
@@ -410,7 +540,7 @@ __global__ void __launch_bounds__(CT_NT, 1) k_certify(CertifyArgs a) {
                 const float r = R[i];
                 float w;
                 if (first) {
-                    w = expf(W[i] - m);
+                    w = W[i] * wscale;
                     W[i] = w;
                     if (r < 1.0f) X[i] = __float_as_uint(rho_of(r));
                 } else {
@@ -467,7 +597,7 @@ __global__ void __launch_bounds__(CT_NT, 1) k_certify(CertifyArgs a) {
     }
     if (first) {  // no Newton pass ran: convert the logits now
         for (int i = tid; i < chunk; i += CT_NT) {
-            W[i] = expf(W[i] - m);
+            W[i] *= wscale;
             if (R[i] < 1.0f) X[i] = __float_as_uint(rho_of(R[i]));
         }
         __syncthreads();
@@ -558,14 +688,14 @@ __global__ void __launch_bounds__(CT_NT, 1) k_certify(CertifyArgs a) {
                         const float Vr = fmaxf(VL - vi, 0.0f);
                         float gD;
                         if (base + i != id1 || b2 == b1) {
-                            const float den = Rr + sqrtf(fmaf(A, A, 2.0f * Vr * l));
-                            gD = bi + (den > 0.0f ? __fdiv_rn(2.0f * vi * l, den) : 0.0f);
+                            const float den = Rr + sqrt_approx(fmaf(A, A, 2.0f * Vr * l));
+                            gD = bi + (den > 0.0f ? __fdividef(2.0f * vi * l, den) : 0.0f);
                         } else {
                             const float A2 = b2 * l * (1.0f / 3.0f);
-                            const float R2 = sqrtf(fmaf(A2, A2, 2.0f * Vr * l));
+                            const float R2 = sqrt_approx(fmaf(A2, A2, 2.0f * Vr * l));
                             const float den = Rr + R2;
                             gD = bi + (A - A2) +
-                                 (den > 0.0f ? __fdiv_rn(fmaf(A - A2, A + A2, 2.0f * vi * l), den) : 0.0f);
+                                 (den > 0.0f ? __fdividef(fmaf(A - A2, A + A2, 2.0f * vi * l), den) : 0.0f);
                         }
                         const uint32_t g = __float_as_uint(fmaxf(gD, 0.0f));
                         X[i] = g;
@@ -691,6 +821,7 @@ __global__ void __launch_bounds__(CT_NT, 1) k_certify(CertifyArgs a) {
         a.qstats[qh] = st;
         if (flags) raise_error(a.err, ERR_NOCONVERGE);
     }
+    if (a.fl_counter) fetch_list_tail<CL>(a, ul, ug);
 }
 
 template <int CL>

@@ -1,12 +1,9 @@
-// k_score.cu -- KVFetch step 1 and the fetch list ("Verify Before You Fetch", summary page,
-// KVFETCH: Verification and Adaptive Fetching, steps 1 and 5).
+// k_score.cu -- KVFetch step 1 ("Verify Before You Fetch", summary page, KVFETCH: Verification
+// and Adaptive Fetching, step 1).
 //
-// k_score     streams the bf16 sketch once per KV head through a TMA bulk-copy ring in shared
-//             memory and scores it against all G query heads of the group (q slices held in
-//             registers; a recursive-halving shuffle reduce leaves each head's logit in a quarter
-//             of the row's lanes).
-// k_fetchlist ORs the G bitmaps of a KV head, removes resident tokens and writes the ascending
-//             id list of rows to fetch.
+// k_score streams the bf16 sketch once per KV head through a TMA bulk-copy ring in shared memory
+// and scores it against all G query heads of the group (q slices held in registers; a
+// recursive-halving shuffle reduce leaves each head's logit in a quarter of the row's lanes).
 #include <math.h>
 
 #include "verkv_common.cuh"
@@ -217,92 +214,6 @@ cudaError_t launch_score(const ScoreArgs &a, int units_layer, cudaStream_t s) {
     VERKV_SCORE(64, 1) VERKV_SCORE(64, 2) VERKV_SCORE(64, 4) VERKV_SCORE(64, 8)
 #undef VERKV_SCORE
     return cudaErrorInvalidValue;
-}
-
-// ---------------------------------------------------------------------------------------------
-constexpr int FL_NT = 1024;
-
-__global__ void __launch_bounds__(FL_NT) k_fetchlist(FetchListArgs a) {
-    __shared__ int wsum[FL_NT / 32];
-    __shared__ int nfw[FL_NT / 32][8];
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int ul = blockIdx.x;
-    const int ug = a.li.unit_global(ul);
-    const int G = a.li.G;
-    const int W = a.W;
-    const uint32_t *res = a.resident + (size_t)ug * W;
-    const uint32_t *F0 = a.F + (size_t)ul * G * W;
-    const int wpt = (W + FL_NT - 1) / FL_NT;
-    const int w0 = tid * wpt, w1 = min(W, w0 + wpt);
-    int my = 0;
-    int nf[8] = {0, 0, 0, 0, 0, 0, 0, 0};
-    for (int w = w0; w < w1; ++w) {
-        const uint32_t rw = res[w];
-        uint32_t f = 0u;
-        for (int g = 0; g < G; ++g) {
-            const uint32_t fg = F0[(size_t)g * W + w];
-            f |= fg;
-            nf[g] += __popc(fg & ~rw);
-        }
-        my += __popc(f & ~rw);
-    }
-    // block exclusive scan of my
-    int incl = my;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-        const int y = __shfl_up_sync(0xFFFFFFFFu, incl, o);
-        if (lane >= o) incl += y;
-    }
-    if (lane == 31) wsum[warp] = incl;
-    for (int g = 0; g < G; ++g) {
-        const int s = warp_sum(nf[g]);
-        if (lane == 0) nfw[warp][g] = s;
-    }
-    __syncthreads();
-    if (warp == 0) {
-        int v = wsum[lane];
-        int x = v;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            const int y = __shfl_up_sync(0xFFFFFFFFu, x, o);
-            if (lane >= o) x += y;
-        }
-        wsum[lane] = x - v;  // exclusive
-        if (lane == 31) {
-            a.counts[ul] = x;
-            if (a.counts_user) a.counts_user[ul] = x;
-            if (a.counts_host) a.counts_host[ul] = x;
-        }
-        if (lane < G) {
-            int t = 0;
-            for (int w = 0; w < FL_NT / 32; ++w) t += nfw[w][lane];
-            a.qstats[ul * G + lane].n_fetch = t;
-        }
-    }
-    __syncthreads();
-    int pos = wsum[warp] + incl - my;
-    int32_t *ids = a.ids + (size_t)ul * a.n;
-    int32_t *idsu = a.ids_user ? a.ids_user + (size_t)ul * a.n : nullptr;
-    int32_t *idsh = a.ids_host ? a.ids_host + (size_t)ul * a.n : nullptr;
-    for (int w = w0; w < w1; ++w) {
-        uint32_t f = 0u;
-        for (int g = 0; g < G; ++g) f |= F0[(size_t)g * W + w];
-        f &= ~res[w];
-        while (f) {
-            const int bit = __ffs(f) - 1;
-            f &= f - 1;
-            const int id = 32 * w + bit;
-            ids[pos] = id;
-            if (idsu) idsu[pos] = id;
-            if (idsh) idsh[pos] = id;
-            ++pos;
-        }
-    }
-}
-
-cudaError_t launch_fetchlist(const FetchListArgs &a, int units_layer, cudaStream_t s) {
-    k_fetchlist<<<units_layer, FL_NT, 0, s>>>(a);
-    return cudaGetLastError();
 }
 
 }  // namespace verkv

@@ -24,7 +24,7 @@ namespace {
 size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 
 struct Layout {
-    size_t err, scores, qstats, F, fids, fcounts, staging, part_piv, part_fet, total;
+    size_t err, flc, scores, qstats, F, fids, fcounts, staging, part_piv, part_fet, total;
     int W, units_layer, qh_layer, max_piv, max_fet;
 };
 
@@ -52,6 +52,7 @@ bool make_layout(const verkv_shape *s, Layout &L) {
         return o;
     };
     L.err = take(256);
+    L.flc = take((size_t)L.units_layer * 4);
     L.scores = take((size_t)L.qh_layer * n * 4);
     L.qstats = take((size_t)L.qh_layer * sizeof(verkv_head_stats));
     L.F = take((size_t)L.qh_layer * L.W * 4);
@@ -133,6 +134,7 @@ struct verkv_ctx {
     verkv_head_stats *qstats = nullptr;
     uint32_t *F = nullptr;
     int32_t *fids = nullptr, *fcounts = nullptr;
+    int32_t *flc = nullptr;  // per-KV-head completion counters of the certify kernel's fetch list
     uint16_t *staging = nullptr;
     float *part_piv = nullptr, *part_fet = nullptr;
     int fetch_mode = VERKV_FETCH_ZEROCOPY;
@@ -267,11 +269,13 @@ verkv_status verkv_create(verkv_ctx **out, int device, void *stream, const verkv
     ctx->F = (uint32_t *)(w + L.F);
     ctx->fids = (int32_t *)(w + L.fids);
     ctx->fcounts = (int32_t *)(w + L.fcounts);
+    ctx->flc = (int32_t *)(w + L.flc);
     ctx->staging = (uint16_t *)(w + L.staging);
     ctx->part_piv = (float *)(w + L.part_piv);
     ctx->part_fet = (float *)(w + L.part_fet);
     e = cudaMemsetAsync(ctx->err, 0, 256, ctx->main);
     if (e == cudaSuccess) e = cudaMemsetAsync(ctx->fcounts, 0, (size_t)L.units_layer * 4, ctx->main);
+    if (e == cudaSuccess) e = cudaMemsetAsync(ctx->flc, 0, (size_t)L.units_layer * 4, ctx->main);
     if (e != cudaSuccess) {
         verkv_destroy(ctx);
         return VERKV_ECUDA;
@@ -432,26 +436,18 @@ verkv_status verkv_attend_verified(verkv_ctx *ctx, int32_t layer, const void *q,
     ca.eps = eps;
     ca.ldelta = (float)log(2.0 / (double)delta);
     ca.li = li;
+    ca.fl_counter = ctx->flc;
+    ca.ids = ctx->fids;
+    ca.counts = ctx->fcounts;
+    ca.ids_user = fetch_ids_out;
+    ca.counts_user = fetch_counts_out;
+    if (ctx->fetch_mode == VERKV_FETCH_MEMCPY) {
+        ca.ids_host = ctx->host_ids_dev;
+        ca.counts_host = ctx->host_counts_dev;
+    }
     VERKV_CUDA(tracked(ctx, VERKV_K_CERTIFY, ctx->main, [&] {
                    return launch_certify(ca, ctx->L.qh_layer, certify_smem_bytes(ca.chunk), ctx->main);
                }), "k_certify");
-
-    FetchListArgs fa{};
-    fa.F = ctx->F;
-    fa.resident = pivotal->resident;
-    fa.ids = ctx->fids;
-    fa.counts = ctx->fcounts;
-    fa.ids_user = fetch_ids_out;
-    fa.counts_user = fetch_counts_out;
-    if (ctx->fetch_mode == VERKV_FETCH_MEMCPY) {
-        fa.ids_host = ctx->host_ids_dev;
-        fa.counts_host = ctx->host_counts_dev;
-    }
-    fa.qstats = ctx->qstats;
-    fa.n = n;
-    fa.W = ctx->L.W;
-    fa.li = li;
-    VERKV_CUDA(tracked(ctx, VERKV_K_FETCHLIST, ctx->main, [&] { return launch_fetchlist(fa, ctx->L.units_layer, ctx->main); }), "k_fetchlist");
     VERKV_CUDA(cudaEventRecord(ctx->e_sel, ctx->main), "cudaEventRecord");
 
     PartialArgs pa{};
@@ -657,7 +653,7 @@ verkv_status verkv_launch_counts(verkv_ctx *ctx, int64_t *out) {
 
 const char *verkv_kernel_name(int k) {
     static const char *names[VERKV_K_COUNT] = {
-        "k_pc_solve", "k_pc_gather", "k_sketch_exact", "k_score", "k_certify", "k_fetchlist",
+        "k_pc_solve", "k_pc_gather", "k_sketch_exact", "k_score", "k_certify",
         "k_partial(pivotal)", "k_partial(host)", "k_partial(staged)", "k_merge"};
     return (k >= 0 && k < VERKV_K_COUNT) ? names[k] : "";
 }

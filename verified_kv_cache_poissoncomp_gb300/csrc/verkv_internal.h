@@ -68,7 +68,9 @@ struct ScoreArgs {
 };
 cudaError_t launch_score(const ScoreArgs &a, int units_layer, cudaStream_t s);
 
-// Certificate and selection per query head (one cluster per query head).
+// Certificate and selection per query head (one cluster per query head).  When fl_counter is
+// set, the last of the G clusters of a KV head to finish also builds that head's fetch list:
+// the ascending ids of (OR_g F_g) & ~resident, and n_fetch of its G query heads.
 struct CertifyArgs {
     const float *scores;          // [qh][n]
     const float *r_full;          // [units][n]
@@ -76,6 +78,13 @@ struct CertifyArgs {
     uint32_t *F;                  // [qh][W]
     verkv_head_stats *qstats;     // [qh]
     uint32_t *err;
+    int32_t *fl_counter;          // [units_layer], zero between calls; null: no fetch list
+    int32_t *ids;                 // [units_layer][n]  (device, used by the fetch)
+    int32_t *counts;              // [units_layer]
+    int32_t *ids_user;            // optional copy (device or mapped host)
+    int32_t *counts_user;
+    int32_t *ids_host;            // optional copy into mapped host memory (MEMCPY mode)
+    int32_t *counts_host;
     int n, W, cl, chunk;
     float eps, ldelta;
     LayerIdx li;
@@ -85,21 +94,6 @@ int certify_cluster_size(int n);
 int certify_chunk(int n, int cl);
 size_t certify_smem_bytes(int chunk);
 
-// Fetch list per KV head: ascending ids of (OR_g F_g) & ~resident.
-struct FetchListArgs {
-    const uint32_t *F;
-    const uint32_t *resident;
-    int32_t *ids;       // [units_layer][n]  (device, used by the fetch)
-    int32_t *counts;    // [units_layer]
-    int32_t *ids_user;  // optional copy (device or mapped host)
-    int32_t *counts_user;
-    int32_t *ids_host;  // optional copy into mapped host memory (MEMCPY mode)
-    int32_t *counts_host;
-    verkv_head_stats *qstats;
-    int n, W;
-    LayerIdx li;
-};
-cudaError_t launch_fetchlist(const FetchListArgs &a, int units_layer, cudaStream_t s);
 
 // ---------------------------------------------------------------------------------------------
 // Shrinkage-weighted partial sums over a row set: the pivotal rows in HBM, fetched rows staged in
