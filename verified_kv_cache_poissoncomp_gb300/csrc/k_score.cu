@@ -43,7 +43,7 @@ __device__ __forceinline__ float reduce_heads(float (&p)[G], int lane, int &head
 }
 
 // TMA bulk-copy pipeline.  Each CTA streams a contiguous span of sketch rows of one KV head (the
-// span is sized so the grid is about three CTAs per SM) through a ring of SC_STAGES shared-memory stages of SC_ROWS rows: thread 0 issues one
+// span is sized so the grid is SC_CTAS_PER_SM CTAs per SM) through a ring of SC_STAGES shared-memory stages of SC_ROWS rows: thread 0 issues one
 // cp.async.bulk per stage that completes on the stage's mbarrier; every warp waits on the barrier,
 // scores its rows from shared memory (16 lanes per 256-byte row: conflict-free 16-byte loads), and
 // after a block barrier the freed stage is refilled.  Waits are bounded by %globaltimer: on expiry
@@ -51,6 +51,7 @@ __device__ __forceinline__ float reduce_heads(float (&p)[G], int lane, int &head
 constexpr int SC_NT = 256;
 constexpr int SC_STAGES = 4;
 constexpr int SC_ROWS = 64;
+constexpr int SC_CTAS_PER_SM = 2;  // resident CTAs per SM the grid is sized for (registers allow two)
 constexpr unsigned long long SC_WAIT_NS = 1000000000ull;  // 1 s
 
 __device__ __forceinline__ unsigned long long globaltimer_ns() {
@@ -93,9 +94,36 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity
     return true;
 }
 
+// Packed pair arithmetic: two f32 lanes in one 64-bit register (fma.rn.f32x2).
+__device__ __forceinline__ unsigned long long pack2(float lo, float hi) {
+    unsigned long long r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+    return r;
+}
+__device__ __forceinline__ float sum2(unsigned long long v) {
+    float lo, hi;
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+    return lo + hi;
+}
+__device__ __forceinline__ unsigned long long ffma2(unsigned long long a, unsigned long long b,
+                                                    unsigned long long c) {
+    unsigned long long d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+    return d;
+}
+// The two bf16 of a 32-bit word as an f32 pair (element 0 in the low half).
+__device__ __forceinline__ unsigned long long bf16x2_to_f32x2(uint32_t w) {
+    return pack2(__uint_as_float(w << 16), __uint_as_float(w & 0xFFFF0000u));
+}
+
+// A row of the sketch is scored by LPR lanes, each holding CPL channels: 16 (two 16-byte vectors,
+// at vector indices cgp and cgp + LPR so the lanes of a row read consecutive 16-byte words) when
+// G <= 4, else 8.  Products accumulate as channel pairs with fma.rn.f32x2, one accumulator pair
+// per head.
 template <int D, int G>
-__global__ void __launch_bounds__(SC_NT) k_score(ScoreArgs a, int spans_per_unit, int span_rows) {
-    constexpr int LPR = D / 8, RPW = 32 / LPR, NW = SC_NT / 32;
+__global__ void __launch_bounds__(SC_NT, SC_CTAS_PER_SM) k_score(ScoreArgs a, int spans_per_unit, int span_rows) {
+    constexpr int CPL = G <= 4 ? 16 : 8, NV = CPL / 8;
+    constexpr int LPR = D / CPL, RPW = 32 / LPR, NW = SC_NT / 32;
     constexpr int ROWB = D * 2;                       // bytes per sketch row
     constexpr int WROWS = SC_ROWS / NW;               // rows per warp per stage
     constexpr int SUBMASK = LPR / G - 1;
@@ -117,11 +145,18 @@ __global__ void __launch_bounds__(SC_NT) k_score(ScoreArgs a, int spans_per_unit
     const unsigned char *src = reinterpret_cast<const unsigned char *>(a.sketch) +
                                ((size_t)ug * a.n + row0) * ROWB;
 
-    float qv[G][8];
+    unsigned long long qp[G][CPL / 2];
 #pragma unroll
     for (int g = 0; g < G; ++g) {
-        const uint4 v = *reinterpret_cast<const uint4 *>(a.q + ((size_t)b * hq + h * G + g) * D + cgp * 8);
-        unpack8(v, qv[g]);
+#pragma unroll
+        for (int v = 0; v < NV; ++v) {
+            const uint4 x = *reinterpret_cast<const uint4 *>(a.q + ((size_t)b * hq + h * G + g) * D +
+                                                             (cgp + LPR * v) * 8);
+            qp[g][4 * v + 0] = bf16x2_to_f32x2(x.x);
+            qp[g][4 * v + 1] = bf16x2_to_f32x2(x.y);
+            qp[g][4 * v + 2] = bf16x2_to_f32x2(x.z);
+            qp[g][4 * v + 3] = bf16x2_to_f32x2(x.w);
+        }
     }
     if (tid == 0) {
         for (int k = 0; k < SC_STAGES; ++k) mbar_init(&full[k], 1);
@@ -153,18 +188,25 @@ __global__ void __launch_bounds__(SC_NT) k_score(ScoreArgs a, int spans_per_unit
 #pragma unroll
         for (int j = 0; j < WROWS / RPW; ++j) {
             const int r = warp * WROWS + j * RPW + rg;  // row within the stage
-            uint4 kv = make_uint4(0, 0, 0, 0);
-            if (r < rows_k) kv = *reinterpret_cast<const uint4 *>(stage + (size_t)r * ROWB + cgp * 16);
-            float kf[8];
-            unpack8(kv, kf);
+            unsigned long long acc[G];
+#pragma unroll
+            for (int g = 0; g < G; ++g) acc[g] = 0ull;
+#pragma unroll
+            for (int v = 0; v < NV; ++v) {
+                uint4 kv = make_uint4(0, 0, 0, 0);
+                if (r < rows_k)
+                    kv = *reinterpret_cast<const uint4 *>(stage + (size_t)r * ROWB + (cgp + LPR * v) * 16);
+                const uint32_t kw[4] = {kv.x, kv.y, kv.z, kv.w};
+#pragma unroll
+                for (int t = 0; t < 4; ++t) {
+                    const unsigned long long kp = bf16x2_to_f32x2(kw[t]);
+#pragma unroll
+                    for (int g = 0; g < G; ++g) acc[g] = ffma2(qp[g][4 * v + t], kp, acc[g]);
+                }
+            }
             float p[G];
 #pragma unroll
-            for (int g = 0; g < G; ++g) {
-                float acc = 0.0f;
-#pragma unroll
-                for (int c = 0; c < 8; ++c) acc = fmaf(qv[g][c], kf[c], acc);
-                p[g] = acc;
-            }
+            for (int g = 0; g < G; ++g) p[g] = sum2(acc[g]);
             int head;
             const float sc = reduce_heads<G, LPR>(p, lane, head);
             if ((cgp & SUBMASK) == 0 && r < rows_k)
@@ -190,7 +232,7 @@ cudaError_t launch_score(const ScoreArgs &a, int units_layer, cudaStream_t s) {
     cudaGetDevice(&dev);
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     const long long total = (long long)units_layer * a.n;
-    long long span_rows = (total + 3LL * sms - 1) / (3LL * sms);
+    long long span_rows = (total + (long long)SC_CTAS_PER_SM * sms - 1) / ((long long)SC_CTAS_PER_SM * sms);
     span_rows = (span_rows + SC_ROWS - 1) / SC_ROWS * SC_ROWS;
     if (span_rows < SC_ROWS) span_rows = SC_ROWS;
     const int spans = (int)((a.n + span_rows - 1) / span_rows);
