@@ -48,6 +48,8 @@ def parse_args():
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--queries", type=int, default=QUERIES)
+    p.add_argument("--eps-sweep", action="store_true",
+                   help="tolerance sweep: throughput and host-traffic statistics per eps")
     return p.parse_args()
 
 
@@ -475,11 +477,115 @@ def run_ours(args, world, rank, local):
         dist.destroy_process_group()
 
 
+EPS_SWEEP = [0.01, 0.02, 0.05, 0.1, 0.2, 0.3, 0.5]
+
+
+def traffic_stats(st, fetched_rows, pivotal_count, n):
+    """Host-traffic statistics of one pass over the queries, in the terms of the pages' traffic
+    table: a decision is one query head's certificate; it fetches when eps-hat(L) >= eps and then
+    moves |F \\ S| rows (the transfer itself is per KV head: the union over its query heads).
+      st            int32 [Q][query heads][16]  verkv_head_stats
+      fetched_rows  int   [Q][KV heads]         rows moved per KV head
+      pivotal_count int   [units]               |H u S| per unit"""
+    certified = st[..., 10].astype(bool)
+    nfetch = st[..., 13].astype(np.float64)
+    fetching = ~certified
+    resident = float(pivotal_count.mean()) / n
+    return {
+        "decisions_fetching_frac": float(fetching.mean()),
+        "context_frac_per_fetching_decision":
+            float((nfetch[fetching] / n).mean()) if fetching.any() else 0.0,
+        "overall_read_frac": resident + float((nfetch / n).mean()),
+        "resident_frac": resident,
+        "kv_head_transfer_frac": float(fetched_rows.mean()) / n,
+    }
+
+
+def run_eps_sweep(args, local):
+    """One GPU: the bench workload at each tolerance of EPS_SWEEP, graph-replayed like the main
+    bench (a step = PoissonComp of the 4 instances + the decode queries)."""
+    import torch
+
+    from verified_kv_cache_poissoncomp_gb300 import binding as B
+    from verified_kv_cache_poissoncomp_gb300 import inputs as I
+    from verified_kv_cache_poissoncomp_gb300.engine import VerKV, default_cap
+
+    B.lib()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    w = I.single_layer_32k(layers=LAYERS, n_queries=args.queries)
+    Q = w.queries.shape[0]
+    stream = torch.cuda.Stream(dev)
+    with torch.cuda.stream(stream):
+        eng = VerKV(w.B, w.L, w.h_kv, w.G, w.d, w.n, default_cap(w.n, w.eta))
+        eng.load(w.tau.reshape(-1, w.n), w.kv.reshape(-1, w.n, 2, w.d))
+        eng.compress(w.eta, w.n_sink, w.n_local, w.seed)
+        eng.sync()
+        q_dev = torch.as_tensor(w.queries.view(np.int16)).to(dev)
+        hq = w.B * w.h_kv * w.G
+        o_all = torch.empty((Q, hq, w.d), dtype=torch.float32, device=dev)
+        lse_all = torch.empty((Q, hq), dtype=torch.float32, device=dev)
+        st_all = torch.empty((Q, hq, 16), dtype=torch.int32, device=dev)
+        fc_all = torch.zeros((Q, w.B * w.h_kv), dtype=torch.int32, device=dev)
+
+    def step(eps):
+        B.verkv_poissoncomp(eng.ctx, eng.tau.data_ptr(), w.eta, B.verkv_hset(w.n_sink, w.n_local),
+                            w.seed, eng.kv.data_ptr(), eng.r_full.data_ptr(), eng.pivotal)
+        for t in range(Q):
+            B.verkv_attend_verified(eng.ctx, int(w.query_layer[t]), q_dev[t].data_ptr(),
+                                    eng.pivotal, eng.r_full.data_ptr(), eng.sketch_desc, eps,
+                                    w.delta, None, fc_all[t].data_ptr())
+            B.verkv_fetch_refine(eng.ctx, None, None, eng.host_kv.data_ptr(),
+                                 o_all[t].data_ptr(), lse_all[t].data_ptr(), st_all[t].data_ptr())
+
+    rows = []
+    counts = None
+    for eps in EPS_SWEEP:
+        with torch.cuda.stream(stream):
+            step(eps)  # eager once: first-use set-up outside the capture
+            B.verkv_sync(eng.ctx)
+            graph = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(graph, stream=stream):
+                step(eps)
+            for _ in range(args.warmup):
+                graph.replay()
+        torch.cuda.synchronize()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        with torch.cuda.stream(stream):
+            for _ in range(args.steps):
+                graph.replay()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        B.verkv_sync(eng.ctx)
+        ms = e0.elapsed_time(e1) / args.steps
+        if counts is None:
+            counts = eng.p_count.cpu().numpy().astype(np.int64)
+        fr = fc_all.cpu().numpy().astype(np.int64)
+        row = {"eps": eps, "queries_per_s": round(Q / (ms * 1e-3), 2), "ms_per_step": round(ms, 4),
+               "h2d_bytes_per_query": int(fr.sum(1).mean() * 2 * w.d)}
+        row.update({k: round(v, 5) for k, v in
+                    traffic_stats(st_all.cpu().numpy(), fr, counts, w.n).items()})
+        rows.append(row)
+        del graph
+    print(json.dumps({"sweep": "eps", "metric": METRIC, "unit": UNIT, "delta": w.delta,
+                      "steps": args.steps, "warmup": args.warmup, "data": "synthetic",
+                      "config": {"workload": "single-layer 32K (the bench workload), "
+                                             f"{Q} decode queries per step", "fetch": "zerocopy",
+                                 "graph": True},
+                      "rows": rows}), flush=True)
+    eng.close()
+
+
 def main():
     args = parse_args()
     world, rank, local = dist_setup()
     if args.impl == "reference":
         run_reference(args, world, rank)
+    elif args.eps_sweep:
+        if rank == 0:
+            run_eps_sweep(args, local)
     else:
         run_ours(args, world, rank, local)
 
