@@ -50,6 +50,8 @@ def parse_args():
     p.add_argument("--queries", type=int, default=QUERIES)
     p.add_argument("--eps-sweep", action="store_true",
                    help="tolerance sweep: throughput and host-traffic statistics per eps")
+    p.add_argument("--dense-offload", action="store_true",
+                   help="the offloaded-dense baseline alone (every row from the host cache)")
     return p.parse_args()
 
 
@@ -501,6 +503,47 @@ def traffic_stats(st, fetched_rows, pivotal_count, n):
     }
 
 
+def time_dense_offload(eng, w, q_dev, stream, steps, warmup):
+    """Queries/s of the offloaded-dense baseline on the engine's workload: each query reads every
+    K|V row of its layer from the page-locked host cache (graph replay of the query loop)."""
+    import torch
+
+    from verified_kv_cache_poissoncomp_gb300 import binding as B
+
+    Q = w.queries.shape[0]
+    hq = w.B * w.h_kv * w.G
+    o = torch.empty((Q, hq, w.d), dtype=torch.float32, device=q_dev.device)
+    lse = torch.empty((Q, hq), dtype=torch.float32, device=q_dev.device)
+
+    def step():
+        for t in range(Q):
+            B.verkv_attend_dense_host(eng.ctx, int(w.query_layer[t]), q_dev[t].data_ptr(),
+                                      eng.host_kv.data_ptr(), o[t].data_ptr(), lse[t].data_ptr())
+
+    with torch.cuda.stream(stream):
+        step()
+        B.verkv_sync(eng.ctx)
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=stream):
+            step()
+        for _ in range(warmup):
+            graph.replay()
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    with torch.cuda.stream(stream):
+        for _ in range(steps):
+            graph.replay()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    B.verkv_sync(eng.ctx)
+    ms = e0.elapsed_time(e1) / steps
+    h2d = w.B * w.h_kv * w.n * 4 * w.d  # every K|V row of the layer, per query
+    return {"queries_per_s": round(Q / (ms * 1e-3), 2), "ms_per_step": round(ms, 4),
+            "h2d_bytes_per_query": int(h2d), "h2d_GBs": round(h2d * Q / (ms * 1e-3) / 1e9, 1)}
+
+
 def run_eps_sweep(args, local):
     """One GPU: the bench workload at each tolerance of EPS_SWEEP, graph-replayed like the main
     bench (a step = PoissonComp of the 4 instances + the decode queries)."""
@@ -569,12 +612,47 @@ def run_eps_sweep(args, local):
                     traffic_stats(st_all.cpu().numpy(), fr, counts, w.n).items()})
         rows.append(row)
         del graph
+    dense = time_dense_offload(eng, w, q_dev, stream, args.steps, args.warmup)
+    for row in rows:
+        row["speedup_vs_dense_offload"] = round(row["queries_per_s"] / dense["queries_per_s"], 3)
+        row["host_bytes_reduction_vs_dense_offload"] = round(
+            dense["h2d_bytes_per_query"] / max(row["h2d_bytes_per_query"], 1), 1)
     print(json.dumps({"sweep": "eps", "metric": METRIC, "unit": UNIT, "delta": w.delta,
+                      "dense_offload": dense,
                       "steps": args.steps, "warmup": args.warmup, "data": "synthetic",
                       "config": {"workload": "single-layer 32K (the bench workload), "
                                              f"{Q} decode queries per step", "fetch": "zerocopy",
                                  "graph": True},
                       "rows": rows}), flush=True)
+    eng.close()
+
+
+def run_dense_offload(args, local):
+    """One GPU: the offloaded-dense baseline on the bench workload, one JSON line."""
+    import torch
+
+    from verified_kv_cache_poissoncomp_gb300 import binding as B
+    from verified_kv_cache_poissoncomp_gb300 import inputs as I
+    from verified_kv_cache_poissoncomp_gb300.engine import VerKV, default_cap
+
+    B.lib()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    w = I.single_layer_32k(layers=LAYERS, n_queries=args.queries)
+    stream = torch.cuda.Stream(dev)
+    with torch.cuda.stream(stream):
+        eng = VerKV(w.B, w.L, w.h_kv, w.G, w.d, w.n, default_cap(w.n, w.eta))
+        eng.load(w.tau.reshape(-1, w.n), w.kv.reshape(-1, w.n, 2, w.d))
+        q_dev = torch.as_tensor(w.queries.view(np.int16)).to(dev)
+    r = time_dense_offload(eng, w, q_dev, stream, args.steps, args.warmup)
+    print(json.dumps({"baseline": "dense-offload", "metric": METRIC, "unit": UNIT,
+                      "value": r["queries_per_s"], "steps": args.steps, "warmup": args.warmup,
+                      "data": "synthetic", "dtype": "bf16",
+                      "config": {"workload": "single-layer 32K (the bench workload), "
+                                             f"{w.queries.shape[0]} decode queries per step; "
+                                             "exact attention, every K|V row read from the "
+                                             "page-locked host cache", "graph": True},
+                      **r}), flush=True)
     eng.close()
 
 
@@ -586,6 +664,9 @@ def main():
     elif args.eps_sweep:
         if rank == 0:
             run_eps_sweep(args, local)
+    elif args.dense_offload:
+        if rank == 0:
+            run_dense_offload(args, local)
     else:
         run_ours(args, world, rank, local)
 

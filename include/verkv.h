@@ -205,6 +205,17 @@ verkv_status verkv_fetch_refine(verkv_ctx *ctx, const int32_t *ids, const int32_
                                 const void *host_kv, float *o_out, float *lse_out,
                                 verkv_head_stats *stats_out);
 
+/* The offloaded-dense baseline (summary page, System Performance: the "Dense (offload)" system
+ * VerKV is compared with): exact attention for every query head of `layer` over all n tokens,
+ * every K|V row read from the page-locked host cache -- nothing of the cache is resident.
+ *   q        device bf16 [batch][kv_heads * q_per_kv][d]
+ *   host_kv  page-locked host bf16 [units][n][2][d]
+ *   o_out    device float [batch][kv_heads * q_per_kv][d]: softmax(q K^T / sqrt(d)) V
+ *   lse_out  optional device float [batch][kv_heads * q_per_kv]: log sum_i exp(q.k_i / sqrt(d))
+ * Uses the context's workspace; independent of verkv_attend_verified (its state is untouched). */
+verkv_status verkv_attend_dense_host(verkv_ctx *ctx, int32_t layer, const void *q,
+                                    const void *host_kv, float *o_out, float *lse_out);
+
 /* Copy the per-query-head fetch sets F of the preceding verkv_attend_verified (Eq. (10):
  * F = L \ L_g[k*:]) into `out`, device or page-locked host uint32
  * [batch * kv_heads * q_per_kv][ceil(n/32)] (bit i%32 of word i/32 set iff token i is in F).
@@ -265,6 +276,8 @@ enum {
     VERKV_K_FETCH_HOST,        /* zero-copy fetch + exact sums over fetched rows  */
     VERKV_K_PARTIAL_STAGED,    /* exact sums over rows staged by cudaMemcpyAsync  */
     VERKV_K_MERGE,             /* merge partials into o, lse and statistics       */
+    VERKV_K_DENSE_HOST,        /* offloaded-dense baseline: all rows from host    */
+    VERKV_K_DENSE_MERGE,       /* its running-max merge                           */
     VERKV_K_COUNT
 };
 

@@ -31,8 +31,9 @@ EXPORTED = ["verkv_workspace_size", "verkv_create", "verkv_destroy", "verkv_set_
             "verkv_poissoncomp", "verkv_sketch_build", "verkv_attend_verified",
             "verkv_fetch_refine", "verkv_selection_bitmap", "verkv_profile_enable",
             "verkv_profile_read", "verkv_launch_counts", "verkv_kernel_name", "verkv_sync",
-            "verkv_last_error", "verkv_status_string", "verkv_certify_noalloc"]
-VERKV_K_COUNT = 9
+            "verkv_last_error", "verkv_status_string", "verkv_certify_noalloc",
+            "verkv_attend_dense_host"]
+VERKV_K_COUNT = 11
 
 
 class verkv_shape(ctypes.Structure):
@@ -105,6 +106,8 @@ def lib():
         L.verkv_attend_verified.restype = ctypes.c_int
         L.verkv_fetch_refine.argtypes = [vp, vp, vp, vp, vp, vp, vp]
         L.verkv_fetch_refine.restype = ctypes.c_int
+        L.verkv_attend_dense_host.argtypes = [vp, i32, vp, vp, vp, vp]
+        L.verkv_attend_dense_host.restype = ctypes.c_int
         L.verkv_selection_bitmap.argtypes = [vp, vp]
         L.verkv_selection_bitmap.restype = ctypes.c_int
         L.verkv_profile_enable.argtypes = [vp, ctypes.c_int]
@@ -179,6 +182,10 @@ def verkv_attend_verified(ctx, layer, q, pivotal, r_full, sketch, eps, delta,
 
 def verkv_fetch_refine(ctx, ids, counts, host_kv, o_out, lse_out=None, stats_out=None):
     _check(lib().verkv_fetch_refine(ctx, ids, counts, host_kv, o_out, lse_out, stats_out), ctx)
+
+
+def verkv_attend_dense_host(ctx, layer, q, host_kv, o_out, lse_out=None):
+    _check(lib().verkv_attend_dense_host(ctx, int(layer), q, host_kv, o_out, lse_out), ctx)
 
 
 def verkv_selection_bitmap(ctx, out):

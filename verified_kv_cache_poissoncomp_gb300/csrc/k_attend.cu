@@ -18,6 +18,8 @@
 //             by token id and only the V rows cross the host link.
 // k_merge     sums the partials in a fixed order and writes o = N-hat / D-hat, m + log D-hat and
 //             the per-head statistics.
+// k_dense_host, k_dense_merge   the offloaded-dense baseline: exact attention over every token with
+//             the K|V rows read from page-locked host memory, online-softmax partials per chunk.
 #include <math.h>
 
 #include "verkv_common.cuh"
@@ -338,6 +340,189 @@ __global__ void __launch_bounds__(MG_NT) k_merge(MergeArgs a) {
 
 cudaError_t launch_merge(const MergeArgs &a, int qheads, cudaStream_t s) {
     k_merge<<<qheads, MG_NT, MG_GROUPS * (a.d + 2) * sizeof(float), s>>>(a);
+    return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------------------------------------
+// k_dense_host: the offloaded-dense baseline.  Each CTA item is PART_ROWS consecutive tokens of
+// one KV head; every K|V row (4d bytes, contiguous) is read from page-locked host memory with all
+// of the warp's row groups in flight, the G logits land in shared memory, the chunk's max per
+// head is taken, and w = exp(logit - max) weights the V rows.  The partial is (N[d], D, max).
+template <int D, int G>
+__global__ void __launch_bounds__(128) k_dense_host(DenseArgs a, int units_layer) {
+    constexpr int LPR = D / 8, RPW = 32 / LPR, NW = 4;
+    constexpr int ITER = (PART_ROWS / NW) / RPW;
+    constexpr int SUBMASK = LPR / G - 1;
+    __shared__ float sS[PART_ROWS][G];
+    __shared__ float sMax[G];
+    __shared__ float sN[NW][G][D];
+    __shared__ float sD[NW][RPW][G];
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int cgp = lane % LPR, rg = lane / LPR;
+    const int myhead = head_of_lane<G, LPR>(lane);
+    const int hq = a.li.kv_heads * G;
+    const int total_items = units_layer * a.chunks;
+    for (int item = blockIdx.x; item < total_items; item += gridDim.x) {
+        const int ul = item / a.chunks, ch = item - ul * a.chunks;
+        const int b = ul / a.li.kv_heads, h = ul - b * a.li.kv_heads;
+        const int ug = a.li.unit_global(ul);
+        float qv[G][8];
+#pragma unroll
+        for (int g = 0; g < G; ++g) {
+            const uint4 v = *reinterpret_cast<const uint4 *>(a.q + ((size_t)b * hq + h * G + g) * D + cgp * 8);
+            unpack8(v, qv[g]);
+        }
+        const uint4 *rows = reinterpret_cast<const uint4 *>(a.rows) + (size_t)ug * a.n * (D / 4);
+        const int rbase = ch * PART_ROWS + warp * (PART_ROWS / NW);
+        uint4 kq[ITER], vq[ITER];
+#pragma unroll
+        for (int u = 0; u < ITER; ++u) {
+            const int row = rbase + u * RPW + rg;
+            kq[u] = make_uint4(0, 0, 0, 0);
+            vq[u] = make_uint4(0, 0, 0, 0);
+            if (row < a.n) {
+                kq[u] = ld_host(rows + (size_t)row * (D / 4) + cgp);
+                vq[u] = ld_host(rows + (size_t)row * (D / 4) + D / 8 + cgp);
+            }
+        }
+        // logits of the chunk
+#pragma unroll
+        for (int u = 0; u < ITER; ++u) {
+            const int rl = warp * (PART_ROWS / NW) + u * RPW + rg;  // row within the chunk
+            float k[8];
+            unpack8(kq[u], k);
+            float p[G];
+#pragma unroll
+            for (int g = 0; g < G; ++g) {
+                float s = 0.0f;
+#pragma unroll
+                for (int c = 0; c < 8; ++c) s = fmaf(qv[g][c], k[c], s);
+                p[g] = s;
+            }
+            const float dot = reduce_heads_a<G, LPR>(p, lane);
+            if ((cgp & SUBMASK) == 0)
+                sS[rl][myhead] = ch * PART_ROWS + rl < a.n ? dot * a.scale : -INFINITY;
+        }
+        __syncthreads();
+        if (tid < G) {
+            float m = -INFINITY;
+            for (int r = 0; r < PART_ROWS; ++r) m = fmaxf(m, sS[r][tid]);
+            sMax[tid] = m;
+        }
+        __syncthreads();
+        float acc[G][8];
+#pragma unroll
+        for (int g = 0; g < G; ++g)
+#pragma unroll
+            for (int c = 0; c < 8; ++c) acc[g][c] = 0.0f;
+        float dacc = 0.0f;
+        const float mh = sMax[myhead];
+#pragma unroll
+        for (int u = 0; u < ITER; ++u) {
+            const int rl = warp * (PART_ROWS / NW) + u * RPW + rg;
+            float v[8];
+            unpack8(vq[u], v);
+            const float s = sS[rl][myhead];
+            const float w = s == -INFINITY ? 0.0f : expf(s - mh);
+            if ((cgp & SUBMASK) == 0) dacc += w;
+#pragma unroll
+            for (int g = 0; g < G; ++g) {
+                const float wg = __shfl_sync(0xFFFFFFFFu, w, rg * LPR + lane_of_head<G, LPR>(g));
+#pragma unroll
+                for (int c = 0; c < 8; ++c) acc[g][c] = fmaf(wg, v[c], acc[g][c]);
+            }
+        }
+#pragma unroll
+        for (int off = LPR; off < 32; off <<= 1)
+#pragma unroll
+            for (int g = 0; g < G; ++g)
+#pragma unroll
+                for (int c = 0; c < 8; ++c) acc[g][c] += __shfl_xor_sync(0xFFFFFFFFu, acc[g][c], off);
+        if (rg == 0) {
+#pragma unroll
+            for (int g = 0; g < G; ++g)
+#pragma unroll
+                for (int c = 0; c < 8; ++c) sN[warp][g][cgp * 8 + c] = acc[g][c];
+        }
+        if ((cgp & SUBMASK) == 0) sD[warp][rg][myhead] = dacc;
+        __syncthreads();
+        float *out = a.part + ((size_t)ul * a.chunks + ch) * G * (D + 2);
+        for (int e = tid; e < G * (D + 2); e += 128) {
+            const int g = e / (D + 2), c = e - g * (D + 2);
+            float t = 0.0f;
+            if (c < D) {
+#pragma unroll
+                for (int w2 = 0; w2 < NW; ++w2) t += sN[w2][g][c];
+            } else if (c == D) {
+#pragma unroll
+                for (int w2 = 0; w2 < NW; ++w2)
+#pragma unroll
+                    for (int j = 0; j < RPW; ++j) t += sD[w2][j][g];
+            } else {
+                t = sMax[g];
+            }
+            out[e] = t;
+        }
+        __syncthreads();
+    }
+}
+
+cudaError_t launch_dense_host(const DenseArgs &a, int units_layer, int grid, cudaStream_t s) {
+    const int G = a.li.G;
+#define VERKV_DENSE(DD, GG)                                                                     \
+    if (a.d == DD && G == GG) {                                                                 \
+        k_dense_host<DD, GG><<<grid, 128, 0, s>>>(a, units_layer);                              \
+        return cudaGetLastError();                                                              \
+    }
+    VERKV_DENSE(128, 1) VERKV_DENSE(128, 2) VERKV_DENSE(128, 4) VERKV_DENSE(128, 8)
+    VERKV_DENSE(64, 1) VERKV_DENSE(64, 2) VERKV_DENSE(64, 4) VERKV_DENSE(64, 8)
+#undef VERKV_DENSE
+    return cudaErrorInvalidValue;
+}
+
+// One CTA per query head: the global max M over the chunk maxima, then every chunk's (N, D)
+// scaled by exp(m_chunk - M), summed by 8 groups over interleaved chunks and the groups in a
+// fixed order; o = N / D, lse = M + log D.
+__global__ void __launch_bounds__(MG_NT) k_dense_merge(DenseArgs a, float *o, float *lse) {
+    extern __shared__ float red[];  // [MG_GROUPS][d + 1]
+    __shared__ float sM;
+    const int qh = blockIdx.x;
+    const int G = a.li.G;
+    const int ul = qh / G, g = qh - ul * G;
+    const int D = a.d, ncol = D + 2;
+    const float *pp = a.part + ((size_t)ul * a.chunks * G + g) * ncol;
+    const size_t stride = (size_t)G * ncol;
+    if (threadIdx.x < 32) {
+        float m = -INFINITY;
+        for (int ch = threadIdx.x; ch < a.chunks; ch += 32) m = fmaxf(m, pp[ch * stride + D + 1]);
+        m = warp_max(m);
+        if (threadIdx.x == 0) sM = m;
+    }
+    __syncthreads();
+    const float M = sM;
+    const int grp = threadIdx.x / 128, c0 = threadIdx.x % 128;
+    for (int c = c0; c <= D; c += 128) {
+        float t = 0.0f;
+        for (int ch = grp; ch < a.chunks; ch += MG_GROUPS)
+            t += pp[ch * stride + c] * expf(pp[ch * stride + D + 1] - M);
+        red[grp * (D + 1) + c] = t;
+    }
+    __syncthreads();
+    if (threadIdx.x <= D) {
+        const int c = threadIdx.x;
+        float t = red[c];
+#pragma unroll
+        for (int k = 1; k < MG_GROUPS; ++k) t += red[k * (D + 1) + c];
+        red[c] = t;
+    }
+    __syncthreads();
+    const float Dh = red[D];
+    for (int c = threadIdx.x; c < D; c += MG_NT) o[(size_t)qh * D + c] = red[c] / Dh;
+    if (threadIdx.x == 0 && lse) lse[qh] = M + logf(Dh);
+}
+
+cudaError_t launch_dense_merge(const DenseArgs &a, int qheads, float *o, float *lse, cudaStream_t s) {
+    k_dense_merge<<<qheads, MG_NT, MG_GROUPS * (a.d + 1) * sizeof(float), s>>>(a, o, lse);
     return cudaGetLastError();
 }
 

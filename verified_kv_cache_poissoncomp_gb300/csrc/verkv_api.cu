@@ -613,6 +613,37 @@ verkv_status verkv_sync(verkv_ctx *ctx) {
     return fail(ctx, VERKV_ENOCONVERGE, "a solve hit its iteration cap");
 }
 
+verkv_status verkv_attend_dense_host(verkv_ctx *ctx, int32_t layer, const void *q,
+                                    const void *host_kv, float *o_out, float *lse_out) {
+    if (!ctx) return VERKV_EINVAL;
+    if (layer < 0 || layer >= ctx->sh.layers) return fail(ctx, VERKV_EINVAL, "dense: bad layer");
+    if (!q || !host_kv || !o_out) return fail(ctx, VERKV_EINVAL, "dense: null pointer");
+    VERKV_CUDA(cudaSetDevice(ctx->device), "cudaSetDevice");
+    cudaPointerAttributes attr;
+    cudaError_t e = cudaPointerGetAttributes(&attr, host_kv);
+    if (e != cudaSuccess || attr.type != cudaMemoryTypeHost || !attr.devicePointer) {
+        cudaGetLastError();
+        return fail(ctx, VERKV_EINVAL, "dense: host_kv is not page-locked host memory");
+    }
+    DenseArgs da{};
+    da.rows = (const uint16_t *)attr.devicePointer;
+    da.q = (const uint16_t *)q;
+    da.part = ctx->part_fet;  // [units_layer][ceil(n / PART_ROWS)][G][d + 2]
+    da.n = ctx->sh.n;
+    da.chunks = ctx->L.max_fet;
+    da.d = ctx->sh.head_dim;
+    da.scale = (float)(1.0 / sqrt((double)da.d));
+    da.li = layer_idx(ctx, layer);
+    const int grid = std::max(1, std::min(ctx->L.units_layer * da.chunks, ctx->sms * 4));
+    VERKV_CUDA(tracked(ctx, VERKV_K_DENSE_HOST, ctx->main, [&] {
+                   return launch_dense_host(da, ctx->L.units_layer, grid, ctx->main);
+               }), "k_dense_host");
+    VERKV_CUDA(tracked(ctx, VERKV_K_DENSE_MERGE, ctx->main, [&] {
+                   return launch_dense_merge(da, ctx->L.qh_layer, o_out, lse_out, ctx->main);
+               }), "k_dense_merge");
+    return VERKV_OK;
+}
+
 verkv_status verkv_selection_bitmap(verkv_ctx *ctx, uint32_t *out) {
     if (!ctx) return VERKV_EINVAL;
     if (!ctx->attended) return fail(ctx, VERKV_ESTATE, "selection_bitmap: no attend has run");
@@ -654,7 +685,8 @@ verkv_status verkv_launch_counts(verkv_ctx *ctx, int64_t *out) {
 const char *verkv_kernel_name(int k) {
     static const char *names[VERKV_K_COUNT] = {
         "k_pc_solve", "k_pc_gather", "k_sketch_exact", "k_score", "k_certify",
-        "k_partial(pivotal)", "k_partial(host)", "k_partial(staged)", "k_merge"};
+        "k_partial(pivotal)", "k_partial(host)", "k_partial(staged)", "k_merge",
+        "k_dense_host", "k_dense_merge"};
     return (k >= 0 && k < VERKV_K_COUNT) ? names[k] : "";
 }
 

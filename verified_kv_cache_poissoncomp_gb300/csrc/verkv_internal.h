@@ -122,6 +122,20 @@ struct PartialArgs {
 };
 cudaError_t launch_partial(const PartialArgs &a, int units_layer, int grid, cudaStream_t s);
 
+// Dense attention over every token of a KV head with the rows read from page-locked host memory
+// (the offloaded-dense baseline): per chunk of PART_ROWS rows a partial (N[d], D, m) with the
+// chunk's own max logit m, merged with running-max rescaling.
+struct DenseArgs {
+    const uint16_t *rows;   // host-mapped [units][n][2][d]
+    const uint16_t *q;      // [B][hq][d]
+    float *part;            // [units_layer][chunks][G][d + 2]
+    int n, chunks, d;
+    float scale;
+    LayerIdx li;
+};
+cudaError_t launch_dense_host(const DenseArgs &a, int units_layer, int grid, cudaStream_t s);
+cudaError_t launch_dense_merge(const DenseArgs &a, int qheads, float *o, float *lse, cudaStream_t s);
+
 // Merge partials into o, lse and the per-head stats.
 struct MergeArgs {
     const float *part_piv;

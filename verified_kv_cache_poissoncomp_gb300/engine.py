@@ -93,6 +93,14 @@ class VerKV:
                              stats.data_ptr() if stats is not None else None)
         return o, lse, stats
 
+    def attend_dense_host(self, layer, q, o=None, lse=None):
+        """The offloaded-dense baseline: exact attention with every row read from the host."""
+        o = torch.empty_like(self.o) if o is None else o
+        lse = torch.empty_like(self.lse) if lse is None else lse
+        B.verkv_attend_dense_host(self.ctx, layer, q.data_ptr(), self.host_kv.data_ptr(),
+                                  o.data_ptr(), lse.data_ptr())
+        return o, lse
+
     def selection_bitmap(self):
         out = torch.empty((self.B * self.h * self.G, self.W), dtype=torch.int32, device=self.dev)
         B.verkv_selection_bitmap(self.ctx, out.data_ptr())
