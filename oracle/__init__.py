@@ -51,6 +51,16 @@ def lib():
         L.vo_refine.argtypes = [_dp, _dp, _fp, _u8p, _u8p, _dp, ctypes.c_double,
                                 ctypes.c_int64, ctypes.c_int, _dp]
         L.vo_refine.restype = None
+        L.vo_f16_round.argtypes = [ctypes.c_double, ctypes.c_int]
+        L.vo_f16_round.restype = ctypes.c_double
+        L.vo_f16_bits.argtypes = [ctypes.c_double]
+        L.vo_f16_bits.restype = ctypes.c_uint16
+        L.vo_f16_value.argtypes = [ctypes.c_uint16]
+        L.vo_f16_value.restype = ctypes.c_double
+        L.vo_q2_row_bytes.argtypes = [ctypes.c_int]
+        L.vo_q2_row_bytes.restype = ctypes.c_int
+        L.vo_q2_build.argtypes = [_fp, ctypes.c_int64, ctypes.c_int, _u8p, _dp]
+        L.vo_q2_build.restype = None
         _lib = L
     return _lib
 
@@ -114,6 +124,34 @@ def logits(q, keys):
     s = np.zeros(n, dtype=np.float64)
     lib().vo_logits(_ptr(q, _dp), _ptr(keys, _dp), n, d, _ptr(s, _dp))
     return s
+
+
+def f16_round(x, direction):
+    """The binary16 value next to x: direction < 0 the largest <= x, > 0 the smallest >= x."""
+    return lib().vo_f16_round(float(x), int(direction))
+
+
+def f16_bits(v):
+    return int(lib().vo_f16_bits(float(v)))
+
+
+def f16_value(h):
+    return lib().vo_f16_value(int(h))
+
+
+def q2_row_bytes(d):
+    return int(lib().vo_q2_row_bytes(int(d)))
+
+
+def q2_sketch(keys_bf16):
+    """The 2-bit sketch of bf16 keys [n][d] (uint16 bits): (rows uint8 [n][row bytes],
+    k-hat float64 [n][d], the exact dequantised keys the certificate scores)."""
+    kf = np.ascontiguousarray(bf16_to_f64(keys_bf16), dtype=np.float32)
+    n, d = kf.shape
+    rows = np.zeros((n, q2_row_bytes(d)), dtype=np.uint8)
+    khat = np.zeros((n, d), dtype=np.float64)
+    lib().vo_q2_build(_ptr(kf, _fp), n, d, _ptr(rows, _u8p), _ptr(khat, _dp))
+    return rows, khat
 
 
 def dense(s, values):

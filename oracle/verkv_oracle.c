@@ -12,8 +12,9 @@
  *
  * Precision: fp64 everywhere, except where a float32 value is itself part of the definition of a
  * decision: r_i is published as float32 and the Bernoulli draw compares a 24-bit uniform against
- * it (vo_poissoncomp).  Every loop is serial; the only library primitives are qsort, exp, log and
- * sqrt.
+ * it (vo_poissoncomp), and the 2-bit sketch's float32 / binary16 quantiser (vo_q2_build) whose
+ * codes are part of the sketch's definition.  Every loop is serial; the only library primitives
+ * are qsort, exp, log, sqrt, floor, ceil, frexp, ldexp and rintf.
  *
  * Parity status: every exported function is pinned by tests/test_oracle_*.py against closed
  * forms, brute force, an independent Philox (Triton's, run by its CPU interpreter), high-precision
@@ -228,6 +229,107 @@ void vo_dense(const double *s, const double *values, int64_t n, int d, double *o
     out[1] = D;
     for (int c = 0; c < d; ++c)
         out[2 + d + c] = N[c] / D;
+}
+
+/* ------------------------------------------------------------------------------------------- */
+/* The 2-bit token sketch (summary page, Error Bound Guarantee: the "2-bit sketch" compared with
+ * the perfect one; abstract page: a token-level sketch of the full KV cache).  The pages give no
+ * layout; ours, per token of a head with d channels, in groups of 32 channels:
+ *   lo    = the largest IEEE binary16 value <= min of the group (clamped to +-65504),
+ *   step  = the smallest binary16 value >= fl((max - lo) / 3) (float32 subtract and divide),
+ *   code  = min(3, max(0, rint(fl(fl(x - lo) / step)))) (0 if step == 0; rint rounds half to even),
+ *   k-hat = lo + code * step, exactly (the key the certificate scores).
+ * Bytes of a row: d/4 bytes of codes (channel c in bits 2(c mod 4) of byte c/4), then per group
+ * lo and step as little-endian binary16, zero-padded to a multiple of 16 bytes. */
+
+/* The binary16 value next to a finite x in direction dir (< 0: largest <= x, > 0: smallest >= x),
+ * with x first clamped to the finite binary16 range. */
+double vo_f16_round(double x, int dir)
+{
+    const double maxf16 = 65504.0;
+    if (x > maxf16) x = maxf16;
+    if (x < -maxf16) x = -maxf16;
+    const double a = fabs(x);
+    double q; /* spacing of binary16 values at |x| */
+    if (a < ldexp(1.0, -14)) {
+        q = ldexp(1.0, -24);
+    } else {
+        int e;
+        frexp(a, &e); /* a in [2^(e-1), 2^e) */
+        q = ldexp(1.0, e - 1 - 10);
+    }
+    const double k = x / q; /* exact: q is a power of two */
+    return (dir < 0 ? floor(k) : ceil(k)) * q;
+}
+
+/* Bits of a binary16 value v (exactly representable). */
+uint16_t vo_f16_bits(double v)
+{
+    uint16_t sign = signbit(v) ? 0x8000u : 0u; /* -0 keeps its sign */
+    const double a = fabs(v);
+    if (a == 0.0) return sign;
+    if (a < ldexp(1.0, -14)) return (uint16_t)(sign | (uint16_t)(a / ldexp(1.0, -24)));
+    int e;
+    const double m = frexp(a, &e); /* a = m 2^e, m in [0.5, 1) */
+    const uint16_t exp16 = (uint16_t)(e - 1 + 15);
+    const uint16_t mant = (uint16_t)((2.0 * m - 1.0) * 1024.0);
+    return (uint16_t)(sign | (uint16_t)(exp16 << 10) | mant);
+}
+
+/* Value of binary16 bits (finite). */
+double vo_f16_value(uint16_t h)
+{
+    const double sign = (h & 0x8000u) ? -1.0 : 1.0;
+    const int e = (h >> 10) & 0x1F;
+    const int m = h & 0x3FF;
+    if (e == 0) return sign * ldexp((double)m, -24);
+    return sign * ldexp(1024.0 + (double)m, e - 25);
+}
+
+int vo_q2_row_bytes(int d)
+{
+    const int raw = d / 4 + 4 * (d / 32);
+    return (raw + 15) / 16 * 16;
+}
+
+/* Quantise n keys (float32 values of bf16 keys, row-major [n][d], d a multiple of 32) into rows
+ * of vo_q2_row_bytes(d) bytes, and write the exact dequantised keys k-hat [n][d]. */
+void vo_q2_build(const float *keys, int64_t n, int d, uint8_t *rows, double *khat)
+{
+    const int rb = vo_q2_row_bytes(d);
+    for (int64_t i = 0; i < n; ++i) {
+        uint8_t *row = rows + i * rb;
+        memset(row, 0, (size_t)rb);
+        for (int gr = 0; gr < d / 32; ++gr) {
+            const float *x = keys + i * d + 32 * gr;
+            float mn = x[0], mx = x[0];
+            for (int c = 1; c < 32; ++c) {
+                if (x[c] < mn) mn = x[c];
+                if (x[c] > mx) mx = x[c];
+            }
+            const float lo = (float)vo_f16_round((double)mn, -1);
+            const float span = mx - lo;         /* float32 */
+            const float third = span / 3.0f;    /* float32 */
+            const float step = (float)vo_f16_round((double)third, +1);
+            for (int c = 0; c < 32; ++c) {
+                int code = 0;
+                if (step > 0.0f) {
+                    const float t = (x[c] - lo) / step; /* float32 subtract, float32 divide */
+                    const float rq = rintf(t);
+                    code = rq < 0.0f ? 0 : (rq > 3.0f ? 3 : (int)rq);
+                }
+                const int ch = 32 * gr + c;
+                row[ch / 4] |= (uint8_t)(code << (2 * (ch % 4)));
+                khat[i * d + ch] = (double)lo + (double)code * (double)step;
+            }
+            const uint16_t lb = vo_f16_bits((double)lo), sb = vo_f16_bits((double)step);
+            uint8_t *par = row + d / 4 + 4 * gr;
+            par[0] = (uint8_t)(lb & 0xFF);
+            par[1] = (uint8_t)(lb >> 8);
+            par[2] = (uint8_t)(sb & 0xFF);
+            par[3] = (uint8_t)(sb >> 8);
+        }
+    }
 }
 
 /* ------------------------------------------------------------------------------------------- */
