@@ -50,6 +50,8 @@ def parse_args():
     p.add_argument("--queries", type=int, default=QUERIES)
     p.add_argument("--eps-sweep", action="store_true",
                    help="tolerance sweep: throughput and host-traffic statistics per eps")
+    p.add_argument("--sketch", choices=["exact", "q2"], default="exact",
+                   help="token sketch: exact bf16 keys (the headline) or the 2-bit sketch")
     p.add_argument("--dense-offload", action="store_true",
                    help="the offloaded-dense baseline alone (every row from the host cache)")
     return p.parse_args()
@@ -263,9 +265,10 @@ def run_ours(args, world, rank, local):
     stream = torch.cuda.Stream(dev)
     mode = B.VERKV_FETCH_MEMCPY if args.fetch_mode == "memcpy" else B.VERKV_FETCH_ZEROCOPY
     with torch.cuda.stream(stream):
-        eng = VerKV(w.B, w.L, w.h_kv, w.G, w.d, w.n, cap, fetch_mode=mode)
+        eng = VerKV(w.B, w.L, w.h_kv, w.G, w.d, w.n, cap, fetch_mode=mode,
+                    sketch_format=sketch_format(args))
         eng.load(w.tau.reshape(-1, w.n), w.kv.reshape(-1, w.n, 2, w.d))
-        eng.compress(w.eta, w.n_sink, w.n_local, w.seed)   # also builds the exact sketch
+        eng.compress(w.eta, w.n_sink, w.n_local, w.seed)   # also builds the sketch
         eng.sync()
         q_dev = torch.as_tensor(w.queries.view(np.int16)).to(dev)          # [Q][1][32][128]
         hq = w.B * w.h_kv * w.G
@@ -370,12 +373,14 @@ def run_ours(args, world, rank, local):
     fetched_rows = fc_all.cpu().numpy().astype(np.int64)          # [Q][units] of the last step
     units_layer = w.B * w.h_kv
     units_all = w.B * w.L * w.h_kv
+    sketch_row_bytes = B.verkv_sketch_bytes(eng.shape, eng.sketch_format) // (units_all * w.n)
+    fetch_row_bytes = (2 if args.sketch == "exact" else 4) * w.d
     algo = {
-        "k_score": ("hbm", units_layer * w.n * w.d * 2),
+        "k_score": ("hbm", units_layer * w.n * sketch_row_bytes),
         "k_certify": ("hbm", units_layer * (w.n * 4 + w.n // 8)),
         "k_partial(pivotal)": ("hbm", int(counts.mean() * units_layer * (4 * w.d + 8))),
-        # with the exact sketch only V rows (2 d bytes) cross the host link
-        "k_partial(host)": ("h2d", int(fetched_rows.sum(1).mean() * 2 * w.d)),
+        # with the exact sketch only V rows (2 d bytes) cross the host link, else K|V rows
+        "k_partial(host)": ("h2d", int(fetched_rows.sum(1).mean() * fetch_row_bytes)),
         "k_pc_solve": ("hbm", int(units_all * w.n * 8.125 + counts.sum() * 8)),
         "k_pc_gather": ("hbm", int(counts.sum() * 2 * 4 * w.d)),
     }
@@ -463,7 +468,8 @@ def run_ours(args, world, rank, local):
                                       "eps=delta=0.05; layer held as 4 independent instances, "
                                       "query t on instance t mod 4",
                           "l2": "inputs larger than L2 (4 x 73 MiB resident state per step)",
-                          "fetch": args.fetch_mode, "graph": graph is not None,
+                          "fetch": args.fetch_mode, "sketch": args.sketch,
+                          "graph": graph is not None,
                           "parallelism": f"replicas x{world}"},
                "roofline": roof, "roofline_hbm": roof_hbm, "rooflines": rooflines,
                "per_kernel_us": {
@@ -480,6 +486,11 @@ def run_ours(args, world, rank, local):
 
 
 EPS_SWEEP = [0.01, 0.02, 0.05, 0.1, 0.2, 0.3, 0.5]
+
+
+def sketch_format(args):
+    from verified_kv_cache_poissoncomp_gb300 import binding as B
+    return B.VERKV_SKETCH_Q2 if args.sketch == "q2" else B.VERKV_SKETCH_EXACT
 
 
 def traffic_stats(st, fetched_rows, pivotal_count, n):
@@ -560,7 +571,8 @@ def run_eps_sweep(args, local):
     Q = w.queries.shape[0]
     stream = torch.cuda.Stream(dev)
     with torch.cuda.stream(stream):
-        eng = VerKV(w.B, w.L, w.h_kv, w.G, w.d, w.n, default_cap(w.n, w.eta))
+        eng = VerKV(w.B, w.L, w.h_kv, w.G, w.d, w.n, default_cap(w.n, w.eta),
+                    sketch_format=sketch_format(args))
         eng.load(w.tau.reshape(-1, w.n), w.kv.reshape(-1, w.n, 2, w.d))
         eng.compress(w.eta, w.n_sink, w.n_local, w.seed)
         eng.sync()
@@ -607,7 +619,7 @@ def run_eps_sweep(args, local):
             counts = eng.p_count.cpu().numpy().astype(np.int64)
         fr = fc_all.cpu().numpy().astype(np.int64)
         row = {"eps": eps, "queries_per_s": round(Q / (ms * 1e-3), 2), "ms_per_step": round(ms, 4),
-               "h2d_bytes_per_query": int(fr.sum(1).mean() * 2 * w.d)}
+               "h2d_bytes_per_query": int(fr.sum(1).mean() * (2 if args.sketch == "exact" else 4) * w.d)}
         row.update({k: round(v, 5) for k, v in
                     traffic_stats(st_all.cpu().numpy(), fr, counts, w.n).items()})
         rows.append(row)
@@ -622,6 +634,7 @@ def run_eps_sweep(args, local):
                       "steps": args.steps, "warmup": args.warmup, "data": "synthetic",
                       "config": {"workload": "single-layer 32K (the bench workload), "
                                              f"{Q} decode queries per step", "fetch": "zerocopy",
+                                 "sketch": args.sketch,
                                  "graph": True},
                       "rows": rows}), flush=True)
     eng.close()

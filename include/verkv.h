@@ -88,8 +88,17 @@ typedef struct {
 
 /* Token-level sketch of the full cache (abstract page; summary page, KVFETCH step 1).
  * VERKV_SKETCH_EXACT: a bf16 copy of every key, [units][n][d] -- the "perfect sketch" of the
- * summary page's Figure 5 and the setting of Theorem 2. */
-enum { VERKV_SKETCH_EXACT = 0 };
+ * summary page's Figure 5 and the setting of Theorem 2.
+ * VERKV_SKETCH_Q2: the "2-bit sketch" of the same figure, in a layout of ours (the pages give
+ *   none): per token a row of R = 16 * ceil((d/4 + d/8) / 16) bytes (48 for d = 128, 32 for
+ *   d = 64), [units][n][R].  Per group of 32 channels, floor = the largest binary16 at or below
+ *   the group's minimum key value and step = the smallest binary16 at or above
+ *   float32((max - floor) / 3) (both clamped to +-65504); code = rint(float32((x - floor) /
+ *   step)) clamped to 0..3 (0 when step is 0).  Bytes: d/4 of codes (channel c in bits
+ *   2 (c mod 4) of byte c/4), then per group floor and step as little-endian binary16, then zero
+ *   padding.  The certificate scores the keys floor + code * step; fetched tokens then move
+ *   their K and V rows, since the GPU holds no exact key. */
+enum { VERKV_SKETCH_EXACT = 0, VERKV_SKETCH_Q2 = 1 };
 typedef struct {
     int32_t format;
     const void *data;
@@ -128,6 +137,9 @@ typedef struct {
     int32_t certified, k_star, n_L, n_fetch, iters, flags;
 } verkv_head_stats;
 
+/* Bytes of a sketch of `format` for every unit of `shape` (0 if the shape or format is invalid). */
+size_t verkv_sketch_bytes(const verkv_shape *shape, int32_t format);
+
 /* Bytes of device workspace a context for `shape` needs (0 if the shape is invalid). */
 size_t verkv_workspace_size(const verkv_shape *shape);
 
@@ -164,8 +176,9 @@ verkv_status verkv_poissoncomp(verkv_ctx *ctx, const float *tau, double eta, ver
                                uint64_t seed, const void *kv_full, float *r_full,
                                const verkv_pivotal *out);
 
-/* Build the sketch from the full device cache.  VERKV_SKETCH_EXACT: copies every key row,
- * kv_full bf16 [units][n][2][d] -> sketch_out bf16 [units][n][d]. */
+/* Build the sketch from the full device cache kv_full bf16 [units][n][2][d] into sketch_out
+ * (device, verkv_sketch_bytes(shape, format) bytes).  VERKV_SKETCH_EXACT copies every key row
+ * (bf16 [units][n][d]); VERKV_SKETCH_Q2 quantises every key row to 2 bits (layout above). */
 verkv_status verkv_sketch_build(verkv_ctx *ctx, const void *kv_full, int32_t format,
                                 void *sketch_out);
 

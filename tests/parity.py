@@ -31,9 +31,10 @@ def bits_to_bool(words, n):
 
 
 # ------------------------------------------------------------------------------------------------
-def make_engine(w, cap=None, fetch_mode=B.VERKV_FETCH_ZEROCOPY):
+def make_engine(w, cap=None, fetch_mode=B.VERKV_FETCH_ZEROCOPY, sketch_format=B.VERKV_SKETCH_EXACT):
     cap = cap or default_cap(w.n, w.eta)
-    eng = VerKV(w.B, w.L, w.h_kv, w.G, w.d, w.n, cap, fetch_mode=fetch_mode)
+    eng = VerKV(w.B, w.L, w.h_kv, w.G, w.d, w.n, cap, fetch_mode=fetch_mode,
+                sketch_format=sketch_format)
     eng.load(w.tau.reshape(-1, w.n), w.kv.reshape(-1, w.n, 2, w.d))
     return eng
 
@@ -88,7 +89,8 @@ def gpu_query(eng, w, t, eps=None, delta=None):
                 ids=eng.fetch_ids.cpu().numpy().copy(), counts=eng.fetch_counts.cpu().numpy().copy())
 
 
-def oracle_query(w, t, pcs, eps=None, delta=None):
+def oracle_query(w, t, pcs, eps=None, delta=None, sketches=None):
+    """sketches: None for the exact sketch, else {(b, l, h): dequantised sketch keys}."""
     eps = w.eps if eps is None else eps
     delta = w.delta if delta is None else delta
     l = int(w.query_layer[t])
@@ -98,9 +100,16 @@ def oracle_query(w, t, pcs, eps=None, delta=None):
             pc = pcs[(b, l, h)]
             K = O.bf16_to_f64(w.kv[b, l, h, :, 0, :])
             V = O.bf16_to_f64(w.kv[b, l, h, :, 1, :])
+            Ks = K if sketches is None else sketches[(b, l, h)]
             qs = O.bf16_to_f64(w.queries[t, b, h * w.G:(h + 1) * w.G])
-            units.append(O.attend_unit(qs, K, K, V, pc["r32"], pc["resident"], eps, delta))
+            units.append(O.attend_unit(qs, Ks, K, V, pc["r32"], pc["resident"], eps, delta))
     return units
+
+
+def oracle_q2_sketches(w):
+    """The oracle's 2-bit sketch of every unit: {(b, l, h): (rows uint8, dequantised keys)}."""
+    return {(b, l, h): O.q2_sketch(w.kv[b, l, h, :, 0, :])
+            for b in range(w.B) for l in range(w.L) for h in range(w.h_kv)}
 
 
 def compare_query(g, units, w, eps=None, report=None):

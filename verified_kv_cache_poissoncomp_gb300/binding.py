@@ -23,11 +23,12 @@ VERKV_ETOOLARGE = 9
 VERKV_NOALLOC_MAX_LOGITS = 1 << 22
 
 VERKV_SKETCH_EXACT = 0
+VERKV_SKETCH_Q2 = 1
 VERKV_FETCH_ZEROCOPY = 0
 VERKV_FETCH_MEMCPY = 1
 VERKV_FETCH_KEYS = 4
 
-EXPORTED = ["verkv_workspace_size", "verkv_create", "verkv_destroy", "verkv_set_fetch_mode",
+EXPORTED = ["verkv_sketch_bytes", "verkv_workspace_size", "verkv_create", "verkv_destroy", "verkv_set_fetch_mode",
             "verkv_poissoncomp", "verkv_sketch_build", "verkv_attend_verified",
             "verkv_fetch_refine", "verkv_selection_bitmap", "verkv_profile_enable",
             "verkv_profile_read", "verkv_launch_counts", "verkv_kernel_name", "verkv_sync",
@@ -86,6 +87,8 @@ def lib():
                                "`python -m verified_kv_cache_poissoncomp_gb300.build`")
         L = ctypes.CDLL(LIB_PATH)
         vp, i32, sz = ctypes.c_void_p, ctypes.c_int32, ctypes.c_size_t
+        L.verkv_sketch_bytes.argtypes = [ctypes.POINTER(verkv_shape), i32]
+        L.verkv_sketch_bytes.restype = sz
         L.verkv_workspace_size.argtypes = [ctypes.POINTER(verkv_shape)]
         L.verkv_workspace_size.restype = sz
         L.verkv_create.argtypes = [ctypes.POINTER(vp), ctypes.c_int, vp,
@@ -145,6 +148,10 @@ def _check(st, ctx=None):
 
 
 # ------------------------------------------------------------------------------------------------
+def verkv_sketch_bytes(shape, fmt):
+    return int(lib().verkv_sketch_bytes(ctypes.byref(shape), int(fmt)))
+
+
 def verkv_workspace_size(shape):
     return int(lib().verkv_workspace_size(ctypes.byref(shape)))
 

@@ -6,9 +6,9 @@
 // k_partial   split-K over a row set: each CTA takes 64 rows of one KV head, each row a contiguous
 //             4d-byte K|V pair read with 16-byte coalesced loads, four row groups in flight per
 //             warp.  It computes the G logits, w = exp(logit - m), the weight of Eq. (5) -- 1 for H
-//             and for tokens of F, lambda / r with lambda = clip(beta r / (w (1 - r)), r, 1) for
-//             sampled, unfetched tokens -- and accumulates D-hat, N-hat and the sample second
-//             moment.  All CTAs of a query head share its shift m, so partials add without
+//             and for tokens of F, lambda / r for sampled, unfetched tokens, with the certificate's
+//             lambda = clip(beta r / (w-hat (1 - r)), r, 1) from the sketch weight w-hat -- and
+//             accumulates D-hat, N-hat and the sample second moment.  All CTAs of a query head share its shift m, so partials add without
 //             rescaling.  Three row sources:
 //               ROWS_PIVOTAL   the pivotal buffer in HBM;
 //               ROWS_STAGED    fetched rows already copied to HBM (the cudaMemcpyAsync fetch);
@@ -135,6 +135,7 @@ __global__ void __launch_bounds__(128) k_partial(PartialArgs a, int units_layer)
         const float mh_ = a.qstats[ul * G + myhead].m;
         const float bh_ = a.qstats[ul * G + myhead].beta;
         const uint32_t *Fh = a.F + (size_t)(ul * G + myhead) * a.W;
+        const float *sc_h = MODE == ROWS_PIVOTAL ? a.scores + (size_t)(ul * G + myhead) * a.n : nullptr;
         float acc[G][8];
 #pragma unroll
         for (int g = 0; g < G; ++g)
@@ -208,9 +209,11 @@ __global__ void __launch_bounds__(128) k_partial(PartialArgs a, int units_layer)
                         if (ru >= 1.0f || inF) {
                             coef = 1.0f;
                         } else {
+                            // lambda is the certificate's: from the sketch weight w-hat
+                            const float wh = expf(sc_h[id[u]] - mh_);
                             float lam = 1.0f;
-                            if (w > 0.0f)
-                                lam = fminf(1.0f, fmaxf(ru, __fdiv_rn(bh_ * ru, w * (1.0f - ru))));
+                            if (wh > 0.0f)
+                                lam = fminf(1.0f, fmaxf(ru, __fdiv_rn(bh_ * ru, wh * (1.0f - ru))));
                             coef = __fdiv_rn(lam, ru);
                         }
                     } else {

@@ -9,6 +9,7 @@
 // rounded root.  Each token's Bernoulli draw is word i%4 of one Philox4x32-10 block per four
 // tokens; warp shuffles assemble the keep bits into the resident bitmap and a cluster-wide scan
 // compacts H u S in ascending token order into the pivotal buffer.
+#include <cuda_fp16.h>
 #include <math.h>
 
 #include "verkv_common.cuh"
@@ -321,6 +322,70 @@ cudaError_t launch_sketch_exact(const uint16_t *kv_full, uint16_t *sketch, int64
     if (blocks < 1) blocks = 1;
     k_sketch_exact<<<(int)blocks, 256, 0, s>>>(reinterpret_cast<const uint4 *>(kv_full),
                                                reinterpret_cast<uint4 *>(sketch), rows, half16);
+    return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------------------------------------
+// The 2-bit sketch: one thread per (token, 32-channel group).  floor = the largest binary16 at or
+// below the group minimum, step = the smallest binary16 at or above fl((max - floor) / 3) (both
+// clamped to the finite binary16 range first), code = rint(fl(fl(x - floor) / step)) in 0..3.
+// Row layout (q2_row_bytes(d) bytes): d/4 bytes of codes, channel c in bits 2(c mod 4) of byte
+// c/4, then per group floor and step as binary16, then zero padding to 16 bytes.
+__global__ void __launch_bounds__(256) k_sketch_q2(const uint16_t *kv_full, uint8_t *sketch,
+                                                   int64_t rows, int d, int row_bytes) {
+    const int ng = d / 32;
+    const int64_t t = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (t >= rows * ng) return;
+    const int64_t i = t / ng;
+    const int gr = (int)(t - i * ng);
+    const uint4 *x4 = reinterpret_cast<const uint4 *>(kv_full + i * 2 * d + 32 * gr);  // K row
+    float x[32];
+#pragma unroll
+    for (int v = 0; v < 4; ++v) {
+        float f[8];
+        unpack8(ldg_stream(x4 + v), f);
+#pragma unroll
+        for (int c = 0; c < 8; ++c) x[8 * v + c] = f[c];
+    }
+    float mn = x[0], mx = x[0];
+#pragma unroll
+    for (int c = 1; c < 32; ++c) {
+        mn = fminf(mn, x[c]);
+        mx = fmaxf(mx, x[c]);
+    }
+    const __half lo_h = __float2half_rd(fminf(fmaxf(mn, -65504.0f), 65504.0f));
+    const float lo = __half2float(lo_h);
+    const float third = __fdiv_rn(__fsub_rn(mx, lo), 3.0f);
+    const __half st_h = __float2half_ru(fminf(third, 65504.0f));
+    const float st = __half2float(st_h);
+    uint32_t w0 = 0u, w1 = 0u;
+#pragma unroll
+    for (int c = 0; c < 32; ++c) {
+        int code = 0;
+        if (st > 0.0f) {
+            const float rq = rintf(__fdiv_rn(__fsub_rn(x[c], lo), st));
+            code = rq < 0.0f ? 0 : (rq > 3.0f ? 3 : (int)rq);
+        }
+        if (c < 16) w0 |= (uint32_t)code << (2 * c);
+        else w1 |= (uint32_t)code << (2 * (c - 16));
+    }
+    uint8_t *row = sketch + i * row_bytes;
+    *reinterpret_cast<uint2 *>(row + 8 * gr) = make_uint2(w0, w1);
+    *reinterpret_cast<uint32_t *>(row + d / 4 + 4 * gr) =
+        (uint32_t)__half_as_ushort(lo_h) | ((uint32_t)__half_as_ushort(st_h) << 16);
+    if (gr == 0)
+        for (int b = d / 4 + 4 * ng; b < row_bytes; b += 4) *reinterpret_cast<uint32_t *>(row + b) = 0u;
+}
+
+int q2_row_bytes(int d) { return (d / 4 + 4 * (d / 32) + 15) / 16 * 16; }
+
+cudaError_t launch_sketch_q2(const uint16_t *kv_full, uint8_t *sketch, int64_t rows, int d,
+                             cudaStream_t s) {
+    const int64_t threads = rows * (d / 32);
+    const int64_t blocks = (threads + 255) / 256;
+    if (blocks > 0x7FFFFFFF) return cudaErrorInvalidValue;
+    k_sketch_q2<<<(int)(blocks < 1 ? 1 : blocks), 256, 0, s>>>(kv_full, sketch, rows, d,
+                                                              q2_row_bytes(d));
     return cudaGetLastError();
 }
 

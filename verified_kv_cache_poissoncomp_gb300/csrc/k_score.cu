@@ -4,6 +4,7 @@
 // k_score streams the bf16 sketch once per KV head through a TMA bulk-copy ring in shared memory
 // and scores it against all G query heads of the group (q slices held in registers; a
 // recursive-halving shuffle reduce leaves each head's logit in a quarter of the row's lanes).
+#include <cuda_fp16.h>
 #include <math.h>
 
 #include "verkv_common.cuh"
@@ -255,6 +256,170 @@ cudaError_t launch_score(const ScoreArgs &a, int units_layer, cudaStream_t s) {
     VERKV_SCORE(128, 1) VERKV_SCORE(128, 2) VERKV_SCORE(128, 4) VERKV_SCORE(128, 8)
     VERKV_SCORE(64, 1) VERKV_SCORE(64, 2) VERKV_SCORE(64, 4) VERKV_SCORE(64, 8)
 #undef VERKV_SCORE
+    return cudaErrorInvalidValue;
+}
+
+// ---------------------------------------------------------------------------------------------
+// Scoring from the 2-bit sketch.  Same TMA ring, SQ_ROWS rows a stage.  A lane holds CPL
+// consecutive channels of a row (its codes are one 32- or 16-bit field, its group's floor and
+// step one 32-bit word) and the matching q values; per head its dot product is
+// floor * sum(q) + step * sum(q * code), the codes turned into floats in pairs for fma.f32x2.
+constexpr int SQ_ROWS = 256;
+
+__device__ __forceinline__ unsigned long long fadd2(unsigned long long a, unsigned long long b) {
+    unsigned long long d;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+
+template <int D, int G>
+__global__ void __launch_bounds__(SC_NT, SC_CTAS_PER_SM) k_score_q2(ScoreArgs a, int spans_per_unit,
+                                                                   int span_rows) {
+    constexpr int CPL = G <= 4 ? 16 : 8;
+    constexpr int LPR = D / CPL, RPW = 32 / LPR, NW = SC_NT / 32;
+    constexpr int ROWB = (D / 4 + 4 * (D / 32) + 15) / 16 * 16;  // bytes per sketch row
+    constexpr int WROWS = SQ_ROWS / NW;
+    constexpr int SUBMASK = LPR / G - 1;
+    constexpr float MAGIC = 8388608.0f;  // 2^23: float bits 0x4B000000 | c equal 2^23 + c
+    extern __shared__ __align__(128) unsigned char ring[];  // [SC_STAGES][SQ_ROWS][ROWB]
+    __shared__ __align__(8) uint64_t full[SC_STAGES];
+    __shared__ int s_abort;
+
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int cgp = lane % LPR, rg = lane / LPR;
+    const int ul = blockIdx.x / spans_per_unit;
+    const int span = blockIdx.x - ul * spans_per_unit;
+    const int b = ul / a.li.kv_heads, h = ul - b * a.li.kv_heads;
+    const int ug = a.li.unit_global(ul);
+    const int hq = a.li.kv_heads * G;
+    const int row0 = span * span_rows;
+    const int nrows = min(a.n - row0, span_rows);
+    if (nrows <= 0) return;  // uniform over the CTA
+    const int nst = (nrows + SQ_ROWS - 1) / SQ_ROWS;
+    const unsigned char *src = reinterpret_cast<const unsigned char *>(a.sketch) +
+                               ((size_t)ug * a.n + row0) * ROWB;
+    const int code_word = (CPL * cgp) / 16, code_shift = (2 * CPL * cgp) % 32;
+    const int par_word = D / 16 + (CPL * cgp) / 32;
+
+    unsigned long long qp[G][CPL / 2];
+    float qs[G];
+#pragma unroll
+    for (int g = 0; g < G; ++g) {
+        qs[g] = 0.0f;
+#pragma unroll
+        for (int v = 0; v < CPL / 8; ++v) {
+            const uint4 x = *reinterpret_cast<const uint4 *>(a.q + ((size_t)b * hq + h * G + g) * D +
+                                                             CPL * cgp + 8 * v);
+            float f[8];
+            unpack8(x, f);
+#pragma unroll
+            for (int t = 0; t < 4; ++t) {
+                qp[g][4 * v + t] = pack2(f[2 * t], f[2 * t + 1]);
+                qs[g] += f[2 * t] + f[2 * t + 1];
+            }
+        }
+    }
+    const unsigned long long neg_magic = pack2(-MAGIC, -MAGIC);
+    if (tid == 0) {
+        for (int k = 0; k < SC_STAGES; ++k) mbar_init(&full[k], 1);
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        s_abort = 0;
+    }
+    __syncthreads();
+    auto issue = [&](int k) {
+        const int rows_k = min(SQ_ROWS, nrows - k * SQ_ROWS);
+        const uint32_t bytes = (uint32_t)rows_k * ROWB;
+        uint64_t *bar = &full[k % SC_STAGES];
+        mbar_expect_tx(bar, bytes);
+        bulk_g2s(ring + (size_t)(k % SC_STAGES) * SQ_ROWS * ROWB, src + (size_t)k * SQ_ROWS * ROWB,
+                 bytes, bar);
+    };
+    if (tid == 0)
+        for (int k = 0; k < min(SC_STAGES, nst); ++k) issue(k);
+
+    float *out = a.scores + (size_t)ul * G * a.n + row0;
+    int consumed = 0;
+    for (int k = 0; k < nst; ++k) {
+        const uint32_t parity = (uint32_t)((k / SC_STAGES) & 1);
+        if (!mbar_wait_bounded(&full[k % SC_STAGES], parity)) s_abort = 1;
+        __syncthreads();
+        if (s_abort) break;
+        consumed = k + 1;
+        const int rows_k = min(SQ_ROWS, nrows - k * SQ_ROWS);
+        const uint32_t *stage = reinterpret_cast<const uint32_t *>(ring + (size_t)(k % SC_STAGES) * SQ_ROWS * ROWB);
+#pragma unroll 2
+        for (int j = 0; j < WROWS / RPW; ++j) {
+            const int r = warp * WROWS + j * RPW + rg;  // row within the stage
+            uint32_t cw = 0u, pw = 0u;
+            if (r < rows_k) {
+                cw = stage[r * (ROWB / 4) + code_word] >> code_shift;
+                pw = stage[r * (ROWB / 4) + par_word];
+            }
+            const float lo = __half2float(__ushort_as_half((unsigned short)(pw & 0xFFFFu)));
+            const float st = __half2float(__ushort_as_half((unsigned short)(pw >> 16)));
+            unsigned long long acc[G];
+#pragma unroll
+            for (int g = 0; g < G; ++g) acc[g] = 0ull;
+#pragma unroll
+            for (int i = 0; i < CPL / 2; ++i) {
+                const uint32_t c0 = (cw >> (4 * i)) & 3u, c1 = (cw >> (4 * i + 2)) & 3u;
+                const unsigned long long cp =
+                    fadd2(pack2(__uint_as_float(0x4B000000u | c0), __uint_as_float(0x4B000000u | c1)),
+                          neg_magic);
+#pragma unroll
+                for (int g = 0; g < G; ++g) acc[g] = ffma2(qp[g][i], cp, acc[g]);
+            }
+            float p[G];
+#pragma unroll
+            for (int g = 0; g < G; ++g) p[g] = fmaf(lo, qs[g], st * sum2(acc[g]));
+            int head;
+            const float sc = reduce_heads<G, LPR>(p, lane, head);
+            if ((cgp & SUBMASK) == 0 && r < rows_k)
+                out[(size_t)head * a.n + k * SQ_ROWS + r] = sc * a.scale;
+        }
+        __syncthreads();  // every warp is done with the stage: refill it
+        if (tid == 0 && k + SC_STAGES < nst) issue(k + SC_STAGES);
+    }
+    if (s_abort) {
+        if (tid == 0) {
+            raise_error(a.err, ERR_TIMEOUT);
+            const int issued = min(nst, consumed + SC_STAGES);
+            for (int k = consumed; k < issued; ++k)
+                mbar_wait_bounded(&full[k % SC_STAGES], (uint32_t)((k / SC_STAGES) & 1));
+        }
+        __syncthreads();
+    }
+}
+
+cudaError_t launch_score_q2(const ScoreArgs &a, int units_layer, cudaStream_t s) {
+    int sms = 0, dev = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    const long long total = (long long)units_layer * a.n;
+    long long span_rows = (total + (long long)SC_CTAS_PER_SM * sms - 1) / ((long long)SC_CTAS_PER_SM * sms);
+    span_rows = (span_rows + SQ_ROWS - 1) / SQ_ROWS * SQ_ROWS;
+    if (span_rows < SQ_ROWS) span_rows = SQ_ROWS;
+    const int spans = (int)((a.n + span_rows - 1) / span_rows);
+    dim3 grid(spans * units_layer);
+    const int G = a.li.G;
+#define VERKV_SCORE_Q2(DD, GG)                                                                  \
+    if (a.d == DD && G == GG) {                                                                 \
+        constexpr int ROWB = (DD / 4 + 4 * (DD / 32) + 15) / 16 * 16;                           \
+        const size_t smem = (size_t)SC_STAGES * SQ_ROWS * ROWB;                                 \
+        static bool attr = false;                                                               \
+        if (!attr) {                                                                            \
+            cudaError_t e = cudaFuncSetAttribute(k_score_q2<DD, GG>,                            \
+                                                 cudaFuncAttributeMaxDynamicSharedMemorySize,   \
+                                                 (int)smem);                                    \
+            if (e != cudaSuccess) return e;                                                     \
+            attr = true;                                                                        \
+        }                                                                                       \
+        k_score_q2<DD, GG><<<grid, SC_NT, smem, s>>>(a, spans, (int)span_rows);                 \
+        return cudaGetLastError();                                                              \
+    }
+    VERKV_SCORE_Q2(128, 1) VERKV_SCORE_Q2(128, 2) VERKV_SCORE_Q2(128, 4) VERKV_SCORE_Q2(128, 8)
+    VERKV_SCORE_Q2(64, 1) VERKV_SCORE_Q2(64, 2) VERKV_SCORE_Q2(64, 4) VERKV_SCORE_Q2(64, 8)
+#undef VERKV_SCORE_Q2
     return cudaErrorInvalidValue;
 }
 

@@ -152,6 +152,7 @@ struct verkv_ctx {
     const int32_t *user_ids = nullptr, *user_counts = nullptr;
     const void *q = nullptr;
     const void *sketch = nullptr;
+    bool sketch_exact = true;  // format of the preceding attend's sketch
     std::string last_error;
     // Measurement
     int64_t launches[VERKV_K_COUNT] = {};
@@ -233,6 +234,14 @@ const char *verkv_status_string(int st) {
         case VERKV_ETOOLARGE: return "VERKV_ETOOLARGE";
         default: return "VERKV_UNKNOWN";
     }
+}
+
+size_t verkv_sketch_bytes(const verkv_shape *shape, int32_t format) {
+    if (!valid_shape(shape)) return 0;
+    const size_t rows = (size_t)shape->batch * shape->layers * shape->kv_heads * shape->n;
+    if (format == VERKV_SKETCH_EXACT) return rows * 2 * shape->head_dim;
+    if (format == VERKV_SKETCH_Q2) return rows * q2_row_bytes(shape->head_dim);
+    return 0;
 }
 
 size_t verkv_workspace_size(const verkv_shape *shape) {
@@ -385,9 +394,17 @@ verkv_status verkv_sketch_build(verkv_ctx *ctx, const void *kv_full, int32_t for
                                 void *sketch_out) {
     if (!ctx) return VERKV_EINVAL;
     if (!kv_full || !sketch_out) return fail(ctx, VERKV_EINVAL, "sketch_build: null pointer");
-    if (format != VERKV_SKETCH_EXACT) return fail(ctx, VERKV_EINVAL, "sketch_build: unknown format");
+    if (format != VERKV_SKETCH_EXACT && format != VERKV_SKETCH_Q2)
+        return fail(ctx, VERKV_EINVAL, "sketch_build: unknown format");
     VERKV_CUDA(cudaSetDevice(ctx->device), "cudaSetDevice");
     const int64_t rows = (int64_t)ctx->sh.batch * ctx->sh.layers * ctx->sh.kv_heads * ctx->sh.n;
+    if (format == VERKV_SKETCH_Q2) {
+        VERKV_CUDA(tracked(ctx, VERKV_K_SKETCH, ctx->main, [&] {
+                       return launch_sketch_q2((const uint16_t *)kv_full, (uint8_t *)sketch_out,
+                                               rows, ctx->sh.head_dim, ctx->main);
+                   }), "k_sketch_q2");
+        return VERKV_OK;
+    }
     VERKV_CUDA(tracked(ctx, VERKV_K_SKETCH, ctx->main, [&] {
                    return launch_sketch_exact((const uint16_t *)kv_full, (uint16_t *)sketch_out,
                                               rows, ctx->sh.head_dim, ctx->main);
@@ -404,7 +421,8 @@ verkv_status verkv_attend_verified(verkv_ctx *ctx, int32_t layer, const void *q,
     if (!q || !pivotal || !r_full || !sketch || !sketch->data || !pivotal->ids || !pivotal->r ||
         !pivotal->kv || !pivotal->count || !pivotal->resident)
         return fail(ctx, VERKV_EINVAL, "attend: null pointer");
-    if (sketch->format != VERKV_SKETCH_EXACT) return fail(ctx, VERKV_EINVAL, "attend: unknown sketch format");
+    if (sketch->format != VERKV_SKETCH_EXACT && sketch->format != VERKV_SKETCH_Q2)
+        return fail(ctx, VERKV_EINVAL, "attend: unknown sketch format");
     if (!(eps > 0.0f) || !(delta > 0.0f) || !(delta < 1.0f) || !isfinite(eps))
         return fail(ctx, VERKV_EINVAL, "attend: need eps > 0 and 0 < delta < 1");
     VERKV_CUDA(cudaSetDevice(ctx->device), "cudaSetDevice");
@@ -420,7 +438,11 @@ verkv_status verkv_attend_verified(verkv_ctx *ctx, int32_t layer, const void *q,
     sa.d = d;
     sa.scale = (float)(1.0 / sqrt((double)d));
     sa.li = li;
-    VERKV_CUDA(tracked(ctx, VERKV_K_SCORE, ctx->main, [&] { return launch_score(sa, ctx->L.units_layer, ctx->main); }), "k_score");
+    if (sketch->format == VERKV_SKETCH_Q2) {
+        VERKV_CUDA(tracked(ctx, VERKV_K_SCORE, ctx->main, [&] { return launch_score_q2(sa, ctx->L.units_layer, ctx->main); }), "k_score_q2");
+    } else {
+        VERKV_CUDA(tracked(ctx, VERKV_K_SCORE, ctx->main, [&] { return launch_score(sa, ctx->L.units_layer, ctx->main); }), "k_score");
+    }
 
     CertifyArgs ca{};
     ca.scores = ctx->scores;
@@ -458,6 +480,7 @@ verkv_status verkv_attend_verified(verkv_ctx *ctx, int32_t layer, const void *q,
     pa.q = (const uint16_t *)q;
     pa.F = ctx->F;
     pa.qstats = ctx->qstats;
+    pa.scores = ctx->scores;
     pa.part = ctx->part_piv;
     pa.row_stride = ctx->sh.cap;
     pa.max_chunks = ctx->L.max_piv;
@@ -481,6 +504,7 @@ verkv_status verkv_attend_verified(verkv_ctx *ctx, int32_t layer, const void *q,
     ctx->user_counts = fetch_counts_out;
     ctx->q = q;
     ctx->sketch = sketch->data;
+    ctx->sketch_exact = sketch->format == VERKV_SKETCH_EXACT;
     return VERKV_OK;
 }
 
@@ -496,7 +520,8 @@ verkv_status verkv_fetch_refine(verkv_ctx *ctx, const int32_t *ids, const int32_
     const LayerIdx li = layer_idx(ctx, ctx->layer);
     const int n = ctx->sh.n, d = ctx->sh.head_dim;
     // With the exact sketch every key is already on the GPU: only V rows move, unless asked.
-    const bool v_only = !ctx->fetch_keys;
+    // A 2-bit sketch holds no exact key, so fetched rows bring their K row too.
+    const bool v_only = !ctx->fetch_keys && ctx->sketch_exact;
     const size_t row_bytes = (size_t)4 * d;                 // a K|V row of the host cache
     const size_t move_bytes = v_only ? (size_t)2 * d : row_bytes;
     const size_t move_off = v_only ? (size_t)2 * d : 0;     // V follows K inside a row

@@ -45,6 +45,11 @@ cudaError_t launch_pc_gather(const uint16_t *kv_full, const int32_t *ids, const 
 cudaError_t launch_sketch_exact(const uint16_t *kv_full, uint16_t *sketch, int64_t rows, int d,
                                 cudaStream_t s);
 
+// The 2-bit sketch: rows of q2_row_bytes(d) bytes per token (codes, per-group floor and step).
+int q2_row_bytes(int d);
+cudaError_t launch_sketch_q2(const uint16_t *kv_full, uint8_t *sketch, int64_t rows, int d,
+                             cudaStream_t s);
+
 // ---------------------------------------------------------------------------------------------
 // Layer-local indexing of a decode call: u' = b * kv_heads + h (units of the layer), query head
 // qh = u' * G + g, global unit u = (b * layers + layer) * kv_heads + h.
@@ -67,6 +72,8 @@ struct ScoreArgs {
     LayerIdx li;
 };
 cudaError_t launch_score(const ScoreArgs &a, int units_layer, cudaStream_t s);
+// The same from the 2-bit sketch (a.sketch points at its rows).
+cudaError_t launch_score_q2(const ScoreArgs &a, int units_layer, cudaStream_t s);
 
 // Certificate and selection per query head (one cluster per query head).  When fl_counter is
 // set, the last of the G clusters of a KV head to finish also builds that head's fetch list:
@@ -112,6 +119,7 @@ struct PartialArgs {
     const uint16_t *q;        // [B][hq][d]
     const uint32_t *F;        // [qh][W]
     const verkv_head_stats *qstats;
+    const float *scores;      // sketch logits [qh][n]: lambda of Definition 2 uses w-hat
     float *part;              // [units_layer][max_chunks][G][d + 2]
     int row_stride;           // cap (pivotal) or n (fetched)
     int max_chunks;

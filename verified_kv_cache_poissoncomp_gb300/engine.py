@@ -21,12 +21,13 @@ def default_cap(n, eta):
 
 class VerKV:
     def __init__(self, batch, layers, kv_heads, q_per_kv, head_dim, n, cap, device=None,
-                 fetch_mode=B.VERKV_FETCH_ZEROCOPY):
+                 fetch_mode=B.VERKV_FETCH_ZEROCOPY, sketch_format=B.VERKV_SKETCH_EXACT):
         self.dev = torch.device("cuda", torch.cuda.current_device() if device is None else device)
         self.shape = B.verkv_shape(batch, layers, kv_heads, q_per_kv, head_dim, n, cap)
         self.B, self.L, self.h, self.G, self.d, self.n, self.cap = (
             batch, layers, kv_heads, q_per_kv, head_dim, n, cap)
         self.units = batch * layers * kv_heads
+        self.sketch_format = sketch_format
         self.W = (n + 31) // 32
         ws = B.verkv_workspace_size(self.shape)
         if ws == 0:
@@ -66,13 +67,18 @@ class VerKV:
         self.host_kv = torch.empty(kv_t.shape, dtype=torch.int16, pin_memory=True)
         self.host_kv.copy_(kv_t)
         self.kv = self.host_kv.to(self.dev)
-        self.sketch = torch.empty((self.units, self.n, self.d), dtype=torch.int16, device=self.dev)
-        self.sketch_desc = B.verkv_sketch(B.VERKV_SKETCH_EXACT, self.sketch.data_ptr())
+        if self.sketch_format == B.VERKV_SKETCH_EXACT:
+            self.sketch = torch.empty((self.units, self.n, self.d), dtype=torch.int16, device=self.dev)
+        else:
+            nbytes = B.verkv_sketch_bytes(self.shape, self.sketch_format)
+            self.sketch = torch.empty((self.units, self.n, nbytes // (self.units * self.n)),
+                                      dtype=torch.uint8, device=self.dev)
+        self.sketch_desc = B.verkv_sketch(self.sketch_format, self.sketch.data_ptr())
 
     def compress(self, eta, n_sink, n_local, seed):
         B.verkv_poissoncomp(self.ctx, self.tau.data_ptr(), eta, B.verkv_hset(n_sink, n_local),
                             seed, self.kv.data_ptr(), self.r_full.data_ptr(), self.pivotal)
-        B.verkv_sketch_build(self.ctx, self.kv.data_ptr(), B.VERKV_SKETCH_EXACT,
+        B.verkv_sketch_build(self.ctx, self.kv.data_ptr(), self.sketch_format,
                              self.sketch.data_ptr())
 
     def attend(self, layer, q, eps, delta, with_ids=True):
