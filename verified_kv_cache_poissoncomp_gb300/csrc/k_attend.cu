@@ -3,9 +3,10 @@
 // Definition 2 / Eq. (5), KVFETCH step 5; abstract page: fetch additional tokens from the CPU and
 // refine the attention computation).
 //
-// k_partial   split-K over a row set: each CTA takes 64 rows of one KV head, each row a contiguous
-//             4d-byte K|V pair read with 16-byte coalesced loads, four row groups in flight per
-//             warp.  It computes the G logits, w = exp(logit - m), the weight of Eq. (5) -- 1 for H
+// k_partial   split-K over a row set: each CTA item is 64 pivotal rows, or up to FET_ITEM_ROWS
+//             fetched rows taken 64 at a time, of one KV head; each row a contiguous 4d-byte K|V
+//             pair read with 16-byte coalesced loads, four row groups in flight per warp (all of
+//             them for host rows), accumulated into one partial.  It computes the G logits, w = exp(logit - m), the weight of Eq. (5) -- 1 for H
 //             and for tokens of F, lambda / r for sampled, unfetched tokens, with the certificate's
 //             lambda = clip(beta r / (w-hat (1 - r)), r, 1) from the sketch weight w-hat -- and
 //             accumulates D-hat, N-hat and the sample second moment.  All CTAs of a query head share its shift m, so partials add without
@@ -115,6 +116,9 @@ __global__ void __launch_bounds__(128) k_partial(PartialArgs a, int units_layer)
     const int myhead = head_of_lane<G, LPR>(lane);
     const int hq = a.li.kv_heads * G;
     const int total_items = units_layer * a.max_chunks;
+    // Pivotal rows: one 64-row block per partial (many CTAs, one round each); fetched rows:
+    // FET_SUB blocks accumulated per partial (fewer partials for the merge).
+    constexpr int ITEM = MODE == ROWS_PIVOTAL ? PART_ROWS : FET_ITEM_ROWS;
 
     for (int item = blockIdx.x; item < total_items; item += gridDim.x) {
         const int ul = item / a.max_chunks;
@@ -124,7 +128,7 @@ __global__ void __launch_bounds__(128) k_partial(PartialArgs a, int units_layer)
         const int src = MODE == ROWS_PIVOTAL ? ug : ul;
         int rows_u = a.count[src];
         if (rows_u > a.row_stride) rows_u = a.row_stride;
-        if (ch * PART_ROWS >= rows_u) continue;  // uniform over the CTA
+        if (ch * ITEM >= rows_u) continue;  // uniform over the CTA
 
         float qv[G][8];
 #pragma unroll
@@ -150,7 +154,11 @@ __global__ void __launch_bounds__(128) k_partial(PartialArgs a, int units_layer)
                             (MODE == ROWS_HOST ? (size_t)ug * a.n : (size_t)src * a.row_stride) * a.row16;
         const uint4 *keys = a.keys ? reinterpret_cast<const uint4 *>(a.keys) + (size_t)ug * a.n * (D / 8)
                                    : nullptr;
-        const int rbase = ch * PART_ROWS + warp * (PART_ROWS / NW);
+#pragma unroll 1
+        for (int sub = 0; sub < ITEM / PART_ROWS; ++sub) {
+        const int cbase = ch * ITEM + sub * PART_ROWS;
+        if (cbase >= rows_u) break;  // uniform over the CTA
+        const int rbase = cbase + warp * (PART_ROWS / NW);
 #pragma unroll 1
         for (int it0 = 0; it0 < ITER; it0 += U) {
             int id[U];
@@ -165,12 +173,15 @@ __global__ void __launch_bounds__(128) k_partial(PartialArgs a, int units_layer)
             }
             uint4 kq[U], vq[U];
             uint32_t fw[U];
+            float shat[U];  // sketch logit of the row for the lane's head (pivotal rows)
 #pragma unroll
             for (int u = 0; u < U; ++u) {
                 kq[u] = make_uint4(0, 0, 0, 0);
                 vq[u] = make_uint4(0, 0, 0, 0);
                 fw[u] = 0u;
+                shat[u] = 0.0f;
                 if (valid[u]) {
+                    if (MODE == ROWS_PIVOTAL && r[u] < 1.0f) shat[u] = sc_h[id[u]];
                     const size_t rr = MODE == ROWS_HOST ? (size_t)id[u] : (size_t)(rbase + (it0 + u) * RPW + rg);
                     if (keys) {
                         kq[u] = ldg_stream(keys + (size_t)id[u] * (D / 8) + cgp);
@@ -210,7 +221,7 @@ __global__ void __launch_bounds__(128) k_partial(PartialArgs a, int units_layer)
                             coef = 1.0f;
                         } else {
                             // lambda is the certificate's: from the sketch weight w-hat
-                            const float wh = expf(sc_h[id[u]] - mh_);
+                            const float wh = expf(shat[u] - mh_);
                             float lam = 1.0f;
                             if (wh > 0.0f)
                                 lam = fminf(1.0f, fmaxf(ru, __fdiv_rn(bh_ * ru, wh * (1.0f - ru))));
@@ -234,6 +245,7 @@ __global__ void __launch_bounds__(128) k_partial(PartialArgs a, int units_layer)
                 }
             }
         }
+        }  // sub
         // Reduce over the row groups of the warp, then over warps (fixed order).
 #pragma unroll
         for (int off = LPR; off < 32; off <<= 1)
@@ -307,7 +319,7 @@ __global__ void __launch_bounds__(MG_NT) k_merge(MergeArgs a) {
     int pc = a.pcount[ug];
     if (pc > a.cap) pc = a.cap;
     const int npc = (pc + PART_ROWS - 1) / PART_ROWS;
-    const int nfc = (a.fcount[ul] + PART_ROWS - 1) / PART_ROWS;
+    const int nfc = (a.fcount[ul] + FET_ITEM_ROWS - 1) / FET_ITEM_ROWS;
     const int grp = threadIdx.x / 128, c0 = threadIdx.x % 128;
     const float *pp = a.part_piv + ((size_t)ul * a.max_piv * G + g) * ncol;
     const float *pf = a.part_fet + ((size_t)ul * a.max_fet * G + g) * ncol;

@@ -25,7 +25,7 @@ size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 
 struct Layout {
     size_t err, flc, scores, qstats, F, fids, fcounts, staging, part_piv, part_fet, total;
-    int W, units_layer, qh_layer, max_piv, max_fet;
+    int W, units_layer, qh_layer, max_piv, max_fet, dense_chunks;
 };
 
 bool valid_shape(const verkv_shape *s) {
@@ -44,7 +44,8 @@ bool make_layout(const verkv_shape *s, Layout &L) {
     L.units_layer = s->batch * s->kv_heads;
     L.qh_layer = L.units_layer * s->q_per_kv;
     L.max_piv = (s->cap + PART_ROWS - 1) / PART_ROWS;
-    L.max_fet = (s->n + PART_ROWS - 1) / PART_ROWS;
+    L.max_fet = (s->n + FET_ITEM_ROWS - 1) / FET_ITEM_ROWS;
+    L.dense_chunks = (s->n + PART_ROWS - 1) / PART_ROWS;  // >= max_fet: sizes the shared buffer
     size_t off = 0;
     auto take = [&](size_t bytes) {
         const size_t o = off;
@@ -60,7 +61,7 @@ bool make_layout(const verkv_shape *s, Layout &L) {
     L.fcounts = take((size_t)L.units_layer * 4);
     L.staging = take((size_t)L.units_layer * n * 4 * d);
     L.part_piv = take((size_t)L.units_layer * L.max_piv * G * (d + 2) * 4);
-    L.part_fet = take((size_t)L.units_layer * L.max_fet * G * (d + 2) * 4);
+    L.part_fet = take((size_t)L.units_layer * L.dense_chunks * G * (d + 2) * 4);
     L.total = off;
     return true;
 }
@@ -653,9 +654,9 @@ verkv_status verkv_attend_dense_host(verkv_ctx *ctx, int32_t layer, const void *
     DenseArgs da{};
     da.rows = (const uint16_t *)attr.devicePointer;
     da.q = (const uint16_t *)q;
-    da.part = ctx->part_fet;  // [units_layer][ceil(n / PART_ROWS)][G][d + 2]
+    da.part = ctx->part_fet;  // [units_layer][dense_chunks][G][d + 2]
     da.n = ctx->sh.n;
-    da.chunks = ctx->L.max_fet;
+    da.chunks = ctx->L.dense_chunks;
     da.d = ctx->sh.head_dim;
     da.scale = (float)(1.0 / sqrt((double)da.d));
     da.li = layer_idx(ctx, layer);

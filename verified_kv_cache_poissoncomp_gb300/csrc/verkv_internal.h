@@ -105,7 +105,9 @@ size_t certify_smem_bytes(int chunk);
 // ---------------------------------------------------------------------------------------------
 // Shrinkage-weighted partial sums over a row set: the pivotal rows in HBM, fetched rows staged in
 // HBM, or fetched rows read by token id straight from page-locked host memory.
-constexpr int PART_ROWS = 64;
+constexpr int PART_ROWS = 64;                      // rows a CTA has in flight
+constexpr int FET_SUB = 4;                         // row blocks per partial for fetched rows
+constexpr int FET_ITEM_ROWS = PART_ROWS * FET_SUB; // rows per partial for fetched rows (pivotal: 64)
 enum { ROWS_PIVOTAL = 0, ROWS_STAGED = 1, ROWS_HOST = 2 };
 struct PartialArgs {
     const uint16_t *rows;     // [src units][row_stride][row16 vectors]; ROWS_HOST: [units][n][2][d]
