@@ -52,6 +52,9 @@ def parse_args():
                    help="tolerance sweep: throughput and host-traffic statistics per eps")
     p.add_argument("--sketch", choices=["exact", "q2"], default="exact",
                    help="token sketch: exact bf16 keys (the headline) or the 2-bit sketch")
+    p.add_argument("--pc-sweep", action="store_true",
+                   help="PoissonComp throughput: 36 layers x 8 KV heads, n in {32K, 128K}, "
+                        "eta in {1/8, 1/16, 1/32}")
     p.add_argument("--dense-offload", action="store_true",
                    help="the offloaded-dense baseline alone (every row from the host cache)")
     return p.parse_args()
@@ -640,6 +643,88 @@ def run_eps_sweep(args, local):
     eng.close()
 
 
+def run_pc_sweep(args, local):
+    """One GPU: verkv_poissoncomp (c solve, Poisson sample, compaction, pivotal K/V gather) over
+    every head of a 36-layer x 8-KV-head cache per call, for n in {32K, 128K} and eta in
+    {1/8, 1/16, 1/32}; H = 4 sink + 512 local; tau lognormal(0, 1.5) normalised per head; K/V
+    bytes random on the device.  One JSON line."""
+    import torch
+
+    from verified_kv_cache_poissoncomp_gb300 import binding as B
+    from verified_kv_cache_poissoncomp_gb300 import inputs as I
+    from verified_kv_cache_poissoncomp_gb300.engine import default_cap
+
+    B.lib()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    layers, kvh, d = 36, 8, 128
+    units = layers * kvh
+    peak, peak_src = measured_peaks()
+    stream = torch.cuda.Stream(dev)
+    rows = []
+    for n in (32768, 131072):
+        tau = torch.from_numpy(I.pc_sweep_tau(units, n)).to(dev)
+        gen = torch.Generator(device=dev)
+        gen.manual_seed(1240)
+        kv = torch.empty((units, n, 2, d), dtype=torch.int16, device=dev)
+        kv.random_(-32768, 32767, generator=gen)
+        r_full = torch.empty((units, n), dtype=torch.float32, device=dev)
+        for eta in (1 / 8, 1 / 16, 1 / 32):
+            cap = default_cap(n, eta)
+            shape = B.verkv_shape(1, layers, kvh, 4, d, n, cap)
+            ws_bytes = B.verkv_workspace_size(shape)
+            ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
+            ids = torch.empty((units, cap), dtype=torch.int32, device=dev)
+            pr = torch.empty((units, cap), dtype=torch.float32, device=dev)
+            pkv = torch.empty((units, cap, 2, d), dtype=torch.int16, device=dev)
+            cnt = torch.empty((units,), dtype=torch.int32, device=dev)
+            res = torch.empty((units, (n + 31) // 32), dtype=torch.int32, device=dev)
+            c = torch.empty((units,), dtype=torch.float32, device=dev)
+            piv = B.verkv_pivotal(ids.data_ptr(), pr.data_ptr(), pkv.data_ptr(), cnt.data_ptr(),
+                                  res.data_ptr(), c.data_ptr())
+            ctx = B.verkv_create(local, stream.cuda_stream, shape, ws.data_ptr(), ws_bytes)
+            H = B.verkv_hset(4, 512)
+
+            def call():
+                B.verkv_poissoncomp(ctx, tau.data_ptr(), eta, H, 0, kv.data_ptr(),
+                                    r_full.data_ptr(), piv)
+
+            with torch.cuda.stream(stream):
+                for _ in range(args.warmup):
+                    call()
+            B.verkv_sync(ctx)
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            with torch.cuda.stream(stream):
+                for _ in range(args.steps):
+                    call()
+            e1.record(stream)
+            torch.cuda.synchronize()
+            B.verkv_sync(ctx)
+            ms = e0.elapsed_time(e1) / args.steps
+            counts = cnt.cpu().numpy().astype(np.int64)
+            # algorithmic bytes: tau in, r out, resident bitmap, ids + r of the sample, and the
+            # gather's read and write of every pivotal K/V row
+            nbytes = units * (8 * n + n // 8) + int(counts.sum()) * (8 + 2 * 4 * d)
+            gbs = nbytes / (ms * 1e-3) / 1e9
+            rows.append({"n": n, "eta": round(eta, 5), "ms_per_call": round(ms, 4),
+                         "heads_per_s": round(units / (ms * 1e-3), 1),
+                         "mean_pivotal_rows": round(float(counts.mean()), 1),
+                         "algorithmic_bytes_per_call": nbytes, "achieved_GBs": round(gbs, 1),
+                         "frac_of_hbm_peak": round(gbs / peak, 4)})
+            B.verkv_destroy(ctx)
+            del ws, ids, pr, pkv, cnt, res, c
+        del kv, tau, r_full
+        torch.cuda.empty_cache()
+    print(json.dumps({"sweep": "poissoncomp", "unit": "heads/s", "steps": args.steps,
+                      "warmup": args.warmup, "data": "synthetic", "hbm_peak_GBs": peak,
+                      "peak_source": peak_src,
+                      "config": {"workload": "36 layers x 8 KV heads per call, d=128, H=4+512, "
+                                             "tau lognormal(0,1.5) normalised per head"},
+                      "rows": rows}), flush=True)
+
+
 def run_dense_offload(args, local):
     """One GPU: the offloaded-dense baseline on the bench workload, one JSON line."""
     import torch
@@ -680,6 +765,9 @@ def main():
     elif args.dense_offload:
         if rank == 0:
             run_dense_offload(args, local)
+    elif args.pc_sweep:
+        if rank == 0:
+            run_pc_sweep(args, local)
     else:
         run_ours(args, world, rank, local)
 

@@ -191,3 +191,14 @@ def single_layer_32k(layers=4, n=32768, n_queries=256, data_seed=1235, **kw):
     return make_workload("single-layer-32k", B=1, L=layers, h_kv=8, G=4, d=128, n=n,
                          eta=1.0 / 16, n_sink=4, n_local=512, n_queries=n_queries,
                          plant_every=4, n_plants=8, data_seed=data_seed, **kw)
+
+
+def pc_sweep_tau(units, n, data_seed=1239):
+    """Importance scores for the PoissonComp throughput sweep: for each of `units` heads,
+    i.i.d. lognormal(0, 1.5) divided by the head's maximum (float32 [units][n])."""
+    rng = np.random.default_rng(data_seed)
+    tau = np.empty((units, n), dtype=np.float32)
+    for u in range(units):
+        x = rng.lognormal(0.0, 1.5, n)
+        tau[u] = (x / x.max()).astype(np.float32)
+    return tau
