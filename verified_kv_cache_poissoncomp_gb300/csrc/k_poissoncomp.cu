@@ -2,11 +2,14 @@
 // Methodology, POISSONCOMP: Eq. (3), the H / L partition and the Poisson sample S).
 //
 // One thread-block cluster per unit (sequence, layer, KV head); each CTA holds up to 32768
-// importance scores in shared memory.  The budget constant c is located by a cluster-wide
-// bisection over float32 c on the reduction sum_i min(1, c tau_i), then finished exactly in
-// fp64 on its linear piece (saturated count s, unsaturated sum T, c = (B - s) / T, repeated until
-// the saturated set stops changing), so the float32 c every decision uses is the correctly
-// rounded root.  Each token's Bernoulli draw is word i%4 of one Philox4x32-10 block per four
+// importance scores in shared memory.  F(c) = sum_i min(1, c tau_i) is concave and piecewise
+// linear, so the budget constant is found by Newton on it, climbing from c = B / sum tau (where
+// F <= B): on the current piece F(c) = s + c T (s saturated tokens, T the unsaturated sum), the
+// next c is (B - s) / T, until the saturated set stops changing (one to three passes on lognormal
+// scores).  The sums are exact: T in 64-bit fixed point (2^-46 per unit of tau) from 32-bit
+// arithmetic, s an integer count, and a token saturates when tau >= the float32 rounded up from
+// 1 / c, so the float32 c every decision uses is the correctly rounded root.  A float32 bisection
+// followed by the same finish is kept as the fallback if Newton has not settled in 8 passes.  Each token's Bernoulli draw is word i%4 of one Philox4x32-10 block per four
 // tokens; warp shuffles assemble the keep bits into the resident bitmap and a cluster-wide scan
 // compacts H u S in ascending token order into the pivotal buffer.
 #include <cuda_fp16.h>
@@ -35,6 +38,16 @@ static size_t pc_smem_bytes(int chunk) {
            2 * PC_MAX_CL * PC_NW * 2 * 8 + PC_NW * 4 + PC_MAX_CL * 4 + 64;
 }
 
+// tau (in (0, 1]) as 64-bit fixed point with 46 fractional bits, from 32-bit arithmetic:
+// the integer part of tau 2^14 and 32 bits of what remains (truncated below 2^-46).
+__device__ __forceinline__ unsigned long long tau_fixed(float x) {
+    const float y = x * 16384.0f;
+    const float hi = truncf(y);
+    return ((unsigned long long)__float2uint_rz(hi) << 32) |
+           (unsigned long long)__float2uint_rz((y - hi) * 4294967296.0f);
+}
+constexpr double TAU_FIXED_UNIT = 1.0 / 70368744177664.0;  // 2^-46
+
 __global__ void __launch_bounds__(PC_NT, 1) k_pc_solve(PcArgs a) {
     extern __shared__ __align__(16) unsigned char smem_raw[];
     PcSmem sm;
@@ -61,6 +74,7 @@ __global__ void __launch_bounds__(PC_NT, 1) k_pc_solve(PcArgs a) {
 
     // 1. Load tau of the non-forced tokens; validate it.
     float tsum = 0.0f, tmin = __int_as_float(0x7F800000);
+    unsigned long long tfix = 0ull;  // exact sum of tau
     bool bad = false;
     for (int i = tid; i < a.chunk; i += PC_NT) {
         const int t = base + i;
@@ -73,6 +87,7 @@ __global__ void __launch_bounds__(PC_NT, 1) k_pc_solve(PcArgs a) {
             }
             tmin = fminf(tmin, x);
             tsum += x;
+            tfix += tau_fixed(x);
         }
         sm.tau[i] = x;
     }
@@ -84,12 +99,48 @@ __global__ void __launch_bounds__(PC_NT, 1) k_pc_solve(PcArgs a) {
         float m[2] = {-tmin, 0.0f};
         red.run(m, OpMax());
         tmin = -m[0];
+        unsigned long long z = 0ull;
+        red64.run_u64(tfix, z);
     }
 
     double c = __longlong_as_double(0x7FF0000000000000LL);  // +inf: every token kept
+    bool solved = false;
     if (a.n_rest > 0 && a.b_rest < (double)a.n_rest) {
+        // 2. Newton on the concave piecewise-linear F from below.  A token saturates at c when
+        //    tau >= 1 / c, i.e. tau >= the float32 rounded up from 1 / c.
+        auto eval_exact = [&](double cc, unsigned long long &sat, unsigned long long &tun) {
+            const float thr = __double2float_ru(1.0 / cc);
+            unsigned long long s = 0ull, T = 0ull;
+            for (int i = tid; i < a.chunk; i += PC_NT) {
+                const float x = sm.tau[i];
+                if (x > 0.0f) {
+                    if (x >= thr) s += 1ull; else T += tau_fixed(x);
+                }
+            }
+            red64.run_u64(T, s);
+            sat = s;
+            tun = T;
+        };
+        const double tsum_exact = (double)tfix * TAU_FIXED_UNIT;
+        c = a.b_rest / tsum_exact * (1.0 - 0x1p-40);  // F(c) <= c sum tau <= B
+        unsigned long long s, T;
+        eval_exact(c, s, T);
+        for (int it = 0; it < 8 && T > 0ull; ++it) {
+            const double cn = (a.b_rest - (double)s) / ((double)T * TAU_FIXED_UNIT);
+            unsigned long long s2, T2;
+            eval_exact(cn, s2, T2);
+            c = cn;
+            if (s2 == s) {
+                solved = true;
+                break;
+            }
+            s = s2;
+            T = T2;
+        }
+    }
+    if (!solved && a.n_rest > 0 && a.b_rest < (double)a.n_rest) {
         const float B = (float)a.b_rest;
-        // 2. Bisection on float32 c.  F(lo) <= B <= F(hi): at lo every tau is scaled below its
+        // Fallback.  Bisection on float32 c: F(lo) <= B <= F(hi): at lo every tau is scaled below its
         //    unclipped sum; at hi = 2 / min tau every token saturates.
         float lo = (float)(a.b_rest / (double)tsum) * 0.999f;
         float hi = 2.0f / tmin;
@@ -139,16 +190,17 @@ __global__ void __launch_bounds__(PC_NT, 1) k_pc_solve(PcArgs a) {
 
     // 4. r_i = min(1, c tau_i) as a float32 product (1 for forced H); the budget check in fp64.
     float *r_full = a.r_full + (size_t)u * n;
-    double rsum = 0.0, zero = 0.0;
+    unsigned long long rfix = 0ull, zero = 0ull;  // exact sum of the float32 r
     for (int i = tid; i < a.chunk; i += PC_NT) {
         const int t = base + i;
         if (t >= n) break;
         const float x = sm.tau[i];
         const float r = (x > 0.0f) ? fminf(1.0f, __fmul_rn(c32, x)) : 1.0f;
         r_full[t] = r;
-        rsum += (double)r;
+        rfix += tau_fixed(r);
     }
-    red64.run(rsum, zero);
+    red64.run_u64(rfix, zero);
+    const double rsum = (double)rfix * TAU_FIXED_UNIT;
     if (!(fabs(rsum - a.eta_n) < 1e-6 * (double)n) && tid == 0 && crank == 0)
         raise_error(a.err, ERR_BUDGET_SUM);
 

@@ -142,6 +142,39 @@ struct ClusterReducer64 {
     int cl;
     int parity;
 
+    // Exact integer sums (a, b) over the cluster, on the same buffers and parity.
+    __device__ __forceinline__ void run_u64(unsigned long long &a, unsigned long long &b) {
+        const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+            a += __shfl_xor_sync(0xFFFFFFFFu, a, o);
+            b += __shfl_xor_sync(0xFFFFFFFFu, b, o);
+        }
+        cg::cluster_group cluster = cg::this_cluster();
+        const unsigned me = cluster.block_rank();
+        unsigned long long *buf = reinterpret_cast<unsigned long long *>(slots + parity * cl * NW * 2);
+        if (lane < cl) {
+            unsigned long long *peer = cluster.map_shared_rank(buf, lane);
+            peer[(me * NW + warp) * 2 + 0] = a;
+            peer[(me * NW + warp) * 2 + 1] = b;
+        }
+        cluster.sync();
+        const int total = cl * NW;
+        unsigned long long sa = 0ull, sb = 0ull;
+        for (int e = lane; e < total; e += 32) {
+            sa += buf[e * 2 + 0];
+            sb += buf[e * 2 + 1];
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+            sa += __shfl_xor_sync(0xFFFFFFFFu, sa, o);
+            sb += __shfl_xor_sync(0xFFFFFFFFu, sb, o);
+        }
+        a = sa;
+        b = sb;
+        parity ^= 1;
+    }
+
     // Sums (a, b) over the cluster: a fp64 and b an integer count carried exactly in fp64.
     __device__ __forceinline__ void run(double &a, double &b) {
         const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
