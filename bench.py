@@ -52,6 +52,9 @@ def parse_args():
                    help="tolerance sweep: throughput and host-traffic statistics per eps")
     p.add_argument("--sketch", choices=["exact", "q2"], default="exact",
                    help="token sketch: exact bf16 keys (the headline) or the 2-bit sketch")
+    p.add_argument("--long128k", action="store_true",
+                   help="the fetch-stressed long-context workload: 128K tokens, batch 4, "
+                        "eta = 1/32, needle sets, eps in {0.02, 0.05}")
     p.add_argument("--pc-sweep", action="store_true",
                    help="PoissonComp throughput: 36 layers x 8 KV heads, n in {32K, 128K}, "
                         "eta in {1/8, 1/16, 1/32}")
@@ -643,6 +646,100 @@ def run_eps_sweep(args, local):
     eng.close()
 
 
+def run_long128k(args, local):
+    """One GPU: the long-context workload with the fetch path stressed (128K tokens, batch 4,
+    8 KV heads x 4 query heads, eta = 1/32, a needle set of 2-25 % of the context per KV head),
+    8 decode queries per step (a query = 128 query heads), for eps in {0.02, 0.05}: throughput,
+    rows fetched, host-link rate and per-kernel times.  One JSON line."""
+    import torch
+
+    from verified_kv_cache_poissoncomp_gb300 import binding as B
+    from verified_kv_cache_poissoncomp_gb300 import inputs as I
+    from verified_kv_cache_poissoncomp_gb300.engine import VerKV, default_cap
+
+    B.lib()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    t0 = time.time()
+    w = I.long_context_128k(n_queries=8)
+    gen_s = time.time() - t0
+    Q = w.queries.shape[0]
+    stream = torch.cuda.Stream(dev)
+    with torch.cuda.stream(stream):
+        eng = VerKV(w.B, w.L, w.h_kv, w.G, w.d, w.n, default_cap(w.n, w.eta),
+                    sketch_format=sketch_format(args))
+        eng.load(w.tau.reshape(-1, w.n), w.kv.reshape(-1, w.n, 2, w.d))
+        eng.compress(w.eta, w.n_sink, w.n_local, w.seed)
+        eng.sync()
+        q_dev = torch.as_tensor(w.queries.view(np.int16)).to(dev)
+        hq = w.B * w.h_kv * w.G
+        o_all = torch.empty((Q, hq, w.d), dtype=torch.float32, device=dev)
+        lse_all = torch.empty((Q, hq), dtype=torch.float32, device=dev)
+        st_all = torch.empty((Q, hq, 16), dtype=torch.int32, device=dev)
+        fc_all = torch.zeros((Q, w.B * w.h_kv), dtype=torch.int32, device=dev)
+    row_bytes = (2 if args.sketch == "exact" else 4) * w.d
+    rows = []
+    for eps in (0.02, 0.05):
+        def step():
+            for t in range(Q):
+                B.verkv_attend_verified(eng.ctx, int(w.query_layer[t]), q_dev[t].data_ptr(),
+                                        eng.pivotal, eng.r_full.data_ptr(), eng.sketch_desc, eps,
+                                        w.delta, None, fc_all[t].data_ptr())
+                B.verkv_fetch_refine(eng.ctx, None, None, eng.host_kv.data_ptr(),
+                                     o_all[t].data_ptr(), lse_all[t].data_ptr(),
+                                     st_all[t].data_ptr())
+
+        with torch.cuda.stream(stream):
+            step()
+            B.verkv_sync(eng.ctx)
+            graph = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(graph, stream=stream):
+                step()
+            for _ in range(args.warmup):
+                graph.replay()
+        torch.cuda.synchronize()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        with torch.cuda.stream(stream):
+            for _ in range(args.steps):
+                graph.replay()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        B.verkv_sync(eng.ctx)
+        ms = e0.elapsed_time(e1) / args.steps
+        B.verkv_profile_enable(eng.ctx, 1)
+        with torch.cuda.stream(stream):
+            step()
+        launches, total_ms = B.verkv_profile_read(eng.ctx)
+        B.verkv_profile_enable(eng.ctx, 0)
+        fr = fc_all.cpu().numpy().astype(np.int64)
+        st = st_all.cpu().numpy()
+        h2d = float(fr.sum(1).mean()) * row_bytes
+        fetch_us = 1e3 * total_ms[B.VERKV_K_FETCH_HOST] / max(launches[B.VERKV_K_FETCH_HOST], 1)
+        rows.append({
+            "eps": eps, "queries_per_s": round(Q / (ms * 1e-3), 2), "ms_per_step": round(ms, 4),
+            "fetched_frac_per_kv_head": {"mean": round(float(fr.mean()) / w.n, 4),
+                                         "min": round(float(fr.min()) / w.n, 4),
+                                         "max": round(float(fr.max()) / w.n, 4)},
+            "certified_frac": round(float(st[..., 10].mean()), 4),
+            "h2d_bytes_per_query": int(h2d), "fetch_GBs": round(h2d / (fetch_us * 1e-6) / 1e9, 1),
+            "per_kernel_us": {B.verkv_kernel_name(k): round(1e3 * total_ms[k] / launches[k], 2)
+                              for k in range(B.VERKV_K_COUNT) if launches[k] > 0},
+            **traffic_stats(st, fr, eng.p_count.cpu().numpy().astype(np.int64), w.n)})
+        del graph
+    print(json.dumps({"workload": "long-128k", "metric": METRIC, "unit": UNIT,
+                      "steps": args.steps, "warmup": args.warmup, "data": "synthetic",
+                      "config": {"workload": "128K tokens, batch 4, 8 KV heads x 4 query heads, "
+                                             "d=128, bf16, eta=1/32, H=4+512, needle sets of "
+                                             "U[2%,25%] of the context per KV head, delta=0.05, "
+                                             f"{Q} decode queries per step", "sketch": args.sketch,
+                                 "graph": True},
+                      "needle_frac_per_kv_head": [round(x, 4) for x in w.meta["needle_frac"].ravel()],
+                      "input_generation_s": round(gen_s, 1), "rows": rows}), flush=True)
+    eng.close()
+
+
 def run_pc_sweep(args, local):
     """One GPU: verkv_poissoncomp (c solve, Poisson sample, compaction, pivotal K/V gather) over
     every head of a 36-layer x 8-KV-head cache per call, for n in {32K, 128K} and eta in
@@ -768,6 +865,9 @@ def main():
     elif args.pc_sweep:
         if rank == 0:
             run_pc_sweep(args, local)
+    elif args.long128k:
+        if rank == 0:
+            run_long128k(args, local)
     else:
         run_ours(args, world, rank, local)
 

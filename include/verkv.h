@@ -281,7 +281,7 @@ verkv_status verkv_certify_noalloc(int device, void *stream, int32_t units, int3
 enum {
     VERKV_K_PC_SOLVE = 0,      /* PoissonComp c solve, r, sample, compaction     */
     VERKV_K_PC_GATHER,         /* pivotal K/V row gather                          */
-    VERKV_K_SKETCH,            /* exact sketch build                              */
+    VERKV_K_SKETCH,            /* sketch build (exact or 2-bit)                   */
     VERKV_K_SCORE,             /* sketch logits for every token and query head    */
     VERKV_K_CERTIFY,           /* beta solve, certificate, selection (Eq. 7-10),
                                   and the per-KV-head fetch id list               */

@@ -79,3 +79,24 @@ def test_noalloc_argument_checks_need_no_gpu(lib):
         bad = list(args)
         bad[i] = v
         assert c(*bad) == B.VERKV_EINVAL, (i, v)
+
+
+def test_kernel_ids_and_names_match_the_header(lib):
+    with open(os.path.join(ROOT, "include", "verkv.h")) as f:
+        text = f.read()
+    body = text[text.index("VERKV_K_PC_SOLVE = 0"):text.index("VERKV_K_COUNT")]
+    ids = re.findall(r"\b(VERKV_K_[A-Z_]+)", body)
+    assert [getattr(B, k) for k in ids] == list(range(len(ids)))
+    assert B.VERKV_K_COUNT == len(ids)
+    assert B.verkv_kernel_name(B.VERKV_K_CERTIFY) == "k_certify"
+    assert B.verkv_kernel_name(B.VERKV_K_COUNT) == ""
+
+
+def test_sketch_bytes(lib):
+    s = B.verkv_shape(2, 3, 8, 4, 128, 32768, 2600)
+    rows = 2 * 3 * 8 * 32768
+    assert B.verkv_sketch_bytes(s, B.VERKV_SKETCH_EXACT) == rows * 256
+    assert B.verkv_sketch_bytes(s, B.VERKV_SKETCH_Q2) == rows * 48
+    s64 = B.verkv_shape(1, 1, 1, 4, 64, 1000, 100)
+    assert B.verkv_sketch_bytes(s64, B.VERKV_SKETCH_Q2) == 1000 * 32
+    assert B.verkv_sketch_bytes(s, 7) == 0

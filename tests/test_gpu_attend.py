@@ -63,6 +63,16 @@ def test_128k_context():
     assert rep["exact_F"] >= 0.9 * rep["heads"]
 
 
+def test_128k_needle_sets_stress_the_fetch():
+    # The long-context workload's generator at reduced width: 128K tokens, eta = 1/32, a needle
+    # set of 2-25 % of the context per KV head; the certificate must fetch much of it.
+    w = I.long_context_128k(B=1, h_kv=2, n_queries=2)
+    rep, outs = _run_all(w)
+    assert rep["exact_F"] >= 0.9 * rep["heads"]
+    fetched = np.array([o["counts"] for o in outs], dtype=np.float64) / w.n
+    assert fetched.mean() > 0.01, fetched
+
+
 def test_memcpy_mode_matches_zerocopy():
     w = I.make_workload("modes", B=1, L=1, h_kv=2, G=4, d=128, n=8192, eta=1 / 8, n_queries=4,
                         plant_every=2)

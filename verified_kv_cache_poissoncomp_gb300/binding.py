@@ -34,7 +34,10 @@ EXPORTED = ["verkv_sketch_bytes", "verkv_workspace_size", "verkv_create", "verkv
             "verkv_profile_read", "verkv_launch_counts", "verkv_kernel_name", "verkv_sync",
             "verkv_last_error", "verkv_status_string", "verkv_certify_noalloc",
             "verkv_attend_dense_host"]
-VERKV_K_COUNT = 11
+# kernel ids (include/verkv.h), in launch order
+(VERKV_K_PC_SOLVE, VERKV_K_PC_GATHER, VERKV_K_SKETCH, VERKV_K_SCORE, VERKV_K_CERTIFY,
+ VERKV_K_PARTIAL_PIVOTAL, VERKV_K_FETCH_HOST, VERKV_K_PARTIAL_STAGED, VERKV_K_MERGE,
+ VERKV_K_DENSE_HOST, VERKV_K_DENSE_MERGE, VERKV_K_COUNT) = range(12)
 
 
 class verkv_shape(ctypes.Structure):

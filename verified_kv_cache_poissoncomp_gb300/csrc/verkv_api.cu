@@ -710,7 +710,7 @@ verkv_status verkv_launch_counts(verkv_ctx *ctx, int64_t *out) {
 
 const char *verkv_kernel_name(int k) {
     static const char *names[VERKV_K_COUNT] = {
-        "k_pc_solve", "k_pc_gather", "k_sketch_exact", "k_score", "k_certify",
+        "k_pc_solve", "k_pc_gather", "k_sketch", "k_score", "k_certify",
         "k_partial(pivotal)", "k_partial(host)", "k_partial(staged)", "k_merge",
         "k_dense_host", "k_dense_merge"};
     return (k >= 0 && k < VERKV_K_COUNT) ? names[k] : "";

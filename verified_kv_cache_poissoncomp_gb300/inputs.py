@@ -202,3 +202,60 @@ def pc_sweep_tau(units, n, data_seed=1239):
         x = rng.lognormal(0.0, 1.5, n)
         tau[u] = (x / x.max()).astype(np.float32)
     return tau
+
+
+def long_context_128k(B=4, L=1, h_kv=8, G=4, d=128, n=131072, eta=1.0 / 32, n_sink=4,
+                      n_local=512, n_queries=8, eps=0.05, delta=0.05, boost=3.0,
+                      p_range=(0.02, 0.25), alpha=4.0, data_seed=1237, philox_seed=0):
+    """Long context with the fetch path stressed (128K tokens, batch 4, eta = 1/32).
+
+    Keys, values, scores and sinks as in make_workload.  In addition every KV head gets a needle
+    set: p n tokens (p ~ U[p_range] per head) at uniform positions outside the forced set, whose
+    keys share a component a u along a random unit direction u of that head; every query adds
+    the same a u, so a needle's logit rises by a^2 / sqrt(d) = boost.  With eta = 1/32 almost all
+    needles are unsampled, so a certificate can only be met by fetching much of the needle set
+    (the fraction actually fetched is measured, not set)."""
+    rng = np.random.default_rng(data_seed)
+    scales = _channel_scales(d, True)
+    a = np.float32(np.sqrt(boost * np.sqrt(d)))
+    tau = np.empty((B, L, h_kv, n), dtype=np.float32)
+    kv = np.empty((B, L, h_kv, n, 2, d), dtype=np.uint16)
+    mus = np.empty((B, L, h_kv, d), dtype=np.float32)
+    us = np.empty((B, L, h_kv, d), dtype=np.float32)
+    pfrac = np.empty((B, L, h_kv), dtype=np.float64)
+    lo, hi = n_sink, n - n_local
+    for b in range(B):
+        for l in range(L):
+            for h in range(h_kv):
+                mu = np.zeros(d, dtype=np.float32)
+                mu[:8] = rng.standard_normal(8, dtype=np.float32)
+                mu /= np.linalg.norm(mu)
+                mus[b, l, h] = mu
+                K = _head_keys(rng, n, d, scales, mu, alpha, 0.5)
+                V = rng.standard_normal((n, d), dtype=np.float32)
+                x = rng.lognormal(0.0, 1.5, n)
+                tau[b, l, h] = (x / x.max()).astype(np.float32)
+                u = rng.standard_normal(d).astype(np.float32)
+                u /= np.linalg.norm(u)
+                us[b, l, h] = u
+                p = rng.uniform(*p_range)
+                pfrac[b, l, h] = p
+                pos = rng.choice(np.arange(lo, hi), size=int(p * (hi - lo)), replace=False)
+                K[pos] += a * u
+                kv[b, l, h, :, 0, :] = f32_to_bf16(K)
+                kv[b, l, h, :, 1, :] = f32_to_bf16(V)
+    Q = n_queries
+    queries = np.empty((Q, B, h_kv * G, d), dtype=np.uint16)
+    query_layer = (np.arange(Q) % L).astype(np.int32)
+    for t in range(Q):
+        l = int(query_layer[t])
+        for b in range(B):
+            for h in range(h_kv):
+                for g in range(G):
+                    q = alpha * mus[b, l, h] + rng.standard_normal(d, dtype=np.float32) + a * us[b, l, h]
+                    queries[t, b, h * G + g] = f32_to_bf16(q)
+    return Workload(name="long-128k", B=B, L=L, h_kv=h_kv, G=G, d=d, n=n, eta=eta,
+                    n_sink=n_sink, n_local=n_local, eps=eps, delta=delta, seed=philox_seed,
+                    tau=tau, kv=kv, queries=queries, query_layer=query_layer,
+                    planted=np.ones(Q, dtype=bool), plant_pos=np.zeros((B, L, h_kv, 0), np.int64),
+                    meta=dict(data_seed=data_seed, boost=boost, needle_frac=pfrac))
