@@ -48,6 +48,10 @@ def lib():
         L.vo_certify.argtypes = [_dp, _fp, _u8p, ctypes.c_int64, ctypes.c_double,
                                  ctypes.c_double, _dp, _i64p, _dp, _dp, _u8p, _i64p, _dp]
         L.vo_certify.restype = ctypes.c_int
+        L.vo_certify_cand.argtypes = [_dp, _fp, _u8p, ctypes.c_int64, ctypes.c_double,
+                                      ctypes.c_double, _u8p, _dp, _i64p, _dp, _dp, _u8p, _i64p,
+                                      _dp, _i64p]
+        L.vo_certify_cand.restype = ctypes.c_int
         L.vo_refine.argtypes = [_dp, _dp, _fp, _u8p, _u8p, _dp, ctypes.c_double,
                                 ctypes.c_int64, ctypes.c_int, _dp]
         L.vo_refine.restype = None
@@ -189,6 +193,49 @@ def certify(s_hat, r32, resident, eps, delta):
                 order=order[:nl], eps_k=eps_k)
 
 
+def certify_cand(s_hat, r32, resident, eps, delta, cand):
+    """KVFetch certificate and selection with only the tokens of L in the mask `cand` fetchable
+    (the shortlist variant; see verkv_oracle.c vo_certify_cand).  Returns certify()'s dict with
+    `order` and `eps_k` over the candidates, plus `exhausted` (every candidate taken and the
+    certificate still not met)."""
+    s_hat = _c(s_hat, np.float64)
+    r32 = _c(r32, np.float32)
+    res = _c(resident, np.uint8)
+    cm = _c(cand, np.uint8)
+    n = s_hat.shape[0]
+    nc = int(np.count_nonzero((r32 < 1.0) & (cm != 0)))
+    scal = np.zeros(8, dtype=np.float64)
+    ints = np.zeros(4, dtype=np.int64)
+    lam = np.zeros(n, dtype=np.float64)
+    g = np.zeros(n, dtype=np.float64)
+    F = np.zeros(n, dtype=np.uint8)
+    order = np.zeros(max(nc, 1), dtype=np.int64)
+    eps_k = np.zeros(nc + 1, dtype=np.float64)
+    exh = np.zeros(1, dtype=np.int64)
+    st = lib().vo_certify_cand(_ptr(s_hat, _dp), _ptr(r32, _fp), _ptr(res, _u8p), n, float(eps),
+                               float(delta), _ptr(cm, _u8p), _ptr(scal, _dp), _ptr(ints, _i64p),
+                               _ptr(lam, _dp), _ptr(g, _dp), _ptr(F, _u8p), _ptr(order, _i64p),
+                               _ptr(eps_k, _dp), _ptr(exh, _i64p))
+    if st != VO_OK:
+        raise OracleError(f"vo_certify_cand status {st}")
+    return dict(m=scal[0], D=scal[1], beta=scal[2], V=scal[3], b=scal[4], l_delta=scal[5],
+                eps_L=scal[6], eps_final=scal[7], certified=bool(ints[0]), k_star=int(ints[1]),
+                n_L=int(ints[2]), n_fetch=int(ints[3]), lam=lam, g=g, F=F.astype(bool),
+                order=order[:nc], eps_k=eps_k, exhausted=bool(exh[0]))
+
+
+def shortlist(s_hat_heads, r32, size):
+    """The per-KV-head shortlist (our reading of the pages' "128-token shortlist per KV head"):
+    the `size` tokens of L (r < 1) with the largest sketch logit over the KV head's query heads,
+    ties to the lower token id.  s_hat_heads [G][n] -> bool mask [n]."""
+    key = np.max(np.asarray(s_hat_heads, dtype=np.float64), axis=0)
+    L = np.nonzero(np.asarray(r32) < 1.0)[0]
+    order = L[np.lexsort((L, -key[L]))]  # key descending, then id ascending
+    mask = np.zeros(key.shape[0], dtype=bool)
+    mask[order[:size]] = True
+    return mask
+
+
 def refine(s, values, r32, resident, F, lam, m):
     """Returned estimator after fetching: dict(D_hat, M2, lse, N_hat[d], o[d])."""
     s = _c(s, np.float64)
@@ -206,8 +253,12 @@ def refine(s, values, r32, resident, F, lam, m):
 
 
 # ------------------------------------------------------------------------------------------------
-def attend_unit(q_heads, sketch_keys, keys, values, r32, resident, eps, delta):
+def attend_unit(q_heads, sketch_keys, keys, values, r32, resident, eps, delta, shortlist_size=0,
+                cand=None):
     """KVFetch + refine for one KV head shared by G query heads (GQA).
+
+    shortlist_size > 0 restricts what may be fetched to the KV head's shortlist (shortlist());
+    `cand` gives that mask directly instead (e.g. the GPU's, to compare the rest given it).
 
     q_heads [G][d], sketch_keys [n][d] (the sketch; equal to keys for the exact sketch),
     keys/values [n][d] (the full cache), all fp64.  Each query head certifies and fetches on its
@@ -217,11 +268,16 @@ def attend_unit(q_heads, sketch_keys, keys, values, r32, resident, eps, delta):
     """
     heads = []
     union = np.zeros(keys.shape[0], dtype=bool)
-    for q in q_heads:
-        s_hat = logits(q, sketch_keys)
-        cert = certify(s_hat, r32, resident, eps, delta)
+    s_hats = [logits(q, sketch_keys) for q in q_heads]
+    if cand is None and shortlist_size > 0:
+        cand = shortlist(s_hats, r32, shortlist_size)
+    for q, s_hat in zip(q_heads, s_hats):
+        if cand is None:
+            cert = certify(s_hat, r32, resident, eps, delta)
+        else:
+            cert = certify_cand(s_hat, r32, resident, eps, delta, cand)
         s = s_hat if sketch_keys is keys else logits(q, keys)
         est = refine(s, values, r32, resident, cert["F"], cert["lam"], cert["m"])
         union |= cert["F"] & ~np.asarray(resident, dtype=bool)
         heads.append(dict(cert=cert, est=est))
-    return dict(heads=heads, fetch_ids=np.nonzero(union)[0].astype(np.int64))
+    return dict(heads=heads, fetch_ids=np.nonzero(union)[0].astype(np.int64), cand=cand)

@@ -476,10 +476,16 @@ static int cmp_gkey(const void *a, const void *b)
  *   ints[4]  = certified, k*, |L|, |F \ S|
  *   lambda[n] (1 outside L), g[n] (0 outside L), F[n] (1 for the k* fetched tokens of L),
  *   order[|L|] (token ids in Eq. (10) order; may be NULL),
- *   eps_k[|L|+1] (eps_hat(L_g[k:]) for every k; may be NULL). */
-int vo_certify(const double *s_hat, const float *r32, const uint8_t *resident, int64_t n,
-               double eps, double delta, double *scal, int64_t *ints, double *lambda, double *g,
-               uint8_t *F, int64_t *order, double *eps_k)
+ *   eps_k[|L|+1] (eps_hat(L_g[k:]) for every k; may be NULL).
+ *
+ * With a candidate mask cand (vo_certify_cand), only tokens of L with cand[i] may be fetched:
+ * the order of Eq. (10) runs over L n cand and every other token of L stays in the remaining set;
+ * order and eps_k then cover the candidates only, and if even all of them leave eps-hat >= eps,
+ * k* is their number and *exhausted is set (the certificate is not met). */
+static int certify_core(const double *s_hat, const float *r32, const uint8_t *resident, int64_t n,
+                        double eps, double delta, double *scal, int64_t *ints, double *lambda,
+                        double *g, uint8_t *F, int64_t *order, double *eps_k, const uint8_t *cand,
+                        int64_t *exhausted)
 {
     if (n <= 0 || !(delta > 0.0) || !(delta < 1.0) || !(eps > 0.0))
         return VO_EINVAL;
@@ -568,22 +574,35 @@ int vo_certify(const double *s_hat, const float *r32, const uint8_t *resident, i
                  (den > 0.0 ? ((A - A2) * (A + A2) + 2.0 * vi[i] * l) / den : 0.0);
         }
         g[i] = gD / D;
+        if (cand && !cand[i])
+            continue;
         keys[k].g = g[i];
         keys[k].id = i;
         ++k;
     }
-    qsort(keys, (size_t)nl, sizeof(vo_gkey), cmp_gkey);
+    const int64_t nc = k; /* tokens the order runs over: L, or L n cand */
+    qsort(keys, (size_t)nc, sizeof(vo_gkey), cmp_gkey);
+    /* Tokens of L outside the candidates always remain. */
+    double base_beta = 0.0, base_var = 0.0, base_bmax = 0.0;
+    if (cand)
+        for (int64_t i = 0; i < n; ++i)
+            if ((double)r32[i] < 1.0 && !cand[i]) {
+                base_beta += ci[i];
+                base_var += vi[i];
+                if (bi[i] > base_bmax)
+                    base_bmax = bi[i];
+            }
 
     /* Eq. (10): eps_hat(L_g[k:]) from suffix sums along the order; nonincreasing in k and 0 at
      * k = |L|.  k* = 0 when certified, else the first k >= 1 below eps. */
-    double s_beta = 0.0, s_var = 0.0, s_bmax = 0.0;
-    double *ek = (double *)malloc(sizeof(double) * (size_t)(nl + 1));
+    double s_beta = base_beta, s_var = base_var, s_bmax = base_bmax;
+    double *ek = (double *)malloc(sizeof(double) * (size_t)(nc + 1));
     if (!ek) {
         free(w); free(bi); free(vi); free(ci); free(keys);
         return VO_ENOMEM;
     }
-    ek[nl] = 0.0;
-    for (int64_t j = nl - 1; j >= 0; --j) {
+    ek[nc] = cand ? (s_beta + bernstein(s_bmax, s_var, l)) / D : 0.0;
+    for (int64_t j = nc - 1; j >= 0; --j) {
         const int64_t i = keys[j].id;
         s_beta += ci[i];
         s_var += vi[i];
@@ -592,14 +611,18 @@ int vo_certify(const double *s_hat, const float *r32, const uint8_t *resident, i
         ek[j] = (s_beta + bernstein(s_bmax, s_var, l)) / D;
     }
     int64_t kstar = 0;
+    int64_t exh = 0;
     if (!certified) {
-        kstar = nl;
-        for (int64_t j = 1; j <= nl; ++j)
+        kstar = nc;
+        for (int64_t j = 1; j <= nc; ++j)
             if (ek[j] < eps) {
                 kstar = j;
                 break;
             }
+        exh = !(ek[kstar] < eps);
     }
+    if (exhausted)
+        *exhausted = exh;
     int64_t nfetch = 0;
     for (int64_t j = 0; j < kstar; ++j) {
         const int64_t i = keys[j].id;
@@ -607,10 +630,10 @@ int vo_certify(const double *s_hat, const float *r32, const uint8_t *resident, i
         nfetch += !resident[i];
     }
     if (order)
-        for (int64_t j = 0; j < nl; ++j)
+        for (int64_t j = 0; j < nc; ++j)
             order[j] = keys[j].id;
     if (eps_k)
-        for (int64_t j = 0; j <= nl; ++j)
+        for (int64_t j = 0; j <= nc; ++j)
             eps_k[j] = ek[j];
 
     scal[0] = m;
@@ -629,6 +652,23 @@ int vo_certify(const double *s_hat, const float *r32, const uint8_t *resident, i
     free(ek);
     free(w); free(bi); free(vi); free(ci); free(keys);
     return VO_OK;
+}
+
+int vo_certify(const double *s_hat, const float *r32, const uint8_t *resident, int64_t n,
+               double eps, double delta, double *scal, int64_t *ints, double *lambda, double *g,
+               uint8_t *F, int64_t *order, double *eps_k)
+{
+    return certify_core(s_hat, r32, resident, n, eps, delta, scal, ints, lambda, g, F, order,
+                        eps_k, NULL, NULL);
+}
+
+int vo_certify_cand(const double *s_hat, const float *r32, const uint8_t *resident, int64_t n,
+                    double eps, double delta, const uint8_t *cand, double *scal, int64_t *ints,
+                    double *lambda, double *g, uint8_t *F, int64_t *order, double *eps_k,
+                    int64_t *exhausted)
+{
+    return certify_core(s_hat, r32, resident, n, eps, delta, scal, ints, lambda, g, F, order,
+                        eps_k, cand, exhausted);
 }
 
 /* ------------------------------------------------------------------------------------------- */
