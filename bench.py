@@ -50,6 +50,8 @@ def parse_args():
     p.add_argument("--queries", type=int, default=QUERIES)
     p.add_argument("--eps-sweep", action="store_true",
                    help="tolerance sweep: throughput and host-traffic statistics per eps")
+    p.add_argument("--shortlist", type=int, default=0,
+                   help="shortlist variant: at most this many fetch candidates per KV head (0: off)")
     p.add_argument("--sketch", choices=["exact", "q2"], default="exact",
                    help="token sketch: exact bf16 keys (the headline) or the 2-bit sketch")
     p.add_argument("--long128k", action="store_true",
@@ -276,6 +278,8 @@ def run_ours(args, world, rank, local):
         eng.load(w.tau.reshape(-1, w.n), w.kv.reshape(-1, w.n, 2, w.d))
         eng.compress(w.eta, w.n_sink, w.n_local, w.seed)   # also builds the sketch
         eng.sync()
+        if args.shortlist:
+            eng.set_shortlist(args.shortlist)
         q_dev = torch.as_tensor(w.queries.view(np.int16)).to(dev)          # [Q][1][32][128]
         hq = w.B * w.h_kv * w.G
         o_all = torch.empty((Q, hq, w.d), dtype=torch.float32, device=dev)
@@ -475,6 +479,7 @@ def run_ours(args, world, rank, local):
                                       "query t on instance t mod 4",
                           "l2": "inputs larger than L2 (4 x 73 MiB resident state per step)",
                           "fetch": args.fetch_mode, "sketch": args.sketch,
+                          "shortlist": args.shortlist,
                           "graph": graph is not None,
                           "parallelism": f"replicas x{world}"},
                "roofline": roof, "roofline_hbm": roof_hbm, "rooflines": rooflines,
@@ -512,6 +517,7 @@ def traffic_stats(st, fetched_rows, pivotal_count, n):
     resident = float(pivotal_count.mean()) / n
     return {
         "decisions_fetching_frac": float(fetching.mean()),
+        "shortlist_exhausted_frac": float(((st[..., 15] & 4) != 0).mean()),
         "context_frac_per_fetching_decision":
             float((nfetch[fetching] / n).mean()) if fetching.any() else 0.0,
         "overall_read_frac": resident + float((nfetch / n).mean()),
@@ -582,6 +588,8 @@ def run_eps_sweep(args, local):
         eng.load(w.tau.reshape(-1, w.n), w.kv.reshape(-1, w.n, 2, w.d))
         eng.compress(w.eta, w.n_sink, w.n_local, w.seed)
         eng.sync()
+        if args.shortlist:
+            eng.set_shortlist(args.shortlist)
         q_dev = torch.as_tensor(w.queries.view(np.int16)).to(dev)
         hq = w.B * w.h_kv * w.G
         o_all = torch.empty((Q, hq, w.d), dtype=torch.float32, device=dev)
@@ -640,7 +648,7 @@ def run_eps_sweep(args, local):
                       "steps": args.steps, "warmup": args.warmup, "data": "synthetic",
                       "config": {"workload": "single-layer 32K (the bench workload), "
                                              f"{Q} decode queries per step", "fetch": "zerocopy",
-                                 "sketch": args.sketch,
+                                 "sketch": args.sketch, "shortlist": args.shortlist,
                                  "graph": True},
                       "rows": rows}), flush=True)
     eng.close()

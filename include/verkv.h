@@ -131,7 +131,8 @@ enum { VERKV_FETCH_ZEROCOPY = 0, VERKV_FETCH_MEMCPY = 1, VERKV_FETCH_KEYS = 4 };
  *   n_L        |L|
  *   n_fetch    |F \ S| for this head (rows not already resident)
  *   iters      iterations of the beta solve
- *   flags      nonzero if the beta solve hit its cap */
+ *   flags      or of: 1 the beta solve hit its cap; 2 the select ran out of passes;
+ *              4 (shortlist variant only) the whole shortlist left eps-hat >= eps */
 typedef struct {
     float m, D, beta, V, b, eps_hat, eps_final, D_hat, M2, lse;
     int32_t certified, k_star, n_L, n_fetch, iters, flags;
@@ -218,6 +219,21 @@ verkv_status verkv_fetch_refine(verkv_ctx *ctx, const int32_t *ids, const int32_
                                 const void *host_kv, float *o_out, float *lse_out,
                                 verkv_head_stats *stats_out);
 
+/* Shortlist variant (summary page, Experimental Setup: "128-token shortlist per KV head"; the
+ * pages give it no further role, so this is our reading).  With size S in 1 .. 256, each later
+ * verkv_attend_verified first picks, per KV head, the S tokens of L with the largest sketch
+ * logit over the KV head's query heads (ties to the lower token id), and a query head whose
+ * certificate fails may fetch only those: the order of Eq. (10) runs over the shortlist while
+ * every other token of L stays in the remaining set.  If the whole shortlist still leaves
+ * eps-hat >= eps, all of it is fetched and the head's stats flags include 4 (the returned
+ * estimator is then not certified).  S = 0 (the default) turns it off.  VERKV_EINVAL otherwise. */
+verkv_status verkv_set_shortlist(verkv_ctx *ctx, int32_t size);
+
+/* Copy the shortlists of the preceding verkv_attend_verified into `out`, device or page-locked
+ * host uint32 [batch * kv_heads][ceil(n/32)] (bit i%32 of word i/32 set iff token i is listed).
+ * Stream-ordered; VERKV_ESTATE if no attend with the shortlist on has run on this context. */
+verkv_status verkv_shortlist_bitmap(verkv_ctx *ctx, uint32_t *out);
+
 /* The offloaded-dense baseline (summary page, System Performance: the "Dense (offload)" system
  * VerKV is compared with): exact attention for every query head of `layer` over all n tokens,
  * every K|V row read from the page-locked host cache -- nothing of the cache is resident.
@@ -291,6 +307,7 @@ enum {
     VERKV_K_MERGE,             /* merge partials into o, lse and statistics       */
     VERKV_K_DENSE_HOST,        /* offloaded-dense baseline: all rows from host    */
     VERKV_K_DENSE_MERGE,       /* its running-max merge                           */
+    VERKV_K_SHORTLIST,         /* per-KV-head fetch shortlist (when enabled)      */
     VERKV_K_COUNT
 };
 

@@ -89,8 +89,9 @@ def gpu_query(eng, w, t, eps=None, delta=None):
                 ids=eng.fetch_ids.cpu().numpy().copy(), counts=eng.fetch_counts.cpu().numpy().copy())
 
 
-def oracle_query(w, t, pcs, eps=None, delta=None, sketches=None):
-    """sketches: None for the exact sketch, else {(b, l, h): dequantised sketch keys}."""
+def oracle_query(w, t, pcs, eps=None, delta=None, sketches=None, cands=None):
+    """sketches: None for the exact sketch, else {(b, l, h): dequantised sketch keys}.
+    cands: None, or {(b, h): bool mask} of fetch candidates (the shortlist variant)."""
     eps = w.eps if eps is None else eps
     delta = w.delta if delta is None else delta
     l = int(w.query_layer[t])
@@ -102,7 +103,9 @@ def oracle_query(w, t, pcs, eps=None, delta=None, sketches=None):
             V = O.bf16_to_f64(w.kv[b, l, h, :, 1, :])
             Ks = K if sketches is None else sketches[(b, l, h)]
             qs = O.bf16_to_f64(w.queries[t, b, h * w.G:(h + 1) * w.G])
-            units.append(O.attend_unit(qs, Ks, K, V, pc["r32"], pc["resident"], eps, delta))
+            cm = None if cands is None else cands[(b, h)]
+            units.append(O.attend_unit(qs, Ks, K, V, pc["r32"], pc["resident"], eps, delta,
+                                       cand=cm))
     return units
 
 
@@ -146,7 +149,16 @@ def compare_query(g, units, w, eps=None, report=None):
             k = int(st["k_star"][qh])
             assert int(Fg.sum()) == k, (qh, int(Fg.sum()), k)
             ek = cert["eps_k"]
-            if not gcert:
+            gexh = bool(st["flags"][qh] & 4)
+            if not gcert and (gexh or cert.get("exhausted")):
+                # shortlist variant: the whole shortlist taken without meeting eps on one side is
+                # allowed only within the tie window on the other
+                nc = len(cert["order"])
+                if gexh:
+                    assert k == nc and ek[nc] >= eps * (1 - EPS_TIE), (qh, k, nc, ek[nc])
+                else:
+                    assert k >= 1 and ek[k] < eps * (1 + EPS_TIE), (qh, k, ek[k])
+            elif not gcert:
                 assert k >= 1 and ek[k] < eps * (1 + EPS_TIE) and ek[k - 1] >= eps * (1 - EPS_TIE), \
                     (qh, k, cert["k_star"], ek[max(k - 1, 0)], ek[k])
             else:

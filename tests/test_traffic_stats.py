@@ -20,3 +20,6 @@ def test_traffic_stats_on_a_hand_made_case():
     assert np.isclose(s["resident_frac"], 75 / n)
     assert np.isclose(s["overall_read_frac"], 75 / n + (150 + 40) / 8 / n)
     assert np.isclose(s["kv_head_transfer_frac"], 160 / 4 / n)
+    assert s["shortlist_exhausted_frac"] == 0.0
+    st[1, 0, 15] = 4
+    assert bench.traffic_stats(st, fetched, counts, n)["shortlist_exhausted_frac"] == 1 / 8

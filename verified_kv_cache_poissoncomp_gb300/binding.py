@@ -33,11 +33,11 @@ EXPORTED = ["verkv_sketch_bytes", "verkv_workspace_size", "verkv_create", "verkv
             "verkv_fetch_refine", "verkv_selection_bitmap", "verkv_profile_enable",
             "verkv_profile_read", "verkv_launch_counts", "verkv_kernel_name", "verkv_sync",
             "verkv_last_error", "verkv_status_string", "verkv_certify_noalloc",
-            "verkv_attend_dense_host"]
+            "verkv_attend_dense_host", "verkv_set_shortlist", "verkv_shortlist_bitmap"]
 # kernel ids (include/verkv.h), in launch order
 (VERKV_K_PC_SOLVE, VERKV_K_PC_GATHER, VERKV_K_SKETCH, VERKV_K_SCORE, VERKV_K_CERTIFY,
  VERKV_K_PARTIAL_PIVOTAL, VERKV_K_FETCH_HOST, VERKV_K_PARTIAL_STAGED, VERKV_K_MERGE,
- VERKV_K_DENSE_HOST, VERKV_K_DENSE_MERGE, VERKV_K_COUNT) = range(12)
+ VERKV_K_DENSE_HOST, VERKV_K_DENSE_MERGE, VERKV_K_SHORTLIST, VERKV_K_COUNT) = range(13)
 
 
 class verkv_shape(ctypes.Structure):
@@ -112,6 +112,10 @@ def lib():
         L.verkv_attend_verified.restype = ctypes.c_int
         L.verkv_fetch_refine.argtypes = [vp, vp, vp, vp, vp, vp, vp]
         L.verkv_fetch_refine.restype = ctypes.c_int
+        L.verkv_shortlist_bitmap.argtypes = [vp, vp]
+        L.verkv_shortlist_bitmap.restype = ctypes.c_int
+        L.verkv_set_shortlist.argtypes = [vp, i32]
+        L.verkv_set_shortlist.restype = ctypes.c_int
         L.verkv_attend_dense_host.argtypes = [vp, i32, vp, vp, vp, vp]
         L.verkv_attend_dense_host.restype = ctypes.c_int
         L.verkv_selection_bitmap.argtypes = [vp, vp]
@@ -192,6 +196,14 @@ def verkv_attend_verified(ctx, layer, q, pivotal, r_full, sketch, eps, delta,
 
 def verkv_fetch_refine(ctx, ids, counts, host_kv, o_out, lse_out=None, stats_out=None):
     _check(lib().verkv_fetch_refine(ctx, ids, counts, host_kv, o_out, lse_out, stats_out), ctx)
+
+
+def verkv_set_shortlist(ctx, size):
+    _check(lib().verkv_set_shortlist(ctx, int(size)), ctx)
+
+
+def verkv_shortlist_bitmap(ctx, out):
+    _check(lib().verkv_shortlist_bitmap(ctx, out), ctx)
 
 
 def verkv_attend_dense_host(ctx, layer, q, host_kv, o_out, lse_out=None):

@@ -152,6 +152,24 @@ __device__ __forceinline__ void token_terms(float w, float r, float rho, float b
     bb = t * fmaxf(1.0f, inv_rho);
 }
 
+// g_i D of Eq. (9) in the rationalised form, as the bits of a non-negative float.
+__device__ __forceinline__ uint32_t g_bits(float bi, float vi, bool is_argmax, float A, float Rr,
+                                           float b2, float VL, float l) {
+    const float Vr = fmaxf(VL - vi, 0.0f);
+    float gD;
+    if (!is_argmax) {
+        const float den = Rr + sqrt_approx(fmaf(A, A, 2.0f * Vr * l));
+        gD = bi + (den > 0.0f ? __fdividef(2.0f * vi * l, den) : 0.0f);
+    } else {
+        const float A2 = b2 * l * (1.0f / 3.0f);
+        const float R2 = sqrt_approx(fmaf(A2, A2, 2.0f * Vr * l));
+        const float den = Rr + R2;
+        gD = bi + (A - A2) +
+             (den > 0.0f ? __fdividef(fmaf(A - A2, A + A2, 2.0f * vi * l), den) : 0.0f);
+    }
+    return __float_as_uint(fmaxf(gD, 0.0f));
+}
+
 __device__ __forceinline__ unsigned long long key64(uint32_t gbits, int token) {
     return ((unsigned long long)gbits << 24) | (unsigned long long)(0xFFFFFF - token);
 }
@@ -451,7 +469,7 @@ __device__ __forceinline__ void fetch_list_tail(const CertifyArgs &a, int ul, in
     }
 }
 
-template <int CL>
+template <int CL, bool SL>
 __global__ void __launch_bounds__(CT_NT, 1) k_certify(CertifyArgs a) {
     extern __shared__ __align__(16) unsigned char smem_raw[];
     float *wrec = reinterpret_cast<float *>(smem_raw);
@@ -645,7 +663,103 @@ __global__ void __launch_bounds__(CT_NT, 1) k_certify(CertifyArgs a) {
     int kstar = 0;
     unsigned long long fthr = ~0ull;  // F = { L tokens with key >= fthr }
     float eps_final = eps_hat;
-    if (!certified) {
+    bool exhausted = false;
+    if constexpr (SL) if (!certified) {
+        // Only the KV head's shortlist may be fetched.  Candidates (at most SHORTLIST_MAX) carry
+        // their key and Lemma 1 terms into a list in rank 0 (the histogram region is free here);
+        // every other token of L stays in the remaining set (its sums all-reduced).  Rank 0 ranks
+        // the list by key and scans it from the end for the first k with eps-hat < eps; the cut
+        // key is sent back to every CTA.
+        struct Cand {
+            unsigned long long key;
+            float bi, vi, bb, pad;
+        };
+        __shared__ int s_nc, s_kstar, s_exh;
+        __shared__ unsigned long long s_fthr;
+        __shared__ float s_efin;
+        Cand *list = reinterpret_cast<Cand *>(hist);                 // [SHORTLIST_MAX]
+        int *rank_of = reinterpret_cast<int *>(list + SHORTLIST_MAX);  // sorted position -> entry
+        const float A = b1 * l * (1.0f / 3.0f);
+        const float Rr = sqrtf(fmaf(A, A, 2.0f * VL * l));
+        const uint32_t *sl = a.shortlist + (size_t)ul * a.W;
+        if (tid == 0) s_nc = 0;
+        cluster.sync();  // rank 0's counter is zero before anyone appends
+        int *cnt0 = cluster.map_shared_rank(&s_nc, 0);
+        Cand *list0 = cluster.map_shared_rank(list, 0);
+        float osb = 0.0f, osv = 0.0f, obm = 0.0f;
+        for (int i = tid; i < chunk; i += CT_NT) {
+            const float r = R[i];
+            if (r < 1.0f) {
+                const int t = base + i;
+                float bi, vi, bb;
+                token_terms(W[i], r, __uint_as_float(X[i]), beta, bi, vi, bb);
+                if ((sl[t >> 5] >> (t & 31)) & 1u) {
+                    const uint32_t g = g_bits(bi, vi, t == id1 && b2 != b1, A, Rr, b2, VL, l);
+                    X[i] = g;
+                    const int slot = atomicAdd(cnt0, 1);
+                    if (slot < SHORTLIST_MAX) list0[slot] = Cand{key64(g, t), bi, vi, bb, 0.0f};
+                } else {
+                    X[i] = 0u;
+                    osb += bi;
+                    osv += vi;
+                    obm = fmaxf(obm, bb);
+                }
+            }
+        }
+        float rec[3] = {warp_sum(osb), warp_sum(osv), warp_max(obm)};
+        cluster_allreduce<CL>(rec, wrec, xrec, parity, [](float (&x)[3], const float (&y)[3]) {
+            x[0] += y[0];
+            x[1] += y[1];
+            x[2] = fmaxf(x[2], y[2]);
+        });
+        if (crank == 0) {
+            const int nc = min(s_nc, SHORTLIST_MAX);
+            for (int j = tid; j < nc; j += CT_NT) {  // keys are unique: ranks are a permutation
+                const unsigned long long kj = list[j].key;
+                int rk = 0;
+                for (int q = 0; q < nc; ++q) rk += list[q].key > kj ? 1 : 0;
+                rank_of[rk] = j;
+            }
+            __syncthreads();
+            if (tid == 0) {
+                float sbv = rec[0], svv = rec[1], smx = rec[2];
+                float ek_next = (sbv + bern(smx, svv, l)) / D;  // eps-hat with every candidate taken
+                int kk = -1;
+                float efin = ek_next;
+                // eps-hat(k) for k = nc .. 1; k* is the smallest k >= 1 with eps-hat(k) < eps
+                for (int k = nc; k >= 1; --k) {
+                    if (ek_next < eps) {
+                        kk = k;
+                        efin = ek_next;
+                    }
+                    const Cand &cd = list[rank_of[k - 1]];
+                    sbv += cd.bi;
+                    svv += cd.vi;
+                    smx = fmaxf(smx, cd.bb);
+                    ek_next = (sbv + bern(smx, svv, l)) / D;
+                }
+                const bool exh = kk < 0;
+                if (exh) {
+                    kk = nc;
+                    efin = (rec[0] + bern(rec[2], rec[1], l)) / D;
+                }
+                const unsigned long long ft = kk >= 1 ? list[rank_of[kk - 1]].key : ~0ull;
+                for (int c2 = 0; c2 < CL; ++c2) {
+                    *cluster.map_shared_rank(&s_fthr, c2) = ft;
+                    *cluster.map_shared_rank(&s_kstar, c2) = kk;
+                    *cluster.map_shared_rank(&s_exh, c2) = exh ? 1 : 0;
+                    *cluster.map_shared_rank(&s_efin, c2) = efin;
+                }
+            }
+        }
+        cluster.sync();
+        fthr = s_fthr;
+        kstar = s_kstar;
+        exhausted = s_exh != 0;
+        eps_final = s_efin;
+        if (s_nc > SHORTLIST_MAX) flags |= 2;  // more candidates than the list holds
+    }
+    if constexpr (!SL) if (!certified) {
         const float A = b1 * l * (1.0f / 3.0f);
         const float Rr = sqrtf(fmaf(A, A, 2.0f * VL * l));
         // Fixed-point scales: every partial sum is at most the whole, which maps to 2^49 (a scale
@@ -685,19 +799,8 @@ __global__ void __launch_bounds__(CT_NT, 1) k_certify(CertifyArgs a) {
                     unsigned long long k;
                     if (pass == 0) {  // the g key (Eq. (9), rationalised) of every token of L
                         token_terms(W[i], r, __uint_as_float(X[i]), beta, bi, vi, bb);
-                        const float Vr = fmaxf(VL - vi, 0.0f);
-                        float gD;
-                        if (base + i != id1 || b2 == b1) {
-                            const float den = Rr + sqrt_approx(fmaf(A, A, 2.0f * Vr * l));
-                            gD = bi + (den > 0.0f ? __fdividef(2.0f * vi * l, den) : 0.0f);
-                        } else {
-                            const float A2 = b2 * l * (1.0f / 3.0f);
-                            const float R2 = sqrt_approx(fmaf(A2, A2, 2.0f * Vr * l));
-                            const float den = Rr + R2;
-                            gD = bi + (A - A2) +
-                                 (den > 0.0f ? __fdividef(fmaf(A - A2, A + A2, 2.0f * vi * l), den) : 0.0f);
-                        }
-                        const uint32_t g = __float_as_uint(fmaxf(gD, 0.0f));
+                        const uint32_t g = g_bits(bi, vi, base + i == id1 && b2 != b1, A, Rr, b2,
+                                                  VL, l);
                         X[i] = g;
                         k = key64(g, base + i);
                     } else {
@@ -795,7 +898,13 @@ __global__ void __launch_bounds__(CT_NT, 1) k_certify(CertifyArgs a) {
     for (int w = warp; w < chunk / 32; w += CT_NW) {
         const int i = 32 * w + lane;
         bool inF = false;
-        if (!certified && R[i] < 1.0f) inF = key64(X[i], base + i) >= fthr;
+        if (!certified && R[i] < 1.0f) {
+            inF = key64(X[i], base + i) >= fthr;
+            if constexpr (SL) {
+                const int t = base + i;
+                inF = inF && t < a.n && ((a.shortlist[(size_t)ul * a.W + (t >> 5)] >> (t & 31)) & 1u);
+            }
+        }
         const uint32_t word = __ballot_sync(0xFFFFFFFFu, inF);
         const int gw = base / 32 + w;
         if (lane == 0 && gw < a.W) Fq[gw] = word;
@@ -817,18 +926,18 @@ __global__ void __launch_bounds__(CT_NT, 1) k_certify(CertifyArgs a) {
         st.n_L = (int)nL;
         st.n_fetch = 0;
         st.iters = iters;
-        st.flags = flags;
+        st.flags = flags | (exhausted ? 4 : 0);
         a.qstats[qh] = st;
         if (flags) raise_error(a.err, ERR_NOCONVERGE);
     }
     if (a.fl_counter) fetch_list_tail<CL>(a, ul, ug);
 }
 
-template <int CL>
+template <int CL, bool SL>
 static cudaError_t launch_certify_cl(const CertifyArgs &a, int qheads, size_t smem, cudaStream_t s) {
     static size_t configured = 0;
     if (smem > configured) {
-        cudaError_t e = cudaFuncSetAttribute(k_certify<CL>,
+        cudaError_t e = cudaFuncSetAttribute(k_certify<CL, SL>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return e;
         configured = smem;
@@ -845,16 +954,179 @@ static cudaError_t launch_certify_cl(const CertifyArgs &a, int qheads, size_t sm
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, k_certify<CL>, a);
+    return cudaLaunchKernelEx(&cfg, k_certify<CL, SL>, a);
 }
 
 cudaError_t launch_certify(const CertifyArgs &a, int qheads, size_t smem, cudaStream_t s) {
+    const bool sl = a.shortlist != nullptr;
     switch (a.cl) {
-        case 1: return launch_certify_cl<1>(a, qheads, smem, s);
-        case 4: return launch_certify_cl<4>(a, qheads, smem, s);
-        case CT_MAX_CL: return launch_certify_cl<CT_MAX_CL>(a, qheads, smem, s);
+        case 1: return sl ? launch_certify_cl<1, true>(a, qheads, smem, s)
+                          : launch_certify_cl<1, false>(a, qheads, smem, s);
+        case 4: return sl ? launch_certify_cl<4, true>(a, qheads, smem, s)
+                          : launch_certify_cl<4, false>(a, qheads, smem, s);
+        case CT_MAX_CL: return sl ? launch_certify_cl<CT_MAX_CL, true>(a, qheads, smem, s)
+                                  : launch_certify_cl<CT_MAX_CL, false>(a, qheads, smem, s);
         default: return cudaErrorInvalidValue;
     }
+}
+
+// ---------------------------------------------------------------------------------------------
+// k_shortlist: one CTA per KV head.  A token of L gets the order-preserving 32-bit image of its
+// largest sketch logit over the G query heads (0 for tokens outside L; kept in shared memory
+// between passes when the unit's keys fit, recomputed otherwise); a most-significant-digit
+// radix select (12, 12 and 8 bits, each pass a 4096-bin shared histogram over the tokens that
+// still match the prefix) finds the size-th largest value T and how many tokens equal to T are
+// still needed; a last pass in token order keeps every token above T and the lowest ids equal to
+// T, writing the bitmap one warp word at a time.
+constexpr int SL_NT = 1024;
+
+__device__ __forceinline__ uint32_t order_key(float x) {
+    const uint32_t b = __float_as_uint(x);
+    return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+}
+
+template <bool CACHED>
+__global__ void __launch_bounds__(SL_NT, 1) k_shortlist(ShortlistArgs a) {
+    extern __shared__ uint32_t s_ord[];  // CACHED: the order key of every token of the unit
+    __shared__ uint32_t hist[4096];
+    __shared__ uint32_t s_prefix, s_need, s_eq, s_nl;
+    __shared__ int s_wcnt[SL_NT / 32];
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int ul = blockIdx.x;
+    const int ug = a.li.unit_global(ul);
+    const int G = a.li.G, n = a.n;
+    const float *rf = a.r_full + (size_t)ug * n;
+    const float *sc = a.scores + (size_t)ul * G * n;
+    auto ord_load = [&](int t) -> uint32_t {
+        if (!(rf[t] < 1.0f)) return 0u;
+        float m = sc[t];
+        for (int g = 1; g < G; ++g) m = fmaxf(m, sc[(size_t)g * n + t]);
+        return order_key(m);
+    };
+    if constexpr (CACHED) {
+#pragma unroll 8
+        for (int t = tid; t < n; t += SL_NT) s_ord[t] = ord_load(t);
+    }
+    auto ord = [&](int t) -> uint32_t {
+        if constexpr (CACHED) return s_ord[t];
+        else return ord_load(t);
+    };
+    if (tid == 0) {
+        s_prefix = 0u;
+        s_need = (uint32_t)a.size;
+        s_nl = 0u;
+    }
+    // |L|: when it does not exceed the size, the whole of L is the shortlist
+    uint32_t cl = 0u;
+    for (int t = tid; t < n; t += SL_NT) cl += ord(t) != 0u ? 1u : 0u;
+    cl = warp_sum(cl);
+    __syncthreads();
+    if (lane == 0) atomicAdd(&s_nl, cl);
+    __syncthreads();
+    const bool all_of_L = s_nl <= (uint32_t)a.size;
+    uint32_t T = 0u, need = 0u, eq = 0u;
+    if (!all_of_L) {
+        const int shifts[3] = {20, 8, 0}, widths[3] = {12, 12, 8};
+        uint32_t mask = 0u;
+        for (int pass = 0; pass < 3; ++pass) {
+            const int sh = shifts[pass], nb = 1 << widths[pass];
+            for (int j = tid; j < 4096; j += SL_NT) hist[j] = 0u;
+            __syncthreads();
+            const uint32_t prefix = s_prefix;
+#pragma unroll 4
+            for (int t = tid; t < n; t += SL_NT) {
+                const uint32_t o = ord(t);
+                if (o != 0u && (o & mask) == prefix) atomicAdd(&hist[(o >> sh) & (uint32_t)(nb - 1)], 1u);
+            }
+            __syncthreads();
+            if (warp == 0) {
+                // bins from the top: lane j takes bins [nb - (j+1) * per, nb - j * per)
+                const int per = nb / 32;
+                uint32_t tot = 0u;
+                for (int q = 0; q < per; ++q) tot += hist[nb - 1 - (lane * per + q)];
+                uint32_t incl = tot;  // inclusive prefix over lanes (lane 0 = the highest bins)
+#pragma unroll
+                for (int o = 1; o < 32; o <<= 1) {
+                    const uint32_t y = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+                    if (lane >= o) incl += y;
+                }
+                const uint32_t excl = incl - tot, nd = s_need;
+                if (excl < nd && nd <= incl) {  // the cut is in this lane's bins
+                    uint32_t acc = excl;
+                    for (int q = 0; q < per; ++q) {
+                        const int bin = nb - 1 - (lane * per + q);
+                        const uint32_t hb = hist[bin];
+                        if (acc + hb >= nd) {
+                            s_need = nd - acc;
+                            s_prefix = prefix | ((uint32_t)bin << sh);
+                            s_eq = hb;
+                            break;
+                        }
+                        acc += hb;
+                    }
+                }
+            }
+            __syncthreads();
+            mask |= (uint32_t)(nb - 1) << sh;
+        }
+        T = s_prefix;
+        need = s_need;
+        eq = s_eq;  // tokens equal to T
+    }
+    // Keep: every token above T, and the `need` lowest ids among those equal to T.
+    uint32_t *out = a.out + (size_t)ul * a.W;
+    uint32_t taken_eq = 0u;
+    for (int c0 = 0; c0 < n; c0 += SL_NT) {
+        const int t = c0 + tid;
+        bool keep = false, tie = false;
+        if (t < n) {
+            if (all_of_L) {
+                keep = ord(t) != 0u;
+            } else {
+                const uint32_t o = ord(t);
+                keep = o > T;
+                tie = o == T;
+            }
+        }
+        if (!all_of_L && eq > need) {  // rank the ties in token order
+            const uint32_t bal = __ballot_sync(0xFFFFFFFFu, tie);
+            if (lane == 0) s_wcnt[warp] = __popc(bal);
+            __syncthreads();
+            uint32_t before = taken_eq;
+            for (int w2 = 0; w2 < warp; ++w2) before += (uint32_t)s_wcnt[w2];
+            before += __popc(bal & ((1u << lane) - 1u));
+            keep = keep || (tie && before < need);
+            uint32_t chunk_ties = 0u;
+            for (int w2 = 0; w2 < SL_NT / 32; ++w2) chunk_ties += (uint32_t)s_wcnt[w2];
+            taken_eq += chunk_ties;
+            __syncthreads();
+        } else {
+            keep = keep || tie;
+        }
+        const uint32_t word = __ballot_sync(0xFFFFFFFFu, keep);
+        const int wi = (c0 >> 5) + warp;
+        if (lane == 0 && wi < a.W) out[wi] = word;
+    }
+}
+
+cudaError_t launch_shortlist(const ShortlistArgs &a, int units_layer, cudaStream_t s) {
+    if (a.size < 1 || a.size > SHORTLIST_MAX) return cudaErrorInvalidValue;
+    // The keys of up to 40960 tokens stay in shared memory between the passes.
+    const size_t smem = (size_t)a.n * 4;
+    if (smem <= 160 * 1024) {
+        static bool attr = false;
+        if (!attr) {
+            cudaError_t e = cudaFuncSetAttribute(k_shortlist<true>,
+                                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                 160 * 1024);
+            if (e != cudaSuccess) return e;
+            attr = true;
+        }
+        k_shortlist<true><<<units_layer, SL_NT, smem, s>>>(a);
+    } else {
+        k_shortlist<false><<<units_layer, SL_NT, 0, s>>>(a);
+    }
+    return cudaGetLastError();
 }
 
 }  // namespace verkv

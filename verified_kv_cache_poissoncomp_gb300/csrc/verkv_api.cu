@@ -24,7 +24,7 @@ namespace {
 size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 
 struct Layout {
-    size_t err, flc, scores, qstats, F, fids, fcounts, staging, part_piv, part_fet, total;
+    size_t err, flc, scores, qstats, F, slb, fids, fcounts, staging, part_piv, part_fet, total;
     int W, units_layer, qh_layer, max_piv, max_fet, dense_chunks;
 };
 
@@ -57,6 +57,7 @@ bool make_layout(const verkv_shape *s, Layout &L) {
     L.scores = take((size_t)L.qh_layer * n * 4);
     L.qstats = take((size_t)L.qh_layer * sizeof(verkv_head_stats));
     L.F = take((size_t)L.qh_layer * L.W * 4);
+    L.slb = take((size_t)L.units_layer * L.W * 4);
     L.fids = take((size_t)L.units_layer * n * 4);
     L.fcounts = take((size_t)L.units_layer * 4);
     L.staging = take((size_t)L.units_layer * n * 4 * d);
@@ -136,6 +137,9 @@ struct verkv_ctx {
     uint32_t *F = nullptr;
     int32_t *fids = nullptr, *fcounts = nullptr;
     int32_t *flc = nullptr;  // per-KV-head completion counters of the certify kernel's fetch list
+    uint32_t *slb = nullptr; // per-KV-head shortlist bitmaps
+    int shortlist = 0;       // shortlist size per KV head; 0: every token of L may be fetched
+    bool shortlisted = false;  // the last attend built shortlists
     uint16_t *staging = nullptr;
     float *part_piv = nullptr, *part_fet = nullptr;
     int fetch_mode = VERKV_FETCH_ZEROCOPY;
@@ -280,6 +284,7 @@ verkv_status verkv_create(verkv_ctx **out, int device, void *stream, const verkv
     ctx->fids = (int32_t *)(w + L.fids);
     ctx->fcounts = (int32_t *)(w + L.fcounts);
     ctx->flc = (int32_t *)(w + L.flc);
+    ctx->slb = (uint32_t *)(w + L.slb);
     ctx->staging = (uint16_t *)(w + L.staging);
     ctx->part_piv = (float *)(w + L.part_piv);
     ctx->part_fet = (float *)(w + L.part_fet);
@@ -445,8 +450,22 @@ verkv_status verkv_attend_verified(verkv_ctx *ctx, int32_t layer, const void *q,
         VERKV_CUDA(tracked(ctx, VERKV_K_SCORE, ctx->main, [&] { return launch_score(sa, ctx->L.units_layer, ctx->main); }), "k_score");
     }
 
+    if (ctx->shortlist > 0) {
+        ShortlistArgs sla{};
+        sla.scores = ctx->scores;
+        sla.r_full = r_full;
+        sla.out = ctx->slb;
+        sla.n = n;
+        sla.W = ctx->L.W;
+        sla.size = ctx->shortlist;
+        sla.li = li;
+        VERKV_CUDA(tracked(ctx, VERKV_K_SHORTLIST, ctx->main, [&] { return launch_shortlist(sla, ctx->L.units_layer, ctx->main); }), "k_shortlist");
+    }
+
     CertifyArgs ca{};
     ca.scores = ctx->scores;
+    ca.shortlist = ctx->shortlist > 0 ? ctx->slb : nullptr;
+    ctx->shortlisted = ctx->shortlist > 0;
     ca.r_full = r_full;
     ca.resident = pivotal->resident;
     ca.F = ctx->F;
@@ -639,6 +658,24 @@ verkv_status verkv_sync(verkv_ctx *ctx) {
     return fail(ctx, VERKV_ENOCONVERGE, "a solve hit its iteration cap");
 }
 
+verkv_status verkv_set_shortlist(verkv_ctx *ctx, int32_t size) {
+    if (!ctx) return VERKV_EINVAL;
+    if (size < 0 || size > SHORTLIST_MAX)
+        return fail(ctx, VERKV_EINVAL, "set_shortlist: size must be 0 (off) or 1 .. 256");
+    ctx->shortlist = size;
+    return VERKV_OK;
+}
+
+verkv_status verkv_shortlist_bitmap(verkv_ctx *ctx, uint32_t *out) {
+    if (!ctx) return VERKV_EINVAL;
+    if (!ctx->shortlisted) return fail(ctx, VERKV_ESTATE, "shortlist_bitmap: no attend with a shortlist");
+    if (!out) return fail(ctx, VERKV_EINVAL, "shortlist_bitmap: null pointer");
+    VERKV_CUDA(cudaSetDevice(ctx->device), "cudaSetDevice");
+    VERKV_CUDA(cudaMemcpyAsync(out, ctx->slb, (size_t)ctx->L.units_layer * ctx->L.W * 4,
+                               cudaMemcpyDefault, ctx->main), "copy shortlist");
+    return VERKV_OK;
+}
+
 verkv_status verkv_attend_dense_host(verkv_ctx *ctx, int32_t layer, const void *q,
                                     const void *host_kv, float *o_out, float *lse_out) {
     if (!ctx) return VERKV_EINVAL;
@@ -712,7 +749,7 @@ const char *verkv_kernel_name(int k) {
     static const char *names[VERKV_K_COUNT] = {
         "k_pc_solve", "k_pc_gather", "k_sketch", "k_score", "k_certify",
         "k_partial(pivotal)", "k_partial(host)", "k_partial(staged)", "k_merge",
-        "k_dense_host", "k_dense_merge"};
+        "k_dense_host", "k_dense_merge", "k_shortlist"};
     return (k >= 0 && k < VERKV_K_COUNT) ? names[k] : "";
 }
 

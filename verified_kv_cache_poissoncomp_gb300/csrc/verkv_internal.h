@@ -92,11 +92,24 @@ struct CertifyArgs {
     int32_t *counts_user;
     int32_t *ids_host;            // optional copy into mapped host memory (MEMCPY mode)
     int32_t *counts_host;
+    const uint32_t *shortlist;    // [units_layer][W] fetch candidates, or null: all of L
     int n, W, cl, chunk;
     float eps, ldelta;
     LayerIdx li;
 };
 cudaError_t launch_certify(const CertifyArgs &a, int qheads, size_t smem, cudaStream_t s);
+
+// The per-KV-head shortlist: the `size` tokens of L with the largest sketch logit over the KV
+// head's query heads (ties to the lower id), as a bitmap [units_layer][W].
+constexpr int SHORTLIST_MAX = 256;
+struct ShortlistArgs {
+    const float *scores;   // [qh][n]
+    const float *r_full;   // [units][n]
+    uint32_t *out;         // [units_layer][W]
+    int n, W, size;
+    LayerIdx li;
+};
+cudaError_t launch_shortlist(const ShortlistArgs &a, int units_layer, cudaStream_t s);
 int certify_cluster_size(int n);
 int certify_chunk(int n, int cl);
 size_t certify_smem_bytes(int chunk);

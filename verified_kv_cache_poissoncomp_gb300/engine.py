@@ -107,6 +107,15 @@ class VerKV:
                                   o.data_ptr(), lse.data_ptr())
         return o, lse
 
+    def set_shortlist(self, size):
+        """Shortlist variant: at most `size` tokens per KV head may be fetched (0: off)."""
+        B.verkv_set_shortlist(self.ctx, size)
+
+    def shortlist_bitmap(self):
+        out = torch.empty((self.B * self.h, self.W), dtype=torch.int32, device=self.dev)
+        B.verkv_shortlist_bitmap(self.ctx, out.data_ptr())
+        return out
+
     def selection_bitmap(self):
         out = torch.empty((self.B * self.h * self.G, self.W), dtype=torch.int32, device=self.dev)
         B.verkv_selection_bitmap(self.ctx, out.data_ptr())
