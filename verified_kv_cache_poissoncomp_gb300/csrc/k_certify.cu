@@ -573,9 +573,9 @@ __global__ void __launch_bounds__(CT_NT, 1) k_certify(CertifyArgs a) {
                         ab += w;
                         S += __uint_as_float(X[i]);
                         pl = fmaxf(pl, fl);
-                        if (fl < r * ph) ph = fminf(ph, __fdiv_rn(fl, r));
+                        if (fl < r * ph) ph = fminf(ph, __fdividef(fl, r));
                     } else if (fl > r * pl) {
-                        pl = fmaxf(pl, __fdiv_rn(fl, r));
+                        pl = fmaxf(pl, __fdividef(fl, r));
                     }
                 }
             }
