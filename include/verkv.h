@@ -19,7 +19,8 @@
  *  - Calls are asynchronous and stream-ordered on the stream given to verkv_create, except that
  *    verkv_fetch_refine in VERKV_FETCH_MEMCPY mode waits on the host for the selection of the
  *    preceding verkv_attend_verified.  Errors detected on the device (invalid tau, pivotal
- *    capacity overflow, a solve that hit its iteration cap) are latched in a device error word
+ *    capacity overflow, a solve that hit its iteration cap, a pivotal or fetch row id outside
+ *    [0, n), whose row is then skipped) are latched in a device error word
  *    and returned by the next verkv_sync.  No call throws; a call that returns an error has not
  *    launched work unless stated.
  *  - Layouts.  A "unit" is one (sequence b, layer l, KV head h) of a verkv_shape; units are

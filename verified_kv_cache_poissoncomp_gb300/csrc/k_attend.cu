@@ -169,6 +169,11 @@ __global__ void __launch_bounds__(128) k_partial(PartialArgs a, int units_layer)
                 const int row = rbase + (it0 + u) * RPW + rg;
                 valid[u] = row < rows_u;
                 id[u] = valid[u] ? ids[row] : 0;
+                if ((unsigned)id[u] >= (unsigned)a.n) {  // not a token of the unit: skip the row
+                    raise_error(a.err, ERR_BADID);
+                    valid[u] = false;
+                    id[u] = 0;
+                }
                 r[u] = (MODE == ROWS_PIVOTAL && valid[u]) ? prs[row] : 1.0f;
             }
             uint4 kq[U], vq[U];

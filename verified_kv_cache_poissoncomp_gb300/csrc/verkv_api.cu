@@ -502,6 +502,7 @@ verkv_status verkv_attend_verified(verkv_ctx *ctx, int32_t layer, const void *q,
     pa.qstats = ctx->qstats;
     pa.scores = ctx->scores;
     pa.part = ctx->part_piv;
+    pa.err = ctx->err;
     pa.row_stride = ctx->sh.cap;
     pa.max_chunks = ctx->L.max_piv;
     pa.n = n;
@@ -551,6 +552,7 @@ verkv_status verkv_fetch_refine(verkv_ctx *ctx, const int32_t *ids, const int32_
     pa.F = ctx->F;
     pa.qstats = ctx->qstats;
     pa.part = ctx->part_fet;
+    pa.err = ctx->err;
     pa.ids = ctx->fids;
     pa.pr = nullptr;
     pa.count = ctx->fcounts;
@@ -654,6 +656,7 @@ verkv_status verkv_sync(verkv_ctx *ctx) {
     if (word & ERR_TAU) return fail(ctx, VERKV_EINVAL, "tau outside (0, 1] or not finite");
     if (word & ERR_CAPACITY) return fail(ctx, VERKV_ECAPACITY, "pivotal set exceeded cap (truncated)");
     if (word & ERR_TIMEOUT) return fail(ctx, VERKV_ETIMEOUT, "a bounded wait on a copy barrier expired");
+    if (word & ERR_BADID) return fail(ctx, VERKV_EINVAL, "a pivotal or fetch row id outside [0, n) (skipped)");
     if (word & ERR_BUDGET_SUM) return fail(ctx, VERKV_ENOCONVERGE, "|sum r - eta n| >= 1e-6 n");
     return fail(ctx, VERKV_ENOCONVERGE, "a solve hit its iteration cap");
 }

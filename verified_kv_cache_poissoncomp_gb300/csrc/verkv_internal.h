@@ -15,6 +15,7 @@ enum : uint32_t {
     ERR_NOCONVERGE = 1u << 2,  // a solve hit its iteration cap
     ERR_BUDGET_SUM = 1u << 3,  // |sum r - eta n| >= 1e-6 n after the c solve
     ERR_TIMEOUT = 1u << 4,     // a bounded wait on a copy barrier expired
+    ERR_BADID = 1u << 5,       // a pivotal or fetch row id outside [0, n) (the row was skipped)
 };
 
 // ---------------------------------------------------------------------------------------------
@@ -136,6 +137,7 @@ struct PartialArgs {
     const verkv_head_stats *qstats;
     const float *scores;      // sketch logits [qh][n]: lambda of Definition 2 uses w-hat
     float *part;              // [units_layer][max_chunks][G][d + 2]
+    uint32_t *err;            // ERR_BADID for a row id outside [0, n)
     int row_stride;           // cap (pivotal) or n (fetched)
     int max_chunks;
     int n, W, d;

@@ -13,6 +13,12 @@ import torch
 from . import binding as B
 
 
+def _check_dense(t, shape, dev, name):
+    """The library reads tensors as dense row-major arrays: refuse anything else."""
+    if t.device != dev or not t.is_contiguous() or t.numel() != int(np.prod(shape)):
+        raise ValueError(f"{name}: a contiguous {list(shape)} tensor on {dev} is required")
+
+
 def default_cap(n, eta):
     """Pivotal capacity: eta n plus 8 standard deviations of a Poisson sample size, plus 64."""
     m = eta * n
@@ -75,6 +81,24 @@ class VerKV:
                                       dtype=torch.uint8, device=self.dev)
         self.sketch_desc = B.verkv_sketch(self.sketch_format, self.sketch.data_ptr())
 
+    def load_device(self, tau, kv, host_kv):
+        """Adopt tensors that already exist: tau float32 [units][n] and kv int16 (bf16 bits)
+        [units][n][2][d] on this device, host_kv the same layout in page-locked host memory."""
+        _check_dense(tau, (self.units, self.n), self.dev, "tau")
+        _check_dense(kv, (self.units, self.n, 2, self.d), self.dev, "kv")
+        if not (host_kv.is_pinned() and host_kv.is_contiguous() and host_kv.numel() == kv.numel()):
+            raise ValueError("host_kv: a contiguous page-locked copy of kv is required")
+        self.tau = tau.reshape(self.units, self.n)
+        self.kv = kv.reshape(self.units, self.n, 2, self.d)
+        self.host_kv = host_kv.reshape(self.units, self.n, 2, self.d)
+        if self.sketch_format == B.VERKV_SKETCH_EXACT:
+            self.sketch = torch.empty((self.units, self.n, self.d), dtype=torch.int16, device=self.dev)
+        else:
+            nbytes = B.verkv_sketch_bytes(self.shape, self.sketch_format)
+            self.sketch = torch.empty((self.units, self.n, nbytes // (self.units * self.n)),
+                                      dtype=torch.uint8, device=self.dev)
+        self.sketch_desc = B.verkv_sketch(self.sketch_format, self.sketch.data_ptr())
+
     def compress(self, eta, n_sink, n_local, seed):
         B.verkv_poissoncomp(self.ctx, self.tau.data_ptr(), eta, B.verkv_hset(n_sink, n_local),
                             seed, self.kv.data_ptr(), self.r_full.data_ptr(), self.pivotal)
@@ -82,7 +106,8 @@ class VerKV:
                              self.sketch.data_ptr())
 
     def attend(self, layer, q, eps, delta, with_ids=True):
-        """q: device bf16 (int16 view) [batch][kv_heads * q_per_kv][d]."""
+        """q: device bf16 (int16 view) [batch][kv_heads * q_per_kv][d], contiguous."""
+        _check_dense(q, (self.B, self.h * self.G, self.d), self.dev, "q")
         self._q = q
         ids = self.fetch_ids.data_ptr() if with_ids else None
         cnt = self.fetch_counts.data_ptr() if with_ids else None

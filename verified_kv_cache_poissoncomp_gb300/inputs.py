@@ -259,3 +259,41 @@ def long_context_128k(B=4, L=1, h_kv=8, G=4, d=128, n=131072, eta=1.0 / 32, n_si
                     tau=tau, kv=kv, queries=queries, query_layer=query_layer,
                     planted=np.ones(Q, dtype=bool), plant_pos=np.zeros((B, L, h_kv, 0), np.int64),
                     meta=dict(data_seed=data_seed, boost=boost, needle_frac=pfrac))
+
+
+def decode_step_cache_torch(units, n, d, G, layers, batch, kv_heads, device, seed=1238,
+                            alpha=4.0, n_sinks=4, sink_gain=8.0):
+    """The full-decode-step cache on the device (torch, seeded), for sizes where numpy
+    generation would take minutes: per unit, tau lognormal(0, 1.5) / max; keys N(0, 1) with the
+    outlier channel scales of make_workload and the first n_sinks keys shifted by sink_gain along
+    the unit's direction mu (attention sinks); values N(0, 1); bf16 by round-to-nearest.  Queries
+    [layers][batch][kv_heads * G][d]: alpha mu + N(0, I).  Returns (tau, kv int16 [units][n][2][d],
+    queries int16)."""
+    import torch
+
+    gen = torch.Generator(device=device)
+    gen.manual_seed(seed)
+    scales = torch.as_tensor(_channel_scales(d, True), device=device)
+    x = torch.exp(1.5 * torch.randn((units, n), generator=gen, device=device))
+    tau = (x / x.max(dim=1, keepdim=True).values).float()
+    mu = torch.zeros((units, d), device=device)
+    mu[:, :8] = torch.randn((units, 8), generator=gen, device=device)
+    mu /= mu.norm(dim=1, keepdim=True)
+    kv = torch.empty((units, n, 2, d), dtype=torch.int16, device=device)
+    for u0 in range(0, units, 64):  # in slices, to bound the float32 temporaries
+        u1 = min(units, u0 + 64)
+        K = torch.randn((u1 - u0, n, d), generator=gen, device=device) * scales
+        K[:, :n_sinks] += sink_gain * mu[u0:u1, None, :]
+        kv[u0:u1, :, 0] = K.to(torch.bfloat16).view(torch.int16)
+        del K
+        V = torch.randn((u1 - u0, n, d), generator=gen, device=device)
+        kv[u0:u1, :, 1] = V.to(torch.bfloat16).view(torch.int16)
+        del V
+    # unit u = (b * layers + l) * kv_heads + h
+    mu4 = mu.view(batch, layers, kv_heads, d).permute(1, 0, 2, 3)  # [layers][batch][kv_heads][d]
+    q = alpha * mu4[:, :, :, None, :] + torch.randn((layers, batch, kv_heads, G, d), generator=gen,
+                                                    device=device)
+    # contiguous [layers][batch][kv_heads * G][d]: the broadcast against the permuted mu4 would
+    # otherwise leave the batch dimension outermost in memory
+    queries = q.reshape(layers, batch, kv_heads * G, d).to(torch.bfloat16).contiguous()
+    return tau, kv, queries.view(torch.int16)
