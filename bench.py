@@ -396,8 +396,9 @@ def run_ours(args, world, rank, local):
         # latency- and issue-bound: judged by warp instructions issued, not bytes
         "k_certify": ("alu", units_layer * (w.G * w.n * 4 + w.n * 4)),  # logits + r
         "k_partial(pivotal)": ("hbm", int(counts.mean() * units_layer * (4 * w.d + 8))),
-        # with the exact sketch only V rows (2 d bytes) cross the host link, else K|V rows
-        "k_partial(host)": ("h2d", int(fetched_rows.sum(1).mean() * fetch_row_bytes)),
+        # with the exact sketch only V rows (2 d bytes) cross the host link, else K|V rows; the
+        # zero-copy refine kernel also sums the pivotal rows (HBM) and merges, but the link binds
+        "k_refine": ("h2d", int(fetched_rows.sum(1).mean() * fetch_row_bytes)),
         "k_pc_solve": ("hbm", int(units_all * w.n * 8.125 + counts.sum() * 8)),
         "k_pc_gather": ("hbm", int(counts.sum() * 2 * 4 * w.d)),
     }
@@ -438,9 +439,9 @@ def run_ours(args, world, rank, local):
     dom_hbm = max(hbm, key=lambda k: per_kernel[k]["launches"] * hbm[k]["algorithmic_bytes_per_launch"]) if hbm else None
     roof_hbm = dict(hbm[dom_hbm], kernel=dom_hbm) if dom_hbm else None
     fetch = None
-    if "k_partial(host)" in rooflines:
-        f = rooflines["k_partial(host)"]
-        fetch = {"kernel": "k_partial(host)", "bytes_per_query": f["algorithmic_bytes_per_launch"],
+    if "k_refine" in rooflines:
+        f = rooflines["k_refine"]
+        fetch = {"kernel": "k_refine", "bytes_per_query": f["algorithmic_bytes_per_launch"],
                  "avg_us": f["avg_us"], "achieved_GBs": f["achieved"], "link_peak_GBs": f["peak"],
                  "frac": f["frac"], "link_peak_source": link_src}
     stats_f = st[..., :10].view(np.float32)

@@ -106,11 +106,13 @@ typedef struct {
 } verkv_sketch;
 
 /* How verkv_fetch_refine moves the selected rows from the host-resident full cache.
- * ZEROCOPY: a kernel on the side stream reads the selected rows straight from page-locked host
- *           memory and accumulates them into the refined estimator in the same pass (no host
- *           round trip, no staging; default).
+ * ZEROCOPY: one kernel on the context's stream reads the selected rows straight from
+ *           page-locked host memory and accumulates them into the refined estimator together
+ *           with the sums over the resident tokens; the merge follows (no host round trip, no
+ *           staging; default).
  * MEMCPY:   the host waits for the selection, gathers the rows into page-locked staging with a
- *           thread pool, and cudaMemcpyAsync moves them on the side stream.
+ *           thread pool, and cudaMemcpyAsync moves them on the side stream while the sums over
+ *           the resident tokens run.
  * With the exact sketch the GPU already holds every key, so by default only the V row of a
  * fetched token crosses the host link and its K row is read from the sketch; or-ing in
  * VERKV_FETCH_KEYS moves the full K|V row instead (same results, twice the link bytes). */
@@ -199,7 +201,8 @@ verkv_status verkv_sketch_build(verkv_ctx *ctx, const void *kv_full, int32_t for
  *                  output may be given without the other)
  * Per query head: sketch logits for all n tokens, w-hat = exp(logit - max), the beta fixed point,
  * the certificate, and when it fails the order of Eq. (9) (ties to the lower token id) and the
- * minimal k* of Eq. (10); then the shrinkage-weighted partial sums over the pivotal set.
+ * minimal k* of Eq. (10).  In MEMCPY mode the shrinkage-weighted partial sums over the pivotal
+ * set follow here; in ZEROCOPY mode verkv_fetch_refine computes them.
  * Asynchronous; results are completed by verkv_fetch_refine, which reads q, the pivotal set and
  * the sketch again: keep them unchanged until it has been issued. */
 verkv_status verkv_attend_verified(verkv_ctx *ctx, int32_t layer, const void *q,
@@ -302,8 +305,10 @@ enum {
     VERKV_K_SCORE,             /* sketch logits for every token and query head    */
     VERKV_K_CERTIFY,           /* beta solve, certificate, selection (Eq. 7-10),
                                   and the per-KV-head fetch id list               */
-    VERKV_K_PARTIAL_PIVOTAL,   /* shrinkage-weighted sums over the pivotal set    */
-    VERKV_K_FETCH_HOST,        /* zero-copy fetch + exact sums over fetched rows  */
+    VERKV_K_PARTIAL_PIVOTAL,   /* shrinkage-weighted sums over the pivotal set
+                                  (MEMCPY mode)                                   */
+    VERKV_K_FETCH_HOST,        /* "k_refine": zero-copy fetch, exact sums over the
+                                  fetched rows and the pivotal sums               */
     VERKV_K_PARTIAL_STAGED,    /* exact sums over rows staged by cudaMemcpyAsync  */
     VERKV_K_MERGE,             /* merge partials into o, lse and statistics       */
     VERKV_K_DENSE_HOST,        /* offloaded-dense baseline: all rows from host    */

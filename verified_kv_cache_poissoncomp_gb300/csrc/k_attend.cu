@@ -3,13 +3,14 @@
 // Definition 2 / Eq. (5), KVFETCH step 5; abstract page: fetch additional tokens from the CPU and
 // refine the attention computation).
 //
-// k_partial   split-K over a row set: each CTA item is 64 pivotal rows, or up to FET_ITEM_ROWS
-//             fetched rows taken 64 at a time, of one KV head; each row a contiguous 4d-byte K|V
-//             pair read with 16-byte coalesced loads, four row groups in flight per warp (all of
-//             them for host rows), accumulated into one partial.  It computes the G logits, w = exp(logit - m), the weight of Eq. (5) -- 1 for H
-//             and for tokens of F, lambda / r for sampled, unfetched tokens, with the certificate's
-//             lambda = clip(beta r / (w-hat (1 - r)), r, 1) from the sketch weight w-hat -- and
-//             accumulates D-hat, N-hat and the sample second moment.  All CTAs of a query head share its shift m, so partials add without
+// k_partial   split-K over a row set: each CTA item is a block of FET_ITEM_ROWS rows of one KV
+//             head, taken 64 at a time; each row a contiguous 4d-byte K|V pair read with 16-byte
+//             coalesced loads, four row groups in flight per warp (all of them for host rows),
+//             accumulated into one partial.  It computes the G logits, w = exp(logit - m), the
+//             weight of Eq. (5) -- 1 for H and for tokens of F, lambda / r for sampled, unfetched
+//             tokens, with the certificate's lambda = clip(beta r / (w-hat (1 - r)), r, 1) from
+//             the sketch weight w-hat -- and accumulates D-hat, N-hat and the sample second
+//             moment.  All CTAs of a query head share its shift m, so partials add without
 //             rescaling.  Three row sources:
 //               ROWS_PIVOTAL   the pivotal buffer in HBM;
 //               ROWS_STAGED    fetched rows already copied to HBM (the cudaMemcpyAsync fetch);
@@ -17,6 +18,8 @@
 //                              id -- the zero-copy fetch and the refine in one pass, no staging.
 //             When the sketch is exact the GPU already holds every key, so K comes from the sketch
 //             by token id and only the V rows cross the host link.
+// k_refine    the zero-copy path's partial sums in one launch: the ROWS_HOST and ROWS_PIVOTAL
+//             items of every KV head.
 // k_merge     sums the partials in a fixed order and writes o = N-hat / D-hat, m + log D-hat and
 //             the per-head statistics.
 // k_dense_host, k_dense_merge   the offloaded-dense baseline: exact attention over every token with
@@ -101,8 +104,11 @@ __device__ __forceinline__ uint4 ld_host(const uint4 *p) {
     return v;
 }
 
-template <int D, int G, int MODE>
-__global__ void __launch_bounds__(128) k_partial(PartialArgs a, int units_layer) {
+// One item of the split-K sums: rows [ch * ITEM, (ch + 1) * ITEM) of layer unit `ul`, taken
+// PART_ROWS at a time.  Returns false, uniformly over the CTA, when the block lies past the
+// unit's rows (nothing is written).
+template <int D, int G, int MODE, int ITEM>
+__device__ __forceinline__ bool partial_item(const PartialArgs &a, int ul, int ch) {
     constexpr int LPR = D / 8, RPW = 32 / LPR, NW = 4;
     constexpr int ITER = (PART_ROWS / NW) / RPW;  // row groups per warp
     // Row groups in flight per warp: all of them for host rows (link latency), else four.
@@ -115,20 +121,14 @@ __global__ void __launch_bounds__(128) k_partial(PartialArgs a, int units_layer)
     const int cgp = lane % LPR, rg = lane / LPR;
     const int myhead = head_of_lane<G, LPR>(lane);
     const int hq = a.li.kv_heads * G;
-    const int total_items = units_layer * a.max_chunks;
-    // Pivotal rows: one 64-row block per partial (many CTAs, one round each); fetched rows:
-    // FET_SUB blocks accumulated per partial (fewer partials for the merge).
-    constexpr int ITEM = MODE == ROWS_PIVOTAL ? PART_ROWS : FET_ITEM_ROWS;
 
-    for (int item = blockIdx.x; item < total_items; item += gridDim.x) {
-        const int ul = item / a.max_chunks;
-        const int ch = item - ul * a.max_chunks;
+    {
         const int b = ul / a.li.kv_heads, h = ul - b * a.li.kv_heads;
         const int ug = a.li.unit_global(ul);
         const int src = MODE == ROWS_PIVOTAL ? ug : ul;
         int rows_u = a.count[src];
         if (rows_u > a.row_stride) rows_u = a.row_stride;
-        if (ch * ITEM >= rows_u) continue;  // uniform over the CTA
+        if (ch * ITEM >= rows_u) return false;  // uniform over the CTA
 
         float qv[G][8];
 #pragma unroll
@@ -291,16 +291,31 @@ __global__ void __launch_bounds__(128) k_partial(PartialArgs a, int units_layer)
         }
         __syncthreads();
     }
+    return true;
+}
+
+// Every row source in blocks of FET_ITEM_ROWS rows (FET_SUB blocks of PART_ROWS accumulated per
+// partial), as in k_refine, so that both fetch modes produce the same partials.
+template <int D, int G, int MODE>
+__global__ void __launch_bounds__(128) k_partial(PartialArgs a, int units_layer) {
+    pdl_wait();
+    pdl_trigger();
+    const int total_items = units_layer * a.max_chunks;
+    for (int item = blockIdx.x; item < total_items; item += gridDim.x) {
+        const int ul = item / a.max_chunks;
+        partial_item<D, G, MODE, FET_ITEM_ROWS>(a, ul, item - ul * a.max_chunks);
+    }
 }
 
 cudaError_t launch_partial(const PartialArgs &a, int units_layer, int grid, cudaStream_t s) {
     const int G = a.li.G;
 #define VERKV_PART(DD, GG)                                                                      \
     if (a.d == DD && G == GG) {                                                                 \
-        if (a.mode == ROWS_PIVOTAL) k_partial<DD, GG, ROWS_PIVOTAL><<<grid, 128, 0, s>>>(a, units_layer); \
-        else if (a.mode == ROWS_STAGED) k_partial<DD, GG, ROWS_STAGED><<<grid, 128, 0, s>>>(a, units_layer); \
-        else k_partial<DD, GG, ROWS_HOST><<<grid, 128, 0, s>>>(a, units_layer);                  \
-        return cudaGetLastError();                                                              \
+        if (a.mode == ROWS_PIVOTAL)                                                             \
+            return launch_pdl(k_partial<DD, GG, ROWS_PIVOTAL>, dim3(grid), dim3(128), 0, s, a, units_layer); \
+        if (a.mode == ROWS_STAGED)                                                              \
+            return launch_pdl(k_partial<DD, GG, ROWS_STAGED>, dim3(grid), dim3(128), 0, s, a, units_layer); \
+        return launch_pdl(k_partial<DD, GG, ROWS_HOST>, dim3(grid), dim3(128), 0, s, a, units_layer); \
     }
     VERKV_PART(128, 1) VERKV_PART(128, 2) VERKV_PART(128, 4) VERKV_PART(128, 8)
     VERKV_PART(64, 1) VERKV_PART(64, 2) VERKV_PART(64, 4) VERKV_PART(64, 8)
@@ -309,13 +324,15 @@ cudaError_t launch_partial(const PartialArgs &a, int units_layer, int grid, cuda
 }
 
 // ---------------------------------------------------------------------------------------------
-// One CTA per query head; 8 groups of 128 threads each sum every eighth chunk of their columns
-// (loads in flight across the groups), then the groups are added in a fixed order.
+// k_merge: one CTA per query head; 8 groups of 128 threads each sum every eighth chunk of their
+// columns (pivotal chunks, then fetched ones), then the groups are added in a fixed order.
 constexpr int MG_NT = 1024;
 constexpr int MG_GROUPS = MG_NT / 128;
 
 __global__ void __launch_bounds__(MG_NT) k_merge(MergeArgs a) {
     extern __shared__ float red[];  // [MG_GROUPS][d + 2]
+    pdl_wait();
+    pdl_trigger();
     const int qh = blockIdx.x;
     const int G = a.li.G;
     const int ul = qh / G, g = qh - ul * G;
@@ -323,7 +340,7 @@ __global__ void __launch_bounds__(MG_NT) k_merge(MergeArgs a) {
     const int D = a.d, ncol = D + 2;
     int pc = a.pcount[ug];
     if (pc > a.cap) pc = a.cap;
-    const int npc = (pc + PART_ROWS - 1) / PART_ROWS;
+    const int npc = (pc + FET_ITEM_ROWS - 1) / FET_ITEM_ROWS;
     const int nfc = (a.fcount[ul] + FET_ITEM_ROWS - 1) / FET_ITEM_ROWS;
     const int grp = threadIdx.x / 128, c0 = threadIdx.x % 128;
     const float *pp = a.part_piv + ((size_t)ul * a.max_piv * G + g) * ncol;
@@ -359,8 +376,36 @@ __global__ void __launch_bounds__(MG_NT) k_merge(MergeArgs a) {
 }
 
 cudaError_t launch_merge(const MergeArgs &a, int qheads, cudaStream_t s) {
-    k_merge<<<qheads, MG_NT, MG_GROUPS * (a.d + 2) * sizeof(float), s>>>(a);
-    return cudaGetLastError();
+    return launch_pdl(k_merge, dim3(qheads), dim3(MG_NT), MG_GROUPS * (a.d + 2) * sizeof(float), s, a);
+}
+
+// ---------------------------------------------------------------------------------------------
+// k_refine: the zero-copy path's partial sums in one launch -- the fetched-row blocks of every
+// layer unit first (so the host reads start at once), then its pivotal blocks (their HBM reads
+// hide behind the host link).  k_merge follows.
+template <int D, int G>
+__global__ void __launch_bounds__(128, 3) k_refine(PartialArgs piv, PartialArgs fet, int units_layer) {
+    pdl_wait();
+    pdl_trigger();
+    const int per_unit = fet.max_chunks + piv.max_chunks;
+    const int total = units_layer * per_unit;
+    for (int item = blockIdx.x; item < total; item += gridDim.x) {
+        const int k = item / units_layer, ul = item - k * units_layer;
+        if (k < fet.max_chunks) partial_item<D, G, ROWS_HOST, FET_ITEM_ROWS>(fet, ul, k);
+        else partial_item<D, G, ROWS_PIVOTAL, FET_ITEM_ROWS>(piv, ul, k - fet.max_chunks);
+    }
+}
+
+cudaError_t launch_refine(const PartialArgs &piv, const PartialArgs &fet, int units_layer, int grid,
+                          cudaStream_t s) {
+    const int G = piv.li.G;
+#define VERKV_REFINE(DD, GG)                                                                    \
+    if (piv.d == DD && G == GG)                                                                 \
+        return launch_pdl(k_refine<DD, GG>, dim3(grid), dim3(128), 0, s, piv, fet, units_layer);
+    VERKV_REFINE(128, 1) VERKV_REFINE(128, 2) VERKV_REFINE(128, 4) VERKV_REFINE(128, 8)
+    VERKV_REFINE(64, 1) VERKV_REFINE(64, 2) VERKV_REFINE(64, 4) VERKV_REFINE(64, 8)
+#undef VERKV_REFINE
+    return cudaErrorInvalidValue;
 }
 
 // ---------------------------------------------------------------------------------------------

@@ -361,6 +361,13 @@ __device__ __forceinline__ void select_step(const Merged &mh, SelState &ss, int 
 // removes the resident tokens, scans the counts and writes the ascending ids, one coalesced
 // store per bitmap word and warp; it then rearms the counter for the next call.
 constexpr int FL_MAX_WPT = 4;  // bitmap words per thread: n <= 131072 = 4 * 32 * CT_NT
+// Tokens (and bitmap words) a thread holds: clusters of 1 and 4 cover n <= 8192 and n <= 32768,
+// so a CTA's chunk is at most 8 * CT_NT tokens and the whole bitmap at most CT_NT words.
+template <int CL>
+struct PerThread {
+    static constexpr int tokens = CL == CT_MAX_CL ? 16 : 8;
+    static constexpr int words = CL == CT_MAX_CL ? FL_MAX_WPT : 1;
+};
 
 __device__ __forceinline__ int atomic_add_acq_rel(int *p, int v) {
     int old;
@@ -387,14 +394,15 @@ __device__ __forceinline__ void fetch_list_tail(const CertifyArgs &a, int ul, in
     if (!s_last) return;
     const uint32_t *res = a.resident + (size_t)ug * W;
     const uint32_t *F0 = a.F + (size_t)ul * G * W;
-    const int wpt = (W + CT_NT - 1) / CT_NT;  // <= FL_MAX_WPT
+    constexpr int WPT = PerThread<CL>::words;
+    const int wpt = (W + CT_NT - 1) / CT_NT;  // <= WPT
     const int w0 = tid * wpt;
-    uint32_t fw[FL_MAX_WPT];
-    int cnt[FL_MAX_WPT];
+    uint32_t fw[WPT];
+    int cnt[WPT];
     int my = 0;
     int nf[8] = {0, 0, 0, 0, 0, 0, 0, 0};
 #pragma unroll
-    for (int i = 0; i < FL_MAX_WPT; ++i) {
+    for (int i = 0; i < WPT; ++i) {
         const int w = w0 + i;
         uint32_t f = 0u;
         if (i < wpt && w < W) {
@@ -455,7 +463,7 @@ __device__ __forceinline__ void fetch_list_tail(const CertifyArgs &a, int ul, in
         int base = __shfl_sync(0xFFFFFFFFu, pos, j);
         const int wj = __shfl_sync(0xFFFFFFFFu, w0, j);
 #pragma unroll
-        for (int i = 0; i < FL_MAX_WPT; ++i) {
+        for (int i = 0; i < WPT; ++i) {
             const uint32_t f = __shfl_sync(0xFFFFFFFFu, fw[i], j);
             if ((f >> lane) & 1u) {
                 const int p = base + __popc(f & below);
@@ -471,6 +479,8 @@ __device__ __forceinline__ void fetch_list_tail(const CertifyArgs &a, int ul, in
 
 template <int CL, bool SL>
 __global__ void __launch_bounds__(CT_NT, 1) k_certify(CertifyArgs a) {
+    pdl_wait();
+    pdl_trigger();
     extern __shared__ __align__(16) unsigned char smem_raw[];
     float *wrec = reinterpret_cast<float *>(smem_raw);
     float *xrec = wrec + CT_NW * CT_REC;
@@ -499,23 +509,30 @@ __global__ void __launch_bounds__(CT_NT, 1) k_certify(CertifyArgs a) {
     float m, D, C, nL;
     float tmax = NEG_INF;
     {
-        for (int i = tid; i < chunk; i += CT_NT) {
-            const int t = base + i;
-            float s = NEG_INF, r = 1.0f;
-            if (t < n) {
-                s = sc[t];
-                r = rf[t];
+        // All of the thread's loads are issued before any is used.
+        constexpr int TPT = PerThread<CL>::tokens;
+        float sv[TPT], rv[TPT];
+#pragma unroll
+        for (int k = 0; k < TPT; ++k) {
+            const int i = tid + k * CT_NT, t = base + i;
+            sv[k] = NEG_INF;
+            rv[k] = 1.0f;
+            if (i < chunk && t < n) {
+                sv[k] = sc[t];
+                rv[k] = rf[t];
             }
-            W[i] = s;
-            R[i] = r;
-            tmax = fmaxf(tmax, s);
+            tmax = fmaxf(tmax, sv[k]);
         }
         float d = 0.f, c = 0.f, cnt = 0.f;
-        for (int i = tid; i < chunk; i += CT_NT) {
-            const float e = tmax == NEG_INF ? 0.0f : expf(W[i] - tmax);  // 0 for padding
+#pragma unroll
+        for (int k = 0; k < TPT; ++k) {
+            const int i = tid + k * CT_NT;
+            if (i >= chunk) break;
+            const float e = tmax == NEG_INF ? 0.0f : expf(sv[k] - tmax);  // 0 for padding
             W[i] = e;  // exp(logit - this thread's max); rescaled to w-hat once m is known
+            R[i] = rv[k];
             d += e;
-            const float r = R[i];
+            const float r = rv[k];
             if (r < 1.0f) {
                 c += e * (1.0f - r);
                 cnt += 1.0f;
@@ -947,13 +964,15 @@ static cudaError_t launch_certify_cl(const CertifyArgs &a, int qheads, size_t sm
     cfg.blockDim = dim3(CT_NT);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = s;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = CL;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;  // see launch_pdl
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = 2;
     return cudaLaunchKernelEx(&cfg, k_certify<CL, SL>, a);
 }
 

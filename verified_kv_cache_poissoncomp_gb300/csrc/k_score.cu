@@ -123,6 +123,8 @@ __device__ __forceinline__ unsigned long long bf16x2_to_f32x2(uint32_t w) {
 // per head.
 template <int D, int G>
 __global__ void __launch_bounds__(SC_NT, SC_CTAS_PER_SM) k_score(ScoreArgs a, int spans_per_unit, int span_rows) {
+    pdl_wait();
+    pdl_trigger();
     constexpr int CPL = G <= 4 ? 16 : 8, NV = CPL / 8;
     constexpr int LPR = D / CPL, RPW = 32 / LPR, NW = SC_NT / 32;
     constexpr int ROWB = D * 2;                       // bytes per sketch row
@@ -250,8 +252,7 @@ cudaError_t launch_score(const ScoreArgs &a, int units_layer, cudaStream_t s) {
             if (e != cudaSuccess) return e;                                                     \
             attr = true;                                                                        \
         }                                                                                       \
-        k_score<DD, GG><<<grid, SC_NT, smem, s>>>(a, spans, (int)span_rows);                                    \
-        return cudaGetLastError();                                                              \
+        return launch_pdl(k_score<DD, GG>, grid, dim3(SC_NT), smem, s, a, spans, (int)span_rows); \
     }
     VERKV_SCORE(128, 1) VERKV_SCORE(128, 2) VERKV_SCORE(128, 4) VERKV_SCORE(128, 8)
     VERKV_SCORE(64, 1) VERKV_SCORE(64, 2) VERKV_SCORE(64, 4) VERKV_SCORE(64, 8)

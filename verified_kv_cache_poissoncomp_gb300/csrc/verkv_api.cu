@@ -43,7 +43,7 @@ bool make_layout(const verkv_shape *s, Layout &L) {
     L.W = (s->n + 31) / 32;
     L.units_layer = s->batch * s->kv_heads;
     L.qh_layer = L.units_layer * s->q_per_kv;
-    L.max_piv = (s->cap + PART_ROWS - 1) / PART_ROWS;
+    L.max_piv = (s->cap + FET_ITEM_ROWS - 1) / FET_ITEM_ROWS;
     L.max_fet = (s->n + FET_ITEM_ROWS - 1) / FET_ITEM_ROWS;
     L.dense_chunks = (s->n + PART_ROWS - 1) / PART_ROWS;  // >= max_fet: sizes the shared buffer
     size_t off = 0;
@@ -219,6 +219,35 @@ LayerIdx layer_idx(const verkv_ctx *ctx, int layer) {
     li.kv_heads = ctx->sh.kv_heads;
     li.G = ctx->sh.q_per_kv;
     return li;
+}
+
+// Arguments of the pivotal partial sums of one layer call.
+PartialArgs pivotal_args(const verkv_ctx *ctx, const verkv_pivotal &piv, const void *q,
+                         const LayerIdx &li) {
+    const int d = ctx->sh.head_dim;
+    PartialArgs pa{};
+    pa.rows = (const uint16_t *)piv.kv;
+    pa.ids = piv.ids;
+    pa.pr = piv.r;
+    pa.count = piv.count;
+    pa.q = (const uint16_t *)q;
+    pa.F = ctx->F;
+    pa.qstats = ctx->qstats;
+    pa.scores = ctx->scores;
+    pa.part = ctx->part_piv;
+    pa.err = ctx->err;
+    pa.row_stride = ctx->sh.cap;
+    pa.max_chunks = ctx->L.max_piv;
+    pa.n = ctx->sh.n;
+    pa.W = ctx->L.W;
+    pa.d = d;
+    pa.mode = ROWS_PIVOTAL;
+    pa.keys = nullptr;
+    pa.row16 = d / 4;
+    pa.voff16 = d / 8;
+    pa.scale = (float)(1.0 / sqrt((double)d));
+    pa.li = li;
+    return pa;
 }
 
 }  // namespace
@@ -490,32 +519,17 @@ verkv_status verkv_attend_verified(verkv_ctx *ctx, int32_t layer, const void *q,
     VERKV_CUDA(tracked(ctx, VERKV_K_CERTIFY, ctx->main, [&] {
                    return launch_certify(ca, ctx->L.qh_layer, certify_smem_bytes(ca.chunk), ctx->main);
                }), "k_certify");
-    VERKV_CUDA(cudaEventRecord(ctx->e_sel, ctx->main), "cudaEventRecord");
+    // MEMCPY mode: verkv_fetch_refine waits on the host for the selection
+    if (ctx->fetch_mode != VERKV_FETCH_ZEROCOPY)
+        VERKV_CUDA(cudaEventRecord(ctx->e_sel, ctx->main), "cudaEventRecord");
 
-    PartialArgs pa{};
-    pa.rows = (const uint16_t *)pivotal->kv;
-    pa.ids = pivotal->ids;
-    pa.pr = pivotal->r;
-    pa.count = pivotal->count;
-    pa.q = (const uint16_t *)q;
-    pa.F = ctx->F;
-    pa.qstats = ctx->qstats;
-    pa.scores = ctx->scores;
-    pa.part = ctx->part_piv;
-    pa.err = ctx->err;
-    pa.row_stride = ctx->sh.cap;
-    pa.max_chunks = ctx->L.max_piv;
-    pa.n = n;
-    pa.W = ctx->L.W;
-    pa.d = d;
-    pa.mode = ROWS_PIVOTAL;
-    pa.keys = nullptr;
-    pa.row16 = d / 4;
-    pa.voff16 = d / 8;
-    pa.scale = sa.scale;
-    pa.li = li;
-    int grid = std::min(ctx->L.units_layer * ctx->L.max_piv, ctx->sms * 8);
-    VERKV_CUDA(tracked(ctx, VERKV_K_PARTIAL_PIVOTAL, ctx->main, [&] { return launch_partial(pa, ctx->L.units_layer, std::max(grid, 1), ctx->main); }), "k_partial");
+    // The pivotal partial sums need only the selection: in MEMCPY mode they run here, during the
+    // host gather; the zero-copy refine kernel of verkv_fetch_refine does them itself.
+    if (ctx->fetch_mode != VERKV_FETCH_ZEROCOPY) {
+        const PartialArgs pa = pivotal_args(ctx, *pivotal, q, li);
+        int grid = std::min(ctx->L.units_layer * ctx->L.max_piv, ctx->sms * 8);
+        VERKV_CUDA(tracked(ctx, VERKV_K_PARTIAL_PIVOTAL, ctx->main, [&] { return launch_partial(pa, ctx->L.units_layer, std::max(grid, 1), ctx->main); }), "k_partial");
+    }
 
     ctx->pending = true;
     ctx->attended = true;
@@ -566,9 +580,24 @@ verkv_status verkv_fetch_refine(verkv_ctx *ctx, const int32_t *ids, const int32_
     pa.keys = v_only ? (const uint16_t *)ctx->sketch : nullptr;
     int grid = std::max(1, std::min(ctx->L.units_layer * ctx->L.max_fet, ctx->sms * 8));
 
+    MergeArgs ma{};
+    ma.part_piv = ctx->part_piv;
+    ma.part_fet = ctx->part_fet;
+    ma.pcount = ctx->piv.count;
+    ma.fcount = ctx->fcounts;
+    ma.qstats = ctx->qstats;
+    ma.o = o_out;
+    ma.lse = lse_out;
+    ma.stats = stats_out;
+    ma.max_piv = ctx->L.max_piv;
+    ma.max_fet = ctx->L.max_fet;
+    ma.cap = ctx->sh.cap;
+    ma.d = d;
+    ma.li = li;
+
     if (ctx->fetch_mode == VERKV_FETCH_ZEROCOPY) {
-        // The fetch and the refine in one kernel on the side stream, reading page-locked host
-        // memory directly; it overlaps the pivotal partial sums on the main stream.
+        // One kernel on the context's stream for the pivotal partial sums and the fetched rows,
+        // read straight from page-locked host memory; the merge follows.
         cudaPointerAttributes attr;
         cudaError_t e = cudaPointerGetAttributes(&attr, host_kv);
         if (e != cudaSuccess || attr.type != cudaMemoryTypeHost || !attr.devicePointer) {
@@ -579,13 +608,12 @@ verkv_status verkv_fetch_refine(verkv_ctx *ctx, const int32_t *ids, const int32_
         pa.mode = ROWS_HOST;
         pa.row16 = d / 4;
         pa.voff16 = d / 8;
-        // Many rows in flight keep the host link busy; the pivotal partial sums on the main
-        // stream finish well within the fetch.
-        grid = std::max(1, std::min(ctx->L.units_layer * ctx->L.max_fet, ctx->sms * 8));
-        VERKV_CUDA(cudaStreamWaitEvent(ctx->side, ctx->e_sel, 0), "cudaStreamWaitEvent");
-        VERKV_CUDA(tracked(ctx, VERKV_K_FETCH_HOST, ctx->side, [&] { return launch_partial(pa, ctx->L.units_layer, grid, ctx->side); }), "k_partial(host)");
-        VERKV_CUDA(cudaEventRecord(ctx->e_fetch, ctx->side), "cudaEventRecord");
-        VERKV_CUDA(cudaStreamWaitEvent(ctx->main, ctx->e_fetch, 0), "cudaStreamWaitEvent");
+        const PartialArgs piv = pivotal_args(ctx, ctx->piv, ctx->q, li);
+        const int items = ctx->L.units_layer * (ctx->L.max_fet + ctx->L.max_piv);
+        grid = std::max(1, std::min(items, ctx->sms * 8));
+        VERKV_CUDA(tracked(ctx, VERKV_K_FETCH_HOST, ctx->main, [&] {
+                       return launch_refine(piv, pa, ctx->L.units_layer, grid, ctx->main);
+                   }), "k_refine");
     } else {
         VERKV_CUDA(cudaEventSynchronize(ctx->e_sel), "cudaEventSynchronize");
         const int U = ctx->L.units_layer;
@@ -625,20 +653,6 @@ verkv_status verkv_fetch_refine(verkv_ctx *ctx, const int32_t *ids, const int32_
         VERKV_CUDA(tracked(ctx, VERKV_K_PARTIAL_STAGED, ctx->main, [&] { return launch_partial(pa, ctx->L.units_layer, grid, ctx->main); }), "k_partial(staged)");
     }
 
-    MergeArgs ma{};
-    ma.part_piv = ctx->part_piv;
-    ma.part_fet = ctx->part_fet;
-    ma.pcount = ctx->piv.count;
-    ma.fcount = ctx->fcounts;
-    ma.qstats = ctx->qstats;
-    ma.o = o_out;
-    ma.lse = lse_out;
-    ma.stats = stats_out;
-    ma.max_piv = ctx->L.max_piv;
-    ma.max_fet = ctx->L.max_fet;
-    ma.cap = ctx->sh.cap;
-    ma.d = d;
-    ma.li = li;
     VERKV_CUDA(tracked(ctx, VERKV_K_MERGE, ctx->main, [&] { return launch_merge(ma, ctx->L.qh_layer, ctx->main); }), "k_merge");
     ctx->pending = false;
     return VERKV_OK;
@@ -751,7 +765,7 @@ verkv_status verkv_launch_counts(verkv_ctx *ctx, int64_t *out) {
 const char *verkv_kernel_name(int k) {
     static const char *names[VERKV_K_COUNT] = {
         "k_pc_solve", "k_pc_gather", "k_sketch", "k_score", "k_certify",
-        "k_partial(pivotal)", "k_partial(host)", "k_partial(staged)", "k_merge",
+        "k_partial(pivotal)", "k_refine", "k_partial(staged)", "k_merge",
         "k_dense_host", "k_dense_merge", "k_shortlist"};
     return (k >= 0 && k < VERKV_K_COUNT) ? names[k] : "";
 }

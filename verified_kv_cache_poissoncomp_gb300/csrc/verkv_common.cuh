@@ -13,6 +13,14 @@ namespace cg = cooperative_groups;
 
 __device__ __forceinline__ void raise_error(uint32_t *err, uint32_t bit) { atomicOr(err, bit); }
 
+// Programmatic dependent launch.  A kernel started through launch_pdl may begin while the kernel
+// before it on the stream is still running: pdl_wait() returns once that kernel has completed
+// and its memory is visible, so every such kernel calls it before touching anything the stream
+// produced.  pdl_trigger() lets the next kernel be scheduled early; it only waits in turn.
+// Without the launch attribute both are no-ops.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 // ---------------------------------------------------------------------------------------------
 // bf16 pairs packed in a 32-bit word: element 0 in the low half.
 __device__ __forceinline__ float bf16lo(uint32_t x) { return __uint_as_float(x << 16); }

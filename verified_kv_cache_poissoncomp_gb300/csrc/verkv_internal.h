@@ -51,6 +51,25 @@ int q2_row_bytes(int d);
 cudaError_t launch_sketch_q2(const uint16_t *kv_full, uint8_t *sketch, int64_t rows, int d,
                              cudaStream_t s);
 
+// Launch `kernel` on stream s with programmatic stream serialisation: it may start before the
+// previous kernel on s has finished, and must call pdl_wait() before reading what the stream
+// produced (the decode path's kernels do so first thing).
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                       Args &&...args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, static_cast<Args &&>(args)...);
+}
+
 // ---------------------------------------------------------------------------------------------
 // Layer-local indexing of a decode call: u' = b * kv_heads + h (units of the layer), query head
 // qh = u' * G + g, global unit u = (b * layers + layer) * kv_heads + h.
@@ -175,5 +194,10 @@ struct MergeArgs {
     LayerIdx li;
 };
 cudaError_t launch_merge(const MergeArgs &a, int qheads, cudaStream_t s);
+
+// The zero-copy path's partial sums in one launch: the ROWS_HOST blocks (fet) and the
+// ROWS_PIVOTAL blocks (piv) of every layer unit; launch_merge follows.
+cudaError_t launch_refine(const PartialArgs &piv, const PartialArgs &fet, int units_layer, int grid,
+                          cudaStream_t s);
 
 }  // namespace verkv
