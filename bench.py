@@ -295,13 +295,15 @@ def run_ours(args, world, rank, local):
         tau_dev = eng.tau
         kv_dev = eng.kv
 
-    def step():
+    # The timed steps ask for no fetch ids or counts (the refine reads the selection bitmaps);
+    # one untimed pass with counts gives the rows moved per KV head for the statistics.
+    def step(counts=False):
         B.verkv_poissoncomp(eng.ctx, tau_dev.data_ptr(), w.eta, B.verkv_hset(w.n_sink, w.n_local),
                             w.seed, kv_dev.data_ptr(), eng.r_full.data_ptr(), eng.pivotal)
         for t in range(Q):
             B.verkv_attend_verified(eng.ctx, int(w.query_layer[t]), q_dev[t].data_ptr(),
                                     eng.pivotal, eng.r_full.data_ptr(), eng.sketch_desc, w.eps,
-                                    w.delta, None, fc_all[t].data_ptr())
+                                    w.delta, None, fc_all[t].data_ptr() if counts else None)
             B.verkv_fetch_refine(eng.ctx, None, None, eng.host_kv.data_ptr(),
                                  o_all[t].data_ptr(), lse_all[t].data_ptr(), st_all[t].data_ptr())
 
@@ -384,6 +386,9 @@ def run_ours(args, world, rank, local):
 
     # Algorithmic bytes per launch of each kernel of the step ("Roofline"); the bound
     # is HBM except for the fetch, which is bound by the host link.
+    with torch.cuda.stream(stream):
+        step(counts=True)
+    B.verkv_sync(eng.ctx)
     counts = eng.p_count.cpu().numpy().astype(np.int64)
     st = st_all.cpu().numpy()
     fetched_rows = fc_all.cpu().numpy().astype(np.int64)          # [Q][units] of the last step
@@ -625,13 +630,13 @@ def run_eps_sweep(args, local):
         st_all = torch.empty((Q, hq, 16), dtype=torch.int32, device=dev)
         fc_all = torch.zeros((Q, w.B * w.h_kv), dtype=torch.int32, device=dev)
 
-    def step(eps):
+    def step(eps, counts=False):  # counts: an untimed pass for the statistics
         B.verkv_poissoncomp(eng.ctx, eng.tau.data_ptr(), w.eta, B.verkv_hset(w.n_sink, w.n_local),
                             w.seed, eng.kv.data_ptr(), eng.r_full.data_ptr(), eng.pivotal)
         for t in range(Q):
             B.verkv_attend_verified(eng.ctx, int(w.query_layer[t]), q_dev[t].data_ptr(),
                                     eng.pivotal, eng.r_full.data_ptr(), eng.sketch_desc, eps,
-                                    w.delta, None, fc_all[t].data_ptr())
+                                    w.delta, None, fc_all[t].data_ptr() if counts else None)
             B.verkv_fetch_refine(eng.ctx, None, None, eng.host_kv.data_ptr(),
                                  o_all[t].data_ptr(), lse_all[t].data_ptr(), st_all[t].data_ptr())
 
@@ -657,6 +662,9 @@ def run_eps_sweep(args, local):
         torch.cuda.synchronize()
         B.verkv_sync(eng.ctx)
         ms = e0.elapsed_time(e1) / args.steps
+        with torch.cuda.stream(stream):
+            step(eps, counts=True)
+        B.verkv_sync(eng.ctx)
         if counts is None:
             counts = eng.p_count.cpu().numpy().astype(np.int64)
         fr = fc_all.cpu().numpy().astype(np.int64)
@@ -716,11 +724,11 @@ def run_long128k(args, local):
     row_bytes = (2 if args.sketch == "exact" else 4) * w.d
     rows = []
     for eps in (0.02, 0.05):
-        def step():
+        def step(counts=False):  # counts: an untimed pass for the statistics
             for t in range(Q):
                 B.verkv_attend_verified(eng.ctx, int(w.query_layer[t]), q_dev[t].data_ptr(),
                                         eng.pivotal, eng.r_full.data_ptr(), eng.sketch_desc, eps,
-                                        w.delta, None, fc_all[t].data_ptr())
+                                        w.delta, None, fc_all[t].data_ptr() if counts else None)
                 B.verkv_fetch_refine(eng.ctx, None, None, eng.host_kv.data_ptr(),
                                      o_all[t].data_ptr(), lse_all[t].data_ptr(),
                                      st_all[t].data_ptr())
@@ -749,6 +757,9 @@ def run_long128k(args, local):
             step()
         launches, total_ms = B.verkv_profile_read(eng.ctx)
         B.verkv_profile_enable(eng.ctx, 0)
+        with torch.cuda.stream(stream):
+            step(counts=True)
+        B.verkv_sync(eng.ctx)
         fr = fc_all.cpu().numpy().astype(np.int64)
         st = st_all.cpu().numpy()
         h2d = float(fr.sum(1).mean()) * row_bytes

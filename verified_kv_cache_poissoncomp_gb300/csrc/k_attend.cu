@@ -3,8 +3,8 @@
 // Definition 2 / Eq. (5), KVFETCH step 5; abstract page: fetch additional tokens from the CPU and
 // refine the attention computation).
 //
-// k_partial   split-K over a row set: each CTA item is a block of FET_ITEM_ROWS rows of one KV
-//             head, taken 64 at a time; each row a contiguous 4d-byte K|V pair read with 16-byte
+// k_partial   split-K over a row set: each CTA item is a block of FET_ITEM_ROWS pivotal rows, or
+//             the fetched rows of one FET_RANGE token-id range, of one KV head, taken 64 at a time; each row a contiguous 4d-byte K|V pair read with 16-byte
 //             coalesced loads, four row groups in flight per warp (all of them for host rows),
 //             accumulated into one partial.  It computes the G logits, w = exp(logit - m), the
 //             weight of Eq. (5) -- 1 for H and for tokens of F, lambda / r for sampled, unfetched
@@ -18,8 +18,9 @@
 //                              id -- the zero-copy fetch and the refine in one pass, no staging.
 //             When the sketch is exact the GPU already holds every key, so K comes from the sketch
 //             by token id and only the V rows cross the host link.
-// k_refine    the zero-copy path's partial sums in one launch: the ROWS_HOST and ROWS_PIVOTAL
-//             items of every KV head.
+// k_refine    the zero-copy path's partial sums in one launch: the ROWS_HOST items of every KV
+//             head, each deriving its rows from the selection bitmaps of one token-id range (no
+//             fetch list needed), and the ROWS_PIVOTAL items.
 // k_merge     sums the partials in a fixed order and writes o = N-hat / D-hat, m + log D-hat and
 //             the per-head statistics.
 // k_dense_host, k_dense_merge   the offloaded-dense baseline: exact attention over every token with
@@ -104,11 +105,14 @@ __device__ __forceinline__ uint4 ld_host(const uint4 *p) {
     return v;
 }
 
-// One item of the split-K sums: rows [ch * ITEM, (ch + 1) * ITEM) of layer unit `ul`, taken
-// PART_ROWS at a time.  Returns false, uniformly over the CTA, when the block lies past the
-// unit's rows (nothing is written).
-template <int D, int G, int MODE, int ITEM>
-__device__ __forceinline__ bool partial_item(const PartialArgs &a, int ul, int ch) {
+// One item of the split-K sums: positions [lo, hi) of a row list of layer unit `ul` (ids[p] is
+// the token id at position p), taken PART_ROWS at a time, into partial `part_idx`.  Row data is
+// addressed by token id (ROWS_HOST: the unit's host cache) or by list position (ROWS_PIVOTAL:
+// the pivotal buffer; ROWS_STAGED: the staged rows).  An empty item writes nothing unless
+// write_empty (then a zero partial).  lo and hi are uniform over the CTA.
+template <int D, int G, int MODE>
+__device__ __forceinline__ void partial_rows(const PartialArgs &a, int ul, int part_idx, int lo,
+                                             int hi, const int32_t *ids, bool write_empty) {
     constexpr int LPR = D / 8, RPW = 32 / LPR, NW = 4;
     constexpr int ITER = (PART_ROWS / NW) / RPW;  // row groups per warp
     // Row groups in flight per warp: all of them for host rows (link latency), else four.
@@ -121,14 +125,12 @@ __device__ __forceinline__ bool partial_item(const PartialArgs &a, int ul, int c
     const int cgp = lane % LPR, rg = lane / LPR;
     const int myhead = head_of_lane<G, LPR>(lane);
     const int hq = a.li.kv_heads * G;
+    if (lo >= hi && !write_empty) return;
 
     {
         const int b = ul / a.li.kv_heads, h = ul - b * a.li.kv_heads;
         const int ug = a.li.unit_global(ul);
         const int src = MODE == ROWS_PIVOTAL ? ug : ul;
-        int rows_u = a.count[src];
-        if (rows_u > a.row_stride) rows_u = a.row_stride;
-        if (ch * ITEM >= rows_u) return false;  // uniform over the CTA
 
         float qv[G][8];
 #pragma unroll
@@ -147,7 +149,6 @@ __device__ __forceinline__ bool partial_item(const PartialArgs &a, int ul, int c
             for (int c = 0; c < 8; ++c) acc[g][c] = 0.0f;
         float dacc = 0.0f, m2acc = 0.0f;
 
-        const int32_t *ids = a.ids + (size_t)src * a.row_stride;
         const float *prs = MODE == ROWS_PIVOTAL ? a.pr + (size_t)src * a.row_stride : nullptr;
         // ROWS_HOST indexes the full host cache of the unit by token id; the others by row.
         const uint4 *rows = reinterpret_cast<const uint4 *>(a.rows) +
@@ -155,9 +156,7 @@ __device__ __forceinline__ bool partial_item(const PartialArgs &a, int ul, int c
         const uint4 *keys = a.keys ? reinterpret_cast<const uint4 *>(a.keys) + (size_t)ug * a.n * (D / 8)
                                    : nullptr;
 #pragma unroll 1
-        for (int sub = 0; sub < ITEM / PART_ROWS; ++sub) {
-        const int cbase = ch * ITEM + sub * PART_ROWS;
-        if (cbase >= rows_u) break;  // uniform over the CTA
+        for (int cbase = lo; cbase < hi; cbase += PART_ROWS) {
         const int rbase = cbase + warp * (PART_ROWS / NW);
 #pragma unroll 1
         for (int it0 = 0; it0 < ITER; it0 += U) {
@@ -167,7 +166,7 @@ __device__ __forceinline__ bool partial_item(const PartialArgs &a, int ul, int c
 #pragma unroll
             for (int u = 0; u < U; ++u) {
                 const int row = rbase + (it0 + u) * RPW + rg;
-                valid[u] = row < rows_u;
+                valid[u] = row < hi;
                 id[u] = valid[u] ? ids[row] : 0;
                 if ((unsigned)id[u] >= (unsigned)a.n) {  // not a token of the unit: skip the row
                     raise_error(a.err, ERR_BADID);
@@ -269,7 +268,7 @@ __device__ __forceinline__ bool partial_item(const PartialArgs &a, int ul, int c
             sM[warp][rg][myhead] = m2acc;
         }
         __syncthreads();
-        float *out = a.part + ((size_t)ul * a.max_chunks + ch) * G * (D + 2);
+        float *out = a.part + ((size_t)ul * a.max_chunks + part_idx) * G * (D + 2);
         for (int e = tid; e < G * (D + 2); e += 128) {
             const int g = e / (D + 2), c = e - g * (D + 2);
             float s = 0.0f;
@@ -291,19 +290,52 @@ __device__ __forceinline__ bool partial_item(const PartialArgs &a, int ul, int c
         }
         __syncthreads();
     }
-    return true;
 }
 
-// Every row source in blocks of FET_ITEM_ROWS rows (FET_SUB blocks of PART_ROWS accumulated per
-// partial), as in k_refine, so that both fetch modes produce the same partials.
+// The fetched rows of layer unit `ul` with token ids in [k * FET_RANGE, (k + 1) * FET_RANGE):
+// positions [lo, hi) of the unit's ascending fetch list (binary search, one thread).
+__device__ __forceinline__ void range_bounds(const int32_t *list, int count, int k, int &lo, int &hi) {
+    __shared__ int s_b[2];
+    if (threadIdx.x == 0) {
+        for (int e = 0; e < 2; ++e) {
+            const int key = (k + e) * FET_RANGE;
+            int l = 0, r = count;  // first position whose id >= key
+            while (l < r) {
+                const int m = (l + r) >> 1;
+                if (list[m] < key) l = m + 1;
+                else r = m;
+            }
+            s_b[e] = l;
+        }
+    }
+    __syncthreads();
+    lo = s_b[0];
+    hi = s_b[1];
+    __syncthreads();
+}
+
+// Pivotal rows in blocks of FET_ITEM_ROWS list positions; staged fetched rows by token-id range
+// (FET_RANGE ids per partial, a zero partial for an empty range), as k_refine reads them from
+// host memory, so that both fetch modes produce the same partials.
 template <int D, int G, int MODE>
 __global__ void __launch_bounds__(128) k_partial(PartialArgs a, int units_layer) {
     pdl_wait();
     pdl_trigger();
     const int total_items = units_layer * a.max_chunks;
     for (int item = blockIdx.x; item < total_items; item += gridDim.x) {
-        const int ul = item / a.max_chunks;
-        partial_item<D, G, MODE, FET_ITEM_ROWS>(a, ul, item - ul * a.max_chunks);
+        const int ul = item / a.max_chunks, ch = item - ul * a.max_chunks;
+        if (MODE == ROWS_PIVOTAL) {
+            const int ug = a.li.unit_global(ul);
+            const int count = min(a.count[ug], a.row_stride);
+            const int lo = ch * FET_ITEM_ROWS;
+            partial_rows<D, G, MODE>(a, ul, ch, lo, min(lo + FET_ITEM_ROWS, count),
+                                     a.ids + (size_t)ug * a.row_stride, false);
+        } else {
+            const int32_t *list = a.ids + (size_t)ul * a.row_stride;
+            int lo, hi;
+            range_bounds(list, min(a.count[ul], a.row_stride), ch, lo, hi);
+            partial_rows<D, G, MODE>(a, ul, ch, lo, hi, list, true);
+        }
     }
 }
 
@@ -325,7 +357,8 @@ cudaError_t launch_partial(const PartialArgs &a, int units_layer, int grid, cuda
 
 // ---------------------------------------------------------------------------------------------
 // k_merge: one CTA per query head; 8 groups of 128 threads each sum every eighth chunk of their
-// columns (pivotal chunks, then fetched ones), then the groups are added in a fixed order.
+// columns (pivotal chunks, then the per-range fetched ones), then the groups are added in a
+// fixed order.
 constexpr int MG_NT = 1024;
 constexpr int MG_GROUPS = MG_NT / 128;
 
@@ -341,7 +374,7 @@ __global__ void __launch_bounds__(MG_NT) k_merge(MergeArgs a) {
     int pc = a.pcount[ug];
     if (pc > a.cap) pc = a.cap;
     const int npc = (pc + FET_ITEM_ROWS - 1) / FET_ITEM_ROWS;
-    const int nfc = (a.fcount[ul] + FET_ITEM_ROWS - 1) / FET_ITEM_ROWS;
+    const int nfc = a.max_fet;  // one partial per token-id range, empty ranges included
     const int grp = threadIdx.x / 128, c0 = threadIdx.x % 128;
     const float *pp = a.part_piv + ((size_t)ul * a.max_piv * G + g) * ncol;
     const float *pf = a.part_fet + ((size_t)ul * a.max_fet * G + g) * ncol;
@@ -370,6 +403,10 @@ __global__ void __launch_bounds__(MG_NT) k_merge(MergeArgs a) {
         st.D_hat = Dh;
         st.M2 = red[D + 1];
         st.lse = st.m + logf(Dh);
+        if (a.nacc) {
+            st.n_fetch = a.nacc[qh];
+            a.nacc[qh] = 0;  // ready for the next call
+        }
         if (a.lse) a.lse[qh] = st.lse;
         if (a.stats) a.stats[qh] = st;
     }
@@ -380,19 +417,67 @@ cudaError_t launch_merge(const MergeArgs &a, int qheads, cudaStream_t s) {
 }
 
 // ---------------------------------------------------------------------------------------------
-// k_refine: the zero-copy path's partial sums in one launch -- the fetched-row blocks of every
+// k_refine: the zero-copy path's partial sums in one launch -- the fetched-row ranges of every
 // layer unit first (so the host reads start at once), then its pivotal blocks (their HBM reads
 // hide behind the host link).  k_merge follows.
 template <int D, int G>
 __global__ void __launch_bounds__(128, 3) k_refine(PartialArgs piv, PartialArgs fet, int units_layer) {
     pdl_wait();
     pdl_trigger();
+    constexpr int WR = FET_RANGE / 32;  // bitmap words per range (one thread each)
+    static_assert(WR == 32 || WR == 64, "the range's words are scanned by one or two warps");
+    __shared__ int32_t s_ids[FET_RANGE];
+    __shared__ int s_wsum[2];
     const int per_unit = fet.max_chunks + piv.max_chunks;
     const int total = units_layer * per_unit;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     for (int item = blockIdx.x; item < total; item += gridDim.x) {
         const int k = item / units_layer, ul = item - k * units_layer;
-        if (k < fet.max_chunks) partial_item<D, G, ROWS_HOST, FET_ITEM_ROWS>(fet, ul, k);
-        else partial_item<D, G, ROWS_PIVOTAL, FET_ITEM_ROWS>(piv, ul, k - fet.max_chunks);
+        const int ug = fet.li.unit_global(ul);
+        if (k < fet.max_chunks) {
+            // The rows to fetch in this token range: (OR over the unit's query heads of F) minus
+            // the resident tokens, compacted in ascending id order; per query head, the count of
+            // its own F minus the resident tokens adds into n_fetch.
+            const int w = k * WR + tid;
+            uint32_t uw = 0u;
+            int nf[G];
+#pragma unroll
+            for (int g = 0; g < G; ++g) nf[g] = 0;
+            if (tid < WR && w < fet.W) {
+                const uint32_t rw = fet.resident[(size_t)ug * fet.W + w];
+#pragma unroll
+                for (int g = 0; g < G; ++g) {
+                    const uint32_t fg = fet.F[(size_t)(ul * G + g) * fet.W + w] & ~rw;
+                    uw |= fg;
+                    nf[g] = __popc(fg);
+                }
+            }
+#pragma unroll
+            for (int g = 0; g < G; ++g) {
+                const int t = warp_sum(nf[g]);
+                if (lane == 0 && warp < WR / 32 && t) atomicAdd(&fet.nacc[ul * G + g], t);
+            }
+            const int c = __popc(uw);
+            int incl = c;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int y = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+                if (lane >= o) incl += y;
+            }
+            if (lane == 31 && warp < 2) s_wsum[warp] = incl;
+            __syncthreads();
+            int pos = incl - c + (warp == 1 ? s_wsum[0] : 0);
+            const int cnt = s_wsum[0] + s_wsum[1];
+            for (uint32_t x = uw; x; x &= x - 1) s_ids[pos++] = w * 32 + (__ffs(x) - 1);
+            __syncthreads();
+            partial_rows<D, G, ROWS_HOST>(fet, ul, k, 0, cnt, s_ids, true);
+        } else {
+            const int ch = k - fet.max_chunks;
+            const int count = min(piv.count[ug], piv.row_stride);
+            const int lo = ch * FET_ITEM_ROWS;
+            partial_rows<D, G, ROWS_PIVOTAL>(piv, ul, ch, lo, min(lo + FET_ITEM_ROWS, count),
+                                             piv.ids + (size_t)ug * piv.row_stride, false);
+        }
     }
 }
 

@@ -24,7 +24,7 @@ namespace {
 size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 
 struct Layout {
-    size_t err, flc, scores, qstats, F, slb, fids, fcounts, staging, part_piv, part_fet, total;
+    size_t err, flc, nacc, scores, qstats, F, slb, fids, fcounts, staging, part_piv, part_fet, total;
     int W, units_layer, qh_layer, max_piv, max_fet, dense_chunks;
 };
 
@@ -44,7 +44,7 @@ bool make_layout(const verkv_shape *s, Layout &L) {
     L.units_layer = s->batch * s->kv_heads;
     L.qh_layer = L.units_layer * s->q_per_kv;
     L.max_piv = (s->cap + FET_ITEM_ROWS - 1) / FET_ITEM_ROWS;
-    L.max_fet = (s->n + FET_ITEM_ROWS - 1) / FET_ITEM_ROWS;
+    L.max_fet = (s->n + FET_RANGE - 1) / FET_RANGE;
     L.dense_chunks = (s->n + PART_ROWS - 1) / PART_ROWS;  // >= max_fet: sizes the shared buffer
     size_t off = 0;
     auto take = [&](size_t bytes) {
@@ -54,6 +54,7 @@ bool make_layout(const verkv_shape *s, Layout &L) {
     };
     L.err = take(256);
     L.flc = take((size_t)L.units_layer * 4);
+    L.nacc = take((size_t)L.qh_layer * 4);
     L.scores = take((size_t)L.qh_layer * n * 4);
     L.qstats = take((size_t)L.qh_layer * sizeof(verkv_head_stats));
     L.F = take((size_t)L.qh_layer * L.W * 4);
@@ -137,6 +138,7 @@ struct verkv_ctx {
     uint32_t *F = nullptr;
     int32_t *fids = nullptr, *fcounts = nullptr;
     int32_t *flc = nullptr;  // per-KV-head completion counters of the certify kernel's fetch list
+    int32_t *nacc = nullptr; // per-query-head n_fetch accumulators of the zero-copy refine
     uint32_t *slb = nullptr; // per-KV-head shortlist bitmaps
     int shortlist = 0;       // shortlist size per KV head; 0: every token of L may be fetched
     bool shortlisted = false;  // the last attend built shortlists
@@ -313,6 +315,7 @@ verkv_status verkv_create(verkv_ctx **out, int device, void *stream, const verkv
     ctx->fids = (int32_t *)(w + L.fids);
     ctx->fcounts = (int32_t *)(w + L.fcounts);
     ctx->flc = (int32_t *)(w + L.flc);
+    ctx->nacc = (int32_t *)(w + L.nacc);
     ctx->slb = (uint32_t *)(w + L.slb);
     ctx->staging = (uint16_t *)(w + L.staging);
     ctx->part_piv = (float *)(w + L.part_piv);
@@ -320,6 +323,7 @@ verkv_status verkv_create(verkv_ctx **out, int device, void *stream, const verkv
     e = cudaMemsetAsync(ctx->err, 0, 256, ctx->main);
     if (e == cudaSuccess) e = cudaMemsetAsync(ctx->fcounts, 0, (size_t)L.units_layer * 4, ctx->main);
     if (e == cudaSuccess) e = cudaMemsetAsync(ctx->flc, 0, (size_t)L.units_layer * 4, ctx->main);
+    if (e == cudaSuccess) e = cudaMemsetAsync(ctx->nacc, 0, (size_t)L.qh_layer * 4, ctx->main);
     if (e != cudaSuccess) {
         verkv_destroy(ctx);
         return VERKV_ECUDA;
@@ -507,7 +511,10 @@ verkv_status verkv_attend_verified(verkv_ctx *ctx, int32_t layer, const void *q,
     ca.eps = eps;
     ca.ldelta = (float)log(2.0 / (double)delta);
     ca.li = li;
-    ca.fl_counter = ctx->flc;
+    // The per-KV-head fetch list is built only for those who read it: the MEMCPY gather, or a
+    // caller asking for ids or counts.  The zero-copy refine reads the selection bitmaps.
+    const bool need_list = ctx->fetch_mode != VERKV_FETCH_ZEROCOPY || fetch_ids_out || fetch_counts_out;
+    ca.fl_counter = need_list ? ctx->flc : nullptr;
     ca.ids = ctx->fids;
     ca.counts = ctx->fcounts;
     ca.ids_user = fetch_ids_out;
@@ -608,6 +615,9 @@ verkv_status verkv_fetch_refine(verkv_ctx *ctx, const int32_t *ids, const int32_
         pa.mode = ROWS_HOST;
         pa.row16 = d / 4;
         pa.voff16 = d / 8;
+        pa.resident = ctx->piv.resident;
+        pa.nacc = ctx->nacc;
+        ma.nacc = ctx->nacc;
         const PartialArgs piv = pivotal_args(ctx, ctx->piv, ctx->q, li);
         const int items = ctx->L.units_layer * (ctx->L.max_fet + ctx->L.max_piv);
         grid = std::max(1, std::min(items, ctx->sms * 8));

@@ -140,7 +140,8 @@ size_t certify_smem_bytes(int chunk);
 // HBM, or fetched rows read by token id straight from page-locked host memory.
 constexpr int PART_ROWS = 64;                      // rows a CTA has in flight
 constexpr int FET_SUB = 4;                         // row blocks per partial for fetched rows
-constexpr int FET_ITEM_ROWS = PART_ROWS * FET_SUB; // rows per partial for fetched rows (pivotal: 64)
+constexpr int FET_ITEM_ROWS = PART_ROWS * FET_SUB; // pivotal list positions per partial
+constexpr int FET_RANGE = 1024;                    // token ids per partial of fetched rows
 enum { ROWS_PIVOTAL = 0, ROWS_STAGED = 1, ROWS_HOST = 2 };
 struct PartialArgs {
     const uint16_t *rows;     // [src units][row_stride][row16 vectors]; ROWS_HOST: [units][n][2][d]
@@ -157,6 +158,9 @@ struct PartialArgs {
     const float *scores;      // sketch logits [qh][n]: lambda of Definition 2 uses w-hat
     float *part;              // [units_layer][max_chunks][G][d + 2]
     uint32_t *err;            // ERR_BADID for a row id outside [0, n)
+    const uint32_t *resident; // ROWS_HOST in k_refine: the resident bitmaps [units][W]
+    int32_t *nacc;            // ROWS_HOST in k_refine: per query head n_fetch accumulators
+                              // [qh], zero on entry (k_merge resets them)
     int row_stride;           // cap (pivotal) or n (fetched)
     int max_chunks;
     int n, W, d;
@@ -190,6 +194,8 @@ struct MergeArgs {
     float *o;                    // [qh][d]
     float *lse;                  // [qh] or null
     verkv_head_stats *stats;     // [qh] or null
+    int32_t *nacc;               // per query head n_fetch counted by k_refine (read and reset),
+                                 // or null: qstats carries it (the certify kernel's fetch list)
     int max_piv, max_fet, cap, d;
     LayerIdx li;
 };
