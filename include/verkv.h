@@ -198,7 +198,10 @@ verkv_status verkv_sketch_build(verkv_ctx *ctx, const void *kv_full, int32_t for
  *                  KV head of this layer, the ascending ids of the union over its query heads of
  *                  F \ S (the rows that must move)
  *   fetch_counts_out optional int32 [batch*kv_heads]: the number of ids per KV head (either
- *                  output may be given without the other)
+ *                  output may be given without the other).  The list is built at the end of the
+ *                  certificate kernel only when one of the two is given or the fetch mode is
+ *                  MEMCPY; in ZEROCOPY mode verkv_fetch_refine reads the selection bitmaps
+ *                  directly, so a caller that needs neither output saves that step.
  * Per query head: sketch logits for all n tokens, w-hat = exp(logit - max), the beta fixed point,
  * the certificate, and when it fails the order of Eq. (9) (ties to the lower token id) and the
  * minimal k* of Eq. (10).  In MEMCPY mode the shrinkage-weighted partial sums over the pivotal
