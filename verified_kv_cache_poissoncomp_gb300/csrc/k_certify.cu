@@ -222,34 +222,30 @@ struct SelState {
     float eps_final;
 };
 
-// One pass's scan of the merged histogram by warp 0 and the select's next state (Eq. (10):
-// eps-hat of the remaining set, nonincreasing as tokens are taken in g order).
-__device__ __forceinline__ void select_step(const Merged &mh, SelState &ss, int lane, float SB,
-                                            float SV, float l, float epsD, float D) {
+// One pass's scan of the merged histogram and the select's next state (Eq. (10): eps-hat of the
+// remaining set, nonincreasing as tokens are taken in g order).  Threads 0..SEL_NT-1 take one bin
+// each: exact integer prefix sums (and a running max) of the bins below it give the remaining
+// set if the cut falls there; the cut bin is the last non-empty bin whose remaining set already
+// certifies, and its thread moves the select on.  The other threads do not take part.
+constexpr int SEL_NT = 256;  // = bins per pass
+struct SelScratch {
+    uint32_t c[SEL_NT / 32], m[SEL_NT / 32];
+    unsigned long long b[SEL_NT / 32], v[SEL_NT / 32];
+    int best[SEL_NT / 32];
+};
+__device__ __forceinline__ void sel_bar() { asm volatile("bar.sync 1, %0;" ::"n"(SEL_NT) : "memory"); }
+
+__device__ __forceinline__ void select_step(const Merged &mh, SelState &ss, SelScratch &sx, int tid,
+                                            float SB, float SV, float l, float epsD, float D) {
+    const int lane = tid & 31, w = tid >> 5;
     const float iSB = SB > 0.0f ? 1.0f / SB : 0.0f;
     const float iSV = SV > 0.0f ? 1.0f / SV : 0.0f;
     const unsigned long long Bb = ss.Bb, Bv = ss.Bv;
     const uint32_t Bm = ss.Bm;
-    // Lane l holds bins 8l .. 8l+7, read with 16-byte loads (conflict-free).
-    const uint4 *pc = reinterpret_cast<const uint4 *>(mh.cnt) + 2 * lane;
-    const uint4 *pm = reinterpret_cast<const uint4 *>(mh.bm) + 2 * lane;
-    const ulonglong2 *pb = reinterpret_cast<const ulonglong2 *>(mh.sb) + 4 * lane;
-    const ulonglong2 *pv = reinterpret_cast<const ulonglong2 *>(mh.sv) + 4 * lane;
-    uint32_t lc, lm;
-    unsigned long long lb = 0ull, lv = 0ull;
-    {
-        const uint4 c0 = pc[0], c1 = pc[1], m0 = pm[0], m1 = pm[1];
-        lc = c0.x + c0.y + c0.z + c0.w + c1.x + c1.y + c1.z + c1.w;
-        lm = max(max(max(m0.x, m0.y), max(m0.z, m0.w)), max(max(m1.x, m1.y), max(m1.z, m1.w)));
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-            const ulonglong2 b = pb[k], v = pv[k];
-            lb += b.x + b.y;
-            lv += v.x + v.y;
-        }
-    }
-    uint32_t ic = lc, im = lm;
-    unsigned long long ib = lb, iv = lv;
+    const uint32_t c = mh.cnt[tid], m = mh.bm[tid];
+    const unsigned long long sb = mh.sb[tid], sv = mh.sv[tid];
+    uint32_t ic = c, im = m;
+    unsigned long long ib = sb, iv = sv;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
         const uint32_t yc = __shfl_up_sync(0xFFFFFFFFu, ic, o);
@@ -263,46 +259,42 @@ __device__ __forceinline__ void select_step(const Merged &mh, SelState &ss, int 
             iv += yv;
         }
     }
-    const uint32_t total = __shfl_sync(0xFFFFFFFFu, ic, 31);
-    uint32_t xc = ic - lc, xm = __shfl_up_sync(0xFFFFFFFFu, im, 1);
+    uint32_t xm = __shfl_up_sync(0xFFFFFFFFu, im, 1);
     if (lane == 0) xm = 0u;
-    unsigned long long xb = ib - lb, xv = iv - lv;
-    int best = -1;
-    uint32_t best_c = 0u, best_n = 0u, best_m = 0u;
-    unsigned long long best_b = 0ull, best_v = 0ull;
-    float best_e = 0.0f;
-#pragma unroll
-    for (int h = 0; h < 2; ++h) {
-        const uint4 c4 = pc[h], m4 = pm[h];
-        const uint32_t cc[4] = {c4.x, c4.y, c4.z, c4.w}, mm[4] = {m4.x, m4.y, m4.z, m4.w};
-        const ulonglong2 b01 = pb[2 * h], b23 = pb[2 * h + 1], v01 = pv[2 * h], v23 = pv[2 * h + 1];
-        const unsigned long long bb[4] = {b01.x, b01.y, b23.x, b23.y};
-        const unsigned long long vv[4] = {v01.x, v01.y, v23.x, v23.y};
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-            const unsigned long long rsb = Bb + xb, rsv = Bv + xv;
-            const uint32_t rm = max(Bm, xm);
-            const float e = u64_to_float(rsb) * iSB + bern(__uint_as_float(rm), u64_to_float(rsv) * iSV, l);
-            if (cc[k] > 0u && e < epsD) {
-                best = lane * 8 + 4 * h + k;
-                best_c = xc;
-                best_n = cc[k];
-                best_m = rm;
-                best_b = rsb;
-                best_v = rsv;
-                best_e = e;
-            }
-            xc += cc[k];
-            xm = max(xm, mm[k]);
-            xb += bb[k];
-            xv += vv[k];
-        }
+    if (lane == 31) {
+        sx.c[w] = ic;
+        sx.m[w] = im;
+        sx.b[w] = ib;
+        sx.v[w] = iv;
     }
-    int jb = best;
+    sel_bar();
+    uint32_t pc = 0u, pm = 0u, total = 0u;
+    unsigned long long pb = 0ull, pv = 0ull;
+#pragma unroll
+    for (int k = 0; k < SEL_NT / 32; ++k) {
+        if (k < w) {
+            pc += sx.c[k];
+            pm = max(pm, sx.m[k]);
+            pb += sx.b[k];
+            pv += sx.v[k];
+        }
+        total += sx.c[k];
+    }
+    // The bins below this one: all earlier warps, then the earlier lanes of this warp.
+    const uint32_t best_c = pc + ic - c;
+    const uint32_t best_m = max(Bm, max(pm, xm));
+    const unsigned long long best_b = Bb + pb + ib - sb, best_v = Bv + pv + iv - sv;
+    const float best_e = u64_to_float(best_b) * iSB + bern(__uint_as_float(best_m), u64_to_float(best_v) * iSV, l);
+    const uint32_t best_n = c;
+    int jb = (c > 0u && best_e < epsD) ? tid : -1;
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) jb = max(jb, __shfl_xor_sync(0xFFFFFFFFu, jb, o));
+    if (lane == 0) sx.best[w] = jb;
+    sel_bar();
+#pragma unroll
+    for (int k = 0; k < SEL_NT / 32; ++k) jb = max(jb, sx.best[k]);
     if (jb < 0) {
-        if (lane == 0) {  // rounding left no bin qualifying: take every candidate
+        if (tid == 0) {  // rounding left no bin qualifying: take every candidate
             ss.kstar = ss.above + (int)total;
             ss.fthr = ss.absorb ? 0ull : ss.cand_lo;
             ss.eps_final =
@@ -311,7 +303,7 @@ __device__ __forceinline__ void select_step(const Merged &mh, SelState &ss, int 
         }
         return;
     }
-    if (best != jb) return;
+    if (tid != jb) return;
     const int cj = (int)best_n;
     ss.Bb = best_b;
     ss.Bv = best_v;
@@ -677,6 +669,7 @@ __global__ void __launch_bounds__(CT_NT, 1) k_certify(CertifyArgs a) {
     // The select's state is uniform over the CTA and lives in shared memory: one lane of warp 0
     // decides each pass and every thread reads the outcome after a barrier.
     __shared__ SelState ss;
+    __shared__ SelScratch sx;
     int kstar = 0;
     unsigned long long fthr = ~0ull;  // F = { L tokens with key >= fthr }
     float eps_final = eps_hat;
@@ -809,42 +802,61 @@ __global__ void __launch_bounds__(CT_NT, 1) k_certify(CertifyArgs a) {
             const int shift = ss.shift;
             const bool absorb = ss.absorb != 0;
             uint32_t bc = 0u, bbm = 0u, bsbh = 0u, bsbl = 0u, bsvh = 0u, bsvl = 0u;
-            for (int i = tid; i < chunk; i += CT_NT) {
-                const float r = R[i];
-                if (r < 1.0f) {
-                    float bi, vi, bb;
-                    unsigned long long k;
-                    if (pass == 0) {  // the g key (Eq. (9), rationalised) of every token of L
+            // Bin one token of L (its key k and Lemma 1 terms given).
+            auto bin_token = [&](unsigned long long k, float bi, float vi, float bb) {
+                uint32_t qbh, qbl, qvh, qvl;
+                fixed_split(bi, SB, qbh, qbl);
+                fixed_split(vi, SV, qvh, qvl);
+                if (absorb && k < lo) {
+                    bc += 1u;
+                    bsbh += qbh;
+                    bsbl += qbl;
+                    bsvh += qvh;
+                    bsvl += qvl;
+                    bbm = max(bbm, __float_as_uint(bb));
+                } else {
+                    const unsigned long long dj = (k - lo) >> shift;
+                    const int bin = dj > 255ull ? 255 : (int)dj;
+                    atomicAdd(&hb.cnt[bin], 1u);
+                    atomicMax(&hb.bm[bin], __float_as_uint(bb));
+                    atomicAdd(&hb.sbh[bin], qbh);
+                    atomicAdd(&hb.sbl[bin], qbl);
+                    atomicAdd(&hb.svh[bin], qvh);
+                    atomicAdd(&hb.svl[bin], qvl);
+                }
+            };
+            if (pass == 0) {
+                // The g key (Eq. (9), rationalised) of every token of L.
+                for (int i = tid; i < chunk; i += CT_NT) {
+                    const float r = R[i];
+                    if (r < 1.0f) {
+                        float bi, vi, bb;
                         token_terms(W[i], r, __uint_as_float(X[i]), beta, bi, vi, bb);
                         const uint32_t g = g_bits(bi, vi, base + i == id1 && b2 != b1, A, Rr, b2,
                                                   VL, l);
                         X[i] = g;
-                        k = key64(g, base + i);
-                    } else {
-                        k = key64(X[i], base + i);
-                        if (!(k >= cand_lo && k < cand_hi)) continue;
-                        token_terms(W[i], r, rho_of(r), beta, bi, vi, bb);
+                        bin_token(key64(g, base + i), bi, vi, bb);
                     }
-                    uint32_t qbh, qbl, qvh, qvl;
-                    fixed_split(bi, SB, qbh, qbl);
-                    fixed_split(vi, SV, qvh, qvl);
-                    if (absorb && k < lo) {
-                        bc += 1u;
-                        bsbh += qbh;
-                        bsbl += qbl;
-                        bsvh += qvh;
-                        bsvl += qvl;
-                        bbm = max(bbm, __float_as_uint(bb));
-                    } else {
-                        const unsigned long long dj = (k - lo) >> shift;
-                        const int bin = dj > 255ull ? 255 : (int)dj;
-                        atomicAdd(&hb.cnt[bin], 1u);
-                        atomicMax(&hb.bm[bin], __float_as_uint(bb));
-                        atomicAdd(&hb.sbh[bin], qbh);
-                        atomicAdd(&hb.sbl[bin], qbl);
-                        atomicAdd(&hb.svh[bin], qvh);
-                        atomicAdd(&hb.svl[bin], qvl);
+                }
+            } else {
+                // Only the candidates (keys in [cand_lo, cand_hi)): the thread's keys are read
+                // with all loads in flight, then its few candidates visited in token order.
+                constexpr int TPT = PerThread<CL>::tokens;
+                uint32_t todo = 0u;
+#pragma unroll
+                for (int q = 0; q < TPT; ++q) {
+                    const int i = tid + q * CT_NT;
+                    if (i < chunk && R[i] < 1.0f) {
+                        const unsigned long long key = key64(X[i], base + i);
+                        if (key >= cand_lo && key < cand_hi) todo |= 1u << q;
                     }
+                }
+                for (; todo; todo &= todo - 1u) {
+                    const int i = tid + (__ffs(todo) - 1) * CT_NT;
+                    const float r = R[i];
+                    float bi, vi, bb;
+                    token_terms(W[i], r, rho_of(r), beta, bi, vi, bb);
+                    bin_token(key64(X[i], base + i), bi, vi, bb);
                 }
             }
             if (absorb) {
@@ -895,10 +907,10 @@ __global__ void __launch_bounds__(CT_NT, 1) k_certify(CertifyArgs a) {
                 }
             }
             __syncthreads();
-            // Warp 0 scans the 256 bins, 8 consecutive bins per lane: remaining(j) = below + bins
-            // < j (exact integers); the cut bin is the last non-empty bin whose remaining set
-            // already certifies.  One lane then moves the select on.
-            if (warp == 0) select_step(mh, ss, lane, SB, SV, l, eps * D, D);
+            // Threads 0..255 scan the 256 bins: remaining(j) = below + bins < j (exact
+            // integers); the cut bin is the last non-empty bin whose remaining set already
+            // certifies.  Its thread then moves the select on.
+            if (tid < SEL_NT) select_step(mh, ss, sx, tid, SB, SV, l, eps * D, D);
             __syncthreads();
             if (ss.done) break;
         }
