@@ -3,10 +3,11 @@
 // Definition 2 / Eq. (5), KVFETCH step 5; abstract page: fetch additional tokens from the CPU and
 // refine the attention computation).
 //
-// k_partial   split-K over a row set: each CTA item is a block of FET_ITEM_ROWS pivotal rows, or
-//             the fetched rows of one FET_RANGE token-id range, of one KV head, taken 64 at a time; each row a contiguous 4d-byte K|V pair read with 16-byte
-//             coalesced loads, four row groups in flight per warp (all of them for host rows),
-//             accumulated into one partial.  It computes the G logits, w = exp(logit - m), the
+// k_partial   split-K over a row set: each CTA item is a block of PIV_ITEM_ROWS pivotal rows, or
+//             the fetched rows of one FET_RANGE token-id range, of one KV head, taken 64 at a
+//             time; each row a contiguous 4d-byte K|V pair read with 16-byte coalesced loads,
+//             four row groups in flight per warp (all of them for host rows), accumulated into
+//             one partial.  It computes the G logits, w = exp(logit - m), the
 //             weight of Eq. (5) -- 1 for H and for tokens of F, lambda / r for sampled, unfetched
 //             tokens, with the certificate's lambda = clip(beta r / (w-hat (1 - r)), r, 1) from
 //             the sketch weight w-hat -- and accumulates D-hat, N-hat and the sample second
@@ -314,7 +315,7 @@ __device__ __forceinline__ void range_bounds(const int32_t *list, int count, int
     __syncthreads();
 }
 
-// Pivotal rows in blocks of FET_ITEM_ROWS list positions; staged fetched rows by token-id range
+// Pivotal rows in blocks of PIV_ITEM_ROWS list positions; staged fetched rows by token-id range
 // (FET_RANGE ids per partial, a zero partial for an empty range), as k_refine reads them from
 // host memory, so that both fetch modes produce the same partials.
 template <int D, int G, int MODE>
@@ -327,14 +328,15 @@ __global__ void __launch_bounds__(128) k_partial(PartialArgs a, int units_layer)
         if (MODE == ROWS_PIVOTAL) {
             const int ug = a.li.unit_global(ul);
             const int count = min(a.count[ug], a.row_stride);
-            const int lo = ch * FET_ITEM_ROWS;
-            partial_rows<D, G, MODE>(a, ul, ch, lo, min(lo + FET_ITEM_ROWS, count),
+            const int lo = ch * PIV_ITEM_ROWS;
+            partial_rows<D, G, MODE>(a, ul, ch, lo, min(lo + PIV_ITEM_ROWS, count),
                                      a.ids + (size_t)ug * a.row_stride, false);
         } else {
             const int32_t *list = a.ids + (size_t)ul * a.row_stride;
             int lo, hi;
             range_bounds(list, min(a.count[ul], a.row_stride), ch, lo, hi);
-            partial_rows<D, G, MODE>(a, ul, ch, lo, hi, list, true);
+            if (threadIdx.x == 0 && lo < hi) atomicOr(&a.rmask[ul * RMASK_W + (ch >> 5)], 1u << (ch & 31));
+            partial_rows<D, G, MODE>(a, ul, ch, lo, hi, list, false);
         }
     }
 }
@@ -357,10 +359,11 @@ cudaError_t launch_partial(const PartialArgs &a, int units_layer, int grid, cuda
 
 // ---------------------------------------------------------------------------------------------
 // k_merge: one CTA per query head; 8 groups of 128 threads each sum every eighth chunk of their
-// columns (pivotal chunks, then the per-range fetched ones), then the groups are added in a
-// fixed order.
+// columns (pivotal chunks, then the per-range fetched ones that hold rows), then the groups are
+// added in a fixed order.
 constexpr int MG_NT = 1024;
 constexpr int MG_GROUPS = MG_NT / 128;
+static_assert(MG_GROUPS == 8, "k_merge picks a group's ranges with the byte mask 0x01010101");
 
 __global__ void __launch_bounds__(MG_NT) k_merge(MergeArgs a) {
     extern __shared__ float red[];  // [MG_GROUPS][d + 2]
@@ -373,8 +376,8 @@ __global__ void __launch_bounds__(MG_NT) k_merge(MergeArgs a) {
     const int D = a.d, ncol = D + 2;
     int pc = a.pcount[ug];
     if (pc > a.cap) pc = a.cap;
-    const int npc = (pc + FET_ITEM_ROWS - 1) / FET_ITEM_ROWS;
-    const int nfc = a.max_fet;  // one partial per token-id range, empty ranges included
+    const int npc = (pc + PIV_ITEM_ROWS - 1) / PIV_ITEM_ROWS;
+    const uint32_t *rm = a.rmask + (size_t)ul * RMASK_W;  // the fetched-row ranges with a partial
     const int grp = threadIdx.x / 128, c0 = threadIdx.x % 128;
     const float *pp = a.part_piv + ((size_t)ul * a.max_piv * G + g) * ncol;
     const float *pf = a.part_fet + ((size_t)ul * a.max_fet * G + g) * ncol;
@@ -383,8 +386,10 @@ __global__ void __launch_bounds__(MG_NT) k_merge(MergeArgs a) {
         float s = 0.0f;
 #pragma unroll 4
         for (int ch = grp; ch < npc; ch += MG_GROUPS) s += pp[ch * stride + c];
-#pragma unroll 4
-        for (int ch = grp; ch < nfc; ch += MG_GROUPS) s += pf[ch * stride + c];
+        // this group's ranges (ch = grp mod MG_GROUPS) in ascending order, the empty ones skipped
+        for (int wd = 0; wd < RMASK_W; ++wd)
+            for (uint32_t bits = rm[wd] & (0x01010101u << grp); bits; bits &= bits - 1u)
+                s += pf[(32 * wd + __ffs(bits) - 1) * stride + c];
         red[grp * ncol + c] = s;
     }
     __syncthreads();
@@ -469,13 +474,14 @@ __global__ void __launch_bounds__(128, 3) k_refine(PartialArgs piv, PartialArgs 
             int pos = incl - c + (warp == 1 ? s_wsum[0] : 0);
             const int cnt = s_wsum[0] + s_wsum[1];
             for (uint32_t x = uw; x; x &= x - 1) s_ids[pos++] = w * 32 + (__ffs(x) - 1);
+            if (tid == 0 && cnt > 0) atomicOr(&fet.rmask[ul * RMASK_W + (k >> 5)], 1u << (k & 31));
             __syncthreads();
-            partial_rows<D, G, ROWS_HOST>(fet, ul, k, 0, cnt, s_ids, true);
+            partial_rows<D, G, ROWS_HOST>(fet, ul, k, 0, cnt, s_ids, false);
         } else {
             const int ch = k - fet.max_chunks;
             const int count = min(piv.count[ug], piv.row_stride);
-            const int lo = ch * FET_ITEM_ROWS;
-            partial_rows<D, G, ROWS_PIVOTAL>(piv, ul, ch, lo, min(lo + FET_ITEM_ROWS, count),
+            const int lo = ch * PIV_ITEM_ROWS;
+            partial_rows<D, G, ROWS_PIVOTAL>(piv, ul, ch, lo, min(lo + PIV_ITEM_ROWS, count),
                                              piv.ids + (size_t)ug * piv.row_stride, false);
         }
     }

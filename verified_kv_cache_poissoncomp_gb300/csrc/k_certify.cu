@@ -938,6 +938,8 @@ __global__ void __launch_bounds__(CT_NT, 1) k_certify(CertifyArgs a) {
         const int gw = base / 32 + w;
         if (lane == 0 && gw < a.W) Fq[gw] = word;
     }
+    // The refine's non-empty-range mask of this KV head starts empty.
+    if (a.rmask && crank == 0 && qh == ul * G && tid < RMASK_W) a.rmask[ul * RMASK_W + tid] = 0u;
     if (tid == 0 && crank == 0) {
         verkv_head_stats st;
         st.m = m;

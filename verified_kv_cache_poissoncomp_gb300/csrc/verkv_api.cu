@@ -24,7 +24,7 @@ namespace {
 size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 
 struct Layout {
-    size_t err, flc, nacc, scores, qstats, F, slb, fids, fcounts, staging, part_piv, part_fet, total;
+    size_t err, flc, nacc, rmask, scores, qstats, F, slb, fids, fcounts, staging, part_piv, part_fet, total;
     int W, units_layer, qh_layer, max_piv, max_fet, dense_chunks;
 };
 
@@ -43,7 +43,7 @@ bool make_layout(const verkv_shape *s, Layout &L) {
     L.W = (s->n + 31) / 32;
     L.units_layer = s->batch * s->kv_heads;
     L.qh_layer = L.units_layer * s->q_per_kv;
-    L.max_piv = (s->cap + FET_ITEM_ROWS - 1) / FET_ITEM_ROWS;
+    L.max_piv = (s->cap + PIV_ITEM_ROWS - 1) / PIV_ITEM_ROWS;
     L.max_fet = (s->n + FET_RANGE - 1) / FET_RANGE;
     L.dense_chunks = (s->n + PART_ROWS - 1) / PART_ROWS;  // >= max_fet: sizes the shared buffer
     size_t off = 0;
@@ -55,6 +55,7 @@ bool make_layout(const verkv_shape *s, Layout &L) {
     L.err = take(256);
     L.flc = take((size_t)L.units_layer * 4);
     L.nacc = take((size_t)L.qh_layer * 4);
+    L.rmask = take((size_t)L.units_layer * RMASK_W * 4);
     L.scores = take((size_t)L.qh_layer * n * 4);
     L.qstats = take((size_t)L.qh_layer * sizeof(verkv_head_stats));
     L.F = take((size_t)L.qh_layer * L.W * 4);
@@ -139,6 +140,7 @@ struct verkv_ctx {
     int32_t *fids = nullptr, *fcounts = nullptr;
     int32_t *flc = nullptr;  // per-KV-head completion counters of the certify kernel's fetch list
     int32_t *nacc = nullptr; // per-query-head n_fetch accumulators of the zero-copy refine
+    uint32_t *rmask = nullptr; // per-KV-head masks of fetched-row ranges holding rows
     uint32_t *slb = nullptr; // per-KV-head shortlist bitmaps
     int shortlist = 0;       // shortlist size per KV head; 0: every token of L may be fetched
     bool shortlisted = false;  // the last attend built shortlists
@@ -316,6 +318,7 @@ verkv_status verkv_create(verkv_ctx **out, int device, void *stream, const verkv
     ctx->fcounts = (int32_t *)(w + L.fcounts);
     ctx->flc = (int32_t *)(w + L.flc);
     ctx->nacc = (int32_t *)(w + L.nacc);
+    ctx->rmask = (uint32_t *)(w + L.rmask);
     ctx->slb = (uint32_t *)(w + L.slb);
     ctx->staging = (uint16_t *)(w + L.staging);
     ctx->part_piv = (float *)(w + L.part_piv);
@@ -324,6 +327,7 @@ verkv_status verkv_create(verkv_ctx **out, int device, void *stream, const verkv
     if (e == cudaSuccess) e = cudaMemsetAsync(ctx->fcounts, 0, (size_t)L.units_layer * 4, ctx->main);
     if (e == cudaSuccess) e = cudaMemsetAsync(ctx->flc, 0, (size_t)L.units_layer * 4, ctx->main);
     if (e == cudaSuccess) e = cudaMemsetAsync(ctx->nacc, 0, (size_t)L.qh_layer * 4, ctx->main);
+    if (e == cudaSuccess) e = cudaMemsetAsync(ctx->rmask, 0, (size_t)L.units_layer * RMASK_W * 4, ctx->main);
     if (e != cudaSuccess) {
         verkv_destroy(ctx);
         return VERKV_ECUDA;
@@ -515,6 +519,7 @@ verkv_status verkv_attend_verified(verkv_ctx *ctx, int32_t layer, const void *q,
     // caller asking for ids or counts.  The zero-copy refine reads the selection bitmaps.
     const bool need_list = ctx->fetch_mode != VERKV_FETCH_ZEROCOPY || fetch_ids_out || fetch_counts_out;
     ca.fl_counter = need_list ? ctx->flc : nullptr;
+    ca.rmask = ctx->rmask;
     ca.ids = ctx->fids;
     ca.counts = ctx->fcounts;
     ca.ids_user = fetch_ids_out;
@@ -574,6 +579,7 @@ verkv_status verkv_fetch_refine(verkv_ctx *ctx, const int32_t *ids, const int32_
     pa.qstats = ctx->qstats;
     pa.part = ctx->part_fet;
     pa.err = ctx->err;
+    pa.rmask = ctx->rmask;
     pa.ids = ctx->fids;
     pa.pr = nullptr;
     pa.count = ctx->fcounts;
@@ -590,6 +596,7 @@ verkv_status verkv_fetch_refine(verkv_ctx *ctx, const int32_t *ids, const int32_
     MergeArgs ma{};
     ma.part_piv = ctx->part_piv;
     ma.part_fet = ctx->part_fet;
+    ma.rmask = ctx->rmask;
     ma.pcount = ctx->piv.count;
     ma.fcount = ctx->fcounts;
     ma.qstats = ctx->qstats;

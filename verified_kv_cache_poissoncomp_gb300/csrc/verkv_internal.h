@@ -113,6 +113,7 @@ struct CertifyArgs {
     int32_t *ids_host;            // optional copy into mapped host memory (MEMCPY mode)
     int32_t *counts_host;
     const uint32_t *shortlist;    // [units_layer][W] fetch candidates, or null: all of L
+    uint32_t *rmask;              // [units_layer][RMASK_W] cleared here for the refine, or null
     int n, W, cl, chunk;
     float eps, ldelta;
     LayerIdx li;
@@ -139,9 +140,10 @@ size_t certify_smem_bytes(int chunk);
 // Shrinkage-weighted partial sums over a row set: the pivotal rows in HBM, fetched rows staged in
 // HBM, or fetched rows read by token id straight from page-locked host memory.
 constexpr int PART_ROWS = 64;                      // rows a CTA has in flight
-constexpr int FET_SUB = 4;                         // row blocks per partial for fetched rows
-constexpr int FET_ITEM_ROWS = PART_ROWS * FET_SUB; // pivotal list positions per partial
+constexpr int PIV_ITEM_ROWS = PART_ROWS;           // pivotal list positions per partial
 constexpr int FET_RANGE = 1024;                    // token ids per partial of fetched rows
+constexpr int RMASK_W = 4;                         // words of a unit's non-empty-range mask
+                                                   // (n <= 131072 = 4 * 32 * FET_RANGE)
 enum { ROWS_PIVOTAL = 0, ROWS_STAGED = 1, ROWS_HOST = 2 };
 struct PartialArgs {
     const uint16_t *rows;     // [src units][row_stride][row16 vectors]; ROWS_HOST: [units][n][2][d]
@@ -161,6 +163,8 @@ struct PartialArgs {
     const uint32_t *resident; // ROWS_HOST in k_refine: the resident bitmaps [units][W]
     int32_t *nacc;            // ROWS_HOST in k_refine: per query head n_fetch accumulators
                               // [qh], zero on entry (k_merge resets them)
+    uint32_t *rmask;          // fetched-row ranges: bit k of [units_layer][RMASK_W] set when
+                              // range k holds rows (only those get a partial); zero on entry
     int row_stride;           // cap (pivotal) or n (fetched)
     int max_chunks;
     int n, W, d;
@@ -196,6 +200,7 @@ struct MergeArgs {
     verkv_head_stats *stats;     // [qh] or null
     int32_t *nacc;               // per query head n_fetch counted by k_refine (read and reset),
                                  // or null: qstats carries it (the certify kernel's fetch list)
+    const uint32_t *rmask;       // [units_layer][RMASK_W]: the fetched-row ranges with a partial
     int max_piv, max_fet, cap, d;
     LayerIdx li;
 };
