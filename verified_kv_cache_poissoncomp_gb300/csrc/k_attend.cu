@@ -430,7 +430,7 @@ __global__ void __launch_bounds__(128, 3) k_refine(PartialArgs piv, PartialArgs 
     pdl_wait();
     pdl_trigger();
     constexpr int WR = FET_RANGE / 32;  // bitmap words per range (one thread each)
-    static_assert(WR == 32 || WR == 64, "the range's words are scanned by one or two warps");
+    static_assert(WR >= 16 && WR <= 64, "the range's words are scanned by at most two warps");
     __shared__ int32_t s_ids[FET_RANGE];
     __shared__ int s_wsum[2];
     const int per_unit = fet.max_chunks + piv.max_chunks;
@@ -460,7 +460,7 @@ __global__ void __launch_bounds__(128, 3) k_refine(PartialArgs piv, PartialArgs 
 #pragma unroll
             for (int g = 0; g < G; ++g) {
                 const int t = warp_sum(nf[g]);
-                if (lane == 0 && warp < WR / 32 && t) atomicAdd(&fet.nacc[ul * G + g], t);
+                if (lane == 0 && warp < (WR + 31) / 32 && t) atomicAdd(&fet.nacc[ul * G + g], t);
             }
             const int c = __popc(uw);
             int incl = c;

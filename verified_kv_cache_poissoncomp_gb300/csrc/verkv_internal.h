@@ -142,8 +142,8 @@ size_t certify_smem_bytes(int chunk);
 constexpr int PART_ROWS = 64;                      // rows a CTA has in flight
 constexpr int PIV_ITEM_ROWS = PART_ROWS;           // pivotal list positions per partial
 constexpr int FET_RANGE = 1024;                    // token ids per partial of fetched rows
-constexpr int RMASK_W = 4;                         // words of a unit's non-empty-range mask
-                                                   // (n <= 131072 = 4 * 32 * FET_RANGE)
+constexpr int RMASK_W = 131072 / FET_RANGE / 32;   // words of a unit's non-empty-range mask
+                                                   // (n <= 131072)
 enum { ROWS_PIVOTAL = 0, ROWS_STAGED = 1, ROWS_HOST = 2 };
 struct PartialArgs {
     const uint16_t *rows;     // [src units][row_stride][row16 vectors]; ROWS_HOST: [units][n][2][d]
