@@ -12,16 +12,17 @@
 //      every token at the current beta -- at its floor (A += w (1 - r)), in the middle (B += w,
 //      S += r / (1 - r)) or at lambda = 1 -- and moves to the root (A + B) / (1 + S) of that
 //      linear piece, a ratio of positive sums; the pass also finds the nearest breakpoints on
-//      either side, and the solve ends as soon as the new root lies between them (three to four
-//      passes from the top of the bracket);
+//      either side, and the solve ends as soon as the new root lies between them.  The first
+//      pass evaluates two points, C and C/4, in one exchange, which brackets the root and starts
+//      Newton closer to it than the top of the bracket (2.7 passes on average instead of 3.4);
 //   +1 beta(L), V(L), the top two b_i (with the argmax id) of Lemma 1;
 //   +k when the certificate fails, a windowed most-significant-digit select over the 56-bit key
 //      (g bits << 24 | 2^24-1-token id) -- g descending, ties to the lower id.  Each pass builds a
 //      256-bin histogram of (count, max b_i, sum beta_i, sum v_i) with the sums in 64-bit fixed
 //      point scaled by beta(L) and V(L), added as two 32-bit halves (native integer atomics;
 //      exact, order-independent sums); the CTAs' histograms are merged over distributed shared
-//      memory and one warp scans the 256 bins for the bin in which eps-hat of the remaining
-//      tokens drops below eps.  The first window spans 32 octaves under the largest possible g
+//      memory and 256 threads, one per bin, scan them for the bin in which eps-hat of the
+//      remaining tokens drops below eps.  The first window spans 32 octaves under the largest possible g
 //      at 8 bins per octave and folds everything below into bin 0; the select ends when the cut
 //      bin holds one token;
 //   tail  the last of a KV head's G clusters to finish builds that head's fetch list (KVFetch
@@ -39,7 +40,9 @@ namespace verkv {
 constexpr int CT_NT = 1024;
 constexpr int CT_NW = CT_NT / 32;
 constexpr int CT_MAX_CL = 8;
-constexpr int CT_REC = 8;   // floats per record in a cluster all-reduce
+constexpr int CT_REC = 16;  // floats per record in a cluster all-reduce
+constexpr int BETA_GRID = 2;           // points of the beta solve's first pass: C and C/4
+constexpr float BETA_GRID_STEP = 0.25f; // (measured against 1, 3 and 4 points on the bench)
 constexpr int BETA_MAXIT = 64;
 constexpr int SEL_MAXPASS = 16;
 
@@ -549,80 +552,135 @@ __global__ void __launch_bounds__(CT_NT, 1) k_certify(CertifyArgs a) {
         nL = rec[3];
     }
 
-    // ---- 2. beta: safeguarded piece-wise Newton from the top of the bracket ----
+    // ---- 2. beta: safeguarded piece-wise Newton ----
+    // h(beta) = beta - sum_L w-hat (1 - lambda(beta)) rises from h(0) <= 0 to h(C) >= 0.  Every
+    // pass evaluates, at a point beta, the sums of the linear piece of h through it and the
+    // nearest breakpoints on either side: the largest one below (pl) and the smallest one at or
+    // above (ph).  A token's breakpoints are w (1 - r), where lambda leaves its floor, and
+    // w (1 - r) / r, where it reaches 1.  The root of the piece through beta is the fixed point
+    // when it lies strictly between pl and ph, or when it reproduces beta (to 1e-6 relative:
+    // float32 sums jitter by an ulp or two).  The first pass evaluates BETA_GRID points C, C/4, ...
+    // together (one cluster exchange), which brackets the root and gives the Newton start; later
+    // passes take one point each.
     float beta = 0.0f;
     int iters = 0, flags = 0;
-    bool first = true;
     const float wscale = tmax == NEG_INF ? 0.0f : expf(tmax - m);  // w-hat = W * wscale
+    // Classify one token of L at beta into the piece sums and nearest breakpoints (fl = w (1 - r)):
+    // at its floor, in the middle, or at lambda = 1; a breakpoint fl / r is computed only where it
+    // can move pl or ph (most tokens sit at their floor: the branches are nearly uniform).
+    auto piece = [](float beta, float w, float r, float fl, float rho, float &ab, float &S,
+                    float &pl, float &ph) {
+        if (beta <= fl) {
+            ab += fl;
+            ph = fminf(ph, fl);
+        } else if (beta * r < fl) {
+            ab += w;
+            S += rho;
+            pl = fmaxf(pl, fl);
+            if (fl < r * ph) ph = fminf(ph, __fdividef(fl, r));
+        } else if (fl > r * pl) {
+            pl = fmaxf(pl, __fdividef(fl, r));
+        }
+    };
     if (C > 0.0f) {
-        float lo = 0.0f, hi = C;  // h(0) <= 0 <= h(C)
-        beta = C;
-        for (iters = 1; iters <= BETA_MAXIT; ++iters) {
-            // Besides the piece's sums, the nearest breakpoints on either side of beta: the
-            // largest one below (pl) and the smallest one at or above (ph).  A token's
-            // breakpoints are w (1 - r), where lambda leaves its floor, and w (1 - r) / r, where
-            // it reaches 1.
-            float ab = 0.f, S = 0.f, pl = 0.f, ph = INFINITY;
-            for (int i = tid; i < chunk; i += CT_NT) {
-                const float r = R[i];
-                float w;
-                if (first) {
-                    w = W[i] * wscale;
-                    W[i] = w;
-                    if (r < 1.0f) X[i] = __float_as_uint(rho_of(r));
-                } else {
-                    w = W[i];
-                }
-                if (r < 1.0f) {
-                    const float fl = w * (1.0f - r);
-                    if (beta <= fl) {
-                        ab += fl;
-                        ph = fminf(ph, fl);
-                    } else if (beta * r < fl) {
-                        ab += w;
-                        S += __uint_as_float(X[i]);
-                        pl = fmaxf(pl, fl);
-                        if (fl < r * ph) ph = fminf(ph, __fdividef(fl, r));
-                    } else if (fl > r * pl) {
-                        pl = fmaxf(pl, __fdividef(fl, r));
+        constexpr int NG = BETA_GRID;
+        float gb[NG], gab[NG], gS[NG], gpl[NG], gph[NG];
+#pragma unroll
+        for (int k = 0; k < NG; ++k) {
+            gb[k] = k == 0 ? C : gb[k - 1] * BETA_GRID_STEP;
+            gab[k] = 0.f;
+            gS[k] = 0.f;
+            gpl[k] = 0.f;
+            gph[k] = INFINITY;
+        }
+        // Pass 1 also turns the logits into w-hat and r into rho = r / (1 - r).
+        for (int i = tid; i < chunk; i += CT_NT) {
+            const float r = R[i];
+            const float w = W[i] * wscale;
+            W[i] = w;
+            if (r < 1.0f) {
+                const float rho = rho_of(r);
+                X[i] = __float_as_uint(rho);
+                const float fl = w * (1.0f - r);
+#pragma unroll
+                for (int k = 0; k < NG; ++k) piece(gb[k], w, r, fl, rho, gab[k], gS[k], gpl[k], gph[k]);
+            }
+        }
+        float rec[4 * NG];
+#pragma unroll
+        for (int k = 0; k < NG; ++k) {
+            rec[4 * k] = warp_sum(gab[k]);
+            rec[4 * k + 1] = warp_sum(gS[k]);
+            rec[4 * k + 2] = warp_max(gpl[k]);
+            rec[4 * k + 3] = warp_min(gph[k]);
+        }
+        cluster_allreduce<CL>(rec, wrec, xrec, parity, [](float (&x)[4 * NG], const float (&y)[4 * NG]) {
+#pragma unroll
+            for (int k = 0; k < NG; ++k) {
+                x[4 * k] += y[4 * k];
+                x[4 * k + 1] += y[4 * k + 1];
+                x[4 * k + 2] = fmaxf(x[4 * k + 2], y[4 * k + 2]);
+                x[4 * k + 3] = fminf(x[4 * k + 3], y[4 * k + 3]);
+            }
+        });
+        // The bracket from the signs of h at the grid points; Newton roots of their pieces are
+        // below the root where h is concave, so the largest inside the bracket starts the rest.
+        float lo = 0.0f, hi = C, start = 0.0f;
+        bool found = false;
+#pragma unroll
+        for (int k = 0; k < NG; ++k) {
+            const float bk = gb[k];
+            const float ab = rec[4 * k], S = rec[4 * k + 1];
+            const float nb = __fdiv_rn(ab, 1.0f + S);
+            if (!found && ((nb > rec[4 * k + 2] && nb < rec[4 * k + 3]) || fabsf(nb - bk) <= 1e-6f * bk)) {
+                beta = nb;
+                found = true;
+            }
+            if (fmaf(bk, 1.0f + S, -ab) < 0.0f) lo = fmaxf(lo, bk);
+            else hi = fminf(hi, bk);
+            start = fmaxf(start, nb);
+        }
+        iters = 1;
+        if (!found) {
+            beta = (start > lo && start < hi) ? start : ((lo > 0.0f) ? sqrtf(lo) * sqrtf(hi) : hi * 0.0625f);
+            for (iters = 2; iters <= BETA_MAXIT; ++iters) {
+                float ab = 0.f, S = 0.f, pl = 0.f, ph = INFINITY;
+                for (int i = tid; i < chunk; i += CT_NT) {
+                    const float r = R[i];
+                    if (r < 1.0f) {
+                        const float w = W[i];
+                        piece(beta, w, r, w * (1.0f - r), __uint_as_float(X[i]), ab, S, pl, ph);
                     }
                 }
-            }
-            first = false;
-            float rec[4] = {warp_sum(ab), warp_sum(S), warp_max(pl), warp_min(ph)};
-            cluster_allreduce<CL>(rec, wrec, xrec, parity,
-                                  [](float (&x)[4], const float (&y)[4]) {
-                                      x[0] += y[0];
-                                      x[1] += y[1];
-                                      x[2] = fmaxf(x[2], y[2]);
-                                      x[3] = fminf(x[3], y[3]);
-                                  });
-            ab = rec[0];
-            S = rec[1];
-            pl = rec[2];
-            ph = rec[3];
-            // The root of the linear piece through beta.  When it lies strictly between the
-            // nearest breakpoints, every token keeps its piece there: it is the fixed point.
-            // When it reproduces beta (to 1e-6 relative: float32 sums jitter by an ulp or two),
-            // likewise; both are tested before the bracket, which rounding can leave an ulp off
-            // the root.
-            float nb = __fdiv_rn(ab, 1.0f + S);
-            if ((nb > pl && nb < ph) || fabsf(nb - beta) <= 1e-6f * beta) {
+                float rec1[4] = {warp_sum(ab), warp_sum(S), warp_max(pl), warp_min(ph)};
+                cluster_allreduce<CL>(rec1, wrec, xrec, parity,
+                                      [](float (&x)[4], const float (&y)[4]) {
+                                          x[0] += y[0];
+                                          x[1] += y[1];
+                                          x[2] = fmaxf(x[2], y[2]);
+                                          x[3] = fminf(x[3], y[3]);
+                                      });
+                ab = rec1[0];
+                S = rec1[1];
+                pl = rec1[2];
+                ph = rec1[3];
+                float nb = __fdiv_rn(ab, 1.0f + S);
+                if ((nb > pl && nb < ph) || fabsf(nb - beta) <= 1e-6f * beta) {
+                    beta = nb;
+                    break;
+                }
+                const float hval = fmaf(beta, 1.0f + S, -ab);
+                if (hval < 0.0f) lo = beta; else hi = beta;
+                if (!(nb > lo && nb < hi)) nb = (lo > 0.0f) ? sqrtf(lo) * sqrtf(hi) : hi * 0.0625f;
                 beta = nb;
-                break;
+                if ((hi - lo) <= 1e-6f * hi) break;
             }
-            const float hval = fmaf(beta, 1.0f + S, -ab);
-            if (hval < 0.0f) lo = beta; else hi = beta;
-            if (!(nb > lo && nb < hi)) nb = (lo > 0.0f) ? sqrtf(lo) * sqrtf(hi) : hi * 0.0625f;
-            beta = nb;
-            if ((hi - lo) <= 1e-6f * hi) break;
+            if (iters > BETA_MAXIT) {
+                iters = BETA_MAXIT;
+                flags = 1;
+            }
         }
-        if (iters > BETA_MAXIT) {
-            iters = BETA_MAXIT;
-            flags = 1;
-        }
-    }
-    if (first) {  // no Newton pass ran: convert the logits now
+    } else {  // no token of L carries weight: only convert the logits
         for (int i = tid; i < chunk; i += CT_NT) {
             W[i] *= wscale;
             if (R[i] < 1.0f) X[i] = __float_as_uint(rho_of(R[i]));
