@@ -382,14 +382,40 @@ __global__ void __launch_bounds__(MG_NT) k_merge(MergeArgs a) {
     const float *pp = a.part_piv + ((size_t)ul * a.max_piv * G + g) * ncol;
     const float *pf = a.part_fet + ((size_t)ul * a.max_fet * G + g) * ncol;
     const size_t stride = (size_t)G * ncol;
+    uint32_t gm[RMASK_W];  // this group's ranges (ch = grp mod MG_GROUPS) that hold rows
+#pragma unroll
+    for (int wd = 0; wd < RMASK_W; ++wd) gm[wd] = rm[wd] & (0x01010101u << grp);
     for (int c = c0; c < ncol; c += 128) {
         float s = 0.0f;
-#pragma unroll 4
-        for (int ch = grp; ch < npc; ch += MG_GROUPS) s += pp[ch * stride + c];
-        // this group's ranges (ch = grp mod MG_GROUPS) in ascending order, the empty ones skipped
-        for (int wd = 0; wd < RMASK_W; ++wd)
-            for (uint32_t bits = rm[wd] & (0x01010101u << grp); bits; bits &= bits - 1u)
-                s += pf[(32 * wd + __ffs(bits) - 1) * stride + c];
+        // The group's pivotal chunks, eight loads in flight, added in chunk order.
+        for (int b0 = grp; b0 < npc; b0 += 8 * MG_GROUPS) {
+            float v[8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                const int ch = b0 + j * MG_GROUPS;
+                v[j] = ch < npc ? pp[ch * stride + c] : 0.0f;
+            }
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+                if (b0 + j * MG_GROUPS < npc) s += v[j];
+        }
+        // Then its fetched-row ranges in ascending order, the empty ones skipped: at most four
+        // per mask word, loaded together.
+#pragma unroll
+        for (int wd = 0; wd < RMASK_W; ++wd) {
+            uint32_t bits = gm[wd];
+            float v[4];
+            bool has[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                has[j] = bits != 0u;
+                v[j] = has[j] ? pf[(32 * wd + __ffs(bits) - 1) * stride + c] : 0.0f;
+                bits &= bits - 1u;
+            }
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+                if (has[j]) s += v[j];
+        }
         red[grp * ncol + c] = s;
     }
     __syncthreads();
