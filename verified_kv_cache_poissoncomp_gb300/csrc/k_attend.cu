@@ -358,81 +358,82 @@ cudaError_t launch_partial(const PartialArgs &a, int units_layer, int grid, cuda
 }
 
 // ---------------------------------------------------------------------------------------------
-// k_merge: one CTA per query head; 8 groups of 128 threads each sum every eighth chunk of their
-// columns (pivotal chunks, then the per-range fetched ones that hold rows), then the groups are
+// k_merge: per query head, d / MG_COLS CTAs, each over MG_COLS columns of N-hat plus the D-hat
+// and second-moment columns: 8 groups of MG_COLS + 2 threads, one column each, sum every eighth
+// chunk (pivotal chunks, then the per-range fetched ones that hold rows), then the groups are
 // added in a fixed order.
-constexpr int MG_NT = 1024;
-constexpr int MG_GROUPS = MG_NT / 128;
+constexpr int MG_GROUPS = 8;
+constexpr int MG_COLS = 64;
+constexpr int MG_TASKS = MG_GROUPS * (MG_COLS + 2);
+constexpr int MG_NT = (MG_TASKS + 31) / 32 * 32;
 static_assert(MG_GROUPS == 8, "k_merge picks a group's ranges with the byte mask 0x01010101");
 
 __global__ void __launch_bounds__(MG_NT) k_merge(MergeArgs a) {
-    extern __shared__ float red[];  // [MG_GROUPS][d + 2]
+    __shared__ float red[MG_GROUPS][MG_COLS + 2];
     pdl_wait();
     pdl_trigger();
-    const int qh = blockIdx.x;
+    const int D = a.d, ncol = D + 2, halves = D / MG_COLS;
+    const int qh = blockIdx.x / halves, half = blockIdx.x - qh * halves;
     const int G = a.li.G;
     const int ul = qh / G, g = qh - ul * G;
     const int ug = a.li.unit_global(ul);
-    const int D = a.d, ncol = D + 2;
     int pc = a.pcount[ug];
     if (pc > a.cap) pc = a.cap;
     const int npc = (pc + PIV_ITEM_ROWS - 1) / PIV_ITEM_ROWS;
-    const uint32_t *rm = a.rmask + (size_t)ul * RMASK_W;  // the fetched-row ranges with a partial
-    const int grp = threadIdx.x / 128, c0 = threadIdx.x % 128;
-    const float *pp = a.part_piv + ((size_t)ul * a.max_piv * G + g) * ncol;
-    const float *pf = a.part_fet + ((size_t)ul * a.max_fet * G + g) * ncol;
-    const size_t stride = (size_t)G * ncol;
-    uint32_t gm[RMASK_W];  // this group's ranges (ch = grp mod MG_GROUPS) that hold rows
-#pragma unroll
-    for (int wd = 0; wd < RMASK_W; ++wd) gm[wd] = rm[wd] & (0x01010101u << grp);
-    for (int c = c0; c < ncol; c += 128) {
+    const int t = threadIdx.x;
+    if (t < MG_TASKS) {
+        const int grp = t / (MG_COLS + 2), j = t - grp * (MG_COLS + 2);
+        const int c = j < MG_COLS ? half * MG_COLS + j : D + (j - MG_COLS);
+        const float *pp = a.part_piv + ((size_t)ul * a.max_piv * G + g) * ncol + c;
+        const float *pf = a.part_fet + ((size_t)ul * a.max_fet * G + g) * ncol + c;
+        const int stride = G * ncol;
+        const uint32_t *rm = a.rmask + (size_t)ul * RMASK_W;  // the fetched-row ranges with a partial
         float s = 0.0f;
         // The group's pivotal chunks, eight loads in flight, added in chunk order.
         for (int b0 = grp; b0 < npc; b0 += 8 * MG_GROUPS) {
             float v[8];
 #pragma unroll
-            for (int j = 0; j < 8; ++j) {
-                const int ch = b0 + j * MG_GROUPS;
-                v[j] = ch < npc ? pp[ch * stride + c] : 0.0f;
+            for (int k = 0; k < 8; ++k) {
+                const int ch = b0 + k * MG_GROUPS;
+                v[k] = ch < npc ? pp[ch * stride] : 0.0f;
             }
 #pragma unroll
-            for (int j = 0; j < 8; ++j)
-                if (b0 + j * MG_GROUPS < npc) s += v[j];
+            for (int k = 0; k < 8; ++k)
+                if (b0 + k * MG_GROUPS < npc) s += v[k];
         }
-        // Then its fetched-row ranges in ascending order, the empty ones skipped: at most four
-        // per mask word, loaded together.
+        // Then its fetched-row ranges (ch = grp mod 8) in ascending order, the empty ones
+        // skipped: at most four per mask word, loaded together.
 #pragma unroll
         for (int wd = 0; wd < RMASK_W; ++wd) {
-            uint32_t bits = gm[wd];
+            uint32_t bits = rm[wd] & (0x01010101u << grp);
             float v[4];
             bool has[4];
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                has[j] = bits != 0u;
-                v[j] = has[j] ? pf[(32 * wd + __ffs(bits) - 1) * stride + c] : 0.0f;
+            for (int k = 0; k < 4; ++k) {
+                has[k] = bits != 0u;
+                v[k] = has[k] ? pf[(32 * wd + __ffs(bits) - 1) * stride] : 0.0f;
                 bits &= bits - 1u;
             }
 #pragma unroll
-            for (int j = 0; j < 4; ++j)
-                if (has[j]) s += v[j];
+            for (int k = 0; k < 4; ++k)
+                if (has[k]) s += v[k];
         }
-        red[grp * ncol + c] = s;
+        red[grp][j] = s;
     }
     __syncthreads();
-    if (threadIdx.x < ncol) {
-        const int c = threadIdx.x;
-        float t = red[c];
+    if (t < MG_COLS + 2) {
+        float tt = red[0][t];
 #pragma unroll
-        for (int k = 1; k < MG_GROUPS; ++k) t += red[k * ncol + c];
-        red[c] = t;  // only this thread reads or writes column c of row 0 now
+        for (int k = 1; k < MG_GROUPS; ++k) tt += red[k][t];
+        red[0][t] = tt;  // only this thread reads or writes column t of row 0 now
     }
     __syncthreads();
-    const float Dh = red[D];
-    for (int c = threadIdx.x; c < D; c += MG_NT) a.o[(size_t)qh * D + c] = red[c] / Dh;
-    if (threadIdx.x == 0) {
+    const float Dh = red[0][MG_COLS];
+    if (t < MG_COLS) a.o[(size_t)qh * D + half * MG_COLS + t] = red[0][t] / Dh;
+    if (half == 0 && t == 0) {
         verkv_head_stats st = a.qstats[qh];
         st.D_hat = Dh;
-        st.M2 = red[D + 1];
+        st.M2 = red[0][MG_COLS + 1];
         st.lse = st.m + logf(Dh);
         if (a.nacc) {
             st.n_fetch = a.nacc[qh];
@@ -444,7 +445,8 @@ __global__ void __launch_bounds__(MG_NT) k_merge(MergeArgs a) {
 }
 
 cudaError_t launch_merge(const MergeArgs &a, int qheads, cudaStream_t s) {
-    return launch_pdl(k_merge, dim3(qheads), dim3(MG_NT), MG_GROUPS * (a.d + 2) * sizeof(float), s, a);
+    if (a.d % MG_COLS) return cudaErrorInvalidValue;
+    return launch_pdl(k_merge, dim3(qheads * (a.d / MG_COLS)), dim3(MG_NT), 0, s, a);
 }
 
 // ---------------------------------------------------------------------------------------------
@@ -662,11 +664,15 @@ cudaError_t launch_dense_host(const DenseArgs &a, int units_layer, int grid, cud
     return cudaErrorInvalidValue;
 }
 
+// Threads of a dense-merge CTA: DM_GROUPS groups of 128, each summing every DM_GROUPS-th chunk.
+constexpr int DM_NT = 1024;
+constexpr int DM_GROUPS = DM_NT / 128;
+
 // One CTA per query head: the global max M over the chunk maxima, then every chunk's (N, D)
 // scaled by exp(m_chunk - M), summed by 8 groups over interleaved chunks and the groups in a
 // fixed order; o = N / D, lse = M + log D.
-__global__ void __launch_bounds__(MG_NT) k_dense_merge(DenseArgs a, float *o, float *lse) {
-    extern __shared__ float red[];  // [MG_GROUPS][d + 1]
+__global__ void __launch_bounds__(DM_NT) k_dense_merge(DenseArgs a, float *o, float *lse) {
+    extern __shared__ float red[];  // [DM_GROUPS][d + 1]
     __shared__ float sM;
     const int qh = blockIdx.x;
     const int G = a.li.G;
@@ -685,7 +691,7 @@ __global__ void __launch_bounds__(MG_NT) k_dense_merge(DenseArgs a, float *o, fl
     const int grp = threadIdx.x / 128, c0 = threadIdx.x % 128;
     for (int c = c0; c <= D; c += 128) {
         float t = 0.0f;
-        for (int ch = grp; ch < a.chunks; ch += MG_GROUPS)
+        for (int ch = grp; ch < a.chunks; ch += DM_GROUPS)
             t += pp[ch * stride + c] * expf(pp[ch * stride + D + 1] - M);
         red[grp * (D + 1) + c] = t;
     }
@@ -694,17 +700,17 @@ __global__ void __launch_bounds__(MG_NT) k_dense_merge(DenseArgs a, float *o, fl
         const int c = threadIdx.x;
         float t = red[c];
 #pragma unroll
-        for (int k = 1; k < MG_GROUPS; ++k) t += red[k * (D + 1) + c];
+        for (int k = 1; k < DM_GROUPS; ++k) t += red[k * (D + 1) + c];
         red[c] = t;
     }
     __syncthreads();
     const float Dh = red[D];
-    for (int c = threadIdx.x; c < D; c += MG_NT) o[(size_t)qh * D + c] = red[c] / Dh;
+    for (int c = threadIdx.x; c < D; c += DM_NT) o[(size_t)qh * D + c] = red[c] / Dh;
     if (threadIdx.x == 0 && lse) lse[qh] = M + logf(Dh);
 }
 
 cudaError_t launch_dense_merge(const DenseArgs &a, int qheads, float *o, float *lse, cudaStream_t s) {
-    k_dense_merge<<<qheads, MG_NT, MG_GROUPS * (a.d + 1) * sizeof(float), s>>>(a, o, lse);
+    k_dense_merge<<<qheads, DM_NT, DM_GROUPS * (a.d + 1) * sizeof(float), s>>>(a, o, lse);
     return cudaGetLastError();
 }
 
