@@ -129,3 +129,28 @@ def test_tiny_tolerance_fetches_all_of_L():
     for gi in range(w.G):
         dn = O.dense(O.logits(O.bf16_to_f64(w.queries[0, 0, gi]), K), V)
         assert np.linalg.norm(g["o"][gi] - dn["o"]) <= 1e-4 * np.linalg.norm(dn["o"])
+
+
+def test_without_fetch_outputs_matches_with_them():
+    # A caller that asks for neither fetch ids nor counts gets no fetch list from the certify
+    # kernel; the refine reads the selection bitmaps either way, so o, lse and the per-head
+    # statistics (n_fetch included) must be the same bits as with the outputs requested.
+    w = I.make_workload("nolist", B=2, L=2, h_kv=2, G=4, d=128, n=20000, eta=1 / 8, n_queries=4,
+                        plant_every=2)
+    eng = P.make_engine(w)
+    eng.compress(w.eta, w.n_sink, w.n_local, w.seed)
+    eng.sync()
+    uncertified = 0
+    for t in range(w.queries.shape[0]):
+        q = torch.as_tensor(w.queries[t].view(np.int16)).to(eng.dev)
+        out = []
+        for with_ids in (True, False):
+            eng.attend(int(w.query_layer[t]), q, w.eps, w.delta, with_ids=with_ids)
+            o, lse, st = eng.fetch_refine()
+            eng.sync()
+            out.append((o.cpu().numpy().copy(), lse.cpu().numpy().copy(), st.cpu().numpy().copy()))
+        (o1, l1, s1), (o2, l2, s2) = out
+        assert np.array_equal(o1, o2) and np.array_equal(l1, l2) and np.array_equal(s1, s2), t
+        uncertified += int((s1[:, 10] == 0).sum())
+    assert uncertified > 0  # the selection and the fetch ran
+    eng.close()
