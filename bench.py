@@ -23,6 +23,7 @@ import os
 import statistics
 import subprocess
 import sys
+import tempfile
 import time
 
 import numpy as np
@@ -108,7 +109,8 @@ class ClockSampler:
     def __init__(self, device_index):
         self.idx = device_index
         self.proc = None
-        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_gpu{device_index}.csv")
+        # the raw samples stay in a scratch file; the JSON line carries their summary
+        self.path = os.path.join(tempfile.gettempdir(), f"verkv_clocks_gpu{device_index}_{os.getpid()}.csv")
 
     def __enter__(self):
         os.makedirs(os.path.dirname(self.path), exist_ok=True)
@@ -384,7 +386,7 @@ def run_ours(args, world, rank, local):
     peak, peak_src = measured_peaks()
     link_src = "measured: 256 MiB page-locked cudaMemcpyAsync, best of 5"
 
-    # Algorithmic bytes per launch of each kernel of the step ("Roofline"); the bound
+    # Algorithmic bytes per launch of each kernel of the step; the bound
     # is HBM except for the fetch, which is bound by the host link.
     with torch.cuda.stream(stream):
         step(counts=True)
