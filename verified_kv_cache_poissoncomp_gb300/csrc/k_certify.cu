@@ -474,8 +474,7 @@ __device__ __forceinline__ void fetch_list_tail(const CertifyArgs &a, int ul, in
 
 template <int CL, bool SL>
 __global__ void __launch_bounds__(CT_NT, 1) k_certify(CertifyArgs a) {
-    pdl_wait();
-    pdl_trigger();
+    pdl_trigger();  // pdl_wait() follows the loads of r, which no early-starting kernel writes
     extern __shared__ __align__(16) unsigned char smem_raw[];
     float *wrec = reinterpret_cast<float *>(smem_raw);
     float *xrec = wrec + CT_NW * CT_REC;
@@ -510,12 +509,13 @@ __global__ void __launch_bounds__(CT_NT, 1) k_certify(CertifyArgs a) {
 #pragma unroll
         for (int k = 0; k < TPT; ++k) {
             const int i = tid + k * CT_NT, t = base + i;
-            sv[k] = NEG_INF;
-            rv[k] = 1.0f;
-            if (i < chunk && t < n) {
-                sv[k] = sc[t];
-                rv[k] = rf[t];
-            }
+            rv[k] = (i < chunk && t < n) ? rf[t] : 1.0f;
+        }
+        pdl_wait();  // the logits come from the kernel before this one
+#pragma unroll
+        for (int k = 0; k < TPT; ++k) {
+            const int i = tid + k * CT_NT, t = base + i;
+            sv[k] = (i < chunk && t < n) ? sc[t] : NEG_INF;
             tmax = fmaxf(tmax, sv[k]);
         }
         float d = 0.f, c = 0.f, cnt = 0.f;

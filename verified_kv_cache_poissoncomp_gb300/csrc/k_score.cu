@@ -123,7 +123,9 @@ __device__ __forceinline__ unsigned long long bf16x2_to_f32x2(uint32_t w) {
 // per head.
 template <int D, int G>
 __global__ void __launch_bounds__(SC_NT, SC_CTAS_PER_SM) k_score(ScoreArgs a, int spans_per_unit, int span_rows) {
-    pdl_wait();
+    // The query and the sketch are never written by a kernel that lets this one start early (the
+    // decode path's kernels write only the workspace and the outputs), so the first stages are
+    // requested before waiting for the previous kernel; the logits are written after it.
     pdl_trigger();
     constexpr int CPL = G <= 4 ? 16 : 8, NV = CPL / 8;
     constexpr int LPR = D / CPL, RPW = 32 / LPR, NW = SC_NT / 32;
@@ -177,6 +179,7 @@ __global__ void __launch_bounds__(SC_NT, SC_CTAS_PER_SM) k_score(ScoreArgs a, in
     };
     if (tid == 0)
         for (int k = 0; k < min(SC_STAGES, nst); ++k) issue(k);
+    pdl_wait();
 
     float *out = a.scores + (size_t)ul * G * a.n + row0;
     int consumed = 0;
