@@ -1081,6 +1081,8 @@ __global__ void __launch_bounds__(SL_NT, 1) k_shortlist(ShortlistArgs a) {
     extern __shared__ uint32_t s_ord[];  // CACHED: the order key of every token of the unit
     __shared__ uint32_t hist[4096];
     __shared__ uint32_t s_prefix, s_need, s_eq, s_nl;
+    pdl_wait();  // the logits come from the kernel before this one
+    pdl_trigger();
     __shared__ int s_wcnt[SL_NT / 32];
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int ul = blockIdx.x;
@@ -1213,11 +1215,9 @@ cudaError_t launch_shortlist(const ShortlistArgs &a, int units_layer, cudaStream
             if (e != cudaSuccess) return e;
             attr = true;
         }
-        k_shortlist<true><<<units_layer, SL_NT, smem, s>>>(a);
-    } else {
-        k_shortlist<false><<<units_layer, SL_NT, 0, s>>>(a);
+        return launch_pdl(k_shortlist<true>, dim3(units_layer), dim3(SL_NT), smem, s, a);
     }
-    return cudaGetLastError();
+    return launch_pdl(k_shortlist<false>, dim3(units_layer), dim3(SL_NT), 0, s, a);
 }
 
 }  // namespace verkv

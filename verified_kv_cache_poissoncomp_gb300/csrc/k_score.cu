@@ -279,6 +279,7 @@ __device__ __forceinline__ unsigned long long fadd2(unsigned long long a, unsign
 template <int D, int G>
 __global__ void __launch_bounds__(SC_NT, SC_CTAS_PER_SM) k_score_q2(ScoreArgs a, int spans_per_unit,
                                                                    int span_rows) {
+    pdl_trigger();  // as in k_score: the first stages are requested before pdl_wait()
     constexpr int CPL = G <= 4 ? 16 : 8;
     constexpr int LPR = D / CPL, RPW = 32 / LPR, NW = SC_NT / 32;
     constexpr int ROWB = (D / 4 + 4 * (D / 32) + 15) / 16 * 16;  // bytes per sketch row
@@ -340,6 +341,7 @@ __global__ void __launch_bounds__(SC_NT, SC_CTAS_PER_SM) k_score_q2(ScoreArgs a,
     };
     if (tid == 0)
         for (int k = 0; k < min(SC_STAGES, nst); ++k) issue(k);
+    pdl_wait();
 
     float *out = a.scores + (size_t)ul * G * a.n + row0;
     int consumed = 0;
@@ -418,8 +420,7 @@ cudaError_t launch_score_q2(const ScoreArgs &a, int units_layer, cudaStream_t s)
             if (e != cudaSuccess) return e;                                                     \
             attr = true;                                                                        \
         }                                                                                       \
-        k_score_q2<DD, GG><<<grid, SC_NT, smem, s>>>(a, spans, (int)span_rows);                 \
-        return cudaGetLastError();                                                              \
+        return launch_pdl(k_score_q2<DD, GG>, grid, dim3(SC_NT), smem, s, a, spans, (int)span_rows); \
     }
     VERKV_SCORE_Q2(128, 1) VERKV_SCORE_Q2(128, 2) VERKV_SCORE_Q2(128, 4) VERKV_SCORE_Q2(128, 8)
     VERKV_SCORE_Q2(64, 1) VERKV_SCORE_Q2(64, 2) VERKV_SCORE_Q2(64, 4) VERKV_SCORE_Q2(64, 8)
