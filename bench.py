@@ -61,6 +61,12 @@ def parse_args():
     p.add_argument("--pc-sweep", action="store_true",
                    help="PoissonComp throughput: 36 layers x 8 KV heads, n in {32K, 128K}, "
                         "eta in {1/8, 1/16, 1/32}")
+    p.add_argument("--pc-n", type=int, nargs="+", default=[32768, 131072],
+                   help="context lengths of the PoissonComp sweep")
+    p.add_argument("--pc-eta", type=float, nargs="+", default=[1 / 8, 1 / 16, 1 / 32],
+                   help="budget fractions of the PoissonComp sweep")
+    p.add_argument("--pc-heads", type=int, default=36 * 8,
+                   help="heads per PoissonComp call (a multiple of 8: layers x 8 KV heads)")
     p.add_argument("--dense-offload", action="store_true",
                    help="the offloaded-dense baseline alone (every row from the host cache)")
     return p.parse_args()
@@ -791,9 +797,9 @@ def run_long128k(args, local):
 
 def run_pc_sweep(args, local):
     """One GPU: verkv_poissoncomp (c solve, Poisson sample, compaction, pivotal K/V gather) over
-    every head of a 36-layer x 8-KV-head cache per call, for n in {32K, 128K} and eta in
-    {1/8, 1/16, 1/32}; H = 4 sink + 512 local; tau lognormal(0, 1.5) normalised per head; K/V
-    bytes random on the device.  One JSON line."""
+    every head of a 36-layer x 8-KV-head cache per call (--pc-heads), for n in {32K, 128K}
+    (--pc-n) and eta in {1/8, 1/16, 1/32} (--pc-eta); H = 4 sink + 512 local; tau lognormal(0,
+    1.5) normalised per head; K/V bytes random on the device.  One JSON line."""
     import torch
 
     from verified_kv_cache_poissoncomp_gb300 import binding as B
@@ -803,19 +809,22 @@ def run_pc_sweep(args, local):
     B.lib()
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
-    layers, kvh, d = 36, 8, 128
+    kvh, d = 8, 128
+    if args.pc_heads < kvh or args.pc_heads % kvh:
+        raise SystemExit("--pc-heads must be a positive multiple of 8")
+    layers = args.pc_heads // kvh
     units = layers * kvh
     peak, peak_src = measured_peaks()
     stream = torch.cuda.Stream(dev)
     rows = []
-    for n in (32768, 131072):
+    for n in args.pc_n:
         tau = torch.from_numpy(I.pc_sweep_tau(units, n)).to(dev)
         gen = torch.Generator(device=dev)
         gen.manual_seed(1240)
         kv = torch.empty((units, n, 2, d), dtype=torch.int16, device=dev)
         kv.random_(-32768, 32767, generator=gen)
         r_full = torch.empty((units, n), dtype=torch.float32, device=dev)
-        for eta in (1 / 8, 1 / 16, 1 / 32):
+        for eta in args.pc_eta:
             cap = default_cap(n, eta)
             shape = B.verkv_shape(1, layers, kvh, 4, d, n, cap)
             ws_bytes = B.verkv_workspace_size(shape)
@@ -866,8 +875,8 @@ def run_pc_sweep(args, local):
     print(json.dumps({"sweep": "poissoncomp", "unit": "heads/s", "steps": args.steps,
                       "warmup": args.warmup, "data": "synthetic", "hbm_peak_GBs": peak,
                       "peak_source": peak_src,
-                      "config": {"workload": "36 layers x 8 KV heads per call, d=128, H=4+512, "
-                                             "tau lognormal(0,1.5) normalised per head"},
+                      "config": {"workload": f"{layers} layers x 8 KV heads per call, d=128, "
+                                             "H=4+512, tau lognormal(0,1.5) normalised per head"},
                       "rows": rows}), flush=True)
 
 

@@ -23,6 +23,7 @@ namespace verkv {
 constexpr int PC_NT = 1024;
 constexpr int PC_NW = PC_NT / 32;
 constexpr int PC_MAX_CL = 8;
+constexpr int PC_LD = 4;  // four-token tau loads in flight per thread
 
 struct PcSmem {
     float *tau;        // [chunk]: tau of non-forced tokens, 0 for forced tokens and padding
@@ -31,27 +32,46 @@ struct PcSmem {
     double *dslots;    // [2][PC_MAX_CL][PC_NW][2]
     int *wcount;       // [PC_NW]
     int *cta_total;    // [PC_MAX_CL]
+    double *bc_c;      // [1]: the current c, written by thread 0
+    float *bc_thr;     // [1]: its float32 saturation threshold
 };
 
 static size_t pc_smem_bytes(int chunk) {
-    return (size_t)chunk * 4 + (size_t)(chunk / 32) * 4 + 2 * PC_MAX_CL * PC_NW * 2 * 4 +
+    return 16 + (size_t)chunk * 4 + (size_t)(chunk / 32) * 4 + 2 * PC_MAX_CL * PC_NW * 2 * 4 +
            2 * PC_MAX_CL * PC_NW * 2 * 8 + PC_NW * 4 + PC_MAX_CL * 4 + 64;
 }
 
-// tau (in (0, 1]) as 64-bit fixed point with 46 fractional bits, from 32-bit arithmetic:
-// the integer part of tau 2^14 and 32 bits of what remains (truncated below 2^-46).
+// tau (in [0, 1]) as 64-bit fixed point with 46 fractional bits, truncated: floor(tau 2^46).
+// With tau = m 2^(e - 150) (m the significand with its implicit bit, e the biased exponent, at
+// most 127 here), floor(tau 2^46) = (m 2^23) >> (127 - e): integer operations only.
 __device__ __forceinline__ unsigned long long tau_fixed(float x) {
-    const float y = x * 16384.0f;
-    const float hi = truncf(y);
-    return ((unsigned long long)__float2uint_rz(hi) << 32) |
-           (unsigned long long)__float2uint_rz((y - hi) * 4294967296.0f);
+    const uint32_t bits = __float_as_uint(x);
+    const uint32_t e = bits >> 23;
+    const unsigned long long m =
+        (unsigned long long)((bits & 0x7FFFFFu) | (e ? 0x800000u : 0u)) << 23;
+    const uint32_t rs = 127u - e;
+    return rs < 64u ? m >> rs : 0ull;
 }
+// r (in [0, 1]) in units of 2^-24, truncated: floor(r 2^24) = m >> (126 - e) below 1 (m the
+// significand with its implicit bit, e the biased exponent), 2^24 at 1.  The budget check sums
+// these: n 2^-24 of truncation is far inside its tolerance.
+__device__ __forceinline__ uint32_t r_fixed24(float r) {
+    const uint32_t bits = __float_as_uint(r);
+    const uint32_t e = bits >> 23;
+    const uint32_t m = (bits & 0x7FFFFFu) | (e ? 0x800000u : 0u);
+    if (e >= 127u) return 1u << 24;
+    const uint32_t rs = 126u - e;
+    return rs < 32u ? m >> rs : 0u;
+}
+constexpr double R_FIXED_UNIT = 1.0 / 16777216.0;  // 2^-24
 constexpr double TAU_FIXED_UNIT = 1.0 / 70368744177664.0;  // 2^-46
 
 __global__ void __launch_bounds__(PC_NT, 1) k_pc_solve(PcArgs a) {
     extern __shared__ __align__(16) unsigned char smem_raw[];
     PcSmem sm;
-    sm.dslots = reinterpret_cast<double *>(smem_raw);
+    sm.bc_c = reinterpret_cast<double *>(smem_raw);
+    sm.bc_thr = reinterpret_cast<float *>(smem_raw + 8);
+    sm.dslots = reinterpret_cast<double *>(smem_raw + 16);
     sm.fslots = reinterpret_cast<float *>(sm.dslots + 2 * PC_MAX_CL * PC_NW * 2);
     sm.tau = sm.fslots + 2 * PC_MAX_CL * PC_NW * 2;
     sm.bits = reinterpret_cast<uint32_t *>(sm.tau + a.chunk);
@@ -72,33 +92,55 @@ __global__ void __launch_bounds__(PC_NT, 1) k_pc_solve(PcArgs a) {
     ClusterReducer<PC_NW, 2> red{sm.fslots, a.cl, 0};
     ClusterReducer64<PC_NW> red64{sm.dslots, a.cl, 0};
 
-    // 1. Load tau of the non-forced tokens; validate it.
-    float tsum = 0.0f, tmin = __int_as_float(0x7F800000);
+    // 1. Load tau of the non-forced tokens; validate it.  Each thread keeps PC_LD four-token
+    //    loads in flight (16-byte vectors when the tau rows are 16-byte aligned).
     unsigned long long tfix = 0ull;  // exact sum of tau
     bool bad = false;
-    for (int i = tid; i < a.chunk; i += PC_NT) {
-        const int t = base + i;
-        float x = 0.0f;
-        if (t < n && !(t < a.n_sink || t >= n - a.n_local)) {
-            x = tau[t];
-            if (!(x > 0.0f && x <= 1.0f)) {  // also catches NaN
-                bad = true;
-                x = 1.0f;
+    const bool vec = (reinterpret_cast<uintptr_t>(a.tau) & 15u) == 0 && (n & 3) == 0;
+    const int nvec = a.chunk / 4;
+    for (int v0 = 0; v0 < nvec; v0 += PC_NT * PC_LD) {
+        float4 xs[PC_LD];
+#pragma unroll
+        for (int k = 0; k < PC_LD; ++k) {
+            const int v = v0 + k * PC_NT + tid;
+            const int t = base + 4 * v;
+            float4 x = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+            if (v < nvec && t < n) {
+                if (vec) {
+                    x = __ldg(reinterpret_cast<const float4 *>(tau + t));
+                } else {
+                    x.x = tau[t];
+                    if (t + 1 < n) x.y = tau[t + 1];
+                    if (t + 2 < n) x.z = tau[t + 2];
+                    if (t + 3 < n) x.w = tau[t + 3];
+                }
             }
-            tmin = fminf(tmin, x);
-            tsum += x;
-            tfix += tau_fixed(x);
+            xs[k] = x;
         }
-        sm.tau[i] = x;
+#pragma unroll
+        for (int k = 0; k < PC_LD; ++k) {
+            const int v = v0 + k * PC_NT + tid;
+            if (v >= nvec) break;
+            float e[4] = {xs[k].x, xs[k].y, xs[k].z, xs[k].w};
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const int t = base + 4 * v + j;
+                float x = 0.0f;
+                if (t < n && !(t < a.n_sink || t >= n - a.n_local)) {
+                    x = e[j];
+                    if (!(x > 0.0f && x <= 1.0f)) {  // also catches NaN
+                        bad = true;
+                        x = 1.0f;
+                    }
+                    tfix += tau_fixed(x);
+                }
+                e[j] = x;
+            }
+            *reinterpret_cast<float4 *>(sm.tau + 4 * v) = make_float4(e[0], e[1], e[2], e[3]);
+        }
     }
     if (bad) raise_error(a.err, ERR_TAU);
     {
-        float v[2] = {tsum, 0.0f};
-        red.run(v, OpSum());
-        tsum = v[0];
-        float m[2] = {-tmin, 0.0f};
-        red.run(m, OpMax());
-        tmin = -m[0];
         unsigned long long z = 0ull;
         red64.run_u64(tfix, z);
     }
@@ -108,27 +150,55 @@ __global__ void __launch_bounds__(PC_NT, 1) k_pc_solve(PcArgs a) {
     if (a.n_rest > 0 && a.b_rest < (double)a.n_rest) {
         // 2. Newton on the concave piecewise-linear F from below.  A token saturates at c when
         //    tau >= 1 / c, i.e. tau >= the float32 rounded up from 1 / c.
-        auto eval_exact = [&](double cc, unsigned long long &sat, unsigned long long &tun) {
-            const float thr = __double2float_ru(1.0 / cc);
-            unsigned long long s = 0ull, T = 0ull;
-            for (int i = tid; i < a.chunk; i += PC_NT) {
-                const float x = sm.tau[i];
-                if (x > 0.0f) {
-                    if (x >= thr) s += 1ull; else T += tau_fixed(x);
+        // The unsaturated sum is the total less the saturated tokens' sum (exact integers), so
+        // a pass converts only the few saturated tau.
+        // The unsaturated sum is the total less the saturated tokens' sum (exact integers), so
+        // a pass converts only the few saturated tau, on a branch the other tokens skip.  thr is
+        // positive, so padding and forced tokens (tau 0 here) never count.
+        auto eval_exact = [&](float thr, unsigned long long &sat, unsigned long long &tun) {
+            unsigned long long s = 0ull, Ts = 0ull;
+            const float4 *t4 = reinterpret_cast<const float4 *>(sm.tau);
+            for (int v = tid; v < a.chunk / 4; v += PC_NT) {
+                const float4 q = t4[v];
+                const uint32_t m = (q.x >= thr ? 1u : 0u) | (q.y >= thr ? 2u : 0u) |
+                                   (q.z >= thr ? 4u : 0u) | (q.w >= thr ? 8u : 0u);
+                if (m) {
+                    s += (unsigned long long)__popc(m);
+                    if (m & 1u) Ts += tau_fixed(q.x);
+                    if (m & 2u) Ts += tau_fixed(q.y);
+                    if (m & 4u) Ts += tau_fixed(q.z);
+                    if (m & 8u) Ts += tau_fixed(q.w);
                 }
             }
-            red64.run_u64(T, s);
+            red64.run_u64(Ts, s);
             sat = s;
-            tun = T;
+            tun = tfix - Ts;
         };
-        const double tsum_exact = (double)tfix * TAU_FIXED_UNIT;
-        c = a.b_rest / tsum_exact * (1.0 - 0x1p-40);  // F(c) <= c sum tau <= B
+        // The scalar fp64 steps (a divide per pass) run on thread 0 and reach the other threads
+        // through shared memory: fp64 throughput is a few operations per clock per SM here, so a
+        // divide on every thread would cost microseconds a pass.  The next write comes after the
+        // next reduction's barrier, so one slot suffices.
+        auto share = [&](double &cc) -> float {
+            if (tid == 0) {
+                *sm.bc_c = cc;
+                *sm.bc_thr = fmaxf(__double2float_ru(1.0 / cc), __int_as_float(1));
+            }
+            __syncthreads();
+            cc = *sm.bc_c;
+            return *sm.bc_thr;
+        };
+        double cc = 0.0;
+        if (tid == 0) cc = a.b_rest / ((double)tfix * TAU_FIXED_UNIT) * (1.0 - 0x1p-40);  // F(c) <= c sum tau <= B
+        float thr = share(cc);
+        c = cc;
         unsigned long long s, T;
-        eval_exact(c, s, T);
+        eval_exact(thr, s, T);
         for (int it = 0; it < 8 && T > 0ull; ++it) {
-            const double cn = (a.b_rest - (double)s) / ((double)T * TAU_FIXED_UNIT);
+            double cn = 0.0;
+            if (tid == 0) cn = (a.b_rest - (double)s) / ((double)T * TAU_FIXED_UNIT);
+            thr = share(cn);
             unsigned long long s2, T2;
-            eval_exact(cn, s2, T2);
+            eval_exact(thr, s2, T2);
             c = cn;
             if (s2 == s) {
                 solved = true;
@@ -142,6 +212,22 @@ __global__ void __launch_bounds__(PC_NT, 1) k_pc_solve(PcArgs a) {
         const float B = (float)a.b_rest;
         // Fallback.  Bisection on float32 c: F(lo) <= B <= F(hi): at lo every tau is scaled below its
         //    unclipped sum; at hi = 2 / min tau every token saturates.
+        float tsum = 0.0f, tmin = __int_as_float(0x7F800000);
+        for (int i = tid; i < a.chunk; i += PC_NT) {
+            const float x = sm.tau[i];
+            if (x > 0.0f) {
+                tmin = fminf(tmin, x);
+                tsum += x;
+            }
+        }
+        {
+            float v[2] = {tsum, 0.0f};
+            red.run(v, OpSum());
+            tsum = v[0];
+            float m[2] = {-tmin, 0.0f};
+            red.run(m, OpMax());
+            tmin = -m[0];
+        }
         float lo = (float)(a.b_rest / (double)tsum) * 0.999f;
         float hi = 2.0f / tmin;
         for (int it = 0; it < 64; ++it) {
@@ -188,24 +274,13 @@ __global__ void __launch_bounds__(PC_NT, 1) k_pc_solve(PcArgs a) {
     }
     const float c32 = (float)c;
 
-    // 4. r_i = min(1, c tau_i) as a float32 product (1 for forced H); the budget check in fp64.
+    // 4-5. r_i = min(1, c tau_i) as a float32 product (1 for forced H), written out and summed
+    //    (in units of 2^-24) for the budget check, and the draws: lane j of a warp takes tokens 4j..4j+3 of a
+    //    128-token group (one Philox block), and shuffles turn the four keep bits of eight lanes
+    //    into one bitmap word.
     float *r_full = a.r_full + (size_t)u * n;
-    unsigned long long rfix = 0ull, zero = 0ull;  // exact sum of the float32 r
-    for (int i = tid; i < a.chunk; i += PC_NT) {
-        const int t = base + i;
-        if (t >= n) break;
-        const float x = sm.tau[i];
-        const float r = (x > 0.0f) ? fminf(1.0f, __fmul_rn(c32, x)) : 1.0f;
-        r_full[t] = r;
-        rfix += tau_fixed(r);
-    }
-    red64.run_u64(rfix, zero);
-    const double rsum = (double)rfix * TAU_FIXED_UNIT;
-    if (!(fabs(rsum - a.eta_n) < 1e-6 * (double)n) && tid == 0 && crank == 0)
-        raise_error(a.err, ERR_BUDGET_SUM);
-
-    // 5. Draws: lane j of a warp takes tokens 4j..4j+3 of a 128-token group (one Philox block),
-    //    and shuffles turn the four keep bits of eight lanes into one bitmap word.
+    const bool rvec = (reinterpret_cast<uintptr_t>(a.r_full) & 15u) == 0 && (n & 3) == 0;
+    uint32_t rfix = 0u;  // sum of floor(r 2^24): chunk / 1024 <= 32 tokens a thread, below 2^30
     const int wchunk = a.chunk / PC_NW;  // tokens per warp, a multiple of 32
     const int wbase = warp * wchunk;
     int wcnt = 0;
@@ -216,16 +291,28 @@ __global__ void __launch_bounds__(PC_NT, 1) k_pc_solve(PcArgs a) {
                                                    (uint32_t)b), a.seed_lo, a.seed_hi);
         const uint32_t words[4] = {blk.x, blk.y, blk.z, blk.w};
         uint32_t nib = 0;
-        if (g0 + 4 * lane < wchunk) {
+        if (g0 + 4 * lane < wchunk && t0 < n) {
+            const float4 q = *reinterpret_cast<const float4 *>(sm.tau + i0);
+            const float xs[4] = {q.x, q.y, q.z, q.w};
+            float rr[4];
 #pragma unroll
             for (int k = 0; k < 4; ++k) {
                 const int t = t0 + k;
+                const float x = xs[k];
+                const float r = (x > 0.0f) ? fminf(1.0f, __fmul_rn(c32, x)) : 1.0f;
+                rr[k] = r;
                 if (t < n) {
-                    const float x = sm.tau[i0 + k];
-                    const float r = (x > 0.0f) ? fminf(1.0f, __fmul_rn(c32, x)) : 1.0f;
+                    rfix += r_fixed24(r);
                     const float uu = (float)(words[k] >> 8) * 0x1p-24f;
                     nib |= (uu < r ? 1u : 0u) << k;
                 }
+            }
+            if (rvec) {
+                *reinterpret_cast<float4 *>(r_full + t0) = make_float4(rr[0], rr[1], rr[2], rr[3]);
+            } else {
+#pragma unroll
+                for (int k = 0; k < 4; ++k)
+                    if (t0 + k < n) r_full[t0 + k] = rr[k];
             }
         }
         uint32_t val = nib << (4 * (lane & 7));
@@ -240,6 +327,12 @@ __global__ void __launch_bounds__(PC_NT, 1) k_pc_solve(PcArgs a) {
     wcnt = warp_sum(wcnt);
     if (lane == 0) sm.wcount[warp] = wcnt;
     __syncthreads();
+    unsigned long long rtot = rfix, zero = 0ull;
+    red64.run_u64(rtot, zero);
+    if (tid == 0 && crank == 0) {
+        const double rsum = (double)rtot * R_FIXED_UNIT;
+        if (!(fabs(rsum - a.eta_n) < 1e-6 * (double)n)) raise_error(a.err, ERR_BUDGET_SUM);
+    }
 
     // Cluster-wide exclusive scan of the per-CTA counts (distributed shared memory).
     if (tid == 0) {
@@ -317,22 +410,40 @@ cudaError_t launch_pc_solve(const PcArgs &a, int units, cudaStream_t s) {
 }
 
 // ---------------------------------------------------------------------------------------------
-// Row copies: one warp per 4d-byte row, 16-byte vectors.
+// Row copies: a warp takes 32 consecutive pivotal slots of one unit, reads their ids at once (a
+// lane each) and keeps PG_ROWS rows of 4d bytes in flight, in 16-byte vectors.
+constexpr int PG_ROWS = 8;
 __global__ void __launch_bounds__(256) k_pc_gather(const uint4 *kv_full, const int32_t *ids,
                                                    const int32_t *count, uint4 *pkv, int units,
                                                    int cap, int n, int row16) {
     const int lane = threadIdx.x & 31;
+    const int groups = (cap + 31) / 32;  // 32-slot groups per unit
     const int64_t gw = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
     const int64_t nw = ((int64_t)gridDim.x * blockDim.x) >> 5;
-    const int64_t total = (int64_t)units * cap;
+    const int64_t total = (int64_t)units * groups;
     for (int64_t item = gw; item < total; item += nw) {
-        const int u = (int)(item / cap);
-        const int slot = (int)(item - (int64_t)u * cap);
-        if (slot >= count[u]) continue;
-        const int id = ids[(size_t)u * cap + slot];
-        const uint4 *src = kv_full + ((size_t)u * n + id) * row16;
-        uint4 *dst = pkv + ((size_t)u * cap + slot) * row16;
-        for (int v = lane; v < row16; v += 32) dst[v] = ldg_stream(src + v);
+        const int u = (int)(item / groups);
+        const int s0 = (int)(item - (int64_t)u * groups) * 32;
+        const int cnt = count[u];
+        if (s0 >= cnt) continue;
+        const int rows = cnt - s0 < 32 ? cnt - s0 : 32;
+        const int my_id = lane < rows ? ids[(size_t)u * cap + s0 + lane] : 0;
+        const uint4 *src = kv_full + (size_t)u * n * row16;
+        uint4 *dst = pkv + ((size_t)u * cap + s0) * row16;
+        for (int r0 = 0; r0 < rows; r0 += PG_ROWS) {
+            int id[PG_ROWS];
+#pragma unroll
+            for (int k = 0; k < PG_ROWS; ++k) id[k] = __shfl_sync(0xFFFFFFFFu, my_id, (r0 + k) & 31);
+            for (int v = lane; v < row16; v += 32) {
+                uint4 buf[PG_ROWS];
+#pragma unroll
+                for (int k = 0; k < PG_ROWS; ++k)
+                    if (r0 + k < rows) buf[k] = ldg_stream(src + (size_t)id[k] * row16 + v);
+#pragma unroll
+                for (int k = 0; k < PG_ROWS; ++k)
+                    if (r0 + k < rows) dst[(size_t)(r0 + k) * row16 + v] = buf[k];
+            }
+        }
     }
 }
 
@@ -342,9 +453,13 @@ cudaError_t launch_pc_gather(const uint16_t *kv_full, const int32_t *ids, const 
     int sms = 0, dev = 0;
     cudaGetDevice(&dev);
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    const int64_t warps = (int64_t)units * cap;
+    int per_sm = 0;
+    cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k_pc_gather, 256, 0);
+    if (e != cudaSuccess) return e;
+    if (per_sm < 1) per_sm = 1;
+    const int64_t warps = (int64_t)units * ((cap + 31) / 32);
     int blocks = (int)((warps + 7) / 8);
-    if (blocks > sms * 8) blocks = sms * 8;
+    if (blocks > sms * per_sm) blocks = sms * per_sm;
     if (blocks < 1) blocks = 1;
     k_pc_gather<<<blocks, 256, 0, s>>>(reinterpret_cast<const uint4 *>(kv_full), ids, count,
                                        reinterpret_cast<uint4 *>(pkv), units, cap, n, row16);
