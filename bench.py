@@ -67,6 +67,11 @@ def parse_args():
                    help="budget fractions of the PoissonComp sweep")
     p.add_argument("--pc-heads", type=int, default=36 * 8,
                    help="heads per PoissonComp call (a multiple of 8: layers x 8 KV heads)")
+    p.add_argument("--estimator", action="store_true",
+                   help="the shrinkage-estimator pass over the pivotal set alone: batch 32 x 8 KV "
+                        "heads x 4 query heads at 32K, eta = 1/16, its HBM rate")
+    p.add_argument("--est-batch", type=int, default=32,
+                   help="sequences in the --estimator workload (8 KV heads each)")
     p.add_argument("--dense-offload", action="store_true",
                    help="the offloaded-dense baseline alone (every row from the host cache)")
     return p.parse_args()
@@ -406,7 +411,7 @@ def run_ours(args, world, rank, local):
     fetch_row_bytes = (2 if args.sketch == "exact" else 4) * w.d
     algo = {
         "k_score": ("hbm", units_layer * w.n * sketch_row_bytes),
-        # latency- and issue-bound: judged by warp instructions issued, not bytes
+        # latency- and issue-bound: measured by warp instructions issued, not bytes
         "k_certify": ("alu", units_layer * (w.G * w.n * 4 + w.n * 4)),  # logits + r
         "k_partial(pivotal)": ("hbm", int(counts.mean() * units_layer * (4 * w.d + 8))),
         # with the exact sketch only V rows (2 d bytes) cross the host link, else K|V rows; the
@@ -880,6 +885,85 @@ def run_pc_sweep(args, local):
                       "rows": rows}), flush=True)
 
 
+def run_estimator(args, local):
+    """One GPU: the shrinkage-estimator attention over the pivotal set (D-hat, N-hat and the
+    second moment), timed alone.  In MEMCPY fetch mode the pivotal sums are their own launch,
+    k_partial(pivotal); in zero-copy mode the same item code runs inside k_refine behind the host
+    reads.  Workload: the decode-step cache generator at batch 32 (--est-batch) x 8 KV heads x 4 query heads,
+    d = 128, n = 32768, eta = 1/16, H = 4 + 512, eps = delta = 0.05; one layer call of 1024 query
+    heads per step, eager (the MEMCPY path waits on the host for the selection).  The pivotal rows
+    (~270 MB a call) are larger than L2, and k_score streams 2 GB of sketch before each pass.
+    One JSON line."""
+    import torch
+
+    from verified_kv_cache_poissoncomp_gb300 import binding as B
+    from verified_kv_cache_poissoncomp_gb300 import inputs as I
+    from verified_kv_cache_poissoncomp_gb300.engine import VerKV, default_cap
+
+    B.lib()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    batch, layers, kvh, G, d, n, eta = args.est_batch, 1, 8, 4, 128, 32768, 1 / 16
+    units = batch * layers * kvh
+    peak, peak_src = measured_peaks()
+    stream = torch.cuda.Stream(dev)
+    with torch.cuda.stream(stream):
+        tau, kv, queries = I.decode_step_cache_torch(units, n, d, G, layers, batch, kvh, dev)
+        host_kv = torch.empty(kv.shape, dtype=torch.int16, pin_memory=True)
+        host_kv.copy_(kv)
+        torch.cuda.synchronize()
+        eng = VerKV(batch, layers, kvh, G, d, n, default_cap(n, eta),
+                    fetch_mode=B.VERKV_FETCH_MEMCPY)
+        eng.load_device(tau, kv, host_kv)
+        eng.compress(eta, 4, 512, 0)
+        eng.sync()
+        q = queries[0].contiguous()
+        hq = batch * kvh * G
+        o = torch.empty((hq, d), dtype=torch.float32, device=dev)
+        lse = torch.empty((hq,), dtype=torch.float32, device=dev)
+        st = torch.empty((hq, 16), dtype=torch.int32, device=dev)
+
+        def step():
+            B.verkv_attend_verified(eng.ctx, 0, q.data_ptr(), eng.pivotal, eng.r_full.data_ptr(),
+                                    eng.sketch_desc, 0.05, 0.05, None, None)
+            B.verkv_fetch_refine(eng.ctx, None, None, eng.host_kv.data_ptr(), o.data_ptr(),
+                                 lse.data_ptr(), st.data_ptr())
+
+        for _ in range(args.warmup):
+            step()
+        B.verkv_sync(eng.ctx)
+        B.verkv_profile_enable(eng.ctx, 1)
+        for _ in range(args.steps):
+            step()
+        launches, total_ms = B.verkv_profile_read(eng.ctx)
+        B.verkv_profile_enable(eng.ctx, 0)
+        B.verkv_sync(eng.ctx)
+    cnt = eng.p_count.cpu().numpy().astype(np.int64)
+    pr = eng.p_r.cpu().numpy()
+    n_l = int(sum(int((pr[u, :cnt[u]] < 1.0).sum()) for u in range(units)))
+    # algorithmic bytes: each pivotal row's K and V (4d), its id and r (8), and for a sampled
+    # row the sketch logit of each of the G query heads (lambda); the queries are negligible
+    nbytes = int(cnt.sum()) * (4 * d + 8) + n_l * 4 * G
+    k = B.VERKV_K_PARTIAL_PIVOTAL
+    us = 1e3 * total_ms[k] / max(launches[k], 1)
+    gbs = nbytes / (us * 1e-6) / 1e9
+    print(json.dumps({
+        "workload": "estimator", "unit": "GB/s", "steps": args.steps, "warmup": args.warmup,
+        "data": "synthetic",
+        "config": {"workload": f"shrinkage-estimator pass over the pivotal set: batch {batch} x 8 "
+                               "KV heads x 4 query heads, d=128, n=32768, bf16, eta=1/16, "
+                               "H=4+512, eps=delta=0.05, MEMCPY fetch mode, eager",
+                   "l2": "pivotal rows larger than L2; the sketch stream flushes it each pass"},
+        "kernel": "k_partial(pivotal)", "launches": int(launches[k]), "avg_us": round(us, 3),
+        "pivotal_rows_per_call": int(cnt.sum()), "sampled_rows_per_call": n_l,
+        "algorithmic_bytes_per_launch": nbytes,
+        "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": peak, "unit": "GB/s",
+                     "frac": round(gbs / peak, 4), "peak_source": peak_src},
+        "per_kernel_us": {B.verkv_kernel_name(j): round(1e3 * total_ms[j] / launches[j], 2)
+                          for j in range(B.VERKV_K_COUNT) if launches[j] > 0}}), flush=True)
+    eng.close()
+
+
 def run_dense_offload(args, local):
     """One GPU: the offloaded-dense baseline on the bench workload, one JSON line."""
     import torch
@@ -926,6 +1010,9 @@ def main():
     elif args.long128k:
         if rank == 0:
             run_long128k(args, local)
+    elif args.estimator:
+        if rank == 0:
+            run_estimator(args, local)
     else:
         run_ours(args, world, rank, local)
 

@@ -7,6 +7,7 @@ import torch
 from tests import parity as P
 from verified_kv_cache_poissoncomp_gb300 import binding as B
 from verified_kv_cache_poissoncomp_gb300 import inputs as I
+from verified_kv_cache_poissoncomp_gb300.engine import default_cap
 
 pytestmark = pytest.mark.gpu
 
@@ -83,6 +84,21 @@ def test_memcpy_mode_matches_zerocopy():
         assert np.array_equal(x["counts"], y["counts"])
         for ul, c in enumerate(x["counts"]):
             assert np.array_equal(x["ids"][ul, :c], y["ids"][ul, :c])
+
+
+@pytest.mark.parametrize("G,d", [(4, 128), (8, 64)])
+def test_staged_pivotal_sums_match_unstaged(G, d):
+    # In MEMCPY mode the pivotal sums run in a kernel that bulk-copies each item's rows, ids and r
+    # into shared memory when the capacity is a multiple of 4 (the default capacity is), else in
+    # one that reads them from global memory; both must give the same bits and match the oracle.
+    w = I.make_workload("staged", B=2, L=1, h_kv=2, G=G, d=d, n=8192, eta=1 / 8, n_queries=3,
+                        plant_every=2)
+    cap = default_cap(w.n, w.eta)
+    assert cap % 4 == 0
+    _, a = _run_all(w, fetch_mode=B.VERKV_FETCH_MEMCPY, cap=cap)
+    _, b = _run_all(w, fetch_mode=B.VERKV_FETCH_MEMCPY, cap=cap + 1)
+    for x, y in zip(a, b):
+        assert np.array_equal(x["o"], y["o"]) and np.array_equal(x["lse"], y["lse"])
 
 
 def test_fetching_keys_too_matches_values_only():

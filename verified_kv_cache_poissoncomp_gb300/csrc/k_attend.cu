@@ -111,13 +111,22 @@ __device__ __forceinline__ uint4 ld_host(const uint4 *p) {
 // addressed by token id (ROWS_HOST: the unit's host cache) or by list position (ROWS_PIVOTAL:
 // the pivotal buffer; ROWS_STAGED: the staged rows).  An empty item writes nothing unless
 // write_empty (then a zero partial).  lo and hi are uniform over the CTA.
-template <int D, int G, int MODE>
+// SMEM (pivotal items of at most PART_ROWS rows only): the item's K|V rows, ids and r were copied
+// to the shared-memory stage `stage` ([PART_ROWS][4D bytes], then PART_ROWS ids, then PART_ROWS
+// r); the same lanes take the same rows in the same order, so the sums are bitwise those of the
+// global-memory path.
+template <int D, int G, int MODE, bool SMEM = false>
 __device__ __forceinline__ void partial_rows(const PartialArgs &a, int ul, int part_idx, int lo,
-                                             int hi, const int32_t *ids, bool write_empty) {
+                                             int hi, const int32_t *ids, bool write_empty,
+                                             const unsigned char *stage = nullptr) {
     constexpr int LPR = D / 8, RPW = 32 / LPR, NW = 4;
     constexpr int ITER = (PART_ROWS / NW) / RPW;  // row groups per warp
-    // Row groups in flight per warp: all of them for host rows (link latency), else four.
-    constexpr int U = MODE == ROWS_HOST ? ITER : (ITER < 4 ? ITER : 4);
+    // Row groups in flight per warp: all of them for host rows (link latency) and for staged
+    // rows (only the id-dependent loads are in flight), else four.
+    constexpr int U = (MODE == ROWS_HOST || SMEM) ? ITER : (ITER < 4 ? ITER : 4);
+    static_assert(!SMEM || MODE == ROWS_PIVOTAL, "staged items are pivotal");
+    const int32_t *s_id = SMEM ? reinterpret_cast<const int32_t *>(stage + PART_ROWS * 4 * D) : nullptr;
+    const float *s_r = SMEM ? reinterpret_cast<const float *>(stage + PART_ROWS * (4 * D + 4)) : nullptr;
     constexpr int SUBMASK = LPR / G - 1;
     __shared__ float sN[NW][G][D];
     __shared__ float sD[NW][RPW][G], sM[NW][RPW][G];
@@ -168,13 +177,13 @@ __device__ __forceinline__ void partial_rows(const PartialArgs &a, int ul, int p
             for (int u = 0; u < U; ++u) {
                 const int row = rbase + (it0 + u) * RPW + rg;
                 valid[u] = row < hi;
-                id[u] = valid[u] ? ids[row] : 0;
+                id[u] = valid[u] ? (SMEM ? s_id[row - lo] : ids[row]) : 0;
                 if ((unsigned)id[u] >= (unsigned)a.n) {  // not a token of the unit: skip the row
                     raise_error(a.err, ERR_BADID);
                     valid[u] = false;
                     id[u] = 0;
                 }
-                r[u] = (MODE == ROWS_PIVOTAL && valid[u]) ? prs[row] : 1.0f;
+                r[u] = (MODE == ROWS_PIVOTAL && valid[u]) ? (SMEM ? s_r[row - lo] : prs[row]) : 1.0f;
             }
             uint4 kq[U], vq[U];
             uint32_t fw[U];
@@ -188,20 +197,32 @@ __device__ __forceinline__ void partial_rows(const PartialArgs &a, int ul, int p
                 if (valid[u]) {
                     if (MODE == ROWS_PIVOTAL && r[u] < 1.0f) shat[u] = sc_h[id[u]];
                     const size_t rr = MODE == ROWS_HOST ? (size_t)id[u] : (size_t)(rbase + (it0 + u) * RPW + rg);
-                    if (keys) {
+                    if (SMEM) {
+                        // K and V come from the stage when the row is summed
+                    } else if (keys) {
                         kq[u] = ldg_stream(keys + (size_t)id[u] * (D / 8) + cgp);
                     } else if (MODE == ROWS_HOST) {
                         kq[u] = ld_host(rows + rr * a.row16 + cgp);
                     } else {
                         kq[u] = ldg_stream(rows + rr * a.row16 + cgp);
                     }
-                    if (MODE == ROWS_HOST) vq[u] = ld_host(rows + rr * a.row16 + a.voff16 + cgp);
-                    else vq[u] = ldg_stream(rows + rr * a.row16 + a.voff16 + cgp);
+                    if (SMEM) {
+                    } else if (MODE == ROWS_HOST) {
+                        vq[u] = ld_host(rows + rr * a.row16 + a.voff16 + cgp);
+                    } else {
+                        vq[u] = ldg_stream(rows + rr * a.row16 + a.voff16 + cgp);
+                    }
                     fw[u] = Fh[id[u] >> 5];
                 }
             }
 #pragma unroll
             for (int u = 0; u < U; ++u) {
+                if (SMEM && valid[u]) {
+                    const uint4 *srow = reinterpret_cast<const uint4 *>(
+                        stage + (size_t)(rbase + (it0 + u) * RPW + rg - lo) * (4 * D));
+                    kq[u] = srow[cgp];
+                    vq[u] = srow[D / 8 + cgp];
+                }
                 float k[8], v[8];
                 unpack8(kq[u], k);
                 unpack8(vq[u], v);
@@ -217,7 +238,8 @@ __device__ __forceinline__ void partial_rows(const PartialArgs &a, int ul, int p
                 // Weight of this row for the lane's head.
                 float cw = 0.0f;
                 if (valid[u]) {
-                    const float w = expf(dot * a.scale - mh_);
+                    // Weights to a few 1e-6 relative (the exp2-based exponential): the sums need 1e-3.
+                    const float w = __expf(dot * a.scale - mh_);
                     const bool inF = (fw[u] >> (id[u] & 31)) & 1u;
                     float coef;
                     if (MODE == ROWS_PIVOTAL) {
@@ -225,12 +247,13 @@ __device__ __forceinline__ void partial_rows(const PartialArgs &a, int ul, int p
                         if (ru >= 1.0f || inF) {
                             coef = 1.0f;
                         } else {
-                            // lambda is the certificate's: from the sketch weight w-hat
-                            const float wh = expf(shat[u] - mh_);
-                            float lam = 1.0f;
-                            if (wh > 0.0f)
-                                lam = fminf(1.0f, fmaxf(ru, __fdiv_rn(bh_ * ru, wh * (1.0f - ru))));
-                            coef = __fdiv_rn(lam, ru);
+                            // lambda is the certificate's, from the sketch weight w-hat, and the
+                            // coefficient lambda / r = clip(beta / (w-hat (1 - r)), 1, 1 / r) is
+                            // taken directly (1 / r when w-hat underflows: lambda = 1).
+                            const float wh = __expf(shat[u] - mh_);
+                            const float ir = __frcp_rn(ru);
+                            coef = ir;
+                            if (wh > 0.0f) coef = fminf(ir, fmaxf(1.0f, __fdividef(bh_, wh * (1.0f - ru))));
                         }
                     } else {
                         coef = inF ? 1.0f : 0.0f;
@@ -341,8 +364,135 @@ __global__ void __launch_bounds__(128) k_partial(PartialArgs a, int units_layer)
     }
 }
 
+// k_partial over the pivotal set with its rows staged by TMA.  A CTA takes the non-empty items
+// blockIdx.x, blockIdx.x + gridDim.x, ...; thread 0 streams each item's K|V rows, ids and r into
+// a ring of PV_STAGES shared-memory stages with cp.async.bulk (one mbarrier per stage), so the
+// next item's rows arrive while the current one is summed; only the id-dependent loads (the
+// sketch logit for lambda, the selection word) go to global memory, all of a warp's at once.
+// Waits are bounded: on expiry the CTA latches ERR_TIMEOUT, waits (bounded) for the copies it
+// issued and returns.
+constexpr int PV_STAGES = 2;
+// Resident CTAs per SM the grid is sized for: three fit the shared memory; with eight query heads
+// per KV head the accumulators need the registers of two.
+__host__ __device__ constexpr int pv_ctas_per_sm(int G) { return G <= 4 ? 3 : 2; }
+template <int D>
+__host__ __device__ constexpr int pv_stage_bytes() { return PIV_ITEM_ROWS * (4 * D + 8); }
+
+template <int D, int G>
+__global__ void __launch_bounds__(128, pv_ctas_per_sm(G)) k_partial_staged(PartialArgs a, int units_layer) {
+    static_assert(PIV_ITEM_ROWS == PART_ROWS, "a staged item is one block of rows");
+    extern __shared__ __align__(128) unsigned char pv_ring[];
+    __shared__ __align__(8) uint64_t full[PV_STAGES];
+    __shared__ int s_abort;
+    constexpr int SB = pv_stage_bytes<D>();
+    const int tid = threadIdx.x;
+    const int total = units_layer * a.max_chunks;
+    // The next non-empty item of this CTA at or after `item` (total when none is left).
+    auto next_item = [&](int item, int &ul, int &lo, int &hi) -> int {
+        for (; item < total; item += gridDim.x) {
+            ul = item / a.max_chunks;
+            const int ug = a.li.unit_global(ul);
+            const int count = min(a.count[ug], a.row_stride);
+            lo = (item - ul * a.max_chunks) * PIV_ITEM_ROWS;
+            if (lo < count) {
+                hi = min(lo + PIV_ITEM_ROWS, count);
+                return item;
+            }
+        }
+        return total;
+    };
+    auto issue = [&](int ul, int lo, int hi, int stage) {
+        const int ug = a.li.unit_global(ul);
+        const size_t base = (size_t)ug * a.row_stride + lo;
+        const uint32_t rows_b = (uint32_t)(hi - lo) * (4 * D);
+        const uint32_t list_b = (uint32_t)((hi - lo + 3) & ~3) * 4;  // within the capacity (a multiple of 4)
+        unsigned char *dst = pv_ring + (size_t)stage * SB;
+        uint64_t *bar = &full[stage];
+        mbar_expect_tx(bar, rows_b + 2 * list_b);
+        bulk_g2s(dst, reinterpret_cast<const unsigned char *>(a.rows) + base * (4 * D), rows_b, bar);
+        bulk_g2s(dst + PIV_ITEM_ROWS * 4 * D, a.ids + base, list_b, bar);
+        bulk_g2s(dst + PIV_ITEM_ROWS * (4 * D + 4), a.pr + base, list_b, bar);
+    };
+    if (tid == 0) {
+        for (int k = 0; k < PV_STAGES; ++k) mbar_init(&full[k], 1);
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        s_abort = 0;
+    }
+    __syncthreads();
+    pdl_wait();
+    pdl_trigger();
+    int pul = 0, plo = 0, phi = 0;  // producer (thread 0): the next item to request
+    int pitem = total, n_issued = 0;
+    if (tid == 0) {
+        pitem = next_item(blockIdx.x, pul, plo, phi);
+        for (int k = 0; k < PV_STAGES && pitem < total; ++k) {
+            issue(pul, plo, phi, k);
+            ++n_issued;
+            pitem = next_item(pitem + gridDim.x, pul, plo, phi);
+        }
+    }
+    int ul = 0, lo = 0, hi = 0, j = 0, consumed = 0;
+    for (int item = next_item(blockIdx.x, ul, lo, hi); item < total;
+         item = next_item(item + gridDim.x, ul, lo, hi), ++j) {
+        const int stage = j % PV_STAGES;
+        if (!mbar_wait_bounded(&full[stage], (uint32_t)((j / PV_STAGES) & 1))) s_abort = 1;
+        __syncthreads();
+        if (s_abort) break;
+        partial_rows<D, G, ROWS_PIVOTAL, true>(a, ul, item - ul * a.max_chunks, lo, hi, nullptr,
+                                               false, pv_ring + (size_t)stage * SB);
+        consumed = j + 1;
+        // partial_rows ends with a block barrier: every warp is done with the stage; refill it.
+        if (tid == 0 && pitem < total) {
+            fence_proxy_async_smem();
+            issue(pul, plo, phi, stage);
+            ++n_issued;
+            pitem = next_item(pitem + gridDim.x, pul, plo, phi);
+        }
+    }
+    if (s_abort) {
+        // Latch the timeout and let the copies this CTA requested land before it exits: items
+        // consumed .. n_issued - 1, item k in stage k % PV_STAGES at phase (k / PV_STAGES) & 1.
+        if (tid == 0) {
+            raise_error(a.err, ERR_TIMEOUT);
+            for (int k = consumed; k < n_issued; ++k)
+                mbar_wait_bounded(&full[k % PV_STAGES], (uint32_t)((k / PV_STAGES) & 1));
+        }
+        __syncthreads();
+    }
+}
+
 cudaError_t launch_partial(const PartialArgs &a, int units_layer, int grid, cudaStream_t s) {
     const int G = a.li.G;
+    // Pivotal items go through the staged kernel when every copy it makes is 16-byte aligned.
+    const bool staged = a.mode == ROWS_PIVOTAL && a.row16 == a.d / 4 && a.voff16 == a.d / 8 &&
+                        !a.keys && (a.row_stride & 3) == 0 &&
+                        (reinterpret_cast<uintptr_t>(a.rows) & 15) == 0 &&
+                        (reinterpret_cast<uintptr_t>(a.ids) & 15) == 0 &&
+                        (reinterpret_cast<uintptr_t>(a.pr) & 15) == 0;
+    if (staged) {
+        int sms = 0, dev = 0;
+        cudaGetDevice(&dev);
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+        const int total = units_layer * a.max_chunks;
+        const int g = std::max(1, std::min(total, sms * pv_ctas_per_sm(G)));
+#define VERKV_PSTAGED(DD, GG)                                                                   \
+        if (a.d == DD && G == GG) {                                                             \
+            const size_t smem = (size_t)PV_STAGES * pv_stage_bytes<DD>();                       \
+            static bool attr = false;                                                           \
+            if (!attr) {                                                                        \
+                cudaError_t e = cudaFuncSetAttribute(k_partial_staged<DD, GG>,                  \
+                                                     cudaFuncAttributeMaxDynamicSharedMemorySize, \
+                                                     (int)smem);                                \
+                if (e != cudaSuccess) return e;                                                 \
+                attr = true;                                                                    \
+            }                                                                                   \
+            return launch_pdl(k_partial_staged<DD, GG>, dim3(g), dim3(128), smem, s, a, units_layer); \
+        }
+        VERKV_PSTAGED(128, 1) VERKV_PSTAGED(128, 2) VERKV_PSTAGED(128, 4) VERKV_PSTAGED(128, 8)
+        VERKV_PSTAGED(64, 1) VERKV_PSTAGED(64, 2) VERKV_PSTAGED(64, 4) VERKV_PSTAGED(64, 8)
+#undef VERKV_PSTAGED
+        return cudaErrorInvalidValue;
+    }
 #define VERKV_PART(DD, GG)                                                                      \
     if (a.d == DD && G == GG) {                                                                 \
         if (a.mode == ROWS_PIVOTAL)                                                             \

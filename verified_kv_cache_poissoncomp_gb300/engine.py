@@ -20,9 +20,12 @@ def _check_dense(t, shape, dev, name):
 
 
 def default_cap(n, eta):
-    """Pivotal capacity: eta n plus 8 standard deviations of a Poisson sample size, plus 64."""
+    """Pivotal capacity: eta n plus 8 standard deviations of a Poisson sample size, plus 64,
+    rounded up to a multiple of 16 (so that every pivotal item's id and r lists start on 16-byte
+    boundaries and can be bulk-copied), at most n."""
     m = eta * n
-    return int(min(n, np.ceil(m + 8.0 * np.sqrt(m)) + 64))
+    c = int(np.ceil(m + 8.0 * np.sqrt(m)) + 64)
+    return int(min(n, (c + 15) // 16 * 16))
 
 
 class VerKV:
