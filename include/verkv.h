@@ -77,7 +77,10 @@ typedef struct {
  *   kv        bf16   [units][cap][2][d]  K row then V row of each pivotal token
  *   count     int32  [units]             |H u S|
  *   resident  uint32 [units][ceil(n/32)] bit i%32 of word i/32 set iff token i is in H u S
- *   c         float  [units]             the PoissonComp constant c (float32; +inf if eta n >= n) */
+ *   c         float  [units]             the PoissonComp constant c (float32; +inf if eta n >= n)
+ * When cap is a multiple of 4 and ids, r and kv start on 16-byte boundaries, the MEMCPY path
+ * bulk-copies each block of 64 pivotal rows (with its ids and r) into shared memory; otherwise it
+ * reads them from global memory.  Both give the same bits. */
 typedef struct {
     int32_t *ids;
     float *r;
