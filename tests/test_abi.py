@@ -100,3 +100,20 @@ def test_sketch_bytes(lib):
     s64 = B.verkv_shape(1, 1, 1, 4, 64, 1000, 100)
     assert B.verkv_sketch_bytes(s64, B.VERKV_SKETCH_Q2) == 1000 * 32
     assert B.verkv_sketch_bytes(s, 7) == 0
+
+
+def test_default_capacity():
+    # eta n plus 8 standard deviations of the Poisson sample size plus 64, rounded up to a
+    # multiple of 16 so that the MEMCPY path can bulk-copy each pivotal item's id and r lists,
+    # and never more than n.
+    import math
+
+    from verified_kv_cache_poissoncomp_gb300.engine import default_cap
+    for n in (1000, 3000, 8192, 20000, 32768, 50001, 131072):
+        for eta in (1 / 32, 1 / 16, 1 / 8, 1 / 4, 1.0):
+            m = eta * n
+            need = m + 8.0 * math.sqrt(m) + 64
+            c = default_cap(n, eta)
+            assert c <= n
+            if c < n:
+                assert c % 16 == 0 and need <= c < need + 17, (n, eta, c)
