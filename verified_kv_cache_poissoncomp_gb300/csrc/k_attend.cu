@@ -10,8 +10,8 @@
 //             one partial.  It computes the G logits, w = exp(logit - m), the
 //             weight of Eq. (5) -- 1 for H and for tokens of F, lambda / r for sampled, unfetched
 //             tokens, with the certificate's lambda = clip(beta r / (w-hat (1 - r)), r, 1) from
-//             the sketch weight w-hat -- and accumulates D-hat, N-hat and the sample second
-//             moment.  All CTAs of a query head share its shift m, so partials add without
+//             the sketch weight w-hat, taken as lambda / r = clip(beta / (w-hat (1 - r)), 1, 1 / r)
+//             -- and accumulates D-hat, N-hat and the sample second moment.  All CTAs of a query head share its shift m, so partials add without
 //             rescaling.  Three row sources:
 //               ROWS_PIVOTAL   the pivotal buffer in HBM;
 //               ROWS_STAGED    fetched rows already copied to HBM (the cudaMemcpyAsync fetch);
@@ -19,6 +19,9 @@
 //                              id -- the zero-copy fetch and the refine in one pass, no staging.
 //             When the sketch is exact the GPU already holds every key, so K comes from the sketch
 //             by token id and only the V rows cross the host link.
+// k_partial_staged   the ROWS_PIVOTAL items of the MEMCPY path with each item's rows, ids and r
+//             bulk-copied into a two-stage shared-memory ring one item ahead; the same item code
+//             reads K and V from shared memory, so the sums are bitwise those of k_partial.
 // k_refine    the zero-copy path's partial sums in one launch: the ROWS_HOST items of every KV
 //             head, each deriving its rows from the selection bitmaps of one token-id range (no
 //             fetch list needed), and the ROWS_PIVOTAL items.
