@@ -17,6 +17,7 @@ import torch
 
 import oracle as O
 from tests import parity as P
+from verified_kv_cache_poissoncomp_gb300 import binding as B
 from verified_kv_cache_poissoncomp_gb300 import inputs as I
 from verified_kv_cache_poissoncomp_gb300.engine import VerKV, default_cap, stats_to_dict
 
@@ -96,3 +97,24 @@ def test_decode_step_sampled_units(cache, eta):
     assert uncertified > 0  # the selection and the fetch ran on sampled heads
     assert rep["exact_F"] >= 0.9 * rep["heads"]
     eng.close()
+
+
+def test_memcpy_mode_matches_zerocopy_at_step_size(cache):
+    # At these shapes every CTA of the MEMCPY path's staged pivotal kernel takes about ten items
+    # (4,672 items over 456 CTAs), so its two-stage ring is refilled and its barrier phases flip;
+    # the two fetch modes must still give the same bits.  Layer 1, to index the second layer.
+    c = cache
+    eta = 1 / 8
+    res = []
+    for mode in (B.VERKV_FETCH_ZEROCOPY, B.VERKV_FETCH_MEMCPY):
+        eng = VerKV(BATCH, LAYERS, KVH, G, D, N, default_cap(N, eta), fetch_mode=mode)
+        eng.load_device(c["tau"], c["kv"], c["host_kv"])
+        eng.compress(eta, 4, 512, 0)
+        eng.sync()
+        eng.attend(1, c["queries"][1], 0.05, 0.05)
+        o, lse, _ = eng.fetch_refine()
+        eng.sync()
+        res.append((o.cpu().numpy(), lse.cpu().numpy()))
+        eng.close()
+    assert np.isfinite(res[0][0]).all()
+    assert np.array_equal(res[0][0], res[1][0]) and np.array_equal(res[0][1], res[1][1])
