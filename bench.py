@@ -885,6 +885,15 @@ def run_pc_sweep(args, local):
                       "rows": rows}), flush=True)
 
 
+def estimator_bytes(count, pivotal_r, d, G):
+    """Algorithmic bytes of one pass of the shrinkage estimator over the pivotal set: each
+    pivotal row's K and V (4d bytes), its id and r (8), and for a sampled row (r < 1) the sketch
+    logit of each of its G query heads (lambda).  count: rows per unit; pivotal_r: [units][cap].
+    Returns (bytes, sampled rows); the queries are negligible."""
+    n_l = int(sum(int((pivotal_r[u, :count[u]] < 1.0).sum()) for u in range(len(count))))
+    return int(np.sum(count)) * (4 * d + 8) + n_l * 4 * G, n_l
+
+
 def run_estimator(args, local):
     """One GPU: the shrinkage-estimator attention over the pivotal set (D-hat, N-hat and the
     second moment), timed alone.  In MEMCPY fetch mode the pivotal sums are their own launch,
@@ -939,11 +948,7 @@ def run_estimator(args, local):
         B.verkv_profile_enable(eng.ctx, 0)
         B.verkv_sync(eng.ctx)
     cnt = eng.p_count.cpu().numpy().astype(np.int64)
-    pr = eng.p_r.cpu().numpy()
-    n_l = int(sum(int((pr[u, :cnt[u]] < 1.0).sum()) for u in range(units)))
-    # algorithmic bytes: each pivotal row's K and V (4d), its id and r (8), and for a sampled
-    # row the sketch logit of each of the G query heads (lambda); the queries are negligible
-    nbytes = int(cnt.sum()) * (4 * d + 8) + n_l * 4 * G
+    nbytes, n_l = estimator_bytes(cnt, eng.p_r.cpu().numpy(), d, G)
     k = B.VERKV_K_PARTIAL_PIVOTAL
     us = 1e3 * total_ms[k] / max(launches[k], 1)
     gbs = nbytes / (us * 1e-6) / 1e9

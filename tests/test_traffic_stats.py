@@ -23,3 +23,12 @@ def test_traffic_stats_on_a_hand_made_case():
     assert s["shortlist_exhausted_frac"] == 0.0
     st[1, 0, 15] = 4
     assert bench.traffic_stats(st, fetched, counts, n)["shortlist_exhausted_frac"] == 1 / 8
+
+
+def test_estimator_bytes_on_a_hand_made_case():
+    # two units: 3 rows (one sampled) and 2 rows (both sampled); rows past the count are ignored
+    r = np.array([[1.0, 0.5, 1.0, 0.1], [0.2, 0.3, 0.9, 0.9]], dtype=np.float32)
+    count = np.array([3, 2])
+    nbytes, n_l = bench.estimator_bytes(count, r, d=128, G=4)
+    assert n_l == 3
+    assert nbytes == 5 * (4 * 128 + 8) + 3 * 4 * 4
