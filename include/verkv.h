@@ -26,6 +26,10 @@
  *  - Layouts.  A "unit" is one (sequence b, layer l, KV head h) of a verkv_shape; units are
  *    numbered u = (b * layers + l) * kv_heads + h.  Query head j of sequence b belongs to KV head
  *    j / q_per_kv (grouped-query attention).  bf16 is IEEE bfloat16 (uint16 bit patterns).
+ *  - Alignment.  bf16 rows and queries (q, the sketch, the pivotal kv, kv_full, host_kv) are
+ *    read in 16-byte vectors or bulk copies and must start on 16-byte boundaries; every other
+ *    array must be 4-byte aligned.  A misaligned pointer is VERKV_EINVAL, returned before any
+ *    launch.
  *  - One context per host thread; calls on one context must not overlap.
  */
 #ifndef VERKV_H
@@ -269,7 +273,8 @@ verkv_status verkv_selection_bitmap(verkv_ctx *ctx, uint32_t *out);
  * verkv_attend_verified (the certificate, beta, k* and F of every query head) without a context
  * and without allocating: the logits live in one array of VERKV_NOALLOC_MAX_LOGITS floats
  * (16 MiB) that the library keeps on every GPU that loads it, until the process exits.
- *   device     the GPU to run on; made current for the call
+ *   device     the GPU to run on; made current for the call, and the caller's current device
+ *              is restored before the call returns
  *   stream     cudaStream_t the kernels are issued on (NULL = legacy default stream)
  *   units      KV heads in this call (consecutive in every array below)   >= 1
  *   q_per_kv   query heads per KV head                                    1, 2, 4, 8
@@ -277,7 +282,8 @@ verkv_status verkv_selection_bitmap(verkv_ctx *ctx, uint32_t *out);
  *   n          tokens per unit                                            1 .. 131072
  *   q          device bf16 [units * q_per_kv][d], 16-byte aligned
  *   sketch     device bf16 [units][n][d] exact sketch, 16-byte aligned
- *   r_full     device float [units][n] from verkv_poissoncomp (r_i < 1 marks L)
+ *   r_full     device float [units][n] from verkv_poissoncomp (r_i < 1 marks L); r_full,
+ *              stats_out, F_out and err_out must be 4-byte aligned
  *   eps, delta the tolerance, as in verkv_attend_verified
  *   stats_out  device verkv_head_stats [units * q_per_kv]: the certificate fields (m, D, beta,
  *              V, b, eps_hat, eps_final, certified, k_star, n_L, iters, flags); D_hat, M2, lse
@@ -288,8 +294,8 @@ verkv_status verkv_selection_bitmap(verkv_ctx *ctx, uint32_t *out);
  *              if a beta solve hit its iteration cap, 16 if a bounded copy wait expired (the
  *              outputs of that call are then not valid)
  * Returns VERKV_ETOOLARGE, launching nothing, when units * q_per_kv * n exceeds
- * VERKV_NOALLOC_MAX_LOGITS; VERKV_EINVAL for another bad argument; VERKV_ECUDA if a CUDA call
- * fails.  The first call on a device also looks up the device address of the array (set-up that
+ * VERKV_NOALLOC_MAX_LOGITS; VERKV_EINVAL for another bad argument (a misaligned pointer
+ * included), checked before any CUDA call; VERKV_ECUDA if a CUDA call fails.  The first call on a device also looks up the device address of the array (set-up that
  * runs once per device); make that first call before any stream capture.  All calls on a GPU
  * share the array, which keeps the last call's logits: nothing in it has to start at zero, as
  * every call writes each logit before reading it, but calls that overlap on the GPU (other

@@ -264,7 +264,8 @@ def attend_unit(q_heads, sketch_keys, keys, values, r32, resident, eps, delta, s
     keys/values [n][d] (the full cache), all fp64.  Each query head certifies and fetches on its
     own; the rows that move for the KV head are the union over its query heads of F \\ S, in
     ascending token id (our reading of GQA: certificates per query head, transfers per KV head).
-    Returns dict(heads=[per-head dicts], fetch_ids=int64[]).
+    Returns dict(heads=[per-head dicts: cert, est, s], fetch_ids=int64[], cand, values, r32,
+    resident).
     """
     heads = []
     union = np.zeros(keys.shape[0], dtype=bool)
@@ -279,5 +280,8 @@ def attend_unit(q_heads, sketch_keys, keys, values, r32, resident, eps, delta, s
         s = s_hat if sketch_keys is keys else logits(q, keys)
         est = refine(s, values, r32, resident, cert["F"], cert["lam"], cert["m"])
         union |= cert["F"] & ~np.asarray(resident, dtype=bool)
-        heads.append(dict(cert=cert, est=est))
-    return dict(heads=heads, fetch_ids=np.nonzero(union)[0].astype(np.int64), cand=cand)
+        heads.append(dict(cert=cert, est=est, s=s))
+    # The exact logits s of each head and the unit's values, r and resident set stay with the
+    # result so that refine() can be re-run for another fetch set F.
+    return dict(heads=heads, fetch_ids=np.nonzero(union)[0].astype(np.int64), cand=cand,
+                values=values, r32=r32, resident=resident)

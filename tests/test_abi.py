@@ -79,6 +79,12 @@ def test_noalloc_argument_checks_need_no_gpu(lib):
         bad = list(args)
         bad[i] = v
         assert c(*bad) == B.VERKV_EINVAL, (i, v)
+    # Misaligned pointers: q and the sketch need 16 bytes (vector loads, bulk copies), the other
+    # arrays 4; each is refused before any launch.
+    for i, v in [(6, 24), (6, 18), (7, 40), (7, 17), (8, 18), (11, 21), (12, 22), (13, 19)]:
+        bad = list(args)
+        bad[i] = v
+        assert c(*bad) == B.VERKV_EINVAL, (i, v)
 
 
 def test_kernel_ids_and_names_match_the_header(lib):

@@ -59,3 +59,48 @@ def test_call_order_and_arguments():
     assert st == B.VERKV_EINVAL
     eng.fetch_refine()
     eng.sync()
+
+
+def test_misaligned_pointers_are_rejected_before_launch():
+    # Every call checks the alignment its kernels rely on (16 bytes for bf16 rows and queries,
+    # 4 for the other arrays) and returns VERKV_EINVAL before launching anything: the offset
+    # pointers below are never dereferenced.
+    w = I.tiny()
+    eng = P.make_engine(w)
+    eng.compress(w.eta, w.n_sink, w.n_local, w.seed)
+    eng.sync()
+    lib = B.lib()
+    q = torch.as_tensor(w.queries[0].view(np.int16)).to(eng.dev)
+    launches = B.verkv_launch_counts(eng.ctx)
+
+    def attend(qp=q.data_ptr(), sketch=eng.sketch.data_ptr(), r=eng.r_full.data_ptr(), ids=None):
+        sk = B.verkv_sketch(B.VERKV_SKETCH_EXACT, sketch)
+        return lib.verkv_attend_verified(eng.ctx, 0, qp, eng.pivotal, r, sk, w.eps, w.delta,
+                                         ids, None)
+
+    assert attend(qp=q.data_ptr() + 8) == B.VERKV_EINVAL
+    assert attend(sketch=eng.sketch.data_ptr() + 2) == B.VERKV_EINVAL
+    assert attend(r=eng.r_full.data_ptr() + 2) == B.VERKV_EINVAL
+    assert attend(ids=eng.fetch_ids.data_ptr() + 1) == B.VERKV_EINVAL
+    pv = B.verkv_pivotal(eng.p_ids.data_ptr(), eng.p_r.data_ptr(), eng.p_kv.data_ptr() + 4,
+                         eng.p_count.data_ptr(), eng.p_res.data_ptr(), eng.p_c.data_ptr())
+    sk = B.verkv_sketch(B.VERKV_SKETCH_EXACT, eng.sketch.data_ptr())
+    assert lib.verkv_attend_verified(eng.ctx, 0, q.data_ptr(), pv, eng.r_full.data_ptr(), sk,
+                                     w.eps, w.delta, None, None) == B.VERKV_EINVAL
+    assert lib.verkv_sketch_build(eng.ctx, eng.kv.data_ptr() + 2, B.VERKV_SKETCH_EXACT,
+                                  eng.sketch.data_ptr()) == B.VERKV_EINVAL
+    assert lib.verkv_poissoncomp(eng.ctx, eng.tau.data_ptr(), w.eta, B.verkv_hset(4, 64), 0,
+                                 eng.kv.data_ptr() + 8, eng.r_full.data_ptr(),
+                                 eng.pivotal) == B.VERKV_EINVAL
+    o = torch.empty_like(eng.o)
+    assert lib.verkv_attend_dense_host(eng.ctx, 0, q.data_ptr(), eng.host_kv.data_ptr() + 2,
+                                       o.data_ptr(), None) == B.VERKV_EINVAL
+    assert B.verkv_launch_counts(eng.ctx) == launches  # nothing was launched
+    eng.attend(0, q, w.eps, w.delta)
+    assert lib.verkv_fetch_refine(eng.ctx, eng._ids, eng._cnt, eng.host_kv.data_ptr() + 4,
+                                  o.data_ptr(), None, None) == B.VERKV_EINVAL
+    assert lib.verkv_fetch_refine(eng.ctx, eng._ids, eng._cnt, eng.host_kv.data_ptr(),
+                                  o.data_ptr() + 2, None, None) == B.VERKV_EINVAL
+    eng.fetch_refine()
+    eng.sync()
+    eng.close()

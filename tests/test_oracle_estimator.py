@@ -115,6 +115,32 @@ def test_estimator_exact_mean_and_variance_by_enumeration():
     np.testing.assert_allclose(meanN, (lam[:, None] * w[:, None] * values).sum(0), rtol=1e-10)
 
 
+def test_lemma1_b_is_the_largest_summand_deviation():
+    # Lemma 1 / Eq. (7) applies Bernstein's inequality to D-hat = sum_H w + sum_L X_i with
+    # independent summands X_i = Z_i lambda_i w_i / r_i; b(L) must be the bound on every summand's
+    # deviation from its mean, max_i max_{Z_i in {0, 1}} |X_i - E X_i|.  Each X_i is read off the
+    # oracle's own estimator by enumerating Z_i for one token at a time (the others unsampled), so
+    # b is pinned to what D-hat computes, not to a second copy of its formula.  The draws put r on
+    # both sides of 1/2, where the larger deviation switches between Z_i = 0 and Z_i = 1.
+    rng = np.random.default_rng(11)
+    for trial in range(12):
+        n, d = int(rng.integers(6, 40)), 2
+        s, r, res_h = _small_problem(rng, n=n, n_h=3, spread=rng.uniform(0.3, 4.0))
+        values = rng.standard_normal((n, d))
+        c = O.certify(s, r, res_h, 0.05, 0.05)
+        none = np.zeros(n, dtype=np.uint8)
+        base = O.refine(s, values, r, res_h, none, c["lam"], c["m"])["D_hat"]
+        b = 0.0
+        for i in np.nonzero(r < 1)[0]:
+            res = res_h.copy()
+            res[i] = 1
+            x1 = O.refine(s, values, r, res, none, c["lam"], c["m"])["D_hat"] - base  # Z_i = 1
+            mean = float(r[i]) * x1                                                  # E X_i
+            b = max(b, abs(x1 - mean), abs(0.0 - mean))
+        assert (r[r < 1] > 0.5).any() and (r[r < 1] < 0.5).any()
+        assert c["b"] == pytest.approx(b, rel=1e-10, abs=1e-300)
+
+
 def _eps_hat_mp(idx, w, r, lam, l, D):
     """eps_hat of the subset idx of L from Eq. (7) with lambda held fixed, in 50-digit arithmetic."""
     w = [float(x) for x in w]

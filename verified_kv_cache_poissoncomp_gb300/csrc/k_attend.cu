@@ -481,14 +481,8 @@ cudaError_t launch_partial(const PartialArgs &a, int units_layer, int grid, cuda
 #define VERKV_PSTAGED(DD, GG)                                                                   \
         if (a.d == DD && G == GG) {                                                             \
             const size_t smem = (size_t)PV_STAGES * pv_stage_bytes<DD>();                       \
-            static bool attr = false;                                                           \
-            if (!attr) {                                                                        \
-                cudaError_t e = cudaFuncSetAttribute(k_partial_staged<DD, GG>,                  \
-                                                     cudaFuncAttributeMaxDynamicSharedMemorySize, \
-                                                     (int)smem);                                \
-                if (e != cudaSuccess) return e;                                                 \
-                attr = true;                                                                    \
-            }                                                                                   \
+            const cudaError_t e = ensure_smem((const void *)k_partial_staged<DD, GG>, smem);   \
+            if (e != cudaSuccess) return e;                                                     \
             return launch_pdl(k_partial_staged<DD, GG>, dim3(g), dim3(128), smem, s, a, units_layer); \
         }
         VERKV_PSTAGED(128, 1) VERKV_PSTAGED(128, 2) VERKV_PSTAGED(128, 4) VERKV_PSTAGED(128, 8)

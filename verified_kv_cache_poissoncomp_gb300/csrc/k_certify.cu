@@ -475,6 +475,7 @@ __device__ __forceinline__ void fetch_list_tail(const CertifyArgs &a, int ul, in
 template <int CL, bool SL>
 __global__ void __launch_bounds__(CT_NT, 1) k_certify(CertifyArgs a) {
     pdl_trigger();  // pdl_wait() follows the loads of r, which no early-starting kernel writes
+    cluster_arrive_relaxed();  // waited on before the first exchange with the peers
     extern __shared__ __align__(16) unsigned char smem_raw[];
     float *wrec = reinterpret_cast<float *>(smem_raw);
     float *xrec = wrec + CT_NW * CT_REC;
@@ -537,6 +538,7 @@ __global__ void __launch_bounds__(CT_NT, 1) k_certify(CertifyArgs a) {
         const float sc_t = tmax == NEG_INF ? 0.0f : expf(tmax - wmax);
         // (max logit, D, C) combine as online-softmax partials; |L| adds.
         float rec[4] = {wmax, warp_sum(d * sc_t), warp_sum(c * sc_t), warp_sum(cnt)};
+        cluster_wait_all();  // every CTA of the cluster is running: its shared memory may be written
         cluster_allreduce<CL>(rec, wrec, xrec, parity, [&](float (&x)[4], const float (&y)[4]) {
             const float M = fmaxf(x[0], y[0]);
             const float fx = x[0] == NEG_INF ? 0.0f : expf(x[0] - M);
@@ -1024,13 +1026,8 @@ __global__ void __launch_bounds__(CT_NT, 1) k_certify(CertifyArgs a) {
 
 template <int CL, bool SL>
 static cudaError_t launch_certify_cl(const CertifyArgs &a, int qheads, size_t smem, cudaStream_t s) {
-    static size_t configured = 0;
-    if (smem > configured) {
-        cudaError_t e = cudaFuncSetAttribute(k_certify<CL, SL>,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        if (e != cudaSuccess) return e;
-        configured = smem;
-    }
+    const cudaError_t e = ensure_smem((const void *)k_certify<CL, SL>, smem);
+    if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(qheads * a.cl);
     cfg.blockDim = dim3(CT_NT);
@@ -1207,14 +1204,8 @@ cudaError_t launch_shortlist(const ShortlistArgs &a, int units_layer, cudaStream
     // The keys of up to 40960 tokens stay in shared memory between the passes.
     const size_t smem = (size_t)a.n * 4;
     if (smem <= 160 * 1024) {
-        static bool attr = false;
-        if (!attr) {
-            cudaError_t e = cudaFuncSetAttribute(k_shortlist<true>,
-                                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                 160 * 1024);
-            if (e != cudaSuccess) return e;
-            attr = true;
-        }
+        const cudaError_t e = ensure_smem((const void *)k_shortlist<true>, 160 * 1024);
+        if (e != cudaSuccess) return e;
         return launch_pdl(k_shortlist<true>, dim3(units_layer), dim3(SL_NT), smem, s, a);
     }
     return launch_pdl(k_shortlist<false>, dim3(units_layer), dim3(SL_NT), 0, s, a);

@@ -91,6 +91,7 @@ __global__ void __launch_bounds__(PC_NT, 1) k_pc_solve(PcArgs a) {
 
     ClusterReducer<PC_NW, 2> red{sm.fslots, a.cl, 0};
     ClusterReducer64<PC_NW> red64{sm.dslots, a.cl, 0};
+    cluster_arrive_relaxed();  // waited on before the first exchange with the peers
 
     // 1. Load tau of the non-forced tokens; validate it.  Each thread keeps PC_LD four-token
     //    loads in flight (16-byte vectors when the tau rows are 16-byte aligned).
@@ -140,6 +141,7 @@ __global__ void __launch_bounds__(PC_NT, 1) k_pc_solve(PcArgs a) {
         }
     }
     if (bad) raise_error(a.err, ERR_TAU);
+    cluster_wait_all();  // every CTA of the cluster is running: its shared memory may be written
     {
         unsigned long long z = 0ull;
         red64.run_u64(tfix, z);
@@ -391,8 +393,7 @@ __global__ void __launch_bounds__(PC_NT, 1) k_pc_solve(PcArgs a) {
 
 cudaError_t launch_pc_solve(const PcArgs &a, int units, cudaStream_t s) {
     const size_t smem = pc_smem_bytes(a.chunk);
-    cudaError_t e = cudaFuncSetAttribute(k_pc_solve, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)smem);
+    cudaError_t e = ensure_smem((const void *)k_pc_solve, smem);
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(units * a.cl);

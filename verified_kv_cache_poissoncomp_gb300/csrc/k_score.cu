@@ -82,9 +82,11 @@ __device__ __forceinline__ unsigned long long bf16x2_to_f32x2(uint32_t w) {
 // per head.
 template <int D, int G>
 __global__ void __launch_bounds__(SC_NT, SC_CTAS_PER_SM) k_score(ScoreArgs a, int spans_per_unit, int span_rows) {
-    // The query and the sketch are never written by a kernel that lets this one start early (the
-    // decode path's kernels write only the workspace and the outputs), so the first stages are
-    // requested before waiting for the previous kernel; the logits are written after it.
+    // The first kernel of a library call is launched without programmatic serialisation: when
+    // it starts, every earlier kernel on the stream (the caller's q projection, a sketch build)
+    // has finished, so q and the first sketch stages are read at once and pdl_wait() returns
+    // immediately.  A launch with the attribute would be safe only after kernels that write
+    // neither q nor the sketch.  The trigger lets the certificate kernel be scheduled early.
     pdl_trigger();
     constexpr int CPL = G <= 4 ? 16 : 8, NV = CPL / 8;
     constexpr int LPR = D / CPL, RPW = 32 / LPR, NW = SC_NT / 32;
@@ -192,7 +194,7 @@ __global__ void __launch_bounds__(SC_NT, SC_CTAS_PER_SM) k_score(ScoreArgs a, in
     }
 }
 
-cudaError_t launch_score(const ScoreArgs &a, int units_layer, cudaStream_t s) {
+cudaError_t launch_score(const ScoreArgs &a, int units_layer, cudaStream_t s, bool pdl) {
     int sms = 0, dev = 0;
     cudaGetDevice(&dev);
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
@@ -206,15 +208,10 @@ cudaError_t launch_score(const ScoreArgs &a, int units_layer, cudaStream_t s) {
     const int G = a.li.G;
 #define VERKV_SCORE(DD, GG)                                                                     \
     if (a.d == DD && G == GG) {                                                                 \
-        static bool attr = false;                                                               \
-        if (!attr) {                                                                            \
-            cudaError_t e = cudaFuncSetAttribute(k_score<DD, GG>,                               \
-                                                 cudaFuncAttributeMaxDynamicSharedMemorySize,   \
-                                                 (int)smem);                                    \
-            if (e != cudaSuccess) return e;                                                     \
-            attr = true;                                                                        \
-        }                                                                                       \
-        return launch_pdl(k_score<DD, GG>, grid, dim3(SC_NT), smem, s, a, spans, (int)span_rows); \
+        const cudaError_t e = ensure_smem((const void *)k_score<DD, GG>, smem);                \
+        if (e != cudaSuccess) return e;                                                         \
+        return launch_opt_pdl(pdl, k_score<DD, GG>, grid, dim3(SC_NT), smem, s, a, spans,       \
+                              (int)span_rows);                                                  \
     }
     VERKV_SCORE(128, 1) VERKV_SCORE(128, 2) VERKV_SCORE(128, 4) VERKV_SCORE(128, 8)
     VERKV_SCORE(64, 1) VERKV_SCORE(64, 2) VERKV_SCORE(64, 4) VERKV_SCORE(64, 8)
@@ -238,7 +235,7 @@ __device__ __forceinline__ unsigned long long fadd2(unsigned long long a, unsign
 template <int D, int G>
 __global__ void __launch_bounds__(SC_NT, SC_CTAS_PER_SM) k_score_q2(ScoreArgs a, int spans_per_unit,
                                                                    int span_rows) {
-    pdl_trigger();  // as in k_score: the first stages are requested before pdl_wait()
+    pdl_trigger();  // launched as k_score is: q and the first stages are read at once
     constexpr int CPL = G <= 4 ? 16 : 8;
     constexpr int LPR = D / CPL, RPW = 32 / LPR, NW = SC_NT / 32;
     constexpr int ROWB = (D / 4 + 4 * (D / 32) + 15) / 16 * 16;  // bytes per sketch row
@@ -356,7 +353,7 @@ __global__ void __launch_bounds__(SC_NT, SC_CTAS_PER_SM) k_score_q2(ScoreArgs a,
     }
 }
 
-cudaError_t launch_score_q2(const ScoreArgs &a, int units_layer, cudaStream_t s) {
+cudaError_t launch_score_q2(const ScoreArgs &a, int units_layer, cudaStream_t s, bool pdl) {
     int sms = 0, dev = 0;
     cudaGetDevice(&dev);
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
@@ -371,15 +368,10 @@ cudaError_t launch_score_q2(const ScoreArgs &a, int units_layer, cudaStream_t s)
     if (a.d == DD && G == GG) {                                                                 \
         constexpr int ROWB = (DD / 4 + 4 * (DD / 32) + 15) / 16 * 16;                           \
         const size_t smem = (size_t)SC_STAGES * SQ_ROWS * ROWB;                                 \
-        static bool attr = false;                                                               \
-        if (!attr) {                                                                            \
-            cudaError_t e = cudaFuncSetAttribute(k_score_q2<DD, GG>,                            \
-                                                 cudaFuncAttributeMaxDynamicSharedMemorySize,   \
-                                                 (int)smem);                                    \
-            if (e != cudaSuccess) return e;                                                     \
-            attr = true;                                                                        \
-        }                                                                                       \
-        return launch_pdl(k_score_q2<DD, GG>, grid, dim3(SC_NT), smem, s, a, spans, (int)span_rows); \
+        const cudaError_t e = ensure_smem((const void *)k_score_q2<DD, GG>, smem);             \
+        if (e != cudaSuccess) return e;                                                         \
+        return launch_opt_pdl(pdl, k_score_q2<DD, GG>, grid, dim3(SC_NT), smem, s, a, spans,    \
+                              (int)span_rows);                                                  \
     }
     VERKV_SCORE_Q2(128, 1) VERKV_SCORE_Q2(128, 2) VERKV_SCORE_Q2(128, 4) VERKV_SCORE_Q2(128, 8)
     VERKV_SCORE_Q2(64, 1) VERKV_SCORE_Q2(64, 2) VERKV_SCORE_Q2(64, 4) VERKV_SCORE_Q2(64, 8)

@@ -23,6 +23,12 @@ namespace {
 
 size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 
+// Alignment the kernels rely on: bf16 rows and queries are read in 16-byte vectors or bulk
+// copies; every other array is read and written in 4-byte words.  A null pointer passes (the
+// null checks are separate).
+bool bad16(const void *p) { return ((uintptr_t)p & 15u) != 0; }
+bool bad4(const void *p) { return ((uintptr_t)p & 3u) != 0; }
+
 struct Layout {
     size_t err, flc, nacc, rmask, scores, qstats, F, slb, fids, fcounts, staging, part_piv, part_fet, total;
     int W, units_layer, qh_layer, max_piv, max_fet, dense_chunks;
@@ -124,6 +130,35 @@ class Pool {
 };
 
 }  // namespace
+
+namespace verkv {
+
+cudaError_t ensure_smem(const void *func, size_t bytes) {
+    struct Entry {
+        int device;
+        const void *func;
+        size_t bytes;
+    };
+    static std::mutex mu;
+    static std::vector<Entry> done;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    std::lock_guard<std::mutex> g(mu);
+    for (Entry &x : done) {
+        if (x.device == dev && x.func == func) {
+            if (x.bytes >= bytes) return cudaSuccess;
+            e = cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+            if (e == cudaSuccess) x.bytes = bytes;
+            return e;
+        }
+    }
+    e = cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+    if (e == cudaSuccess) done.push_back({dev, func, bytes});
+    return e;
+}
+
+}  // namespace verkv
 
 struct verkv_ctx {
     int device = 0;
@@ -395,6 +430,9 @@ verkv_status verkv_poissoncomp(verkv_ctx *ctx, const float *tau, double eta, ver
     const double b_rest = eta_n - (double)forced;
     if (n_rest > 0 && !(b_rest > 0.0))
         return fail(ctx, VERKV_EBUDGET, "poissoncomp: eta * n must exceed the forced H set");
+    if (bad16(kv_full) || bad16(out->kv) || bad4(tau) || bad4(r_full) || bad4(out->ids) ||
+        bad4(out->r) || bad4(out->count) || bad4(out->resident) || bad4(out->c))
+        return fail(ctx, VERKV_EINVAL, "poissoncomp: kv rows need 16-byte, other arrays 4-byte alignment");
     VERKV_CUDA(cudaSetDevice(ctx->device), "cudaSetDevice");
     const int units = ctx->sh.batch * ctx->sh.layers * ctx->sh.kv_heads;
     PcArgs a{};
@@ -439,6 +477,8 @@ verkv_status verkv_sketch_build(verkv_ctx *ctx, const void *kv_full, int32_t for
     if (!kv_full || !sketch_out) return fail(ctx, VERKV_EINVAL, "sketch_build: null pointer");
     if (format != VERKV_SKETCH_EXACT && format != VERKV_SKETCH_Q2)
         return fail(ctx, VERKV_EINVAL, "sketch_build: unknown format");
+    if (bad16(kv_full) || bad16(sketch_out))
+        return fail(ctx, VERKV_EINVAL, "sketch_build: kv_full and the sketch need 16-byte alignment");
     VERKV_CUDA(cudaSetDevice(ctx->device), "cudaSetDevice");
     const int64_t rows = (int64_t)ctx->sh.batch * ctx->sh.layers * ctx->sh.kv_heads * ctx->sh.n;
     if (format == VERKV_SKETCH_Q2) {
@@ -468,6 +508,11 @@ verkv_status verkv_attend_verified(verkv_ctx *ctx, int32_t layer, const void *q,
         return fail(ctx, VERKV_EINVAL, "attend: unknown sketch format");
     if (!(eps > 0.0f) || !(delta > 0.0f) || !(delta < 1.0f) || !isfinite(eps))
         return fail(ctx, VERKV_EINVAL, "attend: need eps > 0 and 0 < delta < 1");
+    if (bad16(q) || bad16(sketch->data) || bad16(pivotal->kv))
+        return fail(ctx, VERKV_EINVAL, "attend: q, the sketch and the pivotal rows need 16-byte alignment");
+    if (bad4(r_full) || bad4(pivotal->ids) || bad4(pivotal->r) || bad4(pivotal->count) ||
+        bad4(pivotal->resident) || bad4(fetch_ids_out) || bad4(fetch_counts_out))
+        return fail(ctx, VERKV_EINVAL, "attend: int32 / float arrays need 4-byte alignment");
     VERKV_CUDA(cudaSetDevice(ctx->device), "cudaSetDevice");
     const LayerIdx li = layer_idx(ctx, layer);
     const int n = ctx->sh.n, d = ctx->sh.head_dim;
@@ -482,9 +527,9 @@ verkv_status verkv_attend_verified(verkv_ctx *ctx, int32_t layer, const void *q,
     sa.scale = (float)(1.0 / sqrt((double)d));
     sa.li = li;
     if (sketch->format == VERKV_SKETCH_Q2) {
-        VERKV_CUDA(tracked(ctx, VERKV_K_SCORE, ctx->main, [&] { return launch_score_q2(sa, ctx->L.units_layer, ctx->main); }), "k_score_q2");
+        VERKV_CUDA(tracked(ctx, VERKV_K_SCORE, ctx->main, [&] { return launch_score_q2(sa, ctx->L.units_layer, ctx->main, false); }), "k_score_q2");
     } else {
-        VERKV_CUDA(tracked(ctx, VERKV_K_SCORE, ctx->main, [&] { return launch_score(sa, ctx->L.units_layer, ctx->main); }), "k_score");
+        VERKV_CUDA(tracked(ctx, VERKV_K_SCORE, ctx->main, [&] { return launch_score(sa, ctx->L.units_layer, ctx->main, false); }), "k_score");
     }
 
     if (ctx->shortlist > 0) {
@@ -563,6 +608,8 @@ verkv_status verkv_fetch_refine(verkv_ctx *ctx, const int32_t *ids, const int32_
     if ((ids && ids != ctx->user_ids) || (counts && counts != ctx->user_counts))
         return fail(ctx, VERKV_EINVAL, "fetch_refine: ids/counts must be the attend outputs or NULL");
     if (!host_kv || !o_out) return fail(ctx, VERKV_EINVAL, "fetch_refine: null pointer");
+    if (bad16(host_kv) || bad4(o_out) || bad4(lse_out) || bad4(stats_out))
+        return fail(ctx, VERKV_EINVAL, "fetch_refine: host_kv needs 16-byte, outputs 4-byte alignment");
     VERKV_CUDA(cudaSetDevice(ctx->device), "cudaSetDevice");
     const LayerIdx li = layer_idx(ctx, ctx->layer);
     const int n = ctx->sh.n, d = ctx->sh.head_dim;
@@ -715,6 +762,8 @@ verkv_status verkv_attend_dense_host(verkv_ctx *ctx, int32_t layer, const void *
     if (!ctx) return VERKV_EINVAL;
     if (layer < 0 || layer >= ctx->sh.layers) return fail(ctx, VERKV_EINVAL, "dense: bad layer");
     if (!q || !host_kv || !o_out) return fail(ctx, VERKV_EINVAL, "dense: null pointer");
+    if (bad16(q) || bad16(host_kv) || bad4(o_out) || bad4(lse_out))
+        return fail(ctx, VERKV_EINVAL, "dense: q and host_kv need 16-byte, outputs 4-byte alignment");
     VERKV_CUDA(cudaSetDevice(ctx->device), "cudaSetDevice");
     cudaPointerAttributes attr;
     cudaError_t e = cudaPointerGetAttributes(&attr, host_kv);

@@ -21,6 +21,19 @@ __device__ __forceinline__ void raise_error(uint32_t *err, uint32_t bit) { atomi
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 
+// Cluster start-up.  A CTA may touch a peer's shared memory only once the peer is known to be
+// running: the CTAs of a cluster are co-scheduled, but nothing orders their start, and a
+// distributed-shared-memory access to a CTA that has not begun (or has already exited) is a
+// launch failure.  Every thread calls cluster_arrive_relaxed() first thing and
+// cluster_wait_all() before its first access to another CTA's shared memory; the barrier's
+// latency hides behind whatever the kernel loads in between.
+__device__ __forceinline__ void cluster_arrive_relaxed() {
+    asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait_all() {
+    asm volatile("barrier.cluster.wait.aligned;" ::: "memory");
+}
+
 // ---------------------------------------------------------------------------------------------
 // bf16 pairs packed in a 32-bit word: element 0 in the low half.
 __device__ __forceinline__ float bf16lo(uint32_t x) { return __uint_as_float(x << 16); }

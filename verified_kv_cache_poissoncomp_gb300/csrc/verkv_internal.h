@@ -51,12 +51,18 @@ int q2_row_bytes(int d);
 cudaError_t launch_sketch_q2(const uint16_t *kv_full, uint8_t *sketch, int64_t rows, int d,
                              cudaStream_t s);
 
+// Raise `func`'s dynamic shared-memory limit to at least `bytes` on the current device.  The
+// attribute is per device, so the limit set is remembered per (device, kernel) under a lock;
+// host threads and devices may call it concurrently.
+cudaError_t ensure_smem(const void *func, size_t bytes);
+
 // Launch `kernel` on stream s with programmatic stream serialisation: it may start before the
 // previous kernel on s has finished, and must call pdl_wait() before reading what the stream
 // produced (the decode path's kernels do so first thing).
+// With pdl false the launch is an ordinary stream-ordered one (pdl_wait() then returns at once).
 template <typename... KArgs, typename... Args>
-cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
-                       Args &&...args) {
+cudaError_t launch_opt_pdl(bool pdl, void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                           cudaStream_t s, Args &&...args) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = grid;
     cfg.blockDim = block;
@@ -66,8 +72,13 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t s
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = pdl ? 1 : 0;
     return cudaLaunchKernelEx(&cfg, kernel, static_cast<Args &&>(args)...);
+}
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                       Args &&...args) {
+    return launch_opt_pdl(true, kernel, grid, block, smem, s, static_cast<Args &&>(args)...);
 }
 
 // ---------------------------------------------------------------------------------------------
@@ -91,9 +102,12 @@ struct ScoreArgs {
     float scale;
     LayerIdx li;
 };
-cudaError_t launch_score(const ScoreArgs &a, int units_layer, cudaStream_t s);
+// `pdl`: launch with programmatic stream serialisation.  The first kernel of a library call must
+// not: it reads the caller's q and sketch, which the caller's preceding kernel may still be
+// writing when it lets dependents start early.
+cudaError_t launch_score(const ScoreArgs &a, int units_layer, cudaStream_t s, bool pdl);
 // The same from the 2-bit sketch (a.sketch points at its rows).
-cudaError_t launch_score_q2(const ScoreArgs &a, int units_layer, cudaStream_t s);
+cudaError_t launch_score_q2(const ScoreArgs &a, int units_layer, cudaStream_t s, bool pdl);
 
 // Certificate and selection per query head (one cluster per query head).  When fl_counter is
 // set, the last of the G clusters of a KV head to finish also builds that head's fetch list:

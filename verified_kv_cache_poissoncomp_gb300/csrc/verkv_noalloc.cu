@@ -39,6 +39,20 @@ cudaError_t logits_address(int device, float **out) {
     return cudaSuccess;
 }
 
+// Puts the caller's current device back when the call returns, on every path.
+class DeviceRestore {
+  public:
+    DeviceRestore() { ok_ = cudaGetDevice(&saved_) == cudaSuccess; }
+    ~DeviceRestore() {
+        if (ok_) cudaSetDevice(saved_);
+    }
+    bool ok() const { return ok_; }
+
+  private:
+    int saved_ = 0;
+    bool ok_ = false;
+};
+
 }  // namespace
 
 extern "C" verkv_status verkv_certify_noalloc(int device, void *stream, int32_t units,
@@ -52,11 +66,18 @@ extern "C" verkv_status verkv_certify_noalloc(int device, void *stream, int32_t 
         !(head_dim == 64 || head_dim == 128) || n < 1 || n > 131072)
         return VERKV_EINVAL;
     if (!q || !sketch || !r_full || !stats_out || !F_out || !err_out) return VERKV_EINVAL;
+    // q is read in 16-byte vectors and the sketch by bulk copies: both need 16-byte alignment;
+    // the rest are read and written as 4-byte words.
+    if ((((uintptr_t)q | (uintptr_t)sketch) & 15u) ||
+        (((uintptr_t)r_full | (uintptr_t)stats_out | (uintptr_t)F_out | (uintptr_t)err_out) & 3u))
+        return VERKV_EINVAL;
     if (!(eps > 0.0f) || !isfinite(eps) || !(delta > 0.0f) || !(delta < 1.0f)) return VERKV_EINVAL;
     if ((int64_t)units * G * n > (int64_t)VERKV_NOALLOC_MAX_LOGITS) return VERKV_ETOOLARGE;
     int ndev = 0;
     if (cudaGetDeviceCount(&ndev) != cudaSuccess) return VERKV_ECUDA;
     if (device < 0 || device >= ndev || device >= kMaxDevices) return VERKV_EINVAL;
+    DeviceRestore restore;
+    if (!restore.ok()) return VERKV_ECUDA;
     if (cudaSetDevice(device) != cudaSuccess) return VERKV_ECUDA;
     float *logits = nullptr;
     if (logits_address(device, &logits) != cudaSuccess) return VERKV_ECUDA;
@@ -80,7 +101,7 @@ extern "C" verkv_status verkv_certify_noalloc(int device, void *stream, int32_t 
     sa.d = head_dim;
     sa.scale = (float)(1.0 / sqrt((double)head_dim));
     sa.li = li;
-    if (launch_score(sa, units, s) != cudaSuccess) return VERKV_ECUDA;
+    if (launch_score(sa, units, s, false) != cudaSuccess) return VERKV_ECUDA;
 
     CertifyArgs ca{};
     ca.scores = logits;
