@@ -9,7 +9,10 @@ exact in fp32, twelve roundings per dot product -- and g inherits about twice th
   * k*: must lie in the oracle's acceptable set {k : eps_o(k) < eps (1 + EPS_TIE) and
     (k = 0 or eps_o(k-1) >= eps (1 - EPS_TIE))} along the oracle's order.
   * F: equal to the oracle's top-k* set, except for swaps among tokens whose oracle g lies within
-    G_TIE relative of g at the cut (float32 logits carry up to ~1e-5 relative error into w-hat).
+    G_TIE = 1e-5 relative of g at the cut, the same window as the decision's.  (float32 logits
+    carry up to ~1.5e-5 relative error into w-hat in the worst case, but over the whole GPU suite
+    -- 1440 query heads at 1K to 128K tokens -- no swap occurred at all: the run reports
+    tie_F = 0 and max_g_gap = 0 in its parity summary line.)
   * D-hat, N-hat, o: error <= 1e-3 (bf16 storage, fp32 accumulation) -- |lse - lse_o| for D-hat,
     and max_c |x_c - x_o,c| / max_c |x_o,c| element by element for N-hat and o -- on every head:
     against the oracle's estimator when the GPU's F equals the oracle's, else against the oracle's
@@ -24,7 +27,7 @@ from verified_kv_cache_poissoncomp_gb300 import binding as B
 from verified_kv_cache_poissoncomp_gb300.engine import VerKV, default_cap, stats_to_dict
 
 EPS_TIE = 1e-5
-G_TIE = 1e-4
+G_TIE = 1e-5
 EST_TOL = 1e-3
 
 
