@@ -56,8 +56,13 @@ def parse_args():
     p.add_argument("--sketch", choices=["exact", "q2"], default="exact",
                    help="token sketch: exact bf16 keys (the headline) or the 2-bit sketch")
     p.add_argument("--long128k", action="store_true",
-                   help="the fetch-stressed long-context workload: 128K tokens, batch 4, "
-                        "eta = 1/32, needle sets, eps in {0.02, 0.05}")
+                   help="the fetch-stressed long-context workload: 128K tokens, --layers layers x "
+                        "batch 4 x 8 KV heads, eta = 1/32, needle sets, eps in {0.02, 0.05}")
+    p.add_argument("--decode-step", action="store_true",
+                   help="the full decode step: --layers layers x batch 8 x 8 KV heads x 4 query "
+                        "heads at 32K, eta in {1/8, 1/32}, eps = delta = 0.05")
+    p.add_argument("--layers", type=int, default=36,
+                   help="layers of the --decode-step and --long128k models")
     p.add_argument("--pc-sweep", action="store_true",
                    help="PoissonComp throughput: 36 layers x 8 KV heads, n in {32K, 128K}, "
                         "eta in {1/8, 1/16, 1/32}")
@@ -703,11 +708,20 @@ def run_eps_sweep(args, local):
     eng.close()
 
 
-def run_long128k(args, local):
-    """One GPU: the long-context workload with the fetch path stressed (128K tokens, batch 4,
-    8 KV heads x 4 query heads, eta = 1/32, a needle set of 2-25 % of the context per KV head),
-    8 decode queries per step (a query = 128 query heads), for eps in {0.02, 0.05}: throughput,
-    rows fetched, host-link rate and per-kernel times.  One JSON line."""
+def run_model_steps(args, local, kind):
+    """One GPU, a whole decode step of a 36-layer model: every layer's attend_verified +
+    fetch_refine for a batch of sequences, the full cache page-locked on the host and the
+    pivotal set plus the exact sketch on the device.
+
+    kind "decode-step": n = 32768, batch 8, 8 KV heads x 4 query heads, d = 128, eta in
+        {1/8, 1/32}, eps = delta = 0.05; tau, sinks and queries as in the single-layer workload,
+        a quarter of the (layer, sequence) queries aimed at unsampled planted keys.
+    kind "long128k": n = 131072, batch 4, eta = 1/32, eps in {0.02, 0.05}, delta = 0.05, a needle
+        set of U[2 %, 25 %] of the context per KV head that the queries favour.
+
+    A query is one layer of one sequence (32 query heads); a step is layers x batch queries.  The
+    first step runs eagerly with a synchronisation and a status check after every call; the timed
+    steps replay a CUDA graph of one step.  One JSON line."""
     import torch
 
     from verified_kv_cache_poissoncomp_gb300 import binding as B
@@ -717,87 +731,123 @@ def run_long128k(args, local):
     B.lib()
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
+    L, KVH, G, D = args.layers, 8, 4, 128
+    if kind == "decode-step":
+        Bt, N = 8, 32768
+        etas, epss = [1 / 8, 1 / 32], [0.05]
+    else:
+        Bt, N = 4, 131072
+        etas, epss = [1 / 32], [0.02, 0.05]
+    delta = 0.05
+    units = Bt * L * KVH
     t0 = time.time()
-    w = I.long_context_128k(n_queries=8)
+    if kind == "decode-step":
+        tau, kv, queries, planted = I.decode_step_cache_torch(units, N, D, G, L, Bt, KVH, dev)
+        extra = {"planted_queries": int(planted.sum())}
+    else:
+        tau, kv, queries, pfrac = I.long_context_torch(units, N, D, G, L, Bt, KVH, dev)
+        extra = {"needle_frac_per_unit": {"mean": round(float(pfrac.mean()), 4),
+                                          "min": round(float(pfrac.min()), 4),
+                                          "max": round(float(pfrac.max()), 4)}}
+    host_kv = torch.empty(kv.shape, dtype=torch.int16, pin_memory=True)
+    host_kv.copy_(kv)
+    torch.cuda.synchronize()
     gen_s = time.time() - t0
-    Q = w.queries.shape[0]
+    hq = Bt * KVH * G
     stream = torch.cuda.Stream(dev)
-    with torch.cuda.stream(stream):
-        eng = VerKV(w.B, w.L, w.h_kv, w.G, w.d, w.n, default_cap(w.n, w.eta),
-                    sketch_format=sketch_format(args))
-        eng.load(w.tau.reshape(-1, w.n), w.kv.reshape(-1, w.n, 2, w.d))
-        eng.compress(w.eta, w.n_sink, w.n_local, w.seed)
-        eng.sync()
-        q_dev = torch.as_tensor(w.queries.view(np.int16)).to(dev)
-        hq = w.B * w.h_kv * w.G
-        o_all = torch.empty((Q, hq, w.d), dtype=torch.float32, device=dev)
-        lse_all = torch.empty((Q, hq), dtype=torch.float32, device=dev)
-        st_all = torch.empty((Q, hq, 16), dtype=torch.int32, device=dev)
-        fc_all = torch.zeros((Q, w.B * w.h_kv), dtype=torch.int32, device=dev)
-    row_bytes = (2 if args.sketch == "exact" else 4) * w.d
     rows = []
-    for eps in (0.02, 0.05):
-        def step(counts=False):  # counts: an untimed pass for the statistics
-            for t in range(Q):
-                B.verkv_attend_verified(eng.ctx, int(w.query_layer[t]), q_dev[t].data_ptr(),
-                                        eng.pivotal, eng.r_full.data_ptr(), eng.sketch_desc, eps,
-                                        w.delta, None, fc_all[t].data_ptr() if counts else None)
-                B.verkv_fetch_refine(eng.ctx, None, None, eng.host_kv.data_ptr(),
-                                     o_all[t].data_ptr(), lse_all[t].data_ptr(),
-                                     st_all[t].data_ptr())
+    for eta in etas:
+        with torch.cuda.stream(stream):
+            eng = VerKV(Bt, L, KVH, G, D, N, default_cap(N, eta))
+            eng.load_device(tau, kv, host_kv)
+            eng.compress(eta, 4, 512, 0)
+            eng.sync()
+            o_all = torch.empty((L, hq, D), dtype=torch.float32, device=dev)
+            lse_all = torch.empty((L, hq), dtype=torch.float32, device=dev)
+            st_all = torch.empty((L, hq, 16), dtype=torch.int32, device=dev)
+            fc_all = torch.zeros((L, Bt * KVH), dtype=torch.int32, device=dev)
+        counts = eng.p_count.cpu().numpy().astype(np.int64)
+        for eps in epss:
+            def step(check=False, with_counts=False):
+                for l in range(L):
+                    B.verkv_attend_verified(eng.ctx, l, queries[l].data_ptr(), eng.pivotal,
+                                            eng.r_full.data_ptr(), eng.sketch_desc, eps, delta,
+                                            None, fc_all[l].data_ptr() if with_counts else None)
+                    if check:
+                        B.verkv_sync(eng.ctx)
+                    B.verkv_fetch_refine(eng.ctx, None, None, eng.host_kv.data_ptr(),
+                                         o_all[l].data_ptr(), lse_all[l].data_ptr(),
+                                         st_all[l].data_ptr())
+                    if check:
+                        B.verkv_sync(eng.ctx)
 
-        with torch.cuda.stream(stream):
-            step()
+            with torch.cuda.stream(stream):
+                step(check=True, with_counts=True)      # checked, and the rows fetched
+            fr = fc_all.cpu().numpy().astype(np.int64)  # [L][B*KVH]
+            st = st_all.cpu().numpy()
+            with torch.cuda.stream(stream):
+                graph = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(graph, stream=stream):
+                    step()
+                for _ in range(args.warmup):
+                    graph.replay()
+            torch.cuda.synchronize()
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            with ClockSampler(local) as clk:
+                e0.record(stream)
+                with torch.cuda.stream(stream):
+                    for _ in range(args.steps):
+                        graph.replay()
+                e1.record(stream)
+                torch.cuda.synchronize()
             B.verkv_sync(eng.ctx)
-            graph = torch.cuda.CUDAGraph()
-            with torch.cuda.graph(graph, stream=stream):
+            ms = e0.elapsed_time(e1) / args.steps
+            del graph
+            B.verkv_profile_enable(eng.ctx, 1)
+            with torch.cuda.stream(stream):
                 step()
-            for _ in range(args.warmup):
-                graph.replay()
-        torch.cuda.synchronize()
-        e0 = torch.cuda.Event(enable_timing=True)
-        e1 = torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        with torch.cuda.stream(stream):
-            for _ in range(args.steps):
-                graph.replay()
-        e1.record(stream)
-        torch.cuda.synchronize()
-        B.verkv_sync(eng.ctx)
-        ms = e0.elapsed_time(e1) / args.steps
-        B.verkv_profile_enable(eng.ctx, 1)
-        with torch.cuda.stream(stream):
-            step()
-        launches, total_ms = B.verkv_profile_read(eng.ctx)
-        B.verkv_profile_enable(eng.ctx, 0)
-        with torch.cuda.stream(stream):
-            step(counts=True)
-        B.verkv_sync(eng.ctx)
-        fr = fc_all.cpu().numpy().astype(np.int64)
-        st = st_all.cpu().numpy()
-        h2d = float(fr.sum(1).mean()) * row_bytes
-        fetch_us = 1e3 * total_ms[B.VERKV_K_FETCH_HOST] / max(launches[B.VERKV_K_FETCH_HOST], 1)
-        rows.append({
-            "eps": eps, "queries_per_s": round(Q / (ms * 1e-3), 2), "ms_per_step": round(ms, 4),
-            "fetched_frac_per_kv_head": {"mean": round(float(fr.mean()) / w.n, 4),
-                                         "min": round(float(fr.min()) / w.n, 4),
-                                         "max": round(float(fr.max()) / w.n, 4)},
-            "certified_frac": round(float(st[..., 10].mean()), 4),
-            "h2d_bytes_per_query": int(h2d), "fetch_GBs": round(h2d / (fetch_us * 1e-6) / 1e9, 1),
-            "per_kernel_us": {B.verkv_kernel_name(k): round(1e3 * total_ms[k] / launches[k], 2)
-                              for k in range(B.VERKV_K_COUNT) if launches[k] > 0},
-            **traffic_stats(st, fr, eng.p_count.cpu().numpy().astype(np.int64), w.n)})
-        del graph
-    print(json.dumps({"workload": "long-128k", "metric": METRIC, "unit": UNIT,
-                      "steps": args.steps, "warmup": args.warmup, "data": "synthetic",
-                      "config": {"workload": "128K tokens, batch 4, 8 KV heads x 4 query heads, "
-                                             "d=128, bf16, eta=1/32, H=4+512, needle sets of "
-                                             "U[2%,25%] of the context per KV head, delta=0.05, "
-                                             f"{Q} decode queries per step", "sketch": args.sketch,
-                                 "graph": True},
-                      "needle_frac_per_kv_head": [round(x, 4) for x in w.meta["needle_frac"].ravel()],
-                      "input_generation_s": round(gen_s, 1), "rows": rows}), flush=True)
-    eng.close()
+            launches, total_ms = B.verkv_profile_read(eng.ctx)
+            B.verkv_profile_enable(eng.ctx, 0)
+            # Algorithmic bytes of a step: per layer call the sketch of every unit, the logits
+            # written and read once, r, and the pivotal rows (K, V, id and r); host bytes: the V
+            # row of every fetched token (the exact sketch holds the keys).
+            units_layer = Bt * KVH
+            hbm = 0
+            for l in range(L):
+                cnt_l = sum(int(counts[(b * L + l) * KVH + h]) for b in range(Bt) for h in range(KVH))
+                hbm += units_layer * N * D * 2 + 2 * hq * N * 4 + units_layer * N * 4 + \
+                    cnt_l * (4 * D + 8)
+            h2d = int(fr.sum()) * 2 * D
+            nfetch = st[..., 13]
+            per_k = {B.verkv_kernel_name(k): {"launches_per_step": int(launches[k]),
+                                              "avg_us": round(1e3 * total_ms[k] / launches[k], 2),
+                                              "ms_per_step": round(total_ms[k], 3)}
+                     for k in range(B.VERKV_K_COUNT) if launches[k] > 0}
+            fetch_ms = total_ms[B.VERKV_K_FETCH_HOST]
+            rows.append({
+                "eta": eta, "eps": eps, "steps_per_s": round(1e3 / ms, 3),
+                "queries_per_s": round(L * Bt * 1e3 / ms, 2), "ms_per_step": round(ms, 3),
+                "hbm_bytes_per_step": hbm, "hbm_GBs": round(hbm / (ms * 1e-3) / 1e9, 1),
+                "h2d_bytes_per_step": h2d,
+                "fetch_GBs_in_k_refine": round(h2d / (fetch_ms * 1e-3) / 1e9, 1) if fetch_ms else None,
+                "fetched_frac_per_kv_head": {"mean": round(float(fr.mean()) / N, 4),
+                                             "min": round(float(fr.min()) / N, 4),
+                                             "max": round(float(fr.max()) / N, 4)},
+                "certified_frac": round(float(st[..., 10].mean()), 4),
+                "fetched_rows_per_query_head": round(float(nfetch.mean()), 1),
+                "per_kernel": per_k, "clocks": clk.summary(),
+                **traffic_stats(st.reshape(-1, 16), fr.reshape(-1), counts, N)})
+        eng.close()
+        del eng, o_all, lse_all, st_all, fc_all
+        torch.cuda.empty_cache()
+    print(json.dumps({"workload": kind, "metric": METRIC, "unit": UNIT, "steps": args.steps,
+                      "warmup": args.warmup, "data": "synthetic", "dtype": "bf16",
+                      "config": {"layers": L, "batch": Bt, "kv_heads": KVH, "q_per_kv": G,
+                                 "head_dim": D, "n": N, "delta": delta,
+                                 "host_cache_GB": round(host_kv.nbytes / 1e9, 1),
+                                 "sketch": "exact", "fetch": "zerocopy", "graph": True},
+                      "input_generation_s": round(gen_s, 1), **extra, "rows": rows}), flush=True)
 
 
 def run_pc_sweep(args, local):
@@ -917,7 +967,7 @@ def run_estimator(args, local):
     peak, peak_src = measured_peaks()
     stream = torch.cuda.Stream(dev)
     with torch.cuda.stream(stream):
-        tau, kv, queries = I.decode_step_cache_torch(units, n, d, G, layers, batch, kvh, dev)
+        tau, kv, queries, _ = I.decode_step_cache_torch(units, n, d, G, layers, batch, kvh, dev)
         host_kv = torch.empty(kv.shape, dtype=torch.int16, pin_memory=True)
         host_kv.copy_(kv)
         torch.cuda.synchronize()
@@ -1014,7 +1064,10 @@ def main():
             run_pc_sweep(args, local)
     elif args.long128k:
         if rank == 0:
-            run_long128k(args, local)
+            run_model_steps(args, local, "long128k")
+    elif args.decode_step:
+        if rank == 0:
+            run_model_steps(args, local, "decode-step")
     elif args.estimator:
         if rank == 0:
             run_estimator(args, local)

@@ -31,7 +31,8 @@ SAMPLED = [0, 13, 38, 63]  # layer-local units u' = b * KVH + h: (0,0), (1,5), (
 def cache():
     dev = torch.device("cuda", 0)
     units = BATCH * LAYERS * KVH
-    tau, kv, queries = I.decode_step_cache_torch(units, N, D, G, LAYERS, BATCH, KVH, dev)
+    tau, kv, queries, planted = I.decode_step_cache_torch(units, N, D, G, LAYERS, BATCH, KVH, dev)
+    assert planted.any()
     host_kv = torch.empty(kv.shape, dtype=torch.int16, pin_memory=True)
     host_kv.copy_(kv)
     torch.cuda.synchronize()

@@ -262,13 +262,17 @@ def long_context_128k(B=4, L=1, h_kv=8, G=4, d=128, n=131072, eta=1.0 / 32, n_si
 
 
 def decode_step_cache_torch(units, n, d, G, layers, batch, kv_heads, device, seed=1238,
-                            alpha=4.0, n_sinks=4, sink_gain=8.0):
+                            alpha=4.0, n_sinks=4, sink_gain=8.0, n_local=512, n_plants=8,
+                            plant_every=4, plant_frac=0.2):
     """The full-decode-step cache on the device (torch, seeded), for sizes where numpy
     generation would take minutes: per unit, tau lognormal(0, 1.5) / max; keys N(0, 1) with the
     outlier channel scales of make_workload and the first n_sinks keys shifted by sink_gain along
     the unit's direction mu (attention sinks); values N(0, 1); bf16 by round-to-nearest.  Queries
-    [layers][batch][kv_heads * G][d]: alpha mu + N(0, I).  Returns (tau, kv int16 [units][n][2][d],
-    queries int16)."""
+    [layers][batch][kv_heads * G][d]: alpha mu + N(0, I).  As in make_workload, every unit has
+    n_plants planted positions outside the forced set carrying the unit's smallest tau, and every
+    plant_every-th (layer, sequence) query is planted: each query head adds a component along one
+    planted key of its KV head, scaled so that key holds about plant_frac of the head's attention
+    mass.  Returns (tau, kv int16 [units][n][2][d], queries int16, planted bool [layers][batch])."""
     import torch
 
     gen = torch.Generator(device=device)
@@ -289,11 +293,100 @@ def decode_step_cache_torch(units, n, d, G, layers, batch, kv_heads, device, see
         V = torch.randn((u1 - u0, n, d), generator=gen, device=device)
         kv[u0:u1, :, 1] = V.to(torch.bfloat16).view(torch.int16)
         del V
+    lo, hi = n_sinks, n - n_local
+    n_plants = max(0, min(n_plants, hi - lo))
+    plant_pos = None
+    if n_plants > 0:
+        # n_plants distinct positions in [lo, hi) per unit: the smallest of random keys
+        keys = torch.rand((units, hi - lo), generator=gen, device=device)
+        plant_pos = keys.topk(n_plants, dim=1, largest=False).indices + lo
+        tmin = tau.min(dim=1, keepdim=True).values
+        tau.scatter_(1, plant_pos, tmin.expand(-1, n_plants))
     # unit u = (b * layers + l) * kv_heads + h
     mu4 = mu.view(batch, layers, kv_heads, d).permute(1, 0, 2, 3)  # [layers][batch][kv_heads][d]
     q = alpha * mu4[:, :, :, None, :] + torch.randn((layers, batch, kv_heads, G, d), generator=gen,
                                                     device=device)
+    planted = torch.zeros((layers, batch), dtype=torch.bool)
+    if n_plants > 0 and plant_every > 0:
+        flat = planted.view(-1)
+        flat[plant_every - 1::plant_every] = True
+        inv_sqrt_d = 1.0 / float(np.sqrt(d))
+        for l in range(layers):
+            for b in range(batch):
+                if not planted[l, b]:
+                    continue
+                for h in range(kv_heads):
+                    u = (b * layers + l) * kv_heads + h
+                    Kh = kv[u, :, 0].view(torch.bfloat16).float()                 # [n][d]
+                    pick = torch.randint(0, n_plants, (G,), generator=gen, device=device)
+                    p = plant_pos[u, pick]                                         # [G]
+                    # The query moves along the planted key without its outlier channels: those
+                    # are shared by every key, so a step along them would lift the other logits
+                    # as much as the plant's.  A few steps settle the mass despite the rest.
+                    v = Kh[p].clone()                                              # [G][d]
+                    v[:, :8] = 0.0
+                    vk = (v * Kh[p]).sum(dim=1).double()
+                    for _ in range(6):
+                        qg = q[l, b, h].to(torch.bfloat16).float()                 # [G][d]
+                        s0 = (qg @ Kh.T).double() * inv_sqrt_d                     # [G][n]
+                        sp = s0.gather(1, p[:, None])[:, 0]
+                        others = s0.scatter(1, p[:, None], float("-inf"))
+                        top = others.max(dim=1).values
+                        mass = torch.exp(others - top[:, None]).sum(dim=1)
+                        target = torch.log(plant_frac / (1.0 - plant_frac) * mass) + top
+                        step = (target - sp) / inv_sqrt_d / vk
+                        q[l, b, h] += step.float()[:, None] * v
     # contiguous [layers][batch][kv_heads * G][d]: the broadcast against the permuted mu4 would
     # otherwise leave the batch dimension outermost in memory
     queries = q.reshape(layers, batch, kv_heads * G, d).to(torch.bfloat16).contiguous()
-    return tau, kv, queries.view(torch.int16)
+    return tau, kv, queries.view(torch.int16), planted
+
+
+def long_context_torch(units, n, d, G, layers, batch, kv_heads, device, seed=1240, alpha=4.0,
+                       n_sinks=4, sink_gain=8.0, n_local=512, boost=3.0, p_range=(0.02, 0.25)):
+    """The long-context workload with the fetch path stressed, generated on the device (torch,
+    seeded) for sizes where numpy would take minutes: scores, keys, values and sinks as in
+    decode_step_cache_torch, and per unit a needle set of p n tokens (p ~ U[p_range]) at uniform
+    positions outside the forced set whose keys share a component a u along a random unit
+    direction u of the unit; every query of the unit adds the same a u, so a needle's logit rises
+    by a^2 / sqrt(d) = boost (as long_context_128k does).  Returns (tau, kv int16 [units][n][2][d],
+    queries int16 [layers][batch][kv_heads * G][d], needle fraction per unit)."""
+    import torch
+
+    gen = torch.Generator(device=device)
+    gen.manual_seed(seed)
+    scales = torch.as_tensor(_channel_scales(d, True), device=device)
+    x = torch.exp(1.5 * torch.randn((units, n), generator=gen, device=device))
+    tau = (x / x.max(dim=1, keepdim=True).values).float()
+    mu = torch.zeros((units, d), device=device)
+    mu[:, :8] = torch.randn((units, 8), generator=gen, device=device)
+    mu /= mu.norm(dim=1, keepdim=True)
+    un = torch.randn((units, d), generator=gen, device=device)
+    un /= un.norm(dim=1, keepdim=True)
+    a = float(np.sqrt(boost * np.sqrt(d)))
+    lo, hi = n_sinks, n - n_local
+    pfrac = torch.empty(units, device=device).uniform_(p_range[0], p_range[1], generator=gen)
+    kv = torch.empty((units, n, 2, d), dtype=torch.int16, device=device)
+    for u0 in range(0, units, 16):  # in slices, to bound the float32 temporaries
+        u1 = min(units, u0 + 16)
+        K = torch.randn((u1 - u0, n, d), generator=gen, device=device) * scales
+        K[:, :n_sinks] += sink_gain * mu[u0:u1, None, :]
+        # needles: the first p (hi - lo) tokens of a random order of [lo, hi)
+        order = torch.rand((u1 - u0, hi - lo), generator=gen, device=device).argsort(dim=1) + lo
+        cnt = (pfrac[u0:u1] * (hi - lo)).long()
+        take = torch.arange(hi - lo, device=device)[None, :] < cnt[:, None]
+        needle = torch.zeros((u1 - u0, n), dtype=torch.bool, device=device)
+        needle.scatter_(1, order, take)
+        K += needle[:, :, None].float() * (a * un[u0:u1, None, :])
+        kv[u0:u1, :, 0] = K.to(torch.bfloat16).view(torch.int16)
+        del K, needle, order
+        V = torch.randn((u1 - u0, n, d), generator=gen, device=device)
+        kv[u0:u1, :, 1] = V.to(torch.bfloat16).view(torch.int16)
+        del V
+    # unit u = (b * layers + l) * kv_heads + h
+    mu4 = mu.view(batch, layers, kv_heads, d).permute(1, 0, 2, 3)
+    un4 = un.view(batch, layers, kv_heads, d).permute(1, 0, 2, 3)
+    q = (alpha * mu4 + a * un4)[:, :, :, None, :] + torch.randn((layers, batch, kv_heads, G, d),
+                                                                generator=gen, device=device)
+    queries = q.reshape(layers, batch, kv_heads * G, d).to(torch.bfloat16).contiguous()
+    return tau, kv, queries.view(torch.int16), pfrac.cpu().numpy()
