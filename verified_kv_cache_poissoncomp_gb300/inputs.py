@@ -261,13 +261,29 @@ def long_context_128k(B=4, L=1, h_kv=8, G=4, d=128, n=131072, eta=1.0 / 32, n_si
                     meta=dict(data_seed=data_seed, boost=boost, needle_frac=pfrac))
 
 
+def _sinks_torch(K, mu, alpha, n_sinks, sink_frac=0.5):
+    """Attention sinks for a slice of units (torch, in place): the first n_sinks keys of each unit
+    move along its direction mu until, for a query alpha mu + N(0, I), they hold about sink_frac
+    of the expected attention mass -- the recipe of _head_keys.  K float32 [u][n][d], mu [u][d]."""
+    import torch
+
+    d = K.shape[-1]
+    base = alpha * torch.einsum("und,ud->un", K, mu) / np.sqrt(d) + (K * K).sum(-1) / (2 * d)
+    top = base.max(dim=1, keepdim=True).values
+    mass = torch.exp(base - top).double().sum(dim=1, keepdim=True)
+    target = torch.log(sink_frac / (1.0 - sink_frac) * mass / n_sinks).float() + top
+    shift = (target - base[:, :n_sinks]) * (np.sqrt(d) / alpha)           # [u][n_sinks]
+    K[:, :n_sinks] += shift[:, :, None] * mu[:, None, :]
+
+
 def decode_step_cache_torch(units, n, d, G, layers, batch, kv_heads, device, seed=1238,
-                            alpha=4.0, n_sinks=4, sink_gain=8.0, n_local=512, n_plants=8,
+                            alpha=4.0, n_sinks=4, sink_frac=0.5, n_local=512, n_plants=8,
                             plant_every=4, plant_frac=0.2):
     """The full-decode-step cache on the device (torch, seeded), for sizes where numpy
     generation would take minutes: per unit, tau lognormal(0, 1.5) / max; keys N(0, 1) with the
-    outlier channel scales of make_workload and the first n_sinks keys shifted by sink_gain along
-    the unit's direction mu (attention sinks); values N(0, 1); bf16 by round-to-nearest.  Queries
+    outlier channel scales of make_workload and the first n_sinks keys moved along the unit's
+    direction mu until they hold about sink_frac of the expected attention mass (attention sinks,
+    as in make_workload); values N(0, 1); bf16 by round-to-nearest.  Queries
     [layers][batch][kv_heads * G][d]: alpha mu + N(0, I).  As in make_workload, every unit has
     n_plants planted positions outside the forced set carrying the unit's smallest tau, and every
     plant_every-th (layer, sequence) query is planted: each query head adds a component along one
@@ -287,7 +303,7 @@ def decode_step_cache_torch(units, n, d, G, layers, batch, kv_heads, device, see
     for u0 in range(0, units, 64):  # in slices, to bound the float32 temporaries
         u1 = min(units, u0 + 64)
         K = torch.randn((u1 - u0, n, d), generator=gen, device=device) * scales
-        K[:, :n_sinks] += sink_gain * mu[u0:u1, None, :]
+        _sinks_torch(K, mu[u0:u1], alpha, n_sinks, sink_frac)
         kv[u0:u1, :, 0] = K.to(torch.bfloat16).view(torch.int16)
         del K
         V = torch.randn((u1 - u0, n, d), generator=gen, device=device)
@@ -343,7 +359,7 @@ def decode_step_cache_torch(units, n, d, G, layers, batch, kv_heads, device, see
 
 
 def long_context_torch(units, n, d, G, layers, batch, kv_heads, device, seed=1240, alpha=4.0,
-                       n_sinks=4, sink_gain=8.0, n_local=512, boost=3.0, p_range=(0.02, 0.25)):
+                       n_sinks=4, sink_frac=0.5, n_local=512, boost=3.0, p_range=(0.02, 0.25)):
     """The long-context workload with the fetch path stressed, generated on the device (torch,
     seeded) for sizes where numpy would take minutes: scores, keys, values and sinks as in
     decode_step_cache_torch, and per unit a needle set of p n tokens (p ~ U[p_range]) at uniform
@@ -370,7 +386,7 @@ def long_context_torch(units, n, d, G, layers, batch, kv_heads, device, seed=124
     for u0 in range(0, units, 16):  # in slices, to bound the float32 temporaries
         u1 = min(units, u0 + 16)
         K = torch.randn((u1 - u0, n, d), generator=gen, device=device) * scales
-        K[:, :n_sinks] += sink_gain * mu[u0:u1, None, :]
+        _sinks_torch(K, mu[u0:u1], alpha, n_sinks, sink_frac)
         # needles: the first p (hi - lo) tokens of a random order of [lo, hi)
         order = torch.rand((u1 - u0, hi - lo), generator=gen, device=device).argsort(dim=1) + lo
         cnt = (pfrac[u0:u1] * (hi - lo)).long()
