@@ -935,13 +935,14 @@ def run_pc_sweep(args, local):
                       "rows": rows}), flush=True)
 
 
-def estimator_bytes(count, pivotal_r, d, G):
+def estimator_bytes(count, pivotal_r, d, G, sketch_logits=False):
     """Algorithmic bytes of one pass of the shrinkage estimator over the pivotal set: each
-    pivotal row's K and V (4d bytes), its id and r (8), and for a sampled row (r < 1) the sketch
-    logit of each of its G query heads (lambda).  count: rows per unit; pivotal_r: [units][cap].
-    Returns (bytes, sampled rows); the queries are negligible."""
+    pivotal row's K and V (4d bytes) and its id and r (8); with a 2-bit sketch (sketch_logits)
+    also, for a sampled row (r < 1), the sketch logit of each of its G query heads (lambda's
+    w-hat; the exact sketch gives the row's own weight).  count: rows per unit; pivotal_r:
+    [units][cap].  Returns (bytes, sampled rows); the queries are negligible."""
     n_l = int(sum(int((pivotal_r[u, :count[u]] < 1.0).sum()) for u in range(len(count))))
-    return int(np.sum(count)) * (4 * d + 8) + n_l * 4 * G, n_l
+    return int(np.sum(count)) * (4 * d + 8) + (n_l * 4 * G if sketch_logits else 0), n_l
 
 
 def run_estimator(args, local):

@@ -31,4 +31,7 @@ def test_estimator_bytes_on_a_hand_made_case():
     count = np.array([3, 2])
     nbytes, n_l = bench.estimator_bytes(count, r, d=128, G=4)
     assert n_l == 3
+    assert nbytes == 5 * (4 * 128 + 8)
+    # with a 2-bit sketch each sampled row also reads the sketch logit of its 4 query heads
+    nbytes, n_l = bench.estimator_bytes(count, r, d=128, G=4, sketch_logits=True)
     assert nbytes == 5 * (4 * 128 + 8) + 3 * 4 * 4

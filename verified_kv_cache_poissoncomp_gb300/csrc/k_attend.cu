@@ -31,6 +31,9 @@
 //             the K|V rows read from page-locked host memory, online-softmax partials per chunk.
 #include <math.h>
 
+#include <algorithm>
+
+#include "pivotal_mma.cuh"
 #include "verkv_common.cuh"
 #include "verkv_internal.h"
 
@@ -109,30 +112,23 @@ __device__ __forceinline__ uint4 ld_host(const uint4 *p) {
     return v;
 }
 
-// One item of the split-K sums: positions [lo, hi) of a row list of layer unit `ul` (ids[p] is
-// the token id at position p), taken PART_ROWS at a time, into partial `part_idx`.  Row data is
-// addressed by token id (ROWS_HOST: the unit's host cache) or by list position (ROWS_PIVOTAL:
-// the pivotal buffer; ROWS_STAGED: the staged rows).  An empty item writes nothing unless
+// One item of the split-K sums over fetched rows: positions [lo, hi) of a row list of layer unit
+// `ul` (ids[p] is the token id at position p), taken PART_ROWS at a time, into partial
+// `part_idx`.  Row data is addressed by token id (ROWS_HOST: the unit's host cache) or by list
+// position (ROWS_STAGED: rows copied to the device).  A fetched row is exact: weight 1 for the
+// query heads whose F holds it, 0 for the others.  An empty item writes nothing unless
 // write_empty (then a zero partial).  lo and hi are uniform over the CTA.
-// SMEM (pivotal items of at most PART_ROWS rows only): the item's K|V rows, ids and r were copied
-// to the shared-memory stage `stage` ([PART_ROWS][4D bytes], then PART_ROWS ids, then PART_ROWS
-// r); the same lanes take the same rows in the same order, so the sums are bitwise those of the
-// global-memory path.
-template <int D, int G, int MODE, bool SMEM = false>
+template <int D, int G, int MODE>
 __device__ __forceinline__ void partial_rows(const PartialArgs &a, int ul, int part_idx, int lo,
-                                             int hi, const int32_t *ids, bool write_empty,
-                                             const unsigned char *stage = nullptr) {
+                                             int hi, const int32_t *ids, bool write_empty) {
+    static_assert(MODE == ROWS_HOST || MODE == ROWS_STAGED, "fetched rows only");
     constexpr int LPR = D / 8, RPW = 32 / LPR, NW = 4;
     constexpr int ITER = (PART_ROWS / NW) / RPW;  // row groups per warp
-    // Row groups in flight per warp: all of them for host rows (link latency) and for staged
-    // rows (only the id-dependent loads are in flight), else four.
-    constexpr int U = (MODE == ROWS_HOST || SMEM) ? ITER : (ITER < 4 ? ITER : 4);
-    static_assert(!SMEM || MODE == ROWS_PIVOTAL, "staged items are pivotal");
-    const int32_t *s_id = SMEM ? reinterpret_cast<const int32_t *>(stage + PART_ROWS * 4 * D) : nullptr;
-    const float *s_r = SMEM ? reinterpret_cast<const float *>(stage + PART_ROWS * (4 * D + 4)) : nullptr;
+    // Row groups in flight per warp: all of them for host rows (link latency), else four.
+    constexpr int U = MODE == ROWS_HOST ? ITER : (ITER < 4 ? ITER : 4);
     constexpr int SUBMASK = LPR / G - 1;
     __shared__ float sN[NW][G][D];
-    __shared__ float sD[NW][RPW][G], sM[NW][RPW][G];
+    __shared__ float sD[NW][RPW][G];
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int cgp = lane % LPR, rg = lane / LPR;
@@ -140,77 +136,63 @@ __device__ __forceinline__ void partial_rows(const PartialArgs &a, int ul, int p
     const int hq = a.li.kv_heads * G;
     if (lo >= hi && !write_empty) return;
 
-    {
-        const int b = ul / a.li.kv_heads, h = ul - b * a.li.kv_heads;
-        const int ug = a.li.unit_global(ul);
-        const int src = MODE == ROWS_PIVOTAL ? ug : ul;
+    const int b = ul / a.li.kv_heads, h = ul - b * a.li.kv_heads;
+    const int ug = a.li.unit_global(ul);
+    float qv[G][8];
+#pragma unroll
+    for (int g = 0; g < G; ++g) {
+        const uint4 v = *reinterpret_cast<const uint4 *>(a.q + ((size_t)b * hq + h * G + g) * D + cgp * 8);
+        unpack8(v, qv[g]);
+    }
+    const float mh_ = a.qstats[ul * G + myhead].m;
+    const uint32_t *Fh = a.F + (size_t)(ul * G + myhead) * a.W;
+    float acc[G][8];
+#pragma unroll
+    for (int g = 0; g < G; ++g)
+#pragma unroll
+        for (int c = 0; c < 8; ++c) acc[g][c] = 0.0f;
+    float dacc = 0.0f;
 
-        float qv[G][8];
-#pragma unroll
-        for (int g = 0; g < G; ++g) {
-            const uint4 v = *reinterpret_cast<const uint4 *>(a.q + ((size_t)b * hq + h * G + g) * D + cgp * 8);
-            unpack8(v, qv[g]);
-        }
-        const float mh_ = a.qstats[ul * G + myhead].m;
-        const float bh_ = a.qstats[ul * G + myhead].beta;
-        const uint32_t *Fh = a.F + (size_t)(ul * G + myhead) * a.W;
-        const float *sc_h = MODE == ROWS_PIVOTAL ? a.scores + (size_t)(ul * G + myhead) * a.n : nullptr;
-        float acc[G][8];
-#pragma unroll
-        for (int g = 0; g < G; ++g)
-#pragma unroll
-            for (int c = 0; c < 8; ++c) acc[g][c] = 0.0f;
-        float dacc = 0.0f, m2acc = 0.0f;
-
-        const float *prs = MODE == ROWS_PIVOTAL ? a.pr + (size_t)src * a.row_stride : nullptr;
-        // ROWS_HOST indexes the full host cache of the unit by token id; the others by row.
-        const uint4 *rows = reinterpret_cast<const uint4 *>(a.rows) +
-                            (MODE == ROWS_HOST ? (size_t)ug * a.n : (size_t)src * a.row_stride) * a.row16;
-        const uint4 *keys = a.keys ? reinterpret_cast<const uint4 *>(a.keys) + (size_t)ug * a.n * (D / 8)
-                                   : nullptr;
+    // ROWS_HOST indexes the full host cache of the unit by token id; ROWS_STAGED by position.
+    const uint4 *rows = reinterpret_cast<const uint4 *>(a.rows) +
+                        (MODE == ROWS_HOST ? (size_t)ug * a.n : (size_t)ul * a.row_stride) * a.row16;
+    const uint4 *keys = a.keys ? reinterpret_cast<const uint4 *>(a.keys) + (size_t)ug * a.n * (D / 8)
+                               : nullptr;
 #pragma unroll 1
-        for (int cbase = lo; cbase < hi; cbase += PART_ROWS) {
+    for (int cbase = lo; cbase < hi; cbase += PART_ROWS) {
         const int rbase = cbase + warp * (PART_ROWS / NW);
 #pragma unroll 1
         for (int it0 = 0; it0 < ITER; it0 += U) {
             int id[U];
-            float r[U];
             bool valid[U];
 #pragma unroll
             for (int u = 0; u < U; ++u) {
                 const int row = rbase + (it0 + u) * RPW + rg;
                 valid[u] = row < hi;
-                id[u] = valid[u] ? (SMEM ? s_id[row - lo] : ids[row]) : 0;
+                id[u] = valid[u] ? ids[row] : 0;
                 if ((unsigned)id[u] >= (unsigned)a.n) {  // not a token of the unit: skip the row
                     raise_error(a.err, ERR_BADID);
                     valid[u] = false;
                     id[u] = 0;
                 }
-                r[u] = (MODE == ROWS_PIVOTAL && valid[u]) ? (SMEM ? s_r[row - lo] : prs[row]) : 1.0f;
             }
             uint4 kq[U], vq[U];
             uint32_t fw[U];
-            float shat[U];  // sketch logit of the row for the lane's head (pivotal rows)
 #pragma unroll
             for (int u = 0; u < U; ++u) {
                 kq[u] = make_uint4(0, 0, 0, 0);
                 vq[u] = make_uint4(0, 0, 0, 0);
                 fw[u] = 0u;
-                shat[u] = 0.0f;
                 if (valid[u]) {
-                    if (MODE == ROWS_PIVOTAL && r[u] < 1.0f) shat[u] = sc_h[id[u]];
                     const size_t rr = MODE == ROWS_HOST ? (size_t)id[u] : (size_t)(rbase + (it0 + u) * RPW + rg);
-                    if (SMEM) {
-                        // K and V come from the stage when the row is summed
-                    } else if (keys) {
+                    if (keys) {
                         kq[u] = ldg_stream(keys + (size_t)id[u] * (D / 8) + cgp);
                     } else if (MODE == ROWS_HOST) {
                         kq[u] = ld_host(rows + rr * a.row16 + cgp);
                     } else {
                         kq[u] = ldg_stream(rows + rr * a.row16 + cgp);
                     }
-                    if (SMEM) {
-                    } else if (MODE == ROWS_HOST) {
+                    if (MODE == ROWS_HOST) {
                         vq[u] = ld_host(rows + rr * a.row16 + a.voff16 + cgp);
                     } else {
                         vq[u] = ldg_stream(rows + rr * a.row16 + a.voff16 + cgp);
@@ -220,12 +202,6 @@ __device__ __forceinline__ void partial_rows(const PartialArgs &a, int ul, int p
             }
 #pragma unroll
             for (int u = 0; u < U; ++u) {
-                if (SMEM && valid[u]) {
-                    const uint4 *srow = reinterpret_cast<const uint4 *>(
-                        stage + (size_t)(rbase + (it0 + u) * RPW + rg - lo) * (4 * D));
-                    kq[u] = srow[cgp];
-                    vq[u] = srow[D / 8 + cgp];
-                }
                 float k[8], v[8];
                 unpack8(kq[u], k);
                 unpack8(vq[u], v);
@@ -238,34 +214,12 @@ __device__ __forceinline__ void partial_rows(const PartialArgs &a, int ul, int p
                     p[g] = s;
                 }
                 const float dot = reduce_heads_a<G, LPR>(p, lane);
-                // Weight of this row for the lane's head.
+                // Weight of this row for the lane's head: exact w if the head's F holds it.
                 float cw = 0.0f;
-                if (valid[u]) {
+                if (valid[u] && ((fw[u] >> (id[u] & 31)) & 1u)) {
                     // Weights to a few 1e-6 relative (the exp2-based exponential): the sums need 1e-3.
-                    const float w = __expf(dot * a.scale - mh_);
-                    const bool inF = (fw[u] >> (id[u] & 31)) & 1u;
-                    float coef;
-                    if (MODE == ROWS_PIVOTAL) {
-                        const float ru = r[u];
-                        if (ru >= 1.0f || inF) {
-                            coef = 1.0f;
-                        } else {
-                            // lambda is the certificate's, from the sketch weight w-hat, and the
-                            // coefficient lambda / r = clip(beta / (w-hat (1 - r)), 1, 1 / r) is
-                            // taken directly (1 / r when w-hat underflows: lambda = 1).
-                            const float wh = __expf(shat[u] - mh_);
-                            const float ir = __frcp_rn(ru);
-                            coef = ir;
-                            if (wh > 0.0f) coef = fminf(ir, fmaxf(1.0f, __fdividef(bh_, wh * (1.0f - ru))));
-                        }
-                    } else {
-                        coef = inF ? 1.0f : 0.0f;
-                    }
-                    cw = coef * w;
-                    if ((cgp & SUBMASK) == 0) {
-                        dacc += cw;
-                        if (MODE == ROWS_PIVOTAL && r[u] < 1.0f && !inF) m2acc += cw * cw * (1.0f - r[u]);
-                    }
+                    cw = __expf(dot * a.scale - mh_);
+                    if ((cgp & SUBMASK) == 0) dacc += cw;
                 }
                 // Every lane of the row needs the weight of every head.
 #pragma unroll
@@ -276,47 +230,84 @@ __device__ __forceinline__ void partial_rows(const PartialArgs &a, int ul, int p
                 }
             }
         }
-        }  // sub
-        // Reduce over the row groups of the warp, then over warps (fixed order).
+    }
+    // Reduce over the row groups of the warp, then over warps (fixed order).
 #pragma unroll
-        for (int off = LPR; off < 32; off <<= 1)
+    for (int off = LPR; off < 32; off <<= 1)
 #pragma unroll
-            for (int g = 0; g < G; ++g)
+        for (int g = 0; g < G; ++g)
 #pragma unroll
-                for (int c = 0; c < 8; ++c) acc[g][c] += __shfl_xor_sync(0xFFFFFFFFu, acc[g][c], off);
-        if (rg == 0) {
+            for (int c = 0; c < 8; ++c) acc[g][c] += __shfl_xor_sync(0xFFFFFFFFu, acc[g][c], off);
+    if (rg == 0) {
 #pragma unroll
-            for (int g = 0; g < G; ++g)
+        for (int g = 0; g < G; ++g)
 #pragma unroll
-                for (int c = 0; c < 8; ++c) sN[warp][g][cgp * 8 + c] = acc[g][c];
+            for (int c = 0; c < 8; ++c) sN[warp][g][cgp * 8 + c] = acc[g][c];
+    }
+    if ((cgp & SUBMASK) == 0) sD[warp][rg][myhead] = dacc;
+    __syncthreads();
+    float *out = a.part + ((size_t)ul * a.max_chunks + part_idx) * G * (D + 2);
+    for (int e = tid; e < G * (D + 2); e += 128) {
+        const int g = e / (D + 2), c = e - g * (D + 2);
+        float s = 0.0f;
+        if (c < D) {
+#pragma unroll
+            for (int w = 0; w < NW; ++w) s += sN[w][g][c];
+        } else if (c == D) {
+#pragma unroll
+            for (int w = 0; w < NW; ++w)
+#pragma unroll
+                for (int j = 0; j < RPW; ++j) s += sD[w][j][g];
+        }  // c == D + 1: a fetched row adds nothing to the second moment
+        out[e] = s;
+    }
+    __syncthreads();
+}
+
+// 16-byte asynchronous copy global -> shared (L2 only), and the wait for all of this thread's.
+__device__ __forceinline__ void cp_async16(void *dst, const void *src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_addr(dst)), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+
+// The pivotal rows [ch PIV_ITEM_ROWS, ...) of layer unit `ul` into partial `ch`, staged by the
+// CTA's 128 threads with 16-byte asynchronous copies (stage rows beyond the unit's count are
+// zeros), PIV_STAGE_ROWS at a time in `buf` (PivLayout<D>::BYTES of shared memory).
+template <int D, int G, bool SKL>
+__device__ __forceinline__ void pivotal_chunk_plain(const PartialArgs &a, int ul, int ch,
+                                                    unsigned char *buf) {
+    using LY = PivLayout<D>;
+    static_assert(piv_red_bytes<D, G>() <= LY::BYTES, "the reduction reuses the stage");
+    const int ug = a.li.unit_global(ul);
+    const int count = min(a.count[ug], a.row_stride);
+    const int lo = ch * PIV_ITEM_ROWS;
+    if (lo >= count) return;  // uniform over the CTA
+    const int hi = min(lo + PIV_ITEM_ROWS, count);
+    PivChunk<D, G, SKL> pc;
+    pc.init(a, ul);
+    const int tid = threadIdx.x;
+    constexpr int VPR = LY::ROWB / 16;  // 16-byte vectors per row
+    const uint4 *src = reinterpret_cast<const uint4 *>(a.rows) + (size_t)ug * a.row_stride * VPR;
+    for (int s0 = lo; s0 < hi; s0 += LY::ROWS) {
+        const int rows = min(LY::ROWS, hi - s0);
+        for (int v = tid; v < LY::ROWS * VPR; v += 128) {
+            const int r = v / VPR, c = v - r * VPR;
+            unsigned char *dst = buf + r * LY::PITCH + c * 16;
+            if (r < rows) cp_async16(dst, src + (size_t)(s0 + r) * VPR + c);
+            else *reinterpret_cast<uint4 *>(dst) = make_uint4(0u, 0u, 0u, 0u);
         }
-        if ((cgp & SUBMASK) == 0) {
-            sD[warp][rg][myhead] = dacc;
-            sM[warp][rg][myhead] = m2acc;
+        if (tid < LY::ROWS) {
+            const size_t at = (size_t)ug * a.row_stride + s0 + tid;
+            reinterpret_cast<int32_t *>(buf + LY::IDS)[tid] = tid < rows ? a.ids[at] : 0;
+            reinterpret_cast<float *>(buf + LY::RS)[tid] = tid < rows ? a.pr[at] : 1.0f;
         }
+        cp_async_wait_all();
         __syncthreads();
-        float *out = a.part + ((size_t)ul * a.max_chunks + part_idx) * G * (D + 2);
-        for (int e = tid; e < G * (D + 2); e += 128) {
-            const int g = e / (D + 2), c = e - g * (D + 2);
-            float s = 0.0f;
-            if (c < D) {
-#pragma unroll
-                for (int w = 0; w < NW; ++w) s += sN[w][g][c];
-            } else if (c == D) {
-#pragma unroll
-                for (int w = 0; w < NW; ++w)
-#pragma unroll
-                    for (int j = 0; j < RPW; ++j) s += sD[w][j][g];
-            } else {
-#pragma unroll
-                for (int w = 0; w < NW; ++w)
-#pragma unroll
-                    for (int j = 0; j < RPW; ++j) s += sM[w][j][g];
-            }
-            out[e] = s;
-        }
+        pc.stage(a, buf, rows);
         __syncthreads();
     }
+    pc.finish(reinterpret_cast<float *>(buf), a.part + ((size_t)ul * a.max_chunks + ch) * G * (D + 2),
+              true, [] { __syncthreads(); });
 }
 
 // The fetched rows of layer unit `ul` with token ids in [k * FET_RANGE, (k + 1) * FET_RANGE):
@@ -341,124 +332,157 @@ __device__ __forceinline__ void range_bounds(const int32_t *list, int count, int
     __syncthreads();
 }
 
-// Pivotal rows in blocks of PIV_ITEM_ROWS list positions; staged fetched rows by token-id range
-// (FET_RANGE ids per partial, a zero partial for an empty range), as k_refine reads them from
-// host memory, so that both fetch modes produce the same partials.
-template <int D, int G, int MODE>
+// Pivotal rows in chunks of PIV_ITEM_ROWS list positions (staged by the CTA itself: the fallback
+// when a pivotal buffer cannot be bulk-copied); staged fetched rows by token-id range (FET_RANGE
+// ids per partial, a zero partial for an empty range), as k_refine reads them from host memory,
+// so that both fetch modes produce the same partials.
+template <int D, int G, int MODE, bool SKL>
 __global__ void __launch_bounds__(128) k_partial(PartialArgs a, int units_layer) {
+    extern __shared__ __align__(128) unsigned char kp_stage[];  // pivotal: PivLayout<D>::BYTES
     pdl_wait();
     pdl_trigger();
     const int total_items = units_layer * a.max_chunks;
     for (int item = blockIdx.x; item < total_items; item += gridDim.x) {
         const int ul = item / a.max_chunks, ch = item - ul * a.max_chunks;
         if (MODE == ROWS_PIVOTAL) {
-            const int ug = a.li.unit_global(ul);
-            const int count = min(a.count[ug], a.row_stride);
-            const int lo = ch * PIV_ITEM_ROWS;
-            partial_rows<D, G, MODE>(a, ul, ch, lo, min(lo + PIV_ITEM_ROWS, count),
-                                     a.ids + (size_t)ug * a.row_stride, false);
+            pivotal_chunk_plain<D, G, SKL>(a, ul, ch, kp_stage);
         } else {
             const int32_t *list = a.ids + (size_t)ul * a.row_stride;
             int lo, hi;
             range_bounds(list, min(a.count[ul], a.row_stride), ch, lo, hi);
             if (threadIdx.x == 0 && lo < hi) atomicOr(&a.rmask[ul * RMASK_W + (ch >> 5)], 1u << (ch & 31));
-            partial_rows<D, G, MODE>(a, ul, ch, lo, hi, list, false);
+            partial_rows<D, G, ROWS_STAGED>(a, ul, ch, lo, hi, list, false);
         }
     }
 }
 
-// k_partial over the pivotal set with its rows staged by TMA.  A CTA takes the non-empty items
-// blockIdx.x, blockIdx.x + gridDim.x, ...; thread 0 streams each item's K|V rows, ids and r into
-// a ring of PV_STAGES shared-memory stages with cp.async.bulk (one mbarrier per stage), so the
-// next item's rows arrive while the current one is summed; only the id-dependent loads (the
-// sketch logit for lambda, the selection word) go to global memory, all of a warp's at once.
-// Waits are bounded: on expiry the CTA latches ERR_TIMEOUT, waits (bounded) for the copies it
-// issued and returns.
-constexpr int PV_STAGES = 2;
-// Resident CTAs per SM the grid is sized for: three fit the shared memory; with eight query heads
-// per KV head the accumulators need the registers of two.
-__host__ __device__ constexpr int pv_ctas_per_sm(int G) { return G <= 4 ? 3 : 2; }
-template <int D>
-__host__ __device__ constexpr int pv_stage_bytes() { return PIV_ITEM_ROWS * (4 * D + 8); }
-
+// k_pivotal: the estimator's pass over the pivotal set on its own (MEMCPY mode, where it runs
+// during the host gather).  Warps 0-3 consume, warp 4 produces: for every stage of PIV_STAGE_ROWS
+// rows of the CTA's chunks (blockIdx.x, blockIdx.x + gridDim.x, ...) the producer waits for the
+// ring slot to be released, then its lanes bulk-copy the rows one by one to their padded
+// positions, and the ids and r, all completing on the slot's mbarrier; the consumers run the
+// stage on the tensor cores and release the slot.  Waits are bounded: on expiry (or once another
+// thread has given up) the kernel keeps its control flow but skips the work, latches ERR_TIMEOUT,
+// waits (bounded) for the copies it issued and returns.
+constexpr int PV_NS = 2;         // ring slots per CTA
+constexpr int PV_CONS = 4;       // consumer warps
+constexpr int PV_NT = 32 * (PV_CONS + 1);
+constexpr int PV_CTAS_PER_SM = 2;
 template <int D, int G>
-__global__ void __launch_bounds__(128, pv_ctas_per_sm(G)) k_partial_staged(PartialArgs a, int units_layer) {
-    static_assert(PIV_ITEM_ROWS == PART_ROWS, "a staged item is one block of rows");
-    extern __shared__ __align__(128) unsigned char pv_ring[];
-    __shared__ __align__(8) uint64_t full[PV_STAGES];
+__host__ __device__ constexpr size_t pv_smem_bytes() {
+    return (size_t)PV_NS * PivLayout<D>::BYTES + piv_red_bytes<D, G>();
+}
+
+template <int D, int G, bool SKL>
+__global__ void __launch_bounds__(PV_NT, PV_CTAS_PER_SM) k_pivotal(PartialArgs a, int units_layer) {
+    using LY = PivLayout<D>;
+    extern __shared__ __align__(128) unsigned char pv_smem[];  // [PV_NS][LY::BYTES], reduction
+    __shared__ __align__(8) uint64_t full[PV_NS], empty[PV_NS];
     __shared__ int s_abort;
-    constexpr int SB = pv_stage_bytes<D>();
-    const int tid = threadIdx.x;
-    const int total = units_layer * a.max_chunks;
-    // The next non-empty item of this CTA at or after `item` (total when none is left).
-    auto next_item = [&](int item, int &ul, int &lo, int &hi) -> int {
-        for (; item < total; item += gridDim.x) {
-            ul = item / a.max_chunks;
-            const int ug = a.li.unit_global(ul);
-            const int count = min(a.count[ug], a.row_stride);
-            lo = (item - ul * a.max_chunks) * PIV_ITEM_ROWS;
-            if (lo < count) {
-                hi = min(lo + PIV_ITEM_ROWS, count);
-                return item;
-            }
-        }
-        return total;
-    };
-    auto issue = [&](int ul, int lo, int hi, int stage) {
-        const int ug = a.li.unit_global(ul);
-        const size_t base = (size_t)ug * a.row_stride + lo;
-        const uint32_t rows_b = (uint32_t)(hi - lo) * (4 * D);
-        const uint32_t list_b = (uint32_t)((hi - lo + 3) & ~3) * 4;  // within the capacity (a multiple of 4)
-        unsigned char *dst = pv_ring + (size_t)stage * SB;
-        uint64_t *bar = &full[stage];
-        mbar_expect_tx(bar, rows_b + 2 * list_b);
-        bulk_g2s(dst, reinterpret_cast<const unsigned char *>(a.rows) + base * (4 * D), rows_b, bar);
-        bulk_g2s(dst + PIV_ITEM_ROWS * 4 * D, a.ids + base, list_b, bar);
-        bulk_g2s(dst + PIV_ITEM_ROWS * (4 * D + 4), a.pr + base, list_b, bar);
-    };
+    __shared__ int s_last[PV_NS];  // the last stage issued into each slot (-1: none)
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    // Rows beyond a stage's count are read as zeros until a consumer writes them (finite values:
+    // their weights are zero, and 0 x finite adds nothing).
+    for (int i = tid; i < PV_NS * LY::BYTES / 16; i += PV_NT)
+        reinterpret_cast<uint4 *>(pv_smem)[i] = make_uint4(0u, 0u, 0u, 0u);
     if (tid == 0) {
-        for (int k = 0; k < PV_STAGES; ++k) mbar_init(&full[k], 1);
+        for (int k = 0; k < PV_NS; ++k) {
+            mbar_init(&full[k], 1);
+            mbar_init(&empty[k], PV_CONS);
+            s_last[k] = -1;
+        }
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         s_abort = 0;
     }
+    fence_proxy_async_smem();  // the zeros before any bulk copy into the same memory
     __syncthreads();
     pdl_wait();
     pdl_trigger();
-    int pul = 0, plo = 0, phi = 0;  // producer (thread 0): the next item to request
-    int pitem = total, n_issued = 0;
-    if (tid == 0) {
-        pitem = next_item(blockIdx.x, pul, plo, phi);
-        for (int k = 0; k < PV_STAGES && pitem < total; ++k) {
-            issue(pul, plo, phi, k);
-            ++n_issued;
-            pitem = next_item(pitem + gridDim.x, pul, plo, phi);
+    volatile int *abort = &s_abort;
+    const int total = units_layer * a.max_chunks;
+    float *red = reinterpret_cast<float *>(pv_smem + PV_NS * LY::BYTES);
+    if (warp == PV_CONS) {
+        int j = 0;
+        for (int item = blockIdx.x; item < total; item += gridDim.x) {
+            const int ul = item / a.max_chunks, ch = item - ul * a.max_chunks;
+            const int ug = a.li.unit_global(ul);
+            const int count = min(a.count[ug], a.row_stride);
+            const int lo = ch * PIV_ITEM_ROWS;
+            if (lo >= count) continue;
+            const int hi = min(lo + PIV_ITEM_ROWS, count);
+            for (int s0 = lo; s0 < hi; s0 += LY::ROWS, ++j) {
+                const int slot = j % PV_NS;
+                bool go = *abort == 0;
+                if (go && j >= PV_NS) {
+                    bool w = true;
+                    if (lane == 0) w = mbar_wait_or_abort(&empty[slot], (uint32_t)(((j / PV_NS) - 1) & 1), abort);
+                    go = __shfl_sync(0xFFFFFFFFu, w ? 1 : 0, 0) != 0;
+                }
+                if (!go) {
+                    if (lane == 0) *abort = 1;
+                    continue;
+                }
+                const int rows = min(LY::ROWS, hi - s0);
+                const uint32_t lb = (uint32_t)((rows + 3) & ~3) * 4;  // within the capacity (a multiple of 4)
+                unsigned char *st = pv_smem + (size_t)slot * LY::BYTES;
+                const size_t at = (size_t)ug * a.row_stride + s0;
+                if (lane == 0) {
+                    mbar_expect_tx(&full[slot], (uint32_t)rows * LY::ROWB + 2 * lb);
+                    s_last[slot] = j;
+                }
+                __syncwarp();
+                const unsigned char *src = reinterpret_cast<const unsigned char *>(a.rows) + at * LY::ROWB;
+                for (int r = lane; r < rows; r += 32)
+                    bulk_g2s(st + r * LY::PITCH, src + (size_t)r * LY::ROWB, LY::ROWB, &full[slot]);
+                if (lane == 0) {
+                    bulk_g2s(st + LY::IDS, a.ids + at, lb, &full[slot]);
+                    bulk_g2s(st + LY::RS, a.pr + at, lb, &full[slot]);
+                }
+            }
+        }
+    } else {
+        int j = 0;
+        for (int item = blockIdx.x; item < total; item += gridDim.x) {
+            const int ul = item / a.max_chunks, ch = item - ul * a.max_chunks;
+            const int ug = a.li.unit_global(ul);
+            const int count = min(a.count[ug], a.row_stride);
+            const int lo = ch * PIV_ITEM_ROWS;
+            if (lo >= count) continue;
+            const int hi = min(lo + PIV_ITEM_ROWS, count);
+            PivChunk<D, G, SKL> pc;
+            pc.init(a, ul);
+            for (int s0 = lo; s0 < hi; s0 += LY::ROWS, ++j) {
+                const int slot = j % PV_NS;
+                bool ok = *abort == 0 && mbar_wait_or_abort(&full[slot], (uint32_t)((j / PV_NS) & 1), abort);
+                ok = __all_sync(0xFFFFFFFFu, ok);
+                unsigned char *st = pv_smem + (size_t)slot * LY::BYTES;
+                const int rows = min(LY::ROWS, hi - s0);
+                if (ok) {
+                    // This warp's rows beyond the count hold an earlier stage's data: zero them.
+                    for (int r = max(rows, warp * 16); r < warp * 16 + 16; ++r)
+                        for (int c = lane; c < LY::ROWB / 16; c += 32)
+                            reinterpret_cast<uint4 *>(st + r * LY::PITCH)[c] = make_uint4(0u, 0u, 0u, 0u);
+                    __syncwarp();
+                    pc.stage(a, st, rows);
+                } else if (lane == 0) {
+                    *abort = 1;
+                }
+                fence_proxy_async_smem();  // generic accesses before the slot's next bulk copy
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&empty[slot]);
+            }
+            pc.finish(red, a.part + ((size_t)ul * a.max_chunks + ch) * G * (D + 2), *abort == 0,
+                      [] { asm volatile("bar.sync 1, %0;" ::"n"(32 * PV_CONS) : "memory"); });
         }
     }
-    int ul = 0, lo = 0, hi = 0, j = 0, consumed = 0;
-    for (int item = next_item(blockIdx.x, ul, lo, hi); item < total;
-         item = next_item(item + gridDim.x, ul, lo, hi), ++j) {
-        const int stage = j % PV_STAGES;
-        if (!mbar_wait_bounded(&full[stage], (uint32_t)((j / PV_STAGES) & 1))) s_abort = 1;
-        __syncthreads();
-        if (s_abort) break;
-        partial_rows<D, G, ROWS_PIVOTAL, true>(a, ul, item - ul * a.max_chunks, lo, hi, nullptr,
-                                               false, pv_ring + (size_t)stage * SB);
-        consumed = j + 1;
-        // partial_rows ends with a block barrier: every warp is done with the stage; refill it.
-        if (tid == 0 && pitem < total) {
-            fence_proxy_async_smem();
-            issue(pul, plo, phi, stage);
-            ++n_issued;
-            pitem = next_item(pitem + gridDim.x, pul, plo, phi);
-        }
-    }
-    if (s_abort) {
-        // Latch the timeout and let the copies this CTA requested land before it exits: items
-        // consumed .. n_issued - 1, item k in stage k % PV_STAGES at phase (k / PV_STAGES) & 1.
+    __syncthreads();
+    if (*abort) {
+        // Latch the timeout and let the copies this CTA issued land before it exits: the last
+        // stage issued into each slot, at its phase.
         if (tid == 0) {
             raise_error(a.err, ERR_TIMEOUT);
-            for (int k = consumed; k < n_issued; ++k)
-                mbar_wait_bounded(&full[k % PV_STAGES], (uint32_t)((k / PV_STAGES) & 1));
+            for (int k = 0; k < PV_NS; ++k)
+                if (s_last[k] >= 0) mbar_wait_bounded(&full[k], (uint32_t)((s_last[k] / PV_NS) & 1));
         }
         __syncthreads();
     }
@@ -466,37 +490,48 @@ __global__ void __launch_bounds__(128, pv_ctas_per_sm(G)) k_partial_staged(Parti
 
 cudaError_t launch_partial(const PartialArgs &a, int units_layer, int grid, cudaStream_t s) {
     const int G = a.li.G;
-    // Pivotal items go through the staged kernel when every copy it makes is 16-byte aligned.
-    const bool staged = a.mode == ROWS_PIVOTAL && a.row16 == a.d / 4 && a.voff16 == a.d / 8 &&
-                        !a.keys && (a.row_stride & 3) == 0 &&
-                        (reinterpret_cast<uintptr_t>(a.rows) & 15) == 0 &&
-                        (reinterpret_cast<uintptr_t>(a.ids) & 15) == 0 &&
-                        (reinterpret_cast<uintptr_t>(a.pr) & 15) == 0;
-    if (staged) {
-        int sms = 0, dev = 0;
-        cudaGetDevice(&dev);
-        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    int sms = 0, dev = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    // Pivotal rows go through the pipelined kernel when every bulk copy it makes is 16-byte
+    // aligned, else through k_partial, which stages them with 16-byte asynchronous copies.
+    const bool bulk = a.mode == ROWS_PIVOTAL && a.row16 == a.d / 4 && a.voff16 == a.d / 8 &&
+                      !a.keys && (a.row_stride & 3) == 0 &&
+                      (reinterpret_cast<uintptr_t>(a.rows) & 15) == 0 &&
+                      (reinterpret_cast<uintptr_t>(a.ids) & 15) == 0 &&
+                      (reinterpret_cast<uintptr_t>(a.pr) & 15) == 0;
+    const bool skl = a.sketch_logits != 0;
+    if (bulk) {
         const int total = units_layer * a.max_chunks;
-        const int g = std::max(1, std::min(total, sms * pv_ctas_per_sm(G)));
-#define VERKV_PSTAGED(DD, GG)                                                                   \
-        if (a.d == DD && G == GG) {                                                             \
-            const size_t smem = (size_t)PV_STAGES * pv_stage_bytes<DD>();                       \
-            const cudaError_t e = ensure_smem((const void *)k_partial_staged<DD, GG>, smem);   \
+        const int g = std::max(1, std::min(total, sms * PV_CTAS_PER_SM));
+#define VERKV_PIVOTAL(DD, GG, SS)                                                               \
+        if (a.d == DD && G == GG && skl == SS) {                                                \
+            const size_t smem = pv_smem_bytes<DD, GG>();                                        \
+            const cudaError_t e = ensure_smem((const void *)k_pivotal<DD, GG, SS>, smem);       \
             if (e != cudaSuccess) return e;                                                     \
-            return launch_pdl(k_partial_staged<DD, GG>, dim3(g), dim3(128), smem, s, a, units_layer); \
+            return launch_pdl(k_pivotal<DD, GG, SS>, dim3(g), dim3(PV_NT), smem, s, a, units_layer); \
         }
-        VERKV_PSTAGED(128, 1) VERKV_PSTAGED(128, 2) VERKV_PSTAGED(128, 4) VERKV_PSTAGED(128, 8)
-        VERKV_PSTAGED(64, 1) VERKV_PSTAGED(64, 2) VERKV_PSTAGED(64, 4) VERKV_PSTAGED(64, 8)
-#undef VERKV_PSTAGED
+        VERKV_PIVOTAL(128, 1, false) VERKV_PIVOTAL(128, 2, false) VERKV_PIVOTAL(128, 4, false) VERKV_PIVOTAL(128, 8, false)
+        VERKV_PIVOTAL(64, 1, false) VERKV_PIVOTAL(64, 2, false) VERKV_PIVOTAL(64, 4, false) VERKV_PIVOTAL(64, 8, false)
+        VERKV_PIVOTAL(128, 1, true) VERKV_PIVOTAL(128, 2, true) VERKV_PIVOTAL(128, 4, true) VERKV_PIVOTAL(128, 8, true)
+        VERKV_PIVOTAL(64, 1, true) VERKV_PIVOTAL(64, 2, true) VERKV_PIVOTAL(64, 4, true) VERKV_PIVOTAL(64, 8, true)
+#undef VERKV_PIVOTAL
         return cudaErrorInvalidValue;
     }
 #define VERKV_PART(DD, GG)                                                                      \
     if (a.d == DD && G == GG) {                                                                 \
-        if (a.mode == ROWS_PIVOTAL)                                                             \
-            return launch_pdl(k_partial<DD, GG, ROWS_PIVOTAL>, dim3(grid), dim3(128), 0, s, a, units_layer); \
-        if (a.mode == ROWS_STAGED)                                                              \
-            return launch_pdl(k_partial<DD, GG, ROWS_STAGED>, dim3(grid), dim3(128), 0, s, a, units_layer); \
-        return launch_pdl(k_partial<DD, GG, ROWS_HOST>, dim3(grid), dim3(128), 0, s, a, units_layer); \
+        if (a.mode == ROWS_PIVOTAL) {                                                           \
+            const size_t smem = PivLayout<DD>::BYTES;                                           \
+            if (skl) {                                                                          \
+                const cudaError_t e = ensure_smem((const void *)k_partial<DD, GG, ROWS_PIVOTAL, true>, smem); \
+                if (e != cudaSuccess) return e;                                                 \
+                return launch_pdl(k_partial<DD, GG, ROWS_PIVOTAL, true>, dim3(grid), dim3(128), smem, s, a, units_layer); \
+            }                                                                                   \
+            const cudaError_t e = ensure_smem((const void *)k_partial<DD, GG, ROWS_PIVOTAL, false>, smem); \
+            if (e != cudaSuccess) return e;                                                     \
+            return launch_pdl(k_partial<DD, GG, ROWS_PIVOTAL, false>, dim3(grid), dim3(128), smem, s, a, units_layer); \
+        }                                                                                       \
+        return launch_pdl(k_partial<DD, GG, ROWS_STAGED, false>, dim3(grid), dim3(128), 0, s, a, units_layer); \
     }
     VERKV_PART(128, 1) VERKV_PART(128, 2) VERKV_PART(128, 4) VERKV_PART(128, 8)
     VERKV_PART(64, 1) VERKV_PART(64, 2) VERKV_PART(64, 4) VERKV_PART(64, 8)
@@ -600,8 +635,9 @@ cudaError_t launch_merge(const MergeArgs &a, int qheads, cudaStream_t s) {
 // k_refine: the zero-copy path's partial sums in one launch -- the fetched-row ranges of every
 // layer unit first (so the host reads start at once), then its pivotal blocks (their HBM reads
 // hide behind the host link).  k_merge follows.
-template <int D, int G>
+template <int D, int G, bool SKL>
 __global__ void __launch_bounds__(128, 3) k_refine(PartialArgs piv, PartialArgs fet, int units_layer) {
+    extern __shared__ __align__(128) unsigned char kr_stage[];  // PivLayout<D>::BYTES
     pdl_wait();
     pdl_trigger();
     constexpr int WR = FET_RANGE / 32;  // bitmap words per range (one thread each)
@@ -653,11 +689,7 @@ __global__ void __launch_bounds__(128, 3) k_refine(PartialArgs piv, PartialArgs 
             __syncthreads();
             partial_rows<D, G, ROWS_HOST>(fet, ul, k, 0, cnt, s_ids, false);
         } else {
-            const int ch = k - fet.max_chunks;
-            const int count = min(piv.count[ug], piv.row_stride);
-            const int lo = ch * PIV_ITEM_ROWS;
-            partial_rows<D, G, ROWS_PIVOTAL>(piv, ul, ch, lo, min(lo + PIV_ITEM_ROWS, count),
-                                             piv.ids + (size_t)ug * piv.row_stride, false);
+            pivotal_chunk_plain<D, G, SKL>(piv, ul, k - fet.max_chunks, kr_stage);
         }
     }
 }
@@ -665,11 +697,26 @@ __global__ void __launch_bounds__(128, 3) k_refine(PartialArgs piv, PartialArgs 
 cudaError_t launch_refine(const PartialArgs &piv, const PartialArgs &fet, int units_layer, int grid,
                           cudaStream_t s) {
     const int G = piv.li.G;
-#define VERKV_REFINE(DD, GG)                                                                    \
-    if (piv.d == DD && G == GG)                                                                 \
-        return launch_pdl(k_refine<DD, GG>, dim3(grid), dim3(128), 0, s, piv, fet, units_layer);
-    VERKV_REFINE(128, 1) VERKV_REFINE(128, 2) VERKV_REFINE(128, 4) VERKV_REFINE(128, 8)
-    VERKV_REFINE(64, 1) VERKV_REFINE(64, 2) VERKV_REFINE(64, 4) VERKV_REFINE(64, 8)
+    const bool skl = piv.sketch_logits != 0;
+    int sms = 0, dev = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    // The grid: the CTAs that are resident at once (every CTA loops over its items).
+#define VERKV_REFINE(DD, GG, SS)                                                                \
+    if (piv.d == DD && G == GG && skl == SS) {                                                  \
+        const size_t smem = PivLayout<DD>::BYTES;                                               \
+        cudaError_t e = ensure_smem((const void *)k_refine<DD, GG, SS>, smem);                  \
+        if (e != cudaSuccess) return e;                                                         \
+        int per_sm = 0;                                                                         \
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k_refine<DD, GG, SS>, 128, smem); \
+        if (e != cudaSuccess) return e;                                                         \
+        const int g = std::max(1, std::min(grid, sms * std::max(per_sm, 1)));                   \
+        return launch_pdl(k_refine<DD, GG, SS>, dim3(g), dim3(128), smem, s, piv, fet, units_layer); \
+    }
+    VERKV_REFINE(128, 1, false) VERKV_REFINE(128, 2, false) VERKV_REFINE(128, 4, false) VERKV_REFINE(128, 8, false)
+    VERKV_REFINE(64, 1, false) VERKV_REFINE(64, 2, false) VERKV_REFINE(64, 4, false) VERKV_REFINE(64, 8, false)
+    VERKV_REFINE(128, 1, true) VERKV_REFINE(128, 2, true) VERKV_REFINE(128, 4, true) VERKV_REFINE(128, 8, true)
+    VERKV_REFINE(64, 1, true) VERKV_REFINE(64, 2, true) VERKV_REFINE(64, 4, true) VERKV_REFINE(64, 8, true)
 #undef VERKV_REFINE
     return cudaErrorInvalidValue;
 }

@@ -262,7 +262,7 @@ LayerIdx layer_idx(const verkv_ctx *ctx, int layer) {
 
 // Arguments of the pivotal partial sums of one layer call.
 PartialArgs pivotal_args(const verkv_ctx *ctx, const verkv_pivotal &piv, const void *q,
-                         const LayerIdx &li) {
+                         const LayerIdx &li, bool sketch_exact) {
     const int d = ctx->sh.head_dim;
     PartialArgs pa{};
     pa.rows = (const uint16_t *)piv.kv;
@@ -286,6 +286,7 @@ PartialArgs pivotal_args(const verkv_ctx *ctx, const verkv_pivotal &piv, const v
     pa.voff16 = d / 8;
     pa.scale = (float)(1.0 / sqrt((double)d));
     pa.li = li;
+    pa.sketch_logits = sketch_exact ? 0 : 1;
     return pa;
 }
 
@@ -583,7 +584,7 @@ verkv_status verkv_attend_verified(verkv_ctx *ctx, int32_t layer, const void *q,
     // The pivotal partial sums need only the selection: in MEMCPY mode they run here, during the
     // host gather; the zero-copy refine kernel of verkv_fetch_refine does them itself.
     if (ctx->fetch_mode != VERKV_FETCH_ZEROCOPY) {
-        const PartialArgs pa = pivotal_args(ctx, *pivotal, q, li);
+        const PartialArgs pa = pivotal_args(ctx, *pivotal, q, li, sketch->format == VERKV_SKETCH_EXACT);
         int grid = std::min(ctx->L.units_layer * ctx->L.max_piv, ctx->sms * 8);
         VERKV_CUDA(tracked(ctx, VERKV_K_PARTIAL_PIVOTAL, ctx->main, [&] { return launch_partial(pa, ctx->L.units_layer, std::max(grid, 1), ctx->main); }), "k_partial");
     }
@@ -672,7 +673,7 @@ verkv_status verkv_fetch_refine(verkv_ctx *ctx, const int32_t *ids, const int32_
         pa.resident = ctx->piv.resident;
         pa.nacc = ctx->nacc;
         ma.nacc = ctx->nacc;
-        const PartialArgs piv = pivotal_args(ctx, ctx->piv, ctx->q, li);
+        const PartialArgs piv = pivotal_args(ctx, ctx->piv, ctx->q, li, ctx->sketch_exact);
         const int items = ctx->L.units_layer * (ctx->L.max_fet + ctx->L.max_piv);
         grid = std::max(1, std::min(items, ctx->sms * 8));
         VERKV_CUDA(tracked(ctx, VERKV_K_FETCH_HOST, ctx->main, [&] {

@@ -153,8 +153,9 @@ size_t certify_smem_bytes(int chunk);
 // ---------------------------------------------------------------------------------------------
 // Shrinkage-weighted partial sums over a row set: the pivotal rows in HBM, fetched rows staged in
 // HBM, or fetched rows read by token id straight from page-locked host memory.
-constexpr int PART_ROWS = 64;                      // rows a CTA has in flight
-constexpr int PIV_ITEM_ROWS = PART_ROWS;           // pivotal list positions per partial
+constexpr int PART_ROWS = 64;                      // fetched rows a CTA has in flight
+constexpr int PIV_STAGE_ROWS = 64;                 // pivotal rows staged in shared memory at once
+constexpr int PIV_ITEM_ROWS = 128;                 // pivotal list positions per partial
 constexpr int FET_RANGE = 1024;                    // token ids per partial of fetched rows
 constexpr int RMASK_W = 131072 / FET_RANGE / 32;   // words of a unit's non-empty-range mask
                                                    // (n <= 131072)
@@ -183,6 +184,8 @@ struct PartialArgs {
     int max_chunks;
     int n, W, d;
     int mode;                 // ROWS_PIVOTAL (global units) / ROWS_STAGED / ROWS_HOST (layer units)
+    int sketch_logits;        // pivotal rows: lambda's w-hat from `scores` (a 2-bit sketch); 0: the
+                              // row's own weight (the exact sketch holds the same key)
     float scale;
     LayerIdx li;
 };
