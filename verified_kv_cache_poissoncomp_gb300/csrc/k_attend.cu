@@ -31,6 +31,8 @@
 //             the K|V rows read from page-locked host memory, online-softmax partials per chunk.
 #include <math.h>
 
+#include <cuda.h>
+
 #include <algorithm>
 
 #include "pivotal_mma.cuh"
@@ -271,8 +273,9 @@ __device__ __forceinline__ void cp_async16(void *dst, const void *src) {
 __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
 
 // The pivotal rows [ch PIV_ITEM_ROWS, ...) of layer unit `ul` into partial `ch`, staged by the
-// CTA's 128 threads with 16-byte asynchronous copies (stage rows beyond the unit's count are
-// zeros), PIV_STAGE_ROWS at a time in `buf` (PivLayout<D>::BYTES of shared memory).
+// CTA's 128 threads with 16-byte asynchronous copies into the swizzled stage layout (stage rows
+// beyond the unit's count are zeros), PIV_STAGE_ROWS at a time in `buf` (PivLayout<D>::BYTES of
+// shared memory, 16-byte aligned).
 template <int D, int G, bool SKL>
 __device__ __forceinline__ void pivotal_chunk_plain(const PartialArgs &a, int ul, int ch,
                                                     unsigned char *buf) {
@@ -291,8 +294,9 @@ __device__ __forceinline__ void pivotal_chunk_plain(const PartialArgs &a, int ul
     for (int s0 = lo; s0 < hi; s0 += LY::ROWS) {
         const int rows = min(LY::ROWS, hi - s0);
         for (int v = tid; v < LY::ROWS * VPR; v += 128) {
-            const int r = v / VPR, c = v - r * VPR;
-            unsigned char *dst = buf + r * LY::PITCH + c * 16;
+            const int r = v / VPR, c = v - r * VPR;  // c: 16-byte chunk of the K|V row
+            constexpr int KC = D / 8;                // chunks of a K (or V) row
+            unsigned char *dst = buf + LY::off(c / KC, r, (c % KC) * 8);
             if (r < rows) cp_async16(dst, src + (size_t)(s0 + r) * VPR + c);
             else *reinterpret_cast<uint4 *>(dst) = make_uint4(0u, 0u, 0u, 0u);
         }
@@ -359,30 +363,43 @@ __global__ void __launch_bounds__(128) k_partial(PartialArgs a, int units_layer)
 // k_pivotal: the estimator's pass over the pivotal set on its own (MEMCPY mode, where it runs
 // during the host gather).  Warps 0-3 consume, warp 4 produces: for every stage of PIV_STAGE_ROWS
 // rows of the CTA's chunks (blockIdx.x, blockIdx.x + gridDim.x, ...) the producer waits for the
-// ring slot to be released, then its lanes bulk-copy the rows one by one to their padded
-// positions, and the ids and r, all completing on the slot's mbarrier; the consumers run the
-// stage on the tensor cores and release the slot.  Waits are bounded: on expiry (or once another
-// thread has given up) the kernel keeps its control flow but skips the work, latches ERR_TIMEOUT,
-// waits (bounded) for the copies it issued and returns.
+// ring slot to be released, then issues one tensor copy per 64-channel box (the tensor map
+// describes the pivotal rows as [rows][K|V][d] bf16 with the 128-byte swizzle) and two bulk copies
+// for the ids and r, all completing on the slot's mbarrier; the consumers run the stage on the
+// tensor cores and release the slot.  Box rows past the unit's count hold other rows (or the
+// zero fill past the buffer); the consumer that owns them zeroes them before use.  Waits are
+// bounded: on expiry (or once another thread has given up) the kernel keeps its control flow but
+// skips the work, latches ERR_TIMEOUT, waits (bounded) for the copies it issued and returns.
 constexpr int PV_NS = 2;         // ring slots per CTA
 constexpr int PV_CONS = 4;       // consumer warps
 constexpr int PV_NT = 32 * (PV_CONS + 1);
 constexpr int PV_CTAS_PER_SM = 2;
 template <int D, int G>
 __host__ __device__ constexpr size_t pv_smem_bytes() {
-    return (size_t)PV_NS * PivLayout<D>::BYTES + piv_red_bytes<D, G>();
+    // 1024 bytes of slack: the ring starts at the first 1024-byte boundary (the swizzle's unit)
+    return 1024 + (size_t)PV_NS * PivLayout<D>::BYTES + piv_red_bytes<D, G>();
+}
+
+// Tensor copy of one box into shared memory, completing on `bar` (coordinates innermost first).
+__device__ __forceinline__ void tma_load_3d(void *dst, const CUtensorMap *map, int x, int y, int z,
+                                            uint64_t *bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes "
+        "[%0], [%1, {%2, %3, %4}], [%5];" ::"r"(smem_addr(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(smem_addr(bar))
+        : "memory");
 }
 
 template <int D, int G, bool SKL>
-__global__ void __launch_bounds__(PV_NT, PV_CTAS_PER_SM) k_pivotal(PartialArgs a, int units_layer) {
+__global__ void __launch_bounds__(PV_NT, PV_CTAS_PER_SM) k_pivotal(PartialArgs a, int units_layer,
+                                                                  const __grid_constant__ CUtensorMap rows_map) {
     using LY = PivLayout<D>;
-    extern __shared__ __align__(128) unsigned char pv_smem[];  // [PV_NS][LY::BYTES], reduction
+    extern __shared__ __align__(1024) unsigned char pv_raw[];
     __shared__ __align__(8) uint64_t full[PV_NS], empty[PV_NS];
     __shared__ int s_abort;
     __shared__ int s_last[PV_NS];  // the last stage issued into each slot (-1: none)
+    unsigned char *pv_smem = pv_raw + ((1024u - (smem_addr(pv_raw) & 1023u)) & 1023u);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    // Rows beyond a stage's count are read as zeros until a consumer writes them (finite values:
-    // their weights are zero, and 0 x finite adds nothing).
     for (int i = tid; i < PV_NS * LY::BYTES / 16; i += PV_NT)
         reinterpret_cast<uint4 *>(pv_smem)[i] = make_uint4(0u, 0u, 0u, 0u);
     if (tid == 0) {
@@ -394,7 +411,7 @@ __global__ void __launch_bounds__(PV_NT, PV_CTAS_PER_SM) k_pivotal(PartialArgs a
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         s_abort = 0;
     }
-    fence_proxy_async_smem();  // the zeros before any bulk copy into the same memory
+    fence_proxy_async_smem();  // the zeros before any copy into the same memory
     __syncthreads();
     pdl_wait();
     pdl_trigger();
@@ -402,6 +419,7 @@ __global__ void __launch_bounds__(PV_NT, PV_CTAS_PER_SM) k_pivotal(PartialArgs a
     const int total = units_layer * a.max_chunks;
     float *red = reinterpret_cast<float *>(pv_smem + PV_NS * LY::BYTES);
     if (warp == PV_CONS) {
+        if (lane == 0) asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&rows_map)) : "memory");
         int j = 0;
         for (int item = blockIdx.x; item < total; item += gridDim.x) {
             const int ul = item / a.max_chunks, ch = item - ul * a.max_chunks;
@@ -412,34 +430,29 @@ __global__ void __launch_bounds__(PV_NT, PV_CTAS_PER_SM) k_pivotal(PartialArgs a
             const int hi = min(lo + PIV_ITEM_ROWS, count);
             for (int s0 = lo; s0 < hi; s0 += LY::ROWS, ++j) {
                 const int slot = j % PV_NS;
+                if (lane != 0) continue;
                 bool go = *abort == 0;
-                if (go && j >= PV_NS) {
-                    bool w = true;
-                    if (lane == 0) w = mbar_wait_or_abort(&empty[slot], (uint32_t)(((j / PV_NS) - 1) & 1), abort);
-                    go = __shfl_sync(0xFFFFFFFFu, w ? 1 : 0, 0) != 0;
-                }
+                if (go && j >= PV_NS)
+                    go = mbar_wait_or_abort(&empty[slot], (uint32_t)(((j / PV_NS) - 1) & 1), abort);
                 if (!go) {
-                    if (lane == 0) *abort = 1;
+                    *abort = 1;
                     continue;
                 }
                 const int rows = min(LY::ROWS, hi - s0);
                 const uint32_t lb = (uint32_t)((rows + 3) & ~3) * 4;  // within the capacity (a multiple of 4)
                 unsigned char *st = pv_smem + (size_t)slot * LY::BYTES;
-                const size_t at = (size_t)ug * a.row_stride + s0;
-                if (lane == 0) {
-                    mbar_expect_tx(&full[slot], (uint32_t)rows * LY::ROWB + 2 * lb);
-                    s_last[slot] = j;
-                }
-                __syncwarp();
-                const unsigned char *src = reinterpret_cast<const unsigned char *>(a.rows) + at * LY::ROWB;
-                for (int r = lane; r < rows; r += 32)
-                    bulk_g2s(st + r * LY::PITCH, src + (size_t)r * LY::ROWB, LY::ROWB, &full[slot]);
-                if (lane == 0) {
-                    bulk_g2s(st + LY::IDS, a.ids + at, lb, &full[slot]);
-                    bulk_g2s(st + LY::RS, a.pr + at, lb, &full[slot]);
-                }
+                const int row_g = ug * a.row_stride + s0;  // row of the tensor map
+                mbar_expect_tx(&full[slot], (uint32_t)(LY::NB * LY::BOX) + 2 * lb);
+                s_last[slot] = j;
+#pragma unroll
+                for (int b = 0; b < LY::NB; ++b)
+                    tma_load_3d(st + b * LY::BOX, &rows_map, (b % LY::HALVES) * 64, b / LY::HALVES,
+                                row_g, &full[slot]);
+                bulk_g2s(st + LY::IDS, a.ids + row_g, lb, &full[slot]);
+                bulk_g2s(st + LY::RS, a.pr + row_g, lb, &full[slot]);
             }
         }
+        __syncwarp();
     } else {
         int j = 0;
         for (int item = blockIdx.x; item < total; item += gridDim.x) {
@@ -458,16 +471,14 @@ __global__ void __launch_bounds__(PV_NT, PV_CTAS_PER_SM) k_pivotal(PartialArgs a
                 unsigned char *st = pv_smem + (size_t)slot * LY::BYTES;
                 const int rows = min(LY::ROWS, hi - s0);
                 if (ok) {
-                    // This warp's rows beyond the count hold an earlier stage's data: zero them.
-                    for (int r = max(rows, warp * 16); r < warp * 16 + 16; ++r)
-                        for (int c = lane; c < LY::ROWB / 16; c += 32)
-                            reinterpret_cast<uint4 *>(st + r * LY::PITCH)[c] = make_uint4(0u, 0u, 0u, 0u);
+                    // This warp's rows past the count hold other rows: zero them.
+                    for (int r = max(rows, warp * 16); r < warp * 16 + 16; ++r) piv_zero_row<D>(st, r);
                     __syncwarp();
                     pc.stage(a, st, rows);
                 } else if (lane == 0) {
                     *abort = 1;
                 }
-                fence_proxy_async_smem();  // generic accesses before the slot's next bulk copy
+                fence_proxy_async_smem();  // generic accesses before the slot's next copy
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&empty[slot]);
             }
@@ -488,15 +499,45 @@ __global__ void __launch_bounds__(PV_NT, PV_CTAS_PER_SM) k_pivotal(PartialArgs a
     }
 }
 
+// The tensor map of a pivotal buffer: [rows][2][d] bf16 (rows = every unit's capacity), boxes of
+// 64 channels x 1 x 64 rows with the 128-byte swizzle.  cuTensorMapEncodeTiled is reached through
+// the runtime's driver entry point (no link against the driver library).
+typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                                  const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                                  const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+static cudaError_t pivotal_rows_map(CUtensorMap *map, const void *rows, long long nrows, int d) {
+    static EncodeTiledFn encode = nullptr;
+    if (!encode) {
+        void *fn = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        const cudaError_t e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000,
+                                                               cudaEnableDefault, &q);
+        if (e != cudaSuccess || q != cudaDriverEntryPointSuccess || !fn) return cudaErrorNotSupported;
+        encode = reinterpret_cast<EncodeTiledFn>(fn);
+    }
+    const cuuint64_t dims[3] = {(cuuint64_t)d, 2, (cuuint64_t)nrows};
+    const cuuint64_t strides[2] = {(cuuint64_t)d * 2, (cuuint64_t)d * 4};
+    const cuuint32_t box[3] = {64, 1, (cuuint32_t)PIV_STAGE_ROWS};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    const CUresult r = encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(rows), dims,
+                              strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                              CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
 cudaError_t launch_partial(const PartialArgs &a, int units_layer, int grid, cudaStream_t s) {
     const int G = a.li.G;
     int sms = 0, dev = 0;
     cudaGetDevice(&dev);
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    // Pivotal rows go through the pipelined kernel when every bulk copy it makes is 16-byte
-    // aligned, else through k_partial, which stages them with 16-byte asynchronous copies.
+    // Pivotal rows go through the pipelined kernel when every copy it makes is 16-byte aligned
+    // and the rows fit the tensor map's 32-bit coordinates, else through k_partial, which stages
+    // them with 16-byte asynchronous copies.
     const bool bulk = a.mode == ROWS_PIVOTAL && a.row16 == a.d / 4 && a.voff16 == a.d / 8 &&
                       !a.keys && (a.row_stride & 3) == 0 &&
+                      (long long)a.units_total * a.row_stride <= 0x7FFFFFFFLL &&  // map coordinates
                       (reinterpret_cast<uintptr_t>(a.rows) & 15) == 0 &&
                       (reinterpret_cast<uintptr_t>(a.ids) & 15) == 0 &&
                       (reinterpret_cast<uintptr_t>(a.pr) & 15) == 0;
@@ -504,12 +545,15 @@ cudaError_t launch_partial(const PartialArgs &a, int units_layer, int grid, cuda
     if (bulk) {
         const int total = units_layer * a.max_chunks;
         const int g = std::max(1, std::min(total, sms * PV_CTAS_PER_SM));
+        CUtensorMap map;
+        const cudaError_t me = pivotal_rows_map(&map, a.rows, (long long)a.units_total * a.row_stride, a.d);
+        if (me != cudaSuccess) return me;
 #define VERKV_PIVOTAL(DD, GG, SS)                                                               \
         if (a.d == DD && G == GG && skl == SS) {                                                \
             const size_t smem = pv_smem_bytes<DD, GG>();                                        \
             const cudaError_t e = ensure_smem((const void *)k_pivotal<DD, GG, SS>, smem);       \
             if (e != cudaSuccess) return e;                                                     \
-            return launch_pdl(k_pivotal<DD, GG, SS>, dim3(g), dim3(PV_NT), smem, s, a, units_layer); \
+            return launch_pdl(k_pivotal<DD, GG, SS>, dim3(g), dim3(PV_NT), smem, s, a, units_layer, map); \
         }
         VERKV_PIVOTAL(128, 1, false) VERKV_PIVOTAL(128, 2, false) VERKV_PIVOTAL(128, 4, false) VERKV_PIVOTAL(128, 8, false)
         VERKV_PIVOTAL(64, 1, false) VERKV_PIVOTAL(64, 2, false) VERKV_PIVOTAL(64, 4, false) VERKV_PIVOTAL(64, 8, false)

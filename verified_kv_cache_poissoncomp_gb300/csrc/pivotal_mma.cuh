@@ -3,20 +3,10 @@
 // with weight 1 on H and on tokens of F, lambda_i / r_i on sampled, unfetched tokens).
 //
 // A pivotal row is 4d bytes (K then V, bf16).  Rows are staged in shared memory PIV_STAGE_ROWS at a
-// time at a padded pitch of 4d + 16 bytes, so that the eight rows of an 8x8 ldmatrix tile fall in
-// eight different 16-byte bank groups.  Per stage, consumer warp w takes rows 16w .. 16w + 15:
-//   1. S = K Q^T with mma.m16n8k16 (bf16 in, f32 accumulate): M = the warp's 16 rows, N = 8 query
-//      heads (G <= 8; columns >= G are zero), K = d in steps of 16.  A comes from the staged K rows
-//      by ldmatrix, B (the query heads) stays in registers for the whole chunk.
-//   2. Each accumulator element (row, head) becomes its weight: w = exp(s / sqrt(d) - m_head), times
-//      1 for H and F, or lambda / r = clip(beta / (w-hat (1 - r)), 1, 1 / r) for a sampled,
-//      unfetched token.  With the exact sketch w-hat is the row's own weight (the sketch holds the
-//      same bf16 key, so the logits agree up to float32 summation order); with the 2-bit sketch it
-//      comes from the certificate's sketch logits.  D-hat and the second moment add in float32.
-//   3. The weights are split into bf16 hi + lo (hi = bf16(w), lo = bf16(w - hi): about 2^-17
-//      relative error) and transposed in registers with movmatrix into the B operand of
-//      O^T += V^T P^T: M = 16 channels per tile, N = 8 heads, K = the warp's 16 rows, A = the staged
-//      V rows by ldmatrix.trans.  Two MMAs per tile (hi, then lo).
+// time, in boxes of 64 rows x 64 channels (128 bytes a row) -- K channels 0-63, (64-127,) then V
+// the same -- with the 128-byte swizzle of the tensor-memory-access unit: the 16-byte chunk c of
+// box row r sits at chunk c xor (r mod 8), so the eight rows of an 8x8 ldmatrix tile fall in eight
+// different bank groups.  Per stage, consumer warp w takes rows 16w .. 16w + 15:
 // After the chunk's stages, the four warps' O^T tiles and sums are added in warp order through
 // shared memory into one partial [G][d + 2] (N-hat, D-hat, second moment).  Every path that sums
 // pivotal rows (the pipelined MEMCPY-mode kernel, the zero-copy refine, the unaligned fallback)
@@ -68,17 +58,35 @@ __device__ __forceinline__ float bf16_lo_f(uint32_t x) { return __uint_as_float(
 __device__ __forceinline__ float bf16_hi_f(uint32_t x) { return __uint_as_float(x & 0xFFFF0000u); }
 
 // ---------------------------------------------------------------------------------------------
-// Shared-memory stage: PIV_STAGE_ROWS rows at PITCH bytes, then the rows' token ids and r.
+// Shared-memory stage: NB boxes of 64 rows x 128 bytes (swizzled), then the rows' token ids and r;
+// stages are a multiple of 1024 bytes so that every box keeps the swizzle's 1024-byte alignment.
 template <int D>
 struct PivLayout {
-    static constexpr int ROWB = 4 * D;        // a K|V row
-    static constexpr int PITCH = ROWB + 16;   // padded: conflict-free ldmatrix
+    static constexpr int ROWB = 4 * D;        // a K|V row in global memory
     static constexpr int ROWS = PIV_STAGE_ROWS;
-    static constexpr int IDS = ROWS * PITCH;  // int32 [ROWS]
+    static constexpr int HALVES = D / 64;     // 64-channel boxes per K (or V) row
+    static constexpr int NB = 2 * HALVES;     // boxes per stage
+    static constexpr int BOX = ROWS * 128;    // bytes per box
+    static constexpr int IDS = NB * BOX;      // int32 [ROWS]
     static constexpr int RS = IDS + ROWS * 4; // float [ROWS]
-    static constexpr int BYTES = RS + ROWS * 4;
-    static_assert(BYTES % 16 == 0, "stages start on 16-byte boundaries");
+    static constexpr int BYTES = (RS + ROWS * 4 + 1023) / 1024 * 1024;
+    static_assert(ROWS == 64 && D % 64 == 0, "boxes of 64 rows x 64 channels");
+    // Byte offset of channels c .. c + 7 (c a multiple of 8) of row r of part p (0 K, 1 V).
+    __host__ __device__ static constexpr int off(int p, int r, int c) {
+        return (p * HALVES + c / 64) * BOX + r * 128 + ((((c % 64) >> 3) ^ (r & 7)) << 4);
+    }
 };
+// Zero row r of a stage (every box's 128-byte line of it), with the 32 lanes of a warp.
+template <int D>
+__device__ __forceinline__ void piv_zero_row(unsigned char *st, int r) {
+    using LY = PivLayout<D>;
+    const int lane = threadIdx.x & 31;
+    if (lane < LY::NB * 8) {
+        uint4 *line = reinterpret_cast<uint4 *>(st + (lane >> 3) * LY::BOX + r * 128);
+        line[lane & 7] = make_uint4(0u, 0u, 0u, 0u);
+    }
+}
+
 // Bytes of the chunk-end reduction: [4 warps][G][D] floats, then [4 warps][G][2].
 template <int D, int G>
 __host__ __device__ constexpr int piv_red_bytes() { return 4 * G * D * 4 + 4 * G * 2 * 4; }
@@ -164,18 +172,21 @@ struct PivChunk {
                 if (SKL) shat[e] = __ldcg(sh[hk] + id[k]);
             }
         }
-        // 1. S = K Q^T for the warp's 16 rows.
+        // 1. S = K Q^T for the warp's 16 rows (even and odd k-steps in two accumulators).
         const uint32_t base = smem_addr(st);
         float c[4] = {0.0f, 0.0f, 0.0f, 0.0f};
         {
+            float c1[4] = {0.0f, 0.0f, 0.0f, 0.0f};
             const int mi = lane >> 3, ri = lane & 7;  // ldmatrix: tile mi, row ri of it
-            const uint32_t arow = base + (uint32_t)((row0 + (mi & 1) * 8 + ri) * LY::PITCH + (mi >> 1) * 16);
+            const int ar = row0 + (mi & 1) * 8 + ri;
 #pragma unroll
             for (int ks = 0; ks < KS; ++ks) {
                 uint32_t af[4];
-                ldsm_x4(af, arow + ks * 32);
-                mma_bf16(c, af, qb[ks][0], qb[ks][1]);
+                ldsm_x4(af, base + (uint32_t)LY::off(0, ar, ks * 16 + (mi >> 1) * 8));
+                mma_bf16((ks & 1) ? c1 : c, af, qb[ks][0], qb[ks][1]);
             }
+#pragma unroll
+            for (int e = 0; e < 4; ++e) c[e] += c1[e];
         }
         // 2. The weight of each (row, head) element: c[e] is row g + 8 (e >> 1), head 2t + (e & 1).
         const float scale = a.scale;
@@ -212,11 +223,11 @@ struct PivChunk {
         {
             // ldmatrix.trans: tile mi covers rows 8 (mi >> 1) .. + 7 and channels 8 (mi & 1) .. + 7
             const int mi = lane >> 3, ri = lane & 7;
-            const uint32_t vrow = base + (uint32_t)((row0 + (mi >> 1) * 8 + ri) * LY::PITCH + 2 * D + (mi & 1) * 16);
+            const int vr = row0 + (mi >> 1) * 8 + ri;
 #pragma unroll
             for (int mt = 0; mt < KS; ++mt) {
                 uint32_t vf[4];
-                ldsm_x4_t(vf, vrow + mt * 32);
+                ldsm_x4_t(vf, base + (uint32_t)LY::off(1, vr, mt * 16 + (mi & 1) * 8));
                 mma_bf16(acc[mt], vf, bh0, bh1);
                 mma_bf16(acc[mt], vf, bl0, bl1);
             }

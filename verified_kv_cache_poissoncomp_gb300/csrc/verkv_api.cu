@@ -276,6 +276,7 @@ PartialArgs pivotal_args(const verkv_ctx *ctx, const verkv_pivotal &piv, const v
     pa.part = ctx->part_piv;
     pa.err = ctx->err;
     pa.row_stride = ctx->sh.cap;
+    pa.units_total = ctx->sh.batch * ctx->sh.layers * ctx->sh.kv_heads;
     pa.max_chunks = ctx->L.max_piv;
     pa.n = ctx->sh.n;
     pa.W = ctx->L.W;

@@ -181,6 +181,7 @@ struct PartialArgs {
     uint32_t *rmask;          // fetched-row ranges: bit k of [units_layer][RMASK_W] set when
                               // range k holds rows (only those get a partial); zero on entry
     int row_stride;           // cap (pivotal) or n (fetched)
+    int units_total;          // pivotal: units of the whole shape (rows of `rows` = units_total * cap)
     int max_chunks;
     int n, W, d;
     int mode;                 // ROWS_PIVOTAL (global units) / ROWS_STAGED / ROWS_HOST (layer units)
