@@ -362,7 +362,7 @@ __global__ void __launch_bounds__(128) k_partial(PartialArgs a, int units_layer)
 
 // k_pivotal: the estimator's pass over the pivotal set on its own (MEMCPY mode, where it runs
 // during the host gather).  Warps 0-3 consume, warp 4 produces: for every stage of PIV_STAGE_ROWS
-// rows of the CTA's chunks (blockIdx.x, blockIdx.x + gridDim.x, ...) the producer waits for the
+// rows of the CTA's chunks (a contiguous run of them) the producer waits for the
 // ring slot to be released, then issues one tensor copy per 64-channel box (the tensor map
 // describes the pivotal rows as [rows][K|V][d] bf16 with the 128-byte swizzle) and two bulk copies
 // for the ids and r, all completing on the slot's mbarrier; the consumers run the stage on the
@@ -373,11 +373,13 @@ __global__ void __launch_bounds__(128) k_partial(PartialArgs a, int units_layer)
 constexpr int PV_NS = 2;         // ring slots per CTA
 constexpr int PV_CONS = 4;       // consumer warps
 constexpr int PV_NT = 32 * (PV_CONS + 1);
-constexpr int PV_CTAS_PER_SM = 2;
+constexpr int PV_CTAS_PER_SM = 3;
 template <int D, int G>
 __host__ __device__ constexpr size_t pv_smem_bytes() {
-    // 1024 bytes of slack: the ring starts at the first 1024-byte boundary (the swizzle's unit)
-    return 1024 + (size_t)PV_NS * PivLayout<D>::BYTES + piv_red_bytes<D, G>();
+    // 1024 bytes of slack: the ring starts at the first 1024-byte boundary (the swizzle's unit).
+    // The chunk-end reduction runs in the ring slot of the chunk's last stage.
+    static_assert(piv_red_bytes<D, G>() <= PivLayout<D>::BYTES, "the reduction fits a slot");
+    return 1024 + (size_t)PV_NS * PivLayout<D>::BYTES;
 }
 
 // Tensor copy of one box into shared memory, completing on `bar` (coordinates innermost first).
@@ -416,15 +418,20 @@ __global__ void __launch_bounds__(PV_NT, PV_CTAS_PER_SM) k_pivotal(PartialArgs a
     pdl_wait();
     pdl_trigger();
     volatile int *abort = &s_abort;
+    // A contiguous run of items per CTA: consecutive chunks of a unit share its queries.
     const int total = units_layer * a.max_chunks;
-    float *red = reinterpret_cast<float *>(pv_smem + PV_NS * LY::BYTES);
+    const int per = (total + gridDim.x - 1) / gridDim.x;
+    const int item0 = min(total, (int)blockIdx.x * per), item1 = min(total, item0 + per);
     if (warp == PV_CONS) {
         if (lane == 0) asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&rows_map)) : "memory");
-        int j = 0;
-        for (int item = blockIdx.x; item < total; item += gridDim.x) {
+        int j = 0, cur = -1, ug = 0, count = 0;
+        for (int item = item0; item < item1; ++item) {
             const int ul = item / a.max_chunks, ch = item - ul * a.max_chunks;
-            const int ug = a.li.unit_global(ul);
-            const int count = min(a.count[ug], a.row_stride);
+            if (ul != cur) {
+                cur = ul;
+                ug = a.li.unit_global(ul);
+                count = min(a.count[ug], a.row_stride);
+            }
             const int lo = ch * PIV_ITEM_ROWS;
             if (lo >= count) continue;
             const int hi = min(lo + PIV_ITEM_ROWS, count);
@@ -454,16 +461,20 @@ __global__ void __launch_bounds__(PV_NT, PV_CTAS_PER_SM) k_pivotal(PartialArgs a
         }
         __syncwarp();
     } else {
-        int j = 0;
-        for (int item = blockIdx.x; item < total; item += gridDim.x) {
+        int j = 0, cur = -1, count = 0;
+        PivChunk<D, G, SKL> pc;
+        for (int item = item0; item < item1; ++item) {
             const int ul = item / a.max_chunks, ch = item - ul * a.max_chunks;
-            const int ug = a.li.unit_global(ul);
-            const int count = min(a.count[ug], a.row_stride);
+            if (ul != cur) {  // the unit's queries and head values, once per unit
+                cur = ul;
+                count = min(a.count[a.li.unit_global(ul)], a.row_stride);
+                pc.load_unit(a, ul);
+            }
             const int lo = ch * PIV_ITEM_ROWS;
             if (lo >= count) continue;
             const int hi = min(lo + PIV_ITEM_ROWS, count);
-            PivChunk<D, G, SKL> pc;
-            pc.init(a, ul);
+            pc.reset();
+            auto cons_bar = [] { asm volatile("bar.sync 1, %0;" ::"n"(32 * PV_CONS) : "memory"); };
             for (int s0 = lo; s0 < hi; s0 += LY::ROWS, ++j) {
                 const int slot = j % PV_NS;
                 bool ok = *abort == 0 && mbar_wait_or_abort(&full[slot], (uint32_t)((j / PV_NS) & 1), abort);
@@ -478,12 +489,18 @@ __global__ void __launch_bounds__(PV_NT, PV_CTAS_PER_SM) k_pivotal(PartialArgs a
                 } else if (lane == 0) {
                     *abort = 1;
                 }
+                if (s0 + LY::ROWS >= hi) {
+                    // The chunk's last stage: its slot holds the reduction once all four warps
+                    // are done with the rows.
+                    cons_bar();
+                    pc.finish(reinterpret_cast<float *>(st),
+                              a.part + ((size_t)ul * a.max_chunks + ch) * G * (D + 2), *abort == 0,
+                              cons_bar);
+                }
                 fence_proxy_async_smem();  // generic accesses before the slot's next copy
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&empty[slot]);
             }
-            pc.finish(red, a.part + ((size_t)ul * a.max_chunks + ch) * G * (D + 2), *abort == 0,
-                      [] { asm volatile("bar.sync 1, %0;" ::"n"(32 * PV_CONS) : "memory"); });
         }
     }
     __syncthreads();

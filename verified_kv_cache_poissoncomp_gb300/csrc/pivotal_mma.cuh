@@ -102,7 +102,8 @@ struct PivChunk {
     const uint32_t *Fh[2];             // selection bitmaps of heads 2t, 2t+1
     const float *sh[2];                // their sketch logits (2-bit sketch only)
 
-    __device__ __forceinline__ void init(const PartialArgs &a, int ul) {
+    // The unit's query fragments and per-head values (a chunk of another unit needs them anew).
+    __device__ __forceinline__ void load_unit(const PartialArgs &a, int ul) {
         const int lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
         const int b = ul / a.li.kv_heads, h = ul - b * a.li.kv_heads;
         const int hq = a.li.kv_heads * G;
@@ -113,14 +114,8 @@ struct PivChunk {
             qb[ks][1] = g < G ? qrow[ks * 8 + 4 + t] : 0u;
         }
 #pragma unroll
-        for (int mt = 0; mt < KS; ++mt)
-#pragma unroll
-            for (int e = 0; e < 4; ++e) acc[mt][e] = 0.0f;
-#pragma unroll
         for (int k = 0; k < 2; ++k) {
             const int hd = 2 * t + k;
-            dsum[k] = 0.0f;
-            m2[k] = 0.0f;
             mh[k] = 0.0f;
             bh[k] = 0.0f;
             Fh[k] = a.F;
@@ -133,6 +128,22 @@ struct PivChunk {
                 if (SKL) sh[k] = a.scores + (size_t)qh * a.n;
             }
         }
+    }
+    // Zero sums for a new chunk.
+    __device__ __forceinline__ void reset() {
+#pragma unroll
+        for (int mt = 0; mt < KS; ++mt)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) acc[mt][e] = 0.0f;
+#pragma unroll
+        for (int k = 0; k < 2; ++k) {
+            dsum[k] = 0.0f;
+            m2[k] = 0.0f;
+        }
+    }
+    __device__ __forceinline__ void init(const PartialArgs &a, int ul) {
+        load_unit(a, ul);
+        reset();
     }
 
     // One stage of `rows` (<= PIV_STAGE_ROWS) rows at `st` (shared memory), this warp's 16 rows.
@@ -189,7 +200,17 @@ struct PivChunk {
             for (int e = 0; e < 4; ++e) c[e] += c1[e];
         }
         // 2. The weight of each (row, head) element: c[e] is row g + 8 (e >> 1), head 2t + (e & 1).
+        //    For a sampled, unfetched token the weight is (lambda / r) w with
+        //    lambda / r = clip(beta / (w-hat (1 - r)), 1, 1 / r); with the exact sketch (w-hat = w)
+        //    that is min(w / r, max(w, beta / (1 - r))), so 1 / r and 1 / (1 - r) are taken once
+        //    per row and no element divides.  1 / r when w-hat underflows (lambda = 1).
         const float scale = a.scale;
+        float ir[2], i1r[2];
+#pragma unroll
+        for (int k = 0; k < 2; ++k) {
+            ir[k] = __fdividef(1.0f, rr[k]);
+            i1r[k] = __fdividef(1.0f, 1.0f - rr[k]);
+        }
         float cw[4];
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
@@ -201,13 +222,13 @@ struct PivChunk {
                 const bool inF = (fw[e] >> (id[k] & 31)) & 1u;
                 float v = w;
                 if (r < 1.0f && !inF) {
-                    // lambda / r = clip(beta / (w-hat (1 - r)), 1, 1 / r); 1 / r when w-hat
-                    // underflows (lambda = 1)
-                    const float wh = SKL ? __expf(shat[e] - mh[hk]) : w;
-                    const float ir = __frcp_rn(r);
-                    float coef = ir;
-                    if (wh > 0.0f) coef = fminf(ir, fmaxf(1.0f, __fdividef(bh[hk], wh * (1.0f - r))));
-                    v = coef * w;
+                    const float lo = bh[hk] * i1r[k];  // beta / (1 - r)
+                    if (SKL) {
+                        const float wh = __expf(shat[e] - mh[hk]);
+                        v = wh > 0.0f ? w * fminf(ir[k], fmaxf(1.0f, __fdividef(lo, wh))) : w * ir[k];
+                    } else {
+                        v = w > 0.0f ? fminf(w * ir[k], fmaxf(w, lo)) : 0.0f;
+                    }
                     m2[hk] = fmaf(v * v, 1.0f - r, m2[hk]);
                 }
                 cw[e] = v;

@@ -155,7 +155,7 @@ size_t certify_smem_bytes(int chunk);
 // HBM, or fetched rows read by token id straight from page-locked host memory.
 constexpr int PART_ROWS = 64;                      // fetched rows a CTA has in flight
 constexpr int PIV_STAGE_ROWS = 64;                 // pivotal rows staged in shared memory at once
-constexpr int PIV_ITEM_ROWS = 128;                 // pivotal list positions per partial
+constexpr int PIV_ITEM_ROWS = 256;                 // pivotal list positions per partial
 constexpr int FET_RANGE = 1024;                    // token ids per partial of fetched rows
 constexpr int RMASK_W = 131072 / FET_RANGE / 32;   // words of a unit's non-empty-range mask
                                                    // (n <= 131072)
