@@ -48,6 +48,8 @@ def parse_args():
     p.add_argument("--no-graph", action="store_true", help="launch eagerly instead of graph replay")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--no-extra", action="store_true",
+                   help="skip the estimator-pass and MEMCPY-fetch measurements of the default run")
     p.add_argument("--queries", type=int, default=QUERIES)
     p.add_argument("--eps-sweep", action="store_true",
                    help="tolerance sweep: throughput and host-traffic statistics per eps")
@@ -175,30 +177,68 @@ class ClockSampler:
 
 
 # ------------------------------------------------------------------------------------------------
-def cpu_baseline(w, pcs_layer0_time=None):
-    """Time the oracle, as it stands, on a bounded sample of the workload (one thread)."""
+def cpu_baseline(w):
+    """Time the oracle, as it stands, on a bounded sample of the workload: on one thread, and on
+    every host core (a thread per core: the oracle's C routines run outside the interpreter lock,
+    over independent (query, KV head) units and PoissonComp heads).  A quarter of the sampled
+    queries are planted, as in the workload.  Scaled to a step of LAYERS layers' PoissonComp +
+    QUERIES queries."""
+    import concurrent.futures as cf
+
     import oracle as O
 
-    t0 = time.perf_counter()
+    cores = os.cpu_count() or 1
+    planted = [t for t in range(w.queries.shape[0]) if w.planted[t]]
+    plain = [t for t in range(w.queries.shape[0]) if not w.planted[t]]
+    KV = {(l, h): (O.bf16_to_f64(w.kv[0, l, h, :, 0, :]), O.bf16_to_f64(w.kv[0, l, h, :, 1, :]))
+          for l in range(LAYERS) for h in range(w.h_kv)}
+
+    def pc(l, h):
+        return O.poissoncomp(w.tau[0, l, h], w.eta, w.n_sink, w.n_local, w.seed, 0, l, h)
+
     pcs = {}
-    for h in range(w.h_kv):
-        pcs[h] = O.poissoncomp(w.tau[0, 0, h], w.eta, w.n_sink, w.n_local, w.seed, 0, 0, h)
-    t_pc_layer = time.perf_counter() - t0
-    sample = [t for t in range(w.queries.shape[0]) if w.query_layer[t] == 0][:8]
+
+    def unit(t, h):
+        l = int(w.query_layer[t])
+        K, V = KV[(l, h)]
+        qs = O.bf16_to_f64(w.queries[t, 0, h * w.G:(h + 1) * w.G])
+        O.attend_unit(qs, K, K, V, pcs[(l, h)]["r32"], pcs[(l, h)]["resident"], w.eps, w.delta)
+
+    # one thread: PoissonComp of every head; 6 plain and 2 planted queries
     t0 = time.perf_counter()
-    for t in sample:
+    for l in range(LAYERS):
         for h in range(w.h_kv):
-            K = O.bf16_to_f64(w.kv[0, 0, h, :, 0, :])
-            V = O.bf16_to_f64(w.kv[0, 0, h, :, 1, :])
-            qs = O.bf16_to_f64(w.queries[t, 0, h * w.G:(h + 1) * w.G])
-            O.attend_unit(qs, K, K, V, pcs[h]["r32"], pcs[h]["resident"], w.eps, w.delta)
-    t_q = (time.perf_counter() - t0) / len(sample)
-    step_s = LAYERS * t_pc_layer + QUERIES * t_q
-    return {"value": QUERIES / step_s, "unit": UNIT, "cores": 1, "kind": "oracle",
-            "sample": f"PoissonComp of 1 layer (8 heads) + {len(sample)} queries "
-                      f"({int(w.planted[sample].sum())} planted) of layer 0, single thread; "
+            pcs[(l, h)] = pc(l, h)
+    t_pc1 = time.perf_counter() - t0                            # all heads of LAYERS layers
+    sample1 = plain[:6] + planted[:2]
+    t0 = time.perf_counter()
+    for t in sample1:
+        for h in range(w.h_kv):
+            unit(t, h)
+    t_q1 = (time.perf_counter() - t0) / len(sample1)            # per query
+    # every core: PoissonComp of all heads again; 2 x cores queries, a quarter planted
+    nq = max(8, 2 * cores)
+    sampleN = plain[:nq - nq // 4] + planted[:nq // 4]
+    with cf.ThreadPoolExecutor(max_workers=cores) as ex:
+        t0 = time.perf_counter()
+        list(ex.map(lambda lh: pc(*lh), [(l, h) for l in range(LAYERS) for h in range(w.h_kv)]))
+        t_pcN = time.perf_counter() - t0
+        t0 = time.perf_counter()
+        list(ex.map(lambda th: unit(*th), [(t, h) for t in sampleN for h in range(w.h_kv)]))
+        t_qN = (time.perf_counter() - t0) / len(sampleN)        # per query
+    step1 = t_pc1 + QUERIES * t_q1
+    stepN = t_pcN + QUERIES * t_qN
+    return {"value": QUERIES / stepN, "unit": UNIT, "cores": cores, "kind": "oracle",
+            "sample": f"all {cores} host cores (a thread each): PoissonComp of {LAYERS} layers x "
+                      f"{w.h_kv} heads and {len(sampleN)} queries "
+                      f"({sum(1 for t in sampleN if w.planted[t])} planted), 32 query heads each; "
                       f"scaled to a step of {LAYERS} layers' PoissonComp + {QUERIES} queries",
-            "seconds": t_pc_layer + t_q * len(sample)}
+            "seconds": round(t_pcN + t_qN * len(sampleN), 2),
+            "single_thread": {"value": QUERIES / step1, "cores": 1,
+                              "sample": f"PoissonComp of {LAYERS} layers x {w.h_kv} heads + "
+                                        f"{len(sample1)} queries "
+                                        f"({sum(1 for t in sample1 if w.planted[t])} planted)",
+                              "seconds": round(t_pc1 + t_q1 * len(sample1), 2)}}
 
 
 def run_reference(args, world, rank):
@@ -331,7 +371,7 @@ def run_ours(args, world, rank, local):
         step()
         B.verkv_sync(eng.ctx)
         after = B.verkv_launch_counts(eng.ctx)
-    launches_per_step = int(sum(a - b for a, b in zip(after, before)))
+    launches_per_step = int(sum(after[k] - before[k] for k in B.KERNEL_IDS))
 
     graph = None
     if not args.no_graph and mode == B.VERKV_FETCH_ZEROCOPY:
@@ -514,6 +554,14 @@ def run_ours(args, world, rank, local):
                "d2h_bytes_per_step": int(o_host.nbytes + lse_host.nbytes + st_host.nbytes),
                "steps": e2e_steps, "launch": "eager C-ABI calls"}
 
+    # The estimator pass on its own (its HBM fraction at 32K, batch 32) and the MEMCPY fetch path
+    # on this workload (copy rate against the link, overlap with the pivotal sums): one GPU only.
+    memcpy = None
+    if rank == 0 and world == 1 and not args.no_extra:
+        est = measure_estimator(32, 10, 3, dev)
+        rooflines["k_partial(pivotal)"] = dict(est["roofline"], workload=est["workload"])
+        memcpy = measure_memcpy_fetch(w, None, q_dev, 32, dev, link)
+
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cpu = cpu_baseline(w)
@@ -536,7 +584,8 @@ def run_ours(args, world, rank, local):
                "roofline": roof, "roofline_hbm": roof_hbm, "rooflines": rooflines,
                "per_kernel_us": {
                    k: round(v["avg_us"], 3) for k, v in per_kernel.items()},
-               "fetch_stats": fetch_stats, "fetch": fetch, "clocks": clk.summary(),
+               "fetch_stats": fetch_stats, "fetch": fetch, "memcpy_fetch": memcpy,
+               "clocks": clk.summary(),
                "gpu_launches": launches_per_step * args.steps,
                "launches_per_step": launches_per_step,
                "e2e": e2e, "cpu_baseline": cpu}
@@ -945,25 +994,22 @@ def estimator_bytes(count, pivotal_r, d, G, sketch_logits=False):
     return int(np.sum(count)) * (4 * d + 8) + (n_l * 4 * G if sketch_logits else 0), n_l
 
 
-def run_estimator(args, local):
-    """One GPU: the shrinkage-estimator attention over the pivotal set (D-hat, N-hat and the
-    second moment), timed alone.  In MEMCPY fetch mode the pivotal sums are their own launch,
-    k_partial(pivotal); in zero-copy mode the same item code runs inside k_refine behind the host
-    reads.  Workload: the decode-step cache generator at batch 32 (--est-batch) x 8 KV heads x 4 query heads,
-    d = 128, n = 32768, eta = 1/16, H = 4 + 512, eps = delta = 0.05; one layer call of 1024 query
-    heads per step, eager (the MEMCPY path waits on the host for the selection).  The pivotal rows
-    (~270 MB a call) are larger than L2, and k_score streams 2 GB of sketch before each pass.
-    One JSON line."""
+def measure_estimator(batch, steps, warmup, dev):
+    """The shrinkage-estimator attention over the pivotal set (D-hat, N-hat and the second
+    moment), timed alone: in MEMCPY fetch mode the pivotal sums are their own launch,
+    k_partial(pivotal) (in zero-copy mode the same stage code runs inside k_refine behind the host
+    reads).  Workload: the decode-step cache generator at `batch` sequences x 8 KV heads x 4
+    query heads, d = 128, n = 32768, eta = 1/16, H = 4 + 512, eps = delta = 0.05; one layer call
+    of batch x 32 query heads per step, eager (the MEMCPY path waits on the host for the
+    selection).  The pivotal rows (~270 MB a call at batch 32) are larger than L2, and k_score
+    streams the sketch (2 GB at batch 32) before each pass.  Returns a dict."""
     import torch
 
     from verified_kv_cache_poissoncomp_gb300 import binding as B
     from verified_kv_cache_poissoncomp_gb300 import inputs as I
     from verified_kv_cache_poissoncomp_gb300.engine import VerKV, default_cap
 
-    B.lib()
-    torch.cuda.set_device(local)
-    dev = torch.device("cuda", local)
-    batch, layers, kvh, G, d, n, eta = args.est_batch, 1, 8, 4, 128, 32768, 1 / 16
+    layers, kvh, G, d, n, eta = 1, 8, 4, 128, 32768, 1 / 16
     units = batch * layers * kvh
     peak, peak_src = measured_peaks()
     stream = torch.cuda.Stream(dev)
@@ -989,11 +1035,11 @@ def run_estimator(args, local):
             B.verkv_fetch_refine(eng.ctx, None, None, eng.host_kv.data_ptr(), o.data_ptr(),
                                  lse.data_ptr(), st.data_ptr())
 
-        for _ in range(args.warmup):
+        for _ in range(warmup):
             step()
         B.verkv_sync(eng.ctx)
         B.verkv_profile_enable(eng.ctx, 1)
-        for _ in range(args.steps):
+        for _ in range(steps):
             step()
         launches, total_ms = B.verkv_profile_read(eng.ctx)
         B.verkv_profile_enable(eng.ctx, 0)
@@ -1003,21 +1049,122 @@ def run_estimator(args, local):
     k = B.VERKV_K_PARTIAL_PIVOTAL
     us = 1e3 * total_ms[k] / max(launches[k], 1)
     gbs = nbytes / (us * 1e-6) / 1e9
-    print(json.dumps({
-        "workload": "estimator", "unit": "GB/s", "steps": args.steps, "warmup": args.warmup,
-        "data": "synthetic",
-        "config": {"workload": f"shrinkage-estimator pass over the pivotal set: batch {batch} x 8 "
-                               "KV heads x 4 query heads, d=128, n=32768, bf16, eta=1/16, "
-                               "H=4+512, eps=delta=0.05, MEMCPY fetch mode, eager",
-                   "l2": "pivotal rows larger than L2; the sketch stream flushes it each pass"},
+    eng.close()
+    del eng, tau, kv, host_kv, queries
+    torch.cuda.empty_cache()
+    return {
+        "workload": f"shrinkage-estimator pass over the pivotal set: batch {batch} x 8 KV heads x "
+                    "4 query heads, d=128, n=32768, bf16, eta=1/16, H=4+512, eps=delta=0.05, "
+                    "MEMCPY fetch mode (the pass is its own launch), eager",
+        "l2": "pivotal rows larger than L2; the sketch stream flushes it each pass",
         "kernel": "k_partial(pivotal)", "launches": int(launches[k]), "avg_us": round(us, 3),
         "pivotal_rows_per_call": int(cnt.sum()), "sampled_rows_per_call": n_l,
-        "algorithmic_bytes_per_launch": nbytes,
         "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": peak, "unit": "GB/s",
-                     "frac": round(gbs / peak, 4), "peak_source": peak_src},
+                     "frac": round(gbs / peak, 4), "avg_us": round(us, 3),
+                     "algorithmic_bytes_per_launch": nbytes,
+                     "traffic": traffic_for("k_partial(pivotal)"), "peak_source": peak_src},
         "per_kernel_us": {B.verkv_kernel_name(j): round(1e3 * total_ms[j] / launches[j], 2)
-                          for j in range(B.VERKV_K_COUNT) if launches[j] > 0}}), flush=True)
+                          for j in range(B.VERKV_K_COUNT) if launches[j] > 0}}
+
+
+def measure_memcpy_fetch(w, pcs_unused, queries, steps_q, dev, link):
+    """The benchmark spec's literal fetch path on the benchmark workload: VERKV_FETCH_MEMCPY (the host
+    waits for the selection, host threads gather the selected V rows into page-locked staging,
+    cudaMemcpyAsync moves them on the side stream, then the staged rows are summed).  Eager calls
+    over `steps_q` queries with per-launch events on both streams; per query the pivotal sums
+    (main stream) against the gather and the copies (side stream).  Returns a dict."""
+    import torch
+
+    from verified_kv_cache_poissoncomp_gb300 import binding as B
+    from verified_kv_cache_poissoncomp_gb300.engine import VerKV, default_cap
+
+    stream = torch.cuda.Stream(dev)
+    Q = min(steps_q, queries.shape[0])
+    hq = w.B * w.h_kv * w.G
+    with torch.cuda.stream(stream):
+        eng = VerKV(w.B, w.L, w.h_kv, w.G, w.d, w.n, default_cap(w.n, w.eta),
+                    fetch_mode=B.VERKV_FETCH_MEMCPY)
+        eng.load(w.tau.reshape(-1, w.n), w.kv.reshape(-1, w.n, 2, w.d))
+        eng.compress(w.eta, w.n_sink, w.n_local, w.seed)
+        eng.sync()
+        o = torch.empty((hq, w.d), dtype=torch.float32, device=dev)
+        counts = torch.zeros((w.B * w.h_kv,), dtype=torch.int32, device=dev)
+
+        def query(t):
+            B.verkv_attend_verified(eng.ctx, int(w.query_layer[t]), queries[t].data_ptr(),
+                                    eng.pivotal, eng.r_full.data_ptr(), eng.sketch_desc, w.eps,
+                                    w.delta, None, counts.data_ptr())
+            B.verkv_fetch_refine(eng.ctx, None, counts.data_ptr(), eng.host_kv.data_ptr(),
+                                 o.data_ptr(), None, None)
+
+        for t in range(4):
+            query(t)
+        B.verkv_sync(eng.ctx)
+        torch.cuda.synchronize()
+        rows = 0
+        piv, gat, cop, call = [], [], [], []
+        t0 = time.perf_counter()
+        B.verkv_profile_enable(eng.ctx, 1)
+        for t in range(Q):
+            query(t)
+            recs = B.verkv_profile_timeline(eng.ctx)
+            rows += int(counts.cpu().numpy().sum())
+            by = {}
+            for kid, a, b in recs:
+                by.setdefault(kid, []).append((a, b))
+            piv.append(by[B.VERKV_K_PARTIAL_PIVOTAL][0])
+            gat.append(by[B.VERKV_K_FETCH_GATHER][0])
+            cop.append(by.get(B.VERKV_K_FETCH_COPY, [(0.0, 0.0)])[0])
+            call.append((recs[0][1], recs[-1][2]))
+            B.verkv_profile_read(eng.ctx)  # discard the records
+        wall = time.perf_counter() - t0
+        B.verkv_profile_enable(eng.ctx, 0)
+        B.verkv_sync(eng.ctx)
     eng.close()
+    row_bytes = 2 * w.d  # V rows: the exact sketch holds the keys
+    copy_ms = sum(b - a for a, b in cop)
+    gather_ms = sum(b - a for a, b in gat)
+    piv_ms = sum(b - a for a, b in piv)
+    # the pivotal sums (main stream) overlapped with the fetch: gather start .. copies' end
+    overlap_ms = sum(max(0.0, min(pb, cb) - max(pa, ga))
+                     for (pa, pb), (ga, _), (_, cb) in zip(piv, gat, cop))
+    h2d = rows * row_bytes
+    return {
+        "workload": "the benchmark workload (single-layer 32K, batch 1) in VERKV_FETCH_MEMCPY mode, "
+                    f"{Q} queries, eager calls with events on both streams",
+        "h2d_bytes": int(h2d), "copy_ms": round(copy_ms, 3),
+        "copy_GBs": round(h2d / (copy_ms * 1e-3) / 1e9, 1) if copy_ms > 0 else None,
+        "link_peak_GBs": round(link, 1),
+        "copy_frac_of_link": round(h2d / (copy_ms * 1e-3) / 1e9 / link, 4) if copy_ms > 0 else None,
+        "gather_ms": round(gather_ms, 3),
+        "gather_GBs": round(h2d / (gather_ms * 1e-3) / 1e9, 1) if gather_ms > 0 else None,
+        "pivotal_sums_ms": round(piv_ms, 3),
+        "pivotal_sums_overlapped_with_fetch_ms": round(overlap_ms, 3),
+        "pivotal_sums_overlap_frac": round(overlap_ms / piv_ms, 4) if piv_ms > 0 else None,
+        "gpu_ms_per_query": round(sum(b - a for a, b in call) / Q, 4),
+        "queries_per_s_eager": round(Q / wall, 1),
+        "note": "per query: k_partial(pivotal) on the main stream starts when the selection is done; "
+                "the host gather (bracketed by events on the idle side stream) and the side-stream "
+                "copies run meanwhile; overlap = time the pivotal sums ran inside [gather start, "
+                "copies end]"}
+
+
+def run_estimator(args, local):
+    """One GPU: the shrinkage-estimator pass over the pivotal set alone (measure_estimator at
+    --est-batch).  One JSON line."""
+    import torch
+
+    from verified_kv_cache_poissoncomp_gb300 import binding as B
+
+    B.lib()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    r = measure_estimator(args.est_batch, args.steps, args.warmup, dev)
+    print(json.dumps({"workload": "estimator", "unit": "GB/s", "steps": args.steps,
+                      "warmup": args.warmup, "data": "synthetic",
+                      "config": {"workload": r["workload"], "l2": r["l2"]}, **{
+                          k: v for k, v in r.items() if k not in ("workload", "l2")}}),
+          flush=True)
 
 
 def run_dense_offload(args, local):

@@ -307,6 +307,22 @@ verkv_status verkv_certify_noalloc(int device, void *stream, int32_t units, int3
                                    verkv_head_stats *stats_out, uint32_t *F_out,
                                    uint32_t *err_out);
 
+/* Failure injection, for tests of the error paths (each affects only this context; nothing
+ * faults, traps or hangs the GPU):
+ *   VERKV_INJECT_COPY_FAIL   value > 0: the next `value` MEMCPY-mode fetch copies fail on the host
+ *                            without reaching CUDA, and verkv_fetch_refine returns VERKV_ECOPY
+ *   VERKV_INJECT_BETA_MAXIT  value >= 1: the beta solve stops after `value` passes (a head that
+ *                            needs more is flagged and verkv_sync returns VERKV_ENOCONVERGE);
+ *                            0 restores the default cap
+ *   VERKV_INJECT_SCORE_STALL value >= 1000: in the next verkv_attend_verified the first CTA of the
+ *                            sketch-scoring kernel arms its first copy barrier for a copy it never
+ *                            issues, and its bounded copy waits give up after `value` ns; the
+ *                            kernel latches VERKV_ETIMEOUT (returned by verkv_sync) and returns,
+ *                            and the context stays usable.  One call only.
+ * Returns VERKV_EINVAL for an unknown `what` or a value out of range. */
+enum { VERKV_INJECT_COPY_FAIL = 1, VERKV_INJECT_BETA_MAXIT = 2, VERKV_INJECT_SCORE_STALL = 3 };
+verkv_status verkv_test_inject(verkv_ctx *ctx, int what, int64_t value);
+
 /* Measurement.  Every kernel launch is counted per kernel; with profiling enabled each launch is
  * also bracketed by two CUDA events on the stream it runs on (host cost ~2 event records).
  * Kernel ids, in launch order: */
@@ -326,6 +342,12 @@ enum {
     VERKV_K_DENSE_HOST,        /* offloaded-dense baseline: all rows from host    */
     VERKV_K_DENSE_MERGE,       /* its running-max merge                           */
     VERKV_K_SHORTLIST,         /* per-KV-head fetch shortlist (when enabled)      */
+    VERKV_K_FETCH_COPY,        /* MEMCPY mode: the side stream's host-to-device
+                                  copies of one fetch (not a kernel; timed with
+                                  events on the side stream when profiling)       */
+    VERKV_K_FETCH_GATHER,      /* MEMCPY mode: the host threads' gather of the
+                                  fetched rows into page-locked staging (events on
+                                  the idle side stream mark its start and end)    */
     VERKV_K_COUNT
 };
 
@@ -336,6 +358,14 @@ verkv_status verkv_profile_enable(verkv_ctx *ctx, int on);
  * milliseconds per kernel id into launches[VERKV_K_COUNT] and total_ms[VERKV_K_COUNT]
  * (caller-zeroed host arrays) and discard the records. */
 verkv_status verkv_profile_read(verkv_ctx *ctx, int64_t *launches, double *total_ms);
+
+/* The recorded launches since the last verkv_profile_read, in record order, without discarding
+ * them: kernel id and start / end in milliseconds from the first record's start event (host
+ * arrays of max_records entries; *n_out the number written, at most max_records).  Waits for the
+ * context's streams.  With MEMCPY mode this shows the side stream's copies (VERKV_K_FETCH_COPY)
+ * against the pivotal sums on the main stream (VERKV_K_PARTIAL_PIVOTAL). */
+verkv_status verkv_profile_timeline(verkv_ctx *ctx, int64_t max_records, int32_t *kernel,
+                                    double *start_ms, double *end_ms, int64_t *n_out);
 
 /* Kernel launches issued by this context since it was created, per kernel id
  * (out[VERKV_K_COUNT], host).  Counts launches made during stream capture once. */

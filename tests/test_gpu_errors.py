@@ -104,3 +104,85 @@ def test_misaligned_pointers_are_rejected_before_launch():
     eng.fetch_refine()
     eng.sync()
     eng.close()
+
+
+def _query_ok(eng, w, t, pcs):
+    """One query through the context, checked against the oracle: the context is usable."""
+    g = P.gpu_query(eng, w, t)
+    P.compare_query(g, P.oracle_query(w, t, pcs), w)
+
+
+def test_fetch_copy_failure_is_reported_and_the_context_recovers():
+    # A host-side failure of the MEMCPY fetch's copy (injected before it reaches CUDA) comes back
+    # as VERKV_ECOPY from verkv_fetch_refine; the next decode call on the context succeeds.
+    w = I.tiny()
+    eng = P.make_engine(w, fetch_mode=B.VERKV_FETCH_MEMCPY)
+    eng.compress(w.eta, w.n_sink, w.n_local, w.seed)
+    eng.sync()
+    pcs = P.oracle_poissoncomp(w)
+    t = int(np.nonzero(w.planted)[0][0])  # a planted query: its certificate fails, rows move
+    B.verkv_test_inject(eng.ctx, B.VERKV_INJECT_COPY_FAIL, 1)
+    q = torch.as_tensor(w.queries[t].view(np.int16)).to(eng.dev)
+    eng.attend(int(w.query_layer[t]), q, w.eps, w.delta)
+    with pytest.raises(B.VerkvError) as e:
+        eng.fetch_refine()
+    assert e.value.status == B.VERKV_ECOPY
+    assert B.verkv_sync_status(eng.ctx) == B.VERKV_OK
+    _query_ok(eng, w, t, pcs)
+    eng.close()
+
+
+def test_beta_iteration_cap_is_reported_and_can_be_lifted():
+    # With the beta solve capped at one pass, heads that need more are flagged (stats flags & 1)
+    # and verkv_sync returns VERKV_ENOCONVERGE; the default cap gives results at the parity bar.
+    w = I.tiny()
+    eng = P.make_engine(w)
+    eng.compress(w.eta, w.n_sink, w.n_local, w.seed)
+    eng.sync()
+    pcs = P.oracle_poissoncomp(w)
+    B.verkv_test_inject(eng.ctx, B.VERKV_INJECT_BETA_MAXIT, 1)
+    flagged = 0
+    for t in range(w.queries.shape[0]):
+        q = torch.as_tensor(w.queries[t].view(np.int16)).to(eng.dev)
+        eng.attend(int(w.query_layer[t]), q, w.eps, w.delta)
+        _, _, st = eng.fetch_refine()
+        status = B.verkv_sync_status(eng.ctx)
+        f = int((st.cpu().numpy()[:, 15] & 1).sum())
+        assert status == (B.VERKV_ENOCONVERGE if f else B.VERKV_OK), (t, status, f)
+        flagged += f
+    assert flagged > 0
+    B.verkv_test_inject(eng.ctx, B.VERKV_INJECT_BETA_MAXIT, 0)
+    for t in range(4):
+        _query_ok(eng, w, t, pcs)
+    eng.close()
+
+
+def test_bounded_copy_wait_expiry_is_reported_and_the_context_recovers():
+    # The scoring kernel's first CTA arms a copy barrier for a copy it never issues; its bounded
+    # wait gives up after 2 ms, the kernel latches VERKV_ETIMEOUT and returns (no trap, no fault),
+    # verkv_sync reports it, and the next call on the same context meets the parity bar.
+    w = I.tiny()
+    eng = P.make_engine(w)
+    eng.compress(w.eta, w.n_sink, w.n_local, w.seed)
+    eng.sync()
+    pcs = P.oracle_poissoncomp(w)
+    B.verkv_test_inject(eng.ctx, B.VERKV_INJECT_SCORE_STALL, 2_000_000)
+    q = torch.as_tensor(w.queries[0].view(np.int16)).to(eng.dev)
+    eng.attend(0, q, w.eps, w.delta)
+    eng.fetch_refine()
+    assert B.verkv_sync_status(eng.ctx) == B.VERKV_ETIMEOUT
+    assert B.verkv_sync_status(eng.ctx) == B.VERKV_OK  # cleared
+    for t in range(4):
+        _query_ok(eng, w, t, pcs)
+    eng.close()
+
+
+def test_injection_arguments_are_checked():
+    w = I.tiny()
+    eng = P.make_engine(w)
+    for what, value in [(0, 1), (B.VERKV_INJECT_COPY_FAIL, -1), (B.VERKV_INJECT_BETA_MAXIT, 65),
+                        (B.VERKV_INJECT_SCORE_STALL, 10)]:
+        with pytest.raises(B.VerkvError) as e:
+            B.verkv_test_inject(eng.ctx, what, value)
+        assert e.value.status == B.VERKV_EINVAL
+    eng.close()

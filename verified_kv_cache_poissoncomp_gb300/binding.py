@@ -33,11 +33,16 @@ EXPORTED = ["verkv_sketch_bytes", "verkv_workspace_size", "verkv_create", "verkv
             "verkv_fetch_refine", "verkv_selection_bitmap", "verkv_profile_enable",
             "verkv_profile_read", "verkv_launch_counts", "verkv_kernel_name", "verkv_sync",
             "verkv_last_error", "verkv_status_string", "verkv_certify_noalloc",
-            "verkv_attend_dense_host", "verkv_set_shortlist", "verkv_shortlist_bitmap"]
+            "verkv_attend_dense_host", "verkv_set_shortlist", "verkv_shortlist_bitmap",
+            "verkv_profile_timeline", "verkv_test_inject"]
+VERKV_INJECT_COPY_FAIL, VERKV_INJECT_BETA_MAXIT, VERKV_INJECT_SCORE_STALL = 1, 2, 3
 # kernel ids (include/verkv.h), in launch order
 (VERKV_K_PC_SOLVE, VERKV_K_PC_GATHER, VERKV_K_SKETCH, VERKV_K_SCORE, VERKV_K_CERTIFY,
  VERKV_K_PARTIAL_PIVOTAL, VERKV_K_FETCH_HOST, VERKV_K_PARTIAL_STAGED, VERKV_K_MERGE,
- VERKV_K_DENSE_HOST, VERKV_K_DENSE_MERGE, VERKV_K_SHORTLIST, VERKV_K_COUNT) = range(13)
+ VERKV_K_DENSE_HOST, VERKV_K_DENSE_MERGE, VERKV_K_SHORTLIST, VERKV_K_FETCH_COPY,
+ VERKV_K_FETCH_GATHER, VERKV_K_COUNT) = range(15)
+# ids that are kernels (the last two time the MEMCPY fetch's copies and host gather)
+KERNEL_IDS = [k for k in range(VERKV_K_COUNT) if k not in (VERKV_K_FETCH_COPY, VERKV_K_FETCH_GATHER)]
 
 
 class verkv_shape(ctypes.Structure):
@@ -124,6 +129,10 @@ def lib():
         L.verkv_profile_enable.restype = ctypes.c_int
         L.verkv_profile_read.argtypes = [vp, vp, vp]
         L.verkv_profile_read.restype = ctypes.c_int
+        L.verkv_profile_timeline.argtypes = [vp, ctypes.c_int64, vp, vp, vp, vp]
+        L.verkv_profile_timeline.restype = ctypes.c_int
+        L.verkv_test_inject.argtypes = [vp, ctypes.c_int, ctypes.c_int64]
+        L.verkv_test_inject.restype = ctypes.c_int
         L.verkv_launch_counts.argtypes = [vp, vp]
         L.verkv_launch_counts.restype = ctypes.c_int
         L.verkv_kernel_name.argtypes = [ctypes.c_int]
@@ -225,6 +234,24 @@ def verkv_profile_read(ctx):
     _check(lib().verkv_profile_read(ctx, ctypes.cast(n, ctypes.c_void_p),
                                     ctypes.cast(t, ctypes.c_void_p)), ctx)
     return list(n), list(t)
+
+
+def verkv_profile_timeline(ctx, max_records=1 << 16):
+    """-> list of (kernel id, start ms, end ms) of the launches recorded since the last
+    verkv_profile_read, times from the first record's start; the records are kept."""
+    k = (ctypes.c_int32 * max_records)()
+    a = (ctypes.c_double * max_records)()
+    b = (ctypes.c_double * max_records)()
+    n = ctypes.c_int64()
+    _check(lib().verkv_profile_timeline(ctx, max_records, ctypes.cast(k, ctypes.c_void_p),
+                                        ctypes.cast(a, ctypes.c_void_p),
+                                        ctypes.cast(b, ctypes.c_void_p), ctypes.byref(n)), ctx)
+    return [(int(k[i]), float(a[i]), float(b[i])) for i in range(n.value)]
+
+
+def verkv_test_inject(ctx, what, value):
+    """Failure injection for tests (VERKV_INJECT_*; see include/verkv.h)."""
+    _check(lib().verkv_test_inject(ctx, int(what), int(value)), ctx)
 
 
 def verkv_launch_counts(ctx):

@@ -155,9 +155,10 @@ __device__ __forceinline__ void partial_rows(const PartialArgs &a, int ul, int p
         for (int c = 0; c < 8; ++c) acc[g][c] = 0.0f;
     float dacc = 0.0f;
 
-    // ROWS_HOST indexes the full host cache of the unit by token id; ROWS_STAGED by position.
+    // ROWS_HOST indexes the full host cache of the unit by token id; ROWS_STAGED by position
+    // from the unit's first staged row.
     const uint4 *rows = reinterpret_cast<const uint4 *>(a.rows) +
-                        (MODE == ROWS_HOST ? (size_t)ug * a.n : (size_t)ul * a.row_stride) * a.row16;
+                        (MODE == ROWS_HOST ? (size_t)ug * a.n : (size_t)a.staged_off[ul]) * a.row16;
     const uint4 *keys = a.keys ? reinterpret_cast<const uint4 *>(a.keys) + (size_t)ug * a.n * (D / 8)
                                : nullptr;
 #pragma unroll 1

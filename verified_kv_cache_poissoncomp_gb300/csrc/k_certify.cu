@@ -645,7 +645,8 @@ __global__ void __launch_bounds__(CT_NT, 1) k_certify(CertifyArgs a) {
         iters = 1;
         if (!found) {
             beta = (start > lo && start < hi) ? start : ((lo > 0.0f) ? sqrtf(lo) * sqrtf(hi) : hi * 0.0625f);
-            for (iters = 2; iters <= BETA_MAXIT; ++iters) {
+            const int maxit = a.beta_maxit > 0 ? a.beta_maxit : BETA_MAXIT;
+            for (iters = 2; iters <= maxit; ++iters) {
                 float ab = 0.f, S = 0.f, pl = 0.f, ph = INFINITY;
                 for (int i = tid; i < chunk; i += CT_NT) {
                     const float r = R[i];
@@ -677,8 +678,8 @@ __global__ void __launch_bounds__(CT_NT, 1) k_certify(CertifyArgs a) {
                 beta = nb;
                 if ((hi - lo) <= 1e-6f * hi) break;
             }
-            if (iters > BETA_MAXIT) {
-                iters = BETA_MAXIT;
+            if (iters > maxit) {
+                iters = maxit;
                 flags = 1;
             }
         }

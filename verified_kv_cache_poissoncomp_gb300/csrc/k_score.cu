@@ -135,6 +135,7 @@ __global__ void __launch_bounds__(SC_NT, SC_CTAS_PER_SM) k_score(ScoreArgs a, in
         const uint32_t bytes = (uint32_t)rows_k * ROWB;
         uint64_t *bar = &full[k % SC_STAGES];
         mbar_expect_tx(bar, bytes);
+        if (a.stall_first && blockIdx.x == 0 && k == 0) return;  // test injection: never issued
         bulk_g2s(ring + (size_t)(k % SC_STAGES) * SC_ROWS * ROWB, src + (size_t)k * SC_ROWS * ROWB,
                  bytes, bar);
     };
@@ -143,10 +144,11 @@ __global__ void __launch_bounds__(SC_NT, SC_CTAS_PER_SM) k_score(ScoreArgs a, in
     pdl_wait();
 
     float *out = a.scores + (size_t)ul * G * a.n + row0;
+    const unsigned long long wait_ns = a.wait_ns ? a.wait_ns : TMA_WAIT_NS;
     int consumed = 0;
     for (int k = 0; k < nst; ++k) {
         const uint32_t parity = (uint32_t)((k / SC_STAGES) & 1);
-        if (!mbar_wait_bounded(&full[k % SC_STAGES], parity)) s_abort = 1;
+        if (!mbar_wait_bounded(&full[k % SC_STAGES], parity, wait_ns)) s_abort = 1;
         __syncthreads();
         if (s_abort) break;
         consumed = k + 1;
@@ -188,7 +190,7 @@ __global__ void __launch_bounds__(SC_NT, SC_CTAS_PER_SM) k_score(ScoreArgs a, in
             raise_error(a.err, ERR_TIMEOUT);
             const int issued = min(nst, consumed + SC_STAGES);
             for (int k = consumed; k < issued; ++k)
-                mbar_wait_bounded(&full[k % SC_STAGES], (uint32_t)((k / SC_STAGES) & 1));
+                mbar_wait_bounded(&full[k % SC_STAGES], (uint32_t)((k / SC_STAGES) & 1), wait_ns);
         }
         __syncthreads();
     }
@@ -292,6 +294,7 @@ __global__ void __launch_bounds__(SC_NT, SC_CTAS_PER_SM) k_score_q2(ScoreArgs a,
         const uint32_t bytes = (uint32_t)rows_k * ROWB;
         uint64_t *bar = &full[k % SC_STAGES];
         mbar_expect_tx(bar, bytes);
+        if (a.stall_first && blockIdx.x == 0 && k == 0) return;  // test injection: never issued
         bulk_g2s(ring + (size_t)(k % SC_STAGES) * SQ_ROWS * ROWB, src + (size_t)k * SQ_ROWS * ROWB,
                  bytes, bar);
     };
@@ -300,10 +303,11 @@ __global__ void __launch_bounds__(SC_NT, SC_CTAS_PER_SM) k_score_q2(ScoreArgs a,
     pdl_wait();
 
     float *out = a.scores + (size_t)ul * G * a.n + row0;
+    const unsigned long long wait_ns = a.wait_ns ? a.wait_ns : TMA_WAIT_NS;
     int consumed = 0;
     for (int k = 0; k < nst; ++k) {
         const uint32_t parity = (uint32_t)((k / SC_STAGES) & 1);
-        if (!mbar_wait_bounded(&full[k % SC_STAGES], parity)) s_abort = 1;
+        if (!mbar_wait_bounded(&full[k % SC_STAGES], parity, wait_ns)) s_abort = 1;
         __syncthreads();
         if (s_abort) break;
         consumed = k + 1;
@@ -347,7 +351,7 @@ __global__ void __launch_bounds__(SC_NT, SC_CTAS_PER_SM) k_score_q2(ScoreArgs a,
             raise_error(a.err, ERR_TIMEOUT);
             const int issued = min(nst, consumed + SC_STAGES);
             for (int k = consumed; k < issued; ++k)
-                mbar_wait_bounded(&full[k % SC_STAGES], (uint32_t)((k / SC_STAGES) & 1));
+                mbar_wait_bounded(&full[k % SC_STAGES], (uint32_t)((k / SC_STAGES) & 1), wait_ns);
         }
         __syncthreads();
     }

@@ -15,11 +15,20 @@
 #include <thread>
 #include <vector>
 
+#include <nvtx3/nvToolsExt.h>
+
 #include "verkv_internal.h"
 
 using namespace verkv;
 
 namespace {
+
+// An NVTX range for the lifetime of the object: each stage of the hot path shows up by name on a
+// profiler's timeline (the calls cost nothing without a tool attached).
+struct NvtxRange {
+    explicit NvtxRange(const char *name) { nvtxRangePushA(name); }
+    ~NvtxRange() { nvtxRangePop(); }
+};
 
 size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 
@@ -33,6 +42,14 @@ struct Layout {
     size_t err, flc, nacc, rmask, scores, qstats, F, slb, fids, fcounts, staging, part_piv, part_fet, total;
     int W, units_layer, qh_layer, max_piv, max_fet, dense_chunks;
 };
+
+// MEMCPY-mode staging (page-locked on the host and its device copy): a header of the layer
+// units' first staged rows (int64, 256-byte aligned), then the fetched rows of every unit,
+// contiguous and unit by unit, so that one copy moves a whole fetch.
+size_t staging_header(int units_layer) { return align256((size_t)units_layer * 8); }
+size_t staging_bytes(int units_layer, size_t n, size_t d) {
+    return staging_header(units_layer) + (size_t)units_layer * n * 4 * d;
+}
 
 bool valid_shape(const verkv_shape *s) {
     if (!s) return false;
@@ -68,7 +85,7 @@ bool make_layout(const verkv_shape *s, Layout &L) {
     L.slb = take((size_t)L.units_layer * L.W * 4);
     L.fids = take((size_t)L.units_layer * n * 4);
     L.fcounts = take((size_t)L.units_layer * 4);
-    L.staging = take((size_t)L.units_layer * n * 4 * d);
+    L.staging = take(staging_bytes(L.units_layer, n, d));
     L.part_piv = take((size_t)L.units_layer * L.max_piv * G * (d + 2) * 4);
     L.part_fet = take((size_t)L.units_layer * L.dense_chunks * G * (d + 2) * 4);
     L.total = off;
@@ -198,6 +215,10 @@ struct verkv_ctx {
     const void *sketch = nullptr;
     bool sketch_exact = true;  // format of the preceding attend's sketch
     std::string last_error;
+    // Failure injection (verkv_test_inject)
+    int64_t inject_copy_fail = 0;    // fetch copies still to fail on the host
+    int beta_maxit = 0;              // 0: the kernel's default cap
+    int64_t score_stall_ns = 0;      // > 0: the next attend's scoring kernel stalls one stage
     // Measurement
     int64_t launches[VERKV_K_COUNT] = {};
     bool prof_on = false;
@@ -289,6 +310,15 @@ PartialArgs pivotal_args(const verkv_ctx *ctx, const verkv_pivotal &piv, const v
     pa.li = li;
     pa.sketch_logits = sketch_exact ? 0 : 1;
     return pa;
+}
+
+// One host-to-device copy of the MEMCPY-mode fetch, on the side stream (or an injected failure).
+cudaError_t copy_rows(verkv_ctx *ctx, void *dst, const void *src, size_t bytes) {
+    if (ctx->inject_copy_fail > 0) {
+        --ctx->inject_copy_fail;
+        return cudaErrorInvalidValue;
+    }
+    return cudaMemcpyAsync(dst, src, bytes, cudaMemcpyHostToDevice, ctx->side);
 }
 
 }  // namespace
@@ -399,7 +429,8 @@ verkv_status verkv_set_fetch_mode(verkv_ctx *ctx, int mode_flags) {
     if (mode == VERKV_FETCH_MEMCPY && !ctx->host_staging) {
         const size_t rows = (size_t)ctx->L.units_layer * ctx->sh.n;
         VERKV_CUDA(cudaSetDevice(ctx->device), "cudaSetDevice");
-        VERKV_CUDA(cudaHostAlloc((void **)&ctx->host_staging, rows * 4 * ctx->sh.head_dim,
+        VERKV_CUDA(cudaHostAlloc((void **)&ctx->host_staging,
+                                 staging_bytes(ctx->L.units_layer, ctx->sh.n, ctx->sh.head_dim),
                                  cudaHostAllocDefault), "cudaHostAlloc(staging)");
         VERKV_CUDA(cudaHostAlloc((void **)&ctx->host_ids, rows * 4, cudaHostAllocMapped),
                    "cudaHostAlloc(ids)");
@@ -432,6 +463,7 @@ verkv_status verkv_poissoncomp(verkv_ctx *ctx, const float *tau, double eta, ver
     const double b_rest = eta_n - (double)forced;
     if (n_rest > 0 && !(b_rest > 0.0))
         return fail(ctx, VERKV_EBUDGET, "poissoncomp: eta * n must exceed the forced H set");
+    const NvtxRange nvtx("verkv_poissoncomp");
     if (bad16(kv_full) || bad16(out->kv) || bad4(tau) || bad4(r_full) || bad4(out->ids) ||
         bad4(out->r) || bad4(out->count) || bad4(out->resident) || bad4(out->c))
         return fail(ctx, VERKV_EINVAL, "poissoncomp: kv rows need 16-byte, other arrays 4-byte alignment");
@@ -516,6 +548,7 @@ verkv_status verkv_attend_verified(verkv_ctx *ctx, int32_t layer, const void *q,
         bad4(pivotal->resident) || bad4(fetch_ids_out) || bad4(fetch_counts_out))
         return fail(ctx, VERKV_EINVAL, "attend: int32 / float arrays need 4-byte alignment");
     VERKV_CUDA(cudaSetDevice(ctx->device), "cudaSetDevice");
+    const NvtxRange nvtx("verkv_attend_verified: score, certificate, selection");
     const LayerIdx li = layer_idx(ctx, layer);
     const int n = ctx->sh.n, d = ctx->sh.head_dim;
 
@@ -528,6 +561,11 @@ verkv_status verkv_attend_verified(verkv_ctx *ctx, int32_t layer, const void *q,
     sa.d = d;
     sa.scale = (float)(1.0 / sqrt((double)d));
     sa.li = li;
+    if (ctx->score_stall_ns > 0) {  // injected: one stalled stage, a short wait limit
+        sa.wait_ns = (unsigned long long)ctx->score_stall_ns;
+        sa.stall_first = 1;
+        ctx->score_stall_ns = 0;
+    }
     if (sketch->format == VERKV_SKETCH_Q2) {
         VERKV_CUDA(tracked(ctx, VERKV_K_SCORE, ctx->main, [&] { return launch_score_q2(sa, ctx->L.units_layer, ctx->main, false); }), "k_score_q2");
     } else {
@@ -562,6 +600,7 @@ verkv_status verkv_attend_verified(verkv_ctx *ctx, int32_t layer, const void *q,
     ca.eps = eps;
     ca.ldelta = (float)log(2.0 / (double)delta);
     ca.li = li;
+    ca.beta_maxit = ctx->beta_maxit;
     // The per-KV-head fetch list is built only for those who read it: the MEMCPY gather, or a
     // caller asking for ids or counts.  The zero-copy refine reads the selection bitmaps.
     const bool need_list = ctx->fetch_mode != VERKV_FETCH_ZEROCOPY || fetch_ids_out || fetch_counts_out;
@@ -613,6 +652,7 @@ verkv_status verkv_fetch_refine(verkv_ctx *ctx, const int32_t *ids, const int32_
     if (bad16(host_kv) || bad4(o_out) || bad4(lse_out) || bad4(stats_out))
         return fail(ctx, VERKV_EINVAL, "fetch_refine: host_kv needs 16-byte, outputs 4-byte alignment");
     VERKV_CUDA(cudaSetDevice(ctx->device), "cudaSetDevice");
+    const NvtxRange nvtx("verkv_fetch_refine: fetch, refine, merge");
     const LayerIdx li = layer_idx(ctx, ctx->layer);
     const int n = ctx->sh.n, d = ctx->sh.head_dim;
     // With the exact sketch every key is already on the GPU: only V rows move, unless asked.
@@ -682,6 +722,9 @@ verkv_status verkv_fetch_refine(verkv_ctx *ctx, const int32_t *ids, const int32_
                    }), "k_refine");
     } else {
         VERKV_CUDA(cudaEventSynchronize(ctx->e_sel), "cudaEventSynchronize");
+        // When profiling, two events on the (idle) side stream bracket the host gather.
+        cudaEvent_t g0 = ctx->prof_on ? prof_event(ctx) : nullptr;
+        if (g0) VERKV_CUDA(cudaEventRecord(g0, ctx->side), "cudaEventRecord");
         const int U = ctx->L.units_layer;
         const unsigned char *src_base = (const unsigned char *)host_kv;
         // Flatten (unit, row) into one index space and split it evenly over the pool.
@@ -689,6 +732,11 @@ verkv_status verkv_fetch_refine(verkv_ctx *ctx, const int32_t *ids, const int32_
         for (int ul = 0; ul < U; ++ul) start[ul + 1] = start[ul] + ctx->host_counts[ul];
         const int64_t total = start[U];
         const int P = ctx->pool->size();
+        const size_t head = staging_header(U);
+        int64_t *offs = reinterpret_cast<int64_t *>(ctx->host_staging);
+        for (int ul = 0; ul < U; ++ul) offs[ul] = start[ul];
+        unsigned char *rows_h = ctx->host_staging + head;
+        nvtxRangePushA("fetch: host gather");
         ctx->pool->run([&](int w) {
             const int64_t lo = total * w / P, hi = total * (w + 1) / P;
             int ul = (int)(std::upper_bound(start.begin(), start.end(), lo) - start.begin()) - 1;
@@ -697,22 +745,28 @@ verkv_status verkv_fetch_refine(verkv_ctx *ctx, const int32_t *ids, const int32_
                 const int64_t j = x - start[ul];
                 const int ug = li.unit_global(ul);
                 const int id = ctx->host_ids[(size_t)ul * n + j];
-                memcpy(ctx->host_staging + ((size_t)ul * n + j) * move_bytes,
+                memcpy(rows_h + (size_t)x * move_bytes,
                        src_base + ((size_t)ug * n + id) * row_bytes + move_off, move_bytes);
             }
         });
-        for (int ul = 0; ul < U; ++ul) {
-            const int cnt = ctx->host_counts[ul];
-            if (cnt <= 0) continue;
-            cudaError_t e = cudaMemcpyAsync((unsigned char *)ctx->staging + (size_t)ul * n * move_bytes,
-                                            ctx->host_staging + (size_t)ul * n * move_bytes,
-                                            (size_t)cnt * move_bytes, cudaMemcpyHostToDevice, ctx->side);
-            if (e != cudaSuccess)
-                return fail(ctx, VERKV_ECOPY, std::string("fetch copy: ") + cudaGetErrorString(e));
+        nvtxRangePop();
+        if (g0) {
+            cudaEvent_t g1 = prof_event(ctx);
+            if (g1) {
+                VERKV_CUDA(cudaEventRecord(g1, ctx->side), "cudaEventRecord");
+                ctx->prof_recs.push_back({VERKV_K_FETCH_GATHER, g0, g1});
+            }
         }
+        // One copy: the header and every unit's rows.
+        const cudaError_t ce = tracked(ctx, VERKV_K_FETCH_COPY, ctx->side, [&]() -> cudaError_t {
+            return copy_rows(ctx, ctx->staging, ctx->host_staging, head + (size_t)total * move_bytes);
+        });
+        if (ce != cudaSuccess)
+            return fail(ctx, VERKV_ECOPY, std::string("fetch copy: ") + cudaGetErrorString(ce));
         VERKV_CUDA(cudaEventRecord(ctx->e_fetch, ctx->side), "cudaEventRecord");
         VERKV_CUDA(cudaStreamWaitEvent(ctx->main, ctx->e_fetch, 0), "cudaStreamWaitEvent");
-        pa.rows = ctx->staging;
+        pa.staged_off = reinterpret_cast<const int64_t *>(ctx->staging);
+        pa.rows = reinterpret_cast<const uint16_t *>(reinterpret_cast<const unsigned char *>(ctx->staging) + head);
         pa.mode = ROWS_STAGED;
         pa.row16 = (int)(move_bytes / 16);
         pa.voff16 = v_only ? 0 : d / 8;
@@ -802,6 +856,27 @@ verkv_status verkv_selection_bitmap(verkv_ctx *ctx, uint32_t *out) {
     return VERKV_OK;
 }
 
+verkv_status verkv_test_inject(verkv_ctx *ctx, int what, int64_t value) {
+    if (!ctx) return VERKV_EINVAL;
+    switch (what) {
+        case VERKV_INJECT_COPY_FAIL:
+            if (value < 0) break;
+            ctx->inject_copy_fail = value;
+            return VERKV_OK;
+        case VERKV_INJECT_BETA_MAXIT:
+            if (value < 0 || value > 64) break;
+            ctx->beta_maxit = (int)value;
+            return VERKV_OK;
+        case VERKV_INJECT_SCORE_STALL:
+            if (value < 1000 || value > 1000000000LL) break;
+            ctx->score_stall_ns = value;
+            return VERKV_OK;
+        default:
+            break;
+    }
+    return fail(ctx, VERKV_EINVAL, "test_inject: unknown injection or value out of range");
+}
+
 verkv_status verkv_profile_enable(verkv_ctx *ctx, int on) {
     if (!ctx) return VERKV_EINVAL;
     ctx->prof_on = on != 0;
@@ -824,6 +899,27 @@ verkv_status verkv_profile_read(verkv_ctx *ctx, int64_t *launches, double *total
     return VERKV_OK;
 }
 
+verkv_status verkv_profile_timeline(verkv_ctx *ctx, int64_t max_records, int32_t *kernel,
+                                    double *start_ms, double *end_ms, int64_t *n_out) {
+    if (!ctx || !kernel || !start_ms || !end_ms || !n_out || max_records < 0) return VERKV_EINVAL;
+    VERKV_CUDA(cudaSetDevice(ctx->device), "cudaSetDevice");
+    VERKV_CUDA(cudaStreamSynchronize(ctx->side), "cudaStreamSynchronize(side)");
+    VERKV_CUDA(cudaStreamSynchronize(ctx->main), "cudaStreamSynchronize(main)");
+    int64_t k = 0;
+    for (const auto &r : ctx->prof_recs) {
+        if (k >= max_records) break;
+        float a = 0.0f, b = 0.0f;
+        VERKV_CUDA(cudaEventElapsedTime(&a, ctx->prof_recs[0].a, r.a), "cudaEventElapsedTime");
+        VERKV_CUDA(cudaEventElapsedTime(&b, ctx->prof_recs[0].a, r.b), "cudaEventElapsedTime");
+        kernel[k] = r.kernel;
+        start_ms[k] = a;
+        end_ms[k] = b;
+        ++k;
+    }
+    *n_out = k;
+    return VERKV_OK;
+}
+
 verkv_status verkv_launch_counts(verkv_ctx *ctx, int64_t *out) {
     if (!ctx || !out) return VERKV_EINVAL;
     for (int k = 0; k < VERKV_K_COUNT; ++k) out[k] = ctx->launches[k];
@@ -834,7 +930,7 @@ const char *verkv_kernel_name(int k) {
     static const char *names[VERKV_K_COUNT] = {
         "k_pc_solve", "k_pc_gather", "k_sketch", "k_score", "k_certify",
         "k_partial(pivotal)", "k_refine", "k_partial(staged)", "k_merge",
-        "k_dense_host", "k_dense_merge", "k_shortlist"};
+        "k_dense_host", "k_dense_merge", "k_shortlist", "fetch_copy", "fetch_gather"};
     return (k >= 0 && k < VERKV_K_COUNT) ? names[k] : "";
 }
 

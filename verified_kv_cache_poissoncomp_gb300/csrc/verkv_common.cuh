@@ -271,12 +271,13 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
         : "memory");
     return done != 0;
 }
-// Wait for phase `parity` of the barrier; false if TMA_WAIT_NS elapsed first.
-__device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity) {
+// Wait for phase `parity` of the barrier; false if limit_ns (TMA_WAIT_NS) elapsed first.
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity,
+                                                  unsigned long long limit_ns = TMA_WAIT_NS) {
     if (mbar_try_wait(bar, parity)) return true;
     const unsigned long long t0 = globaltimer_ns();
     while (!mbar_try_wait(bar, parity))
-        if (globaltimer_ns() - t0 > TMA_WAIT_NS) return false;
+        if (globaltimer_ns() - t0 > limit_ns) return false;
     return true;
 }
 

@@ -101,6 +101,11 @@ struct ScoreArgs {
     int n, d;
     float scale;
     LayerIdx li;
+    // Failure injection for tests (0 in normal use): the bounded copy waits give up after
+    // wait_ns (0: one second), and with stall_first set the first CTA arms its first stage's
+    // barrier for a copy it never issues, so that wait runs out.
+    unsigned long long wait_ns;
+    int stall_first;
 };
 // `pdl`: launch with programmatic stream serialisation.  The first kernel of a library call must
 // not: it reads the caller's q and sketch, which the caller's preceding kernel may still be
@@ -131,6 +136,7 @@ struct CertifyArgs {
     int n, W, cl, chunk;
     float eps, ldelta;
     LayerIdx li;
+    int beta_maxit;               // iteration cap of the beta solve (0: the default, 64)
 };
 cudaError_t launch_certify(const CertifyArgs &a, int qheads, size_t smem, cudaStream_t s);
 
@@ -180,6 +186,8 @@ struct PartialArgs {
                               // [qh], zero on entry (k_merge resets them)
     uint32_t *rmask;          // fetched-row ranges: bit k of [units_layer][RMASK_W] set when
                               // range k holds rows (only those get a partial); zero on entry
+    const int64_t *staged_off; // ROWS_STAGED: first staged row of each layer unit (the staged
+                               // rows of all units are contiguous, unit by unit)
     int row_stride;           // cap (pivotal) or n (fetched)
     int units_total;          // pivotal: units of the whole shape (rows of `rows` = units_total * cap)
     int max_chunks;
