@@ -819,6 +819,9 @@ def run_model_steps(args, local, kind):
         for eps in epss:
             def step(check=False, with_counts=False):
                 for l in range(L):
+                    if check:  # where a failing call would stop
+                        print(f"checked call: eta={eta:.5f} eps={eps} layer={l}", file=sys.stderr,
+                              flush=True)
                     B.verkv_attend_verified(eng.ctx, l, queries[l].data_ptr(), eng.pivotal,
                                             eng.r_full.data_ptr(), eng.sketch_desc, eps, delta,
                                             None, fc_all[l].data_ptr() if with_counts else None)

@@ -474,7 +474,7 @@ __device__ __forceinline__ void fetch_list_tail(const CertifyArgs &a, int ul, in
 
 template <int CL, bool SL>
 __global__ void __launch_bounds__(CT_NT, 1) k_certify(CertifyArgs a) {
-    pdl_trigger();  // pdl_wait() follows the loads of r, which no early-starting kernel writes
+    pdl_trigger();  // the refine kernel after this one may be scheduled early
     cluster_arrive_relaxed();  // waited on before the first exchange with the peers
     extern __shared__ __align__(16) unsigned char smem_raw[];
     float *wrec = reinterpret_cast<float *>(smem_raw);
@@ -512,7 +512,7 @@ __global__ void __launch_bounds__(CT_NT, 1) k_certify(CertifyArgs a) {
             const int i = tid + k * CT_NT, t = base + i;
             rv[k] = (i < chunk && t < n) ? rf[t] : 1.0f;
         }
-        pdl_wait();  // the logits come from the kernel before this one
+        pdl_wait();  // the logits come from the kernel before this one (a no-op: plain launch)
 #pragma unroll
         for (int k = 0; k < TPT; ++k) {
             const int i = tid + k * CT_NT, t = base + i;
@@ -1034,15 +1034,15 @@ static cudaError_t launch_certify_cl(const CertifyArgs &a, int qheads, size_t sm
     cfg.blockDim = dim3(CT_NT);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = s;
-    cudaLaunchAttribute attr[2];
+    cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = CL;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
-    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;  // see launch_pdl
-    attr[1].val.programmaticStreamSerializationAllowed = 1;
+    // In plain stream order: the cluster kernel starts only once the scoring kernel has
+    // finished (no programmatic early start next to a running grid).
     cfg.attrs = attr;
-    cfg.numAttrs = 2;
+    cfg.numAttrs = 1;
     return cudaLaunchKernelEx(&cfg, k_certify<CL, SL>, a);
 }
 

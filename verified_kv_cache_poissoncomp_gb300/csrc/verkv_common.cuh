@@ -31,6 +31,7 @@ __device__ __forceinline__ void cluster_arrive_relaxed() {
     asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
 }
 __device__ __forceinline__ void cluster_wait_all() {
+    __syncwarp();  // the .aligned form wants the whole warp converged
     asm volatile("barrier.cluster.wait.aligned;" ::: "memory");
 }
 
