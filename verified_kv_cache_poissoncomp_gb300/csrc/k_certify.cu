@@ -81,11 +81,17 @@ size_t certify_smem_bytes(int chunk) {
 }
 
 // Cluster-wide all-reduce of a K-float record held identically by the lanes of each warp.
-// `comb(x, y)` sets x to x (+) y and must give the same bits for (x, y) and (y, x).  Warp 0
-// combines the CTA's warp records with a butterfly (so its lanes agree), lanes 0..CL-1 send the
-// CTA record into slot [my rank] of each peer, and after one cluster barrier every thread
-// combines the CL records in rank order.  The two CTA-record buffers alternate: a buffer is
-// rewritten two calls later, after a barrier every peer passes only once it has read it.
+// `comb(x, y)` sets x to x (+) y.  Warp 0 combines the CTA's warp records with a butterfly and
+// takes lane 0's result as the CTA record: a butterfly pairs comb(x, y) on one lane with
+// comb(y, x) on the other, and a comb that is not bitwise symmetric (a multiply-add the compiler
+// contracts) would leave the lanes a rounding apart.  Lanes 0..CL-1 send that one record into
+// slot [my rank] of each peer, and after one cluster barrier every thread combines the CL
+// records in rank order, so every thread of every CTA holds the same bits.  That is what keeps
+// the cluster's control flow uniform: every branch after an exchange (the certificate, the beta
+// passes, the select's passes) is decided from these values, and CTAs that took different
+// branches would meet different cluster barriers.  The two CTA-record buffers alternate: a
+// buffer is rewritten two calls later, after a barrier every peer passes only once it has read
+// it.
 template <int CL, int K, class Comb>
 __device__ __forceinline__ void cluster_allreduce(float (&v)[K], float *wrec, float *xrec,
                                                   int &parity, Comb comb) {
@@ -108,6 +114,8 @@ __device__ __forceinline__ void cluster_allreduce(float (&v)[K], float *wrec, fl
             for (int k = 0; k < K; ++k) y[k] = __shfl_xor_sync(0xFFFFFFFFu, x[k], o);
             comb(x, y);
         }
+#pragma unroll
+        for (int k = 0; k < K; ++k) x[k] = __shfl_sync(0xFFFFFFFFu, x[k], 0);
         if (lane < CL) {
             float *peer = cluster.map_shared_rank(buf, lane);
             const int me = (int)cluster.block_rank();
@@ -543,9 +551,9 @@ __global__ void __launch_bounds__(CT_NT, 1) k_certify(CertifyArgs a) {
             const float M = fmaxf(x[0], y[0]);
             const float fx = x[0] == NEG_INF ? 0.0f : expf(x[0] - M);
             const float fy = y[0] == NEG_INF ? 0.0f : expf(y[0] - M);
-            x[0] = M;
-            x[1] = x[1] * fx + y[1] * fy;
-            x[2] = x[2] * fx + y[2] * fy;
+            x[0] = M;  // products rounded separately: the same bits for (x, y) and (y, x)
+            x[1] = __fadd_rn(__fmul_rn(x[1], fx), __fmul_rn(y[1], fy));
+            x[2] = __fadd_rn(__fmul_rn(x[2], fx), __fmul_rn(y[2], fy));
             x[3] = x[3] + y[3];
         });
         m = rec[0];

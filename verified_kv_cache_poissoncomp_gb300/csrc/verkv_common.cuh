@@ -125,6 +125,7 @@ struct ClusterReducer {
         for (int k = 0; k < K; ++k) {
 #pragma unroll
             for (int o = 16; o > 0; o >>= 1) v[k] = op(v[k], __shfl_xor_sync(0xFFFFFFFFu, v[k], o));
+            v[k] = __shfl_sync(0xFFFFFFFFu, v[k], 0);  // one value per warp, whatever op's symmetry
         }
         cg::cluster_group cluster = cg::this_cluster();
         const unsigned me = cluster.block_rank();
@@ -142,7 +143,7 @@ struct ClusterReducer {
             for (int e = lane + 32; e < total; e += 32) acc = op(acc, b[e * K + k]);
 #pragma unroll
             for (int o = 16; o > 0; o >>= 1) acc = op(acc, __shfl_xor_sync(0xFFFFFFFFu, acc, o));
-            v[k] = acc;
+            v[k] = __shfl_sync(0xFFFFFFFFu, acc, 0);
         }
         parity ^= 1;
     }
