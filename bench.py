@@ -26,6 +26,11 @@ import sys
 import tempfile
 import time
 
+# The oracle's matrix products run on numpy's BLAS: one thread each, so that the timed CPU
+# baselines use exactly the threads they report (one, or one per core).
+for _v in ("OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS", "BLIS_NUM_THREADS"):
+    os.environ.setdefault(_v, "1")
+
 import numpy as np
 
 ROOT = os.path.dirname(os.path.abspath(__file__))
@@ -241,6 +246,19 @@ def cpu_baseline(w):
                               "seconds": round(t_pc1 + t_q1 * len(sample1), 2)}}
 
 
+def bench_config(args, Q, world):
+    """The benchmark workload's description, the same for both arms."""
+    return {"workload": "single-layer 32K: n=32768, 8 KV heads x 4 query heads, "
+                        "d=128, bf16, eta=1/16, H=4 sink+512 local, batch 1, "
+                        f"{Q} decode queries (1/4 aimed at unsampled planted keys), "
+                        "eps=delta=0.05; layer held as 4 independent instances, "
+                        "query t on instance t mod 4",
+            "l2": "inputs larger than L2 (4 x 73 MiB resident state per step)",
+            "fetch": args.fetch_mode, "sketch": args.sketch,
+            "shortlist": args.shortlist,
+            "parallelism": f"replicas x{world}"}
+
+
 def run_reference(args, world, rank):
     """The oracle as the reference arm: each step a bounded sample of the workload."""
     if rank != 0:
@@ -249,17 +267,22 @@ def run_reference(args, world, rank):
     import oracle as O
 
     w = I.single_layer_32k(layers=LAYERS, n_queries=args.queries)
-    per_step = 4
-    state = {"q": 0, "head": 0}
+    # Two queries a step, and one PoissonComp head every fourth step: one head per 8 queries, the
+    # proportion of the benchmark's step (4 layers x 8 heads per 256 queries); a default run of
+    # 43 steps stays within a few minutes.
+    per_step = 2
+    state = {"q": 0, "head": 0, "step": 0}
     pcs = {}
     for h in range(w.h_kv):
         pcs[h] = O.poissoncomp(w.tau[0, 0, h], w.eta, w.n_sink, w.n_local, w.seed, 0, 0, h)
     layer0 = [t for t in range(w.queries.shape[0]) if w.query_layer[t] == 0]
 
     def step():
-        h0 = state["head"] % w.h_kv
-        O.poissoncomp(w.tau[0, 0, h0], w.eta, w.n_sink, w.n_local, w.seed, 0, 0, h0)
-        state["head"] += 1
+        if state["step"] % 4 == 0:
+            h0 = state["head"] % w.h_kv
+            O.poissoncomp(w.tau[0, 0, h0], w.eta, w.n_sink, w.n_local, w.seed, 0, 0, h0)
+            state["head"] += 1
+        state["step"] += 1
         for _ in range(per_step):
             t = layer0[state["q"] % len(layer0)]
             state["q"] += 1
@@ -280,11 +303,12 @@ def run_reference(args, world, rank):
            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
            "ms_per_step": 1e3 * dt / args.steps, "higher_is_better": True, "scaling": "weak",
            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-           "config": {"workload": "single-layer 32K: n=32768, 8 KV heads x 4 query heads, d=128, "
-                                  "eta=1/16, H=4+512, eps=delta=0.05 (oracle sample)"},
+           "config": bench_config(args, w.queries.shape[0], world),
            "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
-                            "sample": f"each step: PoissonComp of 1 head + {per_step} queries "
-                                      "(32 query heads each), single thread"},
+                            "sample": f"each step: {per_step} queries (32 query heads each, "
+                                      "from layer instance 0) and, every fourth step, "
+                                      "PoissonComp of 1 head: the benchmark's proportion of "
+                                      "PoissonComp to queries; single thread"},
            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
                    "d2h_bytes_per_step": 0}}
     print(json.dumps(out), flush=True)
@@ -495,6 +519,26 @@ def run_ours(args, world, rank, local):
                             "algorithmic_bytes_per_launch": int(nbytes),
                             "traffic": traffic_for(k),
                             "peak_source": link_src if bound == "h2d" else peak_src}
+    # k_score against a bare one-launch read of the same sketch bytes: the library streams each
+    # query's layer through the scoring kernel's grid and copy ring with no arithmetic, timed the
+    # same way (an event pair per launch) over the same sequence of layer instances.
+    if "k_score" in rooflines and args.sketch == "exact":
+        pairs = []
+        with torch.cuda.stream(stream):
+            for t in range(min(Q, 72)):
+                e_a = torch.cuda.Event(enable_timing=True)
+                e_b = torch.cuda.Event(enable_timing=True)
+                e_a.record(stream)
+                B.verkv_measure_sketch_stream(eng.ctx, int(w.query_layer[t]), eng.sketch_desc)
+                e_b.record(stream)
+                if t >= 8:  # the first launches warm up
+                    pairs.append((e_a, e_b))
+        B.verkv_sync(eng.ctx)
+        read_us = 1e3 * sum(a.elapsed_time(b) for a, b in pairs) / len(pairs)
+        r = rooflines["k_score"]
+        r["one_launch_read_us"] = round(read_us, 3)
+        r["one_launch_read_GBs"] = round(r["algorithmic_bytes_per_launch"] / (read_us * 1e-6) / 1e9, 1)
+        r["frac_of_one_launch_read"] = round(read_us / r["avg_us"], 4)
     dom = max(per_kernel, key=lambda k: per_kernel[k]["total_ms"])
     roof = dict(rooflines[dom], kernel=dom) if dom in rooflines else None
     # The HBM-bound kernel that moves the most bytes per step (the one whose bandwidth matters).
@@ -571,16 +615,7 @@ def run_ours(args, world, rank, local):
                "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4),
                "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
                "dtype": "bf16", "data": "synthetic",
-               "config": {"workload": "single-layer 32K: n=32768, 8 KV heads x 4 query heads, "
-                                      "d=128, bf16, eta=1/16, H=4 sink+512 local, batch 1, "
-                                      f"{Q} decode queries (1/4 aimed at unsampled planted keys), "
-                                      "eps=delta=0.05; layer held as 4 independent instances, "
-                                      "query t on instance t mod 4",
-                          "l2": "inputs larger than L2 (4 x 73 MiB resident state per step)",
-                          "fetch": args.fetch_mode, "sketch": args.sketch,
-                          "shortlist": args.shortlist,
-                          "graph": graph is not None,
-                          "parallelism": f"replicas x{world}"},
+               "config": dict(bench_config(args, Q, world), graph=graph is not None),
                "roofline": roof, "roofline_hbm": roof_hbm, "rooflines": rooflines,
                "per_kernel_us": {
                    k: round(v["avg_us"], 3) for k, v in per_kernel.items()},

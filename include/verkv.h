@@ -367,6 +367,14 @@ verkv_status verkv_profile_read(verkv_ctx *ctx, int64_t *launches, double *total
 verkv_status verkv_profile_timeline(verkv_ctx *ctx, int64_t max_records, int32_t *kernel,
                                     double *start_ms, double *end_ms, int64_t *n_out);
 
+/* Measurement: stream the exact sketch rows that verkv_attend_verified would score for `layer`
+ * (every KV head of the layer, d * 2 bytes a token) through the scoring kernel's copy grid and
+ * ring, without any arithmetic, on the context's stream (asynchronous).  Its time is that of a
+ * bare one-launch read of the same bytes, the reference the scoring kernel's time is set
+ * against.  The sketch must be VERKV_SKETCH_EXACT with a 16-byte aligned data pointer, else
+ * VERKV_EINVAL; bad layer: VERKV_EINVAL.  Not counted in verkv_launch_counts. */
+verkv_status verkv_measure_sketch_stream(verkv_ctx *ctx, int32_t layer, const verkv_sketch *sketch);
+
 /* Kernel launches issued by this context since it was created, per kernel id
  * (out[VERKV_K_COUNT], host).  Counts launches made during stream capture once. */
 verkv_status verkv_launch_counts(verkv_ctx *ctx, int64_t *out);

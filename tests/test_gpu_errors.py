@@ -186,3 +186,23 @@ def test_injection_arguments_are_checked():
             B.verkv_test_inject(eng.ctx, what, value)
         assert e.value.status == B.VERKV_EINVAL
     eng.close()
+
+
+def test_sketch_stream_measurement_call():
+    # The measurement call streams a layer's exact sketch through the scoring kernel's copy ring;
+    # it checks its arguments on the host and leaves no error behind.
+    w = I.tiny()
+    eng = P.make_engine(w)
+    eng.compress(w.eta, w.n_sink, w.n_local, w.seed)
+    eng.sync()
+    launches = B.verkv_launch_counts(eng.ctx)
+    B.verkv_measure_sketch_stream(eng.ctx, 0, eng.sketch_desc)
+    assert B.verkv_sync_status(eng.ctx) == B.VERKV_OK
+    assert B.verkv_launch_counts(eng.ctx) == launches  # not a decode kernel: not counted
+    lib = B.lib()
+    bad = [(w.L, eng.sketch_desc),
+           (0, B.verkv_sketch(B.VERKV_SKETCH_Q2, eng.sketch.data_ptr())),
+           (0, B.verkv_sketch(B.VERKV_SKETCH_EXACT, eng.sketch.data_ptr() + 8))]
+    for layer, sk in bad:
+        assert lib.verkv_measure_sketch_stream(eng.ctx, layer, sk) == B.VERKV_EINVAL
+    eng.close()

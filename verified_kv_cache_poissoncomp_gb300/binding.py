@@ -34,7 +34,7 @@ EXPORTED = ["verkv_sketch_bytes", "verkv_workspace_size", "verkv_create", "verkv
             "verkv_profile_read", "verkv_launch_counts", "verkv_kernel_name", "verkv_sync",
             "verkv_last_error", "verkv_status_string", "verkv_certify_noalloc",
             "verkv_attend_dense_host", "verkv_set_shortlist", "verkv_shortlist_bitmap",
-            "verkv_profile_timeline", "verkv_test_inject"]
+            "verkv_profile_timeline", "verkv_test_inject", "verkv_measure_sketch_stream"]
 VERKV_INJECT_COPY_FAIL, VERKV_INJECT_BETA_MAXIT, VERKV_INJECT_SCORE_STALL = 1, 2, 3
 # kernel ids (include/verkv.h), in launch order
 (VERKV_K_PC_SOLVE, VERKV_K_PC_GATHER, VERKV_K_SKETCH, VERKV_K_SCORE, VERKV_K_CERTIFY,
@@ -133,6 +133,8 @@ def lib():
         L.verkv_profile_timeline.restype = ctypes.c_int
         L.verkv_test_inject.argtypes = [vp, ctypes.c_int, ctypes.c_int64]
         L.verkv_test_inject.restype = ctypes.c_int
+        L.verkv_measure_sketch_stream.argtypes = [vp, ctypes.c_int32, ctypes.POINTER(verkv_sketch)]
+        L.verkv_measure_sketch_stream.restype = ctypes.c_int
         L.verkv_launch_counts.argtypes = [vp, vp]
         L.verkv_launch_counts.restype = ctypes.c_int
         L.verkv_kernel_name.argtypes = [ctypes.c_int]
@@ -252,6 +254,11 @@ def verkv_profile_timeline(ctx, max_records=1 << 16):
 def verkv_test_inject(ctx, what, value):
     """Failure injection for tests (VERKV_INJECT_*; see include/verkv.h)."""
     _check(lib().verkv_test_inject(ctx, int(what), int(value)), ctx)
+
+
+def verkv_measure_sketch_stream(ctx, layer, sketch):
+    """Stream the layer's exact sketch rows through the scoring kernel's copy ring, no arithmetic."""
+    _check(lib().verkv_measure_sketch_stream(ctx, int(layer), ctypes.byref(sketch)), ctx)
 
 
 def verkv_launch_counts(ctx):

@@ -778,6 +778,23 @@ verkv_status verkv_fetch_refine(verkv_ctx *ctx, const int32_t *ids, const int32_
     return VERKV_OK;
 }
 
+verkv_status verkv_measure_sketch_stream(verkv_ctx *ctx, int32_t layer, const verkv_sketch *sketch) {
+    if (!ctx) return VERKV_EINVAL;
+    if (layer < 0 || layer >= ctx->sh.layers) return fail(ctx, VERKV_EINVAL, "sketch stream: bad layer");
+    if (!sketch || !sketch->data || sketch->format != VERKV_SKETCH_EXACT)
+        return fail(ctx, VERKV_EINVAL, "sketch stream: an exact sketch is required");
+    if (bad16(sketch->data)) return fail(ctx, VERKV_EINVAL, "sketch stream: 16-byte alignment required");
+    VERKV_CUDA(cudaSetDevice(ctx->device), "cudaSetDevice");
+    ScoreArgs sa{};
+    sa.sketch = (const uint16_t *)sketch->data;
+    sa.err = ctx->err;
+    sa.n = ctx->sh.n;
+    sa.d = ctx->sh.head_dim;
+    sa.li = layer_idx(ctx, layer);
+    VERKV_CUDA(launch_sketch_stream(sa, ctx->L.units_layer, ctx->main), "k_sketch_stream");
+    return VERKV_OK;
+}
+
 verkv_status verkv_sync(verkv_ctx *ctx) {
     if (!ctx) return VERKV_EINVAL;
     VERKV_CUDA(cudaSetDevice(ctx->device), "cudaSetDevice");

@@ -113,6 +113,8 @@ struct ScoreArgs {
 cudaError_t launch_score(const ScoreArgs &a, int units_layer, cudaStream_t s, bool pdl);
 // The same from the 2-bit sketch (a.sketch points at its rows).
 cudaError_t launch_score_q2(const ScoreArgs &a, int units_layer, cudaStream_t s, bool pdl);
+// The exact sketch's rows of one layer through k_score's copy ring, with no arithmetic.
+cudaError_t launch_sketch_stream(const ScoreArgs &a, int units_layer, cudaStream_t s);
 
 // Certificate and selection per query head (one cluster per query head).  When fl_counter is
 // set, the last of the G clusters of a KV head to finish also builds that head's fetch list:
