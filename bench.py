@@ -615,7 +615,8 @@ def run_ours(args, world, rank, local):
                "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4),
                "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
                "dtype": "bf16", "data": "synthetic",
-               "config": dict(bench_config(args, Q, world), graph=graph is not None),
+               "config": bench_config(args, Q, world),
+               "launch": "CUDA graph replay" if graph is not None else "eager",
                "roofline": roof, "roofline_hbm": roof_hbm, "rooflines": rooflines,
                "per_kernel_us": {
                    k: round(v["avg_us"], 3) for k, v in per_kernel.items()},
