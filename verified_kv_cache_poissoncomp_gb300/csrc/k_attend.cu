@@ -361,6 +361,58 @@ __global__ void __launch_bounds__(128) k_partial(PartialArgs a, int units_layer)
     }
 }
 
+// The CTA's run of pivotal items (item = unit * max_chunks + chunk, in unit order).  A chunk's first
+// row, counted over the layer's units, is nondecreasing in the item index (a chunk past its unit's
+// count starts at the unit's end), so cutting the rows into gridDim.x equal ranges and giving each
+// chunk to the range that holds its first row splits the items into contiguous runs of about
+// equal rows: at most one chunk more than an equal share.  Every thread of the CTA calls it and
+// gets the same run.
+template <int NT>
+__device__ void pivotal_run(const PartialArgs &a, int units_layer, int &item0, int &item1) {
+    __shared__ int s_wsum[NT / 32];
+    __shared__ int s_cut[2];
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int total_items = units_layer * a.max_chunks;
+    const int per_t = (units_layer + NT - 1) / NT;  // units per thread
+    const int u0 = min(units_layer, tid * per_t), u1 = min(units_layer, u0 + per_t);
+    int mine = 0;
+    for (int u = u0; u < u1; ++u) mine += min(a.count[a.li.unit_global(u)], a.row_stride);
+    int incl = mine;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+        if (lane >= o) incl += y;
+    }
+    if (lane == 31) s_wsum[warp] = incl;
+    if (tid == 0) s_cut[0] = s_cut[1] = total_items;
+    __syncthreads();
+    int base = incl - mine, rows = 0;
+#pragma unroll
+    for (int w = 0; w < NT / 32; ++w) {
+        if (w < warp) base += s_wsum[w];
+        rows += s_wsum[w];
+    }
+    const long long share = ((long long)rows + gridDim.x - 1) / gridDim.x;
+    const long long lo_row = share * blockIdx.x, hi_row = lo_row + share;
+    int first_lo = total_items, first_hi = total_items;
+    long long p = base;
+    for (int u = u0; u < u1; ++u) {
+        const int cnt = min(a.count[a.li.unit_global(u)], a.row_stride);
+        for (int ch = 0; ch < a.max_chunks; ++ch) {
+            const long long start = p + min(ch * PIV_ITEM_ROWS, cnt);
+            const int item = u * a.max_chunks + ch;
+            if (start >= lo_row) first_lo = min(first_lo, item);
+            if (start >= hi_row) first_hi = min(first_hi, item);
+        }
+        p += cnt;
+    }
+    if (first_lo < total_items) atomicMin(&s_cut[0], first_lo);
+    if (first_hi < total_items) atomicMin(&s_cut[1], first_hi);
+    __syncthreads();
+    item0 = s_cut[0];
+    item1 = max(item0, s_cut[1]);
+}
+
 // k_pivotal: the estimator's pass over the pivotal set on its own (MEMCPY mode, where it runs
 // during the host gather).  Warps 0-3 consume, warp 4 produces: for every stage of PIV_STAGE_ROWS
 // rows of the CTA's chunks (a contiguous run of them) the producer waits for the
@@ -419,10 +471,10 @@ __global__ void __launch_bounds__(PV_NT, PV_CTAS_PER_SM) k_pivotal(PartialArgs a
     pdl_wait();
     pdl_trigger();
     volatile int *abort = &s_abort;
-    // A contiguous run of items per CTA: consecutive chunks of a unit share its queries.
-    const int total = units_layer * a.max_chunks;
-    const int per = (total + gridDim.x - 1) / gridDim.x;
-    const int item0 = min(total, (int)blockIdx.x * per), item1 = min(total, item0 + per);
+    // A contiguous run of items per CTA (consecutive chunks of a unit share its queries), with
+    // about the same number of rows in every run.
+    int item0, item1;
+    pivotal_run<PV_NT>(a, units_layer, item0, item1);
     if (warp == PV_CONS) {
         if (lane == 0) asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&rows_map)) : "memory");
         int j = 0, cur = -1, ug = 0, count = 0;
