@@ -13,8 +13,8 @@
 //      S += r / (1 - r)) or at lambda = 1 -- and moves to the root (A + B) / (1 + S) of that
 //      linear piece, a ratio of positive sums; the pass also finds the nearest breakpoints on
 //      either side, and the solve ends as soon as the new root lies between them.  The first
-//      pass evaluates two points, C and C/4, in one exchange, which brackets the root and starts
-//      Newton closer to it than the top of the bracket (2.7 passes on average instead of 3.4);
+//      pass evaluates two points, C/2 and C/8, in one exchange, which brackets the root and starts
+//      Newton closer to it than the top of the bracket (2.5 passes on average instead of 3.4);
 //   +1 beta(L), V(L), the top two b_i (with the argmax id) of Lemma 1;
 //   +k when the certificate fails, a windowed most-significant-digit select over the 56-bit key
 //      (g bits << 24 | 2^24-1-token id) -- g descending, ties to the lower id.  Each pass builds a
@@ -41,8 +41,13 @@ constexpr int CT_NT = 1024;
 constexpr int CT_NW = CT_NT / 32;
 constexpr int CT_MAX_CL = 8;
 constexpr int CT_REC = 16;  // floats per record in a cluster all-reduce
-constexpr int BETA_GRID = 2;           // points of the beta solve's first pass: C and C/4
-constexpr float BETA_GRID_STEP = 0.25f; // (measured against 1, 3 and 4 points on the bench)
+// Points of the beta solve's first pass: C/2 and C/8.  (Measured against 1, 3 and 4 points on the
+// bench; a simulation of the solve over the bench's heads gave 2.53 passes on average with the
+// pair C/2, C/8 against 2.54 with C, C/4, and 52 heads of 1536 needing four passes or more
+// against 132.)
+constexpr int BETA_GRID = 2;
+constexpr float BETA_GRID_FIRST = 0.5f;
+constexpr float BETA_GRID_STEP = 0.25f;
 constexpr int BETA_MAXIT = 64;
 constexpr int SEL_MAXPASS = 16;
 
@@ -569,7 +574,7 @@ __global__ void __launch_bounds__(CT_NT, 1) k_certify(CertifyArgs a) {
     // above (ph).  A token's breakpoints are w (1 - r), where lambda leaves its floor, and
     // w (1 - r) / r, where it reaches 1.  The root of the piece through beta is the fixed point
     // when it lies strictly between pl and ph, or when it reproduces beta (to 1e-6 relative:
-    // float32 sums jitter by an ulp or two).  The first pass evaluates BETA_GRID points C, C/4, ...
+    // float32 sums jitter by an ulp or two).  The first pass evaluates BETA_GRID points C/2, C/8
     // together (one cluster exchange), which brackets the root and gives the Newton start; later
     // passes take one point each.
     float beta = 0.0f;
@@ -597,7 +602,7 @@ __global__ void __launch_bounds__(CT_NT, 1) k_certify(CertifyArgs a) {
         float gb[NG], gab[NG], gS[NG], gpl[NG], gph[NG];
 #pragma unroll
         for (int k = 0; k < NG; ++k) {
-            gb[k] = k == 0 ? C : gb[k - 1] * BETA_GRID_STEP;
+            gb[k] = k == 0 ? BETA_GRID_FIRST * C : gb[k - 1] * BETA_GRID_STEP;
             gab[k] = 0.f;
             gS[k] = 0.f;
             gpl[k] = 0.f;
