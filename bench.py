@@ -9,6 +9,10 @@ quarter are aimed at planted keys PoissonComp did not keep, eps = delta = 0.05. 
 held as 4 independent instances (4 x 73 MiB of resident state > the 129 MB L2) and query t attends
 instance t mod 4, so each query streams its sketch from HBM as it would behind 35 other layers.
 
+The default run also records, in the same JSON line, the estimator pass alone (its HBM rate), the
+MEMCPY fetch path (copy rate and overlap) and whole decode steps of a 36-layer model at 32K
+(batch 8, eta in {1/8, 1/32}) and 128K (batch 4, eps in {0.02, 0.05}) ("model_steps").
+
 One step = PoissonComp over the 4 instances (a1-a3) + 256 decode queries, each through sketch
 scoring, the beta solve, the Bernstein certificate, selection, the fetch of selected rows from
 page-locked host memory, the shrinkage-estimator attention over the pivotal set and the refine
@@ -53,6 +57,10 @@ def parse_args():
     p.add_argument("--no-graph", action="store_true", help="launch eagerly instead of graph replay")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--quiet", action="store_true",
+                   help="--decode-step / --long128k: no per-call progress on stderr")
+    p.add_argument("--no-model-steps", action="store_true",
+                   help="skip the 36-layer decode steps (32K batch 8, 128K batch 4) of the default run")
     p.add_argument("--no-extra", action="store_true",
                    help="skip the estimator-pass and MEMCPY-fetch measurements of the default run")
     p.add_argument("--queries", type=int, default=QUERIES)
@@ -610,6 +618,31 @@ def run_ours(args, world, rank, local):
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cpu = cpu_baseline(w)
 
+    # Whole decode steps of the 36-layer model at 32K (batch 8) and 128K (batch 4), one GPU: a
+    # compact record of each, or why it was skipped.
+    model = None
+    if rank == 0 and world == 1 and not args.no_extra and not args.no_model_steps:
+        model = {}
+        for kind, host_gb in (("decode-step", 38.7), ("long128k", 77.3)):
+            avail = mem_available_gb()
+            if avail is not None and avail < 1.5 * host_gb + 8:
+                model[kind] = {"skipped": f"{avail:.0f} GB of host memory available, "
+                                          f"{host_gb} GB page-locked cache needed"}
+                continue
+            # In a child process: its page-locked cache and device memory go back when it
+            # exits, and a failure there leaves this process's numbers intact.
+            cmd = [sys.executable, os.path.join(ROOT, "bench.py"), f"--{kind}", "--layers", "36",
+                   "--steps", "3", "--warmup", "2", "--quiet"]
+            try:
+                p = subprocess.run(cmd, capture_output=True, text=True, timeout=600)
+                lines = [l for l in p.stdout.splitlines() if l.startswith("{")]
+                if p.returncode == 0 and lines:
+                    model[kind] = compact_model_steps(json.loads(lines[-1]))
+                else:
+                    model[kind] = {"error": f"exit {p.returncode}: " + " | ".join(p.stderr.strip().splitlines()[-2:])}
+            except Exception as e:  # noqa: BLE001 -- recorded in the line, the bench goes on
+                model[kind] = {"error": f"{type(e).__name__}: {e}"}
+
     if rank == 0:
         out = {"metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world,
                "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4),
@@ -624,12 +657,40 @@ def run_ours(args, world, rank, local):
                "clocks": clk.summary(),
                "gpu_launches": launches_per_step * args.steps,
                "launches_per_step": launches_per_step,
-               "e2e": e2e, "cpu_baseline": cpu}
+               "e2e": e2e, "cpu_baseline": cpu, "model_steps": model}
         print(json.dumps(out), flush=True)
-    eng.close()
+    if eng is not None:
+        eng.close()
     if world > 1:
         import torch.distributed as dist
         dist.destroy_process_group()
+
+
+def mem_available_gb():
+    """MemAvailable of the host in GB, or None where /proc/meminfo is missing."""
+    try:
+        with open("/proc/meminfo") as f:
+            for line in f:
+                if line.startswith("MemAvailable:"):
+                    return int(line.split()[1]) / 1e6
+    except OSError:
+        return None
+    return None
+
+
+def compact_model_steps(r):
+    """The model-step record without the per-row traffic details."""
+    keep = ("eta", "eps", "steps_per_s", "queries_per_s", "ms_per_step", "hbm_GBs",
+            "h2d_bytes_per_step", "fetch_GBs_in_k_refine", "fetched_frac_per_kv_head",
+            "certified_frac", "decisions_fetching_frac", "overall_read_frac", "clocks")
+    rows = []
+    for row in r["rows"]:
+        c = {k: row[k] for k in keep if k in row}
+        c["kernel_ms_per_step"] = {k: v["ms_per_step"] for k, v in row["per_kernel"].items()}
+        rows.append(c)
+    return {"config": r["config"], "steps": r["steps"], "warmup": r["warmup"],
+            "launch": "CUDA graph of one step, replayed", "rows": rows,
+            **{k: r[k] for k in ("planted_queries", "needle_frac_per_unit") if k in r}}
 
 
 EPS_SWEEP = [0.01, 0.02, 0.05, 0.1, 0.2, 0.3, 0.5]
@@ -794,6 +855,11 @@ def run_eps_sweep(args, local):
 
 
 def run_model_steps(args, local, kind):
+    print(json.dumps(measure_model_steps(local, kind, args.layers, args.steps, args.warmup,
+                                         verbose=not args.quiet)), flush=True)
+
+
+def measure_model_steps(local, kind, layers, steps, warmup, verbose=True):
     """One GPU, a whole decode step of a 36-layer model: every layer's attend_verified +
     fetch_refine for a batch of sequences, the full cache page-locked on the host and the
     pivotal set plus the exact sketch on the device.
@@ -816,7 +882,7 @@ def run_model_steps(args, local, kind):
     B.lib()
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
-    L, KVH, G, D = args.layers, 8, 4, 128
+    L, KVH, G, D = layers, 8, 4, 128
     if kind == "decode-step":
         Bt, N = 8, 32768
         etas, epss = [1 / 8, 1 / 32], [0.05]
@@ -855,7 +921,7 @@ def run_model_steps(args, local, kind):
         for eps in epss:
             def step(check=False, with_counts=False):
                 for l in range(L):
-                    if check:  # where a failing call would stop
+                    if check and verbose:  # where a failing call would stop
                         print(f"checked call: eta={eta:.5f} eps={eps} layer={l}", file=sys.stderr,
                               flush=True)
                     B.verkv_attend_verified(eng.ctx, l, queries[l].data_ptr(), eng.pivotal,
@@ -877,7 +943,7 @@ def run_model_steps(args, local, kind):
                 graph = torch.cuda.CUDAGraph()
                 with torch.cuda.graph(graph, stream=stream):
                     step()
-                for _ in range(args.warmup):
+                for _ in range(warmup):
                     graph.replay()
             torch.cuda.synchronize()
             e0 = torch.cuda.Event(enable_timing=True)
@@ -885,12 +951,12 @@ def run_model_steps(args, local, kind):
             with ClockSampler(local) as clk:
                 e0.record(stream)
                 with torch.cuda.stream(stream):
-                    for _ in range(args.steps):
+                    for _ in range(steps):
                         graph.replay()
                 e1.record(stream)
                 torch.cuda.synchronize()
             B.verkv_sync(eng.ctx)
-            ms = e0.elapsed_time(e1) / args.steps
+            ms = e0.elapsed_time(e1) / steps
             del graph
             B.verkv_profile_enable(eng.ctx, 1)
             with torch.cuda.stream(stream):
@@ -929,13 +995,13 @@ def run_model_steps(args, local, kind):
         eng.close()
         del eng, o_all, lse_all, st_all, fc_all
         torch.cuda.empty_cache()
-    print(json.dumps({"workload": kind, "metric": METRIC, "unit": UNIT, "steps": args.steps,
-                      "warmup": args.warmup, "data": "synthetic", "dtype": "bf16",
+    return {"workload": kind, "metric": METRIC, "unit": UNIT, "steps": steps,
+                      "warmup": warmup, "data": "synthetic", "dtype": "bf16",
                       "config": {"layers": L, "batch": Bt, "kv_heads": KVH, "q_per_kv": G,
                                  "head_dim": D, "n": N, "delta": delta,
                                  "host_cache_GB": round(host_kv.nbytes / 1e9, 1),
                                  "sketch": "exact", "fetch": "zerocopy", "graph": True},
-                      "input_generation_s": round(gen_s, 1), **extra, "rows": rows}), flush=True)
+                      "input_generation_s": round(gen_s, 1), **extra, "rows": rows}
 
 
 def run_pc_sweep(args, local):
