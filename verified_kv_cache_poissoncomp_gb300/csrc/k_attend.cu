@@ -666,14 +666,19 @@ static_assert(MG_GROUPS == 8, "k_merge picks a group's ranges with the byte mask
 
 __global__ void __launch_bounds__(MG_NT) k_merge(MergeArgs a) {
     __shared__ float red[MG_GROUPS][MG_COLS + 2];
-    pdl_wait();
-    pdl_trigger();
     const int D = a.d, ncol = D + 2, halves = D / MG_COLS;
     const int qh = blockIdx.x / halves, half = blockIdx.x - qh * halves;
     const int G = a.li.G;
     const int ul = qh / G, g = qh - ul * G;
     const int ug = a.li.unit_global(ul);
+    // Read before the wait on the refine kernel: the pivotal counts (PoissonComp) and the head's
+    // certificate statistics were complete before the refine kernel could start, and this kernel
+    // is scheduled only after that start.
     int pc = a.pcount[ug];
+    verkv_head_stats st;
+    if (half == 0 && threadIdx.x == 0) st = a.qstats[qh];
+    pdl_wait();
+    pdl_trigger();
     if (pc > a.cap) pc = a.cap;
     const int npc = (pc + PIV_ITEM_ROWS - 1) / PIV_ITEM_ROWS;
     const int t = threadIdx.x;
@@ -727,7 +732,6 @@ __global__ void __launch_bounds__(MG_NT) k_merge(MergeArgs a) {
     const float Dh = red[0][MG_COLS];
     if (t < MG_COLS) a.o[(size_t)qh * D + half * MG_COLS + t] = red[0][t] / Dh;
     if (half == 0 && t == 0) {
-        verkv_head_stats st = a.qstats[qh];
         st.D_hat = Dh;
         st.M2 = red[0][MG_COLS + 1];
         st.lse = st.m + logf(Dh);
