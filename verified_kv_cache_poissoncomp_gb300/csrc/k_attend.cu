@@ -19,12 +19,14 @@
 //                              id -- the zero-copy fetch and the refine in one pass, no staging.
 //             When the sketch is exact the GPU already holds every key, so K comes from the sketch
 //             by token id and only the V rows cross the host link.
-// k_partial_staged   the ROWS_PIVOTAL items of the MEMCPY path with each item's rows, ids and r
-//             bulk-copied into a two-stage shared-memory ring one item ahead; the same item code
-//             reads K and V from shared memory, so the sums are bitwise those of k_partial.
+// k_pivotal   the pivotal set's pass of the MEMCPY path (during the host gather): a producer warp
+//             streams 64-row stages of K|V rows (TMA tensor copies, 128-byte swizzle), ids and r
+//             into a two-stage shared-memory ring; four consumer warps sum them on the tensor cores
+//             with the stage code of pivotal_mma.cuh, which every pivotal path shares (the same
+//             bits); each CTA takes a run of 256-row chunks holding about an equal share of rows.
 // k_refine    the zero-copy path's partial sums in one launch: the ROWS_HOST items of every KV
 //             head, each deriving its rows from the selection bitmaps of one token-id range (no
-//             fetch list needed), and the ROWS_PIVOTAL items.
+//             fetch list needed), and the pivotal items (the same stage code).
 // k_merge     sums the partials in a fixed order and writes o = N-hat / D-hat, m + log D-hat and
 //             the per-head statistics.
 // k_dense_host, k_dense_merge   the offloaded-dense baseline: exact attention over every token with
