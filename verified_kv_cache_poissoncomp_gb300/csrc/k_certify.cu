@@ -68,9 +68,12 @@ struct Merged {
 };
 constexpr int FIX_SPLIT = 18;
 
-int certify_cluster_size(int n) {
+int certify_cluster_size(int n, int qheads, int sms) {
     if (n <= 8192) return 1;
-    if (n <= 32768) return 4;
+    // Up to 32K tokens: clusters of 4 while the grid fits the GPU in one wave (the kernel then
+    // ends with its slowest head), else clusters of 2 with twice the tokens per CTA: half the CTAs,
+    // and half the exchanges and barriers per token, for grids that take several waves.
+    if (n <= 32768) return (long long)qheads * 4 <= sms ? 4 : 2;
     return CT_MAX_CL;
 }
 int certify_chunk(int n, int cl) {
@@ -369,11 +372,12 @@ __device__ __forceinline__ void select_step(const Merged &mh, SelState &ss, SelS
 // removes the resident tokens, scans the counts and writes the ascending ids, one coalesced
 // store per bitmap word and warp; it then rearms the counter for the next call.
 constexpr int FL_MAX_WPT = 4;  // bitmap words per thread: n <= 131072 = 4 * 32 * CT_NT
-// Tokens (and bitmap words) a thread holds: clusters of 1 and 4 cover n <= 8192 and n <= 32768,
-// so a CTA's chunk is at most 8 * CT_NT tokens and the whole bitmap at most CT_NT words.
+// Tokens (and bitmap words) a thread holds: clusters of 1 and 4 cover n <= 8192 and n <= 32768
+// with a CTA's chunk at most 8 * CT_NT tokens; clusters of 2 (n <= 32768) and of 8 take up to
+// 16 * CT_NT; the whole bitmap is at most CT_NT words except with clusters of 8.
 template <int CL>
 struct PerThread {
-    static constexpr int tokens = CL == CT_MAX_CL ? 16 : 8;
+    static constexpr int tokens = (CL == CT_MAX_CL || CL == 2) ? 16 : 8;
     static constexpr int words = CL == CT_MAX_CL ? FL_MAX_WPT : 1;
 };
 
@@ -1072,6 +1076,8 @@ cudaError_t launch_certify(const CertifyArgs &a, int qheads, size_t smem, cudaSt
     switch (a.cl) {
         case 1: return sl ? launch_certify_cl<1, true>(a, qheads, smem, s)
                           : launch_certify_cl<1, false>(a, qheads, smem, s);
+        case 2: return sl ? launch_certify_cl<2, true>(a, qheads, smem, s)
+                          : launch_certify_cl<2, false>(a, qheads, smem, s);
         case 4: return sl ? launch_certify_cl<4, true>(a, qheads, smem, s)
                           : launch_certify_cl<4, false>(a, qheads, smem, s);
         case CT_MAX_CL: return sl ? launch_certify_cl<CT_MAX_CL, true>(a, qheads, smem, s)

@@ -595,7 +595,7 @@ verkv_status verkv_attend_verified(verkv_ctx *ctx, int32_t layer, const void *q,
     ca.err = ctx->err;
     ca.n = n;
     ca.W = ctx->L.W;
-    ca.cl = certify_cluster_size(n);
+    ca.cl = certify_cluster_size(n, ctx->L.qh_layer, ctx->sms);
     ca.chunk = certify_chunk(n, ca.cl);
     ca.eps = eps;
     ca.ldelta = (float)log(2.0 / (double)delta);

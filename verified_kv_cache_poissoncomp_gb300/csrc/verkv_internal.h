@@ -153,7 +153,7 @@ struct ShortlistArgs {
     LayerIdx li;
 };
 cudaError_t launch_shortlist(const ShortlistArgs &a, int units_layer, cudaStream_t s);
-int certify_cluster_size(int n);
+int certify_cluster_size(int n, int qheads, int sms);
 int certify_chunk(int n, int cl);
 size_t certify_smem_bytes(int chunk);
 

@@ -112,7 +112,9 @@ extern "C" verkv_status verkv_certify_noalloc(int device, void *stream, int32_t 
     ca.err = err_out;
     ca.n = n;
     ca.W = (n + 31) / 32;
-    ca.cl = certify_cluster_size(n);
+    int sms = 0;
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device) != cudaSuccess) return VERKV_ECUDA;
+    ca.cl = certify_cluster_size(n, units * G, sms);
     ca.chunk = certify_chunk(n, ca.cl);
     ca.eps = eps;
     ca.ldelta = (float)log(2.0 / (double)delta);
