@@ -1173,7 +1173,7 @@ def measure_estimator(batch, steps, warmup, dev):
 
 
 def measure_memcpy_fetch(w, pcs_unused, queries, steps_q, dev, link):
-    """The benchmark spec's literal fetch path on the benchmark workload: VERKV_FETCH_MEMCPY (the host
+    """The literal cudaMemcpyAsync fetch path on the benchmark workload: VERKV_FETCH_MEMCPY (the host
     waits for the selection, host threads gather the selected V rows into page-locked staging,
     cudaMemcpyAsync moves them on the side stream, then the staged rows are summed).  Eager calls
     over `steps_q` queries with per-launch events on both streams; per query the pivotal sums
