@@ -1059,8 +1059,7 @@ static cudaError_t launch_certify_cl(const CertifyArgs &a, int qheads, size_t sm
     // When the grid fits the GPU in one wave it may be scheduled while the scoring kernel
     // finishes: it first loads r (written by a call that completed before the scoring kernel, a
     // plain launch, began) and waits for the scoring kernel before it reads the logits.  A grid
-    // of several waves is launched in plain stream order: early-placed clusters slowed a
-    // graph-replayed decode step of 1024 CTAs per call by ~15 %.
+    // of several waves is launched in plain stream order (an early start showed no gain there).
     attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[1].val.programmaticStreamSerializationAllowed = 1;
     int sms = 0, dev = 0;

@@ -164,8 +164,11 @@ size_t certify_smem_bytes(int chunk);
 constexpr int PART_ROWS = 64;                      // fetched rows a CTA has in flight
 constexpr int PIV_STAGE_ROWS = 64;                 // pivotal rows staged in shared memory at once
 constexpr int PIV_ITEM_ROWS = 256;                 // pivotal list positions per partial
-constexpr int FET_RANGE = 1024;                    // token ids per partial of fetched rows
-constexpr int RMASK_W = 131072 / FET_RANGE / 32;   // words of a unit's non-empty-range mask
+// Token ids per partial of fetched rows: a multiple of 32 (whole bitmap words).  (512- and
+// 768-token ranges measured slower: more items and partials for the same rows.)
+constexpr int FET_RANGE = 1024;
+constexpr int RMASK_RANGES = (131072 + FET_RANGE - 1) / FET_RANGE;  // ranges of the largest unit
+constexpr int RMASK_W = (RMASK_RANGES + 31) / 32;                 // words of a unit's range mask
                                                    // (n <= 131072)
 enum { ROWS_PIVOTAL = 0, ROWS_STAGED = 1, ROWS_HOST = 2 };
 struct PartialArgs {
