@@ -437,16 +437,6 @@ __host__ __device__ constexpr size_t pv_smem_bytes() {
     return 1024 + (size_t)PV_NS * PivLayout<D>::BYTES;
 }
 
-// Tensor copy of one box into shared memory, completing on `bar` (coordinates innermost first).
-__device__ __forceinline__ void tma_load_3d(void *dst, const CUtensorMap *map, int x, int y, int z,
-                                            uint64_t *bar) {
-    asm volatile(
-        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes "
-        "[%0], [%1, {%2, %3, %4}], [%5];" ::"r"(smem_addr(dst)),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(smem_addr(bar))
-        : "memory");
-}
-
 template <int D, int G, bool SKL>
 __global__ void __launch_bounds__(PV_NT, PV_CTAS_PER_SM) k_pivotal(PartialArgs a, int units_layer,
                                                                   const __grid_constant__ CUtensorMap rows_map) {
@@ -572,22 +562,10 @@ __global__ void __launch_bounds__(PV_NT, PV_CTAS_PER_SM) k_pivotal(PartialArgs a
 }
 
 // The tensor map of a pivotal buffer: [rows][2][d] bf16 (rows = every unit's capacity), boxes of
-// 64 channels x 1 x 64 rows with the 128-byte swizzle.  cuTensorMapEncodeTiled is reached through
-// the runtime's driver entry point (no link against the driver library).
-typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
-                                  const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
-                                  const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
-                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+// 64 channels x 1 x 64 rows with the 128-byte swizzle.
 static cudaError_t pivotal_rows_map(CUtensorMap *map, const void *rows, long long nrows, int d) {
-    static EncodeTiledFn encode = nullptr;
-    if (!encode) {
-        void *fn = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        const cudaError_t e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000,
-                                                               cudaEnableDefault, &q);
-        if (e != cudaSuccess || q != cudaDriverEntryPointSuccess || !fn) return cudaErrorNotSupported;
-        encode = reinterpret_cast<EncodeTiledFn>(fn);
-    }
+    const EncodeTiledFn encode = tensor_map_encoder();
+    if (!encode) return cudaErrorNotSupported;
     const cuuint64_t dims[3] = {(cuuint64_t)d, 2, (cuuint64_t)nrows};
     const cuuint64_t strides[2] = {(cuuint64_t)d * 2, (cuuint64_t)d * 4};
     const cuuint32_t box[3] = {64, 1, (cuuint32_t)PIV_STAGE_ROWS};

@@ -13,10 +13,42 @@
 // runs these functions in the same order, so all of them produce the same bits.
 #pragma once
 
+#include <cuda.h>
+
 #include "verkv_common.cuh"
 #include "verkv_internal.h"
 
 namespace verkv {
+
+// ---------------------------------------------------------------------------------------------
+// Tensor copies.  One box into shared memory, completing on `bar` (coordinates innermost first).
+__device__ __forceinline__ void tma_load_3d(void *dst, const CUtensorMap *map, int x, int y, int z,
+                                            uint64_t *bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes "
+        "[%0], [%1, {%2, %3, %4}], [%5];" ::"r"(smem_addr(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(smem_addr(bar))
+        : "memory");
+}
+
+// cuTensorMapEncodeTiled, reached through the runtime's driver entry point (no link against the
+// driver library); null where the driver does not provide it.
+typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                                  const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                                  const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+inline EncodeTiledFn tensor_map_encoder() {
+    static EncodeTiledFn encode = nullptr;
+    if (!encode) {
+        void *fn = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        const cudaError_t e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000,
+                                                               cudaEnableDefault, &q);
+        if (e == cudaSuccess && q == cudaDriverEntryPointSuccess && fn)
+            encode = reinterpret_cast<EncodeTiledFn>(fn);
+    }
+    return encode;
+}
 
 // ---------------------------------------------------------------------------------------------
 // PTX wrappers.  Fragment layouts follow the PTX ISA for mma.m16n8k16 with .bf16 operands: with
