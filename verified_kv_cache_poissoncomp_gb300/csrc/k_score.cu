@@ -256,7 +256,7 @@ cudaError_t launch_score(const ScoreArgs &a, int units_layer, cudaStream_t s, bo
 // ---------------------------------------------------------------------------------------------
 // k_sketch_stream: the bytes k_score moves, without its arithmetic -- the same grid, spans, stages
 // and tensor copies, with thread 0 waiting on each stage and refilling its slot at once.  Its time
-// is that of a bare one-launch read of a layer's sketch: the reference k_score's time is judged by.
+// is that of a bare one-launch read of a layer's sketch: the reference k_score's time is set against.
 template <int D>
 __global__ void __launch_bounds__(TC_NT, TC_CTAS_PER_SM) k_sketch_stream(ScoreArgs a, int spans_per_unit,
                                                                        int span_rows,
