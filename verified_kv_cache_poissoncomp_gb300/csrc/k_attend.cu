@@ -732,7 +732,10 @@ cudaError_t launch_merge(const MergeArgs &a, int qheads, cudaStream_t s) {
 // ---------------------------------------------------------------------------------------------
 // k_refine: the zero-copy path's partial sums in one launch -- the fetched-row ranges of every
 // layer unit first (so the host reads start at once), then its pivotal blocks (their HBM reads
-// hide behind the host link).  k_merge follows.
+// hide behind the host link).  When there are more items than resident CTAs (batch 8, 128K), the
+// CTAs take items in that order from a counter (one atomic per item), so a CTA that drew light
+// ranges takes more of them and the launch ends within about one item of its last host read.
+// Each item writes its own partial, so which CTA took it does not change a bit.  k_merge follows.
 template <int D, int G, bool SKL>
 __global__ void __launch_bounds__(128, 3) k_refine(PartialArgs piv, PartialArgs fet, int units_layer) {
     extern __shared__ __align__(128) unsigned char kr_stage[];  // PivLayout<D>::BYTES
@@ -742,10 +745,24 @@ __global__ void __launch_bounds__(128, 3) k_refine(PartialArgs piv, PartialArgs 
     static_assert(WR >= 16 && WR <= 64, "the range's words are scanned by at most two warps");
     __shared__ int32_t s_ids[FET_RANGE];
     __shared__ int s_wsum[2];
+    __shared__ int s_item;
     const int per_unit = fet.max_chunks + piv.max_chunks;
     const int total = units_layer * per_unit;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    for (int item = blockIdx.x; item < total; item += gridDim.x) {
+    // When every item has a CTA of its own (one wave, as at batch 1) CTA b takes item b and no
+    // counter is touched: an atomic round trip per CTA measured slower there.
+    const bool one_wave = total <= (int)gridDim.x;
+    for (int pass = 0;; ++pass) {
+        int item;
+        if (one_wave) {
+            item = pass == 0 ? (int)blockIdx.x : total;
+        } else {
+            if (tid == 0) s_item = atomicAdd(fet.refine_next, 1);
+            __syncthreads();
+            item = s_item;
+            __syncthreads();  // every thread has read it before thread 0 takes the next
+        }
+        if (item >= total) break;
         const int k = item / units_layer, ul = item - k * units_layer;
         const int ug = fet.li.unit_global(ul);
         if (k < fet.max_chunks) {

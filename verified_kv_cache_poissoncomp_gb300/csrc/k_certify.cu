@@ -1018,6 +1018,9 @@ __global__ void __launch_bounds__(CT_NT, 1) k_certify(CertifyArgs a) {
     }
     // The refine's non-empty-range mask of this KV head starts empty.
     if (a.rmask && crank == 0 && qh == ul * G && tid < RMASK_W) a.rmask[ul * RMASK_W + tid] = 0u;
+    // So does the refine's item counter (the refine of the previous call ended before this call's
+    // scoring kernel, a plain launch, began).
+    if (a.refine_next && blockIdx.x == 0 && tid == 0) *a.refine_next = 0;
     if (tid == 0 && crank == 0) {
         verkv_head_stats st;
         st.m = m;

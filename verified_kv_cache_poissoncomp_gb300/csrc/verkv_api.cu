@@ -39,7 +39,7 @@ bool bad16(const void *p) { return ((uintptr_t)p & 15u) != 0; }
 bool bad4(const void *p) { return ((uintptr_t)p & 3u) != 0; }
 
 struct Layout {
-    size_t err, flc, nacc, rmask, scores, qstats, F, slb, fids, fcounts, staging, part_piv, part_fet, total;
+    size_t err, flc, nacc, rmask, rnext, scores, qstats, F, slb, fids, fcounts, staging, part_piv, part_fet, total;
     int W, units_layer, qh_layer, max_piv, max_fet, dense_chunks;
 };
 
@@ -79,6 +79,7 @@ bool make_layout(const verkv_shape *s, Layout &L) {
     L.flc = take((size_t)L.units_layer * 4);
     L.nacc = take((size_t)L.qh_layer * 4);
     L.rmask = take((size_t)L.units_layer * RMASK_W * 4);
+    L.rnext = take(4);
     L.scores = take((size_t)L.qh_layer * n * 4);
     L.qstats = take((size_t)L.qh_layer * sizeof(verkv_head_stats));
     L.F = take((size_t)L.qh_layer * L.W * 4);
@@ -193,6 +194,7 @@ struct verkv_ctx {
     int32_t *flc = nullptr;  // per-KV-head completion counters of the certify kernel's fetch list
     int32_t *nacc = nullptr; // per-query-head n_fetch accumulators of the zero-copy refine
     uint32_t *rmask = nullptr; // per-KV-head masks of fetched-row ranges holding rows
+    int32_t *rnext = nullptr;  // the zero-copy refine's item counter
     uint32_t *slb = nullptr; // per-KV-head shortlist bitmaps
     int shortlist = 0;       // shortlist size per KV head; 0: every token of L may be fetched
     bool shortlisted = false;  // the last attend built shortlists
@@ -386,6 +388,7 @@ verkv_status verkv_create(verkv_ctx **out, int device, void *stream, const verkv
     ctx->flc = (int32_t *)(w + L.flc);
     ctx->nacc = (int32_t *)(w + L.nacc);
     ctx->rmask = (uint32_t *)(w + L.rmask);
+    ctx->rnext = (int32_t *)(w + L.rnext);
     ctx->slb = (uint32_t *)(w + L.slb);
     ctx->staging = (uint16_t *)(w + L.staging);
     ctx->part_piv = (float *)(w + L.part_piv);
@@ -395,6 +398,7 @@ verkv_status verkv_create(verkv_ctx **out, int device, void *stream, const verkv
     if (e == cudaSuccess) e = cudaMemsetAsync(ctx->flc, 0, (size_t)L.units_layer * 4, ctx->main);
     if (e == cudaSuccess) e = cudaMemsetAsync(ctx->nacc, 0, (size_t)L.qh_layer * 4, ctx->main);
     if (e == cudaSuccess) e = cudaMemsetAsync(ctx->rmask, 0, (size_t)L.units_layer * RMASK_W * 4, ctx->main);
+    if (e == cudaSuccess) e = cudaMemsetAsync(ctx->rnext, 0, 4, ctx->main);
     if (e != cudaSuccess) {
         verkv_destroy(ctx);
         return VERKV_ECUDA;
@@ -606,6 +610,7 @@ verkv_status verkv_attend_verified(verkv_ctx *ctx, int32_t layer, const void *q,
     const bool need_list = ctx->fetch_mode != VERKV_FETCH_ZEROCOPY || fetch_ids_out || fetch_counts_out;
     ca.fl_counter = need_list ? ctx->flc : nullptr;
     ca.rmask = ctx->rmask;
+    ca.refine_next = ctx->rnext;
     ca.ids = ctx->fids;
     ca.counts = ctx->fcounts;
     ca.ids_user = fetch_ids_out;
@@ -713,6 +718,7 @@ verkv_status verkv_fetch_refine(verkv_ctx *ctx, const int32_t *ids, const int32_
         pa.voff16 = d / 8;
         pa.resident = ctx->piv.resident;
         pa.nacc = ctx->nacc;
+        pa.refine_next = ctx->rnext;
         ma.nacc = ctx->nacc;
         const PartialArgs piv = pivotal_args(ctx, ctx->piv, ctx->q, li, ctx->sketch_exact);
         const int items = ctx->L.units_layer * (ctx->L.max_fet + ctx->L.max_piv);

@@ -135,6 +135,7 @@ struct CertifyArgs {
     int32_t *counts_host;
     const uint32_t *shortlist;    // [units_layer][W] fetch candidates, or null: all of L
     uint32_t *rmask;              // [units_layer][RMASK_W] cleared here for the refine, or null
+    int32_t *refine_next;         // the refine's item counter, set to 0 here, or null
     int n, W, cl, chunk;
     float eps, ldelta;
     LayerIdx li;
@@ -189,6 +190,8 @@ struct PartialArgs {
     const uint32_t *resident; // ROWS_HOST in k_refine: the resident bitmaps [units][W]
     int32_t *nacc;            // ROWS_HOST in k_refine: per query head n_fetch accumulators
                               // [qh], zero on entry (k_merge resets them)
+    int32_t *refine_next;     // k_refine: the next item to take, 0 on entry (the certify kernel
+                              // of the same call resets it)
     uint32_t *rmask;          // fetched-row ranges: bit k of [units_layer][RMASK_W] set when
                               // range k holds rows (only those get a partial); zero on entry
     const int64_t *staged_off; // ROWS_STAGED: first staged row of each layer unit (the staged
