@@ -142,7 +142,8 @@ enum { VERKV_FETCH_ZEROCOPY = 0, VERKV_FETCH_MEMCPY = 1, VERKV_FETCH_KEYS = 4 };
  *   n_fetch    |F \ S| for this head (rows not already resident)
  *   iters      iterations of the beta solve
  *   flags      or of: 1 the beta solve hit its cap; 2 the select ran out of passes;
- *              4 (shortlist variant only) the whole shortlist left eps-hat >= eps */
+ *              4 (shortlist variant only) the whole shortlist left eps-hat >= eps;
+ *              8 the select ended by ranking its last candidates in one CTA (information only) */
 typedef struct {
     float m, D, beta, V, b, eps_hat, eps_final, D_hat, M2, lse;
     int32_t certified, k_star, n_L, n_fetch, iters, flags;
@@ -319,8 +320,13 @@ verkv_status verkv_certify_noalloc(int device, void *stream, int32_t units, int3
  *                            issues, and its bounded copy waits give up after `value` ns; the
  *                            kernel latches VERKV_ETIMEOUT (returned by verkv_sync) and returns,
  *                            and the context stays usable.  One call only.
+ *   VERKV_INJECT_SELECT_GATHER value 0: the selection never ends by gathering its last candidates
+ *                            into one CTA (clusters of 1 and 4 do by default, when at most 512
+ *                            remain) but runs its histogram passes to the end, for a bitwise
+ *                            comparison of the two; 1 restores the default.
  * Returns VERKV_EINVAL for an unknown `what` or a value out of range. */
-enum { VERKV_INJECT_COPY_FAIL = 1, VERKV_INJECT_BETA_MAXIT = 2, VERKV_INJECT_SCORE_STALL = 3 };
+enum { VERKV_INJECT_COPY_FAIL = 1, VERKV_INJECT_BETA_MAXIT = 2, VERKV_INJECT_SCORE_STALL = 3,
+       VERKV_INJECT_SELECT_GATHER = 4 };
 verkv_status verkv_test_inject(verkv_ctx *ctx, int what, int64_t value);
 
 /* Measurement.  Every kernel launch is counted per kernel; with profiling enabled each launch is

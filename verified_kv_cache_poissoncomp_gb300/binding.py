@@ -36,6 +36,7 @@ EXPORTED = ["verkv_sketch_bytes", "verkv_workspace_size", "verkv_create", "verkv
             "verkv_attend_dense_host", "verkv_set_shortlist", "verkv_shortlist_bitmap",
             "verkv_profile_timeline", "verkv_test_inject", "verkv_measure_sketch_stream"]
 VERKV_INJECT_COPY_FAIL, VERKV_INJECT_BETA_MAXIT, VERKV_INJECT_SCORE_STALL = 1, 2, 3
+VERKV_INJECT_SELECT_GATHER = 4
 # kernel ids (include/verkv.h), in launch order
 (VERKV_K_PC_SOLVE, VERKV_K_PC_GATHER, VERKV_K_SKETCH, VERKV_K_SCORE, VERKV_K_CERTIFY,
  VERKV_K_PARTIAL_PIVOTAL, VERKV_K_FETCH_HOST, VERKV_K_PARTIAL_STAGED, VERKV_K_MERGE,

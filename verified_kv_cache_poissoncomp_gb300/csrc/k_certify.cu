@@ -24,7 +24,8 @@
 //      memory and 256 threads, one per bin, scan them for the bin in which eps-hat of the
 //      remaining tokens drops below eps.  The first window spans 32 octaves under the largest possible g
 //      at 8 bins per octave and folds everything below into bin 0; the select ends when the cut
-//      bin holds one token;
+//      bin holds one token.  With clusters of 1 and 4, once the cut bin holds at most SEL_GATHER
+//      tokens they are gathered into rank 0 and ranked there instead (the same result bits);
 //   tail  the last of a KV head's G clusters to finish builds that head's fetch list (KVFetch
 //      step 5: the rows of the union of the G sets F that are not resident), so the list is
 //      ready when the kernel ends.
@@ -67,6 +68,15 @@ struct Merged {
     unsigned long long sb[256], sv[256];
 };
 constexpr int FIX_SPLIT = 18;
+// A candidate token of the select's cut bin, gathered into rank 0 when the bin holds at most
+// SEL_GATHER tokens: its g bits, token id, w-hat and r (its Lemma 1 terms are recomputed there).
+struct GatherCand {
+    uint32_t g;
+    int token;
+    float w, r;
+};
+constexpr int SEL_GATHER = 512;
+static_assert(SEL_GATHER * 12 <= 6 * 256 * 4, "the rank scratch (order and keys) fits a histogram buffer");
 
 int certify_cluster_size(int n, int qheads, int sms) {
     if (n <= 8192) return 1;
@@ -85,7 +95,8 @@ size_t certify_smem_bytes(int chunk) {
            + (size_t)2 * CT_MAX_CL * CT_REC * 4         // CTA records from the cluster, two buffers
            + 2 * sizeof(Hist)                           // two histogram buffers
            + sizeof(Merged)                             // merged copy
-           + (size_t)chunk * 12 + 64;
+           + (size_t)chunk * 12 + 64
+           + (size_t)SEL_GATHER * sizeof(GatherCand);    // gathered select candidates (clusters of 1, 4)
 }
 
 // Cluster-wide all-reduce of a K-float record held identically by the lanes of each warp.
@@ -237,9 +248,17 @@ struct SelState {
     int shift;                            // bin width 2^shift keys
     int absorb;                           // bin 0 also takes every candidate below lo
     int above;                            // tokens known to be in F
+    int ncand;                            // tokens with keys in [cand_lo, cand_hi)
     int done, kstar;
     float eps_final;
 };
+
+// eps-hat D of a remaining set from its exact fixed-point sums and its max b (float bits), as
+// every select decision evaluates it (Eq. (10)).
+__device__ __forceinline__ float remaining_epsD(unsigned long long sb, unsigned long long sv, uint32_t mb,
+                                                float iSB, float iSV, float l) {
+    return u64_to_float(sb) * iSB + bern(__uint_as_float(mb), u64_to_float(sv) * iSV, l);
+}
 
 // One pass's scan of the merged histogram and the select's next state (Eq. (10): eps-hat of the
 // remaining set, nonincreasing as tokens are taken in g order).  Threads 0..SEL_NT-1 take one bin
@@ -303,7 +322,7 @@ __device__ __forceinline__ void select_step(const Merged &mh, SelState &ss, SelS
     const uint32_t best_c = pc + ic - c;
     const uint32_t best_m = max(Bm, max(pm, xm));
     const unsigned long long best_b = Bb + pb + ib - sb, best_v = Bv + pv + iv - sv;
-    const float best_e = u64_to_float(best_b) * iSB + bern(__uint_as_float(best_m), u64_to_float(best_v) * iSV, l);
+    const float best_e = remaining_epsD(best_b, best_v, best_m, iSB, iSV, l);
     const uint32_t best_n = c;
     int jb = (c > 0u && best_e < epsD) ? tid : -1;
 #pragma unroll
@@ -316,8 +335,7 @@ __device__ __forceinline__ void select_step(const Merged &mh, SelState &ss, SelS
         if (tid == 0) {  // rounding left no bin qualifying: take every candidate
             ss.kstar = ss.above + (int)total;
             ss.fthr = ss.absorb ? 0ull : ss.cand_lo;
-            ss.eps_final =
-                (u64_to_float(Bb) * iSB + bern(__uint_as_float(Bm), u64_to_float(Bv) * iSV, l)) / D;
+            ss.eps_final = remaining_epsD(Bb, Bv, Bm, iSB, iSV, l) / D;
             ss.done = 1;
         }
         return;
@@ -342,6 +360,7 @@ __device__ __forceinline__ void select_step(const Merged &mh, SelState &ss, SelS
             return;
         }
         // Slide the window down at the same resolution; it ends where bin 0 ended.
+        ss.ncand = cj;
         ss.cand_lo = 0ull;
         ss.cand_hi = lo + (1ull << shift);
         const unsigned long long span = 255ull << shift;
@@ -359,6 +378,7 @@ __device__ __forceinline__ void select_step(const Merged &mh, SelState &ss, SelS
         ss.done = 1;
         return;
     }
+    ss.ncand = cj;
     ss.cand_lo = cut_lo;
     ss.cand_hi = cut_lo + (1ull << shift);
     ss.lo = cut_lo;
@@ -489,6 +509,196 @@ __device__ __forceinline__ void fetch_list_tail(const CertifyArgs &a, int ul, in
     }
 }
 
+// The end of the select when the candidates (keys in [cand_lo, cand_hi), ss.ncand of them, at most
+// SEL_GATHER) are few.  Every CTA appends its candidates to rank 0's buffer; rank 0 orders them by
+// key (g descending, ties to the lower id: the keys are unique), recomputes each one's Lemma 1
+// terms and fixed-point parts exactly as the histogram passes do, and forms for every k the sums
+// of the set that remains when the first k are taken: the tokens known to remain plus the
+// candidates after rank k (exact 64-bit suffix sums, a suffix max of b).  k* is the smallest k in
+// [1, ncand] whose remaining set certifies (all of them if rounding leaves none), evaluated with
+// the same expression as the histogram scan, so F, k* and eps-hat are the bits the finer passes
+// would give.  Rank 0 writes the result into every CTA's select state; `ord` is rank 0's scratch
+// of SEL_GATHER ints followed by SEL_GATHER 64-bit keys.
+template <int CL>
+__device__ __noinline__ void gather_select(cg::cluster_group &cluster, int crank, int tid, SelState &ss,
+                                           int &s_gn, GatherCand *gbuf, int *ord, const float *W,
+                                           const float *R, const uint32_t *X, int chunk, int base,
+                                           float beta, float SB, float SV, float l, float epsD,
+                                           float D) {
+    constexpr int TPT = PerThread<CL>::tokens;
+    const int lane = tid & 31, warp = tid >> 5;
+    {
+        // The thread's candidates, their offsets in this CTA (a block scan of the counts) and one
+        // remote atomic per CTA for the CTA's place in rank 0's buffer.
+        __shared__ int s_wc[CT_NW];
+        __shared__ int s_base;
+        const unsigned long long clo = ss.cand_lo, chi = ss.cand_hi;
+        uint32_t cm = 0u;
+#pragma unroll
+        for (int q = 0; q < TPT; ++q) {
+            const int i = tid + q * CT_NT;
+            if (i < chunk && R[i] < 1.0f) {
+                const unsigned long long key = key64(X[i], base + i);
+                if (key >= clo && key < chi) cm |= 1u << q;
+            }
+        }
+        const int c = __popc(cm);
+        int incl = c;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int y = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+            if (lane >= o) incl += y;
+        }
+        if (lane == 31) s_wc[warp] = incl;
+        __syncthreads();
+        if (warp == 0) {
+            const int t = s_wc[lane];
+            int x = t;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int y = __shfl_up_sync(0xFFFFFFFFu, x, o);
+                if (lane >= o) x += y;
+            }
+            s_wc[lane] = x - t;  // exclusive
+            if (lane == 31 && x > 0) s_base = atomicAdd(cluster.map_shared_rank(&s_gn, 0), x);
+        }
+        __syncthreads();
+        if (cm) {
+            GatherCand *gb0 = cluster.map_shared_rank(gbuf, 0);
+            int slot = s_base + s_wc[warp] + incl - c;
+            for (uint32_t m = cm; m; m &= m - 1u, ++slot) {
+                const int i = tid + (__ffs(m) - 1) * CT_NT;
+                if (slot < SEL_GATHER) gb0[slot] = GatherCand{X[i], base + i, W[i], R[i]};
+            }
+        }
+    }
+    cluster.sync();  // every candidate is in rank 0's buffer
+    if (crank == 0) {
+        __shared__ unsigned long long s_sb[CT_NW], s_sv[CT_NW];
+        __shared__ uint32_t s_mb[CT_NW];
+        __shared__ int s_k;
+        const int nc = min(s_gn, SEL_GATHER);
+        unsigned long long *keys = reinterpret_cast<unsigned long long *>(ord + SEL_GATHER);
+        if (tid < nc) keys[tid] = key64(gbuf[tid].g, gbuf[tid].token);
+        if (tid == 0) s_k = nc;  // none certifies: take every candidate
+        __syncthreads();
+        // Rank of candidate j: how many keys exceed its own, counted by P lanes of one warp
+        // (P the largest power of two with P nc <= CT_NT, at most 32) over interleaved keys.
+        {
+            int P = 32;
+            while (P > 1 && P * nc > CT_NT) P >>= 1;
+            const int j = tid / P, part = tid - j * P;
+            int rk = 0;
+            if (j < nc) {
+                const unsigned long long kj = keys[j];
+                int q = part;
+#pragma unroll 1
+                for (; q + 3 * P < nc; q += 4 * P)
+                    rk += (keys[q] > kj ? 1 : 0) + (keys[q + P] > kj ? 1 : 0) +
+                          (keys[q + 2 * P] > kj ? 1 : 0) + (keys[q + 3 * P] > kj ? 1 : 0);
+                for (; q < nc; q += P) rk += keys[q] > kj ? 1 : 0;
+            }
+            for (int o = 1; o < P; o <<= 1) rk += __shfl_xor_sync(0xFFFFFFFFu, rk, o);
+            if (j < nc && part == 0) ord[rk] = j;
+        }
+        __syncthreads();
+        // Thread p holds the candidate of rank p.
+        const float iSB = SB > 0.0f ? 1.0f / SB : 0.0f;
+        const float iSV = SV > 0.0f ? 1.0f / SV : 0.0f;
+        unsigned long long qb = 0ull, qv = 0ull;
+        uint32_t mb = 0u;
+        if (tid < nc) {
+            const GatherCand c = gbuf[ord[tid]];
+            float bi, vi, bb;
+            token_terms(c.w, c.r, rho_of(c.r), beta, bi, vi, bb);
+            uint32_t h, lo;
+            fixed_split(bi, SB, h, lo);
+            qb = ((unsigned long long)h << FIX_SPLIT) + lo;
+            fixed_split(vi, SV, h, lo);
+            qv = ((unsigned long long)h << FIX_SPLIT) + lo;
+            mb = __float_as_uint(bb);
+        }
+        // Exclusive suffix sums (ranks after p) within the warp, then over the later warps.
+        unsigned long long eb = 0ull, ev = 0ull;
+        uint32_t em = 0u;
+        {
+            unsigned long long ib = qb, iv = qv;
+            uint32_t im = mb;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const unsigned long long yb = __shfl_down_sync(0xFFFFFFFFu, ib, o);
+                const unsigned long long yv = __shfl_down_sync(0xFFFFFFFFu, iv, o);
+                const uint32_t ym = __shfl_down_sync(0xFFFFFFFFu, im, o);
+                if (lane + o < 32) {
+                    ib += yb;
+                    iv += yv;
+                    im = max(im, ym);
+                }
+            }
+            if (lane == 0) {
+                s_sb[warp] = ib;
+                s_sv[warp] = iv;
+                s_mb[warp] = im;
+            }
+            eb = ib - qb;
+            ev = iv - qv;
+            const uint32_t xm = __shfl_down_sync(0xFFFFFFFFu, im, 1);
+            em = lane == 31 ? 0u : xm;
+        }
+        __syncthreads();
+        if (warp == 0) {  // exclusive suffix over the warps' totals, in place
+            unsigned long long tb = s_sb[lane], tv = s_sv[lane];
+            uint32_t tm = s_mb[lane];
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const unsigned long long yb = __shfl_down_sync(0xFFFFFFFFu, tb, o);
+                const unsigned long long yv = __shfl_down_sync(0xFFFFFFFFu, tv, o);
+                const uint32_t ym = __shfl_down_sync(0xFFFFFFFFu, tm, o);
+                if (lane + o < 32) {
+                    tb += yb;
+                    tv += yv;
+                    tm = max(tm, ym);
+                }
+            }
+            const unsigned long long xb = __shfl_down_sync(0xFFFFFFFFu, tb, 1);
+            const unsigned long long xv = __shfl_down_sync(0xFFFFFFFFu, tv, 1);
+            const uint32_t xm = __shfl_down_sync(0xFFFFFFFFu, tm, 1);
+            __syncwarp();
+            s_sb[lane] = lane == 31 ? 0ull : xb;
+            s_sv[lane] = lane == 31 ? 0ull : xv;
+            s_mb[lane] = lane == 31 ? 0u : xm;
+        }
+        __syncthreads();
+        eb += s_sb[warp];
+        ev += s_sv[warp];
+        em = max(em, s_mb[warp]);
+        // Taking ranks 0..p (k = p + 1) leaves the known remainder and the ranks after p.
+        float e = 0.0f;
+        bool ok = false;
+        if (tid < nc) {
+            e = remaining_epsD(ss.Bb + eb, ss.Bv + ev, max(ss.Bm, em), iSB, iSV, l);
+            ok = e < epsD;
+        }
+        if (ok) atomicMin(&s_k, tid + 1);
+        __syncthreads();
+        const int ks = s_k;
+        if (tid == ks - 1) {
+            const GatherCand c = gbuf[ord[tid]];
+            const unsigned long long ft = key64(c.g, c.token);
+            const int kstar = ss.above + ks;
+            const float efin = e / D;
+            for (int c2 = 0; c2 < CL; ++c2) {
+                SelState *r = cluster.map_shared_rank(&ss, c2);
+                r->fthr = ft;
+                r->kstar = kstar;
+                r->eps_final = efin;
+                r->done = 1;
+            }
+        }
+    }
+    cluster.sync();  // every CTA holds the result
+}
+
 template <int CL, bool SL>
 __global__ void __launch_bounds__(CT_NT, 1) k_certify(CertifyArgs a) {
     pdl_trigger();  // the refine kernel after this one may be scheduled early
@@ -501,6 +711,7 @@ __global__ void __launch_bounds__(CT_NT, 1) k_certify(CertifyArgs a) {
     float *W = reinterpret_cast<float *>(hist + 2);  // logit, then w-hat
     float *R = W + a.chunk;                          // r (1 for H and padding)
     uint32_t *X = reinterpret_cast<uint32_t *>(R + a.chunk);  // r/(1-r), later the g key
+    GatherCand *gbuf = reinterpret_cast<GatherCand *>(X + a.chunk);  // rank 0: the select's candidates
 
     cg::cluster_group cluster = cg::this_cluster();
     const int crank = (int)cluster.block_rank();
@@ -854,6 +1065,8 @@ __global__ void __launch_bounds__(CT_NT, 1) k_certify(CertifyArgs a) {
         // is capped below the float range; a zero total gives zero sums).
         const float SB = betaL > 0.0f ? fminf(562949953421312.0f / betaL, 1e38f) : 0.0f;
         const float SV = VL > 0.0f ? fminf(562949953421312.0f / VL, 1e38f) : 0.0f;
+        __shared__ int s_gn;  // rank 0: candidates gathered
+        if (tid == 0) s_gn = 0;  // before the first pass's cluster barrier; appends come after it
         if (tid == 0) {
             // Every g_i D is at most eps-hat(L) D; the first window ends just above that.
             const uint32_t top = __float_as_uint(betaL + bern(b1, VL, l)) + 256u;
@@ -868,6 +1081,7 @@ __global__ void __launch_bounds__(CT_NT, 1) k_certify(CertifyArgs a) {
             ss.shift = 44;
             ss.absorb = 1;  // bin 0 also takes every candidate below lo
             ss.above = 0;
+            ss.ncand = 0;
             ss.done = 0;
             ss.kstar = 0;
             ss.eps_final = eps_hat;
@@ -991,6 +1205,20 @@ __global__ void __launch_bounds__(CT_NT, 1) k_certify(CertifyArgs a) {
             if (tid < SEL_NT) select_step(mh, ss, sx, tid, SB, SV, l, eps * D, D);
             __syncthreads();
             if (ss.done) break;
+            // Few candidates left (one-wave grids, where the slowest head sets the launch time):
+            // gather them into rank 0, rank them by key and take k* from exact suffix sums, with
+            // the bits the histogram passes would reach.  Measured faster for clusters of 4 at
+            // batch 1 (38.6 against 39.2 us) and slower for clusters of 2 at batch 8, where most
+            // heads need one more pass at most; clusters of 2 and 8 keep the passes.
+            if constexpr (CL == 1 || CL == 4) {
+                if (a.sel_gather && ss.ncand <= SEL_GATHER) {
+                    gather_select<CL>(cluster, crank, tid, ss, s_gn, gbuf,
+                                      reinterpret_cast<int *>(&hist[(pass + 1) & 1]), W, R, X, chunk,
+                                      base, beta, SB, SV, l, eps * D, D);
+                    flags |= 8;
+                    break;
+                }
+            }
         }
         // Peers may still be reading this CTA's last histogram: no CTA leaves before all have.
         cluster.sync();
@@ -1040,7 +1268,7 @@ __global__ void __launch_bounds__(CT_NT, 1) k_certify(CertifyArgs a) {
         st.iters = iters;
         st.flags = flags | (exhausted ? 4 : 0);
         a.qstats[qh] = st;
-        if (flags) raise_error(a.err, ERR_NOCONVERGE);
+        if (flags & 3) raise_error(a.err, ERR_NOCONVERGE);  // 8 only records the gathered finish
     }
     if (a.fl_counter) fetch_list_tail<CL>(a, ul, ug);
 }

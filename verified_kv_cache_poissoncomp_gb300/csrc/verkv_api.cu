@@ -220,6 +220,7 @@ struct verkv_ctx {
     // Failure injection (verkv_test_inject)
     int64_t inject_copy_fail = 0;    // fetch copies still to fail on the host
     int beta_maxit = 0;              // 0: the kernel's default cap
+    int sel_gather = 1;              // the select's gathered finish (clusters of 1 and 4)
     int64_t score_stall_ns = 0;      // > 0: the next attend's scoring kernel stalls one stage
     // Measurement
     int64_t launches[VERKV_K_COUNT] = {};
@@ -605,6 +606,7 @@ verkv_status verkv_attend_verified(verkv_ctx *ctx, int32_t layer, const void *q,
     ca.ldelta = (float)log(2.0 / (double)delta);
     ca.li = li;
     ca.beta_maxit = ctx->beta_maxit;
+    ca.sel_gather = ctx->sel_gather;
     // The per-KV-head fetch list is built only for those who read it: the MEMCPY gather, or a
     // caller asking for ids or counts.  The zero-copy refine reads the selection bitmaps.
     const bool need_list = ctx->fetch_mode != VERKV_FETCH_ZEROCOPY || fetch_ids_out || fetch_counts_out;
@@ -893,6 +895,10 @@ verkv_status verkv_test_inject(verkv_ctx *ctx, int what, int64_t value) {
         case VERKV_INJECT_SCORE_STALL:
             if (value < 1000 || value > 1000000000LL) break;
             ctx->score_stall_ns = value;
+            return VERKV_OK;
+        case VERKV_INJECT_SELECT_GATHER:
+            if (value < 0 || value > 1) break;
+            ctx->sel_gather = (int)value;
             return VERKV_OK;
         default:
             break;

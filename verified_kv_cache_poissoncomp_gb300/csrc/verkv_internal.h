@@ -140,6 +140,8 @@ struct CertifyArgs {
     float eps, ldelta;
     LayerIdx li;
     int beta_maxit;               // iteration cap of the beta solve (0: the default, 64)
+    int sel_gather;               // 1: clusters of 1 and 4 may end the select by gathering its
+                                  // last candidates into rank 0; 0: histogram passes only (tests)
 };
 cudaError_t launch_certify(const CertifyArgs &a, int qheads, size_t smem, cudaStream_t s);
 

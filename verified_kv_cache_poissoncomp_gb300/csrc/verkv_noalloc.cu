@@ -104,6 +104,7 @@ extern "C" verkv_status verkv_certify_noalloc(int device, void *stream, int32_t 
     if (launch_score(sa, units, s, false) != cudaSuccess) return VERKV_ECUDA;
 
     CertifyArgs ca{};
+    ca.sel_gather = 1;
     ca.scores = logits;
     ca.r_full = r_full;
     ca.resident = nullptr;  // not read by the certify kernel
