@@ -170,3 +170,16 @@ def test_without_fetch_outputs_matches_with_them():
         uncertified += int((s1[:, 10] == 0).sum())
     assert uncertified > 0  # the selection and the fetch ran
     eng.close()
+
+
+@pytest.mark.parametrize("n,G,d", [(40, 4, 128), (64, 4, 128), (65, 4, 128), (200, 4, 128),
+                                   (1000, 4, 128), (40, 8, 64), (65, 8, 64)])
+def test_short_and_ragged_contexts(n, G, d):
+    # Contexts shorter than one 64-row scoring stage or a stage and a row: the scoring kernel's
+    # tensor copies read past the unit's last row (zero fill, not stored), the certificate runs in
+    # one CTA with a partly filled last warp, and the refine's single token range is ragged.
+    w = I.make_workload("short", B=1, L=1, h_kv=2, G=G, d=d, n=n, eta=1 / 2, n_local=8,
+                        n_queries=4, plant_every=2)
+    rep, outs = _run_all(w)
+    assert rep["exact_F"] >= 0.9 * rep["heads"]
+    assert all(np.isfinite(o["o"]).all() and np.isfinite(o["lse"]).all() for o in outs)
