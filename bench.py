@@ -78,6 +78,9 @@ def parse_args():
                         "heads at 32K, eta in {1/8, 1/32}, eps = delta = 0.05")
     p.add_argument("--layers", type=int, default=36,
                    help="layers of the --decode-step and --long128k models")
+    p.add_argument("--groups", type=int, default=4,
+                   help="--decode-step / --long128k: the batch split over this many contexts, each "
+                        "on its own stream (each group's layers run in order; 1: one context)")
     p.add_argument("--pc-sweep", action="store_true",
                    help="PoissonComp throughput: 36 layers x 8 KV heads, n in {32K, 128K}, "
                         "eta in {1/8, 1/16, 1/32}")
@@ -689,7 +692,7 @@ def compact_model_steps(r):
         c["kernel_ms_per_step"] = {k: v["ms_per_step"] for k, v in row["per_kernel"].items()}
         rows.append(c)
     return {"config": r["config"], "steps": r["steps"], "warmup": r["warmup"],
-            "launch": "CUDA graph of one step, replayed", "rows": rows,
+            "launch": r.get("launch", "CUDA graph of one step, replayed"), "rows": rows,
             **{k: r[k] for k in ("planted_queries", "needle_frac_per_unit") if k in r}}
 
 
@@ -856,10 +859,10 @@ def run_eps_sweep(args, local):
 
 def run_model_steps(args, local, kind):
     print(json.dumps(measure_model_steps(local, kind, args.layers, args.steps, args.warmup,
-                                         verbose=not args.quiet)), flush=True)
+                                         verbose=not args.quiet, groups=args.groups)), flush=True)
 
 
-def measure_model_steps(local, kind, layers, steps, warmup, verbose=True):
+def measure_model_steps(local, kind, layers, steps, warmup, verbose=True, groups=4):
     """One GPU, a whole decode step of a 36-layer model: every layer's attend_verified +
     fetch_refine for a batch of sequences, the full cache page-locked on the host and the
     pivotal set plus the exact sketch on the device.
@@ -870,9 +873,14 @@ def measure_model_steps(local, kind, layers, steps, warmup, verbose=True):
     kind "long128k": n = 131072, batch 4, eta = 1/32, eps in {0.02, 0.05}, delta = 0.05, a needle
         set of U[2 %, 25 %] of the context per KV head that the queries favour.
 
-    A query is one layer of one sequence (32 query heads); a step is layers x batch queries.  The
-    first step runs eagerly with a synchronisation and a status check after every call; the timed
-    steps replay a CUDA graph of one step.  One JSON line."""
+    The batch is split into `groups` groups of sequences, one context each on its own stream:
+    a group runs its layers in order (each layer's call depends on the one before, as in a
+    model), and the groups are independent, so one group's host fetch overlaps another's
+    scoring and certificate.  A query is one layer of one sequence (32 query heads); a step is
+    layers x batch queries.  The first step runs eagerly with a synchronisation and a status
+    check after every call; the timed steps replay one CUDA graph of the step (the groups'
+    streams forked from and joined into the first); the per-kernel times come from a further
+    eager step with the groups run one after another.  One JSON line."""
     import torch
 
     from verified_kv_cache_poissoncomp_gb300 import binding as B
@@ -889,6 +897,11 @@ def measure_model_steps(local, kind, layers, steps, warmup, verbose=True):
     else:
         Bt, N = 4, 131072
         etas, epss = [1 / 32], [0.02, 0.05]
+    if groups < 1 or Bt % groups:
+        raise SystemExit(f"--groups must divide the batch ({Bt})")
+    bg = Bt // groups           # sequences per group
+    ug = bg * L * KVH           # cache units per group (sequence-major: a contiguous slice)
+    hg = bg * KVH * G           # query heads per group and layer
     delta = 0.05
     units = Bt * L * KVH
     t0 = time.time()
@@ -905,64 +918,90 @@ def measure_model_steps(local, kind, layers, steps, warmup, verbose=True):
     torch.cuda.synchronize()
     gen_s = time.time() - t0
     hq = Bt * KVH * G
-    stream = torch.cuda.Stream(dev)
+    streams = [torch.cuda.Stream(dev) for _ in range(groups)]
+    s0 = streams[0]
     rows = []
     for eta in etas:
-        with torch.cuda.stream(stream):
-            eng = VerKV(Bt, L, KVH, G, D, N, default_cap(N, eta))
-            eng.load_device(tau, kv, host_kv)
-            eng.compress(eta, 4, 512, 0)
-            eng.sync()
-            o_all = torch.empty((L, hq, D), dtype=torch.float32, device=dev)
-            lse_all = torch.empty((L, hq), dtype=torch.float32, device=dev)
-            st_all = torch.empty((L, hq, 16), dtype=torch.int32, device=dev)
-            fc_all = torch.zeros((L, Bt * KVH), dtype=torch.int32, device=dev)
-        counts = eng.p_count.cpu().numpy().astype(np.int64)
+        engs = []
+        for gi in range(groups):
+            with torch.cuda.stream(streams[gi]):
+                e = VerKV(bg, L, KVH, G, D, N, default_cap(N, eta))
+                e.load_device(tau[gi * ug:(gi + 1) * ug], kv[gi * ug:(gi + 1) * ug],
+                              host_kv[gi * ug:(gi + 1) * ug])
+                e.compress(eta, 4, 512, 0)
+                e.sync()
+            engs.append(e)
+        o_all = torch.empty((L, hq, D), dtype=torch.float32, device=dev)
+        lse_all = torch.empty((L, hq), dtype=torch.float32, device=dev)
+        st_all = torch.empty((L, hq, 16), dtype=torch.int32, device=dev)
+        fc_all = torch.zeros((L, Bt * KVH), dtype=torch.int32, device=dev)
+        # Pivotal counts in the cache's unit order (group by group: the groups are its slices).
+        counts = np.concatenate([e.p_count.cpu().numpy() for e in engs]).astype(np.int64)
         for eps in epss:
-            def step(check=False, with_counts=False):
-                for l in range(L):
-                    if check and verbose:  # where a failing call would stop
-                        print(f"checked call: eta={eta:.5f} eps={eps} layer={l}", file=sys.stderr,
-                              flush=True)
-                    B.verkv_attend_verified(eng.ctx, l, queries[l].data_ptr(), eng.pivotal,
-                                            eng.r_full.data_ptr(), eng.sketch_desc, eps, delta,
-                                            None, fc_all[l].data_ptr() if with_counts else None)
-                    if check:
-                        B.verkv_sync(eng.ctx)
-                    B.verkv_fetch_refine(eng.ctx, None, None, eng.host_kv.data_ptr(),
-                                         o_all[l].data_ptr(), lse_all[l].data_ptr(),
-                                         st_all[l].data_ptr())
-                    if check:
-                        B.verkv_sync(eng.ctx)
+            def step(check=False, with_counts=False, gis=range(groups)):
+                for gi in gis:
+                    e, h0, u0 = engs[gi], gi * hg, gi * bg * KVH
+                    with torch.cuda.stream(streams[gi]):
+                        for l in range(L):
+                            if check and verbose:  # where a failing call would stop
+                                print(f"checked call: eta={eta:.5f} eps={eps} group={gi} layer={l}",
+                                      file=sys.stderr, flush=True)
+                            q = queries[l][gi * bg:(gi + 1) * bg]
+                            B.verkv_attend_verified(
+                                e.ctx, l, q.data_ptr(), e.pivotal, e.r_full.data_ptr(),
+                                e.sketch_desc, eps, delta, None,
+                                fc_all[l, u0:u0 + bg * KVH].data_ptr() if with_counts else None)
+                            if check:
+                                B.verkv_sync(e.ctx)
+                            B.verkv_fetch_refine(e.ctx, None, None, e.host_kv.data_ptr(),
+                                                 o_all[l, h0:h0 + hg].data_ptr(),
+                                                 lse_all[l, h0:h0 + hg].data_ptr(),
+                                                 st_all[l, h0:h0 + hg].data_ptr())
+                            if check:
+                                B.verkv_sync(e.ctx)
 
-            with torch.cuda.stream(stream):
-                step(check=True, with_counts=True)      # checked, and the rows fetched
+            step(check=True, with_counts=True)          # checked, and the rows fetched
+            torch.cuda.synchronize()
             fr = fc_all.cpu().numpy().astype(np.int64)  # [L][B*KVH]
             st = st_all.cpu().numpy()
-            with torch.cuda.stream(stream):
-                graph = torch.cuda.CUDAGraph()
-                with torch.cuda.graph(graph, stream=stream):
-                    step()
+            graph = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(graph, stream=s0):
+                fork = torch.cuda.Event()
+                fork.record(s0)
+                for s in streams[1:]:
+                    s.wait_event(fork)
+                step()
+                for s in streams[1:]:
+                    join = torch.cuda.Event()
+                    join.record(s)
+                    s0.wait_event(join)
+            with torch.cuda.stream(s0):
                 for _ in range(warmup):
                     graph.replay()
             torch.cuda.synchronize()
             e0 = torch.cuda.Event(enable_timing=True)
             e1 = torch.cuda.Event(enable_timing=True)
             with ClockSampler(local) as clk:
-                e0.record(stream)
-                with torch.cuda.stream(stream):
+                e0.record(s0)
+                with torch.cuda.stream(s0):
                     for _ in range(steps):
                         graph.replay()
-                e1.record(stream)
+                e1.record(s0)
                 torch.cuda.synchronize()
-            B.verkv_sync(eng.ctx)
+            for e in engs:
+                B.verkv_sync(e.ctx)
             ms = e0.elapsed_time(e1) / steps
             del graph
-            B.verkv_profile_enable(eng.ctx, 1)
-            with torch.cuda.stream(stream):
-                step()
-            launches, total_ms = B.verkv_profile_read(eng.ctx)
-            B.verkv_profile_enable(eng.ctx, 0)
+            launches = np.zeros(B.VERKV_K_COUNT, dtype=np.int64)
+            total_ms = np.zeros(B.VERKV_K_COUNT)
+            for gi, e in enumerate(engs):  # one group at a time: each kernel's own time
+                B.verkv_profile_enable(e.ctx, 1)
+                step(gis=[gi])
+                torch.cuda.synchronize()
+                n_l, t_l = B.verkv_profile_read(e.ctx)
+                B.verkv_profile_enable(e.ctx, 0)
+                launches += np.asarray(n_l, dtype=np.int64)
+                total_ms += np.asarray(t_l, dtype=np.float64)
             # Algorithmic bytes of a step: per layer call the sketch of every unit, the logits
             # written and read once, r, and the pivotal rows (K, V, id and r); host bytes: the V
             # row of every fetched token (the exact sketch holds the keys).
@@ -976,7 +1015,7 @@ def measure_model_steps(local, kind, layers, steps, warmup, verbose=True):
             nfetch = st[..., 13]
             per_k = {B.verkv_kernel_name(k): {"launches_per_step": int(launches[k]),
                                               "avg_us": round(1e3 * total_ms[k] / launches[k], 2),
-                                              "ms_per_step": round(total_ms[k], 3)}
+                                              "ms_per_step": round(float(total_ms[k]), 3)}
                      for k in range(B.VERKV_K_COUNT) if launches[k] > 0}
             fetch_ms = total_ms[B.VERKV_K_FETCH_HOST]
             rows.append({
@@ -992,15 +1031,18 @@ def measure_model_steps(local, kind, layers, steps, warmup, verbose=True):
                 "fetched_rows_per_query_head": round(float(nfetch.mean()), 1),
                 "per_kernel": per_k, "clocks": clk.summary(),
                 **traffic_stats(st.reshape(-1, 16), fr.reshape(-1), counts, N)})
-        eng.close()
-        del eng, o_all, lse_all, st_all, fc_all
+        for e in engs:
+            e.close()
+        del engs, o_all, lse_all, st_all, fc_all
         torch.cuda.empty_cache()
     return {"workload": kind, "metric": METRIC, "unit": UNIT, "steps": steps,
                       "warmup": warmup, "data": "synthetic", "dtype": "bf16",
                       "config": {"layers": L, "batch": Bt, "kv_heads": KVH, "q_per_kv": G,
                                  "head_dim": D, "n": N, "delta": delta,
                                  "host_cache_GB": round(host_kv.nbytes / 1e9, 1),
-                                 "sketch": "exact", "fetch": "zerocopy", "graph": True},
+                                 "sketch": "exact", "fetch": "zerocopy", "graph": True,
+                                 "groups": groups, "sequences_per_group": bg},
+                      "launch": f"CUDA graph of one step over {groups} contexts on {groups} streams",
                       "input_generation_s": round(gen_s, 1), **extra, "rows": rows}
 
 
