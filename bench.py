@@ -873,7 +873,8 @@ def measure_model_steps(local, kind, layers, steps, warmup, verbose=True, groups
     kind "long128k": n = 131072, batch 4, eta = 1/32, eps in {0.02, 0.05}, delta = 0.05, a needle
         set of U[2 %, 25 %] of the context per KV head that the queries favour.
 
-    The batch is split into `groups` groups of sequences, one context each on its own stream:
+    The batch is split into `groups` groups of sequences, one context each on its own stream
+    (with its sequence offset set, so the Poisson draws are those of the whole-batch context):
     a group runs its layers in order (each layer's call depends on the one before, as in a
     model), and the groups are independent, so one group's host fetch overlaps another's
     scoring and certificate.  A query is one layer of one sequence (32 query heads); a step is
@@ -925,7 +926,7 @@ def measure_model_steps(local, kind, layers, steps, warmup, verbose=True, groups
         engs = []
         for gi in range(groups):
             with torch.cuda.stream(streams[gi]):
-                e = VerKV(bg, L, KVH, G, D, N, default_cap(N, eta))
+                e = VerKV(bg, L, KVH, G, D, N, default_cap(N, eta), seq0=gi * bg)
                 e.load_device(tau[gi * ug:(gi + 1) * ug], kv[gi * ug:(gi + 1) * ug],
                               host_kv[gi * ug:(gi + 1) * ug])
                 e.compress(eta, 4, 512, 0)

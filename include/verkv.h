@@ -170,6 +170,13 @@ void verkv_destroy(verkv_ctx *ctx);
  * MEMCPY allocates page-locked staging of units_per_layer * n * 4d bytes on first use. */
 verkv_status verkv_set_fetch_mode(verkv_ctx *ctx, int mode_flags);
 
+/* Sequence b of this context draws its Poisson sample as sequence seq0 + b (the fourth word of
+ * the Philox counter in verkv_poissoncomp), so that a batch split over several contexts, each
+ * holding the sequences seq0 .. seq0 + batch - 1 of it, draws exactly the sample that one context
+ * for the whole batch would.  seq0 >= 0 (VERKV_EINVAL otherwise); 0 by default.  Takes effect at
+ * the next verkv_poissoncomp. */
+verkv_status verkv_set_sequence_offset(verkv_ctx *ctx, int32_t seq0);
+
 /* PoissonComp (summary page, Methodology, POISSONCOMP: Eq. (3), the H / L partition and the
  * Poisson sample S), for every unit of the shape.
  *   tau     device float [units][n]: normalised importance scores; must be finite and in (0, 1]
@@ -178,7 +185,8 @@ verkv_status verkv_set_fetch_mode(verkv_ctx *ctx, int mode_flags);
  *           outside the forced set (VERKV_EBUDGET, checked on the host before any launch)
  *   H       the forced H set
  *   seed    Philox4x32-10 key; token i of unit (b, l, h) draws word i%4 of the block at counter
- *           (i/4, h, l, b), u_i = (word >> 8) * 2^-24, and is kept iff u_i < r_i
+ *           (i/4, h, l, seq0 + b) (seq0 from verkv_set_sequence_offset, 0 by default),
+ *           u_i = (word >> 8) * 2^-24, and is kept iff u_i < r_i
  *   kv_full device bf16 [units][n][2][d]: the full cache, read to fill out->kv
  *   r_full  device float [units][n] out: r_i = min(1, c tau_i) for every token (1 in H)
  *   out     the pivotal set (every member must point to caller device memory of the sizes above)

@@ -34,7 +34,8 @@ EXPORTED = ["verkv_sketch_bytes", "verkv_workspace_size", "verkv_create", "verkv
             "verkv_profile_read", "verkv_launch_counts", "verkv_kernel_name", "verkv_sync",
             "verkv_last_error", "verkv_status_string", "verkv_certify_noalloc",
             "verkv_attend_dense_host", "verkv_set_shortlist", "verkv_shortlist_bitmap",
-            "verkv_profile_timeline", "verkv_test_inject", "verkv_measure_sketch_stream"]
+            "verkv_profile_timeline", "verkv_test_inject", "verkv_measure_sketch_stream",
+            "verkv_set_sequence_offset"]
 VERKV_INJECT_COPY_FAIL, VERKV_INJECT_BETA_MAXIT, VERKV_INJECT_SCORE_STALL = 1, 2, 3
 VERKV_INJECT_SELECT_GATHER = 4
 # kernel ids (include/verkv.h), in launch order
@@ -107,6 +108,8 @@ def lib():
         L.verkv_destroy.restype = None
         L.verkv_set_fetch_mode.argtypes = [vp, ctypes.c_int]
         L.verkv_set_fetch_mode.restype = ctypes.c_int
+        L.verkv_set_sequence_offset.argtypes = [vp, ctypes.c_int32]
+        L.verkv_set_sequence_offset.restype = ctypes.c_int
         L.verkv_poissoncomp.argtypes = [vp, vp, ctypes.c_double, verkv_hset, ctypes.c_uint64, vp,
                                         vp, ctypes.POINTER(verkv_pivotal)]
         L.verkv_poissoncomp.restype = ctypes.c_int
@@ -188,6 +191,10 @@ def verkv_destroy(ctx):
 
 def verkv_set_fetch_mode(ctx, mode):
     _check(lib().verkv_set_fetch_mode(ctx, int(mode)), ctx)
+
+
+def verkv_set_sequence_offset(ctx, seq0):
+    _check(lib().verkv_set_sequence_offset(ctx, int(seq0)), ctx)
 
 
 def verkv_poissoncomp(ctx, tau, eta, H, seed, kv_full, r_full, pivotal):

@@ -290,7 +290,7 @@ __global__ void __launch_bounds__(PC_NT, 1) k_pc_solve(PcArgs a) {
         const int i0 = wbase + g0 + 4 * lane;  // CTA-local index of my first token
         const int t0 = base + i0;
         const uint4 blk = philox4x32_10(make_uint4((uint32_t)t0 >> 2, (uint32_t)h, (uint32_t)l,
-                                                   (uint32_t)b), a.seed_lo, a.seed_hi);
+                                                   (uint32_t)(a.seq0 + b)), a.seed_lo, a.seed_hi);
         const uint32_t words[4] = {blk.x, blk.y, blk.z, blk.w};
         uint32_t nib = 0;
         if (g0 + 4 * lane < wchunk && t0 < n) {

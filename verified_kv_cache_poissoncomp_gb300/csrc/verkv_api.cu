@@ -221,6 +221,7 @@ struct verkv_ctx {
     int64_t inject_copy_fail = 0;    // fetch copies still to fail on the host
     int beta_maxit = 0;              // 0: the kernel's default cap
     int sel_gather = 1;              // the select's gathered finish (clusters of 1 and 4)
+    int seq0 = 0;                    // Philox sequence index of this context's first sequence
     int64_t score_stall_ns = 0;      // > 0: the next attend's scoring kernel stalls one stage
     // Measurement
     int64_t launches[VERKV_K_COUNT] = {};
@@ -425,6 +426,13 @@ void verkv_destroy(verkv_ctx *ctx) {
     delete ctx;
 }
 
+verkv_status verkv_set_sequence_offset(verkv_ctx *ctx, int32_t seq0) {
+    if (!ctx) return VERKV_EINVAL;
+    if (seq0 < 0) return fail(ctx, VERKV_EINVAL, "sequence offset: must be >= 0");
+    ctx->seq0 = seq0;
+    return VERKV_OK;
+}
+
 verkv_status verkv_set_fetch_mode(verkv_ctx *ctx, int mode_flags) {
     if (!ctx) return VERKV_EINVAL;
     const int mode = mode_flags & ~VERKV_FETCH_KEYS;
@@ -501,6 +509,7 @@ verkv_status verkv_poissoncomp(verkv_ctx *ctx, const float *tau, double eta, ver
     a.chunk = chunk;
     a.seed_lo = (uint32_t)seed;
     a.seed_hi = (uint32_t)(seed >> 32);
+    a.seq0 = ctx->seq0;
     VERKV_CUDA(tracked(ctx, VERKV_K_PC_SOLVE, ctx->main, [&] { return launch_pc_solve(a, units, ctx->main); }), "k_pc_solve");
     VERKV_CUDA(tracked(ctx, VERKV_K_PC_GATHER, ctx->main, [&] {
                    return launch_pc_gather((const uint16_t *)kv_full, out->ids, out->count,

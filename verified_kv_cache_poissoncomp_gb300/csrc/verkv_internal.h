@@ -35,6 +35,7 @@ struct PcArgs {
     int n_rest;              // n - |forced|
     int cl, chunk;           // CTAs per cluster, tokens per CTA (multiple of 1024)
     uint32_t seed_lo, seed_hi;
+    int seq0;                // the first sequence's index in the Philox counter
 };
 cudaError_t launch_pc_solve(const PcArgs &a, int units, cudaStream_t s);
 

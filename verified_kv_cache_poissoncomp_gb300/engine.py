@@ -30,7 +30,10 @@ def default_cap(n, eta):
 
 class VerKV:
     def __init__(self, batch, layers, kv_heads, q_per_kv, head_dim, n, cap, device=None,
-                 fetch_mode=B.VERKV_FETCH_ZEROCOPY, sketch_format=B.VERKV_SKETCH_EXACT):
+                 fetch_mode=B.VERKV_FETCH_ZEROCOPY, sketch_format=B.VERKV_SKETCH_EXACT, seq0=0):
+        """seq0: the index of this context's first sequence in a batch split over several
+        contexts (its Poisson draws are then those of that sequence; see
+        verkv_set_sequence_offset)."""
         self.dev = torch.device("cuda", torch.cuda.current_device() if device is None else device)
         self.shape = B.verkv_shape(batch, layers, kv_heads, q_per_kv, head_dim, n, cap)
         self.B, self.L, self.h, self.G, self.d, self.n, self.cap = (
@@ -47,6 +50,8 @@ class VerKV:
                                   self.workspace.data_ptr(), ws)
         if fetch_mode != B.VERKV_FETCH_ZEROCOPY:
             B.verkv_set_fetch_mode(self.ctx, fetch_mode)
+        if seq0:
+            B.verkv_set_sequence_offset(self.ctx, seq0)
         dv = self.dev
         u, hq = self.units, batch * kv_heads * q_per_kv
         self.r_full = torch.empty((u, n), dtype=torch.float32, device=dv)
