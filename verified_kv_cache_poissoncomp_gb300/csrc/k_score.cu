@@ -103,10 +103,11 @@ constexpr size_t tc_smem_bytes() { return 1024 + (size_t)TC_STAGES * (D / 64) * 
 template <int D, int G>
 __global__ void __launch_bounds__(TC_NT, TC_CTAS_PER_SM) k_score(ScoreArgs a, int spans_per_unit, int span_rows,
                                                                const __grid_constant__ CUtensorMap map) {
-    // The first kernel of a library call is launched without programmatic serialisation: when
-    // it starts, every earlier kernel on the stream (the caller's q projection, a sketch build)
-    // has finished, so the first sketch stages are requested at once and pdl_wait() returns
-    // immediately.  The trigger lets the certificate kernel be scheduled early.
+    // The first kernel of a library call may be launched with programmatic serialisation, so it
+    // can be resident before the kernel ahead of it on the stream (the caller's q projection, a
+    // sketch build, the previous call's merge) has finished: it reads nothing the caller wrote
+    // (the sketch, q) before pdl_wait().  The trigger lets the certificate kernel be scheduled
+    // early.
     pdl_trigger();
     using LY = PivLayout<D>;
     constexpr int KS = D / 16, HALVES = D / 64, STAGE = HALVES * LY::BOX;
@@ -142,11 +143,10 @@ __global__ void __launch_bounds__(TC_NT, TC_CTAS_PER_SM) k_score(ScoreArgs a, in
         for (int hb = 0; hb < HALVES; ++hb)
             tma_load_3d(st + hb * LY::BOX, &map, hb * 64, row0 + k * TC_ROWS, ug, bar);
     };
-    if (tid == 0) {
-        asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&map)) : "memory");
-        for (int k = 0; k < min(TC_STAGES, nst); ++k) issue(k);
-    }
+    if (tid == 0) asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&map)) : "memory");
     pdl_wait();
+    if (tid == 0)
+        for (int k = 0; k < min(TC_STAGES, nst); ++k) issue(k);
     // Q^T as the B operand: query head g of the group (zero for g >= G), channels 2t, 2t + 1 and
     // 2t + 8, 2t + 9 of each k-step, read while the first stages are in flight.
     uint32_t qb[KS][2];
@@ -331,7 +331,7 @@ __device__ __forceinline__ unsigned long long fadd2(unsigned long long a, unsign
 template <int D, int G>
 __global__ void __launch_bounds__(SC_NT, SC_CTAS_PER_SM) k_score_q2(ScoreArgs a, int spans_per_unit,
                                                                    int span_rows) {
-    pdl_trigger();  // launched as k_score is: q and the first stages are read at once
+    pdl_trigger();  // launched as k_score is: nothing the caller wrote is read before pdl_wait()
     constexpr int CPL = G <= 4 ? 16 : 8;
     constexpr int LPR = D / CPL, RPW = 32 / LPR, NW = SC_NT / 32;
     constexpr int ROWB = (D / 4 + 4 * (D / 32) + 15) / 16 * 16;  // bytes per sketch row
@@ -374,9 +374,9 @@ __global__ void __launch_bounds__(SC_NT, SC_CTAS_PER_SM) k_score_q2(ScoreArgs a,
         bulk_g2s(ring + (size_t)(k % SC_STAGES) * SQ_ROWS * ROWB, src + (size_t)k * SQ_ROWS * ROWB,
                  bytes, bar);
     };
+    pdl_wait();
     if (tid == 0)
         for (int k = 0; k < min(SC_STAGES, nst); ++k) issue(k);
-    pdl_wait();
     // q is read while the first stages are in flight.
     unsigned long long qp[G][CPL / 2];
     float qs[G];

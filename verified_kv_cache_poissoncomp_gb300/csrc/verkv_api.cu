@@ -581,9 +581,9 @@ verkv_status verkv_attend_verified(verkv_ctx *ctx, int32_t layer, const void *q,
         ctx->score_stall_ns = 0;
     }
     if (sketch->format == VERKV_SKETCH_Q2) {
-        VERKV_CUDA(tracked(ctx, VERKV_K_SCORE, ctx->main, [&] { return launch_score_q2(sa, ctx->L.units_layer, ctx->main, false); }), "k_score_q2");
+        VERKV_CUDA(tracked(ctx, VERKV_K_SCORE, ctx->main, [&] { return launch_score_q2(sa, ctx->L.units_layer, ctx->main, true); }), "k_score_q2");
     } else {
-        VERKV_CUDA(tracked(ctx, VERKV_K_SCORE, ctx->main, [&] { return launch_score(sa, ctx->L.units_layer, ctx->main, false); }), "k_score");
+        VERKV_CUDA(tracked(ctx, VERKV_K_SCORE, ctx->main, [&] { return launch_score(sa, ctx->L.units_layer, ctx->main, true); }), "k_score");
     }
 
     if (ctx->shortlist > 0) {

@@ -108,9 +108,9 @@ struct ScoreArgs {
     unsigned long long wait_ns;
     int stall_first;
 };
-// `pdl`: launch with programmatic stream serialisation.  The first kernel of a library call must
-// not: it reads the caller's q and sketch, which the caller's preceding kernel may still be
-// writing when it lets dependents start early.
+// `pdl`: launch with programmatic stream serialisation.  Safe for the first kernel of a library
+// call because the scoring kernels read the caller's q and sketch only after pdl_wait(), which
+// returns once the preceding kernel has finished and its writes are visible.
 cudaError_t launch_score(const ScoreArgs &a, int units_layer, cudaStream_t s, bool pdl);
 // The same from the 2-bit sketch (a.sketch points at its rows).
 cudaError_t launch_score_q2(const ScoreArgs &a, int units_layer, cudaStream_t s, bool pdl);
