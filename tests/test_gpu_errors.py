@@ -181,10 +181,13 @@ def test_injection_arguments_are_checked():
     w = I.tiny()
     eng = P.make_engine(w)
     for what, value in [(0, 1), (B.VERKV_INJECT_COPY_FAIL, -1), (B.VERKV_INJECT_BETA_MAXIT, 65),
-                        (B.VERKV_INJECT_SCORE_STALL, 10)]:
+                        (B.VERKV_INJECT_SCORE_STALL, 10), (B.VERKV_INJECT_SELECT_GATHER, 2)]:
         with pytest.raises(B.VerkvError) as e:
             B.verkv_test_inject(eng.ctx, what, value)
         assert e.value.status == B.VERKV_EINVAL
+    with pytest.raises(B.VerkvError) as e:  # a sequence offset below zero
+        B.verkv_set_sequence_offset(eng.ctx, -1)
+    assert e.value.status == B.VERKV_EINVAL
     eng.close()
 
 
